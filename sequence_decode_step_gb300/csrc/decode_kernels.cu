@@ -1,0 +1,809 @@
+// Decode-step kernels for sm_103a (GB300).
+//
+// Every kernel of the step follows one pattern:
+//   1. prefetch what does not depend on the previous kernel (its weight slice,
+//      or the KV rows written by earlier steps) into shared memory with bulk
+//      TMA copies (cp.async.bulk) completing on an mbarrier;
+//   2. griddepcontrol.launch_dependents, so the next kernel of the CUDA graph
+//      can already start its own prefetch;
+//   3. griddepcontrol.wait, then read the activations and compute.
+// The HBM stream therefore does not drain between the kernels of a step.
+// Every wait on an mbarrier is bounded by %globaltimer; on expiry the kernel
+// sets ERR_TIMEOUT in the device error word, waits (again bounded) for its
+// copies in flight and leaves without hanging.
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "qw_internal.h"
+
+namespace qw {
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Bulk (non-tensor) TMA copy global -> shared; both addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar` for at most limit_ns; limit 0 gives up at once.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// Deterministic block sum for 256 threads: warp sums, then the 8 added in order.
+__device__ __forceinline__ float block_sum_256(float v, float* scratch8) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) scratch8[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) t += scratch8[i];
+  return t;
+}
+
+// 8 bf16 weights (one 16-byte load) dotted with 8 floats.
+__device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8], float acc) {
+  acc = fmaf(__uint_as_float(w.x << 16), x[0], acc);
+  acc = fmaf(__uint_as_float(w.x & 0xffff0000u), x[1], acc);
+  acc = fmaf(__uint_as_float(w.y << 16), x[2], acc);
+  acc = fmaf(__uint_as_float(w.y & 0xffff0000u), x[3], acc);
+  acc = fmaf(__uint_as_float(w.z << 16), x[4], acc);
+  acc = fmaf(__uint_as_float(w.z & 0xffff0000u), x[5], acc);
+  acc = fmaf(__uint_as_float(w.w << 16), x[6], acc);
+  acc = fmaf(__uint_as_float(w.w & 0xffff0000u), x[7], acc);
+  return acc;
+}
+
+// Argmax order: larger value wins, equal values go to the lower index.
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// Reduce (best_v, best_i) over the 256 threads; result valid in thread 0.
+__device__ __forceinline__ void block_argmax_256(float& bv, int& bi, float* r8, int* r8i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (am_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) { r8[warp] = bv; r8i[warp] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bv = r8[0];
+    bi = r8i[0];
+    for (int i = 1; i < 8; ++i)
+      if (am_better(r8[i], r8i[i], bv, bi)) { bv = r8[i]; bi = r8i[i]; }
+  }
+}
+
+// ------------------------------------------------------------------ GEMV
+// y = epi(W . pro(x)) for M = 1. CTA b owns output units [n*b/G, n*(b+1)/G),
+// whose weight rows are one contiguous byte range; it streams that range
+// through `n_stages` shared-memory stages with bulk copies. Warps are split
+// into `ks` K-slices (the input slice stays in registers) and 8/ks row groups.
+template <int EPI, int MAXC>
+__global__ void __launch_bounds__(256, 1) gemv_kernel(const GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  float* red8 = reinterpret_cast<float*>(smem + 64);
+  int* red8i = reinterpret_cast<int*>(smem + 96);
+  float* red = reinterpret_cast<float*>(smem + a.off_red);
+  float* xs = reinterpret_cast<float*>(smem + a.off_x);
+  uint8_t* stages = smem + a.off_stage;
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int u_begin = (int)(((long long)a.n_units * b) / G);
+  const int u_end = (int)(((long long)a.n_units * (b + 1)) / G);
+  const int n_my = u_end - u_begin;
+  const int ups = a.units_per_stage;
+  const int n_chunks = (n_my + ups - 1) / ups;
+  const uint32_t unit_bytes = (uint32_t)a.rpu * a.row_bytes;
+  const int NS = a.n_stages;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+    const int pre = n_chunks < NS ? n_chunks : NS;
+    for (int c = 0; c < pre; ++c) {
+      const int nu = min(ups, n_my - c * ups);
+      mbar_expect_tx(&bars[c], nu * unit_bytes);
+      bulk_load(stages + (size_t)c * a.stage_bytes,
+                a.w + (size_t)(u_begin + c * ups) * unit_bytes, nu * unit_bytes, &bars[c]);
+    }
+  }
+  // Weights are in flight; let the next kernel start, then wait for our inputs.
+  pdl_launch_dependents();
+  pdl_wait();
+
+  // Prologue: input vector into shared memory, optional RMSNorm.
+  const int K = a.K;
+  float ss = 0.f;
+  for (int k = tid * 4; k < K; k += 256 * 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.x + k));
+    *reinterpret_cast<float4*>(xs + k) = v;
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+  if (a.norm_g != nullptr) {
+    const float tot = block_sum_256(ss, red8);
+    const float r = 1.0f / sqrtf(tot / (float)K + a.eps);
+    for (int k = tid * 4; k < K; k += 256 * 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) xs[k + e] = xs[k + e] * r * bf16f(a.norm_g[k + e]);
+    }
+  }
+  __syncthreads();
+  if (a.norm_out != nullptr && b == 0) {
+    const int row = a.pos ? *a.pos : 0;
+    for (int k = tid; k < K; k += 256) a.norm_out[(size_t)row * K + k] = xs[k];
+  }
+
+  const int ksz = a.ks, kslice = warp % ksz, grp = warp / ksz, ngrp = 8 / ksz;
+  const int nch = (K + 255) >> 8;
+  const int c_lo = kslice * a.cpw;
+  const int c_hi = min(nch, c_lo + a.cpw);
+  float xr[MAXC][8];
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) {
+    const int col = (c_lo + c) * 256 + lane * 8;
+    const bool on = (c_lo + c < c_hi) && col < K;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xr[c][e] = on ? xs[col + e] : 0.f;
+  }
+
+  float best_v = -INFINITY;
+  int best_i = 0x7fffffff;
+  int saw_nan = 0;
+  int c = 0;
+  bool failed = false;
+  const int cap_row = (a.cap_out != nullptr && a.pos != nullptr) ? *a.pos : 0;
+  for (; c < n_chunks; ++c) {
+    const int st = c % NS;
+    const bool ok = mbar_wait(&bars[st], (uint32_t)((c / NS) & 1), a.wait_ns);
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    const int nu = min(ups, n_my - c * ups);
+    const int nrows = nu * a.rpu;
+    const uint8_t* sw = stages + (size_t)st * a.stage_bytes;
+    for (int r0 = grp * 2; r0 < nrows; r0 += ngrp * 2) {
+      const bool two = r0 + 1 < nrows;
+      const uint8_t* w0 = sw + (size_t)r0 * a.row_bytes;
+      const uint8_t* w1 = w0 + a.row_bytes;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < MAXC; ++cc) {
+        const int col = (c_lo + cc) * 256 + lane * 8;
+        if ((c_lo + cc < c_hi) && col < K) {
+          acc0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[cc], acc0);
+          if (two)
+            acc1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[cc], acc1);
+        }
+      }
+      acc0 = warp_sum(acc0);
+      acc1 = warp_sum(acc1);
+      if (lane == 0) {
+        red[r0 * ksz + kslice] = acc0;
+        if (two) red[(r0 + 1) * ksz + kslice] = acc1;
+      }
+    }
+    __syncthreads();
+    for (int t = tid; t < nu; t += 256) {
+      const int u = u_begin + c * ups + t;
+      float v0 = 0.f;
+      for (int q = 0; q < ksz; ++q) v0 += red[(t * a.rpu) * ksz + q];
+      if (EPI == EPI_STORE) {
+        a.y[u] = v0 + (a.bias ? bf16f(a.bias[u]) : 0.f);
+      } else if (EPI == EPI_RESIDUAL) {
+        const float nv = __ldcg(a.y + u) + v0;
+        a.y[u] = nv;
+        if (a.cap_out) a.cap_out[(size_t)cap_row * a.n_units + u] = nv;
+      } else if (EPI == EPI_SWIGLU) {
+        float v1 = 0.f;
+        for (int q = 0; q < ksz; ++q) v1 += red[(t * 2 + 1) * ksz + q];
+        a.y[u] = v0 / (1.0f + expf(-v0)) * v1;
+      } else {  // EPI_LOGITS
+        a.y[u] = v0;
+        if (v0 != v0) saw_nan = 1;
+        else if (v0 > best_v) { best_v = v0; best_i = u; }
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && c + NS < n_chunks) {
+      const int cn = c + NS;
+      const int nun = min(ups, n_my - cn * ups);
+      mbar_expect_tx(&bars[st], nun * unit_bytes);
+      bulk_load(stages + (size_t)st * a.stage_bytes,
+                a.w + (size_t)(u_begin + cn * ups) * unit_bytes, nun * unit_bytes, &bars[st]);
+    }
+  }
+  if (failed) {
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      const int hi = min(n_chunks, c + NS);
+      for (int cc = c; cc < hi; ++cc)
+        mbar_wait(&bars[cc % NS], (uint32_t)((cc / NS) & 1), kDrainNs);
+    }
+    __syncthreads();
+  }
+  if (EPI != EPI_LOGITS) return;
+
+  // ---- greedy argmax: CTA best, then the last CTA to arrive reduces all of them.
+  const int any_nan = __syncthreads_or(saw_nan);
+  block_argmax_256(best_v, best_i, red8, red8i);
+  if (tid == 0) {
+    a.am.blk_val[b] = any_nan ? __int_as_float(0x7fc00000) : best_v;
+    a.am.blk_idx[b] = best_i;
+    __threadfence();
+    const int prev = atomicAdd(a.am.counter, 1);
+    s_last = (prev == G - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  int nan_seen = 0;
+  for (int i = tid; i < G; i += 256) {
+    const float v = __ldcg(a.am.blk_val + i);
+    const int ix = __ldcg(a.am.blk_idx + i);
+    if (v != v) nan_seen = 1;
+    else if (am_better(v, ix, bv, bi)) { bv = v; bi = ix; }
+  }
+  nan_seen = __syncthreads_or(nan_seen);
+  block_argmax_256(bv, bi, red8, red8i);
+  if (tid == 0) {
+    const int am = nan_seen ? -1 : bi;
+    if (nan_seen) atomicOr(a.err, ERR_NAN);
+    if (a.am.argmax) *a.am.argmax = am;
+    if (a.am.next_token) *a.am.next_token = am;
+    if (a.am.pos) {
+      const int p = *a.am.pos;
+      if (a.am.tokens_by_pos) a.am.tokens_by_pos[p] = am;
+      if (a.am.host_tokens) a.am.host_tokens[p] = am;
+      *a.am.pos = p + 1;
+    }
+    if (a.am.host_status) {
+      a.am.host_status[0] = am;
+      a.am.host_status[1] = *reinterpret_cast<volatile int*>(a.err);
+    }
+    *a.am.counter = 0;
+  }
+}
+
+void plan_gemv(GemvArgs& a, int grid, uint32_t max_stage_bytes, int max_stages) {
+  const int nch = (a.K + 255) / 256;
+  int ks = 1;
+  while (ks < 8 && (nch + ks - 1) / ks > 4) ks *= 2;
+  a.ks = ks;
+  a.cpw = (nch + ks - 1) / ks;
+  const uint32_t unit_bytes = (uint32_t)a.rpu * a.row_bytes;
+  const int units_max = (a.n_units + grid - 1) / grid;
+  if ((uint64_t)units_max * unit_bytes <= max_stage_bytes) {
+    a.units_per_stage = units_max;
+    a.n_stages = 1;
+  } else {
+    int ups = (int)(max_stage_bytes / unit_bytes);
+    if (ups < 1) ups = 1;
+    a.units_per_stage = ups;
+    const int chunks = (units_max + ups - 1) / ups;
+    a.n_stages = chunks < max_stages ? chunks : max_stages;
+  }
+  a.stage_bytes = (uint32_t)a.units_per_stage * unit_bytes;
+  a.off_red = 128;
+  const uint32_t red_bytes = (uint32_t)a.units_per_stage * a.rpu * a.ks * 4;
+  a.off_x = (a.off_red + red_bytes + 15) & ~15u;
+  a.off_stage = (a.off_x + (uint32_t)a.K * 4 + 127) & ~127u;
+}
+
+size_t gemv_smem_bytes(const GemvArgs& a) {
+  return (size_t)a.off_stage + (size_t)a.n_stages * a.stage_bytes;
+}
+
+template <class Kern, class... Args>
+static cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <int EPI>
+static cudaError_t launch_gemv_epi(const GemvArgs& a, int grid, bool pdl, cudaStream_t s) {
+  const size_t smem = gemv_smem_bytes(a);
+  if (a.cpw <= 4) return launch_ex(gemv_kernel<EPI, 4>, dim3(grid), dim3(256), smem, s, pdl, a);
+  if (a.cpw <= 8) return launch_ex(gemv_kernel<EPI, 8>, dim3(grid), dim3(256), smem, s, pdl, a);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemv(int epi, const GemvArgs& a, int grid, bool pdl, cudaStream_t s) {
+  if (gemv_smem_bytes(a) > 227 * 1024) return cudaErrorInvalidValue;
+  switch (epi) {
+    case EPI_STORE: return launch_gemv_epi<EPI_STORE>(a, grid, pdl, s);
+    case EPI_RESIDUAL: return launch_gemv_epi<EPI_RESIDUAL>(a, grid, pdl, s);
+    case EPI_SWIGLU: return launch_gemv_epi<EPI_SWIGLU>(a, grid, pdl, s);
+    case EPI_LOGITS: return launch_gemv_epi<EPI_LOGITS>(a, grid, pdl, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ attention (decode)
+// One CTA per (key split, KV head). The KV rows of earlier positions are fixed,
+// so they are prefetched before the dependency wait; the device position is
+// read there too (only the last kernel of a step changes it). After the wait
+// the CTA forms its group's queries (QK-RMSNorm, RoPE, 1/sqrt(hd)); the CTA
+// whose split holds `pos` also forms k and v, appends them to the cache and
+// patches its staged tile. Scores and an online softmax run tile by tile; the
+// last CTA of a KV head to finish combines the splits in split order.
+constexpr int kAttnTK = 32;
+constexpr int kAttnNS = 3;
+constexpr int kAttnGQ = 8;
+
+template <int HD>
+__host__ __device__ constexpr uint32_t attn_stage_off() {
+  return (64u + 4u * (kAttnGQ * HD + 2 * HD + 2 * kAttnGQ * kAttnTK + 3 * kAttnGQ + 4) + 127u) &
+         ~127u;
+}
+template <int HD>
+__host__ __device__ constexpr uint32_t attn_smem() {
+  return attn_stage_off<HD>() + (uint32_t)kAttnNS * 2u * kAttnTK * HD * 4u;
+}
+
+__device__ __forceinline__ void rope_cs(const float2* row, int pos, int j, int hd, float theta,
+                                        float& c, float& s) {
+  if (row != nullptr) {
+    const float2 v = row[j];
+    c = v.x;
+    s = v.y;
+  } else {
+    const double inv = pow((double)theta, -2.0 * (double)j / (double)hd);
+    double sd, cd;
+    sincos((double)pos * inv, &sd, &cd);
+    c = (float)cd;
+    s = (float)sd;
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
+  constexpr int TK = kAttnTK, NS = kAttnNS, GQM = kAttnGQ, EPL = HD / 32;
+  constexpr int OUTS = (GQM * HD + 255) / 256;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  float* q_s = reinterpret_cast<float*>(smem + 64);  // [GQM][HD]
+  float* kn_s = q_s + GQM * HD;                       // [HD]
+  float* vn_s = kn_s + HD;                            // [HD]
+  float* sc_s = vn_s + HD;                            // [GQM][TK]
+  float* p_s = sc_s + GQM * TK;                       // [GQM][TK]
+  float* ml_s = p_s + GQM * TK;                       // [GQM][2]
+  float* al_s = ml_s + 2 * GQM;                       // [GQM]
+  int* flag_s = reinterpret_cast<int*>(al_s + GQM);
+  float* stage0 = reinterpret_cast<float*>(smem + attn_stage_off<HD>());
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.y, s = blockIdx.x;
+  const int GQ = a.nq / a.nkv;
+  // Read before the dependency wait: only the last kernel of a step writes it.
+  const int pos = a.pos_ptr ? *a.pos_ptr : a.pos_const;
+  const int n_keys = pos + 1;
+  int kps = (n_keys + a.nsplit_max - 1) / a.nsplit_max;
+  kps = kps > a.min_keys ? kps : a.min_keys;
+  kps = (kps + TK - 1) / TK * TK;
+  const int nsplit = (n_keys + kps - 1) / kps;
+  if (s >= nsplit) return;
+  const int k0 = s * kps;
+  const int k1 = min(n_keys, k0 + kps);
+  const int ntiles = (k1 - k0 + TK - 1) / TK;
+  const bool owns_pos = pos >= k0 && pos < k1;
+  float* kc = a.k_cache + (size_t)g * a.cap * HD;
+  float* vc = a.v_cache + (size_t)g * a.cap * HD;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+    const int pre = ntiles < NS ? ntiles : NS;
+    for (int i = 0; i < pre; ++i) {
+      const int t0 = k0 + i * TK, nk = min(TK, k1 - t0);
+      const uint32_t bytes = (uint32_t)nk * HD * 4;
+      float* dK = stage0 + (size_t)i * 2 * TK * HD;
+      mbar_expect_tx(&bars[i], 2 * bytes);
+      bulk_load(dK, kc + (size_t)t0 * HD, bytes, &bars[i]);
+      bulk_load(dK + TK * HD, vc + (size_t)t0 * HD, bytes, &bars[i]);
+    }
+  }
+  if (tid < GQM) {
+    ml_s[2 * tid] = -INFINITY;
+    ml_s[2 * tid + 1] = 0.f;
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+
+  const float scale = 1.0f / sqrtf((float)HD);
+  const float2* rrow = a.rope ? a.rope + (size_t)pos * (HD / 2) : nullptr;
+  for (int hh = warp; hh <= GQ; hh += 8) {
+    const bool isq = hh < GQ;
+    if (!isq && !owns_pos) break;
+    const float* src = a.qkv + (size_t)(isq ? (g * GQ + hh) : (a.nq + g)) * HD;
+    const uint16_t* gain = isq ? a.q_norm : a.k_norm;
+    float v[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[e] = __ldcg(src + lane + 32 * e);
+    if (gain != nullptr) {
+      float sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) sq = fmaf(v[e], v[e], sq);
+      sq = warp_sum(sq);
+      const float r = 1.0f / sqrtf(sq / (float)HD + a.eps);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[e] = v[e] * r * bf16f(gain[lane + 32 * e]);
+    }
+#pragma unroll
+    for (int e = 0; e < EPL / 2; ++e) {
+      float cs, sn;
+      rope_cs(rrow, pos, lane + 32 * e, HD, a.rope_theta, cs, sn);
+      const float x0 = v[e], x1 = v[e + EPL / 2];
+      v[e] = x0 * cs - x1 * sn;
+      v[e + EPL / 2] = x1 * cs + x0 * sn;
+    }
+    if (isq) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) q_s[hh * HD + lane + 32 * e] = v[e] * scale;
+    } else {
+      const float* vsrc = a.qkv + (size_t)(a.nq + a.nkv + g) * HD;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const int d = lane + 32 * e;
+        kn_s[d] = v[e];
+        kc[(size_t)pos * HD + d] = v[e];
+        const float vv = __ldcg(vsrc + d);
+        vn_s[d] = vv;
+        vc[(size_t)pos * HD + d] = vv;
+      }
+    }
+  }
+  __syncthreads();
+
+  float qr[GQM][EPL];
+#pragma unroll
+  for (int h = 0; h < GQM; ++h)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) qr[h][e] = (h < GQ) ? q_s[h * HD + lane * EPL + e] : 0.f;
+
+  float oacc[OUTS];
+#pragma unroll
+  for (int i = 0; i < OUTS; ++i) oacc[i] = 0.f;
+
+  bool failed = false;
+  int it = 0;
+  for (; it < ntiles; ++it) {
+    const int st = it % NS;
+    const bool ok = mbar_wait(&bars[st], (uint32_t)((it / NS) & 1), a.wait_ns);
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    const int t0 = k0 + it * TK, nk = min(TK, k1 - t0);
+    float* Ks = stage0 + (size_t)st * 2 * TK * HD;
+    float* Vs = Ks + TK * HD;
+    if (owns_pos && pos >= t0 && pos < t0 + nk) {
+      for (int e = tid; e < HD; e += 256) {
+        Ks[(pos - t0) * HD + e] = kn_s[e];
+        Vs[(pos - t0) * HD + e] = vn_s[e];
+      }
+      __syncthreads();
+    }
+    for (int j = warp; j < nk; j += 8) {
+      float kv[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) kv[e] = Ks[j * HD + lane * EPL + e];
+#pragma unroll
+      for (int h = 0; h < GQM; ++h) {
+        if (h < GQ) {
+          float p = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) p = fmaf(qr[h][e], kv[e], p);
+          p = warp_sum(p);
+          if (lane == 0) sc_s[h * TK + j] = p;
+        }
+      }
+    }
+    __syncthreads();
+    for (int h = warp; h < GQ; h += 8) {
+      const float sc = lane < nk ? sc_s[h * TK + lane] : -INFINITY;
+      const float tmax = warp_max(sc);
+      const float m_old = ml_s[2 * h], l_old = ml_s[2 * h + 1];
+      const float m_new = fmaxf(m_old, tmax);
+      const float p = lane < nk ? expf(sc - m_new) : 0.f;
+      const float psum = warp_sum(p);
+      const float alpha = expf(m_old - m_new);
+      p_s[h * TK + lane] = p;
+      __syncwarp();
+      if (lane == 0) {
+        ml_s[2 * h] = m_new;
+        ml_s[2 * h + 1] = l_old * alpha + psum;
+        al_s[h] = alpha;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int oi = 0; oi < OUTS; ++oi) {
+      const int idx = tid + oi * 256;
+      if (idx < GQ * HD) {
+        const int h = idx / HD, d = idx % HD;
+        float acc = oacc[oi] * al_s[h];
+        const float* pr = p_s + h * TK;
+        for (int j = 0; j < nk; ++j) acc = fmaf(pr[j], Vs[j * HD + d], acc);
+        oacc[oi] = acc;
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && it + NS < ntiles) {
+      const int nx = it + NS;
+      const int t1 = k0 + nx * TK, nk1 = min(TK, k1 - t1);
+      const uint32_t bytes = (uint32_t)nk1 * HD * 4;
+      mbar_expect_tx(&bars[st], 2 * bytes);
+      bulk_load(Ks, kc + (size_t)t1 * HD, bytes, &bars[st]);
+      bulk_load(Vs, vc + (size_t)t1 * HD, bytes, &bars[st]);
+    }
+  }
+  if (failed) {
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      const int hi = min(ntiles, it + NS);
+      for (int cc = it; cc < hi; ++cc)
+        mbar_wait(&bars[cc % NS], (uint32_t)((cc / NS) & 1), kDrainNs);
+    }
+    __syncthreads();
+  }
+
+  if (nsplit == 1) {
+#pragma unroll
+    for (int oi = 0; oi < OUTS; ++oi) {
+      const int idx = tid + oi * 256;
+      if (idx < GQ * HD) {
+        const int h = idx / HD, d = idx % HD;
+        a.out[(size_t)(g * GQ + h) * HD + d] = oacc[oi] / ml_s[2 * h + 1];
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int oi = 0; oi < OUTS; ++oi) {
+    const int idx = tid + oi * 256;
+    if (idx < GQ * HD) {
+      const int h = idx / HD, d = idx % HD;
+      a.part_o[((size_t)(g * GQ + h) * a.nsplit_max + s) * HD + d] = oacc[oi];
+    }
+  }
+  if (tid < GQ) {
+    const size_t o = ((size_t)(g * GQ + tid) * a.nsplit_max + s) * 2;
+    a.part_ml[o] = ml_s[2 * tid];
+    a.part_ml[o + 1] = ml_s[2 * tid + 1];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&a.counters[g], 1);
+    *flag_s = (prev == nsplit - 1);
+  }
+  __syncthreads();
+  if (!*flag_s) return;
+  __threadfence();
+#pragma unroll
+  for (int oi = 0; oi < OUTS; ++oi) {
+    const int idx = tid + oi * 256;
+    if (idx < GQ * HD) {
+      const int h = idx / HD, d = idx % HD;
+      const size_t base = (size_t)(g * GQ + h) * a.nsplit_max;
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(a.part_ml + (base + s2) * 2));
+      float num = 0.f, den = 0.f;
+      for (int s2 = 0; s2 < nsplit; ++s2) {
+        const float w = expf(__ldcg(a.part_ml + (base + s2) * 2) - M);
+        num = fmaf(w, __ldcg(a.part_o + (base + s2) * HD + d), num);
+        den = fmaf(w, __ldcg(a.part_ml + (base + s2) * 2 + 1), den);
+      }
+      a.out[(size_t)(g * GQ + h) * HD + d] = num / den;
+    }
+  }
+  if (tid == 0) a.counters[g] = 0;
+}
+
+size_t attention_smem_bytes(int hd) { return hd == 64 ? attn_smem<64>() : attn_smem<128>(); }
+int attention_gq_max() { return kAttnGQ; }
+
+cudaError_t launch_attention(const AttnArgs& a, int hd, bool pdl, cudaStream_t s) {
+  const dim3 grid(a.nsplit_max, a.nkv);
+  if (hd == 64)
+    return launch_ex(attn_decode_kernel<64>, grid, dim3(256), attn_smem<64>(), s, pdl, a);
+  if (hd == 128)
+    return launch_ex(attn_decode_kernel<128>, grid, dim3(256), attn_smem<128>(), s, pdl, a);
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------------ embedding gather
+// x = f32(E[token]); the token is the host's (mapped ring, by position) or,
+// when the host left -1 there, the previous step's argmax.
+__global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int pos = *a.pos;
+  int tok = a.tok_ring ? a.tok_ring[pos] : -1;
+  if (tok < 0) tok = *a.next_token;
+  if (tok < 0 || tok >= a.V) {
+    if (threadIdx.x == 0) atomicOr(a.err, ERR_TOKEN);
+    tok = 0;
+  }
+  const uint16_t* row = a.table + (size_t)tok * a.H;
+  for (int i = threadIdx.x; i < a.H; i += blockDim.x) {
+    const float v = bf16f(row[i]);
+    a.x[i] = v;
+    if (a.cap_out) a.cap_out[(size_t)pos * a.H + i] = v;
+  }
+}
+
+cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s) {
+  return launch_ex(embed_kernel, dim3(1), dim3(256), 0, s, false, a);
+}
+
+// ------------------------------------------------------------------ RoPE table
+// cos/sin of p * theta^(-2j/hd), formed in fp64 and rounded to f32 once.
+__global__ void rope_table_kernel(float2* t, int cap, int hd, double theta) {
+  const int half = hd / 2;
+  const long long n = (long long)cap * half;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(i / half), j = (int)(i % half);
+    const double inv = pow(theta, -2.0 * (double)j / (double)hd);
+    double sd, cd;
+    sincos((double)p * inv, &sd, &cd);
+    t[i] = make_float2((float)cd, (float)sd);
+  }
+}
+
+cudaError_t launch_rope_table(float2* table, int cap, int hd, float theta, cudaStream_t s) {
+  rope_table_kernel<<<1024, 256, 0, s>>>(table, cap, hd, (double)theta);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ int4 g128 quantiser
+// One warp per group of 128 inputs; a lane handles 4 consecutive values.
+__global__ void __launch_bounds__(256) quantize_int4_kernel(const float* w, int rows, int cols,
+                                                            uint8_t* packed, uint16_t* scales) {
+  const int G = cols / 128;
+  const long long gi = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gi >= (long long)rows * G) return;
+  const int r = (int)(gi / G), g = (int)(gi % G);
+  const float4 v = *reinterpret_cast<const float4*>(w + (size_t)r * cols + g * 128 + lane * 4);
+  float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  m = warp_max(m);
+  const float s32 = __fdiv_rn(m, 7.0f);
+  const uint32_t u = __float_as_uint(s32);
+  const uint16_t sb = (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+  const float sc = bf16f(sb);
+  const float vals[4] = {v.x, v.y, v.z, v.w};
+  uint32_t nib[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float q = 0.f;
+    if (sc != 0.f) q = fminf(7.f, fmaxf(-7.f, rintf(__fdiv_rn(vals[e], sc))));
+    nib[e] = (uint32_t)((int)q + 8);
+  }
+  const uint16_t two = (uint16_t)((nib[0] | (nib[1] << 4)) | ((nib[2] | (nib[3] << 4)) << 8));
+  *reinterpret_cast<uint16_t*>(packed + (size_t)r * (cols / 2) + g * 64 + lane * 2) = two;
+  if (lane == 0) scales[(size_t)r * G + g] = sb;
+}
+
+cudaError_t launch_quantize_int4(const float* w, int rows, int cols, uint8_t* packed,
+                                 uint16_t* scales, cudaStream_t s) {
+  const long long groups = (long long)rows * (cols / 128);
+  if (groups == 0) return cudaSuccess;
+  const long long blocks = (groups + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  quantize_int4_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, rows, cols, packed, scales);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ attributes
+template <class Kern>
+static cudaError_t allow_smem(Kern k, size_t bytes) {
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+cudaError_t set_kernel_attributes() {
+  const size_t big = 227 * 1024;
+  cudaError_t e = cudaSuccess;
+#define QW_ALLOW(k, b) \
+  if (e == cudaSuccess) e = allow_smem(k, b)
+  QW_ALLOW((gemv_kernel<EPI_STORE, 4>), big);
+  QW_ALLOW((gemv_kernel<EPI_STORE, 8>), big);
+  QW_ALLOW((gemv_kernel<EPI_RESIDUAL, 4>), big);
+  QW_ALLOW((gemv_kernel<EPI_RESIDUAL, 8>), big);
+  QW_ALLOW((gemv_kernel<EPI_SWIGLU, 4>), big);
+  QW_ALLOW((gemv_kernel<EPI_SWIGLU, 8>), big);
+  QW_ALLOW((gemv_kernel<EPI_LOGITS, 4>), big);
+  QW_ALLOW((gemv_kernel<EPI_LOGITS, 8>), big);
+  QW_ALLOW(attn_decode_kernel<64>, attn_smem<64>());
+  QW_ALLOW(attn_decode_kernel<128>, attn_smem<128>());
+#undef QW_ALLOW
+  return e;
+}
+
+}  // namespace qw

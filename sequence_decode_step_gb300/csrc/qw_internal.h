@@ -1,0 +1,105 @@
+// Internal interface between the decode kernels and the engine (not part of the ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qw {
+
+// Bits of the device error word.
+enum : int { ERR_TIMEOUT = 1, ERR_TOKEN = 2, ERR_NAN = 4 };
+
+// Wait bound used to drain copies still in flight after a wait gave up.
+constexpr uint64_t kDrainNs = 2000000000ull;
+
+// GEMV epilogues.
+enum : int { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+
+// Where the greedy argmax of the LM head goes (all optional).
+struct ArgmaxOut {
+  float* blk_val;             // [gridDim.x] per-CTA best logit   (scratch)
+  int* blk_idx;               // [gridDim.x] per-CTA best index   (scratch)
+  int* counter;               // arrival counter, 0 between launches (scratch)
+  int* argmax;                // [1] final greedy id (-1 if a logit was NaN)
+  int* next_token;            // [1] token fed to the next step when the host passes none
+  int* pos;                   // [1] device position; incremented after the argmax is known
+  int* tokens_by_pos;         // [cap] argmax recorded at the step's position
+  volatile int* host_status;  // mapped pinned host [2]: argmax, error word
+  volatile int* host_tokens;  // mapped pinned host [cap]: argmax by position
+};
+
+// y = epilogue(W . prologue(x)); W rows grouped in units of `rpu` rows.
+struct GemvArgs {
+  const uint8_t* w;       // packed bf16 rows, unit u = rows [u*rpu, (u+1)*rpu)
+  int n_units;
+  int rpu;                // rows per unit: 1, or 2 for interleaved gate/up
+  int K;                  // input length (multiple of 8)
+  uint32_t row_bytes;     // K * 2
+  const float* x;         // [K] input
+  const uint16_t* norm_g; // RMSNorm gain of the prologue (bf16 [K]) or nullptr
+  float eps;
+  const uint16_t* bias;   // EPI_STORE: bf16 [n_units] or nullptr
+  float* y;               // output
+  float* norm_out;        // if set, CTA 0 writes the normalised input here (row `pos`)
+  float* cap_out;         // EPI_RESIDUAL: if set, the updated y row is also written here
+  const int* pos;         // device position (capture row index) or nullptr
+  // launch geometry, filled by plan_gemv
+  int ks;                 // warps that split K (1, 2, 4 or 8)
+  int cpw;                // 256-column chunks per warp
+  uint32_t stage_bytes;
+  int n_stages;
+  int units_per_stage;
+  uint32_t off_red, off_x, off_stage;  // shared-memory offsets
+  ArgmaxOut am;           // EPI_LOGITS only
+  int* err;
+  uint64_t wait_ns;
+};
+
+struct AttnArgs {
+  const float* qkv;        // raw [(nq + 2 nkv) * hd]
+  const uint16_t* q_norm;  // bf16 [hd] or nullptr
+  const uint16_t* k_norm;
+  const float2* rope;      // [cap][hd/2] (cos, sin) or nullptr (formed in fp64 in-kernel)
+  float rope_theta;
+  float* k_cache;          // [nkv][cap][hd] of this layer
+  float* v_cache;
+  int cap;
+  const int* pos_ptr;      // device position, or nullptr to use pos_const
+  int pos_const;
+  int nq, nkv;
+  float eps;
+  int nsplit_max, min_keys;
+  float* part_o;           // [nq][nsplit_max][hd] (scratch)
+  float* part_ml;          // [nq][nsplit_max][2]  (scratch)
+  int* counters;           // [nkv] arrival counters, 0 between launches (scratch)
+  float* out;              // [nq * hd]
+  int* err;
+  uint64_t wait_ns;
+};
+
+struct EmbedArgs {
+  const uint16_t* table;   // bf16 [V, H]
+  int V, H;
+  const int* pos;
+  const volatile int* tok_ring;  // mapped host [cap]: token for a position, or -1
+  const int* next_token;
+  float* x;                // [H]
+  float* cap_out;          // capture rows [cap][H] or nullptr
+  int* err;
+};
+
+// ---- planning / launching (decode_kernels.cu) ----
+void plan_gemv(GemvArgs& a, int grid, uint32_t max_stage_bytes, int max_stages);
+size_t gemv_smem_bytes(const GemvArgs& a);
+cudaError_t launch_gemv(int epi, const GemvArgs& a, int grid, bool pdl, cudaStream_t s);
+cudaError_t launch_attention(const AttnArgs& a, int hd, bool pdl, cudaStream_t s);
+size_t attention_smem_bytes(int hd);
+int attention_gq_max();
+constexpr int kAttnMinKeys = 64;
+cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s);
+cudaError_t launch_rope_table(float2* table, int cap, int hd, float theta, cudaStream_t s);
+cudaError_t launch_quantize_int4(const float* w, int rows, int cols, uint8_t* packed,
+                                 uint16_t* scales, cudaStream_t s);
+cudaError_t set_kernel_attributes();
+
+}  // namespace qw
