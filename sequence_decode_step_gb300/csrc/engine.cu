@@ -1,0 +1,917 @@
+// The qw_* C ABI: handle, weight packing, decode-step CUDA graph, stand-alone ops.
+//
+// One decode step is recorded once as a CUDA graph on a private stream and
+// replayed on the handle's stream:
+//   embed -> for each layer [QKV GEMV (+RMSNorm, +bias) -> attention (QK-norm,
+//   RoPE, KV append, split-K flash decode, combine) -> o_proj GEMV (+residual)
+//   -> gate/up GEMV (+RMSNorm, SwiGLU) -> down GEMV (+residual)]
+//   -> LM head GEMV (+final RMSNorm, greedy argmax, pos += 1).
+// Every kernel after the first is launched with programmatic dependent launch,
+// so each one streams its weights while its predecessor finishes. The position,
+// the next token and the greedy id stay on the device; the host token for a
+// position is read by the embed kernel from a mapped pinned ring, and the
+// greedy id and the error word are written to mapped pinned memory.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "qw.h"
+#include "qw_internal.h"
+
+using namespace qw;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+struct LayerW {
+  const uint16_t* qkv = nullptr;       // [(nq+2nkv)*hd, H]
+  const uint16_t* qkv_bias = nullptr;  // [(nq+2nkv)*hd] or null
+  const uint16_t* o = nullptr;         // [H, nq*hd]
+  const uint16_t* gateup = nullptr;    // [2I, H], row 2i gate i, row 2i+1 up i
+  const uint16_t* down = nullptr;      // [H, I]
+  const uint16_t* attn_norm = nullptr;
+  const uint16_t* mlp_norm = nullptr;
+  const uint16_t* q_norm = nullptr;
+  const uint16_t* k_norm = nullptr;
+};
+
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev_);
+    if (prev_ != dev) cudaSetDevice(dev);
+    dev_ = dev;
+  }
+  ~DeviceGuard() {
+    if (prev_ != dev_) cudaSetDevice(prev_);
+  }
+
+ private:
+  int prev_ = 0, dev_ = 0;
+};
+
+bool g_attrs_set[64];
+
+cudaError_t ensure_attributes(int dev) {
+  if (dev >= 0 && dev < 64 && g_attrs_set[dev]) return cudaSuccess;
+  cudaError_t e = set_kernel_attributes();
+  if (e == cudaSuccess && dev >= 0 && dev < 64) g_attrs_set[dev] = true;
+  return e;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct qw_handle {
+  qw_config cfg{};
+  int device = 0, num_sms = 0;
+  cudaStream_t stream = nullptr, cap_stream = nullptr;
+  bool own_stream = false;
+  // weights (library-owned arena)
+  uint8_t* warena = nullptr;
+  size_t warena_bytes = 0;
+  std::vector<LayerW> layers;
+  const uint16_t* embed = nullptr;
+  const uint16_t* lm_head = nullptr;  // aliases embed when tied
+  const uint16_t* final_norm = nullptr;
+  bool weights_loaded = false;
+  // state buffers (one device allocation)
+  uint8_t* sarena = nullptr;
+  float* k_cache = nullptr;  // [L][nkv][cap][hd]
+  float* v_cache = nullptr;
+  float* x = nullptr;
+  float* qkv = nullptr;
+  float* attn_o = nullptr;
+  float* mlp = nullptr;
+  float* logits = nullptr;
+  float2* rope = nullptr;
+  float* part_o = nullptr;
+  float* part_ml = nullptr;
+  int* attn_counters = nullptr;
+  float* blk_val = nullptr;
+  int* blk_idx = nullptr;
+  int* am_counter = nullptr;
+  int* d_pos = nullptr;
+  int* d_next_token = nullptr;
+  int* d_argmax = nullptr;
+  int* d_err = nullptr;
+  int* d_tokens_by_pos = nullptr;
+  int nsplit_max = 1;
+  int lm_grid = 1;
+  // mapped pinned host memory
+  int* h_tok_ring = nullptr;  // [cap]
+  int* h_status = nullptr;    // [2]
+  int* h_tokens = nullptr;    // [cap]
+  int* hd_tok_ring = nullptr;
+  int* hd_status = nullptr;
+  int* hd_tokens = nullptr;
+  // checkpoints
+  bool capture_on = false, cap_valid = false;
+  float* cap_emb = nullptr;
+  float* cap_blk0 = nullptr;
+  float* cap_final = nullptr;
+  int cap_row0 = 0, cap_rows = 0;
+  // graph
+  cudaGraphExec_t exec = nullptr;
+  bool graph_dirty = true;
+  uint64_t wait_ns = 1000000000ull;
+  // host mirror
+  int pos = 0;
+  bool have_prev = false;
+  std::string err;
+};
+
+#define QW_FAIL(h, code, msg)                 \
+  do {                                        \
+    if (h) (h)->err = (msg);                  \
+    else g_last_error = (msg);                \
+    return (code);                            \
+  } while (0)
+
+#define QW_CUDA(h, call)                                                        \
+  do {                                                                          \
+    cudaError_t e_ = (call);                                                    \
+    if (e_ != cudaSuccess) {                                                    \
+      std::string m_ = std::string(#call) + ": " + cudaGetErrorString(e_);      \
+      QW_FAIL(h, QW_ERR_CUDA, m_);                                              \
+    }                                                                           \
+  } while (0)
+
+// ============================================================================ create / destroy
+static int validate_config(const qw_config* c, std::string& why) {
+  if (c->n_layers <= 0 || c->hidden <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 ||
+      c->head_dim <= 0 || c->intermediate <= 0 || c->vocab <= 0) {
+    why = "every dimension must be positive";
+    return QW_ERR_ARG;
+  }
+  if (c->head_dim != 64 && c->head_dim != 128) {
+    why = "head_dim must be 64 or 128";
+    return QW_ERR_ARG;
+  }
+  if (c->n_q_heads % c->n_kv_heads != 0 ||
+      c->n_q_heads / c->n_kv_heads > attention_gq_max()) {
+    why = "n_q_heads must be a multiple of n_kv_heads, at most 8 per kv head";
+    return QW_ERR_ARG;
+  }
+  const int mult = c->weight_format == QW_WEIGHTS_INT4_G128 ? 128 : 8;
+  if (c->hidden % mult || (c->n_q_heads * c->head_dim) % mult || c->intermediate % mult) {
+    why = "hidden, n_q_heads*head_dim and intermediate must be multiples of 8 (128 for int4)";
+    return QW_ERR_ARG;
+  }
+  if (c->hidden > 16384 || c->intermediate > 16384 || c->n_q_heads * c->head_dim > 16384) {
+    why = "hidden, intermediate and n_q_heads*head_dim are limited to 16384";
+    return QW_ERR_ARG;
+  }
+  if (c->weight_format != QW_WEIGHTS_BF16) {
+    why = "weight_format: only QW_WEIGHTS_BF16 is implemented in this build";
+    return QW_ERR_ARG;
+  }
+  if (c->max_ctx <= 0 || c->max_prefill_t < 0) {
+    why = "max_ctx must be positive and max_prefill_t non-negative";
+    return QW_ERR_ARG;
+  }
+  if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) {
+    why = "eps must be >= 0 and rope_theta > 0";
+    return QW_ERR_ARG;
+  }
+  return QW_OK;
+}
+
+static void free_handle(qw_handle* h) {
+  if (!h) return;
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->warena) cudaFree(h->warena);
+  if (h->sarena) cudaFree(h->sarena);
+  if (h->cap_emb) cudaFree(h->cap_emb);
+  if (h->h_tok_ring) cudaFreeHost(h->h_tok_ring);
+  if (h->h_status) cudaFreeHost(h->h_status);
+  if (h->h_tokens) cudaFreeHost(h->h_tokens);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->own_stream && h->stream) cudaStreamDestroy(h->stream);
+  delete h;
+}
+
+static int alloc_state(qw_handle* h) {
+  const qw_config& c = h->cfg;
+  const size_t L = c.n_layers, nkv = c.n_kv_heads, hd = c.head_dim, cap = c.max_ctx;
+  const size_t qkv_rows = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * hd;
+  h->nsplit_max = std::max(1, h->num_sms / c.n_kv_heads);
+  h->lm_grid = std::min({c.vocab, h->num_sms, 1024});
+  struct Piece { void** p; size_t bytes; };
+  const size_t kv_bytes = L * nkv * cap * hd * 4;
+  std::vector<Piece> pieces = {
+      {(void**)&h->k_cache, kv_bytes},
+      {(void**)&h->v_cache, kv_bytes},
+      {(void**)&h->x, (size_t)c.hidden * 4},
+      {(void**)&h->qkv, qkv_rows * 4},
+      {(void**)&h->attn_o, (size_t)c.n_q_heads * hd * 4},
+      {(void**)&h->mlp, (size_t)c.intermediate * 4},
+      {(void**)&h->logits, (size_t)c.vocab * 4},
+      {(void**)&h->rope, cap * (hd / 2) * sizeof(float2)},
+      {(void**)&h->part_o, (size_t)c.n_q_heads * h->nsplit_max * hd * 4},
+      {(void**)&h->part_ml, (size_t)c.n_q_heads * h->nsplit_max * 2 * 4},
+      {(void**)&h->attn_counters, nkv * 4},
+      {(void**)&h->blk_val, (size_t)h->lm_grid * 4},
+      {(void**)&h->blk_idx, (size_t)h->lm_grid * 4},
+      {(void**)&h->am_counter, 4},
+      {(void**)&h->d_pos, 4},
+      {(void**)&h->d_next_token, 4},
+      {(void**)&h->d_argmax, 4},
+      {(void**)&h->d_err, 4},
+      {(void**)&h->d_tokens_by_pos, cap * 4},
+  };
+  size_t total = 0;
+  for (auto& p : pieces) total = align_up(total, 256) + p.bytes;
+  QW_CUDA(h, cudaMalloc((void**)&h->sarena, total));
+  QW_CUDA(h, cudaMemsetAsync(h->sarena, 0, total, h->stream));
+  size_t off = 0;
+  for (auto& p : pieces) {
+    off = align_up(off, 256);
+    *p.p = h->sarena + off;
+    off += p.bytes;
+  }
+  QW_CUDA(h, cudaHostAlloc((void**)&h->h_tok_ring, cap * 4, cudaHostAllocMapped | cudaHostAllocPortable));
+  QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, cap * 4, cudaHostAllocMapped | cudaHostAllocPortable));
+  QW_CUDA(h, cudaHostAlloc((void**)&h->h_status, 64, cudaHostAllocMapped | cudaHostAllocPortable));
+  memset(h->h_tok_ring, 0xff, cap * 4);
+  memset(h->h_tokens, 0xff, cap * 4);
+  h->h_status[0] = -1;
+  h->h_status[1] = 0;
+  QW_CUDA(h, cudaHostGetDevicePointer((void**)&h->hd_tok_ring, h->h_tok_ring, 0));
+  QW_CUDA(h, cudaHostGetDevicePointer((void**)&h->hd_tokens, h->h_tokens, 0));
+  QW_CUDA(h, cudaHostGetDevicePointer((void**)&h->hd_status, h->h_status, 0));
+  QW_CUDA(h, launch_rope_table(h->rope, c.max_ctx, c.head_dim, c.rope_theta, h->stream));
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  return QW_OK;
+}
+
+extern "C" uint32_t qw_abi_version(void) { return QW_ABI_VERSION; }
+extern "C" size_t qw_sizeof_config(void) { return sizeof(qw_config); }
+extern "C" size_t qw_sizeof_weights(void) { return sizeof(qw_weights); }
+extern "C" size_t qw_sizeof_lora(void) { return sizeof(qw_lora); }
+
+extern "C" int qw_create(const qw_config* cfg, void* cuda_stream, qw_handle** out) {
+  if (!cfg || !out) QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_create: null argument");
+  if (cfg->struct_size != sizeof(qw_config) || cfg->abi_version != QW_ABI_VERSION)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ABI,
+            "qw_create: qw_config struct_size/abi_version does not match this library");
+  std::string why;
+  int rc = validate_config(cfg, why);
+  if (rc) QW_FAIL((qw_handle*)nullptr, rc, "qw_create: " + why);
+  qw_handle* h = new qw_handle();
+  h->cfg = *cfg;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e == cudaSuccess) e = ensure_attributes(h->device);
+  if (e == cudaSuccess) {
+    if (cuda_stream) {
+      h->stream = (cudaStream_t)cuda_stream;
+    } else {
+      e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
+      h->own_stream = true;
+    }
+  }
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    g_last_error = std::string("qw_create: ") + cudaGetErrorString(e);
+    free_handle(h);
+    return QW_ERR_CUDA;
+  }
+  rc = alloc_state(h);
+  if (rc) {
+    g_last_error = "qw_create: " + h->err;
+    free_handle(h);
+    return rc;
+  }
+  *out = h;
+  return QW_OK;
+}
+
+extern "C" void qw_destroy(qw_handle* h) {
+  if (!h) return;
+  DeviceGuard dg(h->device);
+  cudaStreamSynchronize(h->stream);
+  free_handle(h);
+}
+
+extern "C" const char* qw_last_error(const qw_handle* h) {
+  return h ? h->err.c_str() : g_last_error.c_str();
+}
+
+// ============================================================================ weights
+extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
+  if (!h || !w) QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: null argument");
+  if (w->struct_size != sizeof(qw_weights))
+    QW_FAIL(h, QW_ERR_ABI, "qw_load_weights: qw_weights struct_size does not match this library");
+  DeviceGuard dg(h->device);
+  const qw_config& c = h->cfg;
+  const int L = c.n_layers;
+  const size_t H = c.hidden, I = c.intermediate, hd = c.head_dim;
+  const size_t qd = (size_t)c.n_q_heads * hd, kd = (size_t)c.n_kv_heads * hd;
+  if (!w->embed || !w->final_norm || !w->attn_norm || !w->q || !w->k || !w->v || !w->o ||
+      !w->mlp_norm || !w->gate || !w->up || !w->down)
+    QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: a required tensor is NULL");
+  if (c.tie_word_embeddings ? (w->lm_head != nullptr) : (w->lm_head == nullptr))
+    QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: lm_head must be NULL iff tie_word_embeddings");
+  if (c.qk_norm && (!w->q_norm || !w->k_norm))
+    QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: qk_norm set but q_norm/k_norm missing");
+  if (c.qkv_bias && (!w->q_bias || !w->k_bias || !w->v_bias))
+    QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: qkv_bias set but a bias is missing");
+  for (int l = 0; l < L; ++l) {
+    if (!w->attn_norm[l] || !w->q[l] || !w->k[l] || !w->v[l] || !w->o[l] || !w->mlp_norm[l] ||
+        !w->gate[l] || !w->up[l] || !w->down[l] || (c.qk_norm && (!w->q_norm[l] || !w->k_norm[l])) ||
+        (c.qkv_bias && (!w->q_bias[l] || !w->k_bias[l] || !w->v_bias[l])))
+      QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: NULL per-layer pointer at layer " + std::to_string(l));
+  }
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  if (h->exec) {
+    cudaGraphExecDestroy(h->exec);
+    h->exec = nullptr;
+  }
+  h->graph_dirty = true;
+  h->weights_loaded = false;
+  if (h->warena) {
+    cudaFree(h->warena);
+    h->warena = nullptr;
+  }
+  // Arena layout, 256-byte aligned pieces.
+  const size_t per_layer = align_up((qd + 2 * kd) * H * 2, 256) +
+                           (c.qkv_bias ? align_up((qd + 2 * kd) * 2, 256) : 0) +
+                           align_up(H * qd * 2, 256) + align_up(2 * I * H * 2, 256) +
+                           align_up(H * I * 2, 256) + 2 * align_up(H * 2, 256) +
+                           (c.qk_norm ? 2 * align_up(hd * 2, 256) : 0);
+  const size_t head = align_up((size_t)c.vocab * H * 2, 256) +
+                      (c.tie_word_embeddings ? 0 : align_up((size_t)c.vocab * H * 2, 256)) +
+                      align_up(H * 2, 256);
+  h->warena_bytes = per_layer * L + head;
+  QW_CUDA(h, cudaMalloc((void**)&h->warena, h->warena_bytes));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = h->warena + off;
+    off += align_up(bytes, 256);
+    return p;
+  };
+  auto cp = [&](void* dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, h->stream);
+  };
+  uint8_t* p = take((size_t)c.vocab * H * 2);
+  QW_CUDA(h, cp(p, w->embed, (size_t)c.vocab * H * 2));
+  h->embed = (const uint16_t*)p;
+  if (c.tie_word_embeddings) {
+    h->lm_head = h->embed;  // one table serves the gather and the output projection
+  } else {
+    p = take((size_t)c.vocab * H * 2);
+    QW_CUDA(h, cp(p, w->lm_head, (size_t)c.vocab * H * 2));
+    h->lm_head = (const uint16_t*)p;
+  }
+  p = take(H * 2);
+  QW_CUDA(h, cp(p, w->final_norm, H * 2));
+  h->final_norm = (const uint16_t*)p;
+  h->layers.assign(L, LayerW());
+  for (int l = 0; l < L; ++l) {
+    LayerW& lw = h->layers[l];
+    p = take((qd + 2 * kd) * H * 2);  // fused [q; k; v] rows
+    QW_CUDA(h, cp(p, w->q[l], qd * H * 2));
+    QW_CUDA(h, cp(p + qd * H * 2, w->k[l], kd * H * 2));
+    QW_CUDA(h, cp(p + (qd + kd) * H * 2, w->v[l], kd * H * 2));
+    lw.qkv = (const uint16_t*)p;
+    if (c.qkv_bias) {
+      p = take((qd + 2 * kd) * 2);
+      QW_CUDA(h, cp(p, w->q_bias[l], qd * 2));
+      QW_CUDA(h, cp(p + qd * 2, w->k_bias[l], kd * 2));
+      QW_CUDA(h, cp(p + (qd + kd) * 2, w->v_bias[l], kd * 2));
+      lw.qkv_bias = (const uint16_t*)p;
+    }
+    p = take(H * qd * 2);
+    QW_CUDA(h, cp(p, w->o[l], H * qd * 2));
+    lw.o = (const uint16_t*)p;
+    p = take(2 * I * H * 2);  // gate row i -> packed row 2i, up row i -> 2i+1
+    QW_CUDA(h, cudaMemcpy2DAsync(p, 2 * H * 2, w->gate[l], H * 2, H * 2, I,
+                                 cudaMemcpyDeviceToDevice, h->stream));
+    QW_CUDA(h, cudaMemcpy2DAsync(p + H * 2, 2 * H * 2, w->up[l], H * 2, H * 2, I,
+                                 cudaMemcpyDeviceToDevice, h->stream));
+    lw.gateup = (const uint16_t*)p;
+    p = take(H * I * 2);
+    QW_CUDA(h, cp(p, w->down[l], H * I * 2));
+    lw.down = (const uint16_t*)p;
+    p = take(H * 2);
+    QW_CUDA(h, cp(p, w->attn_norm[l], H * 2));
+    lw.attn_norm = (const uint16_t*)p;
+    p = take(H * 2);
+    QW_CUDA(h, cp(p, w->mlp_norm[l], H * 2));
+    lw.mlp_norm = (const uint16_t*)p;
+    if (c.qk_norm) {
+      p = take(hd * 2);
+      QW_CUDA(h, cp(p, w->q_norm[l], hd * 2));
+      lw.q_norm = (const uint16_t*)p;
+      p = take(hd * 2);
+      QW_CUDA(h, cp(p, w->k_norm[l], hd * 2));
+      lw.k_norm = (const uint16_t*)p;
+    }
+  }
+  QW_CUDA(h, cudaMemsetAsync(h->d_pos, 0, 4, h->stream));
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  h->pos = 0;
+  h->have_prev = false;
+  h->cap_valid = false;
+  h->weights_loaded = true;
+  return QW_OK;
+}
+
+// ============================================================================ the step graph
+static constexpr uint32_t kSingleStageMax = 112 * 1024;  // whole CTA slice in one stage
+static constexpr uint32_t kStreamStage = 32 * 1024;      // else: 4 stages of 32 KB
+static constexpr int kStreamStages = 4;
+
+static void plan(GemvArgs& a, int grid) {
+  const uint64_t units_max = ((uint64_t)a.n_units + grid - 1) / grid;
+  if (units_max * a.rpu * a.row_bytes <= kSingleStageMax)
+    plan_gemv(a, grid, kSingleStageMax, 1);
+  else
+    plan_gemv(a, grid, kStreamStage, kStreamStages);
+}
+
+static GemvArgs base_gemv(qw_handle* h, const void* w, int n_units, int rpu, int K) {
+  GemvArgs a{};
+  a.w = (const uint8_t*)w;
+  a.n_units = n_units;
+  a.rpu = rpu;
+  a.K = K;
+  a.row_bytes = (uint32_t)K * 2;
+  a.eps = h->cfg.eps;
+  a.err = h->d_err;
+  a.wait_ns = h->wait_ns;
+  a.pos = h->d_pos;
+  return a;
+}
+
+// Launch one step's kernels on stream s (recorded into the graph).
+static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
+  const qw_config& c = h->cfg;
+  const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
+  const int qd = c.n_q_heads * hd, kd = c.n_kv_heads * hd;
+  const int qkv_rows = qd + 2 * kd;
+  const size_t kv_layer = (size_t)c.n_kv_heads * c.max_ctx * hd;
+  cudaError_t e;
+
+  EmbedArgs ea{};
+  ea.table = h->embed;
+  ea.V = c.vocab;
+  ea.H = H;
+  ea.pos = h->d_pos;
+  ea.tok_ring = h->hd_tok_ring;
+  ea.next_token = h->d_next_token;
+  ea.x = h->x;
+  ea.cap_out = h->capture_on ? h->cap_emb : nullptr;
+  ea.err = h->d_err;
+  if ((e = launch_embed(ea, s)) != cudaSuccess) return e;
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& lw = h->layers[l];
+    {  // fused QKV projection with the input RMSNorm in its prologue
+      GemvArgs a = base_gemv(h, lw.qkv, qkv_rows, 1, H);
+      a.x = h->x;
+      a.norm_g = lw.attn_norm;
+      a.bias = lw.qkv_bias;
+      a.y = h->qkv;
+      const int grid = std::min(qkv_rows, h->num_sms);
+      plan(a, grid);
+      if ((e = launch_gemv(EPI_STORE, a, grid, true, s)) != cudaSuccess) return e;
+    }
+    {  // QK-norm, RoPE, KV append, split-K flash decode, combine
+      AttnArgs t{};
+      t.qkv = h->qkv;
+      t.q_norm = lw.q_norm;
+      t.k_norm = lw.k_norm;
+      t.rope = h->rope;
+      t.rope_theta = c.rope_theta;
+      t.k_cache = h->k_cache + (size_t)l * kv_layer;
+      t.v_cache = h->v_cache + (size_t)l * kv_layer;
+      t.cap = c.max_ctx;
+      t.pos_ptr = h->d_pos;
+      t.nq = c.n_q_heads;
+      t.nkv = c.n_kv_heads;
+      t.eps = c.eps;
+      t.nsplit_max = h->nsplit_max;
+      t.min_keys = kAttnMinKeys;
+      t.part_o = h->part_o;
+      t.part_ml = h->part_ml;
+      t.counters = h->attn_counters;
+      t.out = h->attn_o;
+      t.err = h->d_err;
+      t.wait_ns = h->wait_ns;
+      if ((e = launch_attention(t, hd, true, s)) != cudaSuccess) return e;
+    }
+    {  // o_proj + residual
+      GemvArgs a = base_gemv(h, lw.o, H, 1, qd);
+      a.x = h->attn_o;
+      a.y = h->x;
+      const int grid = std::min(H, h->num_sms);
+      plan(a, grid);
+      if ((e = launch_gemv(EPI_RESIDUAL, a, grid, true, s)) != cudaSuccess) return e;
+    }
+    {  // gate/up with the post-attention RMSNorm in its prologue, SwiGLU epilogue
+      GemvArgs a = base_gemv(h, lw.gateup, I, 2, H);
+      a.x = h->x;
+      a.norm_g = lw.mlp_norm;
+      a.y = h->mlp;
+      const int grid = std::min(I, h->num_sms);
+      plan(a, grid);
+      if ((e = launch_gemv(EPI_SWIGLU, a, grid, true, s)) != cudaSuccess) return e;
+    }
+    {  // down + residual (block-0 checkpoint taken here)
+      GemvArgs a = base_gemv(h, lw.down, H, 1, I);
+      a.x = h->mlp;
+      a.y = h->x;
+      a.cap_out = (h->capture_on && l == 0) ? h->cap_blk0 : nullptr;
+      const int grid = std::min(H, h->num_sms);
+      plan(a, grid);
+      if ((e = launch_gemv(EPI_RESIDUAL, a, grid, true, s)) != cudaSuccess) return e;
+    }
+  }
+  {  // final RMSNorm + LM head + greedy argmax; advances the device position
+    GemvArgs a = base_gemv(h, h->lm_head, c.vocab, 1, H);
+    a.x = h->x;
+    a.norm_g = h->final_norm;
+    a.y = h->logits;
+    a.norm_out = h->capture_on ? h->cap_final : nullptr;
+    a.am.blk_val = h->blk_val;
+    a.am.blk_idx = h->blk_idx;
+    a.am.counter = h->am_counter;
+    a.am.argmax = h->d_argmax;
+    a.am.next_token = h->d_next_token;
+    a.am.pos = h->d_pos;
+    a.am.tokens_by_pos = h->d_tokens_by_pos;
+    a.am.host_status = h->hd_status;
+    a.am.host_tokens = h->hd_tokens;
+    plan_gemv(a, h->lm_grid, kStreamStage, kStreamStages);
+    if ((e = launch_gemv(EPI_LOGITS, a, h->lm_grid, true, s)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+static int ensure_graph(qw_handle* h) {
+  if (h->exec && !h->graph_dirty) return QW_OK;
+  if (h->exec) {
+    cudaGraphExecDestroy(h->exec);
+    h->exec = nullptr;
+  }
+  QW_CUDA(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  const cudaError_t le = record_step(h, h->cap_stream);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(h->cap_stream, &graph);
+  if (le != cudaSuccess || ce != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    QW_FAIL(h, QW_ERR_CUDA,
+            std::string("recording the decode step: ") +
+                cudaGetErrorString(le != cudaSuccess ? le : ce));
+  }
+  const cudaError_t ie = cudaGraphInstantiate(&h->exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ie != cudaSuccess) {
+    h->exec = nullptr;
+    QW_FAIL(h, QW_ERR_CUDA, std::string("cudaGraphInstantiate: ") + cudaGetErrorString(ie));
+  }
+  h->graph_dirty = false;
+  return QW_OK;
+}
+
+// Synchronise, then turn the device error word into a status (and clear it).
+static int finish_sync(qw_handle* h) {
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  const int err = ((volatile int*)h->h_status)[1];
+  if (err == 0) return QW_OK;
+  h->h_status[1] = 0;
+  QW_CUDA(h, cudaMemsetAsync(h->d_err, 0, 4, h->stream));
+  QW_CUDA(h, cudaMemsetAsync(h->attn_counters, 0, (size_t)h->cfg.n_kv_heads * 4, h->stream));
+  QW_CUDA(h, cudaMemsetAsync(h->am_counter, 0, 4, h->stream));
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  if (err & ERR_TIMEOUT)
+    QW_FAIL(h, QW_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up; outputs are invalid");
+  if (err & ERR_TOKEN)
+    QW_FAIL(h, QW_ERR_ARG, "the device saw a token outside [0, vocab); token 0 was used");
+  QW_FAIL(h, QW_ERR_NUMERIC, "a logit was NaN; there is no greedy token");
+}
+
+static int check_ready(qw_handle* h, const char* fn) {
+  if (!h) QW_FAIL(h, QW_ERR_ARG, std::string(fn) + ": null handle");
+  if (!h->weights_loaded) QW_FAIL(h, QW_ERR_STATE, std::string(fn) + ": weights not loaded");
+  return QW_OK;
+}
+
+// Queue n graph replays; the host tokens for positions pos..pos+n-1 are in the ring.
+static int run_steps(qw_handle* h, int n) {
+  int rc = ensure_graph(h);
+  if (rc) return rc;
+  h->h_status[0] = -1;
+  for (int i = 0; i < n; ++i) QW_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
+  return QW_OK;
+}
+
+// ============================================================================ stepping
+extern "C" int qw_decode_step(qw_handle* h, int32_t token, float* logits_dev, int32_t* argmax_host) {
+  int rc = check_ready(h, "qw_decode_step");
+  if (rc) return rc;
+  if (token >= h->cfg.vocab) QW_FAIL(h, QW_ERR_ARG, "qw_decode_step: token >= vocab");
+  if (token < 0 && !h->have_prev)
+    QW_FAIL(h, QW_ERR_STATE, "qw_decode_step: token < 0 but no previous step to feed from");
+  if (h->pos + 1 > h->cfg.max_ctx) QW_FAIL(h, QW_ERR_CTX, "qw_decode_step: context is full");
+  DeviceGuard dg(h->device);
+  h->h_tok_ring[h->pos] = token < 0 ? -1 : token;
+  rc = run_steps(h, 1);
+  if (rc) return rc;
+  if (logits_dev)
+    QW_CUDA(h, cudaMemcpyAsync(logits_dev, h->logits, (size_t)h->cfg.vocab * 4,
+                               cudaMemcpyDeviceToDevice, h->stream));
+  h->cap_valid = h->capture_on;
+  h->cap_row0 = h->pos;
+  h->cap_rows = 1;
+  h->pos += 1;
+  h->have_prev = true;
+  if (argmax_host) {
+    rc = finish_sync(h);
+    if (rc) return rc;
+    *argmax_host = ((volatile int*)h->h_status)[0];
+  }
+  return QW_OK;
+}
+
+extern "C" int qw_decode_greedy(qw_handle* h, int32_t token, int32_t n_steps, int32_t* ids_host) {
+  int rc = check_ready(h, "qw_decode_greedy");
+  if (rc) return rc;
+  if (n_steps <= 0) QW_FAIL(h, QW_ERR_ARG, "qw_decode_greedy: n_steps must be positive");
+  if (token >= h->cfg.vocab) QW_FAIL(h, QW_ERR_ARG, "qw_decode_greedy: token >= vocab");
+  if (token < 0 && !h->have_prev)
+    QW_FAIL(h, QW_ERR_STATE, "qw_decode_greedy: token < 0 but no previous step to feed from");
+  if ((int64_t)h->pos + n_steps > h->cfg.max_ctx)
+    QW_FAIL(h, QW_ERR_CTX, "qw_decode_greedy: pos + n_steps > max_ctx");
+  DeviceGuard dg(h->device);
+  const int p0 = h->pos;
+  h->h_tok_ring[p0] = token < 0 ? -1 : token;
+  for (int i = 1; i < n_steps; ++i) h->h_tok_ring[p0 + i] = -1;
+  rc = run_steps(h, n_steps);
+  if (rc) return rc;
+  h->cap_valid = h->capture_on;
+  h->cap_row0 = p0 + n_steps - 1;
+  h->cap_rows = 1;
+  h->pos += n_steps;
+  h->have_prev = true;
+  rc = finish_sync(h);
+  if (rc) return rc;
+  if (ids_host)
+    for (int i = 0; i < n_steps; ++i) ids_host[i] = ((volatile int*)h->h_tokens)[p0 + i];
+  return QW_OK;
+}
+
+extern "C" int qw_prefill(qw_handle* h, const int32_t* ids_host, int32_t T, float* logits_dev,
+                          int32_t* argmax_host) {
+  int rc = check_ready(h, "qw_prefill");
+  if (rc) return rc;
+  if (!ids_host || T <= 0) QW_FAIL(h, QW_ERR_ARG, "qw_prefill: empty prompt");
+  for (int i = 0; i < T; ++i)
+    if (ids_host[i] < 0 || ids_host[i] >= h->cfg.vocab)
+      QW_FAIL(h, QW_ERR_ARG, "qw_prefill: id " + std::to_string(i) + " outside [0, vocab)");
+  if ((int64_t)h->pos + T > h->cfg.max_ctx)
+    QW_FAIL(h, QW_ERR_CTX, "qw_prefill: pos + T > max_ctx");
+  DeviceGuard dg(h->device);
+  const int p0 = h->pos;
+  // Sequential path: one decode step per prompt id, all queued before one sync.
+  for (int i = 0; i < T; ++i) h->h_tok_ring[p0 + i] = ids_host[i];
+  rc = run_steps(h, T);
+  if (rc) return rc;
+  if (logits_dev)
+    QW_CUDA(h, cudaMemcpyAsync(logits_dev, h->logits, (size_t)h->cfg.vocab * 4,
+                               cudaMemcpyDeviceToDevice, h->stream));
+  h->cap_valid = h->capture_on;
+  h->cap_row0 = p0;
+  h->cap_rows = T;
+  h->pos += T;
+  h->have_prev = true;
+  if (argmax_host) {
+    rc = finish_sync(h);
+    if (rc) return rc;
+    *argmax_host = ((volatile int*)h->h_status)[0];
+  }
+  return QW_OK;
+}
+
+extern "C" int qw_reset(qw_handle* h) {
+  if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_reset: null handle");
+  DeviceGuard dg(h->device);
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  QW_CUDA(h, cudaMemsetAsync(h->d_pos, 0, 4, h->stream));
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  h->pos = 0;
+  h->have_prev = false;
+  h->cap_valid = false;
+  return QW_OK;
+}
+
+extern "C" int qw_set_pos(qw_handle* h, int32_t pos) {
+  if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_pos: null handle");
+  if (pos < 0 || pos > h->cfg.max_ctx) QW_FAIL(h, QW_ERR_CTX, "qw_set_pos: pos outside [0, max_ctx]");
+  DeviceGuard dg(h->device);
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  h->h_status[0] = pos;  // staging value for the copy below
+  QW_CUDA(h, cudaMemcpyAsync(h->d_pos, &h->h_status[0], 4, cudaMemcpyHostToDevice, h->stream));
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  h->pos = pos;
+  h->cap_valid = false;
+  return QW_OK;
+}
+
+extern "C" int qw_get_pos(const qw_handle* h, int32_t* pos) {
+  if (!h || !pos) return QW_ERR_ARG;
+  *pos = h->pos;
+  return QW_OK;
+}
+
+extern "C" int qw_kv_cache(qw_handle* h, int32_t layer, float** k_dev, float** v_dev) {
+  if (!h || !k_dev || !v_dev) QW_FAIL(h, QW_ERR_ARG, "qw_kv_cache: null argument");
+  if (layer < 0 || layer >= h->cfg.n_layers) QW_FAIL(h, QW_ERR_ARG, "qw_kv_cache: bad layer");
+  const size_t kv_layer = (size_t)h->cfg.n_kv_heads * h->cfg.max_ctx * h->cfg.head_dim;
+  *k_dev = h->k_cache + (size_t)layer * kv_layer;
+  *v_dev = h->v_cache + (size_t)layer * kv_layer;
+  return QW_OK;
+}
+
+extern "C" int qw_set_lora(qw_handle* h, const qw_lora* lora) {
+  if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_lora: null handle");
+  if (lora == nullptr) return QW_OK;
+  if (lora->struct_size != sizeof(qw_lora)) QW_FAIL(h, QW_ERR_ABI, "qw_set_lora: struct_size mismatch");
+  QW_FAIL(h, QW_ERR_ARG, "qw_set_lora: LoRA is not implemented in this build");
+}
+
+extern "C" int qw_set_wait_limit_ns(qw_handle* h, uint64_t ns) {
+  if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_wait_limit_ns: null handle");
+  h->wait_ns = ns;
+  h->graph_dirty = true;
+  return QW_OK;
+}
+
+// ============================================================================ checkpoints
+extern "C" int qw_set_capture(qw_handle* h, int32_t enable) {
+  if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_capture: null handle");
+  DeviceGuard dg(h->device);
+  const bool on = enable != 0;
+  if (on && !h->cap_emb) {
+    const size_t rows = (size_t)h->cfg.max_ctx * h->cfg.hidden;
+    QW_CUDA(h, cudaMalloc((void**)&h->cap_emb, 3 * rows * 4));
+    h->cap_blk0 = h->cap_emb + rows;
+    h->cap_final = h->cap_emb + 2 * rows;
+  }
+  if (on != h->capture_on) h->graph_dirty = true;
+  h->capture_on = on;
+  h->cap_valid = false;
+  return QW_OK;
+}
+
+extern "C" int qw_capture_size(qw_handle* h, int32_t which, size_t* n_floats) {
+  if (!h || !n_floats) QW_FAIL(h, QW_ERR_ARG, "qw_capture_size: null argument");
+  if (which < 0 || which > 3) QW_FAIL(h, QW_ERR_ARG, "qw_capture_size: which must be 0..3");
+  if (!h->cap_valid) QW_FAIL(h, QW_ERR_NOT_CAPTURED, "qw_capture_size: nothing captured");
+  *n_floats = which == QW_CAPTURE_LOGITS ? (size_t)h->cfg.vocab
+                                         : (size_t)h->cap_rows * h->cfg.hidden;
+  return QW_OK;
+}
+
+extern "C" int qw_get_capture(qw_handle* h, int32_t which, float* out_host, size_t n_floats) {
+  size_t need = 0;
+  int rc = qw_capture_size(h, which, &need);
+  if (rc) return rc;
+  if (!out_host) QW_FAIL(h, QW_ERR_ARG, "qw_get_capture: null buffer");
+  if (n_floats < need) QW_FAIL(h, QW_ERR_SIZE, "qw_get_capture: buffer too small");
+  DeviceGuard dg(h->device);
+  const float* src = which == QW_CAPTURE_LOGITS ? h->logits
+                     : (which == QW_CAPTURE_EMBEDDING ? h->cap_emb
+                        : which == QW_CAPTURE_BLOCK0 ? h->cap_blk0 : h->cap_final) +
+                           (size_t)h->cap_row0 * h->cfg.hidden;
+  QW_CUDA(h, cudaMemcpyAsync(out_host, src, need * 4, cudaMemcpyDeviceToHost, h->stream));
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  return QW_OK;
+}
+
+// ============================================================================ stand-alone ops
+static int op_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QW_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QW_ERR_CUDA;
+  if (ensure_attributes(dev) != cudaSuccess) return QW_ERR_CUDA;
+  return QW_OK;
+}
+
+#define QW_OP_CUDA(call)                                                        \
+  do {                                                                          \
+    cudaError_t e_ = (call);                                                    \
+    if (e_ != cudaSuccess) {                                                    \
+      g_last_error = std::string(#call) + ": " + cudaGetErrorString(e_);        \
+      return QW_ERR_CUDA;                                                       \
+    }                                                                           \
+  } while (0)
+
+extern "C" int qw_quantize_int4_g128(const float* w, int32_t rows, int32_t cols, uint8_t* packed,
+                                     uint16_t* scales, void* stream) {
+  if (!w || !packed || !scales || rows <= 0 || cols <= 0 || cols % 128)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            "qw_quantize_int4_g128: null buffer, empty shape or cols % 128 != 0");
+  QW_OP_CUDA(launch_quantize_int4(w, rows, cols, packed, scales, (cudaStream_t)stream));
+  return QW_OK;
+}
+
+// Attention workspace: [counters (nkv ints) | err int] padded to 256, part_ml, part_o.
+extern "C" size_t qw_attention_workspace_bytes(int32_t nq, int32_t nkv, int32_t hd,
+                                               int32_t n_splits) {
+  if (nq <= 0 || nkv <= 0 || hd <= 0 || n_splits <= 0) return 0;
+  return align_up(((size_t)nkv + 1) * 4, 256) + align_up((size_t)nq * n_splits * 2 * 4, 256) +
+         (size_t)nq * n_splits * hd * 4;
+}
+
+extern "C" int qw_attention_decode(const float* qkv, const uint16_t* q_norm, const uint16_t* k_norm,
+                                   float* k_cache, float* v_cache, int32_t nq, int32_t nkv,
+                                   int32_t hd, int32_t cap, int32_t pos, float eps,
+                                   float rope_theta, int32_t n_splits, float* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!qkv || !k_cache || !v_cache || !out || !workspace)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: null buffer");
+  if ((hd != 64 && hd != 128) || nkv <= 0 || nq % nkv || nq / nkv > attention_gq_max() ||
+      n_splits <= 0 || n_splits > 65535)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: unsupported shape");
+  if (pos < 0 || pos >= cap) QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: pos outside [0, cap)");
+  if (workspace_bytes < qw_attention_workspace_bytes(nq, nkv, hd, n_splits))
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: workspace too small");
+  int sms = 0;
+  if (op_sms(&sms)) QW_FAIL((qw_handle*)nullptr, QW_ERR_CUDA, "qw_attention_decode: no CUDA device");
+  uint8_t* ws = (uint8_t*)workspace;
+  AttnArgs t{};
+  t.qkv = qkv;
+  t.q_norm = q_norm;
+  t.k_norm = k_norm;
+  t.rope = nullptr;  // cos/sin formed in fp64 inside the kernel
+  t.rope_theta = rope_theta;
+  t.k_cache = k_cache;
+  t.v_cache = v_cache;
+  t.cap = cap;
+  t.pos_ptr = nullptr;
+  t.pos_const = pos;
+  t.nq = nq;
+  t.nkv = nkv;
+  t.eps = eps;
+  t.nsplit_max = n_splits;
+  t.min_keys = 32;
+  t.counters = (int*)ws;
+  t.err = (int*)ws + nkv;
+  t.part_ml = (float*)(ws + align_up(((size_t)nkv + 1) * 4, 256));
+  t.part_o = (float*)((uint8_t*)t.part_ml + align_up((size_t)nq * n_splits * 2 * 4, 256));
+  t.out = out;
+  t.wait_ns = 1000000000ull;
+  QW_OP_CUDA(launch_attention(t, hd, false, (cudaStream_t)stream));
+  return QW_OK;
+}
+
+// LM-head workspace: [counter int | err int] padded to 256, blk_val[1024], blk_idx[1024].
+extern "C" size_t qw_lm_head_workspace_bytes(void) { return 256 + 1024 * 4 + 1024 * 4; }
+
+extern "C" int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16_t* table,
+                                 int32_t vocab, int32_t hidden, float eps, float* logits,
+                                 int32_t* argmax_dev, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (!x || !g || !table || !logits || !argmax_dev || !workspace)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_lm_head_argmax: null buffer");
+  if (vocab <= 0 || hidden <= 0 || hidden % 8 || hidden > 16384)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_lm_head_argmax: hidden must be a positive multiple of 8, <= 16384");
+  if (workspace_bytes < qw_lm_head_workspace_bytes())
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_lm_head_argmax: workspace too small");
+  int sms = 0;
+  if (op_sms(&sms)) QW_FAIL((qw_handle*)nullptr, QW_ERR_CUDA, "qw_lm_head_argmax: no CUDA device");
+  uint8_t* ws = (uint8_t*)workspace;
+  const int grid = std::min({vocab, sms, 1024});
+  GemvArgs a{};
+  a.w = (const uint8_t*)table;
+  a.n_units = vocab;
+  a.rpu = 1;
+  a.K = hidden;
+  a.row_bytes = (uint32_t)hidden * 2;
+  a.x = x;
+  a.norm_g = g;
+  a.eps = eps;
+  a.y = logits;
+  a.am.counter = (int*)ws;
+  a.err = (int*)ws + 1;
+  a.am.blk_val = (float*)(ws + 256);
+  a.am.blk_idx = (int*)(ws + 256 + 1024 * 4);
+  a.am.argmax = argmax_dev;
+  a.wait_ns = 1000000000ull;
+  plan_gemv(a, grid, kStreamStage, kStreamStages);
+  QW_OP_CUDA(launch_gemv(EPI_LOGITS, a, grid, false, (cudaStream_t)stream));
+  return QW_OK;
+}
