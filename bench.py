@@ -1,0 +1,395 @@
+"""Benchmark: batch-1 greedy decode of the Qwen3-0.6B-shape model on one GB300.
+
+One step = the "qwen3_0.6b_decode" workload's generation: 128 greedy decode
+tokens (positions 5..132) after a 5-id prompt, each token one pass of the whole
+decode path (embedding, 28 blocks, final norm, LM head, argmax) as one CUDA
+graph replay. Weights (1.19 GB read per token) are larger than L2, so no flush
+is needed between steps. `value` is decode tokens/s with weights and prompt KV
+already in HBM; `e2e` is the same through qw_decode_step with the token coming
+from the host and the greedy id read back every token.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With torchrun, every rank runs an independent replica on its own GPU (the
+path does not shard); the slowest rank's time is used and `value` sums all
+ranks' tokens. `--impl reference` times the CPU oracle on this host instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "qwen3_0.6b_decode"
+PREFILL_WORKLOAD = "qwen3_0.6b_prefill"
+METRIC = "batch-1 decode tok/s (Qwen3-0.6B shape)"
+
+
+def weight_bytes(s) -> int:
+    """Algorithmic weight bytes read per decode token (bf16 linears + LM head)."""
+    per_layer = (s.hidden * s.q_dim + 2 * s.hidden * s.kv_dim + s.q_dim * s.hidden
+                 + 3 * s.hidden * s.intermediate)
+    return 2 * (s.n_layers * per_layer + s.vocab * s.hidden)
+
+
+def kv_bytes(s, pos: int) -> int:
+    """KV bytes read by the token at 0-based position pos (keys 0..pos, f32 K and V)."""
+    return s.n_layers * 2 * s.n_kv_heads * s.head_dim * 4 * (pos + 1)
+
+
+def step_bytes(s, p0: int, n: int) -> int:
+    return n * weight_bytes(s) + sum(kv_bytes(s, p) for p in range(p0, p0 + n))
+
+
+def profiled_traffic(name: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) recorded
+    in a committed ncu summary under profiles/, or None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
+            for ln in f:
+                if ln.startswith("traffic_bytes_per_launch:"):
+                    v = ln.split(":", 1)[1].strip()
+                    return None if v in ("", "null") else int(float(v))
+    except OSError:
+        pass
+    return None
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        rows = []
+        for ln in (self.out or "").splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) >= 9:
+                try:
+                    rows.append((float(f[1]), float(f[2]), f[5:9]))
+                except ValueError:
+                    pass
+        if not rows:
+            return None
+        mx = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[0] > 0.5 * mx] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ============================================================================ GPU arm
+def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
+    import ctypes as C
+    import numpy as np
+    import torch
+    import workload as W
+    from sequence_decode_step_gb300 import _binding as B
+    from sequence_decode_step_gb300.device_model import DeviceModel
+
+    torch.cuda.set_device(local_rank)
+    wl = W.WORKLOADS[WORKLOAD]
+    s = wl.shape
+    n_tok = wl.decode_steps
+    p0 = wl.prompt_len
+    d = W.draw(wl)
+    L = B.lib()
+    stream = torch.cuda.current_stream()
+    # the handle runs on torch's current stream so that CUDA events see its work
+    m = DeviceModel(s, d.weights, max_ctx=p0 + n_tok + 8, stream=stream.cuda_stream)
+    first = m.prefill(d.prompt)
+
+    def one_step(timed_events=None):
+        B.qw_set_pos(m.h, p0)                      # back to the end of the prompt (syncs)
+        if timed_events:
+            timed_events[0].record(stream)
+        rc = L.qw_decode_step(m.h, first, None, None)
+        for _ in range(n_tok - 1):
+            rc |= L.qw_decode_step(m.h, -1, None, None)
+        if timed_events:
+            timed_events[1].record(stream)
+        if rc:
+            raise RuntimeError(B.last_error(m.h))
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            one_step(pairs[i])
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    ms = sum(a.elapsed_time(b) for a, b in pairs)
+    t_max = torch.tensor([ms], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+    ms_max = float(t_max.item())
+
+    # ---- end to end: token from the host, greedy id back to the host, every token
+    e2e_ms = 0.0
+    for i in range(max(1, args.steps // 2)):
+        B.qw_set_pos(m.h, p0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tok = first
+        out = C.c_int32()
+        for _ in range(n_tok):
+            rc = L.qw_decode_step(m.h, tok, None, C.byref(out))
+            if rc:
+                raise RuntimeError(B.last_error(m.h))
+            tok = out.value
+        e2e_ms += (time.perf_counter() - t0) * 1e3
+    e2e_steps = max(1, args.steps // 2)
+
+    # ---- dominant single launch: the LM head GEMV (final norm + [V,H] table + argmax),
+    # the same kernel the graph runs, timed alone with events on its stream
+    lm = lm_head_roofline(L, B, torch, d, s, stream)
+
+    # ---- prefill of T=1024 ids (the prompt path at that length)
+    pre = prefill_timing(torch, W, DeviceModel, stream) if args.prefill else None
+    m.close()
+
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    bytes_step = step_bytes(s, p0, n_tok)
+    tok_total = n_tok * args.steps * world
+    res = {
+        "metric": METRIC, "value": tok_total / (ms_max / 1e3), "unit": "tok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "prompt_ids": p0, "decode_tokens_per_step": n_tok,
+                   "positions": f"{p0}..{p0 + n_tok - 1}", "weights": "bf16 ~N(0,0.02), seed 1",
+                   "l2": "inputs larger than L2: 1.19 GB of weights read per token",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_token": ms_max * 1e3 / (n_tok * args.steps),
+        "step_roofline": {"bound": "hbm", "bytes_per_step": bytes_step,
+                          "achieved": bytes_step / (ms_max / args.steps / 1e3) / 1e9,
+                          "peak": hbm, "unit": "GB/s",
+                          "frac": bytes_step / (ms_max / args.steps / 1e3) / 1e9 / hbm,
+                          "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks
+                          else "fallback 6800 GB/s"},
+        "roofline": lm,
+        "e2e": {"value": n_tok * e2e_steps / (e2e_ms / 1e3), "unit": "tok/s",
+                "h2d_bytes_per_step": 4 * n_tok, "d2h_bytes_per_step": 4 * n_tok},
+        "gpu_launches": args.steps * n_tok * (2 + 5 * s.n_layers),
+        "wall_s_timed_region": wall,
+        "clocks": clk.summary(),
+        "prefill": pre,
+    }
+    return res
+
+
+def lm_head_roofline(L, B, torch, d, s, stream) -> dict:
+    import numpy as np
+    from sequence_decode_step_gb300.device_model import _to_dev
+    table = _to_dev(d.weights["embed"])
+    g = _to_dev(d.weights["final_norm"])
+    x = torch.randn(s.hidden, device="cuda")
+    lg = torch.empty(s.vocab, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(L.qw_lm_head_workspace_bytes(), dtype=torch.uint8, device="cuda")
+
+    def go():
+        rc = L.qw_lm_head_argmax(x.data_ptr(), g.data_ptr(), table.data_ptr(), s.vocab, s.hidden,
+                                 s.eps, lg.data_ptr(), am.data_ptr(), ws.data_ptr(),
+                                 L.qw_lm_head_workspace_bytes(), stream.cuda_stream)
+        if rc:
+            raise RuntimeError(B.last_error())
+
+    for _ in range(5):
+        go()
+    n = 50
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        go()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / n
+    algo = s.vocab * s.hidden * 2 + s.vocab * 4 + s.hidden * 6
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    traffic = profiled_traffic("gemv_lm_head_qwen3_0.6b.md")
+    return {"kernel": "gemv_kernel<EPI_LOGITS> (final RMSNorm + tied LM head + argmax)",
+            "bound": "hbm", "achieved": algo / sec / 1e9, "peak": hbm, "unit": "GB/s",
+            "frac": algo / sec / 1e9 / hbm, "traffic": traffic, "bytes_per_launch": algo,
+            "us_per_launch": sec * 1e6,
+            "peak_source": "measured burst copy (MEASURED_PEAKS.json hbm_gbs)" if peaks
+            else "fallback 6800 GB/s"}
+
+
+def prefill_timing(torch, W, DeviceModel, stream) -> dict:
+    wl = W.WORKLOADS[PREFILL_WORKLOAD]
+    d = W.draw(wl)
+    m = DeviceModel(wl.shape, d.weights, max_ctx=wl.max_ctx, stream=stream.cuda_stream)
+    try:
+        m.prefill(d.prompt[:16])
+        torch.cuda.synchronize()
+        m.reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        m.prefill(d.prompt)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+    finally:
+        m.close()
+    return {"workload": PREFILL_WORKLOAD, "T": wl.prompt_len, "ms": ms,
+            "tok_per_s": wl.prompt_len / (ms / 1e3), "path": "sequential decode steps"}
+
+
+# ============================================================================ CPU oracle legs
+def oracle_sample(budget_s: float, min_tokens: int, max_tokens: int) -> dict:
+    """Time the oracle (as it stands) decoding the benchmark workload on this host.
+
+    Runs in a child process started with OPENBLAS_NUM_THREADS=1, so it is the
+    single-threaded oracle; returns tokens/s over the decode tokens it finished.
+    """
+    import workload as W
+    from oracle import qwen_ref as R
+    wl = W.WORKLOADS[WORKLOAD]
+    d = W.draw(wl)
+    o = R.build_oracle(d, max_ctx=wl.prompt_len + max_tokens + 1, cache_f64=True)
+    cp = o.prefill(d.prompt)
+    tok = R.greedy_argmax(cp["logits"])
+    n = 0
+    t0 = time.perf_counter()
+    while n < max_tokens and (n < min_tokens or time.perf_counter() - t0 < budget_s):
+        tok = R.greedy_argmax(o.decode_step(tok)["logits"])
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"tokens": n, "seconds": dt, "tok_per_s": n / dt}
+
+
+def run_oracle_child(budget_s: float, min_tokens: int, max_tokens: int) -> dict:
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json, bench; print('ORACLE_JSON ' + json.dumps("
+            f"bench.oracle_sample({budget_s}, {min_tokens}, {max_tokens})))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=900)
+    for ln in r.stdout.splitlines():
+        if ln.startswith("ORACLE_JSON "):
+            return json.loads(ln[len("ORACLE_JSON "):])
+    raise RuntimeError("oracle sample failed:\n" + r.stdout[-2000:] + r.stderr[-2000:])
+
+
+def cpu_baseline(budget_s: float = 15.0) -> dict:
+    o = run_oracle_child(budget_s, 2, 128)
+    return {"value": o["tok_per_s"], "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{WORKLOAD}: 5-id prompt prefill (untimed), then {o['tokens']} greedy "
+                      f"decode tokens from position 5 ({o['seconds']:.1f} s), numpy oracle, "
+                      "one BLAS thread"}
+
+
+def run_reference(args) -> dict:
+    """The CPU oracle on this host as the reference arm: each step is a bounded
+    sample of 2 decode tokens of the same workload."""
+    per_step = 2
+    o = run_oracle_child(0.0, per_step * (args.warmup + args.steps),
+                         per_step * (args.warmup + args.steps))
+    # the child times all tokens together; the warm-up tokens are included in its
+    # count, so the rate is tokens / seconds over the whole run
+    v = o["tok_per_s"]
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step / v * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "prompt_ids": 5,
+                       "decode_tokens_per_step": per_step,
+                       "l2": "n/a (CPU)", "parallelism": "single host thread"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{o['tokens']} greedy decode tokens of {WORKLOAD} "
+                                       f"from position 5, numpy oracle, one BLAS thread"},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ============================================================================ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_base", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        res["cpu_baseline"] = cpu_baseline() if args.cpu_base else None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -131,8 +131,9 @@ def causal_gqa_attention(q: np.ndarray, q_pos: np.ndarray, k: np.ndarray, v: np.
     mask = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]  # [Tq, Tk]
     scale = 1.0 / math.sqrt(hd)
     for h in range(nq):
-        kh = k[h // group].astype(F64)
-        vh = v[h // group].astype(F64)
+        if h % group == 0:                    # widen each kv head once per group
+            kh = k[h // group].astype(F64)
+            vh = v[h // group].astype(F64)
         s = (q[:, h, :].astype(F64) @ kh.T) * scale
         s = np.where(mask, s, -np.inf)
         s = s - s.max(axis=1, keepdims=True)

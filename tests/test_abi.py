@@ -1,0 +1,76 @@
+"""C-ABI checks that need no GPU: the library loads, exports what the header
+declares, struct layouts agree, and argument errors come back before any CUDA call.
+
+Regression cases follow the "SuperKittens PR #7" review: a caller struct
+shorter than the library's must be rejected (not read past), and errors must
+be reported, not returned as success.
+"""
+import ctypes as C
+import os
+import subprocess
+
+import pytest
+
+import workload as W
+from sequence_decode_step_gb300 import _binding as B
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(B.LIB_PATH):
+        from sequence_decode_step_gb300 import build_lib
+        build_lib.build()
+    return B.lib()
+
+
+def test_exports_every_header_symbol(L):
+    names = B.header_symbols()
+    assert len(names) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(L, n)
+
+
+def test_struct_layouts_match(L):
+    assert L.qw_abi_version() == B.QW_ABI_VERSION
+    assert L.qw_sizeof_config() == C.sizeof(B.qw_config) == 68
+    assert L.qw_sizeof_weights() == C.sizeof(B.qw_weights) == 208
+    assert L.qw_sizeof_lora() == C.sizeof(B.qw_lora) == 48
+    assert B.qw_weights.lm_head.offset == 24 and B.qw_weights.attn_norm.offset == 40
+
+
+def test_short_config_struct_rejected(L):
+    cfg = B.make_config(W.TINY, 64)
+    cfg.struct_size = C.sizeof(B.qw_config) - 4      # a caller built against an older header
+    h = C.c_void_p()
+    assert L.qw_create(C.byref(cfg), None, C.byref(h)) == B.QW_ERR_ABI
+    assert h.value is None
+    assert "struct_size" in B.last_error()
+    cfg = B.make_config(W.TINY, 64)
+    cfg.abi_version = 99
+    assert L.qw_create(C.byref(cfg), None, C.byref(h)) == B.QW_ERR_ABI
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 96), ("n_kv_heads", 3), ("hidden", 0),
+                                         ("max_ctx", 0), ("hidden", 250)])
+def test_bad_config_rejected_before_cuda(L, field, value):
+    cfg = B.make_config(W.TINY, 64)
+    setattr(cfg, field, value)
+    h = C.c_void_p()
+    assert L.qw_create(C.byref(cfg), None, C.byref(h)) == B.QW_ERR_ARG
+    assert B.last_error()
+
+
+def test_null_arguments_rejected(L):
+    assert L.qw_create(None, None, None) == B.QW_ERR_ARG
+    assert L.qw_load_weights(None, None) == B.QW_ERR_ARG
+    assert L.qw_decode_step(None, 0, None, None) == B.QW_ERR_ARG
+    assert L.qw_quantize_int4_g128(None, 4, 128, None, None, None) == B.QW_ERR_ARG
+    assert L.qw_quantize_int4_g128(1, 4, 100, 1, 1, None) == B.QW_ERR_ARG   # cols % 128
+    assert L.qw_attention_workspace_bytes(16, 8, 128, 19) > 16 * 19 * 128 * 4
+    assert L.qw_lm_head_workspace_bytes() >= 256 + 8 * 1024
+    L.qw_destroy(None)

@@ -1,0 +1,220 @@
+"""Whole-step parity: the qw_* decode path on the GPU against the oracle.
+
+Both sides are fed the oracle's greedy tokens (teacher forcing), so a near-tie
+cannot desynchronise later steps; greedy ids must agree wherever the oracle's
+top-2 margin exceeds 1e-2. Logits are checked at every step and the four
+checkpoints of the "Failed Star / fs, M2" page after prefill and decode.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import workload as W
+from oracle import qwen_ref as R
+from sequence_decode_step_gb300 import _binding as B
+from sequence_decode_step_gb300.device_model import DeviceModel
+
+from gpu_util import MARGIN, top2_margin, violation
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _models(wl, drawn, max_ctx=None, cache_f64=None):
+    m = DeviceModel(wl.shape, drawn.weights, max_ctx or wl.max_ctx)
+    o = R.build_oracle(drawn, max_ctx=max_ctx, cache_f64=cache_f64)
+    return m, o
+
+
+def _teacher_forced(m, o, first_token, steps, check_every=1):
+    """Decode `steps` steps; returns the number of greedy ids compared."""
+    tok, compared = first_token, 0
+    for i in range(steps):
+        want = o.decode_step(tok)["logits"]
+        got_id, got = m.decode(tok, logits=True)
+        if i % check_every == 0 or i == steps - 1:
+            v = violation(got, want)
+            assert v <= 0, f"step {i}: logits off by {v}"
+        ref_id = R.greedy_argmax(want)
+        if top2_margin(want) > MARGIN:
+            assert got_id == ref_id, f"step {i}: greedy {got_id} vs oracle {ref_id}"
+            compared += 1
+        tok = ref_id
+    return compared
+
+
+def _prefill_check(m, o, prompt, capture=True):
+    if capture:
+        m.set_capture(True)
+    am, lg = m.prefill(prompt, logits=True)
+    cp = o.prefill(prompt)
+    assert violation(lg, cp["logits"]) <= 0
+    if capture:
+        H = m.shape.hidden
+        T = len(prompt)
+        for which, key in ((B.QW_CAPTURE_EMBEDDING, "embedding"), (B.QW_CAPTURE_BLOCK0, "block0"),
+                           (B.QW_CAPTURE_FINAL_NORM, "final_norm")):
+            got = m.capture(which).reshape(T, H)
+            assert violation(got, cp[key]) <= 0, key
+        assert violation(m.capture(B.QW_CAPTURE_LOGITS), cp["logits"]) <= 0
+        m.set_capture(False)
+    if top2_margin(cp["logits"]) > MARGIN:
+        assert am == R.greedy_argmax(cp["logits"])
+    return R.greedy_argmax(cp["logits"])
+
+
+# ------------------------------------------------------------------ tiny (8 ids + 16 steps)
+TINY_VARIANTS = {
+    "tiny": (W.TINY, False),
+    "tiny_drawn_gains": (W.TINY, True),
+    "tiny_qwen25_style": (W.TINY.replace(qk_norm=False, qkv_bias=True, tie_word_embeddings=False,
+                                         n_kv_heads=1), True),
+    "tiny_hd128_gq8": (W.TINY.replace(n_q_heads=8, n_kv_heads=1, head_dim=128, hidden=512,
+                                      intermediate=1280), True),
+}
+
+
+@pytest.mark.parametrize("name", list(TINY_VARIANTS))
+def test_tiny_prefill_and_decode(name):
+    shape, gains = TINY_VARIANTS[name]
+    wl = W.Workload(name, shape, seed=0, prompt_len=8, decode_steps=16, max_ctx=64)
+    d = W.draw(wl, drawn_gains=gains)
+    m, o = _models(wl, d)
+    try:
+        tok = _prefill_check(m, o, d.prompt)
+        for l in range(shape.n_layers):          # KV cache rows written by the prompt
+            kd, vd = m.kv(l)
+            assert violation(kd.cpu().numpy()[:, :8], o.k_cache[l][:, :8]) <= 0
+            assert violation(vd.cpu().numpy()[:, :8], o.v_cache[l][:, :8]) <= 0
+        m.set_capture(True)
+        n = _teacher_forced(m, o, tok, wl.decode_steps)
+        assert n >= wl.decode_steps // 2
+        cp_emb = m.capture(B.QW_CAPTURE_EMBEDDING)
+        assert cp_emb.shape == (shape.hidden,)
+        assert m.pos() == 8 + wl.decode_steps
+    finally:
+        m.close()
+
+
+def test_tiny_greedy_loop_matches_steps_and_is_deterministic():
+    wl = W.WORKLOADS["tiny"]
+    d = W.draw(wl)
+    m = DeviceModel(wl.shape, d.weights, wl.max_ctx)
+    try:
+        first = m.prefill(d.prompt)
+        loop = m.greedy(first, 16)
+        m.reset()
+        assert m.prefill(d.prompt) == first
+        steps, tok = [], first
+        logits = []
+        for _ in range(16):
+            tok, lg = m.decode(tok, logits=True)
+            steps.append(tok)
+            logits.append(lg)
+        assert loop == steps
+        m.reset()
+        m.prefill(d.prompt)
+        tok = first
+        for i in range(16):                      # bit-identical run to run
+            tok, lg = m.decode(tok, logits=True)
+            np.testing.assert_array_equal(lg, logits[i])
+        # token < 0 feeds the previous device argmax
+        m.reset()
+        m.prefill(d.prompt)
+        got = [m.decode(-1) for _ in range(16)]
+        assert got == steps
+    finally:
+        m.close()
+
+
+# ------------------------------------------------------------------ Qwen3-0.6B shape
+@pytest.fixture(scope="module")
+def qwen06_decode():
+    wl = W.WORKLOADS["qwen3_0.6b_decode"]
+    d = W.draw(wl)
+    m, o = _models(wl, d)
+    yield wl, d, m, o
+    m.close()
+
+
+def test_qwen3_06b_decode_128_steps(qwen06_decode):
+    wl, d, m, o = qwen06_decode
+    tok = _prefill_check(m, o, d.prompt)
+    n = _teacher_forced(m, o, tok, wl.decode_steps)
+    assert n >= wl.decode_steps // 2
+
+
+def test_qwen3_06b_longctx_8k(qwen06_decode):
+    wl0, _, _, _ = qwen06_decode
+    wl = W.WORKLOADS["qwen3_0.6b_longctx"]
+    d = W.draw(wl)
+    m, o = _models(wl, d)
+    try:
+        for l, (k, v) in enumerate(d.kv):
+            m.set_kv(l, k, v)
+        m.set_pos(wl.kv_prefill)
+        assert o.pos == wl.kv_prefill
+        n = _teacher_forced(m, o, d.start_token, wl.decode_steps)
+        assert n >= wl.decode_steps // 2
+        kd, _ = m.kv(5)                          # rows appended after the prefilled ones
+        p = wl.kv_prefill
+        assert violation(kd.cpu().numpy()[:, p:p + wl.decode_steps],
+                         o.k_cache[5][:, p:p + wl.decode_steps]) <= 0
+    finally:
+        m.close()
+
+
+def test_qwen3_06b_prefill_1024():
+    wl = W.WORKLOADS["qwen3_0.6b_prefill"]
+    d = W.draw(wl)
+    m, o = _models(wl, d)
+    try:
+        am, lg = m.prefill(d.prompt, logits=True)
+        cp = o.prefill(d.prompt)
+        assert violation(lg, cp["logits"]) <= 0
+        for l in (0, 13, 27):
+            kd, vd = m.kv(l)
+            assert violation(kd.cpu().numpy()[:, :1024], o.k_cache[l][:, :1024]) <= 0
+            assert violation(vd.cpu().numpy()[:, :1024], o.v_cache[l][:, :1024]) <= 0
+        assert m.pos() == 1024
+    finally:
+        m.close()
+
+
+# ------------------------------------------------------------------ error paths
+def test_error_paths_on_device():
+    wl = W.WORKLOADS["tiny"]
+    d = W.draw(wl)
+    m = DeviceModel(wl.shape, d.weights, max_ctx=12)
+    L = B.lib()
+    try:
+        out = C.c_int32()
+        assert L.qw_decode_step(m.h, -1, None, C.byref(out)) == B.QW_ERR_STATE
+        assert L.qw_decode_step(m.h, wl.shape.vocab, None, C.byref(out)) == B.QW_ERR_ARG
+        ids = (C.c_int32 * 3)(1, 2, 99999)
+        assert L.qw_prefill(m.h, ids, 3, None, None) == B.QW_ERR_ARG
+        assert L.qw_prefill(m.h, ids, 0, None, None) == B.QW_ERR_ARG          # empty prompt
+        n = C.c_size_t()
+        assert L.qw_capture_size(m.h, 0, C.byref(n)) == B.QW_ERR_NOT_CAPTURED
+        m.set_capture(True)
+        assert L.qw_capture_size(m.h, 0, C.byref(n)) == B.QW_ERR_NOT_CAPTURED  # no forward yet
+        m.prefill(d.prompt)
+        assert L.qw_capture_size(m.h, 0, C.byref(n)) == 0 and n.value == 8 * wl.shape.hidden
+        buf = (C.c_float * 10)()
+        assert L.qw_get_capture(m.h, 0, buf, 10) == B.QW_ERR_SIZE
+        m.set_capture(False)
+        long_ids = (C.c_int32 * 5)(1, 2, 3, 4, 5)
+        assert L.qw_prefill(m.h, long_ids, 5, None, None) == B.QW_ERR_CTX       # 8 + 5 > 12
+        assert m.pos() == 8
+        # a device wait that gives up at once reports QW_ERR_DEVICE_TIMEOUT ...
+        B.qw_set_wait_limit_ns(m.h, 0)
+        assert L.qw_decode_step(m.h, 3, None, C.byref(out)) == B.QW_ERR_DEVICE_TIMEOUT
+        # ... and the handle stays usable afterwards
+        B.qw_set_wait_limit_ns(m.h, 1_000_000_000)
+        m.reset()
+        o = R.build_oracle(d, max_ctx=12)
+        am, lg = m.prefill(d.prompt, logits=True)
+        assert violation(lg, o.prefill(d.prompt)["logits"]) <= 0
+    finally:
+        m.close()
