@@ -782,9 +782,20 @@ cudaError_t launch_quantize_int4(const float* w, int rows, int cols, uint8_t* pa
 }
 
 // ------------------------------------------------------------------ attributes
+// Allow up to `bytes` of dynamic shared memory, capped by what the device
+// grants a block minus the kernel's static shared memory.
 template <class Kern>
 static cudaError_t allow_smem(Kern k, size_t bytes) {
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa{};
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
+  if (e != cudaSuccess) return e;
+  const size_t cap = (size_t)optin - fa.sharedSizeBytes;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)(bytes < cap ? bytes : cap));
 }
 
 cudaError_t set_kernel_attributes() {

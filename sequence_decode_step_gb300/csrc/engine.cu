@@ -803,10 +803,13 @@ extern "C" int qw_get_capture(qw_handle* h, int32_t which, float* out_host, size
 // ============================================================================ stand-alone ops
 static int op_sms(int* sms) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QW_ERR_CUDA;
-  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = ensure_attributes(dev);
+  if (e != cudaSuccess) {
+    g_last_error = std::string("device set-up: ") + cudaGetErrorString(e);
     return QW_ERR_CUDA;
-  if (ensure_attributes(dev) != cudaSuccess) return QW_ERR_CUDA;
+  }
   return QW_OK;
 }
 
@@ -850,7 +853,7 @@ extern "C" int qw_attention_decode(const float* qkv, const uint16_t* q_norm, con
   if (workspace_bytes < qw_attention_workspace_bytes(nq, nkv, hd, n_splits))
     QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: workspace too small");
   int sms = 0;
-  if (op_sms(&sms)) QW_FAIL((qw_handle*)nullptr, QW_ERR_CUDA, "qw_attention_decode: no CUDA device");
+  if (op_sms(&sms)) return QW_ERR_CUDA;
   uint8_t* ws = (uint8_t*)workspace;
   AttnArgs t{};
   t.qkv = qkv;
@@ -892,7 +895,7 @@ extern "C" int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16
   if (workspace_bytes < qw_lm_head_workspace_bytes())
     QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_lm_head_argmax: workspace too small");
   int sms = 0;
-  if (op_sms(&sms)) QW_FAIL((qw_handle*)nullptr, QW_ERR_CUDA, "qw_lm_head_argmax: no CUDA device");
+  if (op_sms(&sms)) return QW_ERR_CUDA;
   uint8_t* ws = (uint8_t*)workspace;
   const int grid = std::min({vocab, sms, 1024});
   GemvArgs a{};
