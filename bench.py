@@ -138,8 +138,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
     p0 = wl.prompt_len
     d = W.draw(wl)
     L = B.lib()
-    stream = torch.cuda.current_stream()
-    # the handle runs on torch's current stream so that CUDA events see its work
+    # a dedicated stream: the handle queues its graph replays on it and the CUDA
+    # events are recorded on it
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
     m = DeviceModel(s, d.weights, max_ctx=p0 + n_tok + 8, stream=stream.cuda_stream)
     first = m.prefill(d.prompt)
 

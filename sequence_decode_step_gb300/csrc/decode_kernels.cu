@@ -17,102 +17,9 @@
 #include <stdint.h>
 
 #include "qw_internal.h"
+#include "qw_ptx.cuh"
 
 namespace qw {
-
-// ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-// Bulk (non-tensor) TMA copy global -> shared; both addresses 16-byte aligned,
-// size a multiple of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for phase `parity` of `bar` for at most limit_ns; limit 0 gives up at once.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (limit_ns == 0) return false;
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
-
-__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-// Deterministic block sum for 256 threads: warp sums, then the 8 added in order.
-__device__ __forceinline__ float block_sum_256(float v, float* scratch8) {
-  v = warp_sum(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) scratch8[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) t += scratch8[i];
-  return t;
-}
-
-// 8 bf16 weights (one 16-byte load) dotted with 8 floats.
-__device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8], float acc) {
-  acc = fmaf(__uint_as_float(w.x << 16), x[0], acc);
-  acc = fmaf(__uint_as_float(w.x & 0xffff0000u), x[1], acc);
-  acc = fmaf(__uint_as_float(w.y << 16), x[2], acc);
-  acc = fmaf(__uint_as_float(w.y & 0xffff0000u), x[3], acc);
-  acc = fmaf(__uint_as_float(w.z << 16), x[4], acc);
-  acc = fmaf(__uint_as_float(w.z & 0xffff0000u), x[5], acc);
-  acc = fmaf(__uint_as_float(w.w << 16), x[6], acc);
-  acc = fmaf(__uint_as_float(w.w & 0xffff0000u), x[7], acc);
-  return acc;
-}
 
 // Argmax order: larger value wins, equal values go to the lower index.
 __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
@@ -328,12 +235,11 @@ __global__ void __launch_bounds__(256, 1) gemv_kernel(const GemvArgs a) {
     if (a.am.pos) {
       const int p = *a.am.pos;
       if (a.am.tokens_by_pos) a.am.tokens_by_pos[p] = am;
-      if (a.am.host_tokens) a.am.host_tokens[p] = am;
       *a.am.pos = p + 1;
     }
-    if (a.am.host_status) {
-      a.am.host_status[0] = am;
-      a.am.host_status[1] = *reinterpret_cast<volatile int*>(a.err);
+    if (a.am.status) {
+      a.am.status[0] = am;
+      a.am.status[1] = *reinterpret_cast<volatile int*>(a.err);
     }
     *a.am.counter = 0;
   }
@@ -704,8 +610,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a) {
   pdl_launch_dependents();
   pdl_wait();
   const int pos = *a.pos;
-  int tok = a.tok_ring ? a.tok_ring[pos] : -1;
-  if (tok < 0) tok = *a.next_token;
+  int tok = a.tok >= 0 ? a.tok : *a.next_token;
   if (tok < 0 || tok >= a.V) {
     if (threadIdx.x == 0) atomicOr(a.err, ERR_TOKEN);
     tok = 0;
@@ -721,6 +626,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a) {
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s) {
   return launch_ex(embed_kernel, dim3(1), dim3(256), 0, s, false, a);
 }
+const void* embed_kernel_fn() { return reinterpret_cast<const void*>(embed_kernel); }
 
 // ------------------------------------------------------------------ RoPE table
 // cos/sin of p * theta^(-2j/hd), formed in fp64 and rounded to f32 once.
@@ -794,8 +700,14 @@ static cudaError_t allow_smem(Kern k, size_t bytes) {
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
   if (e != cudaSuccess) return e;
   const size_t cap = (size_t)optin - fa.sharedSizeBytes;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)(bytes < cap ? bytes : cap));
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(bytes < cap ? bytes : cap));
+  // One carveout for every kernel of the step: an SM never reconfigures between
+  // consecutive kernels, so a kernel can start while its predecessor finishes.
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 cudaError_t set_kernel_attributes() {
@@ -813,6 +725,7 @@ cudaError_t set_kernel_attributes() {
   QW_ALLOW((gemv_kernel<EPI_LOGITS, 8>), big);
   QW_ALLOW(attn_decode_kernel<64>, attn_smem<64>());
   QW_ALLOW(attn_decode_kernel<128>, attn_smem<128>());
+  QW_ALLOW(embed_kernel, 0);
 #undef QW_ALLOW
   return e;
 }

@@ -105,13 +105,10 @@ struct qw_handle {
   int* d_tokens_by_pos = nullptr;
   int nsplit_max = 1;
   int lm_grid = 1;
-  // mapped pinned host memory
-  int* h_tok_ring = nullptr;  // [cap]
-  int* h_status = nullptr;    // [2]
-  int* h_tokens = nullptr;    // [cap]
-  int* hd_tok_ring = nullptr;
-  int* hd_status = nullptr;
-  int* hd_tokens = nullptr;
+  int* d_status = nullptr;  // [2] greedy id, error word (written by the LM head)
+  // pinned host staging
+  int* h_status = nullptr;  // [4]
+  int* h_tokens = nullptr;  // [cap]
   // checkpoints
   bool capture_on = false, cap_valid = false;
   float* cap_emb = nullptr;
@@ -119,7 +116,11 @@ struct qw_handle {
   float* cap_final = nullptr;
   int cap_row0 = 0, cap_rows = 0;
   // graph
+  cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t embed_node = nullptr;  // its token argument is set before each replay
+  EmbedArgs embed_args{};
+  cudaKernelNodeParams embed_params{};
   bool graph_dirty = true;
   uint64_t wait_ns = 1000000000ull;
   // host mirror
@@ -187,10 +188,10 @@ static int validate_config(const qw_config* c, std::string& why) {
 static void free_handle(qw_handle* h) {
   if (!h) return;
   if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->graph) cudaGraphDestroy(h->graph);
   if (h->warena) cudaFree(h->warena);
   if (h->sarena) cudaFree(h->sarena);
   if (h->cap_emb) cudaFree(h->cap_emb);
-  if (h->h_tok_ring) cudaFreeHost(h->h_tok_ring);
   if (h->h_status) cudaFreeHost(h->h_status);
   if (h->h_tokens) cudaFreeHost(h->h_tokens);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
@@ -226,6 +227,7 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->d_argmax, 4},
       {(void**)&h->d_err, 4},
       {(void**)&h->d_tokens_by_pos, cap * 4},
+      {(void**)&h->d_status, 8},
   };
   size_t total = 0;
   for (auto& p : pieces) total = align_up(total, 256) + p.bytes;
@@ -237,16 +239,10 @@ static int alloc_state(qw_handle* h) {
     *p.p = h->sarena + off;
     off += p.bytes;
   }
-  QW_CUDA(h, cudaHostAlloc((void**)&h->h_tok_ring, cap * 4, cudaHostAllocMapped | cudaHostAllocPortable));
-  QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, cap * 4, cudaHostAllocMapped | cudaHostAllocPortable));
-  QW_CUDA(h, cudaHostAlloc((void**)&h->h_status, 64, cudaHostAllocMapped | cudaHostAllocPortable));
-  memset(h->h_tok_ring, 0xff, cap * 4);
+  QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, cap * 4, cudaHostAllocPortable));
+  QW_CUDA(h, cudaHostAlloc((void**)&h->h_status, 16, cudaHostAllocPortable));
   memset(h->h_tokens, 0xff, cap * 4);
-  h->h_status[0] = -1;
-  h->h_status[1] = 0;
-  QW_CUDA(h, cudaHostGetDevicePointer((void**)&h->hd_tok_ring, h->h_tok_ring, 0));
-  QW_CUDA(h, cudaHostGetDevicePointer((void**)&h->hd_tokens, h->h_tokens, 0));
-  QW_CUDA(h, cudaHostGetDevicePointer((void**)&h->hd_status, h->h_status, 0));
+  memset(h->h_status, 0, 16);
   QW_CUDA(h, launch_rope_table(h->rope, c.max_ctx, c.head_dim, c.rope_theta, h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   return QW_OK;
@@ -467,7 +463,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
   ea.V = c.vocab;
   ea.H = H;
   ea.pos = h->d_pos;
-  ea.tok_ring = h->hd_tok_ring;
+  ea.tok = -1;
   ea.next_token = h->d_next_token;
   ea.x = h->x;
   ea.cap_out = h->capture_on ? h->cap_emb : nullptr;
@@ -550,8 +546,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
     a.am.next_token = h->d_next_token;
     a.am.pos = h->d_pos;
     a.am.tokens_by_pos = h->d_tokens_by_pos;
-    a.am.host_status = h->hd_status;
-    a.am.host_tokens = h->hd_tokens;
+    a.am.status = h->d_status;
     plan_gemv(a, h->lm_grid, kStreamStage, kStreamStages);
     if ((e = launch_gemv(EPI_LOGITS, a, h->lm_grid, true, s)) != cudaSuccess) return e;
   }
@@ -564,6 +559,10 @@ static int ensure_graph(qw_handle* h) {
     cudaGraphExecDestroy(h->exec);
     h->exec = nullptr;
   }
+  if (h->graph) {
+    cudaGraphDestroy(h->graph);
+    h->graph = nullptr;
+  }
   QW_CUDA(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
   const cudaError_t le = record_step(h, h->cap_stream);
   cudaGraph_t graph = nullptr;
@@ -575,8 +574,27 @@ static int ensure_graph(qw_handle* h) {
             std::string("recording the decode step: ") +
                 cudaGetErrorString(le != cudaSuccess ? le : ce));
   }
+  h->graph = graph;
+  // Find the embed node: its token argument is rewritten before every replay.
+  size_t n_nodes = 0;
+  QW_CUDA(h, cudaGraphGetNodes(graph, nullptr, &n_nodes));
+  std::vector<cudaGraphNode_t> nodes(n_nodes);
+  QW_CUDA(h, cudaGraphGetNodes(graph, nodes.data(), &n_nodes));
+  h->embed_node = nullptr;
+  for (cudaGraphNode_t nd : nodes) {
+    cudaGraphNodeType t;
+    QW_CUDA(h, cudaGraphNodeGetType(nd, &t));
+    if (t != cudaGraphNodeTypeKernel) continue;
+    cudaKernelNodeParams kp{};
+    QW_CUDA(h, cudaGraphKernelNodeGetParams(nd, &kp));
+    if (kp.func == embed_kernel_fn()) {
+      h->embed_node = nd;
+      h->embed_params = kp;
+      h->embed_args = *reinterpret_cast<const EmbedArgs*>(kp.kernelParams[0]);
+    }
+  }
+  if (!h->embed_node) QW_FAIL(h, QW_ERR_CUDA, "recording the decode step: embed node not found");
   const cudaError_t ie = cudaGraphInstantiate(&h->exec, graph, 0);
-  cudaGraphDestroy(graph);
   if (ie != cudaSuccess) {
     h->exec = nullptr;
     QW_FAIL(h, QW_ERR_CUDA, std::string("cudaGraphInstantiate: ") + cudaGetErrorString(ie));
@@ -587,10 +605,11 @@ static int ensure_graph(qw_handle* h) {
 
 // Synchronise, then turn the device error word into a status (and clear it).
 static int finish_sync(qw_handle* h) {
+  QW_CUDA(h, cudaMemcpyAsync(h->h_status, h->d_status, 8, cudaMemcpyDeviceToHost, h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   const int err = ((volatile int*)h->h_status)[1];
   if (err == 0) return QW_OK;
-  h->h_status[1] = 0;
+  QW_CUDA(h, cudaMemsetAsync(h->d_status, 0, 8, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->d_err, 0, 4, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->attn_counters, 0, (size_t)h->cfg.n_kv_heads * 4, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->am_counter, 0, 4, h->stream));
@@ -608,12 +627,27 @@ static int check_ready(qw_handle* h, const char* fn) {
   return QW_OK;
 }
 
-// Queue n graph replays; the host tokens for positions pos..pos+n-1 are in the ring.
-static int run_steps(qw_handle* h, int n) {
+// Queue n graph replays; step i is fed tokens[i] (or, when tokens is null, `first`
+// for the first step and the device argmax afterwards). The token is the embed
+// node's kernel argument, so no copy is queued per step.
+static int run_steps(qw_handle* h, int n, const int32_t* tokens, int first) {
   int rc = ensure_graph(h);
   if (rc) return rc;
-  h->h_status[0] = -1;
-  for (int i = 0; i < n; ++i) QW_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
+  int last = -2;
+  for (int i = 0; i < n; ++i) {
+    const int tok = tokens ? tokens[i] : (i == 0 ? first : -1);
+    if (tok != last) {
+      EmbedArgs ea = h->embed_args;
+      ea.tok = tok < 0 ? -1 : tok;
+      void* args[1] = {&ea};
+      cudaKernelNodeParams kp = h->embed_params;
+      kp.kernelParams = args;
+      kp.extra = nullptr;
+      QW_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->embed_node, &kp));
+      last = tok;
+    }
+    QW_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
+  }
   return QW_OK;
 }
 
@@ -626,8 +660,7 @@ extern "C" int qw_decode_step(qw_handle* h, int32_t token, float* logits_dev, in
     QW_FAIL(h, QW_ERR_STATE, "qw_decode_step: token < 0 but no previous step to feed from");
   if (h->pos + 1 > h->cfg.max_ctx) QW_FAIL(h, QW_ERR_CTX, "qw_decode_step: context is full");
   DeviceGuard dg(h->device);
-  h->h_tok_ring[h->pos] = token < 0 ? -1 : token;
-  rc = run_steps(h, 1);
+  rc = run_steps(h, 1, nullptr, token);
   if (rc) return rc;
   if (logits_dev)
     QW_CUDA(h, cudaMemcpyAsync(logits_dev, h->logits, (size_t)h->cfg.vocab * 4,
@@ -656,19 +689,20 @@ extern "C" int qw_decode_greedy(qw_handle* h, int32_t token, int32_t n_steps, in
     QW_FAIL(h, QW_ERR_CTX, "qw_decode_greedy: pos + n_steps > max_ctx");
   DeviceGuard dg(h->device);
   const int p0 = h->pos;
-  h->h_tok_ring[p0] = token < 0 ? -1 : token;
-  for (int i = 1; i < n_steps; ++i) h->h_tok_ring[p0 + i] = -1;
-  rc = run_steps(h, n_steps);
+  rc = run_steps(h, n_steps, nullptr, token);
   if (rc) return rc;
   h->cap_valid = h->capture_on;
   h->cap_row0 = p0 + n_steps - 1;
   h->cap_rows = 1;
   h->pos += n_steps;
   h->have_prev = true;
+  if (ids_host)
+    QW_CUDA(h, cudaMemcpyAsync(h->h_tokens + p0, h->d_tokens_by_pos + p0, (size_t)n_steps * 4,
+                               cudaMemcpyDeviceToHost, h->stream));
   rc = finish_sync(h);
   if (rc) return rc;
   if (ids_host)
-    for (int i = 0; i < n_steps; ++i) ids_host[i] = ((volatile int*)h->h_tokens)[p0 + i];
+    for (int i = 0; i < n_steps; ++i) ids_host[i] = h->h_tokens[p0 + i];
   return QW_OK;
 }
 
@@ -685,8 +719,7 @@ extern "C" int qw_prefill(qw_handle* h, const int32_t* ids_host, int32_t T, floa
   DeviceGuard dg(h->device);
   const int p0 = h->pos;
   // Sequential path: one decode step per prompt id, all queued before one sync.
-  for (int i = 0; i < T; ++i) h->h_tok_ring[p0 + i] = ids_host[i];
-  rc = run_steps(h, T);
+  rc = run_steps(h, T, ids_host, 0);
   if (rc) return rc;
   if (logits_dev)
     QW_CUDA(h, cudaMemcpyAsync(logits_dev, h->logits, (size_t)h->cfg.vocab * 4,
@@ -721,8 +754,8 @@ extern "C" int qw_set_pos(qw_handle* h, int32_t pos) {
   if (pos < 0 || pos > h->cfg.max_ctx) QW_FAIL(h, QW_ERR_CTX, "qw_set_pos: pos outside [0, max_ctx]");
   DeviceGuard dg(h->device);
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
-  h->h_status[0] = pos;  // staging value for the copy below
-  QW_CUDA(h, cudaMemcpyAsync(h->d_pos, &h->h_status[0], 4, cudaMemcpyHostToDevice, h->stream));
+  h->h_status[2] = pos;  // staging value for the copy below
+  QW_CUDA(h, cudaMemcpyAsync(h->d_pos, &h->h_status[2], 4, cudaMemcpyHostToDevice, h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   h->pos = pos;
   h->cap_valid = false;

@@ -24,8 +24,7 @@ struct ArgmaxOut {
   int* next_token;            // [1] token fed to the next step when the host passes none
   int* pos;                   // [1] device position; incremented after the argmax is known
   int* tokens_by_pos;         // [cap] argmax recorded at the step's position
-  volatile int* host_status;  // mapped pinned host [2]: argmax, error word
-  volatile int* host_tokens;  // mapped pinned host [cap]: argmax by position
+  int* status;                // [2] argmax and a copy of the error word, for the host
 };
 
 // y = epilogue(W . prologue(x)); W rows grouped in units of `rpu` rows.
@@ -81,8 +80,8 @@ struct EmbedArgs {
   const uint16_t* table;   // bf16 [V, H]
   int V, H;
   const int* pos;
-  const volatile int* tok_ring;  // mapped host [cap]: token for a position, or -1
-  const int* next_token;
+  int tok;                 // token from the host (a graph-node parameter), or -1
+  const int* next_token;   // previous step's argmax, used when tok < 0
   float* x;                // [H]
   float* cap_out;          // capture rows [cap][H] or nullptr
   int* err;
@@ -97,6 +96,7 @@ size_t attention_smem_bytes(int hd);
 int attention_gq_max();
 constexpr int kAttnMinKeys = 64;
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s);
+const void* embed_kernel_fn();
 cudaError_t launch_rope_table(float2* table, int cap, int hd, float theta, cudaStream_t s);
 cudaError_t launch_quantize_int4(const float* w, int rows, int cols, uint8_t* packed,
                                  uint16_t* scales, cudaStream_t s);

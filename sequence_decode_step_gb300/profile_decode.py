@@ -1,0 +1,80 @@
+"""Drive a few decode steps of a workload for profilers (ncu) and quick timing.
+
+  python -m sequence_decode_step_gb300.profile_decode [--workload NAME] [--tokens N]
+         [--lm-head N]
+
+Draws the workload's weights, prefills its prompt (or preloads its KV cache),
+runs N greedy decode tokens as graph replays, then N stand-alone LM-head
+launches, and prints the mean per-token and per-launch times (CUDA events).
+No oracle, no checks: parity lives in tests/.
+"""
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+    import workload as W
+    from sequence_decode_step_gb300 import _binding as B
+    from sequence_decode_step_gb300.device_model import DeviceModel, _to_dev
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="qwen3_0.6b_decode")
+    ap.add_argument("--tokens", type=int, default=8)
+    ap.add_argument("--lm-head", type=int, default=4)
+    args = ap.parse_args()
+    wl = W.WORKLOADS[args.workload]
+    d = W.draw(wl)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    m = DeviceModel(wl.shape, d.weights, max_ctx=max(wl.max_ctx, wl.prompt_len + wl.kv_prefill
+                                                     + args.tokens + 8),
+                    stream=stream.cuda_stream)
+    L = B.lib()
+    if wl.kv_prefill:
+        for l, (k, v) in enumerate(d.kv):
+            m.set_kv(l, k, v)
+        m.set_pos(wl.kv_prefill)
+        first = d.start_token
+    else:
+        first = m.prefill(d.prompt)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    rc = L.qw_decode_step(m.h, first, None, None)
+    for _ in range(args.tokens - 1):
+        rc |= L.qw_decode_step(m.h, -1, None, None)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if rc:
+        raise SystemExit(B.last_error(m.h))
+    print(f"decode: {e0.elapsed_time(e1) * 1e3 / args.tokens:.1f} us/token over {args.tokens}")
+    s = wl.shape
+    if args.lm_head and s.tie_word_embeddings:
+        table, g = _to_dev(d.weights["embed"]), _to_dev(d.weights["final_norm"])
+        x = torch.randn(s.hidden, device="cuda")
+        lg = torch.empty(s.vocab, device="cuda")
+        am = torch.empty(1, dtype=torch.int32, device="cuda")
+        wsb = L.qw_lm_head_workspace_bytes()
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.lm_head):
+            rc |= L.qw_lm_head_argmax(x.data_ptr(), g.data_ptr(), table.data_ptr(), s.vocab,
+                                      s.hidden, s.eps, lg.data_ptr(), am.data_ptr(),
+                                      ws.data_ptr(), wsb, stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if rc:
+            raise SystemExit(B.last_error())
+        print(f"lm head: {e0.elapsed_time(e1) * 1e3 / args.lm_head:.1f} us/launch")
+    m.close()
+
+
+if __name__ == "__main__":
+    main()
