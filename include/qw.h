@@ -259,6 +259,26 @@ int qw_attention_decode(const float* qkv, const uint16_t* q_norm, const uint16_t
                         int32_t cap, int32_t pos, float eps, float rope_theta, int32_t n_splits,
                         float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* qw_attention_decode without a workspace argument, for callers that cannot
+ * allocate device memory (code running while another thread captures a CUDA
+ * graph, allocator-free real-time loops, embedders whose device memory belongs
+ * to someone else's pool). The pages have no counterpart of this call; it is a
+ * deployment convenience. Arguments and results are those of
+ * qw_attention_decode. Its scratch is a fixed file-scope device array of
+ * qw_attention_noalloc_max_bytes() bytes (1 MiB) that every GPU loading this
+ * library keeps until the process exits; shapes whose scratch
+ * (256 + nq*n_splits*(hd+2)*4 bytes, rounded) does not fit return QW_ERR_SIZE.
+ * The first call on a device looks up that array's device address and sets the
+ * kernel attributes, so make it before any stream capture on that device.
+ * Every call shares the one array and clears its counters on `stream`: calls
+ * that overlap on the GPU (different streams, or several host threads) race
+ * and must be serialised by the caller. No call allocates memory. */
+size_t qw_attention_noalloc_max_bytes(void);
+int qw_attention_decode_noalloc(const float* qkv, const uint16_t* q_norm, const uint16_t* k_norm,
+                                float* k_cache, float* v_cache, int32_t nq, int32_t nkv,
+                                int32_t hd, int32_t cap, int32_t pos, float eps,
+                                float rope_theta, int32_t n_splits, float* out, void* stream);
+
 /* Final RMSNorm + LM head + greedy argmax over a bf16 [vocab, hidden] table
  * ("Failed Star / fs, M2": final norm, last row, tied [V,H] projection;
  * "flashmoon demo": argmax in the same submit):
