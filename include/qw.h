@@ -292,6 +292,14 @@ int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16_t* table, 
                       int32_t hidden, float eps, float* logits, int32_t* argmax_dev,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Prefill contraction on tcgen05 tensor cores: C[M,N] = (A_hi + A_lo)[M,K] . B[N,K]^T.
+ * A_hi, A_lo (nullable), B: bf16 row-major DEVICE, 16-byte aligned, K % 8 == 0; C: f32
+ * [M,N] DEVICE. The activation of a layer enters as its two-bf16 split (hi = bf16(x),
+ * lo = bf16(x - hi)) against the exact bf16 weight rows ("Emberglass" README: batched
+ * tiled-GEMM prefill). bn: output-tile width 64, 128 or 256 (0 picks one). */
+int qw_gemm_bf16(const uint16_t* a_hi, const uint16_t* a_lo, const uint16_t* b, int32_t M,
+                 int32_t N, int32_t K, float* c, int32_t bn, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

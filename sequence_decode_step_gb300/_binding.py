@@ -105,6 +105,8 @@ _SIG = {
                                               C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
                                               C.c_int32, C.c_int32, C.c_float, C.c_float,
                                               C.c_int32, C.c_void_p, C.c_void_p]),
+    "qw_gemm_bf16": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                               C.c_int32, C.c_void_p, C.c_int32, C.c_void_p]),
     "qw_lm_head_workspace_bytes": (C.c_size_t, []),
     "qw_lm_head_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                     C.c_float, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,

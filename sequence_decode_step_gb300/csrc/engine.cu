@@ -61,6 +61,7 @@ bool g_attrs_set[64];
 cudaError_t ensure_attributes(int dev) {
   if (dev >= 0 && dev < 64 && g_attrs_set[dev]) return cudaSuccess;
   cudaError_t e = set_kernel_attributes();
+  if (e == cudaSuccess) e = set_gemm_attributes();
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attrs_set[dev] = true;
   return e;
 }
@@ -949,5 +950,33 @@ extern "C" int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16
   a.wait_ns = 1000000000ull;
   plan_gemv(a, grid, kStreamStage, kStreamStages);
   QW_OP_CUDA(launch_gemv(EPI_LOGITS, a, grid, false, (cudaStream_t)stream));
+  return QW_OK;
+}
+
+extern "C" int qw_gemm_bf16(const uint16_t* a_hi, const uint16_t* a_lo, const uint16_t* b,
+                            int32_t M, int32_t N, int32_t K, float* c, int32_t bn, void* stream) {
+  if (!a_hi || !b || !c || M <= 0 || N <= 0 || K <= 0 || K % 8)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_gemm_bf16: null buffer, empty shape or K % 8 != 0");
+  if (bn == 0) bn = N >= 2048 ? 256 : (N >= 512 ? 128 : 64);
+  if (bn != 64 && bn != 128 && bn != 256)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_gemm_bf16: bn must be 0, 64, 128 or 256");
+  int sms = 0;
+  if (op_sms(&sms)) return QW_ERR_CUDA;
+  CUtensorMap ta_hi, ta_lo, tb;
+  if (!make_tmap_bf16_2d(&ta_hi, a_hi, M, K, 128) ||
+      !make_tmap_bf16_2d(&ta_lo, a_lo ? a_lo : a_hi, M, K, 128) ||
+      !make_tmap_bf16_2d(&tb, b, N, K, (uint32_t)bn))
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_gemm_bf16: tensor map rejected (alignment?)");
+  GemmArgs g{};
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.a_split = a_lo ? 2 : 1;
+  g.out = c;
+  g.ldo = N;
+  g.err = gemm_op_err_word();
+  g.wait_ns = 1000000000ull;
+  if (!g.err) QW_FAIL((qw_handle*)nullptr, QW_ERR_CUDA, "qw_gemm_bf16: error word lookup failed");
+  QW_OP_CUDA(launch_gemm(bn, GEPI_STORE, ta_hi, ta_lo, tb, g, (cudaStream_t)stream));
   return QW_OK;
 }

@@ -1,0 +1,274 @@
+// Prefill kernels for sm_103a: the dense contractions run on tcgen05 tensor
+// cores (TMA-fed, TMEM accumulators); the row-wise steps are CUDA-core kernels.
+//
+// GEMM: one CTA computes a 128 x BN tile of C = A . B^T. Warp 0 (one thread)
+// streams A and B k-tiles (64 wide, 128-byte swizzle) with TMA into a ring of
+// shared-memory stages; warp 1 owns the TMEM accumulator (BN columns) and one of
+// its threads issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide slice; warps
+// 2..5 read the accumulator back with tcgen05.ld (one TMEM lane = one row per
+// thread) and apply the epilogue. Activations enter as two bf16 halves
+// (hi = bf16(x), lo = bf16(x - hi)) multiplied against the same exact-bf16
+// weight tile, so the product keeps about 16 bits of the f32 activation.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "qw_internal.h"
+#include "qw_ptx.cuh"
+
+namespace qw {
+
+constexpr int GBM = 128;
+constexpr int GBK = 64;
+constexpr uint32_t kATileBytes = GBM * GBK * 2;  // 16 KB
+
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(l);
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap ta_hi,
+                   const __grid_constant__ CUtensorMap ta_lo,
+                   const __grid_constant__ CUtensorMap tb, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int NS = a.n_stages;
+  const uint32_t stage_bytes = (uint32_t)a.a_split * kATileBytes + (uint32_t)BN * GBK * 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
+  uint64_t* empty = full + NS;
+  uint64_t* accf = empty + NS;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(accf + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * GBM, n0 = blockIdx.x * BN;
+  const int KT = (a.K + GBK - 1) / GBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(accf, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: TMA k-tiles of A (hi[, lo]) and B into the stage ring
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % NS, u = kt / NS;
+      if (u > 0 && !mbar_wait(&empty[s], (uint32_t)((u - 1) & 1), a.wait_ns)) {
+        atomicOr(a.err, ERR_TIMEOUT);
+        break;
+      }
+      uint8_t* st = smem + (size_t)s * stage_bytes;
+      mbar_expect_tx(&full[s], stage_bytes);
+      tma_load_2d(st, &ta_hi, kt * GBK, m0, &full[s]);
+      if (a.a_split == 2) tma_load_2d(st + kATileBytes, &ta_lo, kt * GBK, m0, &full[s]);
+      tma_load_2d(st + a.a_split * kATileBytes, &tb, kt * GBK, n0, &full[s]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(GBM, BN);
+    for (int kt = 0; kt < KT; ++kt) {
+      const int s = kt % NS, u = kt / NS;
+      if (!mbar_wait(&full[s], (uint32_t)(u & 1), a.wait_ns)) {
+        atomicOr(a.err, ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = smem_addr(smem + (size_t)s * stage_bytes);
+      const uint32_t sb = sa + (uint32_t)a.a_split * kATileBytes;
+#pragma unroll
+      for (int k = 0; k < GBK / 16; ++k) {
+        const uint64_t bd = sw128_kmajor_desc(sb + k * 32);
+        tc_mma_bf16(tbase, sw128_kmajor_desc(sa + k * 32), bd, idesc, (kt | k) != 0);
+        if (a.a_split == 2)
+          tc_mma_bf16(tbase, sw128_kmajor_desc(sa + kATileBytes + k * 32), bd, idesc, 1);
+      }
+      tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+    }
+    tc_commit(accf);  // the accumulator is final once every MMA above completed
+    // TMEM is released below only after the MMAs have finished.
+    mbar_wait(accf, 0, kDrainNs);
+  } else if (warp >= 2) {
+    // ---- epilogue: warp w reads TMEM lanes [32 (w % 4), +32) = rows of the tile
+    const bool ok = mbar_wait(accf, 0, a.wait_ns);
+    if (!ok && lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+    tc_fence_after();
+    const int q = warp & 3;
+    const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+      tmem_ld_wait();
+      const int col0 = n0 + c0;
+      if (!ok || row >= a.M || col0 >= a.N) continue;
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+      const int nv = min(16, a.N - col0);
+      if (EPI == GEPI_STORE) {
+        float* o = a.out + (size_t)row * a.ldo + col0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < nv) o[j] = v[j] + (a.bias ? __uint_as_float((uint32_t)a.bias[col0 + j] << 16) : 0.f);
+      } else if (EPI == GEPI_RESID) {
+        float* o = a.out + (size_t)row * a.ldo + col0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (j < nv) {
+            const float nvl = o[j] + v[j];
+            o[j] = nvl;
+            if (a.cap_out) a.cap_out[(size_t)(a.cap_row0 + row) * a.ldo + col0 + j] = nvl;
+          }
+      } else {  // GEPI_SWIGLU
+        const int u0 = col0 / 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (2 * j + 1 < nv) {
+            const float g = v[2 * j], up = v[2 * j + 1];
+            uint16_t hi, lo;
+            split_bf16(g / (1.0f + expf(-g)) * up, hi, lo);
+            a.out_hi[(size_t)row * a.ldb + u0 + j] = hi;
+            a.out_lo[(size_t)row * a.ldb + u0 + j] = lo;
+          }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, BN);
+  }
+}
+
+// ------------------------------------------------------------------ GEMM host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 [rows, cols] (cols contiguous), boxes of 64 columns x box_rows rows,
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (cols * 2) % 16 || (reinterpret_cast<uintptr_t>(base) & 15) || box_rows > 256)
+    return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)GBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kGemmSmemBudget = 200 * 1024;
+
+static int gemm_stages(int bn, int a_split) {
+  const size_t stage = (size_t)a_split * kATileBytes + (size_t)bn * GBK * 2;
+  int ns = (int)((kGemmSmemBudget - 2048) / stage);
+  return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+}
+static size_t gemm_smem(int bn, int a_split, int ns) {
+  return (size_t)ns * ((size_t)a_split * kATileBytes + (size_t)bn * GBK * 2) + 1024 + 256;
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_gemm_t(const CUtensorMap& a_hi, const CUtensorMap& a_lo,
+                                 const CUtensorMap& b, const GemmArgs& g, cudaStream_t s) {
+  const dim3 grid((g.N + BN - 1) / BN, (g.M + GBM - 1) / GBM);
+  gemm_tc_kernel<BN, EPI><<<grid, 192, gemm_smem(BN, g.a_split, g.n_stages), s>>>(a_hi, a_lo, b,
+                                                                                    g);
+  return cudaGetLastError();
+}
+
+template <int BN>
+static cudaError_t launch_gemm_bn(int epi, const CUtensorMap& a_hi, const CUtensorMap& a_lo,
+                                  const CUtensorMap& b, const GemmArgs& g, cudaStream_t s) {
+  switch (epi) {
+    case GEPI_STORE: return launch_gemm_t<BN, GEPI_STORE>(a_hi, a_lo, b, g, s);
+    case GEPI_RESID: return launch_gemm_t<BN, GEPI_RESID>(a_hi, a_lo, b, g, s);
+    case GEPI_SWIGLU: return launch_gemm_t<BN, GEPI_SWIGLU>(a_hi, a_lo, b, g, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& a_hi, const CUtensorMap& a_lo,
+                        const CUtensorMap& b, GemmArgs g, cudaStream_t s) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || (g.a_split != 1 && g.a_split != 2))
+    return cudaErrorInvalidValue;
+  if (epi == GEPI_SWIGLU && (g.N % 2)) return cudaErrorInvalidValue;
+  g.n_stages = gemm_stages(bn, g.a_split);
+  if (bn == 64) return launch_gemm_bn<64>(epi, a_hi, a_lo, b, g, s);
+  if (bn == 128) return launch_gemm_bn<128>(epi, a_hi, a_lo, b, g, s);
+  if (bn == 256) return launch_gemm_bn<256>(epi, a_hi, a_lo, b, g, s);
+  return cudaErrorInvalidValue;
+}
+
+template <int BN>
+static cudaError_t gemm_attrs_bn() {
+  int bytes = 0;
+  for (int split = 1; split <= 2; ++split) {
+    const int b = (int)gemm_smem(BN, split, gemm_stages(BN, split));
+    bytes = b > bytes ? b : bytes;
+  }
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, GEPI_STORE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN, GEPI_RESID>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN, GEPI_SWIGLU>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
+}
+
+static __device__ int g_gemm_op_err;
+
+int* gemm_op_err_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_gemm_op_err) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+cudaError_t set_gemm_attributes() {
+  cudaError_t e = gemm_attrs_bn<64>();
+  if (e == cudaSuccess) e = gemm_attrs_bn<128>();
+  if (e == cudaSuccess) e = gemm_attrs_bn<256>();
+  return e;
+}
+
+}  // namespace qw

@@ -1,5 +1,6 @@
 // Internal interface between the decode kernels and the engine (not part of the ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -101,5 +102,30 @@ cudaError_t launch_rope_table(float2* table, int cap, int hd, float theta, cudaS
 cudaError_t launch_quantize_int4(const float* w, int rows, int cols, uint8_t* packed,
                                  uint16_t* scales, cudaStream_t s);
 cudaError_t set_kernel_attributes();
+
+// ---- prefill (prefill_kernels.cu) ----
+// C[M, N] = (A_hi + A_lo)[M, K] . B[N, K]^T on tcgen05 tensor cores; A and B bf16 K-major.
+enum : int { GEPI_STORE = 0, GEPI_RESID = 1, GEPI_SWIGLU = 2 };
+struct GemmArgs {
+  int M, N, K;
+  int a_split;             // 1: A_hi only; 2: A_hi + A_lo (activation split in two bf16)
+  int n_stages;            // filled by launch_gemm
+  float* out;              // STORE: out[m, n] = acc (+ bias[n]); RESID: out[m, n] += acc
+  int ldo;
+  const uint16_t* bias;    // STORE: bf16 [N] or nullptr
+  uint16_t* out_hi;        // SWIGLU: columns (2i, 2i+1) are (gate_i, up_i); writes
+  uint16_t* out_lo;        //   silu(gate)*up split in two bf16 at [m, i]
+  int ldb;
+  float* cap_out;          // RESID: also write the updated rows at [cap_row0 + m] (or nullptr)
+  int cap_row0;
+  int* err;
+  uint64_t wait_ns;
+};
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows);
+cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& a_hi, const CUtensorMap& a_lo,
+                        const CUtensorMap& b, GemmArgs g, cudaStream_t s);
+cudaError_t set_gemm_attributes();
+int* gemm_op_err_word();
 
 }  // namespace qw
