@@ -62,6 +62,7 @@ cudaError_t ensure_attributes(int dev) {
   if (dev >= 0 && dev < 64 && g_attrs_set[dev]) return cudaSuccess;
   cudaError_t e = set_kernel_attributes();
   if (e == cudaSuccess) e = set_gemm_attributes();
+  if (e == cudaSuccess) e = set_prefill_attributes();
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attrs_set[dev] = true;
   return e;
 }
@@ -106,6 +107,19 @@ struct qw_handle {
   int* d_tokens_by_pos = nullptr;
   int nsplit_max = 1;
   int lm_grid = 1;
+  // batched prefill (T <= max_prefill_t): activations of all rows and their TMA maps
+  int* pf_ids = nullptr;
+  float* pf_x = nullptr;       // [Tmax, H] residual rows
+  uint16_t* pf_xn_hi = nullptr;  // [Tmax, H] normalised rows, two-bf16 split
+  uint16_t* pf_xn_lo = nullptr;
+  float* pf_qkv = nullptr;     // [Tmax, (nq+2nkv) hd]
+  float* pf_q = nullptr;       // [Tmax, nq, hd] after QK-norm, RoPE, 1/sqrt(hd)
+  uint16_t* pf_o_hi = nullptr;   // [Tmax, nq hd] attention output split
+  uint16_t* pf_o_lo = nullptr;
+  uint16_t* pf_m_hi = nullptr;   // [Tmax, I] SwiGLU output split
+  uint16_t* pf_m_lo = nullptr;
+  CUtensorMap tm_xn_hi, tm_xn_lo, tm_o_hi, tm_o_lo, tm_m_hi, tm_m_lo;
+  std::vector<CUtensorMap> tm_qkv, tm_ow, tm_gu, tm_dw;  // per layer, weight side
   int* d_status = nullptr;  // [2] greedy id, error word (written by the LM head)
   // pinned host staging
   int* h_status = nullptr;  // [4]
@@ -127,6 +141,7 @@ struct qw_handle {
   // host mirror
   int pos = 0;
   bool have_prev = false;
+  bool lora_active = false;
   std::string err;
 };
 
@@ -230,6 +245,20 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->d_tokens_by_pos, cap * 4},
       {(void**)&h->d_status, 8},
   };
+  const size_t Tm = (size_t)c.max_prefill_t, H = c.hidden, I = c.intermediate;
+  const size_t qd = (size_t)c.n_q_heads * hd;
+  if (Tm > 0) {
+    pieces.push_back({(void**)&h->pf_ids, Tm * 4});
+    pieces.push_back({(void**)&h->pf_x, Tm * H * 4});
+    pieces.push_back({(void**)&h->pf_xn_hi, Tm * H * 2});
+    pieces.push_back({(void**)&h->pf_xn_lo, Tm * H * 2});
+    pieces.push_back({(void**)&h->pf_qkv, Tm * qkv_rows * 4});
+    pieces.push_back({(void**)&h->pf_q, Tm * qd * 4});
+    pieces.push_back({(void**)&h->pf_o_hi, Tm * qd * 2});
+    pieces.push_back({(void**)&h->pf_o_lo, Tm * qd * 2});
+    pieces.push_back({(void**)&h->pf_m_hi, Tm * I * 2});
+    pieces.push_back({(void**)&h->pf_m_lo, Tm * I * 2});
+  }
   size_t total = 0;
   for (auto& p : pieces) total = align_up(total, 256) + p.bytes;
   QW_CUDA(h, cudaMalloc((void**)&h->sarena, total));
@@ -240,7 +269,16 @@ static int alloc_state(qw_handle* h) {
     *p.p = h->sarena + off;
     off += p.bytes;
   }
-  QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, cap * 4, cudaHostAllocPortable));
+  if (Tm > 0) {
+    bool ok = make_tmap_bf16_2d(&h->tm_xn_hi, h->pf_xn_hi, Tm, H, 128) &&
+              make_tmap_bf16_2d(&h->tm_xn_lo, h->pf_xn_lo, Tm, H, 128) &&
+              make_tmap_bf16_2d(&h->tm_o_hi, h->pf_o_hi, Tm, qd, 128) &&
+              make_tmap_bf16_2d(&h->tm_o_lo, h->pf_o_lo, Tm, qd, 128) &&
+              make_tmap_bf16_2d(&h->tm_m_hi, h->pf_m_hi, Tm, I, 128) &&
+              make_tmap_bf16_2d(&h->tm_m_lo, h->pf_m_lo, Tm, I, 128);
+    if (!ok) QW_FAIL(h, QW_ERR_CUDA, "prefill: TMA descriptor encoding failed");
+  }
+  QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, std::max<size_t>(cap, Tm) * 4, cudaHostAllocPortable));
   QW_CUDA(h, cudaHostAlloc((void**)&h->h_status, 16, cudaHostAllocPortable));
   memset(h->h_tokens, 0xff, cap * 4);
   memset(h->h_status, 0, 16);
@@ -414,6 +452,20 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
       lw.k_norm = (const uint16_t*)p;
     }
   }
+  if (c.max_prefill_t > 0) {
+    h->tm_qkv.resize(L);
+    h->tm_ow.resize(L);
+    h->tm_gu.resize(L);
+    h->tm_dw.resize(L);
+    for (int l = 0; l < L; ++l) {
+      const LayerW& lw = h->layers[l];
+      const bool ok = make_tmap_bf16_2d(&h->tm_qkv[l], lw.qkv, qd + 2 * kd, H, 256) &&
+                      make_tmap_bf16_2d(&h->tm_ow[l], lw.o, H, qd, 64) &&
+                      make_tmap_bf16_2d(&h->tm_gu[l], lw.gateup, 2 * I, H, 256) &&
+                      make_tmap_bf16_2d(&h->tm_dw[l], lw.down, H, I, 64);
+      if (!ok) QW_FAIL(h, QW_ERR_CUDA, "qw_load_weights: TMA descriptor encoding failed");
+    }
+  }
   QW_CUDA(h, cudaMemsetAsync(h->d_pos, 0, 4, h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   h->pos = 0;
@@ -448,6 +500,27 @@ static GemvArgs base_gemv(qw_handle* h, const void* w, int n_units, int rpu, int
   a.wait_ns = h->wait_ns;
   a.pos = h->d_pos;
   return a;
+}
+
+// Final RMSNorm of row x, logits over the (tied or untied) head, greedy argmax;
+// the last CTA records the id at the device position and advances it.
+static cudaError_t launch_lm_head(qw_handle* h, const float* x, float* norm_out, bool pdl,
+                                  cudaStream_t s) {
+  GemvArgs a = base_gemv(h, h->lm_head, h->cfg.vocab, 1, h->cfg.hidden);
+  a.x = x;
+  a.norm_g = h->final_norm;
+  a.y = h->logits;
+  a.norm_out = norm_out;
+  a.am.blk_val = h->blk_val;
+  a.am.blk_idx = h->blk_idx;
+  a.am.counter = h->am_counter;
+  a.am.argmax = h->d_argmax;
+  a.am.next_token = h->d_next_token;
+  a.am.pos = h->d_pos;
+  a.am.tokens_by_pos = h->d_tokens_by_pos;
+  a.am.status = h->d_status;
+  plan_gemv(a, h->lm_grid, kStreamStage, kStreamStages);
+  return launch_gemv(EPI_LOGITS, a, h->lm_grid, pdl, s);
 }
 
 // Launch one step's kernels on stream s (recorded into the graph).
@@ -534,24 +607,8 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       if ((e = launch_gemv(EPI_RESIDUAL, a, grid, true, s)) != cudaSuccess) return e;
     }
   }
-  {  // final RMSNorm + LM head + greedy argmax; advances the device position
-    GemvArgs a = base_gemv(h, h->lm_head, c.vocab, 1, H);
-    a.x = h->x;
-    a.norm_g = h->final_norm;
-    a.y = h->logits;
-    a.norm_out = h->capture_on ? h->cap_final : nullptr;
-    a.am.blk_val = h->blk_val;
-    a.am.blk_idx = h->blk_idx;
-    a.am.counter = h->am_counter;
-    a.am.argmax = h->d_argmax;
-    a.am.next_token = h->d_next_token;
-    a.am.pos = h->d_pos;
-    a.am.tokens_by_pos = h->d_tokens_by_pos;
-    a.am.status = h->d_status;
-    plan_gemv(a, h->lm_grid, kStreamStage, kStreamStages);
-    if ((e = launch_gemv(EPI_LOGITS, a, h->lm_grid, true, s)) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  // final RMSNorm + LM head + greedy argmax; advances the device position
+  return launch_lm_head(h, h->x, h->capture_on ? h->cap_final : nullptr, true, s);
 }
 
 static int ensure_graph(qw_handle* h) {
@@ -707,6 +764,72 @@ extern "C" int qw_decode_greedy(qw_handle* h, int32_t token, int32_t n_steps, in
   return QW_OK;
 }
 
+// One causal pass over T prompt rows: tensor-core GEMMs for the projections,
+// row kernels for norms / QK-norm / RoPE / KV append, flash attention over the
+// cache (positions 0..pos+T-1), then the LM head on the last row.
+static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
+  const qw_config& c = h->cfg;
+  const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
+  const int qd = c.n_q_heads * hd, kd = c.n_kv_heads * hd, qkv_rows = qd + 2 * kd;
+  const size_t kv_layer = (size_t)c.n_kv_heads * c.max_ctx * hd;
+  const int p0 = h->pos;
+  cudaStream_t s = h->stream;
+  QW_CUDA(h, cudaStreamSynchronize(s));  // the staging buffer may still feed an earlier copy
+  memcpy(h->h_tokens, ids_host, (size_t)T * 4);
+  QW_CUDA(h, cudaMemcpyAsync(h->pf_ids, h->h_tokens, (size_t)T * 4, cudaMemcpyHostToDevice, s));
+  QW_CUDA(h, launch_embed_rows(h->pf_ids, T, h->embed, c.vocab, H, h->pf_x,
+                               h->capture_on ? h->cap_emb : nullptr, p0, h->d_err, s));
+  auto gemm = [&](int bn, int epi, const CUtensorMap& ahi, const CUtensorMap& alo,
+                  const CUtensorMap& b, int N, int K, float* out, const uint16_t* bias,
+                  uint16_t* ohi, uint16_t* olo, float* cap) {
+    GemmArgs g{};
+    g.M = T;
+    g.N = N;
+    g.K = K;
+    g.a_split = 2;
+    g.out = out;
+    g.ldo = N;
+    g.bias = bias;
+    g.out_hi = ohi;
+    g.out_lo = olo;
+    g.ldb = N / 2;
+    g.cap_out = cap;
+    g.cap_row0 = p0;
+    g.err = h->d_err;
+    g.wait_ns = h->wait_ns;
+    return launch_gemm(bn, epi, ahi, alo, b, g, s);
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerW& lw = h->layers[l];
+    float* kc = h->k_cache + (size_t)l * kv_layer;
+    float* vc = h->v_cache + (size_t)l * kv_layer;
+    QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, lw.attn_norm, c.eps, h->pf_xn_hi, h->pf_xn_lo,
+                                   nullptr, 0, s));
+    QW_CUDA(h, gemm(256, GEPI_STORE, h->tm_xn_hi, h->tm_xn_lo, h->tm_qkv[l], qkv_rows, H,
+                    h->pf_qkv, lw.qkv_bias, nullptr, nullptr, nullptr));
+    QW_CUDA(h, launch_qk_rope_kv_rows(h->pf_qkv, T, p0, c.n_q_heads, c.n_kv_heads, hd, lw.q_norm,
+                                      lw.k_norm, c.eps, h->rope, h->pf_q, kc, vc, c.max_ctx, s));
+    QW_CUDA(h, launch_attn_prefill(h->pf_q, kc, vc, c.max_ctx, p0, T, c.n_q_heads, c.n_kv_heads,
+                                   hd, h->pf_o_hi, h->pf_o_lo, s));
+    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, h->tm_ow[l], H, qd, h->pf_x, nullptr,
+                    nullptr, nullptr, nullptr));
+    QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, lw.mlp_norm, c.eps, h->pf_xn_hi, h->pf_xn_lo,
+                                   nullptr, 0, s));
+    QW_CUDA(h, gemm(256, GEPI_SWIGLU, h->tm_xn_hi, h->tm_xn_lo, h->tm_gu[l], 2 * I, H, nullptr,
+                    nullptr, h->pf_m_hi, h->pf_m_lo, nullptr));
+    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_m_hi, h->tm_m_lo, h->tm_dw[l], H, I, h->pf_x, nullptr,
+                    nullptr, nullptr, (h->capture_on && l == 0) ? h->cap_blk0 : nullptr));
+  }
+  if (h->capture_on)
+    QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, h->final_norm, c.eps, nullptr, nullptr,
+                                   h->cap_final, p0, s));
+  // The LM head's last CTA records the id at the device position and advances
+  // it, so set it to the last prompt row first.
+  QW_CUDA(h, launch_set_int(h->d_pos, p0 + T - 1, s));
+  QW_CUDA(h, launch_lm_head(h, h->pf_x + (size_t)(T - 1) * H, nullptr, false, s));
+  return QW_OK;
+}
+
 extern "C" int qw_prefill(qw_handle* h, const int32_t* ids_host, int32_t T, float* logits_dev,
                           int32_t* argmax_host) {
   int rc = check_ready(h, "qw_prefill");
@@ -719,8 +842,13 @@ extern "C" int qw_prefill(qw_handle* h, const int32_t* ids_host, int32_t T, floa
     QW_FAIL(h, QW_ERR_CTX, "qw_prefill: pos + T > max_ctx");
   DeviceGuard dg(h->device);
   const int p0 = h->pos;
-  // Sequential path: one decode step per prompt id, all queued before one sync.
-  rc = run_steps(h, T, ids_host, 0);
+  if (T <= h->cfg.max_prefill_t && !h->lora_active) {
+    rc = prefill_batched(h, ids_host, T);
+  } else {
+    // Sequential path ("Emberglass" README, maxPrefillT: longer prompts, or a
+    // prompt while a LoRA is set): one decode step per id, queued before one sync.
+    rc = run_steps(h, T, ids_host, 0);
+  }
   if (rc) return rc;
   if (logits_dev)
     QW_CUDA(h, cudaMemcpyAsync(logits_dev, h->logits, (size_t)h->cfg.vocab * 4,

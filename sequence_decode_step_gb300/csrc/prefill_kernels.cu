@@ -160,6 +160,284 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+
+// ------------------------------------------------------------------ row-wise prefill kernels
+__global__ void __launch_bounds__(256) embed_rows_kernel(const int* ids, const uint16_t* table,
+                                                         int V, int H, float* X, float* cap,
+                                                         int row0, int* err) {
+  const int t = blockIdx.x;
+  int tok = ids[t];
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN);
+    tok = 0;
+  }
+  const uint16_t* src = table + (size_t)tok * H;
+  for (int i = threadIdx.x; i < H; i += 256) {
+    const float v = bf16f(src[i]);
+    X[(size_t)t * H + i] = v;
+    if (cap) cap[(size_t)(row0 + t) * H + i] = v;
+  }
+}
+
+// One row per CTA: y = x * rstd * g, written as a two-bf16 split and/or as f32.
+__global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* X, int H,
+                                                           const uint16_t* g, float eps,
+                                                           uint16_t* out_hi, uint16_t* out_lo,
+                                                           float* out_f32, int f32_row0) {
+  __shared__ float red[8];
+  const int t = blockIdx.x;
+  const float* x = X + (size_t)t * H;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < H; i += 256) ss = fmaf(x[i], x[i], ss);
+  const float tot = block_sum_256(ss, red);
+  const float r = 1.0f / sqrtf(tot / (float)H + eps);
+  for (int i = threadIdx.x; i < H; i += 256) {
+    const float y = x[i] * r * bf16f(g[i]);
+    if (out_hi) {
+      uint16_t hi, lo;
+      split_bf16(y, hi, lo);
+      out_hi[(size_t)t * H + i] = hi;
+      out_lo[(size_t)t * H + i] = lo;
+    }
+    if (out_f32) out_f32[(size_t)(f32_row0 + t) * H + i] = y;
+  }
+}
+
+// Row t (position p0 + t): per-head QK-RMSNorm and RoPE of q and k, q scaled by
+// 1/sqrt(hd) into Q [T][nq][hd]; k and v appended to the cache at their position.
+template <int HD>
+__global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
+    const float* QKV, int p0, int nq, int nkv, const uint16_t* q_norm, const uint16_t* k_norm,
+    float eps, const float2* rope, float* Q, float* kc, float* vc, int cap) {
+  constexpr int EPL = HD / 32;
+  const int t = blockIdx.x, pos = p0 + t;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* row = QKV + (size_t)t * (nq + 2 * nkv) * HD;
+  const float scale = 1.0f / sqrtf((float)HD);
+  const float2* rr = rope + (size_t)pos * (HD / 2);
+  for (int hh = warp; hh < nq + nkv; hh += 8) {
+    const bool isq = hh < nq;
+    const float* src = row + (size_t)hh * HD;
+    const uint16_t* gain = isq ? q_norm : k_norm;
+    float v[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[e] = src[lane + 32 * e];
+    if (gain != nullptr) {
+      float sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) sq = fmaf(v[e], v[e], sq);
+      sq = warp_sum(sq);
+      const float r = 1.0f / sqrtf(sq / (float)HD + eps);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[e] = v[e] * r * bf16f(gain[lane + 32 * e]);
+    }
+#pragma unroll
+    for (int e = 0; e < EPL / 2; ++e) {
+      const float2 cs = rr[lane + 32 * e];
+      const float x0 = v[e], x1 = v[e + EPL / 2];
+      v[e] = x0 * cs.x - x1 * cs.y;
+      v[e + EPL / 2] = x1 * cs.x + x0 * cs.y;
+    }
+    if (isq) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) Q[((size_t)t * nq + hh) * HD + lane + 32 * e] = v[e] * scale;
+    } else {
+      float* dst = kc + ((size_t)(hh - nq) * cap + pos) * HD;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) dst[lane + 32 * e] = v[e];
+    }
+  }
+  const float* vsrc = row + (size_t)(nq + nkv) * HD;
+  for (int i = threadIdx.x; i < nkv * HD; i += 256)
+    vc[((size_t)(i / HD) * cap + pos) * HD + (i % HD)] = vsrc[i];
+}
+
+// Causal attention for a 64-query block of one head, CUDA cores, online softmax
+// over 64-key tiles. Thread (ty, tx) of a 16 x 16 grid owns query rows 4ty..4ty+3,
+// score columns 4tx..4tx+3 and output columns tx*(hd/16)... of those rows.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_prefill_kernel(const float* Q, const float* kc,
+                                                           const float* vc, int cap, int p0, int T,
+                                                           int nq, int nkv, uint16_t* o_hi,
+                                                           uint16_t* o_lo) {
+  constexpr int BQ = 64, BK = 64, DPT = HD / 16;
+  extern __shared__ __align__(16) float sm[];
+  float* Qt = sm;               // [HD][BQ]
+  float* Kt = Qt + HD * BQ;     // [HD][BK]
+  float* Vs = Kt + HD * BK;     // [BK][HD]
+  float* Pt = Vs + BK * HD;     // [BK][BQ]
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int t0 = blockIdx.x * BQ, h = blockIdx.y, g = h / (nq / nkv);
+  const int nrows = min(BQ, T - t0);
+  const int last_key = p0 + t0 + nrows - 1;
+  for (int idx = tid; idx < BQ * HD / 4; idx += 256) {
+    const int r = idx % BQ, d4 = idx / BQ;
+    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nrows) q = *reinterpret_cast<const float4*>(Q + ((size_t)(t0 + r) * nq + h) * HD + d4 * 4);
+    Qt[(d4 * 4 + 0) * BQ + r] = q.x;
+    Qt[(d4 * 4 + 1) * BQ + r] = q.y;
+    Qt[(d4 * 4 + 2) * BQ + r] = q.z;
+    Qt[(d4 * 4 + 3) * BQ + r] = q.w;
+  }
+  float m[4], l[4], acc[4][DPT];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPT; ++e) acc[i][e] = 0.f;
+  }
+  const float* kg = kc + (size_t)g * cap * HD;
+  const float* vg = vc + (size_t)g * cap * HD;
+  const int n_tiles = last_key / BK + 1;
+  for (int kt = 0; kt < n_tiles; ++kt) {
+    const int k0 = kt * BK;
+    __syncthreads();
+    for (int idx = tid; idx < BK * HD / 4; idx += 256) {
+      const int r = idx % BK, d4 = idx / BK;
+      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+      if (k0 + r <= last_key) {
+        kv = *reinterpret_cast<const float4*>(kg + (size_t)(k0 + r) * HD + d4 * 4);
+        vv = *reinterpret_cast<const float4*>(vg + (size_t)(k0 + r) * HD + d4 * 4);
+      }
+      Kt[(d4 * 4 + 0) * BK + r] = kv.x;
+      Kt[(d4 * 4 + 1) * BK + r] = kv.y;
+      Kt[(d4 * 4 + 2) * BK + r] = kv.z;
+      Kt[(d4 * 4 + 3) * BK + r] = kv.w;
+      *reinterpret_cast<float4*>(Vs + r * HD + d4 * 4) = vv;
+    }
+    __syncthreads();
+    float sc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[i][j] = 0.f;
+#pragma unroll 8
+    for (int d = 0; d < HD; ++d) {
+      const float4 q = *reinterpret_cast<const float4*>(Qt + d * BQ + ty * 4);
+      const float4 k = *reinterpret_cast<const float4*>(Kt + d * BK + tx * 4);
+      const float qa[4] = {q.x, q.y, q.z, q.w}, ka[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[i][j] = fmaf(qa[i], ka[j], sc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int qp = p0 + t0 + ty * 4 + i;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (k0 + tx * 4 + j > qp) sc[i][j] = -INFINITY;
+        mx = fmaxf(mx, sc[i][j]);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float mn = fmaxf(m[i], mx);
+      float rs = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float p = (sc[i][j] == -INFINITY) ? 0.f : expf(sc[i][j] - mn);
+        Pt[(tx * 4 + j) * BQ + ty * 4 + i] = p;
+        rs += p;
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+      const float alpha = (m[i] == -INFINITY) ? 0.f : expf(m[i] - mn);
+      l[i] = l[i] * alpha + rs;
+      m[i] = mn;
+#pragma unroll
+      for (int e = 0; e < DPT; ++e) acc[i][e] *= alpha;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int c = 0; c < BK; ++c) {
+      const float4 p = *reinterpret_cast<const float4*>(Pt + c * BQ + ty * 4);
+      const float pa[4] = {p.x, p.y, p.z, p.w};
+      float vv[DPT];
+#pragma unroll
+      for (int e = 0; e < DPT; e += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(Vs + c * HD + tx * DPT + e);
+        vv[e] = v4.x;
+        vv[e + 1] = v4.y;
+        vv[e + 2] = v4.z;
+        vv[e + 3] = v4.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < DPT; ++e) acc[i][e] = fmaf(pa[i], vv[e], acc[i][e]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ty * 4 + i;
+    if (r >= nrows) continue;
+    const float inv = 1.0f / l[i];
+    const size_t base = (size_t)(t0 + r) * nq * HD + (size_t)h * HD + tx * DPT;
+#pragma unroll
+    for (int e = 0; e < DPT; ++e) {
+      uint16_t hi, lo;
+      split_bf16(acc[i][e] * inv, hi, lo);
+      o_hi[base + e] = hi;
+      o_lo[base + e] = lo;
+    }
+  }
+}
+
+__global__ void set_int_kernel(int* p, int v) { *p = v; }
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_embed_rows(const int* ids, int T, const uint16_t* table, int V, int H,
+                              float* X, float* cap, int row0, int* err, cudaStream_t s) {
+  embed_rows_kernel<<<T, 256, 0, s>>>(ids, table, V, H, X, cap, row0, err);
+  return cudaGetLastError();
+}
+cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g, float eps,
+                                uint16_t* hi, uint16_t* lo, float* f32, int f32_row0,
+                                cudaStream_t s) {
+  rmsnorm_rows_kernel<<<T, 256, 0, s>>>(X, H, g, eps, hi, lo, f32, f32_row0);
+  return cudaGetLastError();
+}
+cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
+                                   const uint16_t* qn, const uint16_t* kn, float eps,
+                                   const float2* rope, float* Q, float* kc, float* vc, int cap,
+                                   cudaStream_t s) {
+  if (hd == 64)
+    qk_rope_kv_rows_kernel<64><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, Q, kc, vc, cap);
+  else if (hd == 128)
+    qk_rope_kv_rows_kernel<128><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, Q, kc, vc, cap);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+static size_t attn_prefill_smem(int hd) { return (size_t)(3 * hd * 64 + 64 * 64) * 4; }
+cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
+                                int T, int nq, int nkv, int hd, uint16_t* o_hi, uint16_t* o_lo,
+                                cudaStream_t s) {
+  const dim3 grid((T + 63) / 64, nq);
+  if (hd == 64)
+    attn_prefill_kernel<64><<<grid, 256, attn_prefill_smem(64), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
+  else if (hd == 128)
+    attn_prefill_kernel<128><<<grid, 256, attn_prefill_smem(128), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
+  set_int_kernel<<<1, 1, 0, s>>>(p, v);
+  return cudaGetLastError();
+}
+cudaError_t set_prefill_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)attn_prefill_smem(64));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn_prefill_smem(128));
+  return e;
+}
+
 // ------------------------------------------------------------------ GEMM host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -127,5 +127,19 @@ cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& a_hi, const CUtensor
                         const CUtensorMap& b, GemmArgs g, cudaStream_t s);
 cudaError_t set_gemm_attributes();
 int* gemm_op_err_word();
+cudaError_t launch_embed_rows(const int* ids, int T, const uint16_t* table, int V, int H,
+                              float* X, float* cap, int row0, int* err, cudaStream_t s);
+cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g, float eps,
+                                uint16_t* hi, uint16_t* lo, float* f32, int f32_row0,
+                                cudaStream_t s);
+cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
+                                   const uint16_t* qn, const uint16_t* kn, float eps,
+                                   const float2* rope, float* Q, float* kc, float* vc, int cap,
+                                   cudaStream_t s);
+cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
+                                int T, int nq, int nkv, int hd, uint16_t* o_hi, uint16_t* o_lo,
+                                cudaStream_t s);
+cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
+cudaError_t set_prefill_attributes();
 
 }  // namespace qw

@@ -41,7 +41,7 @@ def _run(M, N, K, bn, split, seed=0):
     scale = np.sqrt(K) * 0.02
     err = np.abs(got - want).max() / scale
     assert np.isfinite(got).all()
-    assert err < 1e-5, err
+    assert err < 5e-5, err   # f32 accumulation over K; a layout slip gives O(1)
     if split:   # the split recovers the f32 activations to ~2^-16
         exact = a.astype(np.float64) @ W.bf16_bits_to_f32(w).astype(np.float64).T
         assert violation(got, exact, 1e-4 * scale, 1e-4) <= 0

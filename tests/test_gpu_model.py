@@ -21,8 +21,8 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-def _models(wl, drawn, max_ctx=None, cache_f64=None):
-    m = DeviceModel(wl.shape, drawn.weights, max_ctx or wl.max_ctx)
+def _models(wl, drawn, max_ctx=None, cache_f64=None, max_prefill_t=0):
+    m = DeviceModel(wl.shape, drawn.weights, max_ctx or wl.max_ctx, max_prefill_t=max_prefill_t)
     o = R.build_oracle(drawn, max_ctx=max_ctx, cache_f64=cache_f64)
     return m, o
 
@@ -75,12 +75,13 @@ TINY_VARIANTS = {
 }
 
 
+@pytest.mark.parametrize("path", ["sequential", "batched"])
 @pytest.mark.parametrize("name", list(TINY_VARIANTS))
-def test_tiny_prefill_and_decode(name):
+def test_tiny_prefill_and_decode(name, path):
     shape, gains = TINY_VARIANTS[name]
     wl = W.Workload(name, shape, seed=0, prompt_len=8, decode_steps=16, max_ctx=64)
     d = W.draw(wl, drawn_gains=gains)
-    m, o = _models(wl, d)
+    m, o = _models(wl, d, max_prefill_t=64 if path == "batched" else 0)
     try:
         tok = _prefill_check(m, o, d.prompt)
         for l in range(shape.n_layers):          # KV cache rows written by the prompt
@@ -166,18 +167,60 @@ def test_qwen3_06b_longctx_8k(qwen06_decode):
 
 
 def test_qwen3_06b_prefill_1024():
+    # one batched causal pass (tensor-core GEMMs) against the oracle's no-cache
+    # prefill, and against 1024 sequential decode steps of the same ids on the GPU
     wl = W.WORKLOADS["qwen3_0.6b_prefill"]
     d = W.draw(wl)
-    m, o = _models(wl, d)
+    m, o = _models(wl, d, max_prefill_t=1024)
+    seq = DeviceModel(wl.shape, d.weights, wl.max_ctx)       # max_prefill_t = 0: sequential
     try:
+        m.set_capture(True)
         am, lg = m.prefill(d.prompt, logits=True)
         cp = o.prefill(d.prompt)
         assert violation(lg, cp["logits"]) <= 0
+        T, H = 1024, wl.shape.hidden
+        for which, key in ((B.QW_CAPTURE_EMBEDDING, "embedding"), (B.QW_CAPTURE_BLOCK0, "block0"),
+                           (B.QW_CAPTURE_FINAL_NORM, "final_norm")):
+            assert violation(m.capture(which).reshape(T, H), cp[key]) <= 0, key
+        am_s, lg_s = seq.prefill(d.prompt, logits=True)
+        assert violation(lg, lg_s) <= 0
+        if top2_margin(cp["logits"]) > MARGIN:
+            assert am == am_s == R.greedy_argmax(cp["logits"])
         for l in (0, 13, 27):
             kd, vd = m.kv(l)
-            assert violation(kd.cpu().numpy()[:, :1024], o.k_cache[l][:, :1024]) <= 0
-            assert violation(vd.cpu().numpy()[:, :1024], o.v_cache[l][:, :1024]) <= 0
-        assert m.pos() == 1024
+            ks, vs = seq.kv(l)
+            kd, vd = kd.cpu().numpy()[:, :T], vd.cpu().numpy()[:, :T]
+            assert violation(kd, o.k_cache[l][:, :T]) <= 0
+            assert violation(vd, o.v_cache[l][:, :T]) <= 0
+            assert violation(kd, ks.cpu().numpy()[:, :T]) <= 0
+            assert violation(vd, vs.cpu().numpy()[:, :T]) <= 0
+        assert m.pos() == seq.pos() == 1024
+        # decoding continues from the batched prefill's cache and greedy id
+        tok = R.greedy_argmax(cp["logits"])
+        _teacher_forced(m, o, tok, 4)
+    finally:
+        m.close()
+        seq.close()
+
+
+def test_batched_prefill_in_two_chunks_and_sequential_fallback():
+    # a second prompt chunk starts at pos = 5 and attends to the first chunk's cache;
+    # a chunk longer than max_prefill_t takes the sequential path
+    wl = W.Workload("chunks", W.TINY, seed=3, max_ctx=64)
+    d = W.draw(wl, drawn_gains=True)
+    ids = list(W.random_ids(W.TINY.vocab, 30, seed=9))
+    m = DeviceModel(W.TINY, d.weights, 64, max_prefill_t=16)
+    o = R.build_oracle(d)
+    try:
+        m.prefill(ids[:5])
+        m.prefill(ids[5:12])
+        m.prefill(ids[12:30])                         # 18 > 16: sequential fallback
+        am, lg = m.decode(ids[0], logits=True)
+        o.prefill(ids)
+        want = o.decode_step(ids[0])["logits"]
+        assert violation(lg, want) <= 0
+        kd, _ = m.kv(1)
+        assert violation(kd.cpu().numpy()[:, :31], o.k_cache[1][:, :31]) <= 0
     finally:
         m.close()
 
