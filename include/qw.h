@@ -215,6 +215,14 @@ int qw_set_capture(qw_handle* h, int32_t enable);
 int qw_capture_size(qw_handle* h, int32_t which, size_t* n_floats);
 int qw_get_capture(qw_handle* h, int32_t which, float* out_host, size_t n_floats);
 
+/* Decode path (test and benchmarking hook). 0: one persistent cooperative kernel
+ * per token (the default whenever the shape fits: bf16 weights, hidden,
+ * intermediate and n_q_heads*head_dim <= 3072); 1: the graph of separate
+ * kernels (always available). Asking for 0 on a shape that does not fit keeps 1.
+ * Both compute the same step; results agree to f32 rounding. */
+int qw_set_decode_path(qw_handle* h, int32_t path);
+int qw_get_decode_path(const qw_handle* h, int32_t* path);
+
 /* Bound, in nanoseconds, of every device-side wait (default 1e9). 0 makes
  * every wait give up at once, which tests the QW_ERR_DEVICE_TIMEOUT path. */
 int qw_set_wait_limit_ns(qw_handle* h, uint64_t ns);

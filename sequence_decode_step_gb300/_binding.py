@@ -91,6 +91,8 @@ _SIG = {
     "qw_capture_size": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_size_t)]),
     "qw_get_capture": (C.c_int, [C.c_void_p, C.c_int32, C.c_void_p, C.c_size_t]),
     "qw_set_wait_limit_ns": (C.c_int, [C.c_void_p, C.c_uint64]),
+    "qw_set_decode_path": (C.c_int, [C.c_void_p, C.c_int32]),
+    "qw_get_decode_path": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32)]),
     "qw_last_error": (C.c_char_p, [C.c_void_p]),
     "qw_destroy": (None, [C.c_void_p]),
     "qw_quantize_int4_g128": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
@@ -246,3 +248,13 @@ def qw_set_wait_limit_ns(h, ns: int) -> None:
 
 def qw_destroy(h) -> None:
     lib().qw_destroy(h)
+
+
+def qw_set_decode_path(h, path: int) -> None:
+    check("qw_set_decode_path", lib().qw_set_decode_path(h, int(path)), h)
+
+
+def qw_get_decode_path(h) -> int:
+    p = C.c_int32()
+    check("qw_get_decode_path", lib().qw_get_decode_path(h, C.byref(p)), h)
+    return p.value

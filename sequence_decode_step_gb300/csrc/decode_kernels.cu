@@ -21,10 +21,6 @@
 
 namespace qw {
 
-// Argmax order: larger value wins, equal values go to the lower index.
-__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
 
 // Reduce (best_v, best_i) over the 256 threads; result valid in thread 0.
 __device__ __forceinline__ void block_argmax_256(float& bv, int& bi, float* r8, int* r8i) {

@@ -17,6 +17,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <string>
 #include <vector>
 
@@ -63,6 +64,7 @@ cudaError_t ensure_attributes(int dev) {
   cudaError_t e = set_kernel_attributes();
   if (e == cudaSuccess) e = set_gemm_attributes();
   if (e == cudaSuccess) e = set_prefill_attributes();
+  if (e == cudaSuccess) e = set_mega_attributes();
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attrs_set[dev] = true;
   return e;
 }
@@ -133,9 +135,18 @@ struct qw_handle {
   // graph
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
-  cudaGraphNode_t embed_node = nullptr;  // its token argument is set before each replay
-  EmbedArgs embed_args{};
-  cudaKernelNodeParams embed_params{};
+  // The graph node that receives the host token (the embed kernel, or the persistent
+  // decode kernel), a copy of its argument block and the token's offset inside it.
+  cudaGraphNode_t tok_node = nullptr;
+  cudaKernelNodeParams tok_params{};
+  std::vector<uint8_t> tok_args;
+  size_t tok_offset = 0;
+  // decode path: the persistent cooperative kernel when the shape fits, else the
+  // multi-kernel graph
+  bool use_mega = false;
+  bool mega_ok = false;
+  LayerDev* d_layers = nullptr;
+  unsigned* bar_slots = nullptr;
   bool graph_dirty = true;
   uint64_t wait_ns = 1000000000ull;
   // host mirror
@@ -206,6 +217,7 @@ static void free_handle(qw_handle* h) {
   if (h->exec) cudaGraphExecDestroy(h->exec);
   if (h->graph) cudaGraphDestroy(h->graph);
   if (h->warena) cudaFree(h->warena);
+  if (h->d_layers) cudaFree(h->d_layers);
   if (h->sarena) cudaFree(h->sarena);
   if (h->cap_emb) cudaFree(h->cap_emb);
   if (h->h_status) cudaFreeHost(h->h_status);
@@ -220,6 +232,10 @@ static int alloc_state(qw_handle* h) {
   const size_t L = c.n_layers, nkv = c.n_kv_heads, hd = c.head_dim, cap = c.max_ctx;
   const size_t qkv_rows = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * hd;
   h->nsplit_max = std::max(1, h->num_sms / c.n_kv_heads);
+  h->mega_ok = c.weight_format == QW_WEIGHTS_BF16 &&
+               mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim, c.head_dim,
+                              c.n_q_heads / c.n_kv_heads);
+  h->use_mega = h->mega_ok;
   h->lm_grid = std::min({c.vocab, h->num_sms, 1024});
   struct Piece { void** p; size_t bytes; };
   const size_t kv_bytes = L * nkv * cap * hd * 4;
@@ -244,6 +260,7 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->d_err, 4},
       {(void**)&h->d_tokens_by_pos, cap * 4},
       {(void**)&h->d_status, 8},
+      {(void**)&h->bar_slots, (size_t)5 * L * 4},
   };
   const size_t Tm = (size_t)c.max_prefill_t, H = c.hidden, I = c.intermediate;
   const size_t qd = (size_t)c.n_q_heads * hd;
@@ -452,6 +469,20 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
       lw.k_norm = (const uint16_t*)p;
     }
   }
+  {
+    std::vector<LayerDev> ld(L);
+    for (int l = 0; l < L; ++l) {
+      const LayerW& lw = h->layers[l];
+      ld[l] = LayerDev{(const uint8_t*)lw.qkv, lw.qkv_bias, (const uint8_t*)lw.o,
+                       (const uint8_t*)lw.gateup, (const uint8_t*)lw.down, lw.attn_norm,
+                       lw.mlp_norm, lw.q_norm, lw.k_norm};
+    }
+    if (h->d_layers) cudaFree(h->d_layers);
+    h->d_layers = nullptr;
+    QW_CUDA(h, cudaMalloc((void**)&h->d_layers, L * sizeof(LayerDev)));
+    QW_CUDA(h, cudaMemcpyAsync(h->d_layers, ld.data(), L * sizeof(LayerDev),
+                               cudaMemcpyHostToDevice, h->stream));
+  }
   if (c.max_prefill_t > 0) {
     h->tm_qkv.resize(L);
     h->tm_ow.resize(L);
@@ -523,8 +554,58 @@ static cudaError_t launch_lm_head(qw_handle* h, const float* x, float* norm_out,
   return launch_gemv(EPI_LOGITS, a, h->lm_grid, pdl, s);
 }
 
+// The persistent kernel's arguments (the token is patched per replay).
+static MegaArgs mega_args(qw_handle* h) {
+  const qw_config& c = h->cfg;
+  MegaArgs m{};
+  m.L = c.n_layers;
+  m.H = c.hidden;
+  m.nq = c.n_q_heads;
+  m.nkv = c.n_kv_heads;
+  m.hd = c.head_dim;
+  m.I = c.intermediate;
+  m.V = c.vocab;
+  m.eps = c.eps;
+  m.embed = h->embed;
+  m.lm_head = (const uint8_t*)h->lm_head;
+  m.final_norm = h->final_norm;
+  m.layers = h->d_layers;
+  m.k_cache = h->k_cache;
+  m.v_cache = h->v_cache;
+  m.cap = c.max_ctx;
+  m.rope = h->rope;
+  m.x = h->x;
+  m.qkv = h->qkv;
+  m.attn_o = h->attn_o;
+  m.mlp = h->mlp;
+  m.logits = h->logits;
+  m.part_o = h->part_o;
+  m.part_ml = h->part_ml;
+  m.attn_counters = h->attn_counters;
+  m.splits = h->nsplit_max;
+  m.am.blk_val = h->blk_val;
+  m.am.blk_idx = h->blk_idx;
+  m.am.counter = h->am_counter;
+  m.am.argmax = h->d_argmax;
+  m.am.next_token = h->d_next_token;
+  m.am.pos = h->d_pos;
+  m.am.tokens_by_pos = h->d_tokens_by_pos;
+  m.am.status = h->d_status;
+  m.pos = h->d_pos;
+  m.tok = -1;
+  m.next_token = h->d_next_token;
+  m.bar_slots = h->bar_slots;
+  m.cap_emb = h->capture_on ? h->cap_emb : nullptr;
+  m.cap_blk0 = h->capture_on ? h->cap_blk0 : nullptr;
+  m.cap_final = h->capture_on ? h->cap_final : nullptr;
+  m.err = h->d_err;
+  m.wait_ns = h->wait_ns;
+  return m;
+}
+
 // Launch one step's kernels on stream s (recorded into the graph).
 static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
+  if (h->use_mega) return launch_mega(mega_args(h), h->nsplit_max * h->cfg.n_kv_heads, s);
   const qw_config& c = h->cfg;
   const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
   const int qd = c.n_q_heads * hd, kd = c.n_kv_heads * hd;
@@ -611,7 +692,21 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
   return launch_lm_head(h, h->x, h->capture_on ? h->cap_final : nullptr, true, s);
 }
 
+static int ensure_graph_once(qw_handle* h);
+
+// Record (or re-record) the step graph; a persistent kernel that cannot be
+// recorded or instantiated (e.g. no cooperative launch) falls back to the
+// multi-kernel graph for the rest of the handle's life.
 static int ensure_graph(qw_handle* h) {
+  const int rc = ensure_graph_once(h);
+  if (rc == QW_OK || !h->use_mega) return rc;
+  h->use_mega = false;
+  h->mega_ok = false;
+  h->graph_dirty = true;
+  return ensure_graph_once(h);
+}
+
+static int ensure_graph_once(qw_handle* h) {
   if (h->exec && !h->graph_dirty) return QW_OK;
   if (h->exec) {
     cudaGraphExecDestroy(h->exec);
@@ -638,20 +733,29 @@ static int ensure_graph(qw_handle* h) {
   QW_CUDA(h, cudaGraphGetNodes(graph, nullptr, &n_nodes));
   std::vector<cudaGraphNode_t> nodes(n_nodes);
   QW_CUDA(h, cudaGraphGetNodes(graph, nodes.data(), &n_nodes));
-  h->embed_node = nullptr;
+  h->tok_node = nullptr;
   for (cudaGraphNode_t nd : nodes) {
     cudaGraphNodeType t;
     QW_CUDA(h, cudaGraphNodeGetType(nd, &t));
     if (t != cudaGraphNodeTypeKernel) continue;
     cudaKernelNodeParams kp{};
     QW_CUDA(h, cudaGraphKernelNodeGetParams(nd, &kp));
+    size_t bytes = 0, off = 0;
     if (kp.func == embed_kernel_fn()) {
-      h->embed_node = nd;
-      h->embed_params = kp;
-      h->embed_args = *reinterpret_cast<const EmbedArgs*>(kp.kernelParams[0]);
+      bytes = sizeof(EmbedArgs);
+      off = offsetof(EmbedArgs, tok);
+    } else if (kp.func == mega_kernel_fn()) {
+      bytes = sizeof(MegaArgs);
+      off = offsetof(MegaArgs, tok);
+    } else {
+      continue;
     }
+    h->tok_node = nd;
+    h->tok_params = kp;
+    h->tok_args.assign((const uint8_t*)kp.kernelParams[0], (const uint8_t*)kp.kernelParams[0] + bytes);
+    h->tok_offset = off;
   }
-  if (!h->embed_node) QW_FAIL(h, QW_ERR_CUDA, "recording the decode step: embed node not found");
+  if (!h->tok_node) QW_FAIL(h, QW_ERR_CUDA, "recording the decode step: token node not found");
   const cudaError_t ie = cudaGraphInstantiate(&h->exec, graph, 0);
   if (ie != cudaSuccess) {
     h->exec = nullptr;
@@ -664,9 +768,11 @@ static int ensure_graph(qw_handle* h) {
 // Synchronise, then turn the device error word into a status (and clear it).
 static int finish_sync(qw_handle* h) {
   QW_CUDA(h, cudaMemcpyAsync(h->h_status, h->d_status, 8, cudaMemcpyDeviceToHost, h->stream));
+  QW_CUDA(h, cudaMemcpyAsync(h->h_status + 3, h->d_err, 4, cudaMemcpyDeviceToHost, h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
-  const int err = ((volatile int*)h->h_status)[1];
+  const int err = ((volatile int*)h->h_status)[1] | ((volatile int*)h->h_status)[3];
   if (err == 0) return QW_OK;
+  QW_CUDA(h, cudaMemsetAsync(h->bar_slots, 0, (size_t)5 * h->cfg.n_layers * 4, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->d_status, 0, 8, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->d_err, 0, 4, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->attn_counters, 0, (size_t)h->cfg.n_kv_heads * 4, h->stream));
@@ -695,13 +801,14 @@ static int run_steps(qw_handle* h, int n, const int32_t* tokens, int first) {
   for (int i = 0; i < n; ++i) {
     const int tok = tokens ? tokens[i] : (i == 0 ? first : -1);
     if (tok != last) {
-      EmbedArgs ea = h->embed_args;
-      ea.tok = tok < 0 ? -1 : tok;
-      void* args[1] = {&ea};
-      cudaKernelNodeParams kp = h->embed_params;
+      std::vector<uint8_t>& buf = h->tok_args;
+      const int v = tok < 0 ? -1 : tok;
+      memcpy(buf.data() + h->tok_offset, &v, sizeof(int));
+      void* args[1] = {buf.data()};
+      cudaKernelNodeParams kp = h->tok_params;
       kp.kernelParams = args;
       kp.extra = nullptr;
-      QW_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->embed_node, &kp));
+      QW_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->tok_node, &kp));
       last = tok;
     }
     QW_CUDA(h, cudaGraphLaunch(h->exec, h->stream));
@@ -1106,5 +1213,20 @@ extern "C" int qw_gemm_bf16(const uint16_t* a_hi, const uint16_t* a_lo, const ui
   g.wait_ns = 1000000000ull;
   if (!g.err) QW_FAIL((qw_handle*)nullptr, QW_ERR_CUDA, "qw_gemm_bf16: error word lookup failed");
   QW_OP_CUDA(launch_gemm(bn, GEPI_STORE, ta_hi, ta_lo, tb, g, (cudaStream_t)stream));
+  return QW_OK;
+}
+
+extern "C" int qw_set_decode_path(qw_handle* h, int32_t path) {
+  if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_decode_path: null handle");
+  if (path != 0 && path != 1) QW_FAIL(h, QW_ERR_ARG, "qw_set_decode_path: path must be 0 or 1");
+  const bool mega = path == 0 && h->mega_ok;
+  if (mega != h->use_mega) h->graph_dirty = true;
+  h->use_mega = mega;
+  return QW_OK;
+}
+
+extern "C" int qw_get_decode_path(const qw_handle* h, int32_t* path) {
+  if (!h || !path) return QW_ERR_ARG;
+  *path = h->use_mega ? 0 : 1;
   return QW_OK;
 }

@@ -142,4 +142,53 @@ cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
 cudaError_t set_prefill_attributes();
 
+// ---- persistent decode step (decode_mega.cu) ----
+struct LayerDev {  // per-layer device pointers of the packed weights
+  const uint8_t* qkv;
+  const uint16_t* qkv_bias;
+  const uint8_t* o;
+  const uint8_t* gateup;
+  const uint8_t* down;
+  const uint16_t* attn_norm;
+  const uint16_t* mlp_norm;
+  const uint16_t* q_norm;
+  const uint16_t* k_norm;
+};
+struct MegaArgs {
+  int L, H, nq, nkv, hd, I, V;
+  float eps;
+  const uint16_t* embed;
+  const uint8_t* lm_head;
+  const uint16_t* final_norm;
+  const LayerDev* layers;  // device array [L]
+  float* k_cache;          // [L][nkv][cap][hd]
+  float* v_cache;
+  int cap;
+  const float2* rope;
+  float* x;                // [H] residual
+  float* qkv;              // [(nq+2nkv) hd]
+  float* attn_o;           // [nq hd]
+  float* mlp;              // [I]
+  float* logits;           // [V]
+  float* part_o;           // [nq][splits][hd]
+  float* part_ml;          // [nq][splits][2]
+  int* attn_counters;      // [nkv]
+  int splits;              // CTAs per KV head (gridDim.x / nkv)
+  ArgmaxOut am;
+  const int* pos;
+  int tok;                 // host token (graph-node argument) or -1: use *next_token
+  const int* next_token;
+  unsigned* bar_slots;     // [5 L] grid-barrier arrival counters
+  float* cap_emb;          // capture rows or nullptr
+  float* cap_blk0;
+  float* cap_final;
+  int* err;
+  uint64_t wait_ns;
+};
+bool mega_supported(int H, int I, int qd, int hd, int gq);
+size_t mega_smem_bytes();
+cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);
+cudaError_t set_mega_attributes();
+const void* mega_kernel_fn();
+
 }  // namespace qw

@@ -102,6 +102,11 @@ __device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8], float 
 }
 
 
+// Argmax order: larger value wins, equal values go to the lower index.
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
 // ------------------------------------------------------------------ TMA tensor copies
 // 2-D tiled load global -> shared (box given by the tensor map), completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,

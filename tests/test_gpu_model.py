@@ -261,3 +261,38 @@ def test_error_paths_on_device():
         assert violation(lg, o.prefill(d.prompt)["logits"]) <= 0
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("workload_name,steps", [("tiny", 16), ("qwen3_0.6b_decode", 24)])
+def test_persistent_and_multikernel_paths_agree(workload_name, steps):
+    # the default decode path (one persistent cooperative kernel per token) and
+    # the graph of separate kernels compute the same step
+    wl = W.WORKLOADS[workload_name]
+    d = W.draw(wl)
+    m, o = _models(wl, d)
+    m2 = DeviceModel(wl.shape, d.weights, wl.max_ctx)
+    try:
+        assert B.qw_get_decode_path(m.h) == 0          # the persistent kernel fits these shapes
+        B.qw_set_decode_path(m2.h, 1)
+        assert B.qw_get_decode_path(m2.h) == 1
+        tok = _prefill_check(m, o, d.prompt, capture=False)
+        m2.prefill(d.prompt)
+        for i in range(steps):
+            want = o.decode_step(tok)["logits"]
+            a1, l1 = m.decode(tok, logits=True)
+            a2, l2 = m2.decode(tok, logits=True)
+            assert violation(l1, want) <= 0 and violation(l2, want) <= 0
+            assert violation(l1, l2, 1e-4, 1e-4) <= 0
+            if top2_margin(want) > MARGIN:
+                assert a1 == a2 == R.greedy_argmax(want)
+            tok = R.greedy_argmax(want)
+        # both paths are deterministic run to run
+        m.reset()
+        m.prefill(d.prompt)
+        ids1 = m.greedy(tok, 8)
+        m.reset()
+        m.prefill(d.prompt)
+        assert m.greedy(tok, 8) == ids1
+    finally:
+        m.close()
+        m2.close()
