@@ -251,8 +251,8 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->part_o, (size_t)c.n_q_heads * h->nsplit_max * hd * 4},
       {(void**)&h->part_ml, (size_t)c.n_q_heads * h->nsplit_max * 2 * 4},
       {(void**)&h->attn_counters, nkv * 4},
-      {(void**)&h->blk_val, (size_t)h->lm_grid * 4},
-      {(void**)&h->blk_idx, (size_t)h->lm_grid * 4},
+      {(void**)&h->blk_val, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
+      {(void**)&h->blk_idx, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->am_counter, 4},
       {(void**)&h->d_pos, 4},
       {(void**)&h->d_next_token, 4},
