@@ -32,6 +32,7 @@ constexpr int kMaxC = 12;                    // input vectors up to 12 x 256 = 3
 constexpr int kTK = 32;                      // keys per attention tile (K + V = 32 KB at hd 128)
 constexpr int kGQ = 8;
 constexpr int kMinKeys = 64;
+constexpr int kUnitPre = 64;                 // units of a phase whose epilogue values are prefetched
 
 enum Kind { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GU = 3, K_DOWN = 4, K_LM = 5 };
 
@@ -50,6 +51,8 @@ struct Smem {
   float p_s[kGQ * kTK];
   float ml_s[2 * kGQ];
   float al_s[kGQ];
+  float unit_s[kUnitPre];        // per-unit values the epilogue needs (residual rows or bias)
+  float pml_s[2 * kGQ * 160];    // split partials (m, l) for the combine
 };
 
 // The contiguous slice of a row-streamed phase owned by CTA b: units [u0, u1),
@@ -186,17 +189,61 @@ __device__ void grid_barrier(const MegaArgs& a, Smem& S, int k, int nbar, bool& 
   abort = S.flag != 0;
 }
 
-// Phase input: xs = v (f32 [K], from L2), optionally RMS-normalised with gain g.
+// Phase input: xs = v (f32 [K], from L2), optionally RMS-normalised with gain g;
+// also prefetches `n_unit` per-unit epilogue values (residual rows or bias) into
+// unit_s. Every load is issued before any is used: each is an L2 round trip.
 __device__ void load_input(const MegaArgs& a, Smem& S, const float* v, int K, const uint16_t* g,
-                           bool from_embed, int tok) {
+                           bool from_embed, int tok, const float* unit_f32,
+                           const uint16_t* unit_bf16, int n_unit) {
+  constexpr int NT = kConsumers * 32;
+  constexpr int NV = (kMaxC * 256) / (4 * NT);  // float4 per thread
   const int tid = threadIdx.x;
-  float ss = 0.f;
-  for (int k = tid; k < K; k += kConsumers * 32) {
-    const float x = from_embed ? bf16f(a.embed[(size_t)tok * K + k]) : __ldcg(v + k);
-    S.xs[k] = x;
-    ss = fmaf(x, x, ss);
+  float4 xv[NV];
+  float uv = 0.f;
+  if (from_embed) {
+    const uint4* e = reinterpret_cast<const uint4*>(a.embed + (size_t)tok * K);
+    uint4 w[(NV + 1) / 2];
+#pragma unroll
+    for (int i = 0; i < (NV + 1) / 2; ++i) {
+      const int idx = tid + i * NT;
+      w[i] = idx * 8 < K ? e[idx] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < (NV + 1) / 2; ++i) {
+      const int idx = tid + i * NT;
+      if (idx * 8 < K) {
+        const uint32_t q[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          S.xs[idx * 8 + 2 * j] = __uint_as_float(q[j] << 16);
+          S.xs[idx * 8 + 2 * j + 1] = __uint_as_float(q[j] & 0xffff0000u);
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int idx = tid + i * NT;
+      xv[i] = idx * 4 < K ? __ldcg(reinterpret_cast<const float4*>(v) + idx)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
+  if (tid < n_unit) uv = unit_f32 ? __ldcg(unit_f32 + tid) : (unit_bf16 ? bf16f(unit_bf16[tid]) : 0.f);
+  float ss = 0.f;
+  if (!from_embed) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int idx = tid + i * NT;
+      if (idx * 4 < K) *reinterpret_cast<float4*>(&S.xs[idx * 4]) = xv[i];
+      ss = fmaf(xv[i].x, xv[i].x, fmaf(xv[i].y, xv[i].y, fmaf(xv[i].z, xv[i].z, fmaf(xv[i].w, xv[i].w, ss))));
+    }
+  }
+  if (tid < n_unit) S.unit_s[tid] = uv;
   if (g != nullptr) {
+    if (from_embed) {
+      csync();
+      for (int k = tid; k < K; k += NT) ss = fmaf(S.xs[k], S.xs[k], ss);
+    }
     ss = warp_sum(ss);
     csync();
     if ((tid & 31) == 0) S.red[tid >> 5] = ss;
@@ -205,7 +252,7 @@ __device__ void load_input(const MegaArgs& a, Smem& S, const float* v, int K, co
 #pragma unroll
     for (int i = 0; i < kConsumers; ++i) tot += S.red[i];
     const float r = 1.0f / sqrtf(tot / (float)K + a.eps);
-    for (int k = tid; k < K; k += kConsumers * 32) S.xs[k] = S.xs[k] * r * bf16f(g[k]);
+    for (int k = tid; k < K; k += NT) S.xs[k] = S.xs[k] * r * bf16f(g[k]);
   }
   csync();
 }
@@ -242,7 +289,7 @@ __device__ __forceinline__ void dot2(const uint8_t* w0, const uint8_t* w1, bool 
 struct GemvOut {
   int epi;                 // EPI_STORE / EPI_RESIDUAL / EPI_SWIGLU / EPI_LOGITS
   float* y;
-  const uint16_t* bias;
+  const uint16_t* bias;    // STORE: bias (its values for this CTA's units are in unit_s)
   float* cap;              // RESIDUAL: capture row base (already offset by pos * n)
   float best_v;            // LOGITS: running best of this warp (lane 0)
   int best_i;
@@ -278,10 +325,11 @@ __device__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, co
             if (j == 1 && !two) break;
             const int uu = u + t + j;
             const float v = j ? v1 : v0;
+            const int iu = uu - sl.u0;
             if (o.epi == EPI_STORE) {
-              o.y[uu] = v + (o.bias ? bf16f(o.bias[uu]) : 0.f);
+              o.y[uu] = v + (o.bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(o.bias[uu])) : 0.f);
             } else if (o.epi == EPI_RESIDUAL) {
-              const float nv = __ldcg(o.y + uu) + v;
+              const float nv = (iu < kUnitPre ? S.unit_s[iu] : __ldcg(o.y + uu)) + v;
               o.y[uu] = nv;
               if (o.cap) o.cap[uu] = nv;
             } else {  // EPI_LOGITS
@@ -482,19 +530,36 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
   csync();
   if (!S.flag) return;
   __threadfence();
+  // Combine: every (m, l) of the group into shared memory at once, then the
+  // partial outputs in batches of 8 independent loads.
+  const int ns = sp.nsplit;
+  for (int i = tid; i < GQ * ns; i += kConsumers * 32) {
+    const int h = i / ns, s2 = i % ns;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) +
+                             (size_t)(g * GQ + h) * a.splits + s2);
+    S.pml_s[2 * i] = ml.x;
+    S.pml_s[2 * i + 1] = ml.y;
+  }
+  csync();
 #pragma unroll
   for (int oi = 0; oi < OUTS; ++oi) {
     const int idx = tid + oi * 256;
     if (idx < GQ * HD) {
       const int h = idx / HD, d = idx % HD;
-      const size_t base = (size_t)(g * GQ + h) * a.splits;
+      const float* pm = S.pml_s + 2 * h * ns;
       float M = -INFINITY;
-      for (int s2 = 0; s2 < sp.nsplit; ++s2) M = fmaxf(M, __ldcg(a.part_ml + (base + s2) * 2));
-      float num = 0.f, den = 0.f;
-      for (int s2 = 0; s2 < sp.nsplit; ++s2) {
-        const float w = expf(__ldcg(a.part_ml + (base + s2) * 2) - M);
-        num = fmaf(w, __ldcg(a.part_o + (base + s2) * HD + d), num);
-        den = fmaf(w, __ldcg(a.part_ml + (base + s2) * 2 + 1), den);
+      for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pm[2 * s2]);
+      float den = 0.f;
+      for (int s2 = 0; s2 < ns; ++s2) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
+      const float* po = a.part_o + (size_t)(g * GQ + h) * a.splits * HD + d;
+      float num = 0.f;
+      for (int s0 = 0; s0 < ns; s0 += 8) {
+        float pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pv[j] = s0 + j < ns ? __ldcg(po + (size_t)(s0 + j) * HD) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j < ns) num = fmaf(expf(pm[2 * (s0 + j)] - M), pv[j], num);
       }
       a.attn_o[(size_t)(g * GQ + h) * HD + d] = num / den;
     }
@@ -623,7 +688,9 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
     const LayerDev& Ld = a.layers[l];
     if (l > 0) grid_barrier(a, S, k++, nbar, abort);
     // fused QKV; layer 0 gathers the embedding row itself and seeds the residual rows it owns
-    load_input(a, S, a.x, a.H, Ld.attn_norm, l == 0, tok);
+    const Slice qs = phase_slice(a, K_QKV, l, b, G);
+    load_input(a, S, a.x, a.H, Ld.attn_norm, l == 0, tok, nullptr,
+               Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr, min(qs.u1 - qs.u0, kUnitPre));
     if (l == 0) {
       const Slice os = phase_slice(a, K_O, 0, b, G);
       const uint16_t* e = a.embed + (size_t)tok * a.H;
@@ -632,7 +699,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
         for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_emb[(size_t)pos * a.H + r] = bf16f(e[r]);
     }
     GemvOut o{EPI_STORE, a.qkv, Ld.qkv_bias, nullptr, -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, phase_slice(a, K_QKV, l, b, G), a.H, 1, o, abort);
+    gemv_dispatch(a, ring, S, c, qs, a.H, 1, o, abort);
     grid_barrier(a, S, k++, nbar, abort);
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
@@ -641,25 +708,29 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
     }
     grid_barrier(a, S, k++, nbar, abort);
     // o_proj + residual
-    load_input(a, S, a.attn_o, qd, nullptr, false, 0);
+    const Slice os = phase_slice(a, K_O, l, b, G);
+    load_input(a, S, a.attn_o, qd, nullptr, false, 0, a.x + os.u0, nullptr,
+               min(os.u1 - os.u0, kUnitPre));
     o = GemvOut{EPI_RESIDUAL, a.x, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, phase_slice(a, K_O, l, b, G), qd, 1, o, abort);
+    gemv_dispatch(a, ring, S, c, os, qd, 1, o, abort);
     grid_barrier(a, S, k++, nbar, abort);
     // gate/up with SwiGLU
-    load_input(a, S, a.x, a.H, Ld.mlp_norm, false, 0);
+    load_input(a, S, a.x, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0);
     o = GemvOut{EPI_SWIGLU, a.mlp, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
     gemv_dispatch(a, ring, S, c, phase_slice(a, K_GU, l, b, G), a.H, 2, o, abort);
     grid_barrier(a, S, k++, nbar, abort);
     // down + residual (block-0 checkpoint)
-    load_input(a, S, a.mlp, a.I, nullptr, false, 0);
+    const Slice ds = phase_slice(a, K_DOWN, l, b, G);
+    load_input(a, S, a.mlp, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
+               min(ds.u1 - ds.u0, kUnitPre));
     o = GemvOut{EPI_RESIDUAL, a.x, nullptr,
                 (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr,
                 -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, phase_slice(a, K_DOWN, l, b, G), a.I, 1, o, abort);
+    gemv_dispatch(a, ring, S, c, ds, a.I, 1, o, abort);
   }
   grid_barrier(a, S, k++, nbar, abort);
   // final RMSNorm + LM head + greedy argmax
-  load_input(a, S, a.x, a.H, a.final_norm, false, 0);
+  load_input(a, S, a.x, a.H, a.final_norm, false, 0, nullptr, nullptr, 0);
   if (a.cap_final && b == 0)
     for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[r];
   GemvOut o{EPI_LOGITS, a.logits, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
