@@ -18,6 +18,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cstddef>
+
 #include "qw_internal.h"
 #include "qw_ptx.cuh"
 
@@ -43,7 +45,8 @@ struct Smem {
   float red[kConsumers];
   int redi[kConsumers];
   int flag;
-  float xs[kMaxC * 256];         // phase input vector (normalised when the phase has a norm)
+  alignas(16) float xs[kMaxC * 256];  // phase input vector (normalised when the phase has a norm);
+                                      // written with float4 stores, so 16-byte aligned
   float q_s[kGQ * 128];
   float kn_s[128];
   float vn_s[128];
@@ -764,6 +767,7 @@ bool mega_supported(int H, int I, int qd, int hd, int gq) {
          (uint32_t)qd * 2 <= kStage;
 }
 
+static_assert(offsetof(Smem, xs) % 16 == 0, "float4 stores into xs need 16-byte alignment");
 size_t mega_smem_bytes() { return (size_t)kNS * kStage + sizeof(Smem); }
 
 cudaError_t set_mega_attributes() {
