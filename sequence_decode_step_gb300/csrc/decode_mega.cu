@@ -232,6 +232,15 @@ __device__ void load_input(const MegaArgs& a, Smem& S, const float* v, int K, co
     }
   }
   if (tid < n_unit) uv = unit_f32 ? __ldcg(unit_f32 + tid) : (unit_bf16 ? bf16f(unit_bf16[tid]) : 0.f);
+  // the norm gain (bf16), 4 per float4 of input, in the same batch of loads
+  uint2 gv[NV];
+  if (g != nullptr) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int idx = tid + i * NT;
+      gv[i] = idx * 4 < K ? *reinterpret_cast<const uint2*>(g + idx * 4) : make_uint2(0, 0);
+    }
+  }
   float ss = 0.f;
   if (!from_embed) {
 #pragma unroll
@@ -255,7 +264,18 @@ __device__ void load_input(const MegaArgs& a, Smem& S, const float* v, int K, co
 #pragma unroll
     for (int i = 0; i < kConsumers; ++i) tot += S.red[i];
     const float r = 1.0f / sqrtf(tot / (float)K + a.eps);
-    for (int k = tid; k < K; k += NT) S.xs[k] = S.xs[k] * r * bf16f(g[k]);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int idx = tid + i * NT;
+      if (idx * 4 < K) {
+        float4 x4 = *reinterpret_cast<const float4*>(&S.xs[idx * 4]);
+        x4.x = x4.x * r * __uint_as_float(gv[i].x << 16);
+        x4.y = x4.y * r * __uint_as_float(gv[i].x & 0xffff0000u);
+        x4.z = x4.z * r * __uint_as_float(gv[i].y << 16);
+        x4.w = x4.w * r * __uint_as_float(gv[i].y & 0xffff0000u);
+        *reinterpret_cast<float4*>(&S.xs[idx * 4]) = x4;
+      }
+    }
   }
   csync();
 }
@@ -266,23 +286,40 @@ __device__ __forceinline__ void x_regs(const Smem& S, int K, float (&xr)[MAXC][8
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) {
     const int col = c * 256 + lane * 8;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) xr[c][e] = col < K ? S.xs[col + e] : 0.f;
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    if (col < K) {
+      lo = *reinterpret_cast<const float4*>(&S.xs[col]);
+      hi = *reinterpret_cast<const float4*>(&S.xs[col + 4]);
+    }
+    xr[c][0] = lo.x; xr[c][1] = lo.y; xr[c][2] = lo.z; xr[c][3] = lo.w;
+    xr[c][4] = hi.x; xr[c][5] = hi.y; xr[c][6] = hi.z; xr[c][7] = hi.w;
   }
 }
 
 // Dot products of two weight rows (bf16, in shared memory) with the register-held input.
 template <int MAXC>
 __device__ __forceinline__ void dot2(const uint8_t* w0, const uint8_t* w1, bool two, int K,
-                                     const float (&xr)[MAXC][8], float& s0, float& s1) {
+                                     const float (&xr)[MAXC > 0 ? MAXC : 1][8], const float* xs,
+                                     float& s0, float& s1) {
   const int lane = threadIdx.x & 31;
   float a0 = 0.f, a1 = 0.f;
+  if (MAXC > 0) {
 #pragma unroll
-  for (int c = 0; c < MAXC; ++c) {
-    const int col = c * 256 + lane * 8;
-    if (col < K) {
-      a0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[c], a0);
-      if (two) a1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[c], a1);
+    for (int c = 0; c < (MAXC > 0 ? MAXC : 1); ++c) {
+      const int col = c * 256 + lane * 8;
+      if (col < K) {
+        a0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[c], a0);
+        if (two) a1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[c], a1);
+      }
+    }
+  } else {
+#pragma unroll 4
+    for (int col = lane * 8; col < K; col += 256) {
+      const float4 lo = *reinterpret_cast<const float4*>(xs + col);
+      const float4 hi = *reinterpret_cast<const float4*>(xs + col + 4);
+      const float xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      a0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xv, a0);
+      if (two) a1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xv, a1);
     }
   }
   s0 = warp_sum(a0);
@@ -304,8 +341,8 @@ template <int MAXC>
 __device__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, const Slice& sl,
                            int K, int rpu, GemvOut& o, bool& abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float xr[MAXC][8];
-  x_regs<MAXC>(S, K, xr);
+  float xr[MAXC > 0 ? MAXC : 1][8];
+  if (MAXC > 0) x_regs<(MAXC > 0 ? MAXC : 1)>(S, K, xr);
   const uint32_t row_bytes = sl.unit_bytes / rpu;
   for (int u = sl.u0; u < sl.u1; u += sl.per_chunk, ++c) {
     const int nu = min(sl.per_chunk, sl.u1 - u);
@@ -321,7 +358,7 @@ __device__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, co
         float v0, v1;
         const bool two = t + 1 < nu;
         dot2<MAXC>(base + (size_t)t * row_bytes, base + (size_t)(t + 1) * row_bytes, two, K, xr,
-                   v0, v1);
+                   S.xs, v0, v1);
         if (lane == 0) {
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -347,7 +384,7 @@ __device__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, co
       for (int t = warp; t < nu; t += kConsumers) {
         float g, up;
         dot2<MAXC>(base + (size_t)t * sl.unit_bytes, base + (size_t)t * sl.unit_bytes + row_bytes,
-                   true, K, xr, g, up);
+                   true, K, xr, S.xs, g, up);
         if (lane == 0) o.y[u + t] = g / (1.0f + expf(-g)) * up;
       }
     }
@@ -361,7 +398,7 @@ __device__ void gemv_dispatch(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
                               int K, int rpu, GemvOut& o, bool& abort) {
   if (K <= 1024) gemv_phase<4>(a, ring, S, c, sl, K, rpu, o, abort);
   else if (K <= 2048) gemv_phase<8>(a, ring, S, c, sl, K, rpu, o, abort);
-  else gemv_phase<12>(a, ring, S, c, sl, K, rpu, o, abort);
+  else gemv_phase<0>(a, ring, S, c, sl, K, rpu, o, abort);  // x read from shared memory
 }
 
 
@@ -688,7 +725,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
   }
   const Split sp = attn_split(a, pos, b);
   for (int l = 0; l < a.L; ++l) {
-    const LayerDev& Ld = a.layers[l];
+    const LayerDev Ld = a.layers[l];  // one batch of loads per layer, kept in registers
     if (l > 0) grid_barrier(a, S, k++, nbar, abort);
     // fused QKV; layer 0 gathers the embedding row itself and seeds the residual rows it owns
     const Slice qs = phase_slice(a, K_QKV, l, b, G);
