@@ -79,9 +79,9 @@ __device__ __forceinline__ Slice make_slice(const uint8_t* w, int n_units, uint3
   return s;
 }
 
-__device__ __forceinline__ Slice phase_slice(const MegaArgs& a, int kind, int l, int b, int G) {
+__device__ __forceinline__ Slice phase_slice(const MegaArgs& a, int kind, const LayerDev& L, int b,
+                                             int G) {
   const int qd = a.nq * a.hd, kd = a.nkv * a.hd;
-  const LayerDev& L = a.layers[l < a.L ? l : 0];
   switch (kind) {
     case K_QKV: return make_slice(L.qkv, qd + 2 * kd, (uint32_t)a.H * 2, b, G);
     case K_O: return make_slice(L.o, a.H, (uint32_t)qd * 2, b, G);
@@ -131,6 +131,9 @@ __device__ __forceinline__ bool csync_or(bool v) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -168,8 +171,9 @@ __device__ void grid_barrier(const MegaArgs& a, Smem& S, int k, int nbar, bool& 
   if (threadIdx.x == 0) {
     unsigned* slot = a.bar_slots + k;
     const unsigned G = gridDim.x;
-    __threadfence();
-    atomicAdd(slot, 1u);
+    // Release: the phase's writes by this CTA (ordered before this thread by the
+    // consumer barrier above) become visible no later than the arrival.
+    red_release_add(slot, 1u);
     if (!abort && a.wait_ns == 0) {
       atomicOr(a.err, ERR_TIMEOUT);
       abort = true;
@@ -184,7 +188,8 @@ __device__ void grid_barrier(const MegaArgs& a, Smem& S, int k, int nbar, bool& 
         }
       }
     }
-    __threadfence();
+    // The acquire poll above, then the consumer barrier below, order every later
+    // read of this CTA after all CTAs' writes of the phase.
     if (blockIdx.x == 0 && !abort) a.bar_slots[(k - 1 + nbar) % nbar] = 0;
     S.flag = abort ? 1 : 0;
   }
@@ -304,13 +309,22 @@ __device__ __forceinline__ void dot2(const uint8_t* w0, const uint8_t* w1, bool 
   const int lane = threadIdx.x & 31;
   float a0 = 0.f, a1 = 0.f;
   if (MAXC > 0) {
+    // one accumulator per 256-column chunk: independent FMA chains, summed in order
+    float p0[MAXC > 0 ? MAXC : 1], p1[MAXC > 0 ? MAXC : 1];
 #pragma unroll
     for (int c = 0; c < (MAXC > 0 ? MAXC : 1); ++c) {
       const int col = c * 256 + lane * 8;
+      p0[c] = 0.f;
+      p1[c] = 0.f;
       if (col < K) {
-        a0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[c], a0);
-        if (two) a1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[c], a1);
+        p0[c] = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[c], 0.f);
+        if (two) p1[c] = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[c], 0.f);
       }
+    }
+#pragma unroll
+    for (int c = 0; c < (MAXC > 0 ? MAXC : 1); ++c) {
+      a0 += p0[c];
+      a1 += p1[c];
     }
   } else {
 #pragma unroll 4
@@ -636,18 +650,19 @@ __device__ void produce(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
   const size_t kv_layer = (size_t)a.nkv * a.cap * a.hd;
   bool ok = true;
   for (int l = 0; l < a.L && ok; ++l) {
-    ok = stream_slice(phase_slice(a, K_QKV, l, b, G));
+    const LayerDev Ld = a.layers[l];
+    ok = stream_slice(phase_slice(a, K_QKV, Ld, b, G));
     const float* kc = a.k_cache + (size_t)l * kv_layer + (size_t)sp.g * a.cap * a.hd;
     const float* vc = a.v_cache + (size_t)l * kv_layer + (size_t)sp.g * a.cap * a.hd;
     for (int t0 = sp.k0; ok && t0 < sp.k1; t0 += kTK) {
       const uint32_t n = (uint32_t)min(kTK, sp.k1 - t0) * a.hd * 4;
       ok = issue(kc + (size_t)t0 * a.hd, n, vc + (size_t)t0 * a.hd, n, (uint32_t)kTK * a.hd * 4);
     }
-    ok = ok && stream_slice(phase_slice(a, K_O, l, b, G));
-    ok = ok && stream_slice(phase_slice(a, K_GU, l, b, G));
-    ok = ok && stream_slice(phase_slice(a, K_DOWN, l, b, G));
+    ok = ok && stream_slice(phase_slice(a, K_O, Ld, b, G));
+    ok = ok && stream_slice(phase_slice(a, K_GU, Ld, b, G));
+    ok = ok && stream_slice(phase_slice(a, K_DOWN, Ld, b, G));
   }
-  if (ok) stream_slice(phase_slice(a, K_LM, 0, b, G));
+  if (ok) stream_slice(phase_slice(a, K_LM, LayerDev{}, b, G));
   // Leave only once every copy issued into this CTA's shared memory has landed.
   for (int cc = c > kNS ? c - kNS : 0; cc < c; ++cc)
     mbar_wait(&S.full[cc % kNS], (uint32_t)((cc / kNS) & 1), kDrainNs);
@@ -728,11 +743,11 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
     const LayerDev Ld = a.layers[l];  // one batch of loads per layer, kept in registers
     if (l > 0) grid_barrier(a, S, k++, nbar, abort);
     // fused QKV; layer 0 gathers the embedding row itself and seeds the residual rows it owns
-    const Slice qs = phase_slice(a, K_QKV, l, b, G);
+    const Slice qs = phase_slice(a, K_QKV, Ld, b, G);
     load_input(a, S, a.x, a.H, Ld.attn_norm, l == 0, tok, nullptr,
                Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr, min(qs.u1 - qs.u0, kUnitPre));
     if (l == 0) {
-      const Slice os = phase_slice(a, K_O, 0, b, G);
+      const Slice os = phase_slice(a, K_O, Ld, b, G);
       const uint16_t* e = a.embed + (size_t)tok * a.H;
       for (int r = os.u0 + tid; r < os.u1; r += kConsumers * 32) a.x[r] = bf16f(e[r]);
       if (a.cap_emb && b == 0)
@@ -748,7 +763,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
     }
     grid_barrier(a, S, k++, nbar, abort);
     // o_proj + residual
-    const Slice os = phase_slice(a, K_O, l, b, G);
+    const Slice os = phase_slice(a, K_O, Ld, b, G);
     load_input(a, S, a.attn_o, qd, nullptr, false, 0, a.x + os.u0, nullptr,
                min(os.u1 - os.u0, kUnitPre));
     o = GemvOut{EPI_RESIDUAL, a.x, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
@@ -757,10 +772,10 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
     // gate/up with SwiGLU
     load_input(a, S, a.x, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0);
     o = GemvOut{EPI_SWIGLU, a.mlp, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, phase_slice(a, K_GU, l, b, G), a.H, 2, o, abort);
+    gemv_dispatch(a, ring, S, c, phase_slice(a, K_GU, Ld, b, G), a.H, 2, o, abort);
     grid_barrier(a, S, k++, nbar, abort);
     // down + residual (block-0 checkpoint)
-    const Slice ds = phase_slice(a, K_DOWN, l, b, G);
+    const Slice ds = phase_slice(a, K_DOWN, Ld, b, G);
     load_input(a, S, a.mlp, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
                min(ds.u1 - ds.u0, kUnitPre));
     o = GemvOut{EPI_RESIDUAL, a.x, nullptr,
@@ -774,7 +789,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
   if (a.cap_final && b == 0)
     for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[r];
   GemvOut o{EPI_LOGITS, a.logits, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
-  gemv_dispatch(a, ring, S, c, phase_slice(a, K_LM, 0, b, G), a.H, 1, o, abort);
+  gemv_dispatch(a, ring, S, c, phase_slice(a, K_LM, LayerDev{}, b, G), a.H, 1, o, abort);
   argmax_finalize(a, S, o, pos);
 }
 
