@@ -358,6 +358,58 @@ __device__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, co
   float xr[MAXC > 0 ? MAXC : 1][8];
   if (MAXC > 0) x_regs<(MAXC > 0 ? MAXC : 1)>(S, K, xr);
   const uint32_t row_bytes = sl.unit_bytes / rpu;
+  const int n_units = sl.u1 - sl.u0;
+  const int n_chunks = (n_units + sl.per_chunk - 1) / sl.per_chunk;
+  if (o.epi != EPI_LOGITS && n_chunks <= kNS) {
+    // The whole phase fits in the ring: wait for every chunk once, then give each
+    // warp its units across chunks (more independent rows per warp), then release all.
+    bool ok = true;
+    for (int j = 0; j < n_chunks; ++j)
+      ok &= ring_wait(a, &S.full[(c + j) % kNS], (uint32_t)(((c + j) / kNS) & 1), abort);
+    if (__any_sync(0xffffffffu, !ok)) {
+      abort = true;
+      c += n_chunks;
+      return;
+    }
+    auto unit_ptr = [&](int i) {  // i-th unit of the slice, in its ring stage
+      const int j = i / sl.per_chunk;
+      return ring + (size_t)((c + j) % kNS) * kStage + (size_t)(i - j * sl.per_chunk) * sl.unit_bytes;
+    };
+    if (rpu == 1) {
+      for (int t = 2 * warp; t < n_units; t += 2 * kConsumers) {
+        float v0, v1;
+        const bool two = t + 1 < n_units;
+        dot2<MAXC>(unit_ptr(t), two ? unit_ptr(t + 1) : unit_ptr(t), two, K, xr, S.xs, v0, v1);
+        if (lane == 0) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            if (jj == 1 && !two) break;
+            const int iu = t + jj, uu = sl.u0 + iu;
+            const float v = jj ? v1 : v0;
+            if (o.epi == EPI_STORE) {
+              o.y[uu] = v + (o.bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(o.bias[uu])) : 0.f);
+            } else {  // EPI_RESIDUAL
+              const float nv = (iu < kUnitPre ? S.unit_s[iu] : __ldcg(o.y + uu)) + v;
+              o.y[uu] = nv;
+              if (o.cap) o.cap[uu] = nv;
+            }
+          }
+        }
+      }
+    } else {
+      for (int t = warp; t < n_units; t += kConsumers) {
+        float g, up;
+        const uint8_t* w = unit_ptr(t);
+        dot2<MAXC>(w, w + row_bytes, true, K, xr, S.xs, g, up);
+        if (lane == 0) o.y[sl.u0 + t] = g / (1.0f + expf(-g)) * up;
+      }
+    }
+    __syncwarp();
+    if (lane == 0)
+      for (int j = 0; j < n_chunks; ++j) mbar_arrive(&S.empty[(c + j) % kNS]);
+    c += n_chunks;
+    return;
+  }
   for (int u = sl.u0; u < sl.u1; u += sl.per_chunk, ++c) {
     const int nu = min(sl.per_chunk, sl.u1 - u);
     const int st = c % kNS;
