@@ -462,9 +462,10 @@ __device__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, co
 template <int MAXC_DUMMY = 0>
 __device__ void gemv_dispatch(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, const Slice& sl,
                               int K, int rpu, GemvOut& o, bool& abort) {
+  // Inputs up to 1024 wide stay in registers; wider ones are read from shared
+  // memory inside the dot (keeps the kernel under its register budget, no spills).
   if (K <= 1024) gemv_phase<4>(a, ring, S, c, sl, K, rpu, o, abort);
-  else if (K <= 2048) gemv_phase<8>(a, ring, S, c, sl, K, rpu, o, abort);
-  else gemv_phase<0>(a, ring, S, c, sl, K, rpu, o, abort);  // x read from shared memory
+  else gemv_phase<0>(a, ring, S, c, sl, K, rpu, o, abort);
 }
 
 
