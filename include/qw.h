@@ -106,8 +106,9 @@ typedef struct qw_weights {
   uint32_t reserved0;
   const void* embed;          /* bf16 [vocab, hidden] */
   const void* final_norm;     /* bf16 [hidden] */
-  const void* lm_head;        /* [vocab, hidden]; must be NULL iff tie_word_embeddings */
-  const void* lm_head_scales; /* int4 lm_head only, else NULL */
+  const void* lm_head;        /* [vocab, hidden]; must be NULL iff tie_word_embeddings;
+                               * int4 (with lm_head_scales) when weight_format is int4 */
+  const void* lm_head_scales; /* bf16 [vocab, hidden/128] for an int4 lm_head, else NULL */
   const void* const* attn_norm; /* bf16 [hidden] */
   const void* const* q;         /* [n_q_heads*head_dim, hidden] */
   const void* const* k;         /* [n_kv_heads*head_dim, hidden] */
@@ -167,8 +168,8 @@ int qw_load_weights(qw_handle* h, const qw_weights* w);
 /* Process T prompt ids (HOST array) at positions pos..pos+T-1, appending their
  * keys and values to the cache; afterwards pos += T. Prompts of at most
  * max_prefill_t ids with no LoRA active run as one batched causal pass; longer
- * prompts, or any prompt while a LoRA is set, run through the sequential
- * decode path ("Emberglass" README, maxPrefillT). logits_dev (DEVICE, vocab
+ * prompts, any prompt while a LoRA is set, and every prompt of an int4 model
+ * run through the sequential decode path ("Emberglass" README, maxPrefillT). logits_dev (DEVICE, vocab
  * floats, nullable) receives the last row's logits; argmax_host (nullable)
  * receives its greedy token and makes the call synchronous.
  * Errors: QW_ERR_ARG (T <= 0, id out of range), QW_ERR_CTX (pos+T > max_ctx). */

@@ -47,7 +47,7 @@ __device__ __forceinline__ void block_argmax_256(float& bv, int& bi, float* r8, 
 // whose weight rows are one contiguous byte range; it streams that range
 // through `n_stages` shared-memory stages with bulk copies. Warps are split
 // into `ks` K-slices (the input slice stays in registers) and 8/ks row groups.
-template <int EPI, int MAXC>
+template <int EPI, int MAXC, int W4>
 __global__ void __launch_bounds__(256, 1) gemv_kernel(const GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -146,9 +146,18 @@ __global__ void __launch_bounds__(256, 1) gemv_kernel(const GemvArgs a) {
       for (int cc = 0; cc < MAXC; ++cc) {
         const int col = (c_lo + cc) * 256 + lane * 8;
         if ((c_lo + cc < c_hi) && col < K) {
-          acc0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[cc], acc0);
-          if (two)
-            acc1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[cc], acc1);
+          if (W4) {  // 8 nibbles (4 bytes) and the scale of their 128-wide group
+            const uint32_t so = a.scale_off + (uint32_t)(col >> 7) * 2;
+            acc0 = dot8_i4(*reinterpret_cast<const uint32_t*>(w0 + col / 2), xr[cc],
+                           bf16f(*reinterpret_cast<const uint16_t*>(w0 + so)), acc0);
+            if (two)
+              acc1 = dot8_i4(*reinterpret_cast<const uint32_t*>(w1 + col / 2), xr[cc],
+                             bf16f(*reinterpret_cast<const uint16_t*>(w1 + so)), acc1);
+          } else {
+            acc0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[cc], acc0);
+            if (two)
+              acc1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[cc], acc1);
+          }
         }
       }
       acc0 = warp_sum(acc0);
@@ -164,7 +173,24 @@ __global__ void __launch_bounds__(256, 1) gemv_kernel(const GemvArgs a) {
       float v0 = 0.f;
       for (int q = 0; q < ksz; ++q) v0 += red[(t * a.rpu) * ksz + q];
       if (EPI == EPI_STORE) {
-        a.y[u] = v0 + (a.bias ? bf16f(a.bias[u]) : 0.f);
+        float v = v0 + (a.bias ? bf16f(a.bias[u]) : 0.f);
+        if (a.lora_bq != nullptr) {  // low-rank update on the q and v rows
+          const uint16_t* brow = nullptr;
+          const float* t = nullptr;
+          if (u < a.lora_q_rows) {
+            brow = a.lora_bq + (size_t)u * a.lora_r;
+            t = a.lora_t;
+          } else if (u >= a.lora_v_row0 && u < a.lora_v_row0 + a.lora_v_rows) {
+            brow = a.lora_bv + (size_t)(u - a.lora_v_row0) * a.lora_r;
+            t = a.lora_t + a.lora_r;
+          }
+          if (brow) {
+            float d = 0.f;
+            for (int j = 0; j < a.lora_r; ++j) d = fmaf(bf16f(brow[j]), __ldcg(t + j), d);
+            v = fmaf(a.lora_scale, d, v);
+          }
+        }
+        a.y[u] = v;
       } else if (EPI == EPI_RESIDUAL) {
         const float nv = __ldcg(a.y + u) + v0;
         a.y[u] = nv;
@@ -289,8 +315,13 @@ static cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cu
 template <int EPI>
 static cudaError_t launch_gemv_epi(const GemvArgs& a, int grid, bool pdl, cudaStream_t s) {
   const size_t smem = gemv_smem_bytes(a);
-  if (a.cpw <= 4) return launch_ex(gemv_kernel<EPI, 4>, dim3(grid), dim3(256), smem, s, pdl, a);
-  if (a.cpw <= 8) return launch_ex(gemv_kernel<EPI, 8>, dim3(grid), dim3(256), smem, s, pdl, a);
+  if (a.w4) {
+    if (a.cpw <= 4) return launch_ex(gemv_kernel<EPI, 4, 1>, dim3(grid), dim3(256), smem, s, pdl, a);
+    if (a.cpw <= 8) return launch_ex(gemv_kernel<EPI, 8, 1>, dim3(grid), dim3(256), smem, s, pdl, a);
+    return cudaErrorInvalidValue;
+  }
+  if (a.cpw <= 4) return launch_ex(gemv_kernel<EPI, 4, 0>, dim3(grid), dim3(256), smem, s, pdl, a);
+  if (a.cpw <= 8) return launch_ex(gemv_kernel<EPI, 8, 0>, dim3(grid), dim3(256), smem, s, pdl, a);
   return cudaErrorInvalidValue;
 }
 
@@ -624,6 +655,28 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s) {
 }
 const void* embed_kernel_fn() { return reinterpret_cast<const void*>(embed_kernel); }
 
+// ------------------------------------------------------------------ int4 row packing
+// Row r of (nib [rows, K/2], scales [rows, K/128]) -> dst row dst_row0 + r * step in
+// the layout nibbles | scales | zero pad (int4_row_bytes(K) bytes per row).
+__global__ void pack_int4_rows_kernel(const uint8_t* nib, const uint16_t* scales, int K,
+                                      uint8_t* dst, int dst_row0, int step) {
+  const int r = blockIdx.x;
+  const uint32_t rb = int4_row_bytes(K), half = (uint32_t)K / 2, G = (uint32_t)K / 128;
+  uint8_t* d = dst + (size_t)(dst_row0 + (size_t)r * step) * rb;
+  const uint8_t* sn = nib + (size_t)r * half;
+  for (uint32_t i = threadIdx.x; i < half; i += blockDim.x) d[i] = sn[i];
+  const uint16_t* ss = scales + (size_t)r * G;
+  for (uint32_t i = threadIdx.x; i < (rb - half) / 2; i += blockDim.x)
+    reinterpret_cast<uint16_t*>(d + half)[i] = i < G ? ss[i] : (uint16_t)0;
+}
+
+cudaError_t launch_pack_int4_rows(const uint8_t* nib, const uint16_t* scales, int rows, int K,
+                                  uint8_t* dst, int dst_row0, int dst_row_step, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  pack_int4_rows_kernel<<<rows, 256, 0, s>>>(nib, scales, K, dst, dst_row0, dst_row_step);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ RoPE table
 // cos/sin of p * theta^(-2j/hd), formed in fp64 and rounded to f32 once.
 __global__ void rope_table_kernel(float2* t, int cap, int hd, double theta) {
@@ -711,14 +764,16 @@ cudaError_t set_kernel_attributes() {
   cudaError_t e = cudaSuccess;
 #define QW_ALLOW(k, b) \
   if (e == cudaSuccess) e = allow_smem(k, b)
-  QW_ALLOW((gemv_kernel<EPI_STORE, 4>), big);
-  QW_ALLOW((gemv_kernel<EPI_STORE, 8>), big);
-  QW_ALLOW((gemv_kernel<EPI_RESIDUAL, 4>), big);
-  QW_ALLOW((gemv_kernel<EPI_RESIDUAL, 8>), big);
-  QW_ALLOW((gemv_kernel<EPI_SWIGLU, 4>), big);
-  QW_ALLOW((gemv_kernel<EPI_SWIGLU, 8>), big);
-  QW_ALLOW((gemv_kernel<EPI_LOGITS, 4>), big);
-  QW_ALLOW((gemv_kernel<EPI_LOGITS, 8>), big);
+#define QW_ALLOW_GEMV(E)                 \
+  QW_ALLOW((gemv_kernel<E, 4, 0>), big); \
+  QW_ALLOW((gemv_kernel<E, 8, 0>), big); \
+  QW_ALLOW((gemv_kernel<E, 4, 1>), big); \
+  QW_ALLOW((gemv_kernel<E, 8, 1>), big)
+  QW_ALLOW_GEMV(EPI_STORE);
+  QW_ALLOW_GEMV(EPI_RESIDUAL);
+  QW_ALLOW_GEMV(EPI_SWIGLU);
+  QW_ALLOW_GEMV(EPI_LOGITS);
+#undef QW_ALLOW_GEMV
   QW_ALLOW(attn_decode_kernel<64>, attn_smem<64>());
   QW_ALLOW(attn_decode_kernel<128>, attn_smem<128>());
   QW_ALLOW(embed_kernel, 0);

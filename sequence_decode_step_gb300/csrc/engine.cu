@@ -153,6 +153,13 @@ struct qw_handle {
   int pos = 0;
   bool have_prev = false;
   bool lora_active = false;
+  // LoRA (borrowed device pointers, per layer) and its A . x_n buffer
+  std::vector<const uint16_t*> lora_qa, lora_qb, lora_va, lora_vb;
+  int lora_rank = 0;
+  float lora_scale = 0.f;
+  float* lora_t = nullptr;  // [2 * 64]
+  bool w4 = false;          // int4 g128 linear weights
+  bool lm_w4 = false;       // int4 LM head (untied int4 models)
   std::string err;
 };
 
@@ -197,8 +204,8 @@ static int validate_config(const qw_config* c, std::string& why) {
     why = "hidden, intermediate and n_q_heads*head_dim are limited to 16384";
     return QW_ERR_ARG;
   }
-  if (c->weight_format != QW_WEIGHTS_BF16) {
-    why = "weight_format: only QW_WEIGHTS_BF16 is implemented in this build";
+  if (c->weight_format != QW_WEIGHTS_BF16 && c->weight_format != QW_WEIGHTS_INT4_G128) {
+    why = "weight_format must be QW_WEIGHTS_BF16 or QW_WEIGHTS_INT4_G128";
     return QW_ERR_ARG;
   }
   if (c->max_ctx <= 0 || c->max_prefill_t < 0) {
@@ -236,6 +243,8 @@ static int alloc_state(qw_handle* h) {
                mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim, c.head_dim,
                               c.n_q_heads / c.n_kv_heads);
   h->use_mega = h->mega_ok;
+  h->w4 = c.weight_format == QW_WEIGHTS_INT4_G128;
+  h->lm_w4 = h->w4 && !c.tie_word_embeddings;
   h->lm_grid = std::min({c.vocab, h->num_sms, 1024});
   struct Piece { void** p; size_t bytes; };
   const size_t kv_bytes = L * nkv * cap * hd * 4;
@@ -261,6 +270,7 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->d_tokens_by_pos, cap * 4},
       {(void**)&h->d_status, 8},
       {(void**)&h->bar_slots, (size_t)5 * L * 4},
+      {(void**)&h->lora_t, 2 * 64 * 4},
   };
   const size_t Tm = (size_t)c.max_prefill_t, H = c.hidden, I = c.intermediate;
   const size_t qd = (size_t)c.n_q_heads * hd;
@@ -377,6 +387,14 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: qk_norm set but q_norm/k_norm missing");
   if (c.qkv_bias && (!w->q_bias || !w->k_bias || !w->v_bias))
     QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: qkv_bias set but a bias is missing");
+  if (h->w4 && (!w->q_scales || !w->k_scales || !w->v_scales || !w->o_scales ||
+                !w->gate_scales || !w->up_scales || !w->down_scales ||
+                (h->lm_w4 && !w->lm_head_scales)))
+    QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: int4 weights need every scales tensor");
+  for (int l = 0; l < L && h->w4; ++l)
+    if (!w->q_scales[l] || !w->k_scales[l] || !w->v_scales[l] || !w->o_scales[l] ||
+        !w->gate_scales[l] || !w->up_scales[l] || !w->down_scales[l])
+      QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: NULL scales at layer " + std::to_string(l));
   for (int l = 0; l < L; ++l) {
     if (!w->attn_norm[l] || !w->q[l] || !w->k[l] || !w->v[l] || !w->o[l] || !w->mlp_norm[l] ||
         !w->gate[l] || !w->up[l] || !w->down[l] || (c.qk_norm && (!w->q_norm[l] || !w->k_norm[l])) ||
@@ -394,14 +412,17 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     cudaFree(h->warena);
     h->warena = nullptr;
   }
+  // Bytes of one packed row of K inputs: bf16, or int4 nibbles + scales (+ pad).
+  auto rb = [&](size_t K) -> size_t { return h->w4 ? int4_row_bytes((int)K) : K * 2; };
+  const size_t lm_rb = h->lm_w4 ? int4_row_bytes((int)H) : H * 2;
   // Arena layout, 256-byte aligned pieces.
-  const size_t per_layer = align_up((qd + 2 * kd) * H * 2, 256) +
+  const size_t per_layer = align_up((qd + 2 * kd) * rb(H), 256) +
                            (c.qkv_bias ? align_up((qd + 2 * kd) * 2, 256) : 0) +
-                           align_up(H * qd * 2, 256) + align_up(2 * I * H * 2, 256) +
-                           align_up(H * I * 2, 256) + 2 * align_up(H * 2, 256) +
+                           align_up(H * rb(qd), 256) + align_up(2 * I * rb(H), 256) +
+                           align_up(H * rb(I), 256) + 2 * align_up(H * 2, 256) +
                            (c.qk_norm ? 2 * align_up(hd * 2, 256) : 0);
   const size_t head = align_up((size_t)c.vocab * H * 2, 256) +
-                      (c.tie_word_embeddings ? 0 : align_up((size_t)c.vocab * H * 2, 256)) +
+                      (c.tie_word_embeddings ? 0 : align_up((size_t)c.vocab * lm_rb, 256)) +
                       align_up(H * 2, 256);
   h->warena_bytes = per_layer * L + head;
   QW_CUDA(h, cudaMalloc((void**)&h->warena, h->warena_bytes));
@@ -419,6 +440,11 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
   h->embed = (const uint16_t*)p;
   if (c.tie_word_embeddings) {
     h->lm_head = h->embed;  // one table serves the gather and the output projection
+  } else if (h->lm_w4) {
+    p = take((size_t)c.vocab * lm_rb);
+    QW_CUDA(h, launch_pack_int4_rows((const uint8_t*)w->lm_head, (const uint16_t*)w->lm_head_scales,
+                                     c.vocab, (int)H, p, 0, 1, h->stream));
+    h->lm_head = (const uint16_t*)p;
   } else {
     p = take((size_t)c.vocab * H * 2);
     QW_CUDA(h, cp(p, w->lm_head, (size_t)c.vocab * H * 2));
@@ -430,10 +456,21 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
   h->layers.assign(L, LayerW());
   for (int l = 0; l < L; ++l) {
     LayerW& lw = h->layers[l];
-    p = take((qd + 2 * kd) * H * 2);  // fused [q; k; v] rows
-    QW_CUDA(h, cp(p, w->q[l], qd * H * 2));
-    QW_CUDA(h, cp(p + qd * H * 2, w->k[l], kd * H * 2));
-    QW_CUDA(h, cp(p + (qd + kd) * H * 2, w->v[l], kd * H * 2));
+    auto pack4 = [&](const void* nib, const void* sc, size_t rows, size_t K, uint8_t* dst,
+                     size_t row0, int step) {
+      return launch_pack_int4_rows((const uint8_t*)nib, (const uint16_t*)sc, (int)rows, (int)K, dst,
+                                   (int)row0, step, h->stream);
+    };
+    p = take((qd + 2 * kd) * rb(H));  // fused [q; k; v] rows
+    if (h->w4) {
+      QW_CUDA(h, pack4(w->q[l], w->q_scales[l], qd, H, p, 0, 1));
+      QW_CUDA(h, pack4(w->k[l], w->k_scales[l], kd, H, p, qd, 1));
+      QW_CUDA(h, pack4(w->v[l], w->v_scales[l], kd, H, p, qd + kd, 1));
+    } else {
+      QW_CUDA(h, cp(p, w->q[l], qd * H * 2));
+      QW_CUDA(h, cp(p + qd * H * 2, w->k[l], kd * H * 2));
+      QW_CUDA(h, cp(p + (qd + kd) * H * 2, w->v[l], kd * H * 2));
+    }
     lw.qkv = (const uint16_t*)p;
     if (c.qkv_bias) {
       p = take((qd + 2 * kd) * 2);
@@ -442,17 +479,24 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
       QW_CUDA(h, cp(p + (qd + kd) * 2, w->v_bias[l], kd * 2));
       lw.qkv_bias = (const uint16_t*)p;
     }
-    p = take(H * qd * 2);
-    QW_CUDA(h, cp(p, w->o[l], H * qd * 2));
+    p = take(H * rb(qd));
+    if (h->w4) QW_CUDA(h, pack4(w->o[l], w->o_scales[l], H, qd, p, 0, 1));
+    else QW_CUDA(h, cp(p, w->o[l], H * qd * 2));
     lw.o = (const uint16_t*)p;
-    p = take(2 * I * H * 2);  // gate row i -> packed row 2i, up row i -> 2i+1
-    QW_CUDA(h, cudaMemcpy2DAsync(p, 2 * H * 2, w->gate[l], H * 2, H * 2, I,
-                                 cudaMemcpyDeviceToDevice, h->stream));
-    QW_CUDA(h, cudaMemcpy2DAsync(p + H * 2, 2 * H * 2, w->up[l], H * 2, H * 2, I,
-                                 cudaMemcpyDeviceToDevice, h->stream));
+    p = take(2 * I * rb(H));  // gate row i -> packed row 2i, up row i -> 2i+1
+    if (h->w4) {
+      QW_CUDA(h, pack4(w->gate[l], w->gate_scales[l], I, H, p, 0, 2));
+      QW_CUDA(h, pack4(w->up[l], w->up_scales[l], I, H, p, 1, 2));
+    } else {
+      QW_CUDA(h, cudaMemcpy2DAsync(p, 2 * H * 2, w->gate[l], H * 2, H * 2, I,
+                                   cudaMemcpyDeviceToDevice, h->stream));
+      QW_CUDA(h, cudaMemcpy2DAsync(p + H * 2, 2 * H * 2, w->up[l], H * 2, H * 2, I,
+                                   cudaMemcpyDeviceToDevice, h->stream));
+    }
     lw.gateup = (const uint16_t*)p;
-    p = take(H * I * 2);
-    QW_CUDA(h, cp(p, w->down[l], H * I * 2));
+    p = take(H * rb(I));
+    if (h->w4) QW_CUDA(h, pack4(w->down[l], w->down_scales[l], H, I, p, 0, 1));
+    else QW_CUDA(h, cp(p, w->down[l], H * I * 2));
     lw.down = (const uint16_t*)p;
     p = take(H * 2);
     QW_CUDA(h, cp(p, w->attn_norm[l], H * 2));
@@ -483,7 +527,7 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     QW_CUDA(h, cudaMemcpyAsync(h->d_layers, ld.data(), L * sizeof(LayerDev),
                                cudaMemcpyHostToDevice, h->stream));
   }
-  if (c.max_prefill_t > 0) {
+  if (c.max_prefill_t > 0 && !h->w4) {
     h->tm_qkv.resize(L);
     h->tm_ow.resize(L);
     h->tm_gu.resize(L);
@@ -519,13 +563,16 @@ static void plan(GemvArgs& a, int grid) {
     plan_gemv(a, grid, kStreamStage, kStreamStages);
 }
 
-static GemvArgs base_gemv(qw_handle* h, const void* w, int n_units, int rpu, int K) {
+static GemvArgs base_gemv(qw_handle* h, const void* w, int n_units, int rpu, int K,
+                          bool w4) {
   GemvArgs a{};
   a.w = (const uint8_t*)w;
   a.n_units = n_units;
   a.rpu = rpu;
   a.K = K;
-  a.row_bytes = (uint32_t)K * 2;
+  a.w4 = w4 ? 1 : 0;
+  a.row_bytes = w4 ? int4_row_bytes(K) : (uint32_t)K * 2;
+  a.scale_off = (uint32_t)K / 2;
   a.eps = h->cfg.eps;
   a.err = h->d_err;
   a.wait_ns = h->wait_ns;
@@ -537,7 +584,7 @@ static GemvArgs base_gemv(qw_handle* h, const void* w, int n_units, int rpu, int
 // the last CTA records the id at the device position and advances it.
 static cudaError_t launch_lm_head(qw_handle* h, const float* x, float* norm_out, bool pdl,
                                   cudaStream_t s) {
-  GemvArgs a = base_gemv(h, h->lm_head, h->cfg.vocab, 1, h->cfg.hidden);
+  GemvArgs a = base_gemv(h, h->lm_head, h->cfg.vocab, 1, h->cfg.hidden, h->lm_w4);
   a.x = x;
   a.norm_g = h->final_norm;
   a.y = h->logits;
@@ -627,12 +674,34 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
 
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& lw = h->layers[l];
+    if (h->lora_active) {  // t = A_q . RMSNorm(x) and A_v . RMSNorm(x), rank entries each
+      for (int j = 0; j < 2; ++j) {
+        GemvArgs a = base_gemv(h, j == 0 ? h->lora_qa[l] : h->lora_va[l], h->lora_rank, 1, H,
+                               false);
+        a.x = h->x;
+        a.norm_g = lw.attn_norm;
+        a.y = h->lora_t + j * h->lora_rank;
+        const int grid = h->lora_rank;
+        plan(a, grid);
+        if ((e = launch_gemv(EPI_STORE, a, grid, true, s)) != cudaSuccess) return e;
+      }
+    }
     {  // fused QKV projection with the input RMSNorm in its prologue
-      GemvArgs a = base_gemv(h, lw.qkv, qkv_rows, 1, H);
+      GemvArgs a = base_gemv(h, lw.qkv, qkv_rows, 1, H, h->w4);
       a.x = h->x;
       a.norm_g = lw.attn_norm;
       a.bias = lw.qkv_bias;
       a.y = h->qkv;
+      if (h->lora_active) {
+        a.lora_bq = h->lora_qb[l];
+        a.lora_bv = h->lora_vb[l];
+        a.lora_t = h->lora_t;
+        a.lora_r = h->lora_rank;
+        a.lora_q_rows = qd;
+        a.lora_v_row0 = qd + kd;
+        a.lora_v_rows = kd;
+        a.lora_scale = h->lora_scale;
+      }
       const int grid = std::min(qkv_rows, h->num_sms);
       plan(a, grid);
       if ((e = launch_gemv(EPI_STORE, a, grid, true, s)) != cudaSuccess) return e;
@@ -662,7 +731,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       if ((e = launch_attention(t, hd, true, s)) != cudaSuccess) return e;
     }
     {  // o_proj + residual
-      GemvArgs a = base_gemv(h, lw.o, H, 1, qd);
+      GemvArgs a = base_gemv(h, lw.o, H, 1, qd, h->w4);
       a.x = h->attn_o;
       a.y = h->x;
       const int grid = std::min(H, h->num_sms);
@@ -670,7 +739,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       if ((e = launch_gemv(EPI_RESIDUAL, a, grid, true, s)) != cudaSuccess) return e;
     }
     {  // gate/up with the post-attention RMSNorm in its prologue, SwiGLU epilogue
-      GemvArgs a = base_gemv(h, lw.gateup, I, 2, H);
+      GemvArgs a = base_gemv(h, lw.gateup, I, 2, H, h->w4);
       a.x = h->x;
       a.norm_g = lw.mlp_norm;
       a.y = h->mlp;
@@ -679,7 +748,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       if ((e = launch_gemv(EPI_SWIGLU, a, grid, true, s)) != cudaSuccess) return e;
     }
     {  // down + residual (block-0 checkpoint taken here)
-      GemvArgs a = base_gemv(h, lw.down, H, 1, I);
+      GemvArgs a = base_gemv(h, lw.down, H, 1, I, h->w4);
       a.x = h->mlp;
       a.y = h->x;
       a.cap_out = (h->capture_on && l == 0) ? h->cap_blk0 : nullptr;
@@ -949,7 +1018,7 @@ extern "C" int qw_prefill(qw_handle* h, const int32_t* ids_host, int32_t T, floa
     QW_FAIL(h, QW_ERR_CTX, "qw_prefill: pos + T > max_ctx");
   DeviceGuard dg(h->device);
   const int p0 = h->pos;
-  if (T <= h->cfg.max_prefill_t && !h->lora_active) {
+  if (T <= h->cfg.max_prefill_t && !h->lora_active && !h->w4) {
     rc = prefill_batched(h, ids_host, T);
   } else {
     // Sequential path ("Emberglass" README, maxPrefillT: longer prompts, or a
@@ -1015,9 +1084,44 @@ extern "C" int qw_kv_cache(qw_handle* h, int32_t layer, float** k_dev, float** v
 
 extern "C" int qw_set_lora(qw_handle* h, const qw_lora* lora) {
   if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_lora: null handle");
-  if (lora == nullptr) return QW_OK;
+  if (lora == nullptr) {  // clear: the next step's graph has no LoRA work at all
+    if (h->lora_active) h->graph_dirty = true;
+    h->lora_active = false;
+    h->lora_qa.clear();
+    h->lora_qb.clear();
+    h->lora_va.clear();
+    h->lora_vb.clear();
+    if (h->mega_ok) h->use_mega = true;
+    return QW_OK;
+  }
   if (lora->struct_size != sizeof(qw_lora)) QW_FAIL(h, QW_ERR_ABI, "qw_set_lora: struct_size mismatch");
-  QW_FAIL(h, QW_ERR_ARG, "qw_set_lora: LoRA is not implemented in this build");
+  if (lora->rank < 1 || lora->rank > 64) QW_FAIL(h, QW_ERR_ARG, "qw_set_lora: rank must be 1..64");
+  const int L = h->cfg.n_layers;
+  if (!lora->q_a || !lora->q_b || !lora->v_a || !lora->v_b)
+    QW_FAIL(h, QW_ERR_ARG, "qw_set_lora: a per-layer array is NULL");
+  for (int l = 0; l < L; ++l) {
+    const void* ptrs[4] = {lora->q_a[l], lora->q_b[l], lora->v_a[l], lora->v_b[l]};
+    for (const void* p : ptrs)
+      if (!p || (reinterpret_cast<uintptr_t>(p) & 15))
+        QW_FAIL(h, QW_ERR_ARG, "qw_set_lora: NULL or unaligned (16 B) tensor at layer " +
+                                   std::to_string(l));
+  }
+  h->lora_qa.assign(L, nullptr);
+  h->lora_qb.assign(L, nullptr);
+  h->lora_va.assign(L, nullptr);
+  h->lora_vb.assign(L, nullptr);
+  for (int l = 0; l < L; ++l) {
+    h->lora_qa[l] = (const uint16_t*)lora->q_a[l];
+    h->lora_qb[l] = (const uint16_t*)lora->q_b[l];
+    h->lora_va[l] = (const uint16_t*)lora->v_a[l];
+    h->lora_vb[l] = (const uint16_t*)lora->v_b[l];
+  }
+  h->lora_rank = lora->rank;
+  h->lora_scale = lora->alpha / (float)lora->rank;
+  h->lora_active = true;
+  h->use_mega = false;  // the LoRA branch runs on the multi-kernel path
+  h->graph_dirty = true;
+  return QW_OK;
 }
 
 extern "C" int qw_set_wait_limit_ns(qw_handle* h, uint64_t ns) {
@@ -1219,7 +1323,7 @@ extern "C" int qw_gemm_bf16(const uint16_t* a_hi, const uint16_t* a_lo, const ui
 extern "C" int qw_set_decode_path(qw_handle* h, int32_t path) {
   if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_decode_path: null handle");
   if (path != 0 && path != 1) QW_FAIL(h, QW_ERR_ARG, "qw_set_decode_path: path must be 0 or 1");
-  const bool mega = path == 0 && h->mega_ok;
+  const bool mega = path == 0 && h->mega_ok && !h->lora_active;
   if (mega != h->use_mega) h->graph_dirty = true;
   h->use_mega = mega;
   return QW_OK;

@@ -30,7 +30,10 @@ struct ArgmaxOut {
 
 // y = epilogue(W . prologue(x)); W rows grouped in units of `rpu` rows.
 struct GemvArgs {
-  const uint8_t* w;       // packed bf16 rows, unit u = rows [u*rpu, (u+1)*rpu)
+  const uint8_t* w;       // packed rows, unit u = rows [u*rpu, (u+1)*rpu)
+  int w4;                 // 0: bf16 rows (K*2 bytes); 1: int4 g128 rows = K/2 nibble bytes,
+                          //    then K/128 bf16 scales at byte `scale_off`, padded to 16 bytes
+  uint32_t scale_off;
   int n_units;
   int rpu;                // rows per unit: 1, or 2 for interleaved gate/up
   int K;                  // input length (multiple of 8)
@@ -51,9 +54,22 @@ struct GemvArgs {
   int units_per_stage;
   uint32_t off_red, off_x, off_stage;  // shared-memory offsets
   ArgmaxOut am;           // EPI_LOGITS only
+  // EPI_STORE only: LoRA on the q rows [0, lora_q_rows) and the v rows
+  // [lora_v_row0, lora_v_row0 + lora_v_rows): y += lora_scale * B[row] . t
+  const uint16_t* lora_bq;  // bf16 [q rows, r] or nullptr
+  const uint16_t* lora_bv;  // bf16 [v rows, r]
+  const float* lora_t;      // [2 r]: A_q . x_n, then A_v . x_n
+  int lora_r, lora_q_rows, lora_v_row0, lora_v_rows;
+  float lora_scale;
   int* err;
   uint64_t wait_ns;
 };
+// Bytes of one int4 g128 row of K inputs in the packed layout above.
+__host__ __device__ inline uint32_t int4_row_bytes(int K) {
+  return (uint32_t)K / 2 + (((uint32_t)K / 128 * 2 + 15) & ~15u);
+}
+cudaError_t launch_pack_int4_rows(const uint8_t* nib, const uint16_t* scales, int rows, int K,
+                                  uint8_t* dst, int dst_row0, int dst_row_step, cudaStream_t s);
 
 struct AttnArgs {
   const float* qkv;        // raw [(nq + 2 nkv) * hd]

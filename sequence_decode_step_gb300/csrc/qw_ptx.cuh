@@ -107,6 +107,27 @@ __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+
+// 8 int4 weights (one 32-bit word: element 2b in the low nibble of byte b, value
+// nibble - 8) dotted with 8 floats, times the group scale. A nibble n becomes the
+// float 2^23 + n by placing it in the mantissa of 2^23 (one byte permute), and
+// subtracting 2^23 + 8 leaves n - 8 exactly.
+__device__ __forceinline__ float i4f(uint32_t v, uint32_t b) {
+  return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7540u | b)) - 8388616.0f;
+}
+__device__ __forceinline__ float dot8_i4(uint32_t w, const float (&x)[8], float s, float acc) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+  float p = i4f(lo, 0) * x[0];
+  p = fmaf(i4f(hi, 0), x[1], p);
+  p = fmaf(i4f(lo, 1), x[2], p);
+  p = fmaf(i4f(hi, 1), x[3], p);
+  p = fmaf(i4f(lo, 2), x[4], p);
+  p = fmaf(i4f(hi, 2), x[5], p);
+  p = fmaf(i4f(lo, 3), x[6], p);
+  p = fmaf(i4f(hi, 3), x[7], p);
+  return fmaf(p, s, acc);
+}
+
 // ------------------------------------------------------------------ TMA tensor copies
 // 2-D tiled load global -> shared (box given by the tensor map), completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,

@@ -63,10 +63,27 @@ class DeviceModel:
         s = self.shape
         keep = []
 
+        int4 = s.weight_format == "int4_g128"
+        L_ = B.lib()
+
         def up(name):
             t = _to_dev(weights[name])
             keep.append(t)
             return t.data_ptr()
+
+        def up_q(name):
+            """float32 [rows, K] -> int4 g128 (packed nibbles, bf16 scales) on the device."""
+            w32 = _to_dev(np.ascontiguousarray(weights[name], dtype=np.float32))
+            rows, K = w32.shape
+            packed = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
+            scales = torch.empty((rows, K // 128), dtype=torch.int16, device="cuda")
+            B.check("qw_quantize_int4_g128",
+                    L_.qw_quantize_int4_g128(w32.data_ptr(), rows, K, packed.data_ptr(),
+                                             scales.data_ptr(), None))
+            keep.extend([packed, scales])
+            torch.cuda.synchronize()
+            del w32
+            return packed.data_ptr(), scales.data_ptr()
 
         L = s.n_layers
         lists = {}
@@ -76,13 +93,27 @@ class DeviceModel:
                 return None
             return B.ptr_array([up(f"layers.{l}.{nm}") for l in range(L)])
 
+        def per_layer_q(nm):
+            ps = [up_q(f"layers.{l}.{nm}") for l in range(L)]
+            return B.ptr_array([p for p, _ in ps]), B.ptr_array([q for _, q in ps])
+
         w = B.qw_weights()
         w.struct_size = C.sizeof(B.qw_weights)
         w.embed = up("embed")
         w.final_norm = up("final_norm")
-        w.lm_head = None if s.tie_word_embeddings else up("lm_head")
-        for nm in ("attn_norm", "q", "k", "v", "o", "mlp_norm", "gate", "up", "down"):
+        if s.tie_word_embeddings:
+            w.lm_head = None
+        elif int4:
+            w.lm_head, w.lm_head_scales = up_q("lm_head")
+        else:
+            w.lm_head = up("lm_head")
+        for nm in ("attn_norm", "mlp_norm"):
             lists[nm] = per_layer(nm)
+        for nm in ("q", "k", "v", "o", "gate", "up", "down"):
+            if int4:
+                lists[nm], lists[nm + "_scales"] = per_layer_q(nm)
+            else:
+                lists[nm] = per_layer(nm)
         lists["q_norm"] = per_layer("q_norm", s.qk_norm)
         lists["k_norm"] = per_layer("k_norm", s.qk_norm)
         for nm in ("q_bias", "k_bias", "v_bias"):
@@ -121,6 +152,27 @@ class DeviceModel:
         k, v = B.qw_kv_cache(self.h, layer)
         shp = (self.shape.n_kv_heads, self.max_ctx, self.shape.head_dim)
         return device_view(k, shp), device_view(v, shp)
+
+    def set_lora(self, lora, alpha: float = 0.0) -> None:
+        """Set (dict 'lora.{l}.q_a' ... of bf16 bits) or clear (None) the adapter; the
+        uploaded tensors are kept alive here because the library borrows them."""
+        if lora is None:
+            B.qw_set_lora(self.h, None)
+            self._lora_keep = None
+            return
+        L = self.shape.n_layers
+        keep = {}
+        arrays = {}
+        for nm in ("q_a", "q_b", "v_a", "v_b"):
+            ts = [_to_dev(lora[f"lora.{l}.{nm}"]) for l in range(L)]
+            keep[nm] = ts
+            arrays[nm] = B.ptr_array([t.data_ptr() for t in ts])
+        rank = lora["lora.0.q_a"].shape[0]
+        st = B.qw_lora(struct_size=C.sizeof(B.qw_lora), rank=rank, alpha=alpha)
+        for nm, arr in arrays.items():
+            setattr(st, nm, C.cast(arr, B.PP))
+        B.qw_set_lora(self.h, st)
+        self._lora_keep = (keep, arrays)
 
     def set_kv(self, layer: int, k: np.ndarray, v: np.ndarray) -> None:
         import torch

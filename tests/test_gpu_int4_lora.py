@@ -1,0 +1,140 @@
+"""Qwen2.5-style decode: int4 group-128 weights (quantised on the device), q/k/v
+biases, no QK-norm, untied int4 LM head, and a LoRA on q_proj and v_proj that is
+set and cleared live ("Emberglass" README: int4 g128, LoRA hot-swap, perfect
+restore on clear).
+
+The GPU quantiser and the oracle's quantiser are separate implementations of the
+same rule (checked bit-exact in test_gpu_ops); each side quantises the same f32
+draws itself. Clearing the adapter must give bit-identical logits to a handle
+that never had one.
+"""
+import numpy as np
+import pytest
+
+import workload as W
+from oracle import qwen_ref as R
+from sequence_decode_step_gb300 import _binding as B
+from sequence_decode_step_gb300.device_model import DeviceModel
+
+from gpu_util import MARGIN, top2_margin, violation
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+TINY_INT4 = W.TINY.replace(weight_format="int4_g128", tie_word_embeddings=False,
+                           int4_lm_head=True, qk_norm=False, qkv_bias=True, n_kv_heads=1)
+
+
+def _lora(d):
+    return {k: v for k, v in d.weights.items() if k.startswith("lora.")}
+
+
+def _run(m, o, tok, steps, check_ids=True):
+    """Teacher-forced steps; returns the GPU logits of every step."""
+    out = []
+    for i in range(steps):
+        want = o.decode_step(tok)["logits"]
+        got_id, got = m.decode(tok, logits=True)
+        assert violation(got, want) <= 0, f"step {i}: off by {violation(got, want)}"
+        if check_ids and top2_margin(want) > MARGIN:
+            assert got_id == R.greedy_argmax(want)
+        out.append(got)
+        tok = R.greedy_argmax(want)
+    return out
+
+
+def test_tiny_int4_decode():
+    wl = W.Workload("t4", TINY_INT4, seed=5, prompt_len=8, decode_steps=16, max_ctx=64)
+    d = W.draw(wl, drawn_gains=True)
+    m = DeviceModel(wl.shape, d.weights, 64, max_prefill_t=64)   # int4 prefill: sequential
+    o = R.build_oracle(d)
+    try:
+        assert B.qw_get_decode_path(m.h) == 1
+        am, lg = m.prefill(d.prompt, logits=True)
+        ref = o.prefill(d.prompt)["logits"]
+        assert violation(lg, ref) <= 0
+        _run(m, o, R.greedy_argmax(ref), 16)
+    finally:
+        m.close()
+
+
+@pytest.mark.parametrize("shape", [TINY_INT4, W.TINY.replace(qkv_bias=True)],
+                         ids=["int4", "bf16"])
+def test_tiny_lora_on_then_cleared(shape):
+    wl = W.Workload("tl", shape, seed=6, prompt_len=6, decode_steps=12, max_ctx=64,
+                    lora=W.LoraShape(4, 8.0))
+    d = W.draw(wl, drawn_gains=True)
+    m = DeviceModel(shape, d.weights, 64, max_prefill_t=64)
+    fresh = DeviceModel(shape, d.weights, 64, max_prefill_t=64)
+    try:
+        # phase A: adapter on (prefill falls back to the sequential path)
+        m.set_lora(_lora(d), 8.0)
+        o = R.build_oracle(d, lora_on=True)
+        am, lg = m.prefill(d.prompt, logits=True)
+        ref = o.prefill(d.prompt)["logits"]
+        assert violation(lg, ref) <= 0
+        base = R.build_oracle(d).prefill(d.prompt)["logits"]
+        assert np.abs(ref - base).max() > 1e-3          # the adapter changes the output
+        _run(m, o, R.greedy_argmax(ref), wl.decode_steps)
+        # phase B: cleared; same inputs as a handle that never had an adapter
+        m.set_lora(None)
+        m.reset()
+        o2 = R.build_oracle(d)
+        am, lg = m.prefill(d.prompt, logits=True)
+        am_f, lg_f = fresh.prefill(d.prompt, logits=True)
+        np.testing.assert_array_equal(lg, lg_f)
+        ref2 = o2.prefill(d.prompt)["logits"]
+        tok = R.greedy_argmax(ref2)
+        for _ in range(wl.decode_steps):
+            want = o2.decode_step(tok)["logits"]
+            _, a = m.decode(tok, logits=True)
+            _, b = fresh.decode(tok, logits=True)
+            np.testing.assert_array_equal(a, b)
+            assert violation(a, want) <= 0
+            tok = R.greedy_argmax(want)
+    finally:
+        m.close()
+        fresh.close()
+
+
+def test_qwen25_3b_int4_lora_4k():
+    wl = W.WORKLOADS["qwen2.5_3b_int4_lora"]
+    d = W.draw(wl)
+    lora = _lora(d)
+    o = R.build_oracle(d, lora_on=True)
+    m = DeviceModel(wl.shape, d.weights, wl.max_ctx)
+    fresh = DeviceModel(wl.shape, d.weights, wl.max_ctx)
+    d.weights = {}                                            # the oracle keeps its own copies
+    P = wl.kv_prefill
+    try:
+        for l, (k, v) in enumerate(d.kv):
+            m.set_kv(l, k, v)
+            fresh.set_kv(l, k, v)
+        m.set_pos(P)
+        fresh.set_pos(P)
+        # phase A: 64 steps with the adapter
+        m.set_lora(lora, wl.lora.alpha)
+        _run(m, o, d.start_token, wl.decode_steps)
+        # phase B: cleared, cache and position restored, 64 steps; bit-identical to a
+        # handle that never had the adapter, and within tolerance of the oracle
+        m.set_lora(None)
+        o.set_lora(None)
+        o.reset()
+        for l, (k, v) in enumerate(d.kv):
+            m.set_kv(l, k, v)
+            o.set_kv(l, k, v)
+        m.set_pos(P)
+        o.pos = P
+        tok = d.start_token
+        for i in range(wl.decode_steps):
+            want = o.decode_step(tok)["logits"]
+            ga, a = m.decode(tok, logits=True)
+            gb, b = fresh.decode(tok, logits=True)
+            np.testing.assert_array_equal(a, b)
+            assert violation(a, want) <= 0, f"step {i}"
+            if top2_margin(want) > MARGIN:
+                assert ga == R.greedy_argmax(want)
+            tok = R.greedy_argmax(want)
+    finally:
+        m.close()
+        fresh.close()
