@@ -122,6 +122,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def aggregate(ms_local: float, tokens_local: int, world: int, device: str = "cuda"):
+    """Replicas only: every rank times its own independent decode; the job's time is
+    the slowest rank's and its throughput is all ranks' tokens over that time.
+    Returns (ms_max, tokens_total)."""
+    if world <= 1:
+        return ms_local, tokens_local
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    n = torch.tensor([tokens_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 # ============================================================================ GPU arm
 def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
     import ctypes as C
@@ -173,11 +188,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
         torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     ms = sum(a.elapsed_time(b) for a, b in pairs)
-    t_max = torch.tensor([ms], device="cuda")
+    ms_max, tok_total = aggregate(ms, n_tok * args.steps, world)
     if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
         torch.distributed.barrier()
-    ms_max = float(t_max.item())
 
     # ---- end to end: token from the host, greedy id back to the host, every token
     e2e_ms = 0.0
@@ -206,7 +219,6 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
     bytes_step = step_bytes(s, p0, n_tok)
-    tok_total = n_tok * args.steps * world
     sec_tok = ms_max / 1e3 / (n_tok * args.steps)
     if path == 0:
         dominant = {"kernel": "decode_mega_kernel (the whole decode step: one persistent cooperative "

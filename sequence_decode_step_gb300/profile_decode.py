@@ -1,7 +1,7 @@
 """Drive a few decode steps of a workload for profilers (ncu) and quick timing.
 
   python -m sequence_decode_step_gb300.profile_decode [--workload NAME] [--tokens N]
-         [--lm-head N]
+         [--lm-head N] [--prefill-reps N] [--path 0|1]
 
 Draws the workload's weights, prefills its prompt (or preloads its KV cache),
 runs N greedy decode tokens as graph replays, then N stand-alone LM-head
@@ -27,6 +27,9 @@ def main():
     ap.add_argument("--workload", default="qwen3_0.6b_decode")
     ap.add_argument("--tokens", type=int, default=8)
     ap.add_argument("--lm-head", type=int, default=4)
+    ap.add_argument("--prefill-reps", type=int, default=0,
+                    help="batched prefills of the workload's prompt to run first")
+    ap.add_argument("--path", type=int, default=0, help="decode path: 0 persistent, 1 graph")
     args = ap.parse_args()
     wl = W.WORKLOADS[args.workload]
     d = W.draw(wl)
@@ -34,16 +37,26 @@ def main():
     torch.cuda.set_stream(stream)
     m = DeviceModel(wl.shape, d.weights, max_ctx=max(wl.max_ctx, wl.prompt_len + wl.kv_prefill
                                                      + args.tokens + 8),
+                    max_prefill_t=wl.prompt_len if args.prefill_reps else 0,
                     stream=stream.cuda_stream)
     L = B.lib()
+    B.qw_set_decode_path(m.h, args.path)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.prefill_reps):
+        m.reset()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        m.prefill(d.prompt)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        print(f"prefill T={len(d.prompt)}: {e0.elapsed_time(e1):.3f} ms")
     if wl.kv_prefill:
         for l, (k, v) in enumerate(d.kv):
             m.set_kv(l, k, v)
         m.set_pos(wl.kv_prefill)
         first = d.start_token
     else:
-        first = m.prefill(d.prompt)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        first = m.prefill(d.prompt) if not args.prefill_reps else m.decode(-1)
     torch.cuda.synchronize()
     e0.record(stream)
     rc = L.qw_decode_step(m.h, first, None, None)
