@@ -124,21 +124,67 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
       const int nv = min(16, a.N - col0);
+      // full 16-column blocks move as 16-byte vectors (ldo, ldb are multiples of 16 B)
+      const bool vec = nv == 16 && (a.ldo % 4) == 0 && (a.ldb % 8) == 0;
       if (EPI == GEPI_STORE) {
         float* o = a.out + (size_t)row * a.ldo + col0;
+        if (vec) {
+          if (a.bias) {
+            const uint4 b0 = *reinterpret_cast<const uint4*>(a.bias + col0);
+            const uint4 b1 = *reinterpret_cast<const uint4*>(a.bias + col0 + 8);
+            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (j < nv) o[j] = v[j] + (a.bias ? __uint_as_float((uint32_t)a.bias[col0 + j] << 16) : 0.f);
+            for (int j = 0; j < 8; ++j) {
+              v[2 * j] += __uint_as_float(bw[j] << 16);
+              v[2 * j + 1] += __uint_as_float(bw[j] & 0xffff0000u);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(o + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < nv) o[j] = v[j] + (a.bias ? __uint_as_float((uint32_t)a.bias[col0 + j] << 16) : 0.f);
+        }
       } else if (EPI == GEPI_RESID) {
         float* o = a.out + (size_t)row * a.ldo + col0;
+        if (vec) {
+          float4 cur[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (j < nv) {
-            const float nvl = o[j] + v[j];
-            o[j] = nvl;
-            if (a.cap_out) a.cap_out[(size_t)(a.cap_row0 + row) * a.ldo + col0 + j] = nvl;
+          for (int j = 0; j < 4; ++j) cur[j] = *reinterpret_cast<const float4*>(o + 4 * j);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 n4 = make_float4(cur[j].x + v[4 * j], cur[j].y + v[4 * j + 1],
+                                          cur[j].z + v[4 * j + 2], cur[j].w + v[4 * j + 3]);
+            *reinterpret_cast<float4*>(o + 4 * j) = n4;
+            if (a.cap_out)
+              *reinterpret_cast<float4*>(a.cap_out + (size_t)(a.cap_row0 + row) * a.ldo + col0 + 4 * j) = n4;
           }
-      } else {  // GEPI_SWIGLU
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < nv) {
+              const float nvl = o[j] + v[j];
+              o[j] = nvl;
+              if (a.cap_out) a.cap_out[(size_t)(a.cap_row0 + row) * a.ldo + col0 + j] = nvl;
+            }
+        }
+      } else if (vec) {  // GEPI_SWIGLU, 8 units as one 16-byte store per half
+        uint16_t hi[8], lo[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float g = v[2 * j], up = v[2 * j + 1];
+          split_bf16(g / (1.0f + expf(-g)) * up, hi[j], lo[j]);
+        }
+        const size_t off = (size_t)row * a.ldb + col0 / 2;
+        *reinterpret_cast<uint4*>(a.out_hi + off) =
+            make_uint4(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16),
+                       hi[4] | ((uint32_t)hi[5] << 16), hi[6] | ((uint32_t)hi[7] << 16));
+        *reinterpret_cast<uint4*>(a.out_lo + off) =
+            make_uint4(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16),
+                       lo[4] | ((uint32_t)lo[5] << 16), lo[6] | ((uint32_t)lo[7] << 16));
+      } else {  // GEPI_SWIGLU tail
         const int u0 = col0 / 2;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -270,14 +316,23 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(const float* Q, const
   const int t0 = blockIdx.x * BQ, h = blockIdx.y, g = h / (nq / nkv);
   const int nrows = min(BQ, T - t0);
   const int last_key = p0 + t0 + nrows - 1;
-  for (int idx = tid; idx < BQ * HD / 4; idx += 256) {
-    const int r = idx % BQ, d4 = idx / BQ;
-    float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < nrows) q = *reinterpret_cast<const float4*>(Q + ((size_t)(t0 + r) * nq + h) * HD + d4 * 4);
-    Qt[(d4 * 4 + 0) * BQ + r] = q.x;
-    Qt[(d4 * 4 + 1) * BQ + r] = q.y;
-    Qt[(d4 * 4 + 2) * BQ + r] = q.z;
-    Qt[(d4 * 4 + 3) * BQ + r] = q.w;
+  constexpr int NL = BQ * HD / 4 / 256;  // float4 per thread per tile (8 at hd 128)
+  {
+    float4 q[NL];
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {  // every load in flight before any is used
+      const int idx = tid + i * 256, r = idx % BQ, d4 = idx / BQ;
+      q[i] = r < nrows ? *reinterpret_cast<const float4*>(Q + ((size_t)(t0 + r) * nq + h) * HD + d4 * 4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int idx = tid + i * 256, r = idx % BQ, d4 = idx / BQ;
+      Qt[(d4 * 4 + 0) * BQ + r] = q[i].x;
+      Qt[(d4 * 4 + 1) * BQ + r] = q[i].y;
+      Qt[(d4 * 4 + 2) * BQ + r] = q[i].z;
+      Qt[(d4 * 4 + 3) * BQ + r] = q[i].w;
+    }
   }
   float m[4], l[4], acc[4][DPT];
 #pragma unroll
@@ -292,19 +347,31 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(const float* Q, const
   const int n_tiles = last_key / BK + 1;
   for (int kt = 0; kt < n_tiles; ++kt) {
     const int k0 = kt * BK;
+    // K is stored transposed (key index fastest across threads: conflict-free
+    // stores); V row-major with the dimension fastest (coalesced loads and
+    // conflict-free stores). All loads of the tile are issued before any store.
+    float4 kv[NL], vv[NL];
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int idx = tid + i * 256;
+      const int rk = idx % BK, dk = idx / BK;
+      const int rv = idx / (HD / 4), dv = idx % (HD / 4);
+      kv[i] = k0 + rk <= last_key ? *reinterpret_cast<const float4*>(kg + (size_t)(k0 + rk) * HD + dk * 4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      vv[i] = k0 + rv <= last_key ? *reinterpret_cast<const float4*>(vg + (size_t)(k0 + rv) * HD + dv * 4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     __syncthreads();
-    for (int idx = tid; idx < BK * HD / 4; idx += 256) {
-      const int r = idx % BK, d4 = idx / BK;
-      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (k0 + r <= last_key) {
-        kv = *reinterpret_cast<const float4*>(kg + (size_t)(k0 + r) * HD + d4 * 4);
-        vv = *reinterpret_cast<const float4*>(vg + (size_t)(k0 + r) * HD + d4 * 4);
-      }
-      Kt[(d4 * 4 + 0) * BK + r] = kv.x;
-      Kt[(d4 * 4 + 1) * BK + r] = kv.y;
-      Kt[(d4 * 4 + 2) * BK + r] = kv.z;
-      Kt[(d4 * 4 + 3) * BK + r] = kv.w;
-      *reinterpret_cast<float4*>(Vs + r * HD + d4 * 4) = vv;
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int idx = tid + i * 256;
+      const int rk = idx % BK, dk = idx / BK;
+      const int rv = idx / (HD / 4), dv = idx % (HD / 4);
+      Kt[(dk * 4 + 0) * BK + rk] = kv[i].x;
+      Kt[(dk * 4 + 1) * BK + rk] = kv[i].y;
+      Kt[(dk * 4 + 2) * BK + rk] = kv[i].z;
+      Kt[(dk * 4 + 3) * BK + rk] = kv[i].w;
+      *reinterpret_cast<float4*>(Vs + rv * HD + dv * 4) = vv[i];
     }
     __syncthreads();
     float sc[4][4];
