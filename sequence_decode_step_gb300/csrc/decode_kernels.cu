@@ -499,6 +499,8 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
         Ks[(pos - t0) * HD + e] = kn_s[e];
         Vs[(pos - t0) * HD + e] = vn_s[e];
       }
+      // order these generic writes before a later bulk copy into the same stage
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncthreads();
     }
     for (int j = warp; j < nk; j += 8) {

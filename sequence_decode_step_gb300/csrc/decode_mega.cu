@@ -6,13 +6,27 @@
 // streams the bytes with bulk TMA copies into a ring of shared-memory stages.
 // None of these bytes depend on activations, so the producer runs ahead of
 // the consumers across phase boundaries and the HBM stream never drains.
-// Warps 0..7 consume: each phase waits on a grid barrier for its input vector,
-// reads it from L2, and works through its chunks from the ring. The embedding
-// gather is done redundantly by every CTA, so layer 0 needs no barrier; a
-// token has 5 L grid barriers. Every wait is bounded (%globaltimer); a wait
-// that gives up sets ERR_TIMEOUT and the kernel runs on to its end without
-// hanging. All reductions have a fixed order, so results are bit-identical
-// run to run.
+// Warps 0..7 consume: each phase reads its input vector from L2 and works
+// through its chunks from the ring.
+//
+// There is no grid barrier. Every activation a phase hands to the next one
+// (residual x, fused q/k/v, attention output, SwiGLU output) is stored as a
+// 64-bit word: the f32 value in the low half and a tag in the high half, the
+// tag naming the token launch (a device epoch) and the phase that wrote it.
+// A single 64-bit store is single-copy atomic, so a reader that polls the
+// words of its input until all carry the expected tag has both waited for and
+// loaded the data in the same L2 round trip. A phase waits only for what it
+// reads: the attention of a KV head starts as soon as that head's q/k/v rows
+// are in, independently of the other heads.
+//
+// Reuse of a buffer is safe without a barrier because every overwrite of a
+// tagged vector depends, through the chain of full-vector inputs, on every
+// reader of the previous contents having finished (each reader also writes an
+// output the overwriter transitively needs); a CTA with no rows in a phase
+// therefore does not read that phase's input at all. Every wait is bounded
+// (%globaltimer); a wait that gives up sets ERR_TIMEOUT and the kernel runs on
+// to its end without hanging. All reductions have a fixed order, so results
+// are bit-identical run to run.
 
 #include <cuda_runtime.h>
 #include <math.h>
@@ -26,7 +40,10 @@
 namespace qw {
 namespace {
 
-constexpr int kConsumers = 8;                // consumer warps
+// 7 consumer warps + 1 producer warp: 8 warps are 2 per SM sub-partition, which
+// leaves 255 registers per thread (9 warps would cap them at 168 and spill).
+constexpr int kConsumers = 7;                // consumer warps
+constexpr int kNT = kConsumers * 32;         // consumer threads
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kNS = 6;                       // ring stages
 constexpr uint32_t kStage = 32 * 1024;       // bytes per stage
@@ -131,20 +148,14 @@ __device__ __forceinline__ bool csync_or(bool v) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ bool err_set(const MegaArgs& a) {
   return (*reinterpret_cast<volatile int*>(a.err) & ERR_TIMEOUT) != 0;
 }
 
 // Wait for a ring stage (or any mbarrier) with the kernel's bound; gives up at
-// once when another CTA already reported a timeout.
+// once when another CTA already reported a timeout. Reading %globaltimer costs
+// far more than a try_wait, so the clock (and the error word) is looked at only
+// every 16th failed try; the bound starts counting at the first look.
 __device__ bool ring_wait(const MegaArgs& a, uint64_t* bar, uint32_t parity, bool& abort) {
   if (abort) return false;
   if (a.wait_ns == 0) {  // a zero bound gives up at once (tests the error path)
@@ -152,11 +163,14 @@ __device__ bool ring_wait(const MegaArgs& a, uint64_t* bar, uint32_t parity, boo
     abort = true;
     return false;
   }
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > a.wait_ns || err_set(a)) {
+    if ((n & 15u) != 0) continue;
+    const uint64_t now = globaltimer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > a.wait_ns || err_set(a)) {
       atomicOr(a.err, ERR_TIMEOUT);
       abort = true;
       return false;
@@ -164,60 +178,107 @@ __device__ bool ring_wait(const MegaArgs& a, uint64_t* bar, uint32_t parity, boo
   }
 }
 
-// Grid barrier k of the token: every CTA's consumers arrive once; CTA 0 clears
-// the previous slot (all CTAs have left it once all have arrived here).
-__device__ void grid_barrier(const MegaArgs& a, Smem& S, int k, int nbar, bool& abort) {
-  abort = csync_or(abort);
-  if (threadIdx.x == 0) {
-    unsigned* slot = a.bar_slots + k;
-    const unsigned G = gridDim.x;
-    // Release: the phase's writes by this CTA (ordered before this thread by the
-    // consumer barrier above) become visible no later than the arrival.
-    red_release_add(slot, 1u);
-    if (!abort && a.wait_ns == 0) {
-      atomicOr(a.err, ERR_TIMEOUT);
-      abort = true;
-    }
-    if (!abort) {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire(slot) < G) {
-        if (globaltimer_ns() - t0 > a.wait_ns || err_set(a)) {
-          atomicOr(a.err, ERR_TIMEOUT);
-          abort = true;
-          break;
-        }
-      }
-    }
-    // The acquire poll above, then the consumer barrier below, order every later
-    // read of this CTA after all CTAs' writes of the phase.
-    if (blockIdx.x == 0 && !abort) a.bar_slots[(k - 1 + nbar) % nbar] = 0;
-    S.flag = abort ? 1 : 0;
-  }
-  csync();
-  abort = S.flag != 0;
+// Tagged activation words: value bits low, tag high.
+__device__ __forceinline__ float word_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ uint32_t word_tag(uint64_t w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
+  const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ void ld_words2(const uint64_t* p, uint64_t& w0, uint64_t& w1) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+               : "=l"(w0), "=l"(w1)
+               : "l"(p)
+               : "memory");
 }
 
-// Phase input: xs = v (f32 [K], from L2), optionally RMS-normalised with gain g;
-// also prefetches `n_unit` per-unit epilogue values (residual rows or bias) into
-// unit_s. Every load is issued before any is used: each is an L2 round trip.
-__device__ void load_input(const MegaArgs& a, Smem& S, const float* v, int K, const uint16_t* g,
-                           bool from_embed, int tok, const float* unit_f32,
-                           const uint16_t* unit_bf16, int n_unit) {
+// One more round `n` of a poll found data missing: give up (ERR_TIMEOUT) at once
+// when the bound is zero, else once the bound has passed or another CTA gave up.
+// The clock and the error word are looked at only every 32nd round (a read of
+// %globaltimer costs more than the L2 round trip of a poll); the bound starts
+// counting at the first look.
+__device__ __forceinline__ void poll_bound(const MegaArgs& a, uint32_t n, uint64_t& t0,
+                                           bool& abort) {
+  if (a.wait_ns == 0) {
+    atomicOr(a.err, ERR_TIMEOUT);
+    abort = true;
+    return;
+  }
+  if ((n & 31u) != 0) return;
+  const uint64_t now = globaltimer_ns();
+  if (t0 == 0) {
+    t0 = now;
+  } else if (now - t0 > a.wait_ns || err_set(a)) {
+    atomicOr(a.err, ERR_TIMEOUT);
+    abort = true;
+  }
+}
+
+// Per lane: words src[lane + 32 e], e < N, once all carry `tag`.
+template <int N>
+__device__ __forceinline__ void poll_row(const MegaArgs& a, const uint64_t* src, uint32_t tag,
+                                         float (&v)[N], bool& abort) {
+  const int lane = threadIdx.x & 31;
+  uint64_t w[N];
+  unsigned pend = (1u << N) - 1u;
+  uint64_t t0 = 0;
+  for (uint32_t n = 1; pend && !abort; ++n) {
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if ((pend >> e) & 1u) w[e] = ld_word(src + lane + 32 * e);
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if (((pend >> e) & 1u) && word_tag(w[e]) == tag) pend &= ~(1u << e);
+    if (pend) poll_bound(a, n, t0, abort);
+  }
+#pragma unroll
+  for (int e = 0; e < N; ++e) v[e] = abort ? 0.f : word_value(w[e]);
+}
+
+// Phase input: xs = v[0, K) once every word carries `tag` (or the embedding row
+// of `tok`), RMS-normalised with gain g when given; also prefetches `n_unit`
+// per-unit epilogue values (this CTA's own residual rows, or bias) into unit_s.
+// Every load of a round is issued before any is used: each is an L2 round trip.
+// Out of line: its word pairs in flight would otherwise push the inlined token
+// loop past the register budget (spills go to L2, since shared memory takes
+// nearly all of L1).
+template <int NP>  // (value, tag) word pairs per thread: K <= 2 * NP * kNT
+__device__ __noinline__ void load_input_n(const MegaArgs& a, Smem& S, const uint64_t* v,
+                                          uint32_t tag, int K, const uint16_t* g, bool from_embed,
+                                          int tok, const uint64_t* unit_own,
+                                          const uint16_t* unit_bf16, int n_unit, bool& abort) {
   constexpr int NT = kConsumers * 32;
-  constexpr int NV = (kMaxC * 256) / (4 * NT);  // float4 per thread
   const int tid = threadIdx.x;
-  float4 xv[NV];
   float uv = 0.f;
+  if (tid < n_unit)
+    uv = unit_own ? word_value(__ldcg(unit_own + tid)) : (unit_bf16 ? bf16f(unit_bf16[tid]) : 0.f);
+  // the norm gain (bf16), one pair per word pair, in the same batch of loads
+  uint32_t gv[NP];
+  if (g != nullptr) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int idx = tid + i * NT;
+      gv[i] = idx * 2 < K ? *reinterpret_cast<const uint32_t*>(g + idx * 2) : 0u;
+    }
+  }
+  float ss = 0.f;
   if (from_embed) {
     const uint4* e = reinterpret_cast<const uint4*>(a.embed + (size_t)tok * K);
-    uint4 w[(NV + 1) / 2];
+    constexpr int NE = (NP + 3) / 4;
+    uint4 w[NE];
 #pragma unroll
-    for (int i = 0; i < (NV + 1) / 2; ++i) {
+    for (int i = 0; i < NE; ++i) {
       const int idx = tid + i * NT;
       w[i] = idx * 8 < K ? e[idx] : make_uint4(0, 0, 0, 0);
     }
+    csync();  // the previous phase's readers of xs / unit_s are done
 #pragma unroll
-    for (int i = 0; i < (NV + 1) / 2; ++i) {
+    for (int i = 0; i < NE; ++i) {
       const int idx = tid + i * NT;
       if (idx * 8 < K) {
         const uint32_t q[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
@@ -229,30 +290,31 @@ __device__ void load_input(const MegaArgs& a, Smem& S, const float* v, int K, co
       }
     }
   } else {
+    uint64_t w[NP][2];
+    unsigned pend = 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int idx = tid + i * NT;
-      xv[i] = idx * 4 < K ? __ldcg(reinterpret_cast<const float4*>(v) + idx)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < NP; ++i)
+      if ((tid + i * NT) * 2 < K) pend |= 1u << i;
+    uint64_t t0 = 0;
+    for (uint32_t n = 1; pend && !abort; ++n) {
+#pragma unroll
+      for (int i = 0; i < NP; ++i)
+        if ((pend >> i) & 1u) ld_words2(v + 2 * (tid + i * NT), w[i][0], w[i][1]);
+#pragma unroll
+      for (int i = 0; i < NP; ++i)
+        if (((pend >> i) & 1u) && word_tag(w[i][0]) == tag && word_tag(w[i][1]) == tag)
+          pend &= ~(1u << i);
+      if (pend) poll_bound(a, n, t0, abort);
     }
-  }
-  if (tid < n_unit) uv = unit_f32 ? __ldcg(unit_f32 + tid) : (unit_bf16 ? bf16f(unit_bf16[tid]) : 0.f);
-  // the norm gain (bf16), 4 per float4 of input, in the same batch of loads
-  uint2 gv[NV];
-  if (g != nullptr) {
+    csync();  // the previous phase's readers of xs / unit_s are done
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
+    for (int i = 0; i < NP; ++i) {
       const int idx = tid + i * NT;
-      gv[i] = idx * 4 < K ? *reinterpret_cast<const uint2*>(g + idx * 4) : make_uint2(0, 0);
-    }
-  }
-  float ss = 0.f;
-  if (!from_embed) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int idx = tid + i * NT;
-      if (idx * 4 < K) *reinterpret_cast<float4*>(&S.xs[idx * 4]) = xv[i];
-      ss = fmaf(xv[i].x, xv[i].x, fmaf(xv[i].y, xv[i].y, fmaf(xv[i].z, xv[i].z, fmaf(xv[i].w, xv[i].w, ss))));
+      if (idx * 2 < K) {
+        const float x0 = word_value(w[i][0]), x1 = word_value(w[i][1]);
+        *reinterpret_cast<float2*>(&S.xs[idx * 2]) = make_float2(x0, x1);
+        ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+      }
     }
   }
   if (tid < n_unit) S.unit_s[tid] = uv;
@@ -270,19 +332,29 @@ __device__ void load_input(const MegaArgs& a, Smem& S, const float* v, int K, co
     for (int i = 0; i < kConsumers; ++i) tot += S.red[i];
     const float r = 1.0f / sqrtf(tot / (float)K + a.eps);
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
+    for (int i = 0; i < NP; ++i) {
       const int idx = tid + i * NT;
-      if (idx * 4 < K) {
-        float4 x4 = *reinterpret_cast<const float4*>(&S.xs[idx * 4]);
-        x4.x = x4.x * r * __uint_as_float(gv[i].x << 16);
-        x4.y = x4.y * r * __uint_as_float(gv[i].x & 0xffff0000u);
-        x4.z = x4.z * r * __uint_as_float(gv[i].y << 16);
-        x4.w = x4.w * r * __uint_as_float(gv[i].y & 0xffff0000u);
-        *reinterpret_cast<float4*>(&S.xs[idx * 4]) = x4;
+      if (idx * 2 < K) {
+        float2 x2 = *reinterpret_cast<const float2*>(&S.xs[idx * 2]);
+        x2.x = x2.x * r * __uint_as_float(gv[i] << 16);
+        x2.y = x2.y * r * __uint_as_float(gv[i] & 0xffff0000u);
+        *reinterpret_cast<float2*>(&S.xs[idx * 2]) = x2;
       }
     }
   }
-  csync();
+  abort = csync_or(abort);
+}
+
+__device__ __forceinline__ void load_input(const MegaArgs& a, Smem& S, const uint64_t* v,
+                                           uint32_t tag, int K, const uint16_t* g, bool from_embed,
+                                           int tok, const uint64_t* unit_own,
+                                           const uint16_t* unit_bf16, int n_unit, bool& abort) {
+  constexpr int NP_1K = (1024 + 2 * kNT - 1) / (2 * kNT);      // pairs per thread, K <= 1024
+  constexpr int NP_MAX = (kMaxC * 256 + 2 * kNT - 1) / (2 * kNT);
+  if (K <= 2 * NP_1K * kNT)
+    load_input_n<NP_1K>(a, S, v, tag, K, g, from_embed, tok, unit_own, unit_bf16, n_unit, abort);
+  else
+    load_input_n<NP_MAX>(a, S, v, tag, K, g, from_embed, tok, unit_own, unit_bf16, n_unit, abort);
 }
 
 template <int MAXC>
@@ -340,132 +412,106 @@ __device__ __forceinline__ void dot2(const uint8_t* w0, const uint8_t* w1, bool 
   s1 = warp_sum(a1);
 }
 
-struct GemvOut {
-  int epi;                 // EPI_STORE / EPI_RESIDUAL / EPI_SWIGLU / EPI_LOGITS
-  float* y;
-  const uint16_t* bias;    // STORE: bias (its values for this CTA's units are in unit_s)
-  float* cap;              // RESIDUAL: capture row base (already offset by pos * n)
-  float best_v;            // LOGITS: running best of this warp (lane 0)
-  int best_i;
+// LM head: this warp's running best logit (lane 0) and whether it saw a NaN.
+struct Best {
+  float v;
+  int i;
   int nan;
 };
 
-// Consume the chunks of one row-streamed phase; chunk counter c advances.
-template <int MAXC>
-__device__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, const Slice& sl,
-                           int K, int rpu, GemvOut& o, bool& abort) {
+// Consume the chunks of one row-streamed phase (units [u0, u1) of `unit_bytes`
+// each, `per_chunk` to a ring stage); chunk counter c advances by the phase's
+// chunks. Each instantiation is compiled on its own (no inlining into the token
+// loop), with the epilogue fixed at compile time:
+//   EPI_STORE    y[u] = w_u . xs (+ bias[u])                  (tagged words)
+//   EPI_RESIDUAL y[u] = y[u] + w_u . xs  (own rows; also to cap) (tagged words)
+//   EPI_SWIGLU   y[u] = silu(g_u . xs) * (up_u . xs)          (tagged words)
+//   EPI_LOGITS   logits[u] = w_u . xs, running greedy best    (plain f32)
+// When the phase fits in the ring every chunk is waited for once and each warp
+// takes its units across chunks; otherwise the chunks are taken one at a time.
+template <int MAXC, int EPI>
+__device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
+                                        const uint8_t* base, int u0, int u1, uint32_t unit_bytes,
+                                        int per_chunk, int K, uint64_t* ty, uint32_t tag,
+                                        const uint16_t* bias, float* cap, Best& best,
+                                        bool& abort) {
+  (void)base;
+  constexpr int XR = MAXC > 0 ? MAXC : 1;
+  constexpr int STEP = EPI == EPI_SWIGLU ? 1 : 2;  // units per warp iteration
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float xr[MAXC > 0 ? MAXC : 1][8];
-  if (MAXC > 0) x_regs<(MAXC > 0 ? MAXC : 1)>(S, K, xr);
-  const uint32_t row_bytes = sl.unit_bytes / rpu;
-  const int n_units = sl.u1 - sl.u0;
-  const int n_chunks = (n_units + sl.per_chunk - 1) / sl.per_chunk;
-  if (o.epi != EPI_LOGITS && n_chunks <= kNS) {
-    // The whole phase fits in the ring: wait for every chunk once, then give each
-    // warp its units across chunks (more independent rows per warp), then release all.
+  float xr[XR][8];
+  if (MAXC > 0) x_regs<XR>(S, K, xr);
+  const uint32_t row_bytes = EPI == EPI_SWIGLU ? unit_bytes / 2 : unit_bytes;
+  const int n_units = u1 - u0;
+  const int n_chunks = (n_units + per_chunk - 1) / per_chunk;
+  const int group = (EPI != EPI_LOGITS && n_chunks <= kNS) ? n_chunks : 1;
+  for (int g0 = 0; g0 < n_chunks && !abort; g0 += group) {
+    const int gn = min(group, n_chunks - g0);
     bool ok = true;
-    for (int j = 0; j < n_chunks; ++j)
-      ok &= ring_wait(a, &S.full[(c + j) % kNS], (uint32_t)(((c + j) / kNS) & 1), abort);
-    if (__any_sync(0xffffffffu, !ok)) {
-      abort = true;
-      c += n_chunks;
-      return;
+    for (int j = 0; j < gn; ++j) {
+      const int cc = c + g0 + j;
+      ok &= ring_wait(a, &S.full[cc % kNS], (uint32_t)((cc / kNS) & 1), abort);
     }
-    auto unit_ptr = [&](int i) {  // i-th unit of the slice, in its ring stage
-      const int j = i / sl.per_chunk;
-      return ring + (size_t)((c + j) % kNS) * kStage + (size_t)(i - j * sl.per_chunk) * sl.unit_bytes;
+    if (__any_sync(0xffffffffu, !ok)) {  // the whole warp gives up together
+      abort = true;
+      break;
+    }
+    auto unit_ptr = [&](int t) {  // t-th unit of the slice, in its ring stage
+      const int j = t / per_chunk;
+      return ring + (size_t)((c + j) % kNS) * kStage + (size_t)(t - j * per_chunk) * unit_bytes;
     };
-    if (rpu == 1) {
-      for (int t = 2 * warp; t < n_units; t += 2 * kConsumers) {
-        float v0, v1;
-        const bool two = t + 1 < n_units;
-        dot2<MAXC>(unit_ptr(t), two ? unit_ptr(t + 1) : unit_ptr(t), two, K, xr, S.xs, v0, v1);
-        if (lane == 0) {
+    const int ua = g0 * per_chunk, ub = min(n_units, (g0 + gn) * per_chunk);
+    for (int t = ua + STEP * warp; t < ub; t += STEP * kConsumers) {
+      float v0, v1;
+      if (EPI == EPI_SWIGLU) {
+        const uint8_t* w = unit_ptr(t);
+        dot2<MAXC>(w, w + row_bytes, true, K, xr, S.xs, v0, v1);
+        if (lane == 0) st_tagged(ty + u0 + t, v0 / (1.0f + expf(-v0)) * v1, tag);
+        continue;
+      }
+      const bool two = t + 1 < ub;
+      const uint8_t* w0 = unit_ptr(t);
+      dot2<MAXC>(w0, two ? unit_ptr(t + 1) : w0, two, K, xr, S.xs, v0, v1);
+      if (lane == 0) {
 #pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            if (jj == 1 && !two) break;
-            const int iu = t + jj, uu = sl.u0 + iu;
-            const float v = jj ? v1 : v0;
-            if (o.epi == EPI_STORE) {
-              o.y[uu] = v + (o.bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(o.bias[uu])) : 0.f);
-            } else {  // EPI_RESIDUAL
-              const float nv = (iu < kUnitPre ? S.unit_s[iu] : __ldcg(o.y + uu)) + v;
-              o.y[uu] = nv;
-              if (o.cap) o.cap[uu] = nv;
-            }
+        for (int jj = 0; jj < 2; ++jj) {
+          if (jj == 1 && !two) break;
+          const int iu = t + jj, uu = u0 + iu;
+          const float v = jj ? v1 : v0;
+          if (EPI == EPI_STORE) {
+            st_tagged(ty + uu, v + (bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(bias[uu])) : 0.f),
+                      tag);
+          } else if (EPI == EPI_RESIDUAL) {
+            const float nv = (iu < kUnitPre ? S.unit_s[iu] : word_value(__ldcg(ty + uu))) + v;
+            st_tagged(ty + uu, nv, tag);
+            if (cap) cap[uu] = nv;
+          } else {  // EPI_LOGITS
+            a.logits[uu] = v;
+            if (v != v) best.nan = 1;
+            else if (v > best.v) { best.v = v; best.i = uu; }
           }
         }
-      }
-    } else {
-      for (int t = warp; t < n_units; t += kConsumers) {
-        float g, up;
-        const uint8_t* w = unit_ptr(t);
-        dot2<MAXC>(w, w + row_bytes, true, K, xr, S.xs, g, up);
-        if (lane == 0) o.y[sl.u0 + t] = g / (1.0f + expf(-g)) * up;
       }
     }
     __syncwarp();
     if (lane == 0)
-      for (int j = 0; j < n_chunks; ++j) mbar_arrive(&S.empty[(c + j) % kNS]);
-    c += n_chunks;
-    return;
+      for (int j = 0; j < gn; ++j) mbar_arrive(&S.empty[(c + g0 + j) % kNS]);
   }
-  for (int u = sl.u0; u < sl.u1; u += sl.per_chunk, ++c) {
-    const int nu = min(sl.per_chunk, sl.u1 - u);
-    const int st = c % kNS;
-    const bool ok = ring_wait(a, &S.full[st], (uint32_t)((c / kNS) & 1), abort);
-    if (__any_sync(0xffffffffu, !ok)) {  // the whole warp gives up together
-      abort = true;
-      continue;
-    }
-    const uint8_t* base = ring + (size_t)st * kStage;
-    if (rpu == 1) {
-      for (int t = 2 * warp; t < nu; t += 2 * kConsumers) {
-        float v0, v1;
-        const bool two = t + 1 < nu;
-        dot2<MAXC>(base + (size_t)t * row_bytes, base + (size_t)(t + 1) * row_bytes, two, K, xr,
-                   S.xs, v0, v1);
-        if (lane == 0) {
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (j == 1 && !two) break;
-            const int uu = u + t + j;
-            const float v = j ? v1 : v0;
-            const int iu = uu - sl.u0;
-            if (o.epi == EPI_STORE) {
-              o.y[uu] = v + (o.bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(o.bias[uu])) : 0.f);
-            } else if (o.epi == EPI_RESIDUAL) {
-              const float nv = (iu < kUnitPre ? S.unit_s[iu] : __ldcg(o.y + uu)) + v;
-              o.y[uu] = nv;
-              if (o.cap) o.cap[uu] = nv;
-            } else {  // EPI_LOGITS
-              o.y[uu] = v;
-              if (v != v) o.nan = 1;
-              else if (v > o.best_v) { o.best_v = v; o.best_i = uu; }
-            }
-          }
-        }
-      }
-    } else {  // interleaved gate/up pairs
-      for (int t = warp; t < nu; t += kConsumers) {
-        float g, up;
-        dot2<MAXC>(base + (size_t)t * sl.unit_bytes, base + (size_t)t * sl.unit_bytes + row_bytes,
-                   true, K, xr, S.xs, g, up);
-        if (lane == 0) o.y[u + t] = g / (1.0f + expf(-g)) * up;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[st]);
-  }
+  c += n_chunks;
 }
 
-template <int MAXC_DUMMY = 0>
-__device__ void gemv_dispatch(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, const Slice& sl,
-                              int K, int rpu, GemvOut& o, bool& abort) {
-  // Inputs up to 1024 wide stay in registers; wider ones are read from shared
-  // memory inside the dot (keeps the kernel under its register budget, no spills).
-  if (K <= 1024) gemv_phase<4>(a, ring, S, c, sl, K, rpu, o, abort);
-  else gemv_phase<0>(a, ring, S, c, sl, K, rpu, o, abort);
+// Inputs up to 1024 wide stay in registers; wider ones are read from shared
+// memory inside the dot (keeps the kernel under its register budget).
+template <int EPI>
+__device__ __forceinline__ void gemv(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
+                                     const Slice& sl, int K, uint64_t* ty, uint32_t tag,
+                                     const uint16_t* bias, float* cap, Best& best, bool& abort) {
+  if (K <= 1024)
+    gemv_phase<4, EPI>(a, ring, S, c, sl.base, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty,
+                       tag, bias, cap, best, abort);
+  else
+    gemv_phase<0, EPI>(a, ring, S, c, sl.base, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty,
+                       tag, bias, cap, best, abort);
 }
 
 
@@ -474,9 +520,9 @@ __device__ void gemv_dispatch(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
 // softmax, then a partial (or the final output when there is one split); the
 // last CTA of a KV head to arrive combines the splits in split order.
 template <int HD>
-__device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l, int pos,
-                           const Split& sp, bool& abort) {
-  constexpr int EPL = HD / 32, OUTS = (kGQ * HD + 255) / 256;
+__device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l, int pos,
+                           const Split& sp, uint32_t tag_in, uint32_t tag_out, bool& abort) {
+  constexpr int EPL = HD / 32, OUTS = (kGQ * HD + kNT - 1) / kNT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int GQ = a.nq / a.nkv, g = sp.g;
   const LayerDev& Ld = a.layers[l];
@@ -493,11 +539,10 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
   for (int hh = warp; hh <= GQ; hh += kConsumers) {
     const bool isq = hh < GQ;
     if (!isq && !owns_pos) break;
-    const float* src = a.qkv + (size_t)(isq ? (g * GQ + hh) : (a.nq + g)) * HD;
+    const uint64_t* src = a.qkv + (size_t)(isq ? (g * GQ + hh) : (a.nq + g)) * HD;
     const uint16_t* gain = isq ? Ld.q_norm : Ld.k_norm;
     float v[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) v[e] = __ldcg(src + lane + 32 * e);
+    poll_row<EPL>(a, src, tag_in, v, abort);
     if (gain != nullptr) {
       float sq = 0.f;
 #pragma unroll
@@ -518,19 +563,19 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
 #pragma unroll
       for (int e = 0; e < EPL; ++e) S.q_s[hh * HD + lane + 32 * e] = v[e] * scale;
     } else {
-      const float* vsrc = a.qkv + (size_t)(a.nq + a.nkv + g) * HD;
+      float vv[EPL];
+      poll_row<EPL>(a, a.qkv + (size_t)(a.nq + a.nkv + g) * HD, tag_in, vv, abort);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
         const int d = lane + 32 * e;
         S.kn_s[d] = v[e];
         kc[(size_t)pos * HD + d] = v[e];
-        const float vv = __ldcg(vsrc + d);
-        S.vn_s[d] = vv;
-        vc[(size_t)pos * HD + d] = vv;
+        S.vn_s[d] = vv[e];
+        vc[(size_t)pos * HD + d] = vv[e];
       }
     }
   }
-  csync();
+  abort = csync_or(abort);
   float qr[kGQ][EPL];
 #pragma unroll
   for (int h = 0; h < kGQ; ++h)
@@ -553,6 +598,9 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
           Ks[(pos - t0) * HD + e] = S.kn_s[e];
           Vs[(pos - t0) * HD + e] = S.vn_s[e];
         }
+        // these generic writes into a ring stage must be ordered before the
+        // producer's next bulk copy into the same stage (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         csync();
       }
       for (int j = warp; j < nk; j += kConsumers) {
@@ -590,7 +638,7 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
       csync();
 #pragma unroll
       for (int oi = 0; oi < OUTS; ++oi) {
-        const int idx = tid + oi * 256;
+        const int idx = tid + oi * kNT;
         if (idx < GQ * HD) {
           const int h = idx / HD, d = idx % HD;
           float acc = oacc[oi] * S.al_s[h];
@@ -607,17 +655,17 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
   if (sp.nsplit == 1) {
 #pragma unroll
     for (int oi = 0; oi < OUTS; ++oi) {
-      const int idx = tid + oi * 256;
+      const int idx = tid + oi * kNT;
       if (idx < GQ * HD) {
         const int h = idx / HD, d = idx % HD;
-        a.attn_o[(size_t)(g * GQ + h) * HD + d] = oacc[oi] / S.ml_s[2 * h + 1];
+        st_tagged(a.attn_o + (size_t)(g * GQ + h) * HD + d, oacc[oi] / S.ml_s[2 * h + 1], tag_out);
       }
     }
     return;
   }
 #pragma unroll
   for (int oi = 0; oi < OUTS; ++oi) {
-    const int idx = tid + oi * 256;
+    const int idx = tid + oi * kNT;
     if (idx < GQ * HD) {
       const int h = idx / HD, d = idx % HD;
       a.part_o[((size_t)(g * GQ + h) * a.splits + sp.s) * HD + d] = oacc[oi];
@@ -631,7 +679,7 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
   __threadfence();
   csync();
   if (tid == 0) {
-    const int prev = atomicAdd(&a.attn_counters[g], 1);
+    const int prev = atomicAdd(&a.attn_counters[l * a.nkv + g], 1);
     S.flag = (prev == sp.nsplit - 1);
   }
   csync();
@@ -650,7 +698,7 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
   csync();
 #pragma unroll
   for (int oi = 0; oi < OUTS; ++oi) {
-    const int idx = tid + oi * 256;
+    const int idx = tid + oi * kNT;
     if (idx < GQ * HD) {
       const int h = idx / HD, d = idx % HD;
       const float* pm = S.pml_s + 2 * h * ns;
@@ -668,11 +716,11 @@ __device__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, in
         for (int j = 0; j < 8; ++j)
           if (s0 + j < ns) num = fmaf(expf(pm[2 * (s0 + j)] - M), pv[j], num);
       }
-      a.attn_o[(size_t)(g * GQ + h) * HD + d] = num / den;
+      st_tagged(a.attn_o + (size_t)(g * GQ + h) * HD + d, num / den, tag_out);
     }
   }
   csync();
-  if (tid == 0) a.attn_counters[g] = 0;
+  if (tid == 0) a.attn_counters[l * a.nkv + g] = 0;  // not used again in this launch
 }
 
 
@@ -722,12 +770,12 @@ __device__ void produce(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
 }
 
 // ---- greedy argmax across the grid (last CTA to arrive reduces in order)
-__device__ void argmax_finalize(const MegaArgs& a, Smem& S, GemvOut& o, int pos) {
+__device__ void argmax_finalize(const MegaArgs& a, Smem& S, const Best& o, int pos, uint32_t epoch) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, G = gridDim.x;
   if (lane == 0) {
-    S.red[warp] = o.nan ? __int_as_float(0x7fc00000) : o.best_v;
-    S.redi[warp] = o.best_i;
+    S.red[warp] = o.nan ? __int_as_float(0x7fc00000) : o.v;
+    S.redi[warp] = o.i;
   }
   csync();
   if (tid == 0) {
@@ -777,73 +825,82 @@ __device__ void argmax_finalize(const MegaArgs& a, Smem& S, GemvOut& o, int pos)
     a.am.status[0] = am;
     a.am.status[1] = *reinterpret_cast<volatile int*>(a.err);
     *a.am.counter = 0;
+    *a.epoch = epoch + 1u;  // every CTA read the epoch at its start
   }
 }
 
 // ---- consumers: the phases of one token
-__device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
+// Phase k of the token writes its output words with tag(k): per layer l, 5l+0
+// fused q/k/v, 5l+1 attention output, 5l+2 residual after o_proj, 5l+3 SwiGLU
+// output, 5l+4 residual after down.
+__device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint32_t epoch) {
   const int b = blockIdx.x, G = gridDim.x, tid = threadIdx.x;
-  const int nbar = 5 * a.L, qd = a.nq * a.hd;
+  const int qd = a.nq * a.hd;
+  const uint32_t tag0 = epoch * (uint32_t)(5 * a.L + 1) + 1u;
   bool abort = false;
-  int c = 0, k = 0;
+  int c = 0;
   int tok = a.tok >= 0 ? a.tok : __ldcg(a.next_token);
   if (tok < 0 || tok >= a.V) {
     if (tid == 0 && b == 0) atomicOr(a.err, ERR_TOKEN);
     tok = 0;
   }
   const Split sp = attn_split(a, pos, b);
+  Best best{-INFINITY, 0x7fffffff, 0};
   for (int l = 0; l < a.L; ++l) {
     const LayerDev Ld = a.layers[l];  // one batch of loads per layer, kept in registers
-    if (l > 0) grid_barrier(a, S, k++, nbar, abort);
+    const uint32_t tq = tag0 + 5u * l, ta = tq + 1u, to = tq + 2u, tg = tq + 3u, td = tq + 4u;
     // fused QKV; layer 0 gathers the embedding row itself and seeds the residual rows it owns
     const Slice qs = phase_slice(a, K_QKV, Ld, b, G);
-    load_input(a, S, a.x, a.H, Ld.attn_norm, l == 0, tok, nullptr,
-               Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr, min(qs.u1 - qs.u0, kUnitPre));
     if (l == 0) {
       const Slice os = phase_slice(a, K_O, Ld, b, G);
       const uint16_t* e = a.embed + (size_t)tok * a.H;
-      for (int r = os.u0 + tid; r < os.u1; r += kConsumers * 32) a.x[r] = bf16f(e[r]);
+      for (int r = os.u0 + tid; r < os.u1; r += kConsumers * 32) st_tagged(a.x + r, bf16f(e[r]), 0u);
       if (a.cap_emb && b == 0)
         for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_emb[(size_t)pos * a.H + r] = bf16f(e[r]);
     }
-    GemvOut o{EPI_STORE, a.qkv, Ld.qkv_bias, nullptr, -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, qs, a.H, 1, o, abort);
-    grid_barrier(a, S, k++, nbar, abort);
+    if (qs.u1 > qs.u0) {
+      load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
+                 Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr, min(qs.u1 - qs.u0, kUnitPre), abort);
+      gemv<EPI_STORE>(a, ring, S, c, qs, a.H, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
+    }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
-      if (a.hd == 64) attn_phase<64>(a, ring, S, c, l, pos, sp, abort);
-      else attn_phase<128>(a, ring, S, c, l, pos, sp, abort);
+      if (a.hd == 64) attn_phase<64>(a, ring, S, c, l, pos, sp, tq, ta, abort);
+      else attn_phase<128>(a, ring, S, c, l, pos, sp, tq, ta, abort);
     }
-    grid_barrier(a, S, k++, nbar, abort);
     // o_proj + residual
     const Slice os = phase_slice(a, K_O, Ld, b, G);
-    load_input(a, S, a.attn_o, qd, nullptr, false, 0, a.x + os.u0, nullptr,
-               min(os.u1 - os.u0, kUnitPre));
-    o = GemvOut{EPI_RESIDUAL, a.x, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, os, qd, 1, o, abort);
-    grid_barrier(a, S, k++, nbar, abort);
+    if (os.u1 > os.u0) {
+      load_input(a, S, a.attn_o, ta, qd, nullptr, false, 0, a.x + os.u0, nullptr,
+                 min(os.u1 - os.u0, kUnitPre), abort);
+      gemv<EPI_RESIDUAL>(a, ring, S, c, os, qd, a.x, to, nullptr, nullptr, best, abort);
+    }
     // gate/up with SwiGLU
-    load_input(a, S, a.x, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0);
-    o = GemvOut{EPI_SWIGLU, a.mlp, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, phase_slice(a, K_GU, Ld, b, G), a.H, 2, o, abort);
-    grid_barrier(a, S, k++, nbar, abort);
+    const Slice gs = phase_slice(a, K_GU, Ld, b, G);
+    if (gs.u1 > gs.u0) {
+      load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0, abort);
+      gemv<EPI_SWIGLU>(a, ring, S, c, gs, a.H, a.mlp, tg, nullptr, nullptr, best, abort);
+    }
     // down + residual (block-0 checkpoint)
     const Slice ds = phase_slice(a, K_DOWN, Ld, b, G);
-    load_input(a, S, a.mlp, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
-               min(ds.u1 - ds.u0, kUnitPre));
-    o = GemvOut{EPI_RESIDUAL, a.x, nullptr,
-                (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr,
-                -INFINITY, 0x7fffffff, 0};
-    gemv_dispatch(a, ring, S, c, ds, a.I, 1, o, abort);
+    if (ds.u1 > ds.u0) {
+      load_input(a, S, a.mlp, tg, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
+                 min(ds.u1 - ds.u0, kUnitPre), abort);
+      gemv<EPI_RESIDUAL>(a, ring, S, c, ds, a.I, a.x, td, nullptr,
+                         (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr, best,
+                         abort);
+    }
   }
-  grid_barrier(a, S, k++, nbar, abort);
   // final RMSNorm + LM head + greedy argmax
-  load_input(a, S, a.x, a.H, a.final_norm, false, 0, nullptr, nullptr, 0);
-  if (a.cap_final && b == 0)
-    for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[r];
-  GemvOut o{EPI_LOGITS, a.logits, nullptr, nullptr, -INFINITY, 0x7fffffff, 0};
-  gemv_dispatch(a, ring, S, c, phase_slice(a, K_LM, LayerDev{}, b, G), a.H, 1, o, abort);
-  argmax_finalize(a, S, o, pos);
+  const Slice ls = phase_slice(a, K_LM, LayerDev{}, b, G);
+  if (ls.u1 > ls.u0 || (a.cap_final && b == 0)) {
+    load_input(a, S, a.x, tag0 + 5u * (a.L - 1) + 4u, a.H, a.final_norm, false, 0, nullptr,
+               nullptr, 0, abort);
+    if (a.cap_final && b == 0)
+      for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[r];
+    gemv<EPI_LOGITS>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
+  }
+  argmax_finalize(a, S, best, pos, epoch);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs a) {
@@ -860,14 +917,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs
   __syncthreads();
   // The position changes only at the end of a token, so every thread reads it once.
   const int pos = __ldcg(a.pos);
-  if (threadIdx.x < kConsumers * 32) consume(a, ring, S, pos);
+  const uint32_t epoch = __ldcg(a.epoch);
+  if (threadIdx.x < kConsumers * 32) consume(a, ring, S, pos, epoch);
   else if (threadIdx.x == kConsumers * 32) produce(a, ring, S, pos);
 }
 
 }  // namespace
 
-bool mega_supported(int H, int I, int qd, int hd, int gq) {
+bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers) {
   return H <= kMaxC * 256 && I <= kMaxC * 256 && qd <= kMaxC * 256 && (hd == 64 || hd == 128) &&
+         H % 8 == 0 && I % 8 == 0 && qd % 8 == 0 && n_layers >= 1 &&
          gq >= 1 && gq <= kGQ && (uint32_t)H * 4 <= kStage && (uint32_t)I * 2 <= kStage &&
          (uint32_t)qd * 2 <= kStage;
 }

@@ -146,7 +146,12 @@ struct qw_handle {
   bool use_mega = false;
   bool mega_ok = false;
   LayerDev* d_layers = nullptr;
-  unsigned* bar_slots = nullptr;
+  // the persistent kernel's activations as tagged words, and its launch epoch
+  uint64_t* mx = nullptr;
+  uint64_t* mqkv = nullptr;
+  uint64_t* mattn = nullptr;
+  uint64_t* mmlp = nullptr;
+  uint32_t* d_epoch = nullptr;
   bool graph_dirty = true;
   uint64_t wait_ns = 1000000000ull;
   // host mirror
@@ -241,7 +246,7 @@ static int alloc_state(qw_handle* h) {
   h->nsplit_max = std::max(1, h->num_sms / c.n_kv_heads);
   h->mega_ok = c.weight_format == QW_WEIGHTS_BF16 &&
                mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim, c.head_dim,
-                              c.n_q_heads / c.n_kv_heads);
+                              c.n_q_heads / c.n_kv_heads, c.n_layers);
   h->use_mega = h->mega_ok;
   h->w4 = c.weight_format == QW_WEIGHTS_INT4_G128;
   h->lm_w4 = h->w4 && !c.tie_word_embeddings;
@@ -259,7 +264,7 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->rope, cap * (hd / 2) * sizeof(float2)},
       {(void**)&h->part_o, (size_t)c.n_q_heads * h->nsplit_max * hd * 4},
       {(void**)&h->part_ml, (size_t)c.n_q_heads * h->nsplit_max * 2 * 4},
-      {(void**)&h->attn_counters, nkv * 4},
+      {(void**)&h->attn_counters, L * nkv * 4},
       {(void**)&h->blk_val, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->blk_idx, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->am_counter, 4},
@@ -269,7 +274,11 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->d_err, 4},
       {(void**)&h->d_tokens_by_pos, cap * 4},
       {(void**)&h->d_status, 8},
-      {(void**)&h->bar_slots, (size_t)5 * L * 4},
+      {(void**)&h->mx, (size_t)c.hidden * 8},
+      {(void**)&h->mqkv, qkv_rows * 8},
+      {(void**)&h->mattn, (size_t)c.n_q_heads * hd * 8},
+      {(void**)&h->mmlp, (size_t)c.intermediate * 8},
+      {(void**)&h->d_epoch, 4},
       {(void**)&h->lora_t, 2 * 64 * 4},
   };
   const size_t Tm = (size_t)c.max_prefill_t, H = c.hidden, I = c.intermediate;
@@ -621,10 +630,11 @@ static MegaArgs mega_args(qw_handle* h) {
   m.v_cache = h->v_cache;
   m.cap = c.max_ctx;
   m.rope = h->rope;
-  m.x = h->x;
-  m.qkv = h->qkv;
-  m.attn_o = h->attn_o;
-  m.mlp = h->mlp;
+  m.x = h->mx;
+  m.qkv = h->mqkv;
+  m.attn_o = h->mattn;
+  m.mlp = h->mmlp;
+  m.epoch = h->d_epoch;
   m.logits = h->logits;
   m.part_o = h->part_o;
   m.part_ml = h->part_ml;
@@ -641,7 +651,6 @@ static MegaArgs mega_args(qw_handle* h) {
   m.pos = h->d_pos;
   m.tok = -1;
   m.next_token = h->d_next_token;
-  m.bar_slots = h->bar_slots;
   m.cap_emb = h->capture_on ? h->cap_emb : nullptr;
   m.cap_blk0 = h->capture_on ? h->cap_blk0 : nullptr;
   m.cap_final = h->capture_on ? h->cap_final : nullptr;
@@ -841,10 +850,10 @@ static int finish_sync(qw_handle* h) {
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   const int err = ((volatile int*)h->h_status)[1] | ((volatile int*)h->h_status)[3];
   if (err == 0) return QW_OK;
-  QW_CUDA(h, cudaMemsetAsync(h->bar_slots, 0, (size_t)5 * h->cfg.n_layers * 4, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->d_status, 0, 8, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->d_err, 0, 4, h->stream));
-  QW_CUDA(h, cudaMemsetAsync(h->attn_counters, 0, (size_t)h->cfg.n_kv_heads * 4, h->stream));
+  QW_CUDA(h, cudaMemsetAsync(h->attn_counters, 0,
+                             (size_t)h->cfg.n_layers * h->cfg.n_kv_heads * 4, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->am_counter, 0, 4, h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   if (err & ERR_TIMEOUT)

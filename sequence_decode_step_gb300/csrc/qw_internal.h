@@ -181,27 +181,28 @@ struct MegaArgs {
   float* v_cache;
   int cap;
   const float2* rope;
-  float* x;                // [H] residual
-  float* qkv;              // [(nq+2nkv) hd]
-  float* attn_o;           // [nq hd]
-  float* mlp;              // [I]
+  // activations as tagged words (f32 value low, phase tag high)
+  uint64_t* x;             // [H] residual
+  uint64_t* qkv;           // [(nq+2nkv) hd]
+  uint64_t* attn_o;        // [nq hd]
+  uint64_t* mlp;           // [I]
+  uint32_t* epoch;         // launches so far; tags are derived from it
   float* logits;           // [V]
   float* part_o;           // [nq][splits][hd]
   float* part_ml;          // [nq][splits][2]
-  int* attn_counters;      // [nkv]
+  int* attn_counters;      // [L][nkv]: one arrival counter per layer and KV head
   int splits;              // CTAs per KV head (gridDim.x / nkv)
   ArgmaxOut am;
   const int* pos;
   int tok;                 // host token (graph-node argument) or -1: use *next_token
   const int* next_token;
-  unsigned* bar_slots;     // [5 L] grid-barrier arrival counters
   float* cap_emb;          // capture rows or nullptr
   float* cap_blk0;
   float* cap_final;
   int* err;
   uint64_t wait_ns;
 };
-bool mega_supported(int H, int I, int qd, int hd, int gq);
+bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers);
 size_t mega_smem_bytes();
 cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);
 cudaError_t set_mega_attributes();

@@ -55,11 +55,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for phase `parity` of `bar` for at most limit_ns; limit 0 gives up at once.
 static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (limit_ns == 0) return false;
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  // %globaltimer is read only every 16th failed try (it costs far more than a
+  // try_wait); the bound starts counting at the first read.
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if ((n & 15u) != 0) continue;
+    const uint64_t now = globaltimer_ns();
+    if (t0 == 0) t0 = now;
+    else if (now - t0 > limit_ns) return false;
   }
 }
 
