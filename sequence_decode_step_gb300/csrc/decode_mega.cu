@@ -50,7 +50,8 @@ constexpr uint32_t kStage = 32 * 1024;       // bytes per stage
 constexpr int kMaxC = 12;                    // input vectors up to 12 x 256 = 3072 wide
 constexpr int kTK = 32;                      // keys per attention tile (K + V = 32 KB at hd 128)
 constexpr int kGQ = 8;
-constexpr int kMinKeys = 64;
+constexpr int kMinKeys = 128;               // keys per split at least (one pass)
+constexpr int kPass = 4;                     // tiles per attention pass
 constexpr int kUnitPre = 64;                 // units of a phase whose epilogue values are prefetched
 
 enum Kind { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GU = 3, K_DOWN = 4, K_LM = 5 };
@@ -67,12 +68,11 @@ struct Smem {
   float q_s[kGQ * 128];
   float kn_s[128];
   float vn_s[128];
-  float sc_s[kGQ * kTK];
-  float p_s[kGQ * kTK];
   float ml_s[2 * kGQ];
   float al_s[kGQ];
   float unit_s[kUnitPre];        // per-unit values the epilogue needs (residual rows or bias)
-  float pml_s[2 * kGQ * 160];    // split partials (m, l) for the combine
+  float pml_s[2 * kGQ * 160];    // split partials (m, l) for the combine; before it, the
+                                 // scores and probabilities of an attention pass
 };
 
 // The contiguous slice of a row-streamed phase owned by CTA b: units [u0, u1),
@@ -576,81 +576,139 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     }
   }
   abort = csync_or(abort);
-  float qr[kGQ][EPL];
-#pragma unroll
-  for (int h = 0; h < kGQ; ++h)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) qr[h][e] = (h < GQ) ? S.q_s[h * HD + lane * EPL + e] : 0.f;
   float oacc[OUTS];
 #pragma unroll
   for (int i = 0; i < OUTS; ++i) oacc[i] = 0.f;
-
-  for (int t0 = sp.k0; t0 < sp.k1; t0 += kTK, ++c) {
-    const int st = c % kNS;
-    const int nk = min(kTK, sp.k1 - t0);
-    ring_wait(a, &S.full[st], (uint32_t)((c / kNS) & 1), abort);
+  // Keys in passes of up to `pt` tiles, all resident in the ring at once: scores
+  // of every (key, head), one online-softmax update per head, P.V per (tile,
+  // head), then the per-tile partial outputs folded in tile order. Scratch: the
+  // scores and probabilities live in pml_s (free until the combine), the P.V
+  // partials in xs (free during attention).
+  constexpr int DPL = HD / 32;  // output dims per lane in P.V
+  const int pt = min(kPass, (kMaxC * 256) / (GQ * HD));
+  float* sc = S.pml_s;                      // [GQ][pt * kTK]
+  float* pp = S.pml_s + kGQ * kPass * kTK;  // [GQ][pt * kTK]
+  float* part = S.xs;                       // [pt][GQ][HD]
+  const int stride = pt * kTK;
+  for (int p0 = sp.k0; p0 < sp.k1; p0 += stride) {
+    const int nkp = min(stride, sp.k1 - p0);
+    const int nt = (nkp + kTK - 1) / kTK;
+    for (int t = 0; t < nt; ++t)
+      ring_wait(a, &S.full[(c + t) % kNS], (uint32_t)(((c + t) / kNS) & 1), abort);
     abort = csync_or(abort);
-    float* Ks = reinterpret_cast<float*>(ring + (size_t)st * kStage);
-    float* Vs = Ks + kTK * HD;
+    auto kt = [&](int t) { return reinterpret_cast<float*>(ring + (size_t)((c + t) % kNS) * kStage); };
     if (!abort) {
-      if (owns_pos && pos >= t0 && pos < t0 + nk) {
-        for (int e = tid; e < HD; e += kConsumers * 32) {
-          Ks[(pos - t0) * HD + e] = S.kn_s[e];
-          Vs[(pos - t0) * HD + e] = S.vn_s[e];
+      if (owns_pos && pos >= p0 && pos < p0 + nkp) {
+        float* Kp = kt((pos - p0) / kTK) + ((pos - p0) % kTK) * HD;
+        for (int e = tid; e < HD; e += kNT) {
+          Kp[e] = S.kn_s[e];
+          Kp[kTK * HD + e] = S.vn_s[e];
         }
         // these generic writes into a ring stage must be ordered before the
         // producer's next bulk copy into the same stage (async proxy)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         csync();
       }
-      for (int j = warp; j < nk; j += kConsumers) {
-        float kv[EPL];
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) kv[e] = Ks[j * HD + lane * EPL + e];
-#pragma unroll
-        for (int h = 0; h < kGQ; ++h) {
-          if (h < GQ) {
-            float p = 0.f;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) p = fmaf(qr[h][e], kv[e], p);
-            p = warp_sum(p);
-            if (lane == 0) S.sc_s[h * kTK + j] = p;
+      // scores: lane j takes key j of a tile; it walks the head dimension from a
+      // lane-rotated start, so the 32 lanes hit 32 different banks
+      for (int task = warp; task < nt * GQ; task += kConsumers) {
+        const int t = task / GQ, h = task % GQ;
+        const int j = t * kTK + lane;
+        float s = -INFINITY;
+        if (j < nkp) {
+          const float* kr = kt(t) + lane * HD;
+          const float* qh = S.q_s + h * HD;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 8
+          for (int d = 0; d < HD; d += 4) {
+            const int d0 = (d + lane) & (HD - 1), d1 = (d + 1 + lane) & (HD - 1);
+            const int d2 = (d + 2 + lane) & (HD - 1), d3 = (d + 3 + lane) & (HD - 1);
+            s0 = fmaf(qh[d0], kr[d0], s0);
+            s1 = fmaf(qh[d1], kr[d1], s1);
+            s2 = fmaf(qh[d2], kr[d2], s2);
+            s3 = fmaf(qh[d3], kr[d3], s3);
           }
+          s = (s0 + s1) + (s2 + s3);
         }
+        sc[h * stride + j] = s;
       }
       csync();
+      // online softmax, one warp per head
       for (int h = warp; h < GQ; h += kConsumers) {
-        const float sc = lane < nk ? S.sc_s[h * kTK + lane] : -INFINITY;
-        const float tmax = warp_max(sc);
+        float sv[kPass];
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kPass; ++i) {
+          const int k = lane + 32 * i;
+          sv[i] = k < nkp ? sc[h * stride + k] : -INFINITY;
+          m = fmaxf(m, sv[i]);
+        }
         const float m_old = S.ml_s[2 * h], l_old = S.ml_s[2 * h + 1];
-        const float m_new = fmaxf(m_old, tmax);
-        const float p = lane < nk ? expf(sc - m_new) : 0.f;
-        const float psum = warp_sum(p);
+        const float m_new = fmaxf(m_old, warp_max(m));
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPass; ++i) {
+          const int k = lane + 32 * i;
+          if (k < nt * kTK) {
+            const float e = k < nkp ? expf(sv[i] - m_new) : 0.f;
+            pp[h * stride + k] = e;
+            ps += e;
+          }
+        }
+        ps = warp_sum(ps);
         const float alpha = expf(m_old - m_new);
-        S.p_s[h * kTK + lane] = p;
-        __syncwarp();
         if (lane == 0) {
           S.ml_s[2 * h] = m_new;
-          S.ml_s[2 * h + 1] = l_old * alpha + psum;
+          S.ml_s[2 * h + 1] = l_old * alpha + ps;
           S.al_s[h] = alpha;
         }
       }
       csync();
+      // P.V of one (tile, head): lane holds DPL adjacent output dims
+      for (int task = warp; task < nt * GQ; task += kConsumers) {
+        const int t = task / GQ, h = task % GQ;
+        const int nk = min(kTK, nkp - t * kTK);
+        const float* Vt = kt(t) + kTK * HD + lane * DPL;
+        const float* pr = pp + h * stride + t * kTK;
+        float acc[DPL];
 #pragma unroll
-      for (int oi = 0; oi < OUTS; ++oi) {
-        const int idx = tid + oi * kNT;
-        if (idx < GQ * HD) {
-          const int h = idx / HD, d = idx % HD;
-          float acc = oacc[oi] * S.al_s[h];
-          const float* pr = S.p_s + h * kTK;
-          for (int j = 0; j < nk; ++j) acc = fmaf(pr[j], Vs[j * HD + d], acc);
-          oacc[oi] = acc;
+        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+        for (int j = 0; j < nk; ++j) {
+          const float pj = pr[j];
+          if constexpr (DPL == 4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(Vt + j * HD);
+            acc[0] = fmaf(pj, v4.x, acc[0]);
+            acc[1] = fmaf(pj, v4.y, acc[1]);
+            acc[2] = fmaf(pj, v4.z, acc[2]);
+            acc[3] = fmaf(pj, v4.w, acc[3]);
+          } else {
+            const float2 v2 = *reinterpret_cast<const float2*>(Vt + j * HD);
+            acc[0] = fmaf(pj, v2.x, acc[0]);
+            acc[1] = fmaf(pj, v2.y, acc[1]);
+          }
         }
+        float* dst = part + (t * GQ + h) * HD + lane * DPL;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) dst[i] = acc[i];
       }
     }
     csync();
-    if (lane == 0) mbar_arrive(&S.empty[st]);
+    if (lane == 0)
+      for (int t = 0; t < nt; ++t) mbar_arrive(&S.empty[(c + t) % kNS]);
+    c += nt;
+    // fold the pass into the running outputs, tiles in order
+#pragma unroll
+    for (int oi = 0; oi < OUTS; ++oi) {
+      const int idx = tid + oi * kNT;
+      if (idx < GQ * HD && !abort) {
+        const int h = idx / HD, d = idx % HD;
+        float acc = oacc[oi] * S.al_s[h];
+        for (int t = 0; t < nt; ++t) acc += part[(t * GQ + h) * HD + d];
+        oacc[oi] = acc;
+      }
+    }
   }
+  csync();
 
   if (sp.nsplit == 1) {
 #pragma unroll
@@ -932,6 +990,7 @@ bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers) {
 }
 
 static_assert(offsetof(Smem, xs) % 16 == 0, "float4 stores into xs need 16-byte alignment");
+static_assert(2 * kGQ * kPass * kTK <= 2 * kGQ * 160, "an attention pass's scores fit in pml_s");
 size_t mega_smem_bytes() { return (size_t)kNS * kStage + sizeof(Smem); }
 
 cudaError_t set_mega_attributes() {
