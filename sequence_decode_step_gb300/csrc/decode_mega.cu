@@ -501,19 +501,20 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
 }
 
 // Inputs up to 1024 wide stay in registers; wider ones are read from shared
-// memory inside the dot (keeps the kernel under its register budget).
-template <int EPI>
+// memory inside the dot (keeps the kernel under its register budget). X is the
+// kernel's compile-time knowledge of the width: 1 at most 1024, 0 wider, 2 decided
+// at run time (both bodies compiled in).
+template <int EPI, int X>
 __device__ __forceinline__ void gemv(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
                                      const Slice& sl, int K, uint64_t* ty, uint32_t tag,
                                      const uint16_t* bias, float* cap, Best& best, bool& abort) {
-  if (K <= 1024)
+  if (X == 1 || (X == 2 && K <= 1024))
     gemv_phase<4, EPI>(a, ring, S, c, sl.base, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty,
                        tag, bias, cap, best, abort);
   else
     gemv_phase<0, EPI>(a, ring, S, c, sl.base, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty,
                        tag, bias, cap, best, abort);
 }
-
 
 // Split-K attention of CTA b: QK-norm + RoPE of its group's queries (and of the
 // new key when its split holds pos), tiles of 32 keys from the ring, online
@@ -891,6 +892,11 @@ __device__ void argmax_finalize(const MegaArgs& a, Smem& S, const Best& o, int p
 // Phase k of the token writes its output words with tag(k): per layer l, 5l+0
 // fused q/k/v, 5l+1 attention output, 5l+2 residual after o_proj, 5l+3 SwiGLU
 // output, 5l+4 residual after down.
+// HD: head dim (0: either, decided at run time); XH, XQ, XI: width classes of
+// the hidden, q and intermediate inputs (see gemv). Only the variants a shape
+// needs are compiled into its kernel: the token loop's code is large and every
+// unused variant inlined into it costs instruction-cache misses.
+template <int HD, int XH, int XQ, int XI>
 __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint32_t epoch) {
   const int b = blockIdx.x, G = gridDim.x, tid = threadIdx.x;
   const int qd = a.nq * a.hd;
@@ -919,11 +925,11 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     if (qs.u1 > qs.u0) {
       load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
                  Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr, min(qs.u1 - qs.u0, kUnitPre), abort);
-      gemv<EPI_STORE>(a, ring, S, c, qs, a.H, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
+      gemv<EPI_STORE, XH>(a, ring, S, c, qs, a.H, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
     }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
-      if (a.hd == 64) attn_phase<64>(a, ring, S, c, l, pos, sp, tq, ta, abort);
+      if (HD == 64 || (HD == 0 && a.hd == 64)) attn_phase<64>(a, ring, S, c, l, pos, sp, tq, ta, abort);
       else attn_phase<128>(a, ring, S, c, l, pos, sp, tq, ta, abort);
     }
     // o_proj + residual
@@ -931,20 +937,20 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     if (os.u1 > os.u0) {
       load_input(a, S, a.attn_o, ta, qd, nullptr, false, 0, a.x + os.u0, nullptr,
                  min(os.u1 - os.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL>(a, ring, S, c, os, qd, a.x, to, nullptr, nullptr, best, abort);
+      gemv<EPI_RESIDUAL, XQ>(a, ring, S, c, os, qd, a.x, to, nullptr, nullptr, best, abort);
     }
     // gate/up with SwiGLU
     const Slice gs = phase_slice(a, K_GU, Ld, b, G);
     if (gs.u1 > gs.u0) {
       load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0, abort);
-      gemv<EPI_SWIGLU>(a, ring, S, c, gs, a.H, a.mlp, tg, nullptr, nullptr, best, abort);
+      gemv<EPI_SWIGLU, XH>(a, ring, S, c, gs, a.H, a.mlp, tg, nullptr, nullptr, best, abort);
     }
     // down + residual (block-0 checkpoint)
     const Slice ds = phase_slice(a, K_DOWN, Ld, b, G);
     if (ds.u1 > ds.u0) {
       load_input(a, S, a.mlp, tg, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
                  min(ds.u1 - ds.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL>(a, ring, S, c, ds, a.I, a.x, td, nullptr,
+      gemv<EPI_RESIDUAL, XI>(a, ring, S, c, ds, a.I, a.x, td, nullptr,
                          (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr, best,
                          abort);
     }
@@ -956,11 +962,12 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
                nullptr, 0, abort);
     if (a.cap_final && b == 0)
       for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[r];
-    gemv<EPI_LOGITS>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
+    gemv<EPI_LOGITS, XH>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
   }
   argmax_finalize(a, S, best, pos, epoch);
 }
 
+template <int HD, int XH, int XQ, int XI>
 __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -976,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs
   // The position changes only at the end of a token, so every thread reads it once.
   const int pos = __ldcg(a.pos);
   const uint32_t epoch = __ldcg(a.epoch);
-  if (threadIdx.x < kConsumers * 32) consume(a, ring, S, pos, epoch);
+  if (threadIdx.x < kConsumers * 32) consume<HD, XH, XQ, XI>(a, ring, S, pos, epoch);
   else if (threadIdx.x == kConsumers * 32) produce(a, ring, S, pos);
 }
 
@@ -993,17 +1000,33 @@ static_assert(offsetof(Smem, xs) % 16 == 0, "float4 stores into xs need 16-byte 
 static_assert(2 * kGQ * kPass * kTK <= 2 * kGQ * 160, "an attention pass's scores fit in pml_s");
 size_t mega_smem_bytes() { return (size_t)kNS * kStage + sizeof(Smem); }
 
+// The kernel for a shape: the Qwen3-0.6B class (head dim 128, hidden <= 1024, q
+// and intermediate wider) gets its own instantiation; other shapes the generic one.
+static const void* mega_kernel_for(const MegaArgs& a) {
+  if (a.hd == 128 && a.H <= 1024 && a.nq * a.hd > 1024 && a.I > 1024)
+    return reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0>);
+  return reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2>);
+}
+
 cudaError_t set_mega_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(decode_mega_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)mega_smem_bytes());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_mega_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+  const void* fns[2] = {reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0>),
+                        reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2>)};
+  cudaError_t e = cudaSuccess;
+  for (const void* f : fns) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)mega_smem_bytes());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+  }
   return e;
 }
 
-const void* mega_kernel_fn() { return reinterpret_cast<const void*>(decode_mega_kernel); }
+bool is_mega_kernel(const void* fn) {
+  return fn == reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0>) ||
+         fn == reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2>);
+}
 
 cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -1016,7 +1039,8 @@ cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_mega_kernel, a);
+  void* args[] = {const_cast<MegaArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, mega_kernel_for(a), args);
 }
 
 }  // namespace qw

@@ -822,7 +822,7 @@ static int ensure_graph_once(qw_handle* h) {
     if (kp.func == embed_kernel_fn()) {
       bytes = sizeof(EmbedArgs);
       off = offsetof(EmbedArgs, tok);
-    } else if (kp.func == mega_kernel_fn()) {
+    } else if (is_mega_kernel(kp.func)) {
       bytes = sizeof(MegaArgs);
       off = offsetof(MegaArgs, tok);
     } else {

@@ -206,6 +206,6 @@ bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers);
 size_t mega_smem_bytes();
 cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);
 cudaError_t set_mega_attributes();
-const void* mega_kernel_fn();
+bool is_mega_kernel(const void* fn);  // one of the persistent kernel instantiations
 
 }  // namespace qw
