@@ -240,6 +240,15 @@ __device__ __forceinline__ void poll_row(const MegaArgs& a, const uint64_t* src,
   for (int e = 0; e < N; ++e) v[e] = abort ? 0.f : word_value(w[e]);
 }
 
+// Position of input element k in xs: within each 256-wide chunk, the eight
+// elements 8l .. 8l+7 that lane l multiplies sit as two float4 at 4l and 128 + 4l,
+// so a warp reading one float4 per lane touches 512 contiguous bytes (no bank
+// conflicts); a plain layout (32-byte lane stride) costs twice the wavefronts.
+__device__ __forceinline__ int xs_pos(int k) {
+  const int c = k >> 8, r = k & 255, l = r >> 3, j = r & 7;
+  return (c << 8) + ((j & 4) << 5) + (l << 2) + (j & 3);
+}
+
 // Phase input: xs = v[0, K) once every word carries `tag` (or the embedding row
 // of `tok`), RMS-normalised with gain g when given; also prefetches `n_unit`
 // per-unit epilogue values (this CTA's own residual rows, or bias) into unit_s.
@@ -281,12 +290,13 @@ __device__ __noinline__ void load_input_n(const MegaArgs& a, Smem& S, const uint
     for (int i = 0; i < NE; ++i) {
       const int idx = tid + i * NT;
       if (idx * 8 < K) {
-        const uint32_t q[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          S.xs[idx * 8 + 2 * j] = __uint_as_float(q[j] << 16);
-          S.xs[idx * 8 + 2 * j + 1] = __uint_as_float(q[j] & 0xffff0000u);
-        }
+        float* d = &S.xs[(idx >> 5) * 256 + (idx & 31) * 4];
+        *reinterpret_cast<float4*>(d) =
+            make_float4(__uint_as_float(w[i].x << 16), __uint_as_float(w[i].x & 0xffff0000u),
+                        __uint_as_float(w[i].y << 16), __uint_as_float(w[i].y & 0xffff0000u));
+        *reinterpret_cast<float4*>(d + 128) =
+            make_float4(__uint_as_float(w[i].z << 16), __uint_as_float(w[i].z & 0xffff0000u),
+                        __uint_as_float(w[i].w << 16), __uint_as_float(w[i].w & 0xffff0000u));
       }
     }
   } else {
@@ -312,7 +322,7 @@ __device__ __noinline__ void load_input_n(const MegaArgs& a, Smem& S, const uint
       const int idx = tid + i * NT;
       if (idx * 2 < K) {
         const float x0 = word_value(w[i][0]), x1 = word_value(w[i][1]);
-        *reinterpret_cast<float2*>(&S.xs[idx * 2]) = make_float2(x0, x1);
+        *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = make_float2(x0, x1);
         ss = fmaf(x0, x0, fmaf(x1, x1, ss));
       }
     }
@@ -321,7 +331,10 @@ __device__ __noinline__ void load_input_n(const MegaArgs& a, Smem& S, const uint
   if (g != nullptr) {
     if (from_embed) {
       csync();
-      for (int k = tid; k < K; k += NT) ss = fmaf(S.xs[k], S.xs[k], ss);
+      for (int k = tid; k < K; k += NT) {
+        const float xk = S.xs[xs_pos(k)];
+        ss = fmaf(xk, xk, ss);
+      }
     }
     ss = warp_sum(ss);
     csync();
@@ -335,10 +348,10 @@ __device__ __noinline__ void load_input_n(const MegaArgs& a, Smem& S, const uint
     for (int i = 0; i < NP; ++i) {
       const int idx = tid + i * NT;
       if (idx * 2 < K) {
-        float2 x2 = *reinterpret_cast<const float2*>(&S.xs[idx * 2]);
+        float2 x2 = *reinterpret_cast<const float2*>(&S.xs[xs_pos(idx * 2)]);
         x2.x = x2.x * r * __uint_as_float(gv[i] << 16);
         x2.y = x2.y * r * __uint_as_float(gv[i] & 0xffff0000u);
-        *reinterpret_cast<float2*>(&S.xs[idx * 2]) = x2;
+        *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = x2;
       }
     }
   }
@@ -365,130 +378,196 @@ __device__ __forceinline__ void x_regs(const Smem& S, int K, float (&xr)[MAXC][8
     const int col = c * 256 + lane * 8;
     float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
     if (col < K) {
-      lo = *reinterpret_cast<const float4*>(&S.xs[col]);
-      hi = *reinterpret_cast<const float4*>(&S.xs[col + 4]);
+      lo = *reinterpret_cast<const float4*>(&S.xs[c * 256 + lane * 4]);
+      hi = *reinterpret_cast<const float4*>(&S.xs[c * 256 + 128 + lane * 4]);
     }
     xr[c][0] = lo.x; xr[c][1] = lo.y; xr[c][2] = lo.z; xr[c][3] = lo.w;
     xr[c][4] = hi.x; xr[c][5] = hi.y; xr[c][6] = hi.z; xr[c][7] = hi.w;
   }
 }
 
-// Dot products of two weight rows (bf16, in shared memory) with the register-held input.
-template <int MAXC>
-__device__ __forceinline__ void dot2(const uint8_t* w0, const uint8_t* w1, bool two, int K,
+// Per-lane partial dots of NR weight rows (bf16, in shared memory) with the input:
+// the input either held in registers (MAXC chunks of 256) or read from xs.
+template <int NR, int MAXC>
+__device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
                                      const float (&xr)[MAXC > 0 ? MAXC : 1][8], const float* xs,
-                                     float& s0, float& s1) {
+                                     float (&out)[NR]) {
   const int lane = threadIdx.x & 31;
-  float a0 = 0.f, a1 = 0.f;
-  if (MAXC > 0) {
-    // one accumulator per 256-column chunk: independent FMA chains, summed in order
-    float p0[MAXC > 0 ? MAXC : 1], p1[MAXC > 0 ? MAXC : 1];
+  if constexpr (MAXC > 0) {
+    // one FMA chain per (row, chunk), summed over chunks in order
+    float p[NR][MAXC];
 #pragma unroll
-    for (int c = 0; c < (MAXC > 0 ? MAXC : 1); ++c) {
+    for (int c = 0; c < MAXC; ++c) {
       const int col = c * 256 + lane * 8;
-      p0[c] = 0.f;
-      p1[c] = 0.f;
-      if (col < K) {
-        p0[c] = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[c], 0.f);
-        if (two) p1[c] = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xr[c], 0.f);
-      }
+      uint4 wv[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        wv[r] = col < K ? *reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2)
+                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) p[r][c] = dot8(wv[r], xr[c], 0.f);
     }
 #pragma unroll
-    for (int c = 0; c < (MAXC > 0 ? MAXC : 1); ++c) {
-      a0 += p0[c];
-      a1 += p1[c];
+    for (int r = 0; r < NR; ++r) {
+      float t = 0.f;
+#pragma unroll
+      for (int c = 0; c < MAXC; ++c) t += p[r][c];
+      out[r] = t;
     }
   } else {
-#pragma unroll 4
-    for (int col = lane * 8; col < K; col += 256) {
-      const float4 lo = *reinterpret_cast<const float4*>(xs + col);
-      const float4 hi = *reinterpret_cast<const float4*>(xs + col + 4);
-      const float xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-      a0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xv, a0);
-      if (two) a1 = dot8(*reinterpret_cast<const uint4*>(w1 + (size_t)col * 2), xv, a1);
+    // two chains per row (even and odd chunks), added at the end
+    float a0[NR], a1[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) a0[r] = a1[r] = 0.f;
+    const float* xl = xs + lane * 4;
+    int col = lane * 8, cb = 0;
+#pragma unroll 1
+    for (; col + 256 < K; col += 512, cb += 512) {
+      const float4 l0 = *reinterpret_cast<const float4*>(xl + cb);
+      const float4 h0 = *reinterpret_cast<const float4*>(xl + cb + 128);
+      const float4 l1 = *reinterpret_cast<const float4*>(xl + cb + 256);
+      const float4 h1 = *reinterpret_cast<const float4*>(xl + cb + 384);
+      const float x0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
+      const float x1[8] = {l1.x, l1.y, l1.z, l1.w, h1.x, h1.y, h1.z, h1.w};
+      uint4 wa[NR], wb[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        wa[r] = *reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2);
+        wb[r] = *reinterpret_cast<const uint4*>(w[r] + (size_t)(col + 256) * 2);
+      }
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        a0[r] = dot8(wa[r], x0, a0[r]);
+        a1[r] = dot8(wb[r], x1, a1[r]);
+      }
     }
+    if (col < K) {
+      const float4 l0 = *reinterpret_cast<const float4*>(xl + cb);
+      const float4 h0 = *reinterpret_cast<const float4*>(xl + cb + 128);
+      const float x0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        a0[r] = dot8(*reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2), x0, a0[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) out[r] = a0[r] + a1[r];
   }
-  s0 = warp_sum(a0);
-  s1 = warp_sum(a1);
 }
 
-// LM head: this warp's running best logit (lane 0) and whether it saw a NaN.
+// Sum NR (a power of two) per-lane partials over the warp with a transposing
+// butterfly: each halving step exchanges half of the remaining values, so NR rows
+// cost NR - 1 + 5 - log2(NR) shuffles instead of 5 NR. Afterwards lanes
+// [r * 32/NR, (r + 1) * 32/NR) hold the full sum of row r. Fixed order.
+template <int NR>
+__device__ __forceinline__ float rows_reduce(const float (&v)[NR], int lane) {
+  float cur[NR];
+#pragma unroll
+  for (int i = 0; i < NR; ++i) cur[i] = v[i];
+#pragma unroll
+  for (int s = 0, n = NR, bit = 16; s < 5; ++s, bit >>= 1) {
+    if (n > 1) {
+      const bool up = lane & bit;
+      const int h = n / 2;
+#pragma unroll
+      for (int i = 0; i < (NR > 1 ? NR / 2 : 1); ++i) {
+        if (i < h) {
+          const float keep = up ? cur[i + h] : cur[i], send = up ? cur[i] : cur[i + h];
+          cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+      }
+      n = h;
+    } else {
+      cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], bit);
+    }
+  }
+  return cur[0];
+}
+
+// LM head: each lane's running best logit and whether it saw a NaN (merged over
+// the warp at the end of the phase).
 struct Best {
   float v;
   int i;
   int nan;
 };
 
+// Wait for the n chunks starting at chunk c (all of a phase that fits in the
+// ring); done before the phase's input poll, so it stays off the critical path.
+__device__ __forceinline__ void prewait(const MegaArgs& a, Smem& S, int c, int n, bool& abort) {
+  if (n > kNS) return;
+  for (int j = 0; j < n; ++j) ring_wait(a, &S.full[(c + j) % kNS], (uint32_t)(((c + j) / kNS) & 1), abort);
+}
+
 // Consume the chunks of one row-streamed phase (units [u0, u1) of `unit_bytes`
 // each, `per_chunk` to a ring stage); chunk counter c advances by the phase's
-// chunks. Each instantiation is compiled on its own (no inlining into the token
-// loop), with the epilogue fixed at compile time:
-//   EPI_STORE    y[u] = w_u . xs (+ bias[u])                  (tagged words)
-//   EPI_RESIDUAL y[u] = y[u] + w_u . xs  (own rows; also to cap) (tagged words)
-//   EPI_SWIGLU   y[u] = silu(g_u . xs) * (up_u . xs)          (tagged words)
-//   EPI_LOGITS   logits[u] = w_u . xs, running greedy best    (plain f32)
-// When the phase fits in the ring every chunk is waited for once and each warp
-// takes its units across chunks; otherwise the chunks are taken one at a time.
-template <int MAXC, int EPI>
+// chunks. The epilogue, fixed at compile time:
+//   EPI_STORE    y[u] = w_u . xs (+ bias[u])                     (tagged words)
+//   EPI_RESIDUAL y[u] = y[u] + w_u . xs  (own rows; also to cap)   (tagged words)
+//   EPI_SWIGLU   y[u] = silu(g_u . xs) * (up_u . xs)             (tagged words)
+//   EPI_LOGITS   logits[u] = w_u . xs, running greedy best       (plain f32)
+// A warp takes NR rows per iteration (NR / 2 gate/up units for SwiGLU). When the
+// phase fits in the ring its chunks were waited for by prewait() and the warps
+// take units across chunks; otherwise the chunks are taken one at a time.
+template <int MAXC, int EPI, int NR>
 __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
-                                        const uint8_t* base, int u0, int u1, uint32_t unit_bytes,
-                                        int per_chunk, int K, uint64_t* ty, uint32_t tag,
-                                        const uint16_t* bias, float* cap, Best& best,
-                                        bool& abort) {
-  (void)base;
+                                           int u0, int u1, uint32_t unit_bytes, int per_chunk,
+                                           int K, uint64_t* ty, uint32_t tag,
+                                           const uint16_t* bias, float* cap, Best& best,
+                                           bool& abort) {
   constexpr int XR = MAXC > 0 ? MAXC : 1;
-  constexpr int STEP = EPI == EPI_SWIGLU ? 1 : 2;  // units per warp iteration
+  constexpr int RPU = EPI == EPI_SWIGLU ? 2 : 1;  // rows per unit
+  constexpr int UPI = NR / RPU;                   // units per warp iteration
+  constexpr int SH = 32 / NR;                     // lanes per reduced row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float xr[XR][8];
   if (MAXC > 0) x_regs<XR>(S, K, xr);
-  const uint32_t row_bytes = EPI == EPI_SWIGLU ? unit_bytes / 2 : unit_bytes;
+  const uint32_t row_bytes = unit_bytes / RPU;
   const int n_units = u1 - u0;
   const int n_chunks = (n_units + per_chunk - 1) / per_chunk;
-  const int group = (EPI != EPI_LOGITS && n_chunks <= kNS) ? n_chunks : 1;
+  const bool whole = EPI != EPI_LOGITS && n_chunks <= kNS;  // waited for by prewait()
+  const int group = whole ? n_chunks : 1;
   for (int g0 = 0; g0 < n_chunks && !abort; g0 += group) {
     const int gn = min(group, n_chunks - g0);
-    bool ok = true;
-    for (int j = 0; j < gn; ++j) {
-      const int cc = c + g0 + j;
-      ok &= ring_wait(a, &S.full[cc % kNS], (uint32_t)((cc / kNS) & 1), abort);
-    }
-    if (__any_sync(0xffffffffu, !ok)) {  // the whole warp gives up together
-      abort = true;
-      break;
-    }
-    auto unit_ptr = [&](int t) {  // t-th unit of the slice, in its ring stage
-      const int j = t / per_chunk;
-      return ring + (size_t)((c + j) % kNS) * kStage + (size_t)(t - j * per_chunk) * unit_bytes;
-    };
-    const int ua = g0 * per_chunk, ub = min(n_units, (g0 + gn) * per_chunk);
-    for (int t = ua + STEP * warp; t < ub; t += STEP * kConsumers) {
-      float v0, v1;
-      if (EPI == EPI_SWIGLU) {
-        const uint8_t* w = unit_ptr(t);
-        dot2<MAXC>(w, w + row_bytes, true, K, xr, S.xs, v0, v1);
-        if (lane == 0) st_tagged(ty + u0 + t, v0 / (1.0f + expf(-v0)) * v1, tag);
-        continue;
+    if (!whole) {
+      const bool ok = ring_wait(a, &S.full[(c + g0) % kNS], (uint32_t)(((c + g0) / kNS) & 1), abort);
+      if (__any_sync(0xffffffffu, !ok)) {  // the whole warp gives up together
+        abort = true;
+        break;
       }
-      const bool two = t + 1 < ub;
-      const uint8_t* w0 = unit_ptr(t);
-      dot2<MAXC>(w0, two ? unit_ptr(t + 1) : w0, two, K, xr, S.xs, v0, v1);
-      if (lane == 0) {
+    }
+    const int ua = g0 * per_chunk, ub = min(n_units, (g0 + gn) * per_chunk);
+    for (int t = ua + UPI * warp; t < ub; t += UPI * kConsumers) {
+      const uint8_t* w[NR];
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          if (jj == 1 && !two) break;
-          const int iu = t + jj, uu = u0 + iu;
-          const float v = jj ? v1 : v0;
-          if (EPI == EPI_STORE) {
-            st_tagged(ty + uu, v + (bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(bias[uu])) : 0.f),
-                      tag);
-          } else if (EPI == EPI_RESIDUAL) {
-            const float nv = (iu < kUnitPre ? S.unit_s[iu] : word_value(__ldcg(ty + uu))) + v;
+      for (int r = 0; r < NR; ++r) {
+        const int tu = min(t + r / RPU, ub - 1);  // rows past the slice reuse its last row
+        const int j = tu / per_chunk;
+        w[r] = ring + (size_t)((c + j) % kNS) * kStage + (size_t)(tu - j * per_chunk) * unit_bytes +
+               (r % RPU) * row_bytes;
+      }
+      float v[NR];
+      dotn<NR, MAXC>(w, K, xr, S.xs, v);
+      const float sum = rows_reduce<NR>(v, lane);
+      if constexpr (EPI == EPI_SWIGLU) {
+        const float up = __shfl_down_sync(0xffffffffu, sum, SH);  // row 2k+1 onto row 2k
+        if (lane % (2 * SH) == 0) {
+          const int iu = t + lane / (2 * SH);
+          if (iu < ub) st_tagged(ty + u0 + iu, sum / (1.0f + expf(-sum)) * up, tag);
+        }
+      } else if (lane % SH == 0) {
+        const int iu = t + lane / SH, uu = u0 + iu;
+        if (iu < ub) {
+          if constexpr (EPI == EPI_STORE) {
+            st_tagged(ty + uu,
+                      sum + (bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(bias[uu])) : 0.f), tag);
+          } else if constexpr (EPI == EPI_RESIDUAL) {
+            const float nv = (iu < kUnitPre ? S.unit_s[iu] : word_value(__ldcg(ty + uu))) + sum;
             st_tagged(ty + uu, nv, tag);
             if (cap) cap[uu] = nv;
           } else {  // EPI_LOGITS
-            a.logits[uu] = v;
-            if (v != v) best.nan = 1;
-            else if (v > best.v) { best.v = v; best.i = uu; }
+            a.logits[uu] = sum;
+            if (sum != sum) best.nan = 1;
+            else if (sum > best.v) { best.v = sum; best.i = uu; }
           }
         }
       }
@@ -504,16 +583,21 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
 // memory inside the dot (keeps the kernel under its register budget). X is the
 // kernel's compile-time knowledge of the width: 1 at most 1024, 0 wider, 2 decided
 // at run time (both bodies compiled in).
-template <int EPI, int X>
+template <int EPI, int X, int NR>
 __device__ __forceinline__ void gemv(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
                                      const Slice& sl, int K, uint64_t* ty, uint32_t tag,
                                      const uint16_t* bias, float* cap, Best& best, bool& abort) {
   if (X == 1 || (X == 2 && K <= 1024))
-    gemv_phase<4, EPI>(a, ring, S, c, sl.base, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty,
-                       tag, bias, cap, best, abort);
+    gemv_phase<4, EPI, NR>(a, ring, S, c, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty, tag,
+                           bias, cap, best, abort);
   else
-    gemv_phase<0, EPI>(a, ring, S, c, sl.base, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty,
-                       tag, bias, cap, best, abort);
+    gemv_phase<0, EPI, NR>(a, ring, S, c, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty, tag,
+                           bias, cap, best, abort);
+}
+
+// Chunks of a slice (the producer streams them in this count).
+__device__ __forceinline__ int slice_chunks(const Slice& sl) {
+  return (sl.u1 - sl.u0 + sl.per_chunk - 1) / sl.per_chunk;
 }
 
 // Split-K attention of CTA b: QK-norm + RoPE of its group's queries (and of the
@@ -923,9 +1007,10 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
         for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_emb[(size_t)pos * a.H + r] = bf16f(e[r]);
     }
     if (qs.u1 > qs.u0) {
+      prewait(a, S, c, slice_chunks(qs), abort);
       load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
                  Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr, min(qs.u1 - qs.u0, kUnitPre), abort);
-      gemv<EPI_STORE, XH>(a, ring, S, c, qs, a.H, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
+      gemv<EPI_STORE, XH, 4>(a, ring, S, c, qs, a.H, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
     }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
@@ -935,22 +1020,25 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     // o_proj + residual
     const Slice os = phase_slice(a, K_O, Ld, b, G);
     if (os.u1 > os.u0) {
+      prewait(a, S, c, slice_chunks(os), abort);
       load_input(a, S, a.attn_o, ta, qd, nullptr, false, 0, a.x + os.u0, nullptr,
                  min(os.u1 - os.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XQ>(a, ring, S, c, os, qd, a.x, to, nullptr, nullptr, best, abort);
+      gemv<EPI_RESIDUAL, XQ, 2>(a, ring, S, c, os, qd, a.x, to, nullptr, nullptr, best, abort);
     }
     // gate/up with SwiGLU
     const Slice gs = phase_slice(a, K_GU, Ld, b, G);
     if (gs.u1 > gs.u0) {
+      prewait(a, S, c, slice_chunks(gs), abort);
       load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0, abort);
-      gemv<EPI_SWIGLU, XH>(a, ring, S, c, gs, a.H, a.mlp, tg, nullptr, nullptr, best, abort);
+      gemv<EPI_SWIGLU, XH, 8>(a, ring, S, c, gs, a.H, a.mlp, tg, nullptr, nullptr, best, abort);
     }
     // down + residual (block-0 checkpoint)
     const Slice ds = phase_slice(a, K_DOWN, Ld, b, G);
     if (ds.u1 > ds.u0) {
+      prewait(a, S, c, slice_chunks(ds), abort);
       load_input(a, S, a.mlp, tg, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
                  min(ds.u1 - ds.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XI>(a, ring, S, c, ds, a.I, a.x, td, nullptr,
+      gemv<EPI_RESIDUAL, XI, 2>(a, ring, S, c, ds, a.I, a.x, td, nullptr,
                          (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr, best,
                          abort);
     }
@@ -961,8 +1049,16 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     load_input(a, S, a.x, tag0 + 5u * (a.L - 1) + 4u, a.H, a.final_norm, false, 0, nullptr,
                nullptr, 0, abort);
     if (a.cap_final && b == 0)
-      for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[r];
-    gemv<EPI_LOGITS, XH>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
+      for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[xs_pos(r)];
+    gemv<EPI_LOGITS, XH, 2>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
+  }
+  // each lane holding rows kept its own best: merge them onto lane 0 (ties to the lower index)
+  best.nan = __any_sync(0xffffffffu, best.nan != 0) ? 1 : 0;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best.v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, best.i, off);
+    if (am_better(ov, oi, best.v, best.i)) { best.v = ov; best.i = oi; }
   }
   argmax_finalize(a, S, best, pos, epoch);
 }
