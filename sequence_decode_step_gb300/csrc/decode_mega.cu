@@ -148,6 +148,11 @@ __device__ __forceinline__ bool csync_or(bool v) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
+// One arrival standing for all consumer warps (after a consumer barrier).
+__device__ __forceinline__ void mbar_arrive_all(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(kConsumers)
+               : "memory");
+}
 __device__ __forceinline__ bool err_set(const MegaArgs& a) {
   return (*reinterpret_cast<volatile int*>(a.err) & ERR_TIMEOUT) != 0;
 }
@@ -605,12 +610,21 @@ __device__ __forceinline__ int slice_chunks(const Slice& sl) {
 // softmax, then a partial (or the final output when there is one split); the
 // last CTA of a KV head to arrive combines the splits in split order.
 template <int HD>
-__device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l, int pos,
-                           const Split& sp, uint32_t tag_in, uint32_t tag_out, bool& abort) {
+__device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l,
+                                           int pos, const Split& sp, const LayerDev& Ld,
+                                           uint32_t tag_in, uint32_t tag_out, bool& abort) {
   constexpr int EPL = HD / 32, OUTS = (kGQ * HD + kNT - 1) / kNT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int GQ = a.nq / a.nkv, g = sp.g;
-  const LayerDev& Ld = a.layers[l];
+  // keys in passes of up to `pt` tiles; the first pass's tiles are waited for now,
+  // before the q/k/v poll, so those waits overlap the hand-over from QKV
+  const int pt = min(kPass, (kMaxC * 256) / (GQ * HD));
+  const int stride = pt * kTK;
+  {
+    const int nt0 = (min(stride, sp.k1 - sp.k0) + kTK - 1) / kTK;
+    for (int t = 0; t < nt0; ++t)
+      ring_wait(a, &S.full[(c + t) % kNS], (uint32_t)(((c + t) / kNS) & 1), abort);
+  }
   const size_t kv_layer = (size_t)a.nkv * a.cap * HD;
   float* kc = a.k_cache + (size_t)l * kv_layer + (size_t)g * a.cap * HD;
   float* vc = a.v_cache + (size_t)l * kv_layer + (size_t)g * a.cap * HD;
@@ -664,22 +678,22 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
   float oacc[OUTS];
 #pragma unroll
   for (int i = 0; i < OUTS; ++i) oacc[i] = 0.f;
-  // Keys in passes of up to `pt` tiles, all resident in the ring at once: scores
-  // of every (key, head), one online-softmax update per head, P.V per (tile,
-  // head), then the per-tile partial outputs folded in tile order. Scratch: the
-  // scores and probabilities live in pml_s (free until the combine), the P.V
-  // partials in xs (free during attention).
-  constexpr int DPL = HD / 32;  // output dims per lane in P.V
-  const int pt = min(kPass, (kMaxC * 256) / (GQ * HD));
+  // Per pass: scores of every (key, head), one online-softmax update per head,
+  // P.V per tile, then the per-tile partial outputs folded in tile order. A warp
+  // takes a whole 32-key tile: lanes split the head dimension (DPL dims each), so
+  // K and V rows are read as 512 contiguous bytes, and a 32-way transposing
+  // reduction leaves key j's score on lane j. Scratch: scores and probabilities
+  // in pml_s (free until the combine), P.V partials in xs (free during attention).
+  constexpr int DPL = HD / 32;
   float* sc = S.pml_s;                      // [GQ][pt * kTK]
   float* pp = S.pml_s + kGQ * kPass * kTK;  // [GQ][pt * kTK]
   float* part = S.xs;                       // [pt][GQ][HD]
-  const int stride = pt * kTK;
   for (int p0 = sp.k0; p0 < sp.k1; p0 += stride) {
     const int nkp = min(stride, sp.k1 - p0);
     const int nt = (nkp + kTK - 1) / kTK;
-    for (int t = 0; t < nt; ++t)
-      ring_wait(a, &S.full[(c + t) % kNS], (uint32_t)(((c + t) / kNS) & 1), abort);
+    if (p0 != sp.k0)
+      for (int t = 0; t < nt; ++t)
+        ring_wait(a, &S.full[(c + t) % kNS], (uint32_t)(((c + t) / kNS) & 1), abort);
     abort = csync_or(abort);
     auto kt = [&](int t) { return reinterpret_cast<float*>(ring + (size_t)((c + t) % kNS) * kStage); };
     if (!abort) {
@@ -694,28 +708,50 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         csync();
       }
-      // scores: lane j takes key j of a tile; it walks the head dimension from a
-      // lane-rotated start, so the 32 lanes hit 32 different banks
-      for (int task = warp; task < nt * GQ; task += kConsumers) {
-        const int t = task / GQ, h = task % GQ;
-        const int j = t * kTK + lane;
-        float s = -INFINITY;
-        if (j < nkp) {
-          const float* kr = kt(t) + lane * HD;
-          const float* qh = S.q_s + h * HD;
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll 8
-          for (int d = 0; d < HD; d += 4) {
-            const int d0 = (d + lane) & (HD - 1), d1 = (d + 1 + lane) & (HD - 1);
-            const int d2 = (d + 2 + lane) & (HD - 1), d3 = (d + 3 + lane) & (HD - 1);
-            s0 = fmaf(qh[d0], kr[d0], s0);
-            s1 = fmaf(qh[d1], kr[d1], s1);
-            s2 = fmaf(qh[d2], kr[d2], s2);
-            s3 = fmaf(qh[d3], kr[d3], s3);
+      // scores, two heads and eight keys at a time: lane partials over its DPL dims,
+      // then a transposing reduction leaves key r of the group on lanes 4r .. 4r+3
+      for (int t = warp; t < nt; t += kConsumers) {
+        const float* Kt = kt(t) + lane * DPL;
+        const int nk = min(kTK, nkp - t * kTK);
+        for (int h0 = 0; h0 < GQ; h0 += 2) {
+          const bool two = h0 + 1 < GQ;
+          float q0[DPL], q1[DPL];
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) {
+            q0[e] = S.q_s[h0 * HD + lane * DPL + e];
+            q1[e] = two ? S.q_s[(h0 + 1) * HD + lane * DPL + e] : 0.f;
           }
-          s = (s0 + s1) + (s2 + s3);
+#pragma unroll 1
+          for (int j0 = 0; j0 < kTK; j0 += 8) {
+            float s0[8], s1[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float kv[DPL];
+              if constexpr (DPL == 4) {
+                const float4 k4 = *reinterpret_cast<const float4*>(Kt + (j0 + j) * HD);
+                kv[0] = k4.x; kv[1] = k4.y; kv[2 % DPL] = k4.z; kv[3 % DPL] = k4.w;
+              } else {
+                const float2 k2 = *reinterpret_cast<const float2*>(Kt + (j0 + j) * HD);
+                kv[0] = k2.x; kv[1] = k2.y;
+              }
+              float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+              for (int e = 0; e < DPL; ++e) {
+                a0 = fmaf(q0[e], kv[e], a0);
+                a1 = fmaf(q1[e], kv[e], a1);
+              }
+              s0[j] = a0;
+              s1[j] = a1;
+            }
+            const float r0 = rows_reduce<8>(s0, lane);
+            const float r1 = rows_reduce<8>(s1, lane);
+            if ((lane & 3) == 0) {
+              const int j = j0 + (lane >> 2);  // keys past the split hold stale rows
+              sc[h0 * stride + t * kTK + j] = j < nk ? r0 : -INFINITY;
+              if (two) sc[(h0 + 1) * stride + t * kTK + j] = j < nk ? r1 : -INFINITY;
+            }
+          }
         }
-        sc[h * stride + j] = s;
       }
       csync();
       // online softmax, one warp per head
@@ -749,37 +785,48 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
         }
       }
       csync();
-      // P.V of one (tile, head): lane holds DPL adjacent output dims
-      for (int task = warp; task < nt * GQ; task += kConsumers) {
-        const int t = task / GQ, h = task % GQ;
+      // P.V of one tile, two heads at a time: lane holds DPL adjacent output dims
+      for (int t = warp; t < nt; t += kConsumers) {
         const int nk = min(kTK, nkp - t * kTK);
         const float* Vt = kt(t) + kTK * HD + lane * DPL;
-        const float* pr = pp + h * stride + t * kTK;
-        float acc[DPL];
+        for (int h0 = 0; h0 < GQ; h0 += 2) {
+          const bool two = h0 + 1 < GQ;
+          const float* p0r = pp + h0 * stride + t * kTK;
+          const float* p1r = pp + (two ? h0 + 1 : h0) * stride + t * kTK;
+          float c0[DPL], c1[DPL];
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-        for (int j = 0; j < nk; ++j) {
-          const float pj = pr[j];
-          if constexpr (DPL == 4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(Vt + j * HD);
-            acc[0] = fmaf(pj, v4.x, acc[0]);
-            acc[1] = fmaf(pj, v4.y, acc[1]);
-            acc[2] = fmaf(pj, v4.z, acc[2]);
-            acc[3] = fmaf(pj, v4.w, acc[3]);
-          } else {
-            const float2 v2 = *reinterpret_cast<const float2*>(Vt + j * HD);
-            acc[0] = fmaf(pj, v2.x, acc[0]);
-            acc[1] = fmaf(pj, v2.y, acc[1]);
+          for (int e = 0; e < DPL; ++e) c0[e] = c1[e] = 0.f;
+          for (int j = 0; j < nk; ++j) {
+            float vv[DPL];
+            if constexpr (DPL == 4) {
+              const float4 v4 = *reinterpret_cast<const float4*>(Vt + j * HD);
+              vv[0] = v4.x; vv[1] = v4.y; vv[2 % DPL] = v4.z; vv[3 % DPL] = v4.w;
+            } else {
+              const float2 v2 = *reinterpret_cast<const float2*>(Vt + j * HD);
+              vv[0] = v2.x; vv[1] = v2.y;
+            }
+            const float pa = p0r[j], pb = p1r[j];
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) {
+              c0[e] = fmaf(pa, vv[e], c0[e]);
+              c1[e] = fmaf(pb, vv[e], c1[e]);
+            }
+          }
+          float* d0 = part + (t * GQ + h0) * HD + lane * DPL;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) d0[e] = c0[e];
+          if (two) {
+            float* d1 = part + (t * GQ + h0 + 1) * HD + lane * DPL;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) d1[e] = c1[e];
           }
         }
-        float* dst = part + (t * GQ + h) * HD + lane * DPL;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) dst[i] = acc[i];
       }
     }
     csync();
-    if (lane == 0)
-      for (int t = 0; t < nt; ++t) mbar_arrive(&S.empty[(c + t) % kNS]);
+    // the pass's stages are free: one counted arrival each, by one thread
+    if (tid == 0)
+      for (int t = 0; t < nt; ++t) mbar_arrive_all(&S.empty[(c + t) % kNS]);
     c += nt;
     // fold the pass into the running outputs, tiles in order
 #pragma unroll
@@ -1014,8 +1061,8 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
-      if (HD == 64 || (HD == 0 && a.hd == 64)) attn_phase<64>(a, ring, S, c, l, pos, sp, tq, ta, abort);
-      else attn_phase<128>(a, ring, S, c, l, pos, sp, tq, ta, abort);
+      if (HD == 64 || (HD == 0 && a.hd == 64)) attn_phase<64>(a, ring, S, c, l, pos, sp, Ld, tq, ta, abort);
+      else attn_phase<128>(a, ring, S, c, l, pos, sp, Ld, tq, ta, abort);
     }
     // o_proj + residual
     const Slice os = phase_slice(a, K_O, Ld, b, G);
