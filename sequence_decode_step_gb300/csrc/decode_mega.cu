@@ -108,27 +108,41 @@ __device__ __forceinline__ Slice phase_slice(const MegaArgs& a, int kind, const 
   }
 }
 
-// Key split of CTA b in the attention phase (all derived from the device position).
+// Attention work of CTA b (all derived from the device position): KV head g and
+// either a key split s (its query heads all together, partials combined by the
+// last split to arrive) or, when the keys fit one split, query head h0 of the
+// group over all keys (the group's heads on separate CTAs, no combine).
 struct Split {
   int g, s, k0, k1, nsplit;
+  int h0, nh;  // the group's query heads [h0, h0 + nh) handled here
   bool active;
 };
 __device__ __forceinline__ Split attn_split(const MegaArgs& a, int pos, int b) {
   Split r;
   r.g = b / a.splits;
   r.s = b % a.splits;
+  const int gq = a.nq / a.nkv;
   const int n_keys = pos + 1;
   int kps = (n_keys + a.splits - 1) / a.splits;
   kps = kps > kMinKeys ? kps : kMinKeys;
   kps = (kps + kTK - 1) / kTK * kTK;
   r.nsplit = (n_keys + kps - 1) / kps;
-  r.active = r.g < a.nkv && r.s < r.nsplit;
-  r.k0 = r.s * kps;
-  r.k1 = min(n_keys, r.k0 + kps);
+  r.h0 = 0;
+  r.nh = gq;
+  if (r.nsplit == 1 && gq > 1 && gq <= a.splits) {  // split the heads instead of the keys
+    r.active = r.g < a.nkv && r.s < gq;
+    r.h0 = r.s;
+    r.nh = 1;
+    r.k0 = 0;
+    r.k1 = n_keys;
+  } else {
+    r.active = r.g < a.nkv && r.s < r.nsplit;
+    r.k0 = r.s * kps;
+    r.k1 = min(n_keys, r.k0 + kps);
+  }
   if (!r.active) r.k0 = r.k1 = 0;
   return r;
 }
-
 
 __device__ __forceinline__ void csync() {  // the 8 consumer warps only
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
@@ -615,7 +629,8 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
                                            uint32_t tag_in, uint32_t tag_out, bool& abort) {
   constexpr int EPL = HD / 32, OUTS = (kGQ * HD + kNT - 1) / kNT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int GQ = a.nq / a.nkv, g = sp.g;
+  // GQ: query heads handled here; HB: global index of the first of them
+  const int GQ = sp.nh, g = sp.g, HB = g * (a.nq / a.nkv) + sp.h0;
   // keys in passes of up to `pt` tiles; the first pass's tiles are waited for now,
   // before the q/k/v poll, so those waits overlap the hand-over from QKV
   const int pt = min(kPass, (kMaxC * 256) / (GQ * HD));
@@ -638,8 +653,15 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
   for (int hh = warp; hh <= GQ; hh += kConsumers) {
     const bool isq = hh < GQ;
     if (!isq && !owns_pos) break;
-    const uint64_t* src = a.qkv + (size_t)(isq ? (g * GQ + hh) : (a.nq + g)) * HD;
+    const uint64_t* src = a.qkv + (size_t)(isq ? (HB + hh) : (a.nq + g)) * HD;
     const uint16_t* gain = isq ? Ld.q_norm : Ld.k_norm;
+    // the norm gains and the RoPE row do not depend on the polled data: load them first
+    float gv[EPL];
+    float2 csv[EPL / 2];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) gv[e] = gain != nullptr ? bf16f(gain[lane + 32 * e]) : 1.f;
+#pragma unroll
+    for (int e = 0; e < EPL / 2; ++e) csv[e] = rrow[lane + 32 * e];
     float v[EPL];
     poll_row<EPL>(a, src, tag_in, v, abort);
     if (gain != nullptr) {
@@ -649,11 +671,11 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       sq = warp_sum(sq);
       const float r = 1.0f / sqrtf(sq / (float)HD + a.eps);
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) v[e] = v[e] * r * bf16f(gain[lane + 32 * e]);
+      for (int e = 0; e < EPL; ++e) v[e] = v[e] * r * gv[e];
     }
 #pragma unroll
     for (int e = 0; e < EPL / 2; ++e) {
-      const float2 cs = rrow[lane + 32 * e];
+      const float2 cs = csv[e];
       const float x0 = v[e], x1 = v[e + EPL / 2];
       v[e] = x0 * cs.x - x1 * cs.y;
       v[e + EPL / 2] = x1 * cs.x + x0 * cs.y;
@@ -668,9 +690,11 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int e = 0; e < EPL; ++e) {
         const int d = lane + 32 * e;
         S.kn_s[d] = v[e];
-        kc[(size_t)pos * HD + d] = v[e];
         S.vn_s[d] = vv[e];
-        vc[(size_t)pos * HD + d] = vv[e];
+        if (sp.h0 == 0) {  // one CTA of the group appends the row
+          kc[(size_t)pos * HD + d] = v[e];
+          vc[(size_t)pos * HD + d] = vv[e];
+        }
       }
     }
   }
@@ -848,7 +872,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       const int idx = tid + oi * kNT;
       if (idx < GQ * HD) {
         const int h = idx / HD, d = idx % HD;
-        st_tagged(a.attn_o + (size_t)(g * GQ + h) * HD + d, oacc[oi] / S.ml_s[2 * h + 1], tag_out);
+        st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, oacc[oi] / S.ml_s[2 * h + 1], tag_out);
       }
     }
     return;
@@ -858,11 +882,11 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     const int idx = tid + oi * kNT;
     if (idx < GQ * HD) {
       const int h = idx / HD, d = idx % HD;
-      a.part_o[((size_t)(g * GQ + h) * a.splits + sp.s) * HD + d] = oacc[oi];
+      a.part_o[((size_t)(HB + h) * a.splits + sp.s) * HD + d] = oacc[oi];
     }
   }
   if (tid < GQ) {
-    const size_t o = ((size_t)(g * GQ + tid) * a.splits + sp.s) * 2;
+    const size_t o = ((size_t)(HB + tid) * a.splits + sp.s) * 2;
     a.part_ml[o] = S.ml_s[2 * tid];
     a.part_ml[o + 1] = S.ml_s[2 * tid + 1];
   }
@@ -881,7 +905,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
   for (int i = tid; i < GQ * ns; i += kConsumers * 32) {
     const int h = i / ns, s2 = i % ns;
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) +
-                             (size_t)(g * GQ + h) * a.splits + s2);
+                             (size_t)(HB + h) * a.splits + s2);
     S.pml_s[2 * i] = ml.x;
     S.pml_s[2 * i + 1] = ml.y;
   }
@@ -896,7 +920,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pm[2 * s2]);
       float den = 0.f;
       for (int s2 = 0; s2 < ns; ++s2) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
-      const float* po = a.part_o + (size_t)(g * GQ + h) * a.splits * HD + d;
+      const float* po = a.part_o + (size_t)(HB + h) * a.splits * HD + d;
       float num = 0.f;
       for (int s0 = 0; s0 < ns; s0 += 8) {
         float pv[8];
@@ -906,7 +930,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
         for (int j = 0; j < 8; ++j)
           if (s0 + j < ns) num = fmaf(expf(pm[2 * (s0 + j)] - M), pv[j], num);
       }
-      st_tagged(a.attn_o + (size_t)(g * GQ + h) * HD + d, num / den, tag_out);
+      st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, num / den, tag_out);
     }
   }
   csync();
