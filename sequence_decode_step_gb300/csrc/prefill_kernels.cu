@@ -298,156 +298,216 @@ __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
     vc[((size_t)(i / HD) * cap + pos) * HD + (i % HD)] = vsrc[i];
 }
 
-// Causal attention for a 64-query block of one head, CUDA cores, online softmax
-// over 64-key tiles. Thread (ty, tx) of a 16 x 16 grid owns query rows 4ty..4ty+3,
-// score columns 4tx..4tx+3 and output columns tx*(hd/16)... of those rows.
+// ---- causal attention on tensor cores (mma.sync m16n8k16, bf16 operands, f32 accumulate)
+// Every f32 operand x enters as two bf16 terms hi = bf16(x), lo = bf16(x - hi); a product
+// a.b is formed as a_hi.b_hi + a_hi.b_lo + a_lo.b_hi (the lo.lo term is below f32
+// rounding of the sum), so scores and outputs carry about 16 bits of the f32 values.
+__device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo_col, uint16_t hi_col) {
+  return (uint32_t)lo_col | ((uint32_t)hi_col << 16);
+}
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  uint16_t h0, l0, h1, l1;
+  split_bf16(x0, h0, l0);
+  split_bf16(x1, h1, l1);
+  hi = pack_bf16x2(h0, h1);
+  lo = pack_bf16x2(l0, l1);
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// One CTA: 64 query rows of one head (4 warps x 16 rows), keys in tiles of 64 up to
+// the block's last position. Per tile, K and V (f32 in the cache) are split into bf16
+// hi/lo rows in shared memory, padded to HD + 8 elements so ldmatrix rows of 16 bytes
+// fall in distinct banks. Scores S = Q.K^T and the online softmax stay in registers
+// (the m16n8 accumulator layout is reused as the A fragment of P.V).
 template <int HD>
-__global__ void __launch_bounds__(256) attn_prefill_kernel(const float* Q, const float* kc,
-                                                           const float* vc, int cap, int p0, int T,
-                                                           int nq, int nkv, uint16_t* o_hi,
-                                                           uint16_t* o_lo) {
-  constexpr int BQ = 64, BK = 64, DPT = HD / 16;
-  extern __shared__ __align__(16) float sm[];
-  float* Qt = sm;               // [HD][BQ]
-  float* Kt = Qt + HD * BQ;     // [HD][BK]
-  float* Vs = Kt + HD * BK;     // [BK][HD]
-  float* Pt = Vs + BK * HD;     // [BK][BQ]
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  const int t0 = blockIdx.x * BQ, h = blockIdx.y, g = h / (nq / nkv);
+__global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q, const float* kc,
+                                                              const float* vc, int cap, int p0,
+                                                              int T, int nq, int nkv,
+                                                              uint16_t* o_hi, uint16_t* o_lo) {
+  constexpr int BQ = 64, BK = 64, LD = HD + 8, KS = HD / 16, NO = HD / 8;
+  extern __shared__ __align__(16) uint16_t smh[];
+  uint16_t* Kh = smh;
+  uint16_t* Kl = Kh + BK * LD;
+  uint16_t* Vh = Kl + BK * LD;
+  uint16_t* Vl = Vh + BK * LD;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  // heavy (late) query blocks first: they have the most key tiles
+  const int qb = gridDim.x - 1 - blockIdx.x;
+  const int t0 = qb * BQ, h = blockIdx.y, kvh = h / (nq / nkv);
   const int nrows = min(BQ, T - t0);
   const int last_key = p0 + t0 + nrows - 1;
-  constexpr int NL = BQ * HD / 4 / 256;  // float4 per thread per tile (8 at hd 128)
-  {
-    float4 q[NL];
+  const int r0 = t0 + warp * 16 + g;  // this lane's two rows: r0 and r0 + 8 (block-relative t)
+  // Q fragments (A operand, row-major 16 x 16 per k-step), split hi/lo
+  uint32_t qh[KS][4], ql[KS][4];
 #pragma unroll
-    for (int i = 0; i < NL; ++i) {  // every load in flight before any is used
-      const int idx = tid + i * 256, r = idx % BQ, d4 = idx / BQ;
-      q[i] = r < nrows ? *reinterpret_cast<const float4*>(Q + ((size_t)(t0 + r) * nq + h) * HD + d4 * 4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+  for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-    for (int i = 0; i < NL; ++i) {
-      const int idx = tid + i * 256, r = idx % BQ, d4 = idx / BQ;
-      Qt[(d4 * 4 + 0) * BQ + r] = q[i].x;
-      Qt[(d4 * 4 + 1) * BQ + r] = q[i].y;
-      Qt[(d4 * 4 + 2) * BQ + r] = q[i].z;
-      Qt[(d4 * 4 + 3) * BQ + r] = q[i].w;
+    for (int j = 0; j < 4; ++j) {
+      const int row = r0 + (j & 1) * 8, col = ks * 16 + 2 * t + (j >> 1) * 8;
+      float2 v = make_float2(0.f, 0.f);
+      if (row < T) v = *reinterpret_cast<const float2*>(Q + ((size_t)row * nq + h) * HD + col);
+      split2(v.x, v.y, qh[ks][j], ql[ks][j]);
     }
   }
-  float m[4], l[4], acc[4][DPT];
+  float o[NO][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.f;
+  for (int nb = 0; nb < NO; ++nb)
 #pragma unroll
-    for (int e = 0; e < DPT; ++e) acc[i][e] = 0.f;
-  }
-  const float* kg = kc + (size_t)g * cap * HD;
-  const float* vg = vc + (size_t)g * cap * HD;
+    for (int j = 0; j < 4; ++j) o[nb][j] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int qp0 = p0 + r0, qp1 = qp0 + 8;
+  const float* kg = kc + (size_t)kvh * cap * HD;
+  const float* vg = vc + (size_t)kvh * cap * HD;
   const int n_tiles = last_key / BK + 1;
   for (int kt = 0; kt < n_tiles; ++kt) {
     const int k0 = kt * BK;
-    // K is stored transposed (key index fastest across threads: conflict-free
-    // stores); V row-major with the dimension fastest (coalesced loads and
-    // conflict-free stores). All loads of the tile are issued before any store.
-    float4 kv[NL], vv[NL];
-#pragma unroll
-    for (int i = 0; i < NL; ++i) {
-      const int idx = tid + i * 256;
-      const int rk = idx % BK, dk = idx / BK;
-      const int rv = idx / (HD / 4), dv = idx % (HD / 4);
-      kv[i] = k0 + rk <= last_key ? *reinterpret_cast<const float4*>(kg + (size_t)(k0 + rk) * HD + dk * 4)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      vv[i] = k0 + rv <= last_key ? *reinterpret_cast<const float4*>(vg + (size_t)(k0 + rv) * HD + dv * 4)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < NL; ++i) {
-      const int idx = tid + i * 256;
-      const int rk = idx % BK, dk = idx / BK;
-      const int rv = idx / (HD / 4), dv = idx % (HD / 4);
-      Kt[(dk * 4 + 0) * BK + rk] = kv[i].x;
-      Kt[(dk * 4 + 1) * BK + rk] = kv[i].y;
-      Kt[(dk * 4 + 2) * BK + rk] = kv[i].z;
-      Kt[(dk * 4 + 3) * BK + rk] = kv[i].w;
-      *reinterpret_cast<float4*>(Vs + rv * HD + dv * 4) = vv[i];
-    }
-    __syncthreads();
-    float sc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sc[i][j] = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < HD; ++d) {
-      const float4 q = *reinterpret_cast<const float4*>(Qt + d * BQ + ty * 4);
-      const float4 k = *reinterpret_cast<const float4*>(Kt + d * BK + tx * 4);
-      const float qa[4] = {q.x, q.y, q.z, q.w}, ka[4] = {k.x, k.y, k.z, k.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) sc[i][j] = fmaf(qa[i], ka[j], sc[i][j]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int qp = p0 + t0 + ty * 4 + i;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (k0 + tx * 4 + j > qp) sc[i][j] = -INFINITY;
-        mx = fmaxf(mx, sc[i][j]);
-      }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float mn = fmaxf(m[i], mx);
-      float rs = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float p = (sc[i][j] == -INFINITY) ? 0.f : expf(sc[i][j] - mn);
-        Pt[(tx * 4 + j) * BQ + ty * 4 + i] = p;
-        rs += p;
-      }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
-      const float alpha = (m[i] == -INFINITY) ? 0.f : expf(m[i] - mn);
-      l[i] = l[i] * alpha + rs;
-      m[i] = mn;
-#pragma unroll
-      for (int e = 0; e < DPT; ++e) acc[i][e] *= alpha;
-    }
-    __syncthreads();
+    __syncthreads();  // the previous tile's readers are done
+    constexpr int NL = BK * HD / 4 / 128;  // float4 of K (and of V) per thread
 #pragma unroll 4
-    for (int c = 0; c < BK; ++c) {
-      const float4 p = *reinterpret_cast<const float4*>(Pt + c * BQ + ty * 4);
-      const float pa[4] = {p.x, p.y, p.z, p.w};
-      float vv[DPT];
-#pragma unroll
-      for (int e = 0; e < DPT; e += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(Vs + c * HD + tx * DPT + e);
-        vv[e] = v4.x;
-        vv[e + 1] = v4.y;
-        vv[e + 2] = v4.z;
-        vv[e + 3] = v4.w;
+    for (int i = 0; i < NL; ++i) {
+      const int idx = tid + i * 128, r = idx / (HD / 4), c4 = (idx % (HD / 4)) * 4;
+      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+      if (k0 + r <= last_key) {
+        kv = *reinterpret_cast<const float4*>(kg + (size_t)(k0 + r) * HD + c4);
+        vv = *reinterpret_cast<const float4*>(vg + (size_t)(k0 + r) * HD + c4);
       }
+      uint32_t h01, l01, h23, l23;
+      split2(kv.x, kv.y, h01, l01);
+      split2(kv.z, kv.w, h23, l23);
+      *reinterpret_cast<uint2*>(Kh + r * LD + c4) = make_uint2(h01, h23);
+      *reinterpret_cast<uint2*>(Kl + r * LD + c4) = make_uint2(l01, l23);
+      split2(vv.x, vv.y, h01, l01);
+      split2(vv.z, vv.w, h23, l23);
+      *reinterpret_cast<uint2*>(Vh + r * LD + c4) = make_uint2(h01, h23);
+      *reinterpret_cast<uint2*>(Vl + r * LD + c4) = make_uint2(l01, l23);
+    }
+    __syncthreads();
+    // S = Q K^T: 8 n-blocks of 8 keys
+    float sc[BK / 8][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+    for (int nb = 0; nb < BK / 8; ++nb)
 #pragma unroll
-        for (int e = 0; e < DPT; ++e) acc[i][e] = fmaf(pa[i], vv[e], acc[i][e]);
+      for (int j = 0; j < 4; ++j) sc[nb][j] = 0.f;
+    const int mrow = lane & 7, mi = lane >> 3;  // ldmatrix: matrix mi, row mrow
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+      for (int nb = 0; nb < BK / 8; nb += 2) {
+        const int key = (nb + (mi >> 1)) * 8 + mrow, col = ks * 16 + (mi & 1) * 8;
+        uint32_t bh0, bh1, bh2, bh3, bl0, bl1, bl2, bl3;
+        ldsm_x4(smem_addr(Kh + key * LD + col), bh0, bh1, bh2, bh3);
+        ldsm_x4(smem_addr(Kl + key * LD + col), bl0, bl1, bl2, bl3);
+        mma_bf16(sc[nb], qh[ks], bh0, bh1);
+        mma_bf16(sc[nb], qh[ks], bl0, bl1);
+        mma_bf16(sc[nb], ql[ks], bh0, bh1);
+        mma_bf16(sc[nb + 1], qh[ks], bh2, bh3);
+        mma_bf16(sc[nb + 1], qh[ks], bl2, bl3);
+        mma_bf16(sc[nb + 1], ql[ks], bh2, bh3);
+      }
+    }
+    // causal mask and online softmax (rows r0 and r0 + 8; a quad of lanes shares a row)
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < BK / 8; ++nb) {
+      const int key = k0 + nb * 8 + 2 * t;
+      if (key > qp0) sc[nb][0] = -INFINITY;
+      if (key + 1 > qp0) sc[nb][1] = -INFINITY;
+      if (key > qp1) sc[nb][2] = -INFINITY;
+      if (key + 1 > qp1) sc[nb][3] = -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
+      mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = m0 == -INFINITY ? 0.f : expf(m0 - mn0);
+    const float al1 = m1 == -INFINITY ? 0.f : expf(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < BK / 8; ++nb) {
+      sc[nb][0] = sc[nb][0] == -INFINITY ? 0.f : expf(sc[nb][0] - mn0);
+      sc[nb][1] = sc[nb][1] == -INFINITY ? 0.f : expf(sc[nb][1] - mn0);
+      sc[nb][2] = sc[nb][2] == -INFINITY ? 0.f : expf(sc[nb][2] - mn1);
+      sc[nb][3] = sc[nb][3] == -INFINITY ? 0.f : expf(sc[nb][3] - mn1);
+      rs0 += sc[nb][0] + sc[nb][1];
+      rs1 += sc[nb][2] + sc[nb][3];
+    }
+    l0 = l0 * al0 + rs0;  // per-lane partial row sums; the quad adds them at the end
+    l1 = l1 * al1 + rs1;
+#pragma unroll
+    for (int nb = 0; nb < NO; ++nb) {
+      o[nb][0] *= al0;
+      o[nb][1] *= al0;
+      o[nb][2] *= al1;
+      o[nb][3] *= al1;
+    }
+    // O += P V: 4 k-steps of 16 keys; P's A fragment comes from two score n-blocks
+#pragma unroll
+    for (int kk = 0; kk < BK / 16; ++kk) {
+      uint32_t ph[4], pl[4];
+      split2(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+      split2(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+      split2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+      split2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+      for (int nb = 0; nb < NO; nb += 2) {
+        // V rows kk*16 .. +15 (keys), columns nb*8 .. +15 (dims), transposed fragments
+        const int key = kk * 16 + (mi & 1) * 8 + mrow, col = (nb + (mi >> 1)) * 8;
+        uint32_t bh0, bh1, bh2, bh3, bl0, bl1, bl2, bl3;
+        ldsm_x4_t(smem_addr(Vh + key * LD + col), bh0, bh1, bh2, bh3);
+        ldsm_x4_t(smem_addr(Vl + key * LD + col), bl0, bl1, bl2, bl3);
+        mma_bf16(o[nb], ph, bh0, bh1);
+        mma_bf16(o[nb], ph, bl0, bl1);
+        mma_bf16(o[nb], pl, bh0, bh1);
+        mma_bf16(o[nb + 1], ph, bh2, bh3);
+        mma_bf16(o[nb + 1], ph, bl2, bl3);
+        mma_bf16(o[nb + 1], pl, bh2, bh3);
+      }
     }
   }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = ty * 4 + i;
-    if (r >= nrows) continue;
-    const float inv = 1.0f / l[i];
-    const size_t base = (size_t)(t0 + r) * nq * HD + (size_t)h * HD + tx * DPT;
-#pragma unroll
-    for (int e = 0; e < DPT; ++e) {
-      uint16_t hi, lo;
-      split_bf16(acc[i][e] * inv, hi, lo);
-      o_hi[base + e] = hi;
-      o_lo[base + e] = lo;
+  for (int nb = 0; nb < NO; ++nb) {
+    const int col = h * HD + nb * 8 + 2 * t;
+    if (r0 < t0 + nrows) {
+      uint32_t hi, lo;
+      split2(o[nb][0] * inv0, o[nb][1] * inv0, hi, lo);
+      *reinterpret_cast<uint32_t*>(o_hi + (size_t)r0 * nq * HD + col) = hi;
+      *reinterpret_cast<uint32_t*>(o_lo + (size_t)r0 * nq * HD + col) = lo;
+    }
+    if (r0 + 8 < t0 + nrows) {
+      uint32_t hi, lo;
+      split2(o[nb][2] * inv1, o[nb][3] * inv1, hi, lo);
+      *reinterpret_cast<uint32_t*>(o_hi + (size_t)(r0 + 8) * nq * HD + col) = hi;
+      *reinterpret_cast<uint32_t*>(o_lo + (size_t)(r0 + 8) * nq * HD + col) = lo;
     }
   }
 }
@@ -478,15 +538,15 @@ cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int 
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
-static size_t attn_prefill_smem(int hd) { return (size_t)(3 * hd * 64 + 64 * 64) * 4; }
+static size_t attn_prefill_tc_smem(int hd) { return (size_t)4 * 64 * (hd + 8) * 2; }
 cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
                                 int T, int nq, int nkv, int hd, uint16_t* o_hi, uint16_t* o_lo,
                                 cudaStream_t s) {
   const dim3 grid((T + 63) / 64, nq);
   if (hd == 64)
-    attn_prefill_kernel<64><<<grid, 256, attn_prefill_smem(64), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
+    attn_prefill_tc_kernel<64><<<grid, 128, attn_prefill_tc_smem(64), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
   else if (hd == 128)
-    attn_prefill_kernel<128><<<grid, 256, attn_prefill_smem(128), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
+    attn_prefill_tc_kernel<128><<<grid, 128, attn_prefill_tc_smem(128), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -496,12 +556,11 @@ cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
   return cudaGetLastError();
 }
 cudaError_t set_prefill_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<64>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)attn_prefill_smem(64));
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn_prefill_tc_smem(64));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_prefill_smem(128));
+    e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn_prefill_tc_smem(128));
   return e;
 }
 
