@@ -333,22 +333,50 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-// One CTA: 64 query rows of one head (4 warps x 16 rows), keys in tiles of 64 up to
-// the block's last position. Per tile, K and V (f32 in the cache) are split into bf16
-// hi/lo rows in shared memory, padded to HD + 8 elements so ldmatrix rows of 16 bytes
-// fall in distinct banks. Scores S = Q.K^T and the online softmax stay in registers
-// (the m16n8 accumulator layout is reused as the A fragment of P.V).
+// K and V of keys [0, n) of every KV head, split into bf16 hi/lo rows of HD + 8
+// elements (the padding keeps the attention kernel's ldmatrix rows in distinct
+// banks): dst[4][nkv][rows][HD + 8] = {K hi, K lo, V hi, V lo}. One warp per (key, head).
 template <int HD>
-__global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q, const float* kc,
-                                                              const float* vc, int cap, int p0,
-                                                              int T, int nq, int nkv,
-                                                              uint16_t* o_hi, uint16_t* o_lo) {
-  constexpr int BQ = 64, BK = 64, LD = HD + 8, KS = HD / 16, NO = HD / 8;
-  extern __shared__ __align__(16) uint16_t smh[];
-  uint16_t* Kh = smh;
-  uint16_t* Kl = Kh + BK * LD;
-  uint16_t* Vh = Kl + BK * LD;
-  uint16_t* Vl = Vh + BK * LD;
+__global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const float* vc, int cap,
+                                                       int n, int nkv, int rows, uint16_t* dst) {
+  constexpr int LD = HD + 8, EPL = HD / 32;
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (wid >= n * nkv) return;
+  const int key = wid % n, kvh = wid / n;
+  const size_t plane = (size_t)nkv * rows * LD;
+  const size_t row = ((size_t)kvh * rows + key) * LD;
+  const float* ks = kc + ((size_t)kvh * cap + key) * HD;
+  const float* vs = vc + ((size_t)kvh * cap + key) * HD;
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2) {
+    const int d = lane * EPL + e;
+    const float2 k2 = *reinterpret_cast<const float2*>(ks + d);
+    const float2 v2 = *reinterpret_cast<const float2*>(vs + d);
+    uint32_t kh, kl, vh, vl;
+    split2(k2.x, k2.y, kh, kl);
+    split2(v2.x, v2.y, vh, vl);
+    *reinterpret_cast<uint32_t*>(dst + row + d) = kh;
+    *reinterpret_cast<uint32_t*>(dst + plane + row + d) = kl;
+    *reinterpret_cast<uint32_t*>(dst + 2 * plane + row + d) = vh;
+    *reinterpret_cast<uint32_t*>(dst + 3 * plane + row + d) = vl;
+  }
+}
+
+// One CTA: 64 query rows of one head (4 warps x 16 rows), keys in tiles of BK up to
+// the block's last position. The tiles of pre-split K/V rows (kv_split_kernel) come
+// in by one bulk copy per array into a double buffer, the next tile's copies issued
+// before the current tile is used. Scores S = Q.K^T and the online softmax stay in
+// registers (the m16n8 accumulator layout is reused as the A fragment of P.V).
+template <int HD, int BK>
+__global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q,
+                                                              const uint16_t* kvs, int rows,
+                                                              int p0, int T, int nq, int nkv,
+                                                              uint16_t* o_hi, uint16_t* o_lo,
+                                                              int* err, uint64_t wait_ns) {
+  constexpr int BQ = 64, LD = HD + 8, KS = HD / 16, NO = HD / 8;
+  constexpr uint32_t kArr = (uint32_t)BK * LD * 2;  // bytes of one array's tile
+  extern __shared__ __align__(128) uint8_t smraw[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smraw + 2 * 4 * kArr);  // [2]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   // heavy (late) query blocks first: they have the most key tiles
@@ -357,6 +385,26 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q, co
   const int nrows = min(BQ, T - t0);
   const int last_key = p0 + t0 + nrows - 1;
   const int r0 = t0 + warp * 16 + g;  // this lane's two rows: r0 and r0 + 8 (block-relative t)
+  const size_t plane = (size_t)nkv * rows * LD;
+  const uint16_t* src = kvs + (size_t)kvh * rows * LD;
+  const int n_tiles = last_key / BK + 1;
+  // a whole tile of each array (rows past the last key hold zeros or older keys:
+  // finite, and masked); buffer b = kt & 1, its barrier completes phase kt >> 1
+  auto issue = [&](int kt) {
+    const int b = kt & 1;
+    mbar_expect_tx(&bar[b], 4 * kArr);
+#pragma unroll
+    for (int arr = 0; arr < 4; ++arr)
+      bulk_load(smraw + (size_t)(b * 4 + arr) * kArr, src + arr * plane + (size_t)kt * BK * LD,
+                kArr, &bar[b]);
+  };
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_barrier_init();
+    issue(0);
+    if (n_tiles > 1) issue(1);
+  }
   // Q fragments (A operand, row-major 16 x 16 per k-step), split hi/lo
   uint32_t qh[KS][4], ql[KS][4];
 #pragma unroll
@@ -369,6 +417,7 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q, co
       split2(v.x, v.y, qh[ks][j], ql[ks][j]);
     }
   }
+  __syncthreads();  // barrier initialisation visible to all threads
   float o[NO][4];
 #pragma unroll
   for (int nb = 0; nb < NO; ++nb)
@@ -376,32 +425,19 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q, co
     for (int j = 0; j < 4; ++j) o[nb][j] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const int qp0 = p0 + r0, qp1 = qp0 + 8;
-  const float* kg = kc + (size_t)kvh * cap * HD;
-  const float* vg = vc + (size_t)kvh * cap * HD;
-  const int n_tiles = last_key / BK + 1;
+  bool ok = true;
   for (int kt = 0; kt < n_tiles; ++kt) {
-    const int k0 = kt * BK;
-    __syncthreads();  // the previous tile's readers are done
-    constexpr int NL = BK * HD / 4 / 128;  // float4 of K (and of V) per thread
-#pragma unroll 4
-    for (int i = 0; i < NL; ++i) {
-      const int idx = tid + i * 128, r = idx / (HD / 4), c4 = (idx % (HD / 4)) * 4;
-      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (k0 + r <= last_key) {
-        kv = *reinterpret_cast<const float4*>(kg + (size_t)(k0 + r) * HD + c4);
-        vv = *reinterpret_cast<const float4*>(vg + (size_t)(k0 + r) * HD + c4);
-      }
-      uint32_t h01, l01, h23, l23;
-      split2(kv.x, kv.y, h01, l01);
-      split2(kv.z, kv.w, h23, l23);
-      *reinterpret_cast<uint2*>(Kh + r * LD + c4) = make_uint2(h01, h23);
-      *reinterpret_cast<uint2*>(Kl + r * LD + c4) = make_uint2(l01, l23);
-      split2(vv.x, vv.y, h01, l01);
-      split2(vv.z, vv.w, h23, l23);
-      *reinterpret_cast<uint2*>(Vh + r * LD + c4) = make_uint2(h01, h23);
-      *reinterpret_cast<uint2*>(Vl + r * LD + c4) = make_uint2(l01, l23);
+    const int k0 = kt * BK, b = kt & 1;
+    const bool got = mbar_wait(&bar[b], (uint32_t)((kt >> 1) & 1), wait_ns);
+    ok = __syncthreads_and(got) != 0;  // one decision for the whole block
+    if (!ok) {  // gave up: outputs invalid, the host sees the error word
+      if (tid == 0) atomicOr(err, ERR_TIMEOUT);
+      break;
     }
-    __syncthreads();
+    const uint16_t* Kh = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 0) * kArr);
+    const uint16_t* Kl = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 1) * kArr);
+    const uint16_t* Vh = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 2) * kArr);
+    const uint16_t* Vl = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 3) * kArr);
     // S = Q K^T: 8 n-blocks of 8 keys
     float sc[BK / 8][4];
 #pragma unroll
@@ -488,6 +524,19 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q, co
         mma_bf16(o[nb + 1], pl, bh2, bh3);
       }
     }
+    // buffer b is free once every warp has read it (generic proxy; ordered before the
+    // bulk copy that refills it): refill it with tile kt + 2
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0 && kt + 2 < n_tiles) issue(kt + 2);
+  }
+  if (!ok) {  // copies may still be in flight into this CTA's shared memory
+    if (tid == 0)
+      for (int b = 0; b < 2; ++b) {
+        mbar_wait(&bar[b], 0, kDrainNs);
+        mbar_wait(&bar[b], 1, kDrainNs);
+      }
+    return;
   }
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -538,17 +587,27 @@ cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int 
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
-static size_t attn_prefill_tc_smem(int hd) { return (size_t)4 * 64 * (hd + 8) * 2; }
+constexpr int kAttnBK = 32;  // keys per tile: 2 buffers x 4 arrays = 70 KB at hd 128, two CTAs per SM
+static size_t attn_prefill_tc_smem(int hd) { return (size_t)2 * 4 * kAttnBK * (hd + 8) * 2 + 16; }
+size_t kv_split_bytes(int nkv, int rows, int hd) { return (size_t)4 * nkv * rows * (hd + 8) * 2; }
+int kv_split_rows(int max_ctx) { return (max_ctx + kAttnBK - 1) / kAttnBK * kAttnBK; }
 cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
-                                int T, int nq, int nkv, int hd, uint16_t* o_hi, uint16_t* o_lo,
+                                int T, int nq, int nkv, int hd, uint16_t* kvs, int rows,
+                                uint16_t* o_hi, uint16_t* o_lo, int* err, uint64_t wait_ns,
                                 cudaStream_t s) {
-  const dim3 grid((T + 63) / 64, nq);
-  if (hd == 64)
-    attn_prefill_tc_kernel<64><<<grid, 128, attn_prefill_tc_smem(64), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
-  else if (hd == 128)
-    attn_prefill_tc_kernel<128><<<grid, 128, attn_prefill_tc_smem(128), s>>>(Q, kc, vc, cap, p0, T, nq, nkv, o_hi, o_lo);
-  else
+  const int n = p0 + T;  // keys this pass reads
+  const dim3 grid((T + 63) / 64, nq), sgrid((n * nkv + 7) / 8);
+  if (hd == 64) {
+    kv_split_kernel<64><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, nkv, rows, kvs);
+    attn_prefill_tc_kernel<64, kAttnBK><<<grid, 128, attn_prefill_tc_smem(64), s>>>(
+        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, err, wait_ns);
+  } else if (hd == 128) {
+    kv_split_kernel<128><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, nkv, rows, kvs);
+    attn_prefill_tc_kernel<128, kAttnBK><<<grid, 128, attn_prefill_tc_smem(128), s>>>(
+        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, err, wait_ns);
+  } else {
     return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
@@ -556,10 +615,10 @@ cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
   return cudaGetLastError();
 }
 cudaError_t set_prefill_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<64, kAttnBK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)attn_prefill_tc_smem(64));
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128, kAttnBK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)attn_prefill_tc_smem(128));
   return e;
 }
