@@ -121,6 +121,7 @@ struct qw_handle {
   uint16_t* pf_m_hi = nullptr;   // [Tmax, I] SwiGLU output split
   uint16_t* pf_m_lo = nullptr;
   uint16_t* pf_kvs = nullptr;    // K, V of the context split into bf16 hi/lo rows (attention)
+  void* pf_attn_part = nullptr;  // partial attention outputs of split query blocks + counters
   int kvs_rows = 0;
   CUtensorMap tm_xn_hi, tm_xn_lo, tm_o_hi, tm_o_lo, tm_m_hi, tm_m_lo;
   std::vector<CUtensorMap> tm_qkv, tm_ow, tm_gu, tm_dw;  // per layer, weight side
@@ -298,6 +299,8 @@ static int alloc_state(qw_handle* h) {
     pieces.push_back({(void**)&h->pf_m_lo, Tm * I * 2});
     h->kvs_rows = kv_split_rows(c.max_ctx);
     pieces.push_back({(void**)&h->pf_kvs, kv_split_bytes(c.n_kv_heads, h->kvs_rows, c.head_dim)});
+    pieces.push_back({(void**)&h->pf_attn_part,
+                      attn_part_bytes(c.n_q_heads, (int)Tm, c.max_ctx, c.head_dim)});
   }
   size_t total = 0;
   for (auto& p : pieces) total = align_up(total, 256) + p.bytes;
@@ -999,8 +1002,8 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
     QW_CUDA(h, launch_qk_rope_kv_rows(h->pf_qkv, T, p0, c.n_q_heads, c.n_kv_heads, hd, lw.q_norm,
                                       lw.k_norm, c.eps, h->rope, h->pf_q, kc, vc, c.max_ctx, s));
     QW_CUDA(h, launch_attn_prefill(h->pf_q, kc, vc, c.max_ctx, p0, T, c.n_q_heads, c.n_kv_heads,
-                                   hd, h->pf_kvs, h->kvs_rows, h->pf_o_hi, h->pf_o_lo, h->d_err,
-                                   h->wait_ns, s));
+                                   hd, h->pf_kvs, h->kvs_rows, h->pf_o_hi, h->pf_o_lo,
+                                   h->pf_attn_part, c.max_prefill_t, h->d_err, h->wait_ns, s));
     QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, h->tm_ow[l], H, qd, h->pf_x, nullptr,
                     nullptr, nullptr, nullptr));
     QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, lw.mlp_norm, c.eps, h->pf_xn_hi, h->pf_xn_lo,

@@ -367,31 +367,51 @@ __global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const fl
 // in by one bulk copy per array into a double buffer, the next tile's copies issued
 // before the current tile is used. Scores S = Q.K^T and the online softmax stay in
 // registers (the m16n8 accumulator layout is reused as the A fragment of P.V).
+// Split of the causal work: query block qb reads n_tiles(qb) key tiles; they are cut
+// into chunks of at most CH tiles, one CTA each, listed heavy block first.
+struct AttnSplit {
+  float* part_o;     // [nq][nqb][max_ch][64][HD] unnormalised partial outputs
+  float2* part_ml;   // [nq][nqb][max_ch][64] (row max, row sum)
+  int* counters;     // [nq][nqb] arrivals, 0 between launches
+  int max_ch, ch;
+};
+
 template <int HD, int BK>
 __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q,
                                                               const uint16_t* kvs, int rows,
                                                               int p0, int T, int nq, int nkv,
                                                               uint16_t* o_hi, uint16_t* o_lo,
-                                                              int* err, uint64_t wait_ns) {
+                                                              const AttnSplit sp, int* err,
+                                                              uint64_t wait_ns) {
   constexpr int BQ = 64, LD = HD + 8, KS = HD / 16, NO = HD / 8;
   constexpr uint32_t kArr = (uint32_t)BK * LD * 2;  // bytes of one array's tile
   extern __shared__ __align__(128) uint8_t smraw[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smraw + 2 * 4 * kArr);  // [2]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
-  // heavy (late) query blocks first: they have the most key tiles
-  const int qb = gridDim.x - 1 - blockIdx.x;
+  // this CTA's (query block, key chunk): blocks from the last (heaviest) down
+  const int nqb = (T + BQ - 1) / BQ;
+  int qb = nqb - 1, chunk = blockIdx.x, nch = 1;
+  for (;; --qb) {
+    const int nr = min(BQ, T - qb * BQ);
+    const int nt = (p0 + qb * BQ + nr - 1) / BK + 1;
+    nch = (nt + sp.ch - 1) / sp.ch;
+    if (chunk < nch || qb == 0) break;
+    chunk -= nch;
+  }
   const int t0 = qb * BQ, h = blockIdx.y, kvh = h / (nq / nkv);
   const int nrows = min(BQ, T - t0);
   const int last_key = p0 + t0 + nrows - 1;
   const int r0 = t0 + warp * 16 + g;  // this lane's two rows: r0 and r0 + 8 (block-relative t)
   const size_t plane = (size_t)nkv * rows * LD;
   const uint16_t* src = kvs + (size_t)kvh * rows * LD;
-  const int n_tiles = last_key / BK + 1;
+  const int kt0 = chunk * sp.ch, kt1 = min(last_key / BK + 1, kt0 + sp.ch);
+  const int n_tiles = kt1 - kt0;
   // a whole tile of each array (rows past the last key hold zeros or older keys:
-  // finite, and masked); buffer b = kt & 1, its barrier completes phase kt >> 1
-  auto issue = [&](int kt) {
-    const int b = kt & 1;
+  // finite, and masked); the i-th tile of the chunk uses buffer i & 1, whose
+  // barrier completes phase i >> 1
+  auto issue = [&](int i) {
+    const int b = i & 1, kt = kt0 + i;
     mbar_expect_tx(&bar[b], 4 * kArr);
 #pragma unroll
     for (int arr = 0; arr < 4; ++arr)
@@ -426,9 +446,9 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q,
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const int qp0 = p0 + r0, qp1 = qp0 + 8;
   bool ok = true;
-  for (int kt = 0; kt < n_tiles; ++kt) {
-    const int k0 = kt * BK, b = kt & 1;
-    const bool got = mbar_wait(&bar[b], (uint32_t)((kt >> 1) & 1), wait_ns);
+  for (int i = 0; i < n_tiles; ++i) {
+    const int k0 = (kt0 + i) * BK, b = i & 1;
+    const bool got = mbar_wait(&bar[b], (uint32_t)((i >> 1) & 1), wait_ns);
     ok = __syncthreads_and(got) != 0;  // one decision for the whole block
     if (!ok) {  // gave up: outputs invalid, the host sees the error word
       if (tid == 0) atomicOr(err, ERR_TIMEOUT);
@@ -528,20 +548,82 @@ __global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q,
     // bulk copy that refills it): refill it with tile kt + 2
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
-    if (tid == 0 && kt + 2 < n_tiles) issue(kt + 2);
+    if (tid == 0 && i + 2 < n_tiles) issue(i + 2);
   }
   if (!ok) {  // copies may still be in flight into this CTA's shared memory
-    if (tid == 0)
+    if (tid == 0) {
       for (int b = 0; b < 2; ++b) {
         mbar_wait(&bar[b], 0, kDrainNs);
         mbar_wait(&bar[b], 1, kDrainNs);
       }
+      // still arrive, so the block's counter is back at 0 for the next launch
+      if (nch > 1 && atomicAdd(&sp.counters[h * nqb + qb], 1) == nch - 1)
+        sp.counters[h * nqb + qb] = 0;
+    }
     return;
   }
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  if (nch > 1) {  // one chunk of several: partial results, the last to arrive merges
+    const int rr = warp * 16 + g;  // block-relative rows rr and rr + 8
+    const size_t slot = ((size_t)h * nqb + qb) * sp.max_ch;
+    float* po = sp.part_o + (slot + chunk) * BQ * HD;
+#pragma unroll
+    for (int nb = 0; nb < NO; ++nb) {
+      const int d = nb * 8 + 2 * t;
+      *reinterpret_cast<float2*>(po + rr * HD + d) = make_float2(o[nb][0], o[nb][1]);
+      *reinterpret_cast<float2*>(po + (rr + 8) * HD + d) = make_float2(o[nb][2], o[nb][3]);
+    }
+    if (t == 0) {
+      sp.part_ml[(slot + chunk) * BQ + rr] = make_float2(m0, l0);
+      sp.part_ml[(slot + chunk) * BQ + rr + 8] = make_float2(m1, l1);
+    }
+    __threadfence();
+    __syncthreads();
+    int* last = reinterpret_cast<int*>(smraw);
+    if (tid == 0) *last = atomicAdd(&sp.counters[h * nqb + qb], 1) == nch - 1;
+    __syncthreads();
+    if (!*last) return;
+    __threadfence();
+    // merge in chunk order: per row, weights exp(m_c - M) / sum_c exp(m_c - M) l_c
+    float* wsm = reinterpret_cast<float*>(smraw) + 4;  // [BQ][nch]
+    if (tid < BQ) {
+      float M = -INFINITY;
+      for (int c2 = 0; c2 < nch; ++c2) M = fmaxf(M, __ldcg(&sp.part_ml[(slot + c2) * BQ + tid]).x);
+      float den = 0.f;
+      for (int c2 = 0; c2 < nch; ++c2) {
+        const float2 ml = __ldcg(&sp.part_ml[(slot + c2) * BQ + tid]);
+        const float w = ml.x == -INFINITY ? 0.f : expf(ml.x - M);
+        wsm[tid * nch + c2] = w;
+        den = fmaf(w, ml.y, den);
+      }
+      const float inv = 1.0f / den;
+      for (int c2 = 0; c2 < nch; ++c2) wsm[tid * nch + c2] *= inv;
+    }
+    __syncthreads();
+    for (int idx = 2 * tid; idx < BQ * HD; idx += 2 * 128) {
+      const int rr2 = idx / HD, d = idx % HD;
+      float a0 = 0.f, a1 = 0.f;
+      for (int c2 = 0; c2 < nch; ++c2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(
+            sp.part_o + (slot + c2) * BQ * HD + rr2 * HD + d));
+        const float w = wsm[rr2 * nch + c2];
+        a0 = fmaf(w, v.x, a0);
+        a1 = fmaf(w, v.y, a1);
+      }
+      if (rr2 < nrows) {
+        uint32_t hi, lo;
+        split2(a0, a1, hi, lo);
+        const size_t off = (size_t)(t0 + rr2) * nq * HD + h * HD + d;
+        *reinterpret_cast<uint32_t*>(o_hi + off) = hi;
+        *reinterpret_cast<uint32_t*>(o_lo + off) = lo;
+      }
+    }
+    if (tid == 0) sp.counters[h * nqb + qb] = 0;  // not used again in this launch
+    return;
+  }
   const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
 #pragma unroll
   for (int nb = 0; nb < NO; ++nb) {
@@ -591,20 +673,43 @@ constexpr int kAttnBK = 32;  // keys per tile: 2 buffers x 4 arrays = 70 KB at h
 static size_t attn_prefill_tc_smem(int hd) { return (size_t)2 * 4 * kAttnBK * (hd + 8) * 2 + 16; }
 size_t kv_split_bytes(int nkv, int rows, int hd) { return (size_t)4 * nkv * rows * (hd + 8) * 2; }
 int kv_split_rows(int max_ctx) { return (max_ctx + kAttnBK - 1) / kAttnBK * kAttnBK; }
+constexpr int kAttnChunk = 8;  // key tiles per CTA at most (causal work balanced across CTAs)
+int attn_max_chunks(int max_ctx) {
+  return ((max_ctx + kAttnBK - 1) / kAttnBK + kAttnChunk - 1) / kAttnChunk;
+}
+size_t attn_part_bytes(int nq, int max_t, int max_ctx, int hd) {
+  const size_t nqb = (size_t)(max_t + 63) / 64, slots = (size_t)nq * nqb * attn_max_chunks(max_ctx);
+  return slots * 64 * ((size_t)hd * 4 + 8) + (size_t)nq * nqb * 4;
+}
 cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
                                 int T, int nq, int nkv, int hd, uint16_t* kvs, int rows,
-                                uint16_t* o_hi, uint16_t* o_lo, int* err, uint64_t wait_ns,
-                                cudaStream_t s) {
+                                uint16_t* o_hi, uint16_t* o_lo, void* part, int max_t,
+                                int* err, uint64_t wait_ns, cudaStream_t s) {
   const int n = p0 + T;  // keys this pass reads
-  const dim3 grid((T + 63) / 64, nq), sgrid((n * nkv + 7) / 8);
+  const int nqb = (T + 63) / 64, maxqb = (max_t + 63) / 64;
+  AttnSplit sp;
+  sp.ch = kAttnChunk;
+  sp.max_ch = attn_max_chunks(cap);
+  const size_t slots = (size_t)nq * maxqb * sp.max_ch;
+  sp.part_o = reinterpret_cast<float*>(part);
+  sp.part_ml = reinterpret_cast<float2*>(sp.part_o + slots * 64 * hd);
+  sp.counters = reinterpret_cast<int*>(sp.part_ml + slots * 64);
+  int items = 0;  // (query block, key chunk) pairs per head
+  for (int qb = 0; qb < nqb; ++qb) {
+    const int nr = min(64, T - qb * 64);
+    const int nt = (p0 + qb * 64 + nr - 1) / kAttnBK + 1;
+    items += (nt + kAttnChunk - 1) / kAttnChunk;
+  }
+  // counters are indexed [head][block] with this launch's block count
+  const dim3 grid(items, nq), sgrid((n * nkv + 7) / 8);
   if (hd == 64) {
     kv_split_kernel<64><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, nkv, rows, kvs);
     attn_prefill_tc_kernel<64, kAttnBK><<<grid, 128, attn_prefill_tc_smem(64), s>>>(
-        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, err, wait_ns);
+        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, sp, err, wait_ns);
   } else if (hd == 128) {
     kv_split_kernel<128><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, nkv, rows, kvs);
     attn_prefill_tc_kernel<128, kAttnBK><<<grid, 128, attn_prefill_tc_smem(128), s>>>(
-        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, err, wait_ns);
+        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, sp, err, wait_ns);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -153,10 +153,12 @@ cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int 
                                    const float2* rope, float* Q, float* kc, float* vc, int cap,
                                    cudaStream_t s);
 // kvs: scratch of kv_split_bytes(nkv, rows, hd) with rows = kv_split_rows(cap), zeroed once
+// part: scratch of attn_part_bytes(nq, max_t, cap, hd), zeroed once (T <= max_t)
 cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
                                 int T, int nq, int nkv, int hd, uint16_t* kvs, int rows,
-                                uint16_t* o_hi, uint16_t* o_lo, int* err, uint64_t wait_ns,
-                                cudaStream_t s);
+                                uint16_t* o_hi, uint16_t* o_lo, void* part, int max_t,
+                                int* err, uint64_t wait_ns, cudaStream_t s);
+size_t attn_part_bytes(int nq, int max_t, int max_ctx, int hd);
 size_t kv_split_bytes(int nkv, int rows, int hd);
 int kv_split_rows(int max_ctx);
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
