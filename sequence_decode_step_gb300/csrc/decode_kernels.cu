@@ -376,7 +376,6 @@ __device__ __forceinline__ void rope_cs(const float2* row, int pos, int j, int h
 template <int HD>
 __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
   constexpr int TK = kAttnTK, NS = kAttnNS, GQM = kAttnGQ, EPL = HD / 32;
-  constexpr int OUTS = (GQM * HD + 255) / 256;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* q_s = reinterpret_cast<float*>(smem + 64);  // [GQM][HD]
@@ -478,9 +477,11 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) qr[h][e] = (h < GQ) ? q_s[h * HD + lane * EPL + e] : 0.f;
 
-  float oacc[OUTS];
+  // P.V and outputs: a thread owns 4 adjacent output dims of one head
+  constexpr int OUT4 = (GQM * HD / 4 + 255) / 256;
+  float4 oacc[OUT4];
 #pragma unroll
-  for (int i = 0; i < OUTS; ++i) oacc[i] = 0.f;
+  for (int i = 0; i < OUT4; ++i) oacc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 
   bool failed = false;
   int it = 0;
@@ -503,20 +504,26 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncthreads();
     }
-    for (int j = warp; j < nk; j += 8) {
-      float kv[EPL];
+    {  // scores: warp w takes keys 4w..4w+3 for every head; one transposing reduction of
+       // the 32 (key, head) partials leaves (key lane / 8, head lane % 8) on each lane
+      float v[4 * GQM];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) kv[e] = Ks[j * HD + lane * EPL + e];
+      for (int k = 0; k < 4; ++k) {
+        const int j = warp * 4 + k;
+        float kv[EPL];
 #pragma unroll
-      for (int h = 0; h < GQM; ++h) {
-        if (h < GQ) {
+        for (int e = 0; e < EPL; ++e) kv[e] = j < nk ? Ks[j * HD + lane * EPL + e] : 0.f;
+#pragma unroll
+        for (int h = 0; h < GQM; ++h) {
           float p = 0.f;
 #pragma unroll
           for (int e = 0; e < EPL; ++e) p = fmaf(qr[h][e], kv[e], p);
-          p = warp_sum(p);
-          if (lane == 0) sc_s[h * TK + j] = p;
+          v[k * GQM + h] = p;
         }
       }
+      const float sc = rows_reduce<4 * GQM>(v, lane);
+      const int j = warp * 4 + lane / GQM, h = lane % GQM;
+      if (j < nk && h < GQ) sc_s[h * TK + j] = sc;
     }
     __syncthreads();
     for (int h = warp; h < GQ; h += 8) {
@@ -537,13 +544,21 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
     }
     __syncthreads();
 #pragma unroll
-    for (int oi = 0; oi < OUTS; ++oi) {
+    for (int oi = 0; oi < OUT4; ++oi) {
       const int idx = tid + oi * 256;
-      if (idx < GQ * HD) {
-        const int h = idx / HD, d = idx % HD;
-        float acc = oacc[oi] * al_s[h];
+      if (idx < GQ * HD / 4) {
+        const int h = idx / (HD / 4), d4 = (idx % (HD / 4)) * 4;
+        const float al = al_s[h];
+        float4 acc = make_float4(oacc[oi].x * al, oacc[oi].y * al, oacc[oi].z * al, oacc[oi].w * al);
         const float* pr = p_s + h * TK;
-        for (int j = 0; j < nk; ++j) acc = fmaf(pr[j], Vs[j * HD + d], acc);
+        for (int j = 0; j < nk; ++j) {
+          const float pj = pr[j];
+          const float4 v4 = *reinterpret_cast<const float4*>(Vs + j * HD + d4);
+          acc.x = fmaf(pj, v4.x, acc.x);
+          acc.y = fmaf(pj, v4.y, acc.y);
+          acc.z = fmaf(pj, v4.z, acc.z);
+          acc.w = fmaf(pj, v4.w, acc.w);
+        }
         oacc[oi] = acc;
       }
     }
@@ -569,21 +584,24 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
 
   if (nsplit == 1) {
 #pragma unroll
-    for (int oi = 0; oi < OUTS; ++oi) {
+    for (int oi = 0; oi < OUT4; ++oi) {
       const int idx = tid + oi * 256;
-      if (idx < GQ * HD) {
-        const int h = idx / HD, d = idx % HD;
-        a.out[(size_t)(g * GQ + h) * HD + d] = oacc[oi] / ml_s[2 * h + 1];
+      if (idx < GQ * HD / 4) {
+        const int h = idx / (HD / 4), d4 = (idx % (HD / 4)) * 4;
+        const float inv = 1.0f / ml_s[2 * h + 1];
+        *reinterpret_cast<float4*>(a.out + (size_t)(g * GQ + h) * HD + d4) =
+            make_float4(oacc[oi].x * inv, oacc[oi].y * inv, oacc[oi].z * inv, oacc[oi].w * inv);
       }
     }
     return;
   }
 #pragma unroll
-  for (int oi = 0; oi < OUTS; ++oi) {
+  for (int oi = 0; oi < OUT4; ++oi) {
     const int idx = tid + oi * 256;
-    if (idx < GQ * HD) {
-      const int h = idx / HD, d = idx % HD;
-      a.part_o[((size_t)(g * GQ + h) * a.nsplit_max + s) * HD + d] = oacc[oi];
+    if (idx < GQ * HD / 4) {
+      const int h = idx / (HD / 4), d4 = (idx % (HD / 4)) * 4;
+      *reinterpret_cast<float4*>(a.part_o + ((size_t)(g * GQ + h) * a.nsplit_max + s) * HD + d4) =
+          oacc[oi];
     }
   }
   if (tid < GQ) {
@@ -600,23 +618,53 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
   __syncthreads();
   if (!*flag_s) return;
   __threadfence();
-#pragma unroll
-  for (int oi = 0; oi < OUTS; ++oi) {
-    const int idx = tid + oi * 256;
-    if (idx < GQ * HD) {
-      const int h = idx / HD, d = idx % HD;
-      const size_t base = (size_t)(g * GQ + h) * a.nsplit_max;
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(a.part_ml + (base + s2) * 2));
-      float num = 0.f, den = 0.f;
-      for (int s2 = 0; s2 < nsplit; ++s2) {
-        const float w = expf(__ldcg(a.part_ml + (base + s2) * 2) - M);
-        num = fmaf(w, __ldcg(a.part_o + (base + s2) * HD + d), num);
-        den = fmaf(w, __ldcg(a.part_ml + (base + s2) * 2 + 1), den);
-      }
-      a.out[(size_t)(g * GQ + h) * HD + d] = num / den;
+  // Combine (last split to arrive): per head, weights exp(m_s - M) and their l-weighted
+  // sum (a warp per head), then each thread sums 4 output dims over the splits in
+  // order, 16 float4 loads in flight at a time.
+  float* wsm = stage0;  // [GQ][nsplit] (the tile stages are free now)
+  float* den_s = wsm + GQM * a.nsplit_max;
+  for (int h = warp; h < GQ; h += 8) {
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + (size_t)(g * GQ + h) * a.nsplit_max;
+    float m = -INFINITY;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) m = fmaxf(m, __ldcg(ml + s2).x);
+    m = warp_max(m);
+    float dsum = 0.f;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) {
+      const float2 v2 = __ldcg(ml + s2);
+      const float w = expf(v2.x - m);
+      wsm[h * nsplit + s2] = w;
+      dsum = fmaf(w, v2.y, dsum);
     }
+    dsum = warp_sum(dsum);
+    if (lane == 0) den_s[h] = dsum;
   }
+  __syncthreads();
+  for (int idx = tid; idx < GQ * HD / 4; idx += 256) {
+    const int h = idx / (HD / 4), d4 = (idx % (HD / 4)) * 4;
+    const float* po = a.part_o + (size_t)(g * GQ + h) * a.nsplit_max * HD + d4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit; s0 += 16) {
+      float4 pv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        pv[j] = s0 + j < nsplit ? __ldcg(reinterpret_cast<const float4*>(po + (size_t)(s0 + j) * HD))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (s0 + j < nsplit) {
+          const float w = wsm[h * nsplit + s0 + j];
+          acc.x = fmaf(w, pv[j].x, acc.x);
+          acc.y = fmaf(w, pv[j].y, acc.y);
+          acc.z = fmaf(w, pv[j].z, acc.z);
+          acc.w = fmaf(w, pv[j].w, acc.w);
+        }
+      }
+    }
+    const float inv = 1.0f / den_s[h];
+    *reinterpret_cast<float4*>(a.out + (size_t)(g * GQ + h) * HD + d4) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+  __syncthreads();
   if (tid == 0) a.counters[g] = 0;
 }
 

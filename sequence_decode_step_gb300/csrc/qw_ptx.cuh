@@ -106,6 +106,35 @@ __device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8], float 
 }
 
 
+// Sum NR (a power of two) per-lane partials over the warp with a transposing
+// butterfly: each halving step exchanges half of the remaining values, so NR rows
+// cost NR - 1 + 5 - log2(NR) shuffles instead of 5 NR. Afterwards lanes
+// [r * 32/NR, (r + 1) * 32/NR) hold the full sum of row r. Fixed order.
+template <int NR>
+__device__ __forceinline__ float rows_reduce(const float (&v)[NR], int lane) {
+  float cur[NR];
+#pragma unroll
+  for (int i = 0; i < NR; ++i) cur[i] = v[i];
+#pragma unroll
+  for (int s = 0, n = NR, bit = 16; s < 5; ++s, bit >>= 1) {
+    if (n > 1) {
+      const bool up = lane & bit;
+      const int h = n / 2;
+#pragma unroll
+      for (int i = 0; i < (NR > 1 ? NR / 2 : 1); ++i) {
+        if (i < h) {
+          const float keep = up ? cur[i + h] : cur[i], send = up ? cur[i] : cur[i + h];
+          cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+      }
+      n = h;
+    } else {
+      cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], bit);
+    }
+  }
+  return cur[0];
+}
+
 // Argmax order: larger value wins, equal values go to the lower index.
 __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
