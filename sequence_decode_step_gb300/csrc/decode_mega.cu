@@ -82,30 +82,45 @@ struct Slice {
   int u0, u1;
   uint32_t unit_bytes;
   int per_chunk;  // units per ring stage
+  int n_chunks;   // ring stages the slice takes
 };
 
+// Units a warp takes per GEMV iteration in each phase (rows per iteration / rows
+// per unit); a ring stage holds a whole number of them when it can.
+__host__ __device__ constexpr int phase_upi(int kind) {
+  return kind == K_QKV ? 4 : kind == K_GU ? 4 : kind == K_LM ? 8 : 2;
+}
+
+// 32-bit arithmetic throughout: n_units * G stays far below 2^31 for every shape
+// the kernel takes (checked on the host).
 __device__ __forceinline__ Slice make_slice(const uint8_t* w, int n_units, uint32_t unit_bytes,
-                                            int b, int G) {
+                                            int upi, int b, int G) {
   Slice s;
   s.base = w;
-  s.u0 = (int)(((long long)n_units * b) / G);
-  s.u1 = (int)(((long long)n_units * (b + 1)) / G);
+  s.u0 = (int)(((uint32_t)n_units * (uint32_t)b) / (uint32_t)G);
+  s.u1 = (int)(((uint32_t)n_units * (uint32_t)(b + 1)) / (uint32_t)G);
   s.unit_bytes = unit_bytes;
   int pc = (int)(kStage / unit_bytes);
-  s.per_chunk = pc < 1 ? 1 : pc;
+  pc = pc >= upi ? pc / upi * upi : (pc < 1 ? 1 : pc);
+  s.per_chunk = pc;
+  s.n_chunks = (s.u1 - s.u0 + pc - 1) / pc;
   return s;
 }
 
-__device__ __forceinline__ Slice phase_slice(const MegaArgs& a, int kind, const LayerDev& L, int b,
-                                             int G) {
+// Geometry of a phase (its base is set per layer by the producer; the consumers
+// never read it).
+__device__ __forceinline__ Slice phase_slice(const MegaArgs& a, int kind, int b, int G) {
   const int qd = a.nq * a.hd, kd = a.nkv * a.hd;
   switch (kind) {
-    case K_QKV: return make_slice(L.qkv, qd + 2 * kd, (uint32_t)a.H * 2, b, G);
-    case K_O: return make_slice(L.o, a.H, (uint32_t)qd * 2, b, G);
-    case K_GU: return make_slice(L.gateup, a.I, (uint32_t)a.H * 4, b, G);
-    case K_DOWN: return make_slice(L.down, a.H, (uint32_t)a.I * 2, b, G);
-    default: return make_slice(a.lm_head, a.V, (uint32_t)a.H * 2, b, G);
+    case K_QKV: return make_slice(nullptr, qd + 2 * kd, (uint32_t)a.H * 2, phase_upi(K_QKV), b, G);
+    case K_O: return make_slice(nullptr, a.H, (uint32_t)qd * 2, phase_upi(K_O), b, G);
+    case K_GU: return make_slice(nullptr, a.I, (uint32_t)a.H * 4, phase_upi(K_GU), b, G);
+    case K_DOWN: return make_slice(nullptr, a.H, (uint32_t)a.I * 2, phase_upi(K_DOWN), b, G);
+    default: return make_slice(a.lm_head, a.V, (uint32_t)a.H * 2, phase_upi(K_LM), b, G);
   }
+}
+__device__ __forceinline__ const uint8_t* phase_base(int kind, const LayerDev& L) {
+  return kind == K_QKV ? L.qkv : kind == K_O ? L.o : kind == K_GU ? L.gateup : L.down;
 }
 
 // Attention work of CTA b (all derived from the device position): KV head g and
@@ -488,65 +503,66 @@ __device__ __forceinline__ void prewait(const MegaArgs& a, Smem& S, int c, int n
   for (int j = 0; j < n; ++j) ring_wait(a, &S.full[(c + j) % kNS], (uint32_t)(((c + j) / kNS) & 1), abort);
 }
 
-// Consume the chunks of one row-streamed phase (units [u0, u1) of `unit_bytes`
-// each, `per_chunk` to a ring stage); chunk counter c advances by the phase's
-// chunks. The epilogue, fixed at compile time:
+// Consume the chunks of one row-streamed phase (slice units [u0, u1) of
+// `unit_bytes` each, `per_chunk` to a ring stage); chunk counter c advances by the
+// phase's chunks. The epilogue, fixed at compile time:
 //   EPI_STORE    y[u] = w_u . xs (+ bias[u])                     (tagged words)
 //   EPI_RESIDUAL y[u] = y[u] + w_u . xs  (own rows; also to cap)   (tagged words)
 //   EPI_SWIGLU   y[u] = silu(g_u . xs) * (up_u . xs)             (tagged words)
 //   EPI_LOGITS   logits[u] = w_u . xs, running greedy best       (plain f32)
 // A warp takes NR rows per iteration (NR / 2 gate/up units for SwiGLU). When the
-// phase fits in the ring its chunks were waited for by prewait() and the warps
-// take units across chunks; otherwise the chunks are taken one at a time.
+// phase fits in the ring its chunks were waited for by prewait() and released
+// together at the end; otherwise each warp waits for and releases them one at a time.
 template <int MAXC, int EPI, int NR>
 __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
-                                           int u0, int u1, uint32_t unit_bytes, int per_chunk,
-                                           int K, uint64_t* ty, uint32_t tag,
+                                           const Slice& sl, int K, uint64_t* ty, uint32_t tag,
                                            const uint16_t* bias, float* cap, Best& best,
                                            bool& abort) {
   constexpr int XR = MAXC > 0 ? MAXC : 1;
   constexpr int RPU = EPI == EPI_SWIGLU ? 2 : 1;  // rows per unit
-  constexpr int UPI = NR / RPU;                   // units per warp iteration
+  constexpr int UPI = NR / RPU;                   // units per warp iteration (one item)
   constexpr int SH = 32 / NR;                     // lanes per reduced row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float xr[XR][8];
   if (MAXC > 0) x_regs<XR>(S, K, xr);
-  const uint32_t row_bytes = unit_bytes / RPU;
-  const int n_units = u1 - u0;
-  const int n_chunks = (n_units + per_chunk - 1) / per_chunk;
+  const int pc = sl.per_chunk, n_units = sl.u1 - sl.u0, n_chunks = sl.n_chunks;
+  const uint32_t unit_bytes = sl.unit_bytes, row_bytes = unit_bytes / RPU;
   const bool whole = EPI != EPI_LOGITS && n_chunks <= kNS;  // waited for by prewait()
-  const int group = whole ? n_chunks : 1;
-  for (int g0 = 0; g0 < n_chunks && !abort; g0 += group) {
-    const int gn = min(group, n_chunks - g0);
+  // Items of UPI units are dealt to the warps round-robin, the count running on
+  // from stage to stage; an item never straddles two stages (a stage holds a
+  // whole number of items, or one partial item), so a row's address is its
+  // stage's base plus a multiple of the unit size: no division per row.
+  int first = warp;  // this warp's first item in the current stage
+  for (int j = 0; j < n_chunks && !abort; ++j) {
     if (!whole) {
-      const bool ok = ring_wait(a, &S.full[(c + g0) % kNS], (uint32_t)(((c + g0) / kNS) & 1), abort);
+      const bool ok = ring_wait(a, &S.full[(c + j) % kNS], (uint32_t)(((c + j) / kNS) & 1), abort);
       if (__any_sync(0xffffffffu, !ok)) {  // the whole warp gives up together
         abort = true;
         break;
       }
     }
-    const int ua = g0 * per_chunk, ub = min(n_units, (g0 + gn) * per_chunk);
-    for (int t = ua + UPI * warp; t < ub; t += UPI * kConsumers) {
+    const int cu0 = j * pc, cn = min(pc, n_units - cu0);  // units [cu0, cu0 + cn) of the slice
+    const uint8_t* stage = ring + (size_t)((c + j) % kNS) * kStage;
+    const int items = (cn + UPI - 1) / UPI;
+    int k = first;
+    for (; k < items; k += kConsumers) {
+      const int t = k * UPI;
       const uint8_t* w[NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const int tu = min(t + r / RPU, ub - 1);  // rows past the slice reuse its last row
-        const int j = tu / per_chunk;
-        w[r] = ring + (size_t)((c + j) % kNS) * kStage + (size_t)(tu - j * per_chunk) * unit_bytes +
-               (r % RPU) * row_bytes;
-      }
+      for (int r = 0; r < NR; ++r)  // rows past the stage's units reuse its last unit
+        w[r] = stage + (size_t)min(t + r / RPU, cn - 1) * unit_bytes + (r % RPU) * row_bytes;
       float v[NR];
       dotn<NR, MAXC>(w, K, xr, S.xs, v);
       const float sum = rows_reduce<NR>(v, lane);
       if constexpr (EPI == EPI_SWIGLU) {
         const float up = __shfl_down_sync(0xffffffffu, sum, SH);  // row 2k+1 onto row 2k
-        if (lane % (2 * SH) == 0) {
-          const int iu = t + lane / (2 * SH);
-          if (iu < ub) st_tagged(ty + u0 + iu, sum / (1.0f + expf(-sum)) * up, tag);
-        }
-      } else if (lane % SH == 0) {
-        const int iu = t + lane / SH, uu = u0 + iu;
-        if (iu < ub) {
+        const int tl = t + lane / (2 * SH);
+        if (lane % (2 * SH) == 0 && tl < cn)
+          st_tagged(ty + sl.u0 + cu0 + tl, sum / (1.0f + expf(-sum)) * up, tag);
+      } else {
+        const int tl = t + lane / SH;
+        if (lane % SH == 0 && tl < cn) {
+          const int iu = cu0 + tl, uu = sl.u0 + iu;
           if constexpr (EPI == EPI_STORE) {
             st_tagged(ty + uu,
                       sum + (bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(bias[uu])) : 0.f), tag);
@@ -562,9 +578,16 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
         }
       }
     }
+    first = k - items;
+    if (!whole) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[(c + j) % kNS]);
+    }
+  }
+  if (whole && !abort) {
     __syncwarp();
     if (lane == 0)
-      for (int j = 0; j < gn; ++j) mbar_arrive(&S.empty[(c + g0 + j) % kNS]);
+      for (int j = 0; j < n_chunks; ++j) mbar_arrive(&S.empty[(c + j) % kNS]);
   }
   c += n_chunks;
 }
@@ -578,17 +601,13 @@ __device__ __forceinline__ void gemv(const MegaArgs& a, uint8_t* ring, Smem& S, 
                                      const Slice& sl, int K, uint64_t* ty, uint32_t tag,
                                      const uint16_t* bias, float* cap, Best& best, bool& abort) {
   if (X == 1 || (X == 2 && K <= 1024))
-    gemv_phase<4, EPI, NR>(a, ring, S, c, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty, tag,
-                           bias, cap, best, abort);
+    gemv_phase<4, EPI, NR>(a, ring, S, c, sl, K, ty, tag, bias, cap, best, abort);
   else
-    gemv_phase<0, EPI, NR>(a, ring, S, c, sl.u0, sl.u1, sl.unit_bytes, sl.per_chunk, K, ty, tag,
-                           bias, cap, best, abort);
+    gemv_phase<0, EPI, NR>(a, ring, S, c, sl, K, ty, tag, bias, cap, best, abort);
 }
 
 // Chunks of a slice (the producer streams them in this count).
-__device__ __forceinline__ int slice_chunks(const Slice& sl) {
-  return (sl.u1 - sl.u0 + sl.per_chunk - 1) / sl.per_chunk;
-}
+__device__ __forceinline__ int slice_chunks(const Slice& sl) { return sl.n_chunks; }
 
 // Split-K attention of CTA b: QK-norm + RoPE of its group's queries (and of the
 // new key when its split holds pos), tiles of 32 keys from the ring, online
@@ -934,21 +953,28 @@ __device__ void produce(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
   };
   const Split sp = attn_split(a, pos, b);
   const size_t kv_layer = (size_t)a.nkv * a.cap * a.hd;
+  const Slice geo[5] = {phase_slice(a, K_QKV, b, G), Slice{}, phase_slice(a, K_O, b, G),
+                        phase_slice(a, K_GU, b, G), phase_slice(a, K_DOWN, b, G)};
+  auto layer_slice = [&](int kind, const LayerDev& Ld) {
+    Slice sl = geo[kind];
+    sl.base = phase_base(kind, Ld);
+    return sl;
+  };
   bool ok = true;
   for (int l = 0; l < a.L && ok; ++l) {
     const LayerDev Ld = a.layers[l];
-    ok = stream_slice(phase_slice(a, K_QKV, Ld, b, G));
+    ok = stream_slice(layer_slice(K_QKV, Ld));
     const float* kc = a.k_cache + (size_t)l * kv_layer + (size_t)sp.g * a.cap * a.hd;
     const float* vc = a.v_cache + (size_t)l * kv_layer + (size_t)sp.g * a.cap * a.hd;
     for (int t0 = sp.k0; ok && t0 < sp.k1; t0 += kTK) {
       const uint32_t n = (uint32_t)min(kTK, sp.k1 - t0) * a.hd * 4;
       ok = issue(kc + (size_t)t0 * a.hd, n, vc + (size_t)t0 * a.hd, n, (uint32_t)kTK * a.hd * 4);
     }
-    ok = ok && stream_slice(phase_slice(a, K_O, Ld, b, G));
-    ok = ok && stream_slice(phase_slice(a, K_GU, Ld, b, G));
-    ok = ok && stream_slice(phase_slice(a, K_DOWN, Ld, b, G));
+    ok = ok && stream_slice(layer_slice(K_O, Ld));
+    ok = ok && stream_slice(layer_slice(K_GU, Ld));
+    ok = ok && stream_slice(layer_slice(K_DOWN, Ld));
   }
-  if (ok) stream_slice(phase_slice(a, K_LM, LayerDev{}, b, G));
+  if (ok) stream_slice(phase_slice(a, K_LM, b, G));
   // Leave only once every copy issued into this CTA's shared memory has landed.
   for (int cc = c > kNS ? c - kNS : 0; cc < c; ++cc)
     mbar_wait(&S.full[cc % kNS], (uint32_t)((cc / kNS) & 1), kDrainNs);
@@ -1036,13 +1062,14 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
   }
   const Split sp = attn_split(a, pos, b);
   Best best{-INFINITY, 0x7fffffff, 0};
+  // the phases' slices are the same in every layer
+  const Slice qs = phase_slice(a, K_QKV, b, G), os = phase_slice(a, K_O, b, G);
+  const Slice gs = phase_slice(a, K_GU, b, G), ds = phase_slice(a, K_DOWN, b, G);
   for (int l = 0; l < a.L; ++l) {
     const LayerDev Ld = a.layers[l];  // one batch of loads per layer, kept in registers
     const uint32_t tq = tag0 + 5u * l, ta = tq + 1u, to = tq + 2u, tg = tq + 3u, td = tq + 4u;
     // fused QKV; layer 0 gathers the embedding row itself and seeds the residual rows it owns
-    const Slice qs = phase_slice(a, K_QKV, Ld, b, G);
     if (l == 0) {
-      const Slice os = phase_slice(a, K_O, Ld, b, G);
       const uint16_t* e = a.embed + (size_t)tok * a.H;
       for (int r = os.u0 + tid; r < os.u1; r += kConsumers * 32) st_tagged(a.x + r, bf16f(e[r]), 0u);
       if (a.cap_emb && b == 0)
@@ -1060,7 +1087,6 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       else attn_phase<128>(a, ring, S, c, l, pos, sp, Ld, tq, ta, abort);
     }
     // o_proj + residual
-    const Slice os = phase_slice(a, K_O, Ld, b, G);
     if (os.u1 > os.u0) {
       prewait(a, S, c, slice_chunks(os), abort);
       load_input(a, S, a.attn_o, ta, qd, nullptr, false, 0, a.x + os.u0, nullptr,
@@ -1068,14 +1094,12 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       gemv<EPI_RESIDUAL, XQ, 2>(a, ring, S, c, os, qd, a.x, to, nullptr, nullptr, best, abort);
     }
     // gate/up with SwiGLU
-    const Slice gs = phase_slice(a, K_GU, Ld, b, G);
     if (gs.u1 > gs.u0) {
       prewait(a, S, c, slice_chunks(gs), abort);
       load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0, abort);
       gemv<EPI_SWIGLU, XH, 8>(a, ring, S, c, gs, a.H, a.mlp, tg, nullptr, nullptr, best, abort);
     }
     // down + residual (block-0 checkpoint)
-    const Slice ds = phase_slice(a, K_DOWN, Ld, b, G);
     if (ds.u1 > ds.u0) {
       prewait(a, S, c, slice_chunks(ds), abort);
       load_input(a, S, a.mlp, tg, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
@@ -1086,13 +1110,13 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     }
   }
   // final RMSNorm + LM head + greedy argmax
-  const Slice ls = phase_slice(a, K_LM, LayerDev{}, b, G);
+  const Slice ls = phase_slice(a, K_LM, b, G);
   if (ls.u1 > ls.u0 || (a.cap_final && b == 0)) {
     load_input(a, S, a.x, tag0 + 5u * (a.L - 1) + 4u, a.H, a.final_norm, false, 0, nullptr,
                nullptr, 0, abort);
     if (a.cap_final && b == 0)
       for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[xs_pos(r)];
-    gemv<EPI_LOGITS, XH, 2>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
+    gemv<EPI_LOGITS, XH, 8>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
   }
   // each lane holding rows kept its own best: merge them onto lane 0 (ties to the lower index)
   best.nan = __any_sync(0xffffffffu, best.nan != 0) ? 1 : 0;

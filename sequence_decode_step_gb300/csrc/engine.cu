@@ -249,7 +249,8 @@ static int alloc_state(qw_handle* h) {
   h->nsplit_max = std::max(1, h->num_sms / c.n_kv_heads);
   h->mega_ok = c.weight_format == QW_WEIGHTS_BF16 &&
                mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim, c.head_dim,
-                              c.n_q_heads / c.n_kv_heads, c.n_layers);
+                              c.n_q_heads / c.n_kv_heads, c.n_layers) &&
+               (int64_t)c.vocab * h->num_sms < (int64_t)1 << 31;  // 32-bit slice arithmetic
   h->use_mega = h->mega_ok;
   h->w4 = c.weight_format == QW_WEIGHTS_INT4_G128;
   h->lm_w4 = h->w4 && !c.tie_word_embeddings;
