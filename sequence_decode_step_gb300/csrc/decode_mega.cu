@@ -253,25 +253,33 @@ __device__ __forceinline__ void poll_bound(const MegaArgs& a, uint32_t n, uint64
   }
 }
 
-// Per lane: words src[lane + 32 e], e < N, once all carry `tag`.
+// Per lane: words src[lane + 32 e], e < N, once all carry `tag`; with src2, the
+// words src2[lane + 32 e] as well, polled in the same rounds (one L2 round trip
+// for both rows when they are there).
 template <int N>
-__device__ __forceinline__ void poll_row(const MegaArgs& a, const uint64_t* src, uint32_t tag,
-                                         float (&v)[N], bool& abort) {
+__device__ __forceinline__ void poll_row(const MegaArgs& a, const uint64_t* src,
+                                         const uint64_t* src2, uint32_t tag, float (&v)[N],
+                                         float (&v2)[N], bool& abort) {
   const int lane = threadIdx.x & 31;
-  uint64_t w[N];
-  unsigned pend = (1u << N) - 1u;
+  uint64_t w[2 * N];
+#pragma unroll
+  for (int e = 0; e < 2 * N; ++e) w[e] = 0;
+  unsigned pend = src2 != nullptr ? (1u << (2 * N)) - 1u : (1u << N) - 1u;
   uint64_t t0 = 0;
   for (uint32_t n = 1; pend && !abort; ++n) {
 #pragma unroll
-    for (int e = 0; e < N; ++e)
-      if ((pend >> e) & 1u) w[e] = ld_word(src + lane + 32 * e);
+    for (int e = 0; e < 2 * N; ++e)
+      if ((pend >> e) & 1u) w[e] = ld_word((e < N ? src : src2) + lane + 32 * (e % N));
 #pragma unroll
-    for (int e = 0; e < N; ++e)
+    for (int e = 0; e < 2 * N; ++e)
       if (((pend >> e) & 1u) && word_tag(w[e]) == tag) pend &= ~(1u << e);
     if (pend) poll_bound(a, n, t0, abort);
   }
 #pragma unroll
-  for (int e = 0; e < N; ++e) v[e] = abort ? 0.f : word_value(w[e]);
+  for (int e = 0; e < N; ++e) {
+    v[e] = abort ? 0.f : word_value(w[e]);
+    v2[e] = abort ? 0.f : word_value(w[N + e]);
+  }
 }
 
 // Position of input element k in xs: within each 256-wide chunk, the eight
@@ -652,8 +660,10 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     for (int e = 0; e < EPL; ++e) gv[e] = gain != nullptr ? bf16f(gain[lane + 32 * e]) : 1.f;
 #pragma unroll
     for (int e = 0; e < EPL / 2; ++e) csv[e] = rrow[lane + 32 * e];
-    float v[EPL];
-    poll_row<EPL>(a, src, tag_in, v, abort);
+    // the key row's warp polls the value row in the same rounds
+    float v[EPL], vv[EPL];
+    poll_row<EPL>(a, src, isq ? nullptr : a.qkv + (size_t)(a.nq + a.nkv + g) * HD, tag_in, v, vv,
+                  abort);
     if (gain != nullptr) {
       float sq = 0.f;
 #pragma unroll
@@ -674,8 +684,6 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
 #pragma unroll
       for (int e = 0; e < EPL; ++e) S.q_s[hh * HD + lane + 32 * e] = v[e] * scale;
     } else {
-      float vv[EPL];
-      poll_row<EPL>(a, a.qkv + (size_t)(a.nq + a.nkv + g) * HD, tag_in, vv, abort);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
         const int d = lane + 32 * e;
@@ -701,10 +709,16 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
   constexpr int DPL = HD / 32;
   float* sc = S.pml_s;                      // [GQ][pt * kTK]
   float* pp = S.pml_s + kGQ * kPass * kTK;  // [GQ][pt * kTK]
-  float* part = S.xs;                       // [pt][GQ][HD]
+  float* part = S.xs;                       // [nt * KP][GQ][HD]
   for (int p0 = sp.k0; p0 < sp.k1; p0 += stride) {
     const int nkp = min(stride, sp.k1 - p0);
     const int nt = (nkp + kTK - 1) / kTK;
+    // P.V splits each tile into KP = 2^kpl parts (up to 4) while the parts still
+    // go one per warp and their partials fit in xs
+    int kpl = 0;
+    while (kpl < 2 && nt * (2 << kpl) <= kConsumers && nt * (2 << kpl) * GQ * HD <= kMaxC * 256)
+      ++kpl;
+    const int KP = 1 << kpl;
     if (p0 != sp.k0)
       for (int t = 0; t < nt; ++t)
         ring_wait(a, &S.full[(c + t) % kNS], (uint32_t)(((c + t) / kNS) & 1), abort);
@@ -722,21 +736,30 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         csync();
       }
-      // scores, two heads and eight keys at a time: lane partials over its DPL dims,
-      // then a transposing reduction leaves key r of the group on lanes 4r .. 4r+3
-      for (int t = warp; t < nt; t += kConsumers) {
+      // scores, two heads and eight keys at a time, the (tile, 8-key group) pairs
+      // dealt round-robin to the warps: lane partials over its DPL dims, then a
+      // transposing reduction leaves key r of the group on lanes 4r .. 4r+3
+      constexpr int GPT = kTK / 8;  // 8-key groups per tile
+      for (int gi = warp; gi < nt * GPT; gi += kConsumers) {
+        const int t = gi / GPT, j0 = (gi % GPT) * 8;
         const float* Kt = kt(t) + lane * DPL;
         const int nk = min(kTK, nkp - t * kTK);
         for (int h0 = 0; h0 < GQ; h0 += 2) {
           const bool two = h0 + 1 < GQ;
+          if (j0 >= nk) {  // the group lies wholly past the keys
+            if (lane < 8) {
+              sc[h0 * stride + t * kTK + j0 + lane] = -INFINITY;
+              if (two) sc[(h0 + 1) * stride + t * kTK + j0 + lane] = -INFINITY;
+            }
+            continue;
+          }
           float q0[DPL], q1[DPL];
 #pragma unroll
           for (int e = 0; e < DPL; ++e) {
             q0[e] = S.q_s[h0 * HD + lane * DPL + e];
             q1[e] = two ? S.q_s[(h0 + 1) * HD + lane * DPL + e] : 0.f;
           }
-#pragma unroll 1
-          for (int j0 = 0; j0 < kTK; j0 += 8) {
+          {
             float s0[8], s1[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -799,9 +822,11 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
         }
       }
       csync();
-      // P.V of one tile, two heads at a time: lane holds DPL adjacent output dims
-      for (int t = warp; t < nt; t += kConsumers) {
-        const int nk = min(kTK, nkp - t * kTK);
+      // P.V of one tile part (kTK / KP keys), two heads at a time, the parts dealt
+      // round-robin to the warps: lane holds DPL adjacent output dims
+      for (int i = warp; i < nt * KP; i += kConsumers) {
+        const int t = i >> kpl, ja = (i & (KP - 1)) * (kTK >> kpl);
+        const int jb = min(min(kTK, nkp - t * kTK), ja + (kTK >> kpl));
         const float* Vt = kt(t) + kTK * HD + lane * DPL;
         for (int h0 = 0; h0 < GQ; h0 += 2) {
           const bool two = h0 + 1 < GQ;
@@ -810,7 +835,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
           float c0[DPL], c1[DPL];
 #pragma unroll
           for (int e = 0; e < DPL; ++e) c0[e] = c1[e] = 0.f;
-          for (int j = 0; j < nk; ++j) {
+          for (int j = ja; j < jb; ++j) {
             float vv[DPL];
             if constexpr (DPL == 4) {
               const float4 v4 = *reinterpret_cast<const float4*>(Vt + j * HD);
@@ -826,11 +851,11 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
               c1[e] = fmaf(pb, vv[e], c1[e]);
             }
           }
-          float* d0 = part + (t * GQ + h0) * HD + lane * DPL;
+          float* d0 = part + (i * GQ + h0) * HD + lane * DPL;
 #pragma unroll
           for (int e = 0; e < DPL; ++e) d0[e] = c0[e];
           if (two) {
-            float* d1 = part + (t * GQ + h0 + 1) * HD + lane * DPL;
+            float* d1 = part + (i * GQ + h0 + 1) * HD + lane * DPL;
 #pragma unroll
             for (int e = 0; e < DPL; ++e) d1[e] = c1[e];
           }
@@ -849,7 +874,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       if (idx < GQ * HD && !abort) {
         const int h = idx / HD, d = idx % HD;
         float acc = oacc[oi] * S.al_s[h];
-        for (int t = 0; t < nt; ++t) acc += part[(t * GQ + h) * HD + d];
+        for (int i = 0; i < nt * KP; ++i) acc += part[(i * GQ + h) * HD + d];
         oacc[oi] = acc;
       }
     }
