@@ -292,14 +292,17 @@ __device__ __forceinline__ int xs_pos(int k) {
 }
 
 // Phase input: xs = v[0, K) once every word carries `tag` (or the embedding row
-// of `tok`), RMS-normalised with gain g when given; also prefetches `n_unit`
+// of `tok`), times the norm gain g when given; returns the RMS factor
+// 1 / sqrt(mean v^2 + eps) (1 without g), which the GEMV applies to each dot
+// product: W (r g.v) = r (W (g.v)), so the factor's block reduction shares the
+// input's one barrier instead of adding a pass over xs. Also prefetches `n_unit`
 // per-unit epilogue values (this CTA's own residual rows, or bias) into unit_s.
 // Every load of a round is issued before any is used: each is an L2 round trip.
 // Out of line: its word pairs in flight would otherwise push the inlined token
 // loop past the register budget (spills go to L2, since shared memory takes
 // nearly all of L1).
 template <int NP>  // (value, tag) word pairs per thread: K <= 2 * NP * kNT
-__device__ __noinline__ void load_input_n(const MegaArgs& a, Smem& S, const uint64_t* v,
+__device__ __noinline__ float load_input_n(const MegaArgs& a, Smem& S, const uint64_t* v,
                                           uint32_t tag, int K, const uint16_t* g, bool from_embed,
                                           int tok, const uint64_t* unit_own,
                                           const uint16_t* unit_bf16, int n_unit, bool& abort) {
@@ -358,58 +361,51 @@ __device__ __noinline__ void load_input_n(const MegaArgs& a, Smem& S, const uint
           pend &= ~(1u << i);
       if (pend) poll_bound(a, n, t0, abort);
     }
-    csync();  // the previous phase's readers of xs / unit_s are done
+    csync();  // the previous phase's readers of xs / unit_s / red are done
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
       const int idx = tid + i * NT;
       if (idx * 2 < K) {
         const float x0 = word_value(w[i][0]), x1 = word_value(w[i][1]);
-        *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = make_float2(x0, x1);
         ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+        const float g0 = g != nullptr ? __uint_as_float(gv[i] << 16) : 1.f;
+        const float g1 = g != nullptr ? __uint_as_float(gv[i] & 0xffff0000u) : 1.f;
+        *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = make_float2(x0 * g0, x1 * g1);
       }
     }
   }
   if (tid < n_unit) S.unit_s[tid] = uv;
   if (g != nullptr) {
-    if (from_embed) {
+    if (from_embed) {  // once per token: the gain goes on in a second pass
       csync();
       for (int k = tid; k < K; k += NT) {
         const float xk = S.xs[xs_pos(k)];
         ss = fmaf(xk, xk, ss);
+        S.xs[xs_pos(k)] = xk * bf16f(g[k]);
       }
     }
     ss = warp_sum(ss);
-    csync();
     if ((tid & 31) == 0) S.red[tid >> 5] = ss;
-    csync();
-    float tot = 0.f;
-#pragma unroll
-    for (int i = 0; i < kConsumers; ++i) tot += S.red[i];
-    const float r = 1.0f / sqrtf(tot / (float)K + a.eps);
-#pragma unroll
-    for (int i = 0; i < NP; ++i) {
-      const int idx = tid + i * NT;
-      if (idx * 2 < K) {
-        float2 x2 = *reinterpret_cast<const float2*>(&S.xs[xs_pos(idx * 2)]);
-        x2.x = x2.x * r * __uint_as_float(gv[i] << 16);
-        x2.y = x2.y * r * __uint_as_float(gv[i] & 0xffff0000u);
-        *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = x2;
-      }
-    }
   }
   abort = csync_or(abort);
+  if (g == nullptr) return 1.f;
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kConsumers; ++i) tot += S.red[i];
+  return 1.0f / sqrtf(tot / (float)K + a.eps);
 }
 
-__device__ __forceinline__ void load_input(const MegaArgs& a, Smem& S, const uint64_t* v,
+__device__ __forceinline__ float load_input(const MegaArgs& a, Smem& S, const uint64_t* v,
                                            uint32_t tag, int K, const uint16_t* g, bool from_embed,
                                            int tok, const uint64_t* unit_own,
                                            const uint16_t* unit_bf16, int n_unit, bool& abort) {
   constexpr int NP_1K = (1024 + 2 * kNT - 1) / (2 * kNT);      // pairs per thread, K <= 1024
   constexpr int NP_MAX = (kMaxC * 256 + 2 * kNT - 1) / (2 * kNT);
   if (K <= 2 * NP_1K * kNT)
-    load_input_n<NP_1K>(a, S, v, tag, K, g, from_embed, tok, unit_own, unit_bf16, n_unit, abort);
-  else
-    load_input_n<NP_MAX>(a, S, v, tag, K, g, from_embed, tok, unit_own, unit_bf16, n_unit, abort);
+    return load_input_n<NP_1K>(a, S, v, tag, K, g, from_embed, tok, unit_own, unit_bf16, n_unit,
+                               abort);
+  return load_input_n<NP_MAX>(a, S, v, tag, K, g, from_embed, tok, unit_own, unit_bf16, n_unit,
+                              abort);
 }
 
 template <int MAXC>
@@ -523,7 +519,8 @@ __device__ __forceinline__ void prewait(const MegaArgs& a, Smem& S, int c, int n
 // together at the end; otherwise each warp waits for and releases them one at a time.
 template <int MAXC, int EPI, int NR>
 __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
-                                           const Slice& sl, int K, uint64_t* ty, uint32_t tag,
+                                           const Slice& sl, int K, float rs, uint64_t* ty,
+                                           uint32_t tag,
                                            const uint16_t* bias, float* cap, Best& best,
                                            bool& abort) {
   constexpr int XR = MAXC > 0 ? MAXC : 1;
@@ -561,7 +558,7 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
         w[r] = stage + (size_t)min(t + r / RPU, cn - 1) * unit_bytes + (r % RPU) * row_bytes;
       float v[NR];
       dotn<NR, MAXC>(w, K, xr, S.xs, v);
-      const float sum = rows_reduce<NR>(v, lane);
+      const float sum = rows_reduce<NR>(v, lane) * rs;  // the input's RMS factor
       if constexpr (EPI == EPI_SWIGLU) {
         const float up = __shfl_down_sync(0xffffffffu, sum, SH);  // row 2k+1 onto row 2k
         const int tl = t + lane / (2 * SH);
@@ -606,12 +603,12 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
 // at run time (both bodies compiled in).
 template <int EPI, int X, int NR>
 __device__ __forceinline__ void gemv(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
-                                     const Slice& sl, int K, uint64_t* ty, uint32_t tag,
+                                     const Slice& sl, int K, float rs, uint64_t* ty, uint32_t tag,
                                      const uint16_t* bias, float* cap, Best& best, bool& abort) {
   if (X == 1 || (X == 2 && K <= 1024))
-    gemv_phase<4, EPI, NR>(a, ring, S, c, sl, K, ty, tag, bias, cap, best, abort);
+    gemv_phase<4, EPI, NR>(a, ring, S, c, sl, K, rs, ty, tag, bias, cap, best, abort);
   else
-    gemv_phase<0, EPI, NR>(a, ring, S, c, sl, K, ty, tag, bias, cap, best, abort);
+    gemv_phase<0, EPI, NR>(a, ring, S, c, sl, K, rs, ty, tag, bias, cap, best, abort);
 }
 
 // Chunks of a slice (the producer streams them in this count).
@@ -1009,6 +1006,7 @@ __device__ void produce(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
 __device__ void argmax_finalize(const MegaArgs& a, Smem& S, const Best& o, int pos, uint32_t epoch) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, G = gridDim.x;
+  csync();  // every warp has read the LM head input's RMS factor out of red
   if (lane == 0) {
     S.red[warp] = o.nan ? __int_as_float(0x7fc00000) : o.v;
     S.redi[warp] = o.i;
@@ -1102,9 +1100,10 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     }
     if (qs.u1 > qs.u0) {
       prewait(a, S, c, slice_chunks(qs), abort);
-      load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
-                 Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr, min(qs.u1 - qs.u0, kUnitPre), abort);
-      gemv<EPI_STORE, XH, 4>(a, ring, S, c, qs, a.H, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
+      const float rn = load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
+                                  Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr,
+                                  min(qs.u1 - qs.u0, kUnitPre), abort);
+      gemv<EPI_STORE, XH, 4>(a, ring, S, c, qs, a.H, rn, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
     }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
@@ -1116,20 +1115,21 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       prewait(a, S, c, slice_chunks(os), abort);
       load_input(a, S, a.attn_o, ta, qd, nullptr, false, 0, a.x + os.u0, nullptr,
                  min(os.u1 - os.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XQ, 2>(a, ring, S, c, os, qd, a.x, to, nullptr, nullptr, best, abort);
+      gemv<EPI_RESIDUAL, XQ, 2>(a, ring, S, c, os, qd, 1.f, a.x, to, nullptr, nullptr, best, abort);
     }
     // gate/up with SwiGLU
     if (gs.u1 > gs.u0) {
       prewait(a, S, c, slice_chunks(gs), abort);
-      load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0, abort);
-      gemv<EPI_SWIGLU, XH, 8>(a, ring, S, c, gs, a.H, a.mlp, tg, nullptr, nullptr, best, abort);
+      const float rn = load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0,
+                                  abort);
+      gemv<EPI_SWIGLU, XH, 8>(a, ring, S, c, gs, a.H, rn, a.mlp, tg, nullptr, nullptr, best, abort);
     }
     // down + residual (block-0 checkpoint)
     if (ds.u1 > ds.u0) {
       prewait(a, S, c, slice_chunks(ds), abort);
       load_input(a, S, a.mlp, tg, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
                  min(ds.u1 - ds.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XI, 2>(a, ring, S, c, ds, a.I, a.x, td, nullptr,
+      gemv<EPI_RESIDUAL, XI, 2>(a, ring, S, c, ds, a.I, 1.f, a.x, td, nullptr,
                          (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr, best,
                          abort);
     }
@@ -1137,11 +1137,12 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
   // final RMSNorm + LM head + greedy argmax
   const Slice ls = phase_slice(a, K_LM, b, G);
   if (ls.u1 > ls.u0 || (a.cap_final && b == 0)) {
-    load_input(a, S, a.x, tag0 + 5u * (a.L - 1) + 4u, a.H, a.final_norm, false, 0, nullptr,
-               nullptr, 0, abort);
+    const float rn = load_input(a, S, a.x, tag0 + 5u * (a.L - 1) + 4u, a.H, a.final_norm, false,
+                                0, nullptr, nullptr, 0, abort);
     if (a.cap_final && b == 0)
-      for (int r = tid; r < a.H; r += kConsumers * 32) a.cap_final[(size_t)pos * a.H + r] = S.xs[xs_pos(r)];
-    gemv<EPI_LOGITS, XH, 8>(a, ring, S, c, ls, a.H, nullptr, 0u, nullptr, nullptr, best, abort);
+      for (int r = tid; r < a.H; r += kConsumers * 32)
+        a.cap_final[(size_t)pos * a.H + r] = S.xs[xs_pos(r)] * rn;
+    gemv<EPI_LOGITS, XH, 8>(a, ring, S, c, ls, a.H, rn, nullptr, 0u, nullptr, nullptr, best, abort);
   }
   // each lane holding rows kept its own best: merge them onto lane 0 (ties to the lower index)
   best.nan = __any_sync(0xffffffffu, best.nan != 0) ? 1 : 0;
