@@ -85,10 +85,14 @@ struct Slice {
   int n_chunks;   // ring stages the slice takes
 };
 
-// Units a warp takes per GEMV iteration in each phase (rows per iteration / rows
-// per unit); a ring stage holds a whole number of them when it can.
+// Rows a warp takes per GEMV iteration in each phase (a power of two up to 8; for
+// gate/up, rows of interleaved gate/up pairs).
+constexpr int kNrQkv = 2, kNrO = 1, kNrGu = 4, kNrDown = 1, kNrLm = 8;
+// Units per iteration (rows / rows per unit); a ring stage holds a whole number
+// of them when it can.
 __host__ __device__ constexpr int phase_upi(int kind) {
-  return kind == K_QKV ? 4 : kind == K_GU ? 4 : kind == K_LM ? 8 : 2;
+  return kind == K_QKV ? kNrQkv : kind == K_O ? kNrO : kind == K_GU ? kNrGu / 2
+       : kind == K_DOWN ? kNrDown : kNrLm;
 }
 
 // 32-bit arithmetic throughout: n_units * G stays far below 2^31 for every shape
@@ -159,7 +163,7 @@ __device__ __forceinline__ Split attn_split(const MegaArgs& a, int pos, int b) {
   return r;
 }
 
-__device__ __forceinline__ void csync() {  // the 8 consumer warps only
+__device__ __forceinline__ void csync() {  // the consumer warps only
   asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
 }
 // Named barrier over the consumer warps that also ORs a flag across them, so a
@@ -1103,7 +1107,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       const float rn = load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
                                   Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr,
                                   min(qs.u1 - qs.u0, kUnitPre), abort);
-      gemv<EPI_STORE, XH, 4>(a, ring, S, c, qs, a.H, rn, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
+      gemv<EPI_STORE, XH, kNrQkv>(a, ring, S, c, qs, a.H, rn, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
     }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
@@ -1115,21 +1119,21 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       prewait(a, S, c, slice_chunks(os), abort);
       load_input(a, S, a.attn_o, ta, qd, nullptr, false, 0, a.x + os.u0, nullptr,
                  min(os.u1 - os.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XQ, 2>(a, ring, S, c, os, qd, 1.f, a.x, to, nullptr, nullptr, best, abort);
+      gemv<EPI_RESIDUAL, XQ, kNrO>(a, ring, S, c, os, qd, 1.f, a.x, to, nullptr, nullptr, best, abort);
     }
     // gate/up with SwiGLU
     if (gs.u1 > gs.u0) {
       prewait(a, S, c, slice_chunks(gs), abort);
       const float rn = load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0,
                                   abort);
-      gemv<EPI_SWIGLU, XH, 8>(a, ring, S, c, gs, a.H, rn, a.mlp, tg, nullptr, nullptr, best, abort);
+      gemv<EPI_SWIGLU, XH, kNrGu>(a, ring, S, c, gs, a.H, rn, a.mlp, tg, nullptr, nullptr, best, abort);
     }
     // down + residual (block-0 checkpoint)
     if (ds.u1 > ds.u0) {
       prewait(a, S, c, slice_chunks(ds), abort);
       load_input(a, S, a.mlp, tg, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
                  min(ds.u1 - ds.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XI, 2>(a, ring, S, c, ds, a.I, 1.f, a.x, td, nullptr,
+      gemv<EPI_RESIDUAL, XI, kNrDown>(a, ring, S, c, ds, a.I, 1.f, a.x, td, nullptr,
                          (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr, best,
                          abort);
     }
@@ -1142,7 +1146,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     if (a.cap_final && b == 0)
       for (int r = tid; r < a.H; r += kConsumers * 32)
         a.cap_final[(size_t)pos * a.H + r] = S.xs[xs_pos(r)] * rn;
-    gemv<EPI_LOGITS, XH, 8>(a, ring, S, c, ls, a.H, rn, nullptr, 0u, nullptr, nullptr, best, abort);
+    gemv<EPI_LOGITS, XH, kNrLm>(a, ring, S, c, ls, a.H, rn, nullptr, 0u, nullptr, nullptr, best, abort);
   }
   // each lane holding rows kept its own best: merge them onto lane 0 (ties to the lower index)
   best.nan = __any_sync(0xffffffffu, best.nan != 0) ? 1 : 0;
