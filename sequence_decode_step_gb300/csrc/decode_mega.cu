@@ -1,12 +1,12 @@
 // The decode step as one persistent cooperative kernel (one CTA per SM).
 //
-// Warp 8 of every CTA is a producer: it walks the CTA's share of every phase
+// The last warp of every CTA is a producer: it walks the CTA's share of every phase
 // of the token in order (per layer: fused QKV rows, the KV tiles of its key
 // split, o_proj rows, gate/up row pairs, down rows; then LM-head rows) and
 // streams the bytes with bulk TMA copies into a ring of shared-memory stages.
 // None of these bytes depend on activations, so the producer runs ahead of
 // the consumers across phase boundaries and the HBM stream never drains.
-// Warps 0..7 consume: each phase reads its input vector from L2 and works
+// The other warps consume: each phase reads its input vector from L2 and works
 // through its chunks from the ring.
 //
 // There is no grid barrier. Every activation a phase hands to the next one
@@ -37,12 +37,22 @@
 #include "qw_internal.h"
 #include "qw_ptx.cuh"
 
+// The consumer warp count is fixed per build of this file: 7 by default (short
+// contexts), and decode_mega_wide.cu builds it again with 11 under another
+// namespace for long contexts, where the attention passes dominate and spread
+// over more warps (at short context the GEMV phases have too few rows per CTA
+// for the extra warps, and the wider barriers cost more).
+#ifndef QW_MEGA_CONSUMERS
+#define QW_MEGA_CONSUMERS 7
+#define QW_MEGA_NS mega
+#endif
+
 namespace qw {
 namespace {
 
-// 7 consumer warps + 1 producer warp: 8 warps are 2 per SM sub-partition, which
-// leaves 255 registers per thread (9 warps would cap them at 168 and spill).
-constexpr int kConsumers = 7;                // consumer warps
+// consumer warps + 1 producer warp; 8 warps leave 255 registers per thread, 12
+// warps 168 (both fit the kernel without spills)
+constexpr int kConsumers = QW_MEGA_CONSUMERS;
 constexpr int kNT = kConsumers * 32;         // consumer threads
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kNS = 6;                       // ring stages
@@ -51,6 +61,11 @@ constexpr int kMaxC = 12;                    // input vectors up to 12 x 256 = 3
 constexpr int kTK = 32;                      // keys per attention tile (K + V = 32 KB at hd 128)
 constexpr int kGQ = 8;
 constexpr int kMinKeys = 128;               // keys per split at least (one pass)
+// Up to this many keys a group's query heads go to separate CTAs over all keys
+// (several passes, no combine); beyond it the keys are split and combined.
+// Measured (us/token, Qwen3-0.6B shape): at 129-256 keys 686 vs 734 with the
+// key split; at 257-384 keys the head split's three passes lose (784 vs 739).
+constexpr int kHeadSplitKeys = 256;
 constexpr int kPass = 4;                     // tiles per attention pass
 constexpr int kUnitPre = 64;                 // units of a phase whose epilogue values are prefetched
 
@@ -148,7 +163,8 @@ __device__ __forceinline__ Split attn_split(const MegaArgs& a, int pos, int b) {
   r.nsplit = (n_keys + kps - 1) / kps;
   r.h0 = 0;
   r.nh = gq;
-  if (r.nsplit == 1 && gq > 1 && gq <= a.splits) {  // split the heads instead of the keys
+  if (n_keys <= kHeadSplitKeys && gq > 1 && gq <= a.splits) {  // split the heads, not the keys
+    r.nsplit = 1;
     r.active = r.g < a.nkv && r.s < gq;
     r.h0 = r.s;
     r.nh = 1;
@@ -1181,6 +1197,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs
 
 }  // namespace
 
+namespace QW_MEGA_NS {
+
 bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers) {
   return H <= kMaxC * 256 && I <= kMaxC * 256 && qd <= kMaxC * 256 && (hd == 64 || hd == 128) &&
          H % 8 == 0 && I % 8 == 0 && qd % 8 == 0 && n_layers >= 1 &&
@@ -1235,4 +1253,5 @@ cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s) {
   return cudaLaunchKernelExC(&cfg, mega_kernel_for(a), args);
 }
 
+}  // namespace QW_MEGA_NS
 }  // namespace qw

@@ -64,7 +64,8 @@ cudaError_t ensure_attributes(int dev) {
   cudaError_t e = set_kernel_attributes();
   if (e == cudaSuccess) e = set_gemm_attributes();
   if (e == cudaSuccess) e = set_prefill_attributes();
-  if (e == cudaSuccess) e = set_mega_attributes();
+  if (e == cudaSuccess) e = mega::set_mega_attributes();
+  if (e == cudaSuccess) e = mega_wide::set_mega_attributes();
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attrs_set[dev] = true;
   return e;
 }
@@ -148,6 +149,7 @@ struct qw_handle {
   // multi-kernel graph
   bool use_mega = false;
   bool mega_ok = false;
+  bool mega_wide = false;  // the recorded step uses the 11-warp build (long contexts)
   LayerDev* d_layers = nullptr;
   // the persistent kernel's activations as tagged words, and its launch epoch
   uint64_t* mx = nullptr;
@@ -248,8 +250,10 @@ static int alloc_state(qw_handle* h) {
   const size_t qkv_rows = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * hd;
   h->nsplit_max = std::max(1, h->num_sms / c.n_kv_heads);
   h->mega_ok = c.weight_format == QW_WEIGHTS_BF16 &&
-               mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim, c.head_dim,
-                              c.n_q_heads / c.n_kv_heads, c.n_layers) &&
+               mega::mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim,
+                                    c.head_dim, c.n_q_heads / c.n_kv_heads, c.n_layers) &&
+               mega_wide::mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim,
+                                         c.head_dim, c.n_q_heads / c.n_kv_heads, c.n_layers) &&
                (int64_t)c.vocab * h->num_sms < (int64_t)1 << 31;  // 32-bit slice arithmetic
   h->use_mega = h->mega_ok;
   h->w4 = c.weight_format == QW_WEIGHTS_INT4_G128;
@@ -669,7 +673,9 @@ static MegaArgs mega_args(qw_handle* h) {
 
 // Launch one step's kernels on stream s (recorded into the graph).
 static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
-  if (h->use_mega) return launch_mega(mega_args(h), h->nsplit_max * h->cfg.n_kv_heads, s);
+  if (h->use_mega)
+    return (h->mega_wide ? mega_wide::launch_mega : mega::launch_mega)(
+        mega_args(h), h->nsplit_max * h->cfg.n_kv_heads, s);
   const qw_config& c = h->cfg;
   const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
   const int qd = c.n_q_heads * hd, kd = c.n_kv_heads * hd;
@@ -830,7 +836,7 @@ static int ensure_graph_once(qw_handle* h) {
     if (kp.func == embed_kernel_fn()) {
       bytes = sizeof(EmbedArgs);
       off = offsetof(EmbedArgs, tok);
-    } else if (is_mega_kernel(kp.func)) {
+    } else if (mega::is_mega_kernel(kp.func) || mega_wide::is_mega_kernel(kp.func)) {
       bytes = sizeof(MegaArgs);
       off = offsetof(MegaArgs, tok);
     } else {
@@ -880,11 +886,24 @@ static int check_ready(qw_handle* h, const char* fn) {
 // Queue n graph replays; step i is fed tokens[i] (or, when tokens is null, `first`
 // for the first step and the device argmax afterwards). The token is the embed
 // node's kernel argument, so no copy is queued per step.
+// Each step runs the persistent kernel build that suits its position: 7 consumer
+// warps below kMegaWideFrom keys, 11 from there on (the graph is re-recorded when
+// the choice changes, which happens at most once per pass through the context).
+static constexpr int kMegaWideFrom = 1536;
+
 static int run_steps(qw_handle* h, int n, const int32_t* tokens, int first) {
-  int rc = ensure_graph(h);
-  if (rc) return rc;
   int last = -2;
   for (int i = 0; i < n; ++i) {
+    const bool wide = h->use_mega && h->pos + i >= kMegaWideFrom;
+    if (wide != h->mega_wide) {
+      h->mega_wide = wide;
+      h->graph_dirty = true;
+    }
+    if (!h->exec || h->graph_dirty) {
+      const int rc = ensure_graph(h);
+      if (rc) return rc;
+      last = -2;  // a new graph: its token node gets the token again
+    }
     const int tok = tokens ? tokens[i] : (i == 0 ? first : -1);
     if (tok != last) {
       std::vector<uint8_t>& buf = h->tok_args;

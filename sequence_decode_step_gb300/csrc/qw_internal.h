@@ -208,10 +208,20 @@ struct MegaArgs {
   int* err;
   uint64_t wait_ns;
 };
+// Two builds of the kernel: mega (7 consumer warps) and mega_wide (11).
+namespace mega {
 bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers);
 size_t mega_smem_bytes();
 cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);
 cudaError_t set_mega_attributes();
-bool is_mega_kernel(const void* fn);  // one of the persistent kernel instantiations
+bool is_mega_kernel(const void* fn);  // one of this build's kernel instantiations
+}  // namespace mega
+namespace mega_wide {
+bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers);
+size_t mega_smem_bytes();
+cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);
+cudaError_t set_mega_attributes();
+bool is_mega_kernel(const void* fn);
+}  // namespace mega_wide
 
 }  // namespace qw

@@ -146,10 +146,14 @@ def test_qwen3_06b_decode_128_steps(qwen06_decode):
     assert n >= wl.decode_steps // 2
 
 
-def test_qwen3_06b_longctx_8k(qwen06_decode):
-    wl0, _, _, _ = qwen06_decode
+@pytest.fixture(scope="module")
+def longctx_drawn():
     wl = W.WORKLOADS["qwen3_0.6b_longctx"]
-    d = W.draw(wl)
+    return wl, W.draw(wl)
+
+
+def test_qwen3_06b_longctx_8k(qwen06_decode, longctx_drawn):
+    wl, d = longctx_drawn
     m, o = _models(wl, d)
     try:
         for l, (k, v) in enumerate(d.kv):
@@ -162,6 +166,26 @@ def test_qwen3_06b_longctx_8k(qwen06_decode):
         p = wl.kv_prefill
         assert violation(kd.cpu().numpy()[:, p:p + wl.decode_steps],
                          o.k_cache[5][:, p:p + wl.decode_steps]) <= 0
+    finally:
+        m.close()
+
+
+def test_decode_across_the_long_context_switch(longctx_drawn):
+    # positions 1532..1539: the step switches from the 7-warp to the 11-warp
+    # build of the persistent kernel at 1536 keys (the graph is re-recorded);
+    # every step matches the oracle on both sides of the switch
+    wl, d = longctx_drawn
+    m, o = _models(wl, d)
+    try:
+        for l, (k, v) in enumerate(d.kv):
+            m.set_kv(l, k, v)
+        m.set_pos(1532)
+        o.pos = 1532
+        assert B.qw_get_decode_path(m.h) == 0
+        n = _teacher_forced(m, o, d.start_token, 8)
+        assert n >= 4
+        kd, _ = m.kv(3)
+        assert violation(kd.cpu().numpy()[:, 1532:1540], o.k_cache[3][:, 1532:1540]) <= 0
     finally:
         m.close()
 
