@@ -909,39 +909,49 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     }
     return;
   }
+  // Key split: every split but the first publishes its partial outputs and
+  // (m, l) per head as tagged words; split 0 polls them (one L2 round trip once
+  // they are there) and combines in split order. The partial slots are reused
+  // by the next layer only after the combined output has gone through o_proj,
+  // gate/up, down and the next QKV, all of which the writers wait for.
+  const size_t hs = (size_t)a.splits * (HD + 2);  // words per query head
+  uint64_t* mp = a.mpart + (size_t)HB * hs;
+  if (sp.s != 0) {
+    uint64_t* my = mp + (size_t)sp.s * (HD + 2);
 #pragma unroll
-  for (int oi = 0; oi < OUTS; ++oi) {
-    const int idx = tid + oi * kNT;
-    if (idx < GQ * HD) {
-      const int h = idx / HD, d = idx % HD;
-      a.part_o[((size_t)(HB + h) * a.splits + sp.s) * HD + d] = oacc[oi];
+    for (int oi = 0; oi < OUTS; ++oi) {
+      const int idx = tid + oi * kNT;
+      if (idx < GQ * HD) {
+        const int h = idx / HD, d = idx % HD;
+        st_tagged(my + (size_t)h * hs + d, oacc[oi], tag_out);
+      }
     }
+    if (tid < GQ) {
+      st_tagged(my + (size_t)tid * hs + HD, S.ml_s[2 * tid], tag_out);
+      st_tagged(my + (size_t)tid * hs + HD + 1, S.ml_s[2 * tid + 1], tag_out);
+    }
+    return;
   }
-  if (tid < GQ) {
-    const size_t o = ((size_t)(HB + tid) * a.splits + sp.s) * 2;
-    a.part_ml[o] = S.ml_s[2 * tid];
-    a.part_ml[o + 1] = S.ml_s[2 * tid + 1];
-  }
-  __threadfence();
-  csync();
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.attn_counters[l * a.nkv + g], 1);
-    S.flag = (prev == sp.nsplit - 1);
-  }
-  csync();
-  if (!S.flag) return;
-  __threadfence();
-  // Combine: every (m, l) of the group into shared memory at once, then the
-  // partial outputs in batches of 8 independent loads.
   const int ns = sp.nsplit;
-  for (int i = tid; i < GQ * ns; i += kConsumers * 32) {
+  for (int i = tid; i < GQ * ns; i += kNT) {
     const int h = i / ns, s2 = i % ns;
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) +
-                             (size_t)(HB + h) * a.splits + s2);
-    S.pml_s[2 * i] = ml.x;
-    S.pml_s[2 * i + 1] = ml.y;
+    float m = S.ml_s[2 * h], lsum = S.ml_s[2 * h + 1];
+    if (s2 != 0) {
+      const uint64_t* src = mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + HD;
+      uint64_t w0 = 0, w1 = 0;
+      uint64_t t0 = 0;
+      for (uint32_t n = 1; !abort; ++n) {
+        ld_words2(src, w0, w1);
+        if (word_tag(w0) == tag_out && word_tag(w1) == tag_out) break;
+        poll_bound(a, n, t0, abort);
+      }
+      m = word_value(w0);
+      lsum = word_value(w1);
+    }
+    S.pml_s[2 * i] = m;
+    S.pml_s[2 * i + 1] = lsum;
   }
-  csync();
+  abort = csync_or(abort);
 #pragma unroll
   for (int oi = 0; oi < OUTS; ++oi) {
     const int idx = tid + oi * kNT;
@@ -952,21 +962,33 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pm[2 * s2]);
       float den = 0.f;
       for (int s2 = 0; s2 < ns; ++s2) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
-      const float* po = a.part_o + (size_t)(HB + h) * a.splits * HD + d;
-      float num = 0.f;
-      for (int s0 = 0; s0 < ns; s0 += 8) {
-        float pv[8];
+      const uint64_t* po = mp + (size_t)h * hs + d;
+      float num = expf(pm[0] - M) * oacc[oi];
+      for (int s0 = 1; s0 < ns; s0 += 8) {  // the others' outputs, 8 polled loads at a time
+        uint64_t w[8];
+        unsigned pend = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) pv[j] = s0 + j < ns ? __ldcg(po + (size_t)(s0 + j) * HD) : 0.f;
+        for (int j = 0; j < 8; ++j) {
+          w[j] = 0;
+          if (s0 + j < ns) pend |= 1u << j;
+        }
+        uint64_t t0 = 0;
+        for (uint32_t n = 1; pend && !abort; ++n) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if ((pend >> j) & 1u) w[j] = ld_word(po + (size_t)(s0 + j) * (HD + 2));
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (((pend >> j) & 1u) && word_tag(w[j]) == tag_out) pend &= ~(1u << j);
+          if (pend) poll_bound(a, n, t0, abort);
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (s0 + j < ns) num = fmaf(expf(pm[2 * (s0 + j)] - M), pv[j], num);
+          if (s0 + j < ns) num = fmaf(expf(pm[2 * (s0 + j)] - M), word_value(w[j]), num);
       }
       st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, num / den, tag_out);
     }
   }
-  csync();
-  if (tid == 0) a.attn_counters[l * a.nkv + g] = 0;  // not used again in this launch
 }
 
 

@@ -100,6 +100,7 @@ struct qw_handle {
   float* part_o = nullptr;
   float* part_ml = nullptr;
   int* attn_counters = nullptr;
+  uint64_t* mpart = nullptr;  // the persistent kernel's key-split partials (tagged words)
   float* blk_val = nullptr;
   int* blk_idx = nullptr;
   int* am_counter = nullptr;
@@ -273,6 +274,7 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->part_o, (size_t)c.n_q_heads * h->nsplit_max * hd * 4},
       {(void**)&h->part_ml, (size_t)c.n_q_heads * h->nsplit_max * 2 * 4},
       {(void**)&h->attn_counters, L * nkv * 4},
+      {(void**)&h->mpart, (size_t)c.n_q_heads * h->nsplit_max * (hd + 2) * 8},
       {(void**)&h->blk_val, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->blk_idx, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->am_counter, 4},
@@ -648,9 +650,7 @@ static MegaArgs mega_args(qw_handle* h) {
   m.mlp = h->mmlp;
   m.epoch = h->d_epoch;
   m.logits = h->logits;
-  m.part_o = h->part_o;
-  m.part_ml = h->part_ml;
-  m.attn_counters = h->attn_counters;
+  m.mpart = h->mpart;
   m.splits = h->nsplit_max;
   m.am.blk_val = h->blk_val;
   m.am.blk_idx = h->blk_idx;

@@ -194,9 +194,8 @@ struct MegaArgs {
   uint64_t* mlp;           // [I]
   uint32_t* epoch;         // launches so far; tags are derived from it
   float* logits;           // [V]
-  float* part_o;           // [nq][splits][hd]
-  float* part_ml;          // [nq][splits][2]
-  int* attn_counters;      // [L][nkv]: one arrival counter per layer and KV head
+  uint64_t* mpart;         // [nq][splits][hd + 2] key-split partials as tagged words: the
+                           // unnormalised output, then the running max m and sum l
   int splits;              // CTAs per KV head (gridDim.x / nkv)
   ArgmaxOut am;
   const int* pos;
