@@ -62,10 +62,10 @@ constexpr int kTK = 32;                      // keys per attention tile (K + V =
 constexpr int kGQ = 8;
 constexpr int kMinKeys = 128;               // keys per split at least (one pass)
 // Up to this many keys a group's query heads go to separate CTAs over all keys
-// (several passes, no combine); beyond it the keys are split and combined.
-// Measured (us/token, Qwen3-0.6B shape): at 129-256 keys 686 vs 734 with the
-// key split; at 257-384 keys the head split's three passes lose (784 vs 739).
-constexpr int kHeadSplitKeys = 256;
+// (one pass, no combine); beyond it the keys are split and combined. Measured
+// (us/token, Qwen3-0.6B shape, same box) at 145-256 keys: 652-680 with the key
+// split against 662-705 with the head split's two passes.
+constexpr int kHeadSplitKeys = 128;
 constexpr int kPass = 4;                     // tiles per attention pass
 constexpr int kUnitPre = 64;                 // units of a phase whose epilogue values are prefetched
 
