@@ -143,9 +143,9 @@ __device__ __forceinline__ const uint8_t* phase_base(int kind, const LayerDev& L
 }
 
 // Attention work of CTA b (all derived from the device position): KV head g and
-// either a key split s (its query heads all together, partials combined by the
-// last split to arrive) or, when the keys fit one split, query head h0 of the
-// group over all keys (the group's heads on separate CTAs, no combine).
+// either a key split s (its query heads all together, partials combined by
+// split 0) or, up to kHeadSplitKeys keys, query head h0 of the group over all
+// keys (the group's heads on separate CTAs, no combine).
 struct Split {
   int g, s, k0, k1, nsplit;
   int h0, nh;  // the group's query heads [h0, h0 + nh) handled here
@@ -636,8 +636,9 @@ __device__ __forceinline__ int slice_chunks(const Slice& sl) { return sl.n_chunk
 
 // Split-K attention of CTA b: QK-norm + RoPE of its group's queries (and of the
 // new key when its split holds pos), tiles of 32 keys from the ring, online
-// softmax, then a partial (or the final output when there is one split); the
-// last CTA of a KV head to arrive combines the splits in split order.
+// softmax, then a partial (or the final output when there is one split); split
+// 0 of a KV head polls the other splits' partials and combines them in split
+// order.
 template <int HD>
 __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l,
                                            int pos, const Split& sp, const LayerDev& Ld,
