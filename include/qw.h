@@ -301,6 +301,34 @@ int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16_t* table, 
                       int32_t hidden, float eps, float* logits, int32_t* argmax_dev,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Sampling on the device ("flashmoon demo" README: greedy plus temperature / top-k /
+ * top-p sampling, temp = 0 meaning greedy; the demo reads every logits row back to
+ * the host to sample, at about 2.7x the cost of the decode step). Here only the id
+ * leaves the device. With the k largest logits ordered by (logit descending, index
+ * ascending) and l_0 the largest:
+ *   w_i = exp((l_i - l_0) / temperature)   (f64, i < k)
+ *   the nucleus is the shortest prefix whose running sum of w reaches top_p times the
+ *   sum over all k; the token is the first candidate of the nucleus whose running sum
+ *   exceeds u times the nucleus sum.
+ *   temperature <= 0 (or top_k == 1): the greedy argmax (ties -> lowest id).
+ *   logits: f32 [vocab] DEVICE; vocab >= 1; top_k in [1, 256], larger than vocab is
+ *   clamped to vocab; top_p in (0, 1] (>= 1: no nucleus cut); u in [0, 1), the
+ *   uniform draw, supplied by the caller (the library draws no random numbers);
+ *   token_dev: int32 [1] DEVICE, receives the id, or -1 when the row holds a NaN or
+ *   no finite logit; workspace: DEVICE scratch of qw_sample_workspace_bytes(vocab,
+ *   top_k) bytes, no initialisation needed. QW_ERR_ARG for arguments outside these
+ *   ranges (also when vocab / 16384 * top_k > 4096, the final sort's capacity). */
+size_t qw_sample_workspace_bytes(int32_t vocab, int32_t top_k);
+int qw_sample(const float* logits, int32_t vocab, float temperature, int32_t top_k, float top_p,
+              float u, int32_t* token_dev, void* workspace, size_t workspace_bytes, void* stream);
+
+/* qw_sample over the handle's logits of its last step (qw_decode_step,
+ * qw_decode_greedy or qw_prefill), on the handle's stream and with its own
+ * workspace; writes the id to *token_host (synchronises). QW_ERR_STATE before any
+ * step, QW_ERR_NUMERIC when the row holds a NaN or no finite logit. */
+int qw_sample_last(qw_handle* h, float temperature, int32_t top_k, float top_p, float u,
+                   int32_t* token_host);
+
 /* Prefill contraction on tcgen05 tensor cores: C[M,N] = (A_hi + A_lo)[M,K] . B[N,K]^T.
  * A_hi, A_lo (nullable), B: bf16 row-major DEVICE, 16-byte aligned, K % 8 == 0; C: f32
  * [M,N] DEVICE. The activation of a layer enters as its two-bf16 split (hi = bf16(x),

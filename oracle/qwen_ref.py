@@ -150,6 +150,66 @@ def greedy_argmax(logits: np.ndarray) -> int:
     return int(np.argmax(logits))
 
 
+def sample_logits(logits: np.ndarray, temperature: float, top_k: int, top_p: float, u: float):
+    """Temperature / top-k / top-p sampling of one logits row with the draw u in [0, 1).
+
+    "flashmoon demo" page: greedy plus temperature/top-k/top-p sampling, temp = 0
+    meaning greedy. The page gives no formula; the reading used here:
+      candidates: the top_k largest logits (top_k clamped to the row), ordered by
+        logit descending, index ascending;
+      w_i = exp((l_i - l_0) / T) in float64, l_0 the largest;
+      nucleus: the shortest prefix whose running sum (in candidate order) reaches
+        top_p times the sum over all candidates (top_p >= 1: all of them);
+      token: the first candidate of the nucleus whose running sum exceeds u times
+        the nucleus sum.
+      T <= 0 or top_k == 1: the greedy argmax.
+    Returns (token, margin): margin is the smallest relative distance between a
+    running sum and either threshold it was compared with near the decision, so a
+    test can tell a decision that float rounding could flip. NaN -> FloatingPointError;
+    no finite logit -> FloatingPointError.
+    """
+    x = np.asarray(logits, dtype=np.float32)
+    if np.isnan(x).any():
+        raise FloatingPointError("NaN logit")
+    k = min(int(top_k), x.size)
+    order = np.lexsort((np.arange(x.size), -x.astype(np.float64)))[:k]  # logit desc, index asc
+    l = x[order].astype(np.float64)
+    if not np.isfinite(l[0]) or l[0] == -np.inf:
+        raise FloatingPointError("no finite logit")
+    if not temperature > 0 or k == 1:
+        return int(order[0]), np.inf
+    w = np.exp((l - l[0]) / float(temperature))
+    run = np.empty(k)
+    acc = 0.0
+    for i in range(k):                       # running sums in candidate order
+        acc += w[i]
+        run[i] = acc
+    need = float(np.float32(top_p)) * run[-1]
+    cut = k - 1
+    for i in range(k):
+        if run[i] >= need:
+            cut = i
+            break
+    target = float(np.float32(u)) * run[cut]
+    pick = cut
+    for i in range(cut + 1):
+        if run[i] > target:
+            pick = i
+            break
+    # decision margins (relative to the total): how far the running sums on either
+    # side of each decision sit from its threshold (the last candidate always
+    # meets the nucleus threshold, so it is no margin)
+    near = [np.inf]
+    if cut < k - 1:
+        near.append(run[cut] - need)
+    if cut > 0:
+        near.append(need - run[cut - 1])
+    near.append(run[pick] - target)
+    if pick > 0:
+        near.append(target - run[pick - 1])
+    return int(order[pick]), float(min(near) / run[-1])
+
+
 # ----------------------------------------------------------------------------- int4 group-128
 INT4_GROUP = 128
 

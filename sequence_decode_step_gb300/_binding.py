@@ -109,6 +109,11 @@ _SIG = {
                                               C.c_int32, C.c_void_p, C.c_void_p]),
     "qw_gemm_bf16": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                C.c_int32, C.c_void_p, C.c_int32, C.c_void_p]),
+    "qw_sample_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "qw_sample": (C.c_int, [C.c_void_p, C.c_int32, C.c_float, C.c_int32, C.c_float, C.c_float,
+                            C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "qw_sample_last": (C.c_int, [C.c_void_p, C.c_float, C.c_int32, C.c_float, C.c_float,
+                                 C.POINTER(C.c_int32)]),
     "qw_lm_head_workspace_bytes": (C.c_size_t, []),
     "qw_lm_head_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                     C.c_float, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
@@ -252,6 +257,23 @@ def qw_destroy(h) -> None:
 
 def qw_set_decode_path(h, path: int) -> None:
     check("qw_set_decode_path", lib().qw_set_decode_path(h, int(path)), h)
+
+
+def qw_sample_last(h, temperature: float, top_k: int, top_p: float, u: float) -> int:
+    """Sampled id from the handle's last logits (temperature / top-k / top-p, draw u)."""
+    t = C.c_int32()
+    check("qw_sample_last", lib().qw_sample_last(h, float(temperature), int(top_k), float(top_p),
+                                                 float(u), C.byref(t)), h)
+    return t.value
+
+
+def qw_sample(logits_ptr: int, vocab: int, temperature: float, top_k: int, top_p: float,
+              u: float, token_ptr: int, workspace_ptr: int, workspace_bytes: int,
+              stream: Optional[int] = None) -> None:
+    """Queue one sampling of a device logits row; the id lands in device memory."""
+    check("qw_sample", lib().qw_sample(logits_ptr, int(vocab), float(temperature), int(top_k),
+                                       float(top_p), float(u), token_ptr, workspace_ptr,
+                                       int(workspace_bytes), stream))
 
 
 def qw_get_decode_path(h) -> int:

@@ -897,7 +897,8 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       }
     }
   }
-  csync();
+  // No barrier here: what follows reads only registers and ml_s (stable since the
+  // last softmax step), and the next writer of xs and pml_s passes a barrier first.
 
   if (sp.nsplit == 1) {
 #pragma unroll

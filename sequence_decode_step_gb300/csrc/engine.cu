@@ -64,6 +64,7 @@ cudaError_t ensure_attributes(int dev) {
   cudaError_t e = set_kernel_attributes();
   if (e == cudaSuccess) e = set_gemm_attributes();
   if (e == cudaSuccess) e = set_prefill_attributes();
+  if (e == cudaSuccess) e = set_sample_attributes();
   if (e == cudaSuccess) e = mega::set_mega_attributes();
   if (e == cudaSuccess) e = mega_wide::set_mega_attributes();
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attrs_set[dev] = true;
@@ -101,6 +102,8 @@ struct qw_handle {
   float* part_ml = nullptr;
   int* attn_counters = nullptr;
   uint64_t* mpart = nullptr;  // the persistent kernel's key-split partials (tagged words)
+  void* sample_ws = nullptr;  // qw_sample_last's workspace (top_k up to kMaxSampleTopK)
+  int* d_sample_tok = nullptr;
   float* blk_val = nullptr;
   int* blk_idx = nullptr;
   int* am_counter = nullptr;
@@ -129,7 +132,7 @@ struct qw_handle {
   std::vector<CUtensorMap> tm_qkv, tm_ow, tm_gu, tm_dw;  // per layer, weight side
   int* d_status = nullptr;  // [2] greedy id, error word (written by the LM head)
   // pinned host staging
-  int* h_status = nullptr;  // [4]
+  int* h_status = nullptr;  // [8]: argmax, error, set_pos staging, error copy, sampled id
   int* h_tokens = nullptr;  // [cap]
   // checkpoints
   bool capture_on = false, cap_valid = false;
@@ -275,6 +278,8 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->part_ml, (size_t)c.n_q_heads * h->nsplit_max * 2 * 4},
       {(void**)&h->attn_counters, L * nkv * 4},
       {(void**)&h->mpart, (size_t)c.n_q_heads * h->nsplit_max * (hd + 2) * 8},
+      {(void**)&h->sample_ws, sample_workspace_bytes(c.vocab, kMaxSampleTopK)},
+      {(void**)&h->d_sample_tok, 4},
       {(void**)&h->blk_val, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->blk_idx, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->am_counter, 4},
@@ -329,9 +334,9 @@ static int alloc_state(qw_handle* h) {
     if (!ok) QW_FAIL(h, QW_ERR_CUDA, "prefill: TMA descriptor encoding failed");
   }
   QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, std::max<size_t>(cap, Tm) * 4, cudaHostAllocPortable));
-  QW_CUDA(h, cudaHostAlloc((void**)&h->h_status, 16, cudaHostAllocPortable));
+  QW_CUDA(h, cudaHostAlloc((void**)&h->h_status, 32, cudaHostAllocPortable));
   memset(h->h_tokens, 0xff, cap * 4);
-  memset(h->h_status, 0, 16);
+  memset(h->h_status, 0, 32);
   QW_CUDA(h, launch_rope_table(h->rope, c.max_ctx, c.head_dim, c.rope_theta, h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   return QW_OK;
@@ -1326,6 +1331,58 @@ extern "C" int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16
   a.wait_ns = 1000000000ull;
   plan_gemv(a, grid, kStreamStage, kStreamStages);
   QW_OP_CUDA(launch_gemv(EPI_LOGITS, a, grid, false, (cudaStream_t)stream));
+  return QW_OK;
+}
+
+extern "C" size_t qw_sample_workspace_bytes(int32_t vocab, int32_t top_k) {
+  if (vocab < 1 || top_k < 1) return 0;
+  return sample_workspace_bytes(vocab, std::min(top_k, vocab));
+}
+
+static int sample_args_ok(int32_t vocab, int32_t top_k, float top_p, float u, const char* fn) {
+  if (vocab < 1 || top_k < 1 || top_k > kMaxSampleTopK || !sample_shape_ok(vocab, std::min(top_k, vocab)))
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            std::string(fn) + ": top_k must be in [1, 256] and vocab / 16384 * top_k <= 4096");
+  if (!(top_p > 0.f)) QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, std::string(fn) + ": top_p must be > 0");
+  if (!(u >= 0.f && u < 1.f)) QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, std::string(fn) + ": u must be in [0, 1)");
+  return QW_OK;
+}
+
+extern "C" int qw_sample(const float* logits, int32_t vocab, float temperature, int32_t top_k,
+                         float top_p, float u, int32_t* token_dev, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!logits || !token_dev || !workspace)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_sample: null buffer");
+  int rc = sample_args_ok(vocab, top_k, top_p, u, "qw_sample");
+  if (rc) return rc;
+  if (workspace_bytes < qw_sample_workspace_bytes(vocab, top_k))
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_sample: workspace too small");
+  int sms = 0;
+  if (op_sms(&sms)) return QW_ERR_CUDA;
+  QW_OP_CUDA(launch_sample(logits, vocab, top_k, temperature, top_p, u, token_dev, workspace,
+                           (cudaStream_t)stream));
+  return QW_OK;
+}
+
+extern "C" int qw_sample_last(qw_handle* h, float temperature, int32_t top_k, float top_p, float u,
+                              int32_t* token_host) {
+  int rc = check_ready(h, "qw_sample_last");
+  if (rc) return rc;
+  if (!token_host) QW_FAIL(h, QW_ERR_ARG, "qw_sample_last: null token_host");
+  if (h->pos == 0) QW_FAIL(h, QW_ERR_STATE, "qw_sample_last: no step has produced logits yet");
+  rc = sample_args_ok(h->cfg.vocab, top_k, top_p, u, "qw_sample_last");
+  if (rc) {
+    h->err = g_last_error;
+    return rc;
+  }
+  DeviceGuard dg(h->device);
+  QW_CUDA(h, launch_sample(h->logits, h->cfg.vocab, top_k, temperature, top_p, u, h->d_sample_tok,
+                           h->sample_ws, h->stream));
+  QW_CUDA(h, cudaMemcpyAsync(&h->h_status[4], h->d_sample_tok, 4, cudaMemcpyDeviceToHost, h->stream));
+  QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  const int id = ((volatile int*)h->h_status)[4];
+  if (id < 0) QW_FAIL(h, QW_ERR_NUMERIC, "qw_sample_last: the logits hold a NaN or no finite value");
+  *token_host = id;
   return QW_OK;
 }
 

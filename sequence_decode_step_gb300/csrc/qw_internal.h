@@ -164,6 +164,14 @@ int kv_split_rows(int max_ctx);
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
 cudaError_t set_prefill_attributes();
 
+// ---- sampling (sample.cu) ----
+constexpr int kMaxSampleTopK = 256;
+size_t sample_workspace_bytes(int V, int k);
+bool sample_shape_ok(int V, int k);  // k <= kMaxSampleTopK and the final sort fits one CTA
+cudaError_t set_sample_attributes();
+cudaError_t launch_sample(const float* logits, int V, int k, float temperature, float top_p, float u,
+                          int32_t* token, void* workspace, cudaStream_t s);
+
 // ---- persistent decode step (decode_mega.cu) ----
 struct LayerDev {  // per-layer device pointers of the packed weights
   const uint8_t* qkv;

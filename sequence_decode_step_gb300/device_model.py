@@ -141,6 +141,10 @@ class DeviceModel:
     def greedy(self, token: int, n: int):
         return B.qw_decode_greedy(self.h, token, n)
 
+    def sample(self, temperature: float, top_k: int, top_p: float, u: float) -> int:
+        """Sampled id from the logits of the last step (the row stays on the device)."""
+        return B.qw_sample_last(self.h, temperature, top_k, top_p, u)
+
     def _logits_buf(self):
         import torch
         if not hasattr(self, "_lg"):

@@ -74,3 +74,23 @@ def test_null_arguments_rejected(L):
     assert L.qw_attention_workspace_bytes(16, 8, 128, 19) > 16 * 19 * 128 * 4
     assert L.qw_lm_head_workspace_bytes() >= 256 + 8 * 1024
     L.qw_destroy(None)
+
+
+def test_sample_arguments_checked_before_cuda(L):
+    # qw_sample validates its arguments on the host: no device is touched here
+    V = 151936
+    ws = L.qw_sample_workspace_bytes(V, 64)
+    assert ws >= (V // 1024) * 64 * 8
+    assert L.qw_sample_workspace_bytes(0, 8) == 0
+    assert L.qw_sample(None, V, 1.0, 8, 0.9, 0.5, None, None, 0, None) == B.QW_ERR_ARG
+    bad = [(V, 1.0, 0, 0.9, 0.5),      # top_k below 1
+           (V, 1.0, 257, 0.9, 0.5),    # top_k above 256
+           (V, 1.0, 8, 0.0, 0.5),      # top_p not above 0
+           (V, 1.0, 8, 0.9, 1.0),      # u not below 1
+           (V, 1.0, 8, 0.9, -0.1),     # u below 0
+           (0, 1.0, 8, 0.9, 0.5),      # empty row
+           (1 << 22, 1.0, 256, 0.9, 0.5)]  # final sort would exceed one CTA
+    for vocab, t, k, p, u in bad:
+        assert L.qw_sample(1, vocab, t, k, p, u, 1, 1, 1 << 30, None) == B.QW_ERR_ARG, (vocab, k, p, u)
+    assert L.qw_sample(1, V, 1.0, 64, 0.9, 0.5, 1, 1, ws - 8, None) == B.QW_ERR_ARG  # workspace
+    assert L.qw_sample_last(None, 1.0, 8, 0.9, 0.5, None) == B.QW_ERR_ARG

@@ -208,6 +208,72 @@ def test_argmax_ties_and_nan():
         R.greedy_argmax(np.array([1.0, np.nan], np.float32))
 
 
+# ------------------------------------------------------------------ sampling
+# Hand example: probabilities 0.1, 0.2, 0.3, 0.4 on ids 0..3 (logits log p, T = 1).
+# Candidate order 3, 2, 1, 0 with cumulative probability 0.4, 0.7, 0.9, 1.0.
+_P4 = np.log(np.array([0.1, 0.2, 0.3, 0.4], np.float32))
+
+
+@pytest.mark.parametrize("k,p,u,want", [
+    (4, 1.0, 0.10, 3), (4, 1.0, 0.50, 2), (4, 1.0, 0.80, 1), (4, 1.0, 0.95, 0),
+    (4, 0.6, 0.50, 3), (4, 0.6, 0.60, 2),   # nucleus {3, 2}: cumulative 4/7, 1 of 0.7
+    (4, 0.35, 0.99, 3),                     # nucleus {3} alone (0.4 reaches 0.35)
+    (2, 1.0, 0.50, 3), (2, 1.0, 0.60, 2),   # top-2 renormalised: 4/7, 3/7
+    (9, 1.0, 0.95, 0),                      # top_k above the row is the whole row
+])
+def test_sampling_hand_example(k, p, u, want):
+    got, margin = R.sample_logits(_P4, 1.0, k, p, u)
+    assert got == want and margin > 1e-3
+
+
+def test_sampling_greedy_cases_and_errors():
+    assert R.sample_logits(_P4, 0.0, 4, 1.0, 0.9)[0] == 3     # temp = 0 is greedy
+    assert R.sample_logits(_P4, -1.0, 4, 1.0, 0.9)[0] == 3
+    assert R.sample_logits(_P4, 1.0, 1, 1.0, 0.9)[0] == 3     # top_k = 1 is greedy
+    tie = np.array([0.5, 2.0, 2.0, 1.0], np.float32)
+    assert R.sample_logits(tie, 0.0, 4, 1.0, 0.0)[0] == R.greedy_argmax(tie) == 1
+    with pytest.raises(FloatingPointError):
+        R.sample_logits(np.array([1.0, np.nan], np.float32), 1.0, 2, 1.0, 0.5)
+    with pytest.raises(FloatingPointError):
+        R.sample_logits(np.full(3, -np.inf, np.float32), 1.0, 2, 1.0, 0.5)
+
+
+def test_sampling_equal_logits_split_u_by_index():
+    # four equal logits: each candidate holds a quarter of [0, 1), in index order
+    x = np.full(4, 1.5, np.float32)
+    for u, want in ((0.0, 0), (0.24, 0), (0.26, 1), (0.6, 2), (0.99, 3)):
+        assert R.sample_logits(x, 0.7, 4, 1.0, u)[0] == want
+
+
+def test_sampling_frequencies_are_the_truncated_softmax():
+    # inverse-CDF property: over a uniform grid of u the frequencies are the
+    # softmax at temperature T restricted to the nucleus of the top k, renormalised
+    rng = _rng(5)
+    x = rng.standard_normal(40).astype(np.float32)
+    T, k, p, N = 0.8, 12, 0.9, 20000
+    counts = np.zeros(40)
+    for j in range(N):
+        counts[R.sample_logits(x, T, k, p, (j + 0.5) / N)[0]] += 1
+    idx = np.argsort(-x.astype(np.float64), kind="stable")[:k]
+    e = np.exp((x[idx].astype(np.float64) - x[idx[0]]) / T)
+    c = np.cumsum(e) / e.sum()
+    n = int(np.argmax(c >= np.float32(p))) + 1
+    want = np.zeros(40)
+    want[idx[:n]] = e[:n] / e[:n].sum()
+    assert np.abs(counts / N - want).max() <= 2.0 / N
+    assert counts[np.setdiff1d(np.arange(40), idx[:n])].sum() == 0
+
+
+def test_sampling_temperature_scales_the_logits():
+    rng = _rng(6)
+    x = rng.standard_normal(64).astype(np.float32)
+    for u in np.linspace(0.01, 0.99, 25):
+        a = R.sample_logits(x, 2.0, 16, 0.95, u)
+        b = R.sample_logits((x / 2).astype(np.float32), 1.0, 16, 0.95, u)
+        if min(a[1], b[1]) > 1e-6:
+            assert a[0] == b[0]
+
+
 # ------------------------------------------------------------------ int4 g128
 def _read_int4_golden():
     vals, deq = {}, {}
