@@ -211,6 +211,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
     # ---- dominant single launch: the LM head GEMV (final norm + [V,H] table + argmax),
     # the same kernel the graph runs, timed alone with events on its stream
     lm = lm_head_roofline(L, B, torch, d, s, stream)
+    smp = sampling_timing(L, B, torch, s, stream)
 
     # ---- prefill of T=1024 ids (the prompt path at that length)
     pre = prefill_timing(torch, W, DeviceModel, stream) if args.prefill else None
@@ -252,6 +253,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
                           else "fallback 6800 GB/s"},
         "roofline": dominant,
         "lm_head_gemv": lm,
+        "sampling": smp,
         "decode_path": "persistent" if path == 0 else "multi-kernel graph",
         "e2e": {"value": n_tok * e2e_steps / (e2e_ms / 1e3), "unit": "tok/s",
                 "h2d_bytes_per_step": 4 * n_tok, "d2h_bytes_per_step": 4 * n_tok},
@@ -261,6 +263,36 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
         "prefill": pre,
     }
     return res
+
+
+def sampling_timing(L, B, torch, s, stream) -> dict:
+    """qw_sample over one logits row of the workload's vocabulary (on-device
+    temperature / top-k / top-p; the alternative is reading the row back)."""
+    T, k, p = 0.7, 50, 0.9
+    x = torch.randn(s.vocab, device="cuda") * 3
+    tok = torch.empty(1, dtype=torch.int32, device="cuda")
+    wsb = L.qw_sample_workspace_bytes(s.vocab, k)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+
+    def go(u):
+        rc = L.qw_sample(x.data_ptr(), s.vocab, T, k, p, u, tok.data_ptr(), ws.data_ptr(), wsb,
+                         stream.cuda_stream)
+        if rc:
+            raise RuntimeError(B.last_error())
+
+    for i in range(5):
+        go(0.1 * i)
+    n = 100
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n):
+        go((i + 0.5) / n)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"us_per_call": e0.elapsed_time(e1) * 1e3 / n, "vocab": s.vocab, "temperature": T,
+            "top_k": k, "top_p": p, "launches_per_call": 3,
+            "readback_bytes_avoided": s.vocab * 4}
 
 
 def lm_head_roofline(L, B, torch, d, s, stream) -> dict:
