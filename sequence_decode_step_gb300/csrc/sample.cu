@@ -47,11 +47,20 @@ __device__ __forceinline__ float unpack_val(uint64_t p) {
 }
 
 // In-place bitonic sort of n (a power of two) 64-bit keys in shared memory,
-// largest first, by all threads of the block.
+// largest first, by all threads of the block (a power-of-two warp count). Warp w
+// owns the compare-exchange pairs [wP, (w+1)P): a stage whose stride is at most P
+// touches only that warp's elements and needs no block barrier, so only the few
+// wide stages pay one (__syncthreads before and after them).
 __device__ void sort_desc(uint64_t* s, int n) {
+  const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = max(1, (n / 2) / nw);
+  const int p0 = min(n / 2, w * P), p1 = min(n / 2, p0 + P);
+  bool synced = true;  // the caller synchronised the block before the call
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+      const bool local = stride <= P;
+      if (!local && !synced) __syncthreads();
+      for (int i = p0 + lane; i < p1; i += 32) {
         const int lo = 2 * i - (i & (stride - 1));
         const int hi = lo + stride;
         const bool desc = (lo & size) == 0;
@@ -61,9 +70,16 @@ __device__ void sort_desc(uint64_t* s, int n) {
           s[hi] = a;
         }
       }
-      __syncthreads();
+      if (local) {
+        __syncwarp();
+        synced = false;
+      } else {
+        __syncthreads();
+        synced = true;
+      }
     }
   }
+  if (!synced) __syncthreads();
 }
 
 __device__ __forceinline__ int pow2_at_least(int n) {
