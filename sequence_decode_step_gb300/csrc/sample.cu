@@ -20,6 +20,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "qw_internal.h"
 
 namespace qw {
@@ -46,40 +48,59 @@ __device__ __forceinline__ float unpack_val(uint64_t p) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// In-place bitonic sort of n (a power of two) 64-bit keys in shared memory,
-// largest first, by all threads of the block (a power-of-two warp count). Warp w
-// owns the compare-exchange pairs [wP, (w+1)P): a stage whose stride is at most P
-// touches only that warp's elements and needs no block barrier, so only the few
-// wide stages pay one (__syncthreads before and after them).
-__device__ void sort_desc(uint64_t* s, int n) {
-  const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = max(1, (n / 2) / nw);
-  const int p0 = min(n / 2, w * P), p1 = min(n / 2, p0 + P);
-  bool synced = true;  // the caller synchronised the block before the call
+// Bitonic sort, largest first, of n = E * blockDim.x 64-bit keys held E per
+// thread in registers (thread t holds elements t*E .. t*E+E-1). A stage of
+// stride s exchanges element i with i ^ s: inside the thread when s < E, with a
+// lane of the same warp by shuffle when s < 32 E, and through shared memory `x`
+// (n keys) only for the few wider stages. Element i keeps the larger key of its
+// pair when it is the lower index of a descending block or the upper index of
+// an ascending one.
+template <int E>
+__device__ void sort_regs(uint64_t (&v)[E], uint64_t* x, int n) {
+  const int t = threadIdx.x;
   for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const bool local = stride <= P;
-      if (!local && !synced) __syncthreads();
-      for (int i = p0 + lane; i < p1; i += 32) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t a = s[lo], b = s[hi];
-        if ((a < b) == desc) {
-          s[lo] = b;
-          s[hi] = a;
+    for (int st = size >> 1; st > 0; st >>= 1) {
+      if (st < E) {
+#pragma unroll
+        for (int sc = 1; sc < E; sc <<= 1) {  // the stride as a compile-time value,
+          if (sc != st) continue;              // so v stays in registers
+#pragma unroll
+          for (int r = 0; r < E; ++r) {
+            const int pr = r ^ sc;
+            if (pr > r) {
+              const int i = t * E + r;
+              const bool desc = (i & size) == 0;  // r is the lower index of the pair
+              const uint64_t a = v[r], b = v[pr];
+              const bool swap = desc ? (a < b) : (a > b);
+              v[r] = swap ? b : a;
+              v[pr] = swap ? a : b;
+            }
+          }
         }
-      }
-      if (local) {
-        __syncwarp();
-        synced = false;
+      } else if (st < 32 * E) {
+        const int lm = st / E;  // partner lane distance
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int i = t * E + r;
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, v[r], lm);
+          const bool keep_max = ((i & size) == 0) == ((i & st) == 0);
+          v[r] = keep_max ? (v[r] > o ? v[r] : o) : (v[r] < o ? v[r] : o);
+        }
       } else {
+#pragma unroll
+        for (int r = 0; r < E; ++r) x[t * E + r] = v[r];
         __syncthreads();
-        synced = true;
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int i = t * E + r;
+          const uint64_t o = x[i ^ st];
+          const bool keep_max = ((i & size) == 0) == ((i & st) == 0);
+          v[r] = keep_max ? (v[r] > o ? v[r] : o) : (v[r] < o ? v[r] : o);
+        }
+        __syncthreads();
       }
     }
   }
-  if (!synced) __syncthreads();
 }
 
 __device__ __forceinline__ int pow2_at_least(int n) {
@@ -88,18 +109,43 @@ __device__ __forceinline__ int pow2_at_least(int n) {
   return p;
 }
 
-// Level 1: slice b of the row, its best k (padding keys are 0, below every logit).
+// Level 1: slice b of the row (4 logits per thread), its best k (padding keys are
+// 0, below every logit).
 __global__ void __launch_bounds__(256) sample_l1_kernel(const float* __restrict__ logits, int V,
                                                        int k, uint64_t* __restrict__ out) {
-  __shared__ uint64_t s[kSlice];
-  const int b = blockIdx.x, base = b * kSlice;
-  for (int i = threadIdx.x; i < kSlice; i += blockDim.x) {
-    const int g = base + i;
-    s[i] = g < V ? pack(__ldg(logits + g), (uint32_t)g) : 0ull;
+  __shared__ uint64_t x[kSlice];
+  const int b = blockIdx.x, i0 = b * kSlice + threadIdx.x * 4;
+  uint64_t v[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int g = i0 + r;
+    v[r] = g < V ? pack(__ldg(logits + g), (uint32_t)g) : 0ull;
   }
-  __syncthreads();
-  sort_desc(s, kSlice);
-  for (int i = threadIdx.x; i < k; i += blockDim.x) out[(size_t)b * k + i] = s[i];
+  sort_regs<4>(v, x, kSlice);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = threadIdx.x * 4 + r;
+    if (i < k) out[(size_t)b * k + i] = v[r];
+  }
+}
+
+// Best k of `cnt` keys at `in` into out[0, k), sorted (1024 E >= cnt keys, the
+// rest padded with 0; 1024 threads; x is the sort's exchange space).
+template <int E>
+__device__ void top_k_block(const uint64_t* __restrict__ in, int cnt, int k, uint64_t* x,
+                            uint64_t* __restrict__ out) {
+  uint64_t v[E];
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    const int i = threadIdx.x * E + r;
+    v[r] = i < cnt ? in[i] : 0ull;
+  }
+  sort_regs<E>(v, x, E * blockDim.x);
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    const int i = threadIdx.x * E + r;
+    if (i < k) out[i] = v[r];
+  }
 }
 
 // Level 2: the best k of up to kFan level-1 lists.
@@ -108,12 +154,12 @@ __global__ void __launch_bounds__(1024) sample_l2_kernel(const uint64_t* __restr
   extern __shared__ uint64_t s2[];
   const int b = blockIdx.x;
   const int l0 = b * kFan, nl = min(kFan, n_lists - l0);
-  const int n = pow2_at_least(kFan * k);
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    s2[i] = i < nl * k ? in[(size_t)l0 * k + i] : 0ull;
-  __syncthreads();
-  sort_desc(s2, n);
-  for (int i = threadIdx.x; i < k; i += blockDim.x) out[(size_t)b * k + i] = s2[i];
+  const int n = max(1024, pow2_at_least(kFan * k));
+  const uint64_t* src = in + (size_t)l0 * k;
+  uint64_t* dst = out + (size_t)b * k;
+  if (n == 1024) top_k_block<1>(src, nl * k, k, s2, dst);
+  else if (n == 2048) top_k_block<2>(src, nl * k, k, s2, dst);
+  else top_k_block<4>(src, nl * k, k, s2, dst);
 }
 
 // Level 3: the best k of all level-2 lists, then the draw (thread 0 walks the
@@ -121,19 +167,22 @@ __global__ void __launch_bounds__(1024) sample_l2_kernel(const uint64_t* __restr
 __global__ void __launch_bounds__(1024) sample_l3_kernel(const uint64_t* __restrict__ in, int n_lists,
                                                         int k, float temperature, float top_p,
                                                         float u, int32_t* __restrict__ token) {
-  extern __shared__ uint64_t s3[];
+  extern __shared__ uint64_t s3[];  // [n] exchange space, then the k candidates
   __shared__ double w[kMaxSampleTopK];
-  const int n = pow2_at_least(n_lists * k);
-  for (int i = threadIdx.x; i < n; i += blockDim.x) s3[i] = i < n_lists * k ? in[i] : 0ull;
+  __shared__ uint64_t cand[kMaxSampleTopK];
+  const int n = max(1024, pow2_at_least(n_lists * k));
+  if (n == 1024) top_k_block<1>(in, n_lists * k, k, s3, cand);
+  else if (n == 2048) top_k_block<2>(in, n_lists * k, k, s3, cand);
+  else top_k_block<4>(in, n_lists * k, k, s3, cand);
   __syncthreads();
-  sort_desc(s3, n);
-  const float l0 = unpack_val(s3[0]);
+  uint64_t* s3c = cand;
+  const float l0 = unpack_val(s3c[0]);
   const bool bad = (l0 != l0) || l0 == -INFINITY;  // a NaN in the row, or nothing finite
   const bool greedy = !(temperature > 0.f) || k == 1;
   if (!bad && !greedy) {
     const double t = (double)temperature;
     for (int i = threadIdx.x; i < k; i += blockDim.x)
-      w[i] = exp(((double)unpack_val(s3[i]) - (double)l0) / t);
+      w[i] = exp(((double)unpack_val(s3c[i]) - (double)l0) / t);
   }
   __syncthreads();
   if (threadIdx.x != 0) return;
@@ -142,7 +191,7 @@ __global__ void __launch_bounds__(1024) sample_l3_kernel(const uint64_t* __restr
     return;
   }
   if (greedy) {
-    *token = (int32_t)unpack_idx(s3[0]);
+    *token = (int32_t)unpack_idx(s3c[0]);
     return;
   }
   // running sums in candidate order (kept in w), then the two searches
@@ -166,7 +215,7 @@ __global__ void __launch_bounds__(1024) sample_l3_kernel(const uint64_t* __restr
       pick = i;
       break;
     }
-  *token = (int32_t)unpack_idx(s3[pick]);
+  *token = (int32_t)unpack_idx(s3c[pick]);
 }
 
 }  // namespace
@@ -212,9 +261,9 @@ cudaError_t launch_sample(const float* logits, int V, int k, float temperature, 
   uint64_t* w1 = (uint64_t*)workspace;
   uint64_t* w2 = w1 + (size_t)n1 * k;
   sample_l1_kernel<<<n1, 256, 0, s>>>(logits, V, k, w1);
-  const size_t smem2 = (size_t)pow2_host(kFan * k) * 8;
+  const size_t smem2 = (size_t)std::max(1024, pow2_host(kFan * k)) * 8;
   sample_l2_kernel<<<n2, 1024, smem2, s>>>(w1, n1, k, w2);
-  const size_t smem3 = (size_t)pow2_host(n2 * k) * 8;
+  const size_t smem3 = (size_t)std::max(1024, pow2_host(n2 * k)) * 8;
   sample_l3_kernel<<<1, 1024, smem3, s>>>(w2, n2, k, temperature, top_p, u, token);
   return cudaGetLastError();
 }

@@ -1,7 +1,7 @@
 """Drive a few decode steps of a workload for profilers (ncu) and quick timing.
 
   python -m sequence_decode_step_gb300.profile_decode [--workload NAME] [--tokens N]
-         [--lm-head N] [--prefill-reps N] [--path 0|1]
+         [--lm-head N] [--prefill-reps N] [--path 0|1] [--sample N]
 
 Draws the workload's weights, prefills its prompt (or preloads its KV cache),
 runs N greedy decode tokens as graph replays, then N stand-alone LM-head
@@ -30,6 +30,8 @@ def main():
     ap.add_argument("--prefill-reps", type=int, default=0,
                     help="batched prefills of the workload's prompt to run first")
     ap.add_argument("--path", type=int, default=0, help="decode path: 0 persistent, 1 graph")
+    ap.add_argument("--sample", type=int, default=0,
+                    help="qw_sample calls on the handle's last logits row (T 0.7, top_k 50, top_p 0.9)")
     args = ap.parse_args()
     wl = W.WORKLOADS[args.workload]
     d = W.draw(wl)
@@ -86,6 +88,20 @@ def main():
         if rc:
             raise SystemExit(B.last_error())
         print(f"lm head: {e0.elapsed_time(e1) * 1e3 / args.lm_head:.1f} us/launch")
+    if args.sample:
+        tok = torch.empty(1, dtype=torch.int32, device="cuda")
+        wsb = L.qw_sample_workspace_bytes(s.vocab, 50)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        lg = m._logits_buf()
+        m.decode(-1, logits=True)  # one more step, its logits row in lg
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.sample):
+            B.qw_sample(lg.data_ptr(), s.vocab, 0.7, 50, 0.9, (i + 0.5) / args.sample,
+                        tok.data_ptr(), ws.data_ptr(), wsb, stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        print(f"sample: {e0.elapsed_time(e1) * 1e3 / args.sample:.1f} us/call, last id {int(tok.item())}")
     m.close()
 
 
