@@ -806,6 +806,9 @@ static int ensure_graph(qw_handle* h) {
 static int ensure_graph_once(qw_handle* h) {
   if (h->exec && !h->graph_dirty) return QW_OK;
   if (h->exec) {
+    // replays of the old graph may still be queued (a greedy run crossing the
+    // switch between kernel builds): let them finish before it goes
+    QW_CUDA(h, cudaStreamSynchronize(h->stream));
     cudaGraphExecDestroy(h->exec);
     h->exec = nullptr;
   }

@@ -186,6 +186,16 @@ def test_decode_across_the_long_context_switch(longctx_drawn):
         assert n >= 4
         kd, _ = m.kv(3)
         assert violation(kd.cpu().numpy()[:, 1532:1540], o.k_cache[3][:, 1532:1540]) <= 0
+        # a device-resident greedy run across the switch (the graph is replaced while
+        # earlier replays are queued) gives the ids of the same run step by step
+        m.set_pos(1532)
+        ids_run = m.greedy(d.start_token, 8)
+        m.set_pos(1532)
+        ids_steps, tok = [], d.start_token
+        for _ in range(8):
+            tok = m.decode(tok)
+            ids_steps.append(tok)
+        assert list(ids_run) == ids_steps
     finally:
         m.close()
 
