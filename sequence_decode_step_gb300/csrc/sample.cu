@@ -226,10 +226,10 @@ static int pow2_host(int n) {
   return p;
 }
 
-int sample_levels(int V, int* n1, int* n2) {
+// CTAs of levels 1 and 2 for a row of V logits.
+static void sample_levels(int V, int* n1, int* n2) {
   *n1 = (V + kSlice - 1) / kSlice;
   *n2 = (*n1 + kFan - 1) / kFan;
-  return 0;
 }
 
 size_t sample_workspace_bytes(int V, int k) {
