@@ -476,3 +476,88 @@ def test_int4_model_uses_exact_dequantised_weights():
         p, s = R.int4_quantize(d.weights[name])
         np.testing.assert_array_equal(m.w[name], R.int4_dequantize(p, s))
     assert "embed" not in m.int4
+
+
+# ------------------------------------------------------------------ block wiring (hand-set weights)
+# The "Failed Star / fs, M2" page, "One prefill, all shapes visible", gives the block as
+# two sublayers on the residual bus: attention (read through the attention-input norm)
+# then the SwiGLU MLP (read through the post-attention norm), each added back; the
+# "SuperKittens PR #7" page names the fused kernel SiLU(gate) * up. The two cases below
+# set every weight by hand to small bf16-exact values so each intermediate is a number
+# derived in the comments; swapping gate/up, the two sublayer gains, or the q/k norm
+# gains moves the result far outside the tolerance.
+def _bits(a):
+    return W.f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def _hand_model(weights, **kw):
+    cfg = R.Config(n_layers=1, hidden=4, n_q_heads=1, n_kv_heads=1, head_dim=2,
+                   intermediate=2, vocab=3, eps=0.0, **kw)
+    return R.OracleModel(cfg, {k: _bits(v) for k, v in weights.items()}, max_ctx=4)
+
+
+def test_block_wiring_gate_up_and_sublayer_gains_hand_case():
+    E = [[2, 0, 0, 0], [0, 0, 0, 1], [1, 1, 1, 1]]
+    m = _hand_model({
+        "embed": E,
+        "layers.0.attn_norm": [0.25, 1, 1, 1],
+        "layers.0.q": np.zeros((2, 4)), "layers.0.k": np.zeros((2, 4)),
+        "layers.0.v": [[2, 0, 0, 0], [0, 0, 0, 0]],
+        "layers.0.o": [[0, 0], [2, 0], [2, 0], [2, 0]],
+        "layers.0.mlp_norm": [0.5, 0.25, 1, 2],
+        "layers.0.gate": [[4, 0, 0, 0], [0, 0, 0, 0]],
+        "layers.0.up": [[0, 12, 0, 0], [0, 0, 0, 0]],
+        "layers.0.down": [[0, 0], [0, 0], [0, 0], [1, 0]],
+        "final_norm": [1, 1, 1, 1],
+    }, qk_norm=False)
+    cp = m.decode_step(0)
+    # x = E[0] = (2,0,0,0): mean square 1, so the attention input is x * attn_norm = (0.5,0,0,0);
+    # v = (1, 0); one visible key, so the attention output is v; o_proj adds (0,2,2,2).
+    # x1 = (2,2,2,2): mean square 4, root 2, so the MLP input is mlp_norm = (0.5,0.25,1,2);
+    # gate = 4 * 0.5 = 2, up = 12 * 0.25 = 3; m0 = silu(2) * 3 = 6 / (1 + e^-2); down adds m0 to x[3].
+    m0 = 6.0 / (1.0 + math.exp(-2.0))
+    x2 = np.array([2.0, 2.0, 2.0, 2.0 + m0])
+    np.testing.assert_allclose(cp["block0"][0], x2, rtol=1e-6)
+    h = x2 / math.sqrt(np.mean(x2 * x2))
+    np.testing.assert_allclose(cp["final_norm"][0], h, rtol=1e-6)
+    np.testing.assert_allclose(cp["logits"], np.array(E, np.float64) @ h, rtol=1e-6, atol=1e-7)
+    # wrong wirings land far away: silu(3) * 2 for a swapped gate/up; with the two gains
+    # swapped the attention input is (1,0,0,0), o_proj adds (0,4,4,4) and x1 = (2,4,4,4)
+    assert abs(6.0 / (1.0 + math.exp(-3.0)) - m0) > 0.4
+    assert abs(cp["block0"][0][1] - 4.0) > 1.0
+
+
+def test_block_wiring_qk_norm_gains_rope_and_causal_mask_hand_case():
+    E = [[2, 0, 0, 0], [0, 2, 0, 0], [1, 1, 1, 1]]
+    m = _hand_model({
+        "embed": E,
+        "layers.0.attn_norm": [1, 1, 1, 1],
+        "layers.0.q": [[0.5, 0.5, 0, 0], [0, 0.5, 0, 0]],    # q(id 0) = (1, 0), q(id 1) = (1, 1)
+        "layers.0.k": [[0.5, 0.5, 0, 0], [0, 0.5, 0, 0]],    # k(id 0) = (1, 0), k(id 1) = (1, 1)
+        "layers.0.v": [[0.5, 0, 0, 0], [0, 0.5, 0, 0]],      # v(id 0) = (1, 0), v(id 1) = (0, 1)
+        "layers.0.q_norm": [2, 1], "layers.0.k_norm": [1, 4],
+        "layers.0.o": [[0, 0], [0, 0], [1, 0], [0, 1]],
+        "layers.0.mlp_norm": [1, 1, 1, 1],
+        "layers.0.gate": np.zeros((2, 4)), "layers.0.up": np.zeros((2, 4)),
+        "layers.0.down": np.zeros((4, 2)),
+        "final_norm": [1, 1, 1, 1],
+    }, qk_norm=True, rope_theta=1e6)
+    cp = m.prefill([0, 1])
+    # Row 1 (position 1). QK-norm over head_dim 2 with eps 0: q = (1,1) has RMS 1 -> times (2,1) = (2, 1);
+    # k0 = (1,0) has RMS 1/sqrt(2) -> (sqrt2, 0); k1 = (1,1) -> (1, 4). head_dim 2 has one
+    # rotary pair with inv_freq 1, so position 1 turns by 1 rad and position 0 not at all:
+    #   s0 = R(1)(2,1) . (sqrt2, 0) / sqrt2 = 2 cos1 - sin1
+    #   s1 = R(1)(2,1) . R(1)(1,4) / sqrt2 = (2 + 4) / sqrt2          (rotation-invariant)
+    # The output is p0 v0 + p1 v1 = (p0, p1); o_proj puts it on x[2], x[3].
+    c, s = math.cos(1.0), math.sin(1.0)
+    s0, s1 = 2 * c - s, 6 / math.sqrt(2)
+    p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    x1 = np.array([0.0, 2.0, p0, 1.0 - p0])
+    np.testing.assert_allclose(cp["block0"][1], x1, rtol=1e-6, atol=1e-7)
+    # row 0 sees only its own key: output v0 = (1, 0)
+    np.testing.assert_allclose(cp["block0"][0], [2.0, 0.0, 1.0, 0.0], rtol=1e-6, atol=1e-7)
+    h = x1 / math.sqrt(np.mean(x1 * x1))
+    np.testing.assert_allclose(cp["logits"], np.array(E, np.float64) @ h, rtol=1e-6, atol=1e-7)
+    # swapped q/k norm gains would give s0 = 2 cos1 - 8 sin1: p0 moves far
+    p0_swapped = 1.0 / (1.0 + math.exp(s1 - (2 * c - 8 * s)))
+    assert abs(p0_swapped - p0) > 0.01
