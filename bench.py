@@ -48,18 +48,63 @@ def step_bytes(s, p0: int, n: int) -> int:
     return n * weight_bytes(s) + sum(kv_bytes(s, p) for p in range(p0, p0 + n))
 
 
-def profiled_traffic(name: str):
-    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) recorded
-    in a committed ncu summary under profiles/, or None."""
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the two
+# kernels the JSON line reports, each from one ncu capture of a build, keyed by the
+# SHA-256 of the source files that build compiles from. ncu cannot run inside a
+# timed bench, so the figure is recorded here; as soon as a listed source changes
+# the digest no longer matches and the line reports traffic as null.
+KERNEL_SOURCES = {
+    "decode_mega": ["decode_mega.cu", "qw_ptx.cuh", "qw_internal.h"],
+    "lm_head_gemv": ["decode_kernels.cu", "qw_ptx.cuh", "qw_internal.h"],
+}
+NCU_TRAFFIC = {
+    # kernel: (sources digest, bytes per launch, what was captured)
+}
+
+
+def sources_digest(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sequence_decode_step_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """(bytes per launch, note) from the ncu capture of this exact build, or (None, why)."""
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec is None:
+        return None, "no ncu capture recorded for this kernel"
+    digest, nbytes, what = rec
+    if digest != sources_digest(kernel):
+        return None, "the kernel's sources changed since its ncu capture"
+    return nbytes, f"ncu capture of this build ({what}), not measured in this run"
+
+
+def host_cpu() -> dict:
+    """CPU model and logical core count of this host."""
+    model = ""
     try:
-        with open(os.path.join(ROOT, "profiles", name)) as f:
-            for ln in f:
-                if ln.startswith("traffic_bytes_per_launch:"):
-                    v = ln.split(":", 1)[1].strip()
-                    return None if v in ("", "null") else int(float(v))
-    except OSError:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
         pass
-    return None
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"cpu_model": model or platform.processor() or platform.machine(),
+            "nproc": os.cpu_count()}
 
 
 def measured_peaks() -> dict:
@@ -227,7 +272,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
                     "bound": "hbm", "bytes_per_launch": bytes_step / n_tok,
                     "achieved": bytes_step / n_tok / sec_tok / 1e9, "peak": hbm, "unit": "GB/s",
                     "frac": bytes_step / n_tok / sec_tok / 1e9 / hbm,
-                    "traffic": profiled_traffic("decode_mega_qwen3_0.6b.md"),
+                    "traffic": recorded_traffic("decode_mega")[0],
+                    "traffic_source": recorded_traffic("decode_mega")[1],
                     "us_per_launch": sec_tok * 1e6,
                     "timing": "CUDA events on the launching stream around the timed steps, "
                               "divided by the launches (one per token)",
@@ -339,10 +385,11 @@ def lm_head_roofline(L, B, torch, d, s, stream) -> dict:
     algo = s.vocab * s.hidden * 2 + s.vocab * 4 + s.hidden * 6
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
-    traffic = profiled_traffic("gemv_lm_head_qwen3_0.6b.md")
+    traffic, traffic_src = recorded_traffic("lm_head_gemv")
     return {"kernel": "gemv_kernel<EPI_LOGITS> (final RMSNorm + tied LM head + argmax)",
             "bound": "hbm", "achieved": algo / sec / 1e9, "peak": hbm, "unit": "GB/s",
-            "frac": algo / sec / 1e9 / hbm, "traffic": traffic, "bytes_per_launch": algo,
+            "frac": algo / sec / 1e9 / hbm, "traffic": traffic, "traffic_source": traffic_src,
+            "bytes_per_launch": algo,
             "us_per_launch": sec * 1e6,
             "peak_source": "measured burst copy (MEASURED_PEAKS.json hbm_gbs)" if peaks
             else "fallback 6800 GB/s"}
@@ -437,7 +484,7 @@ def cpu_baseline(budget_s: float = 15.0) -> dict:
     return {"value": o["tok_per_s"], "unit": "tok/s", "cores": 1, "kind": "oracle",
             "sample": f"{WORKLOAD}: 5-id prompt prefill (untimed), then {o['tokens']} greedy "
                       f"decode tokens from position 5 ({o['seconds']:.1f} s), numpy oracle, "
-                      "one BLAS thread"}
+                      "one BLAS thread", **host_cpu()}
 
 
 def run_reference(args) -> dict:
@@ -458,7 +505,8 @@ def run_reference(args) -> dict:
                        "l2": "n/a (CPU)", "parallelism": "single host thread"},
             "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
                              "sample": f"{o['tokens']} greedy decode tokens of {WORKLOAD} "
-                                       f"from position 5, numpy oracle, one BLAS thread"},
+                                       f"from position 5, numpy oracle, one BLAS thread",
+                             **host_cpu()},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

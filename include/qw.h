@@ -220,7 +220,11 @@ int qw_get_capture(qw_handle* h, int32_t which, float* out_host, size_t n_floats
  * per token (the default whenever the shape fits: bf16 weights, hidden,
  * intermediate and n_q_heads*head_dim <= 3072); 1: the graph of separate
  * kernels (always available). Asking for 0 on a shape that does not fit keeps 1.
- * Both compute the same step; results agree to f32 rounding. */
+ * Both compute the same step; results agree to f32 rounding. If the persistent
+ * kernel cannot be recorded on this device (no cooperative launch), the handle
+ * switches to 1 for the rest of its life: the step still succeeds, one line goes
+ * to stderr, qw_last_error(h) holds a note saying why, and qw_get_decode_path
+ * returns 1. */
 int qw_set_decode_path(qw_handle* h, int32_t path);
 int qw_get_decode_path(const qw_handle* h, int32_t* path);
 
@@ -229,7 +233,8 @@ int qw_get_decode_path(const qw_handle* h, int32_t* path);
 int qw_set_wait_limit_ns(qw_handle* h, uint64_t ns);
 
 /* Text of the last error on this handle (or of the last failed handle-less
- * call when h is NULL). Valid until the next call. */
+ * call when h is NULL), or the note of a decode-path switch (see
+ * qw_set_decode_path). Valid until the next call. */
 const char* qw_last_error(const qw_handle* h);
 
 void qw_destroy(qw_handle* h);
@@ -258,10 +263,14 @@ int qw_quantize_int4_g128(const float* w, int32_t rows, int32_t cols, uint8_t* p
  *   q_norm, k_norm: bf16 [hd] DEVICE or NULL
  *   k_cache, v_cache: f32 [nkv, cap, hd] DEVICE; row pos is written
  *   out:       f32 [nq * hd] DEVICE
- *   n_splits:  most key splits per KV head (>= 1)
+ *   n_splits:  most key splits per KV head, with (nq / nkv) * (n_splits + 1) at most
+ *              192 * hd (the combine keeps its weights in the kernel's tile buffers)
  *   workspace: DEVICE scratch of qw_attention_workspace_bytes(...) bytes,
  *              zero-filled before its first use and left zeroed by every call.
- * Errors: QW_ERR_ARG for unsupported shapes, pos outside [0, cap), or a short workspace. */
+ * Errors: QW_ERR_ARG for unsupported shapes (nq or nkv <= 0 included), too many
+ * splits, pos outside [0, cap), or a short workspace; all are found on the host
+ * before any launch. A device-side wait that gives up is not reported by this
+ * unit-check op (its outputs are then invalid); the decode step reports it. */
 size_t qw_attention_workspace_bytes(int32_t nq, int32_t nkv, int32_t hd, int32_t n_splits);
 int qw_attention_decode(const float* qkv, const uint16_t* q_norm, const uint16_t* k_norm,
                         float* k_cache, float* v_cache, int32_t nq, int32_t nkv, int32_t hd,
@@ -281,7 +290,9 @@ int qw_attention_decode(const float* qkv, const uint16_t* q_norm, const uint16_t
  * kernel attributes, so make it before any stream capture on that device.
  * Every call shares the one array and clears its counters on `stream`: calls
  * that overlap on the GPU (different streams, or several host threads) race
- * and must be serialised by the caller. No call allocates memory. */
+ * and must be serialised by the caller. No call allocates memory. Failures set
+ * qw_last_error(NULL) text like the other handle-less calls; a device-side wait
+ * that gives up is not reported, as for qw_attention_decode. */
 size_t qw_attention_noalloc_max_bytes(void);
 int qw_attention_decode_noalloc(const float* qkv, const uint16_t* q_norm, const uint16_t* k_norm,
                                 float* k_cache, float* v_cache, int32_t nq, int32_t nkv,
@@ -300,6 +311,25 @@ size_t qw_lm_head_workspace_bytes(void);
 int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16_t* table, int32_t vocab,
                       int32_t hidden, float eps, float* logits, int32_t* argmax_dev,
                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* int4 group-128 matrix-vector product, the contraction the decode step runs for
+ * int4 weights ("Emberglass" README, "Why it's hard": int4 group-128 weights,
+ * dequantised inside the matvec):
+ *   y[r] = sum_c W'[r][c] x[c],  W'[r][c] = (nibble(r, c) - 8) * scale[r][c / 128]
+ *   packed: u8 [rows, cols/2] DEVICE, element 2i in the low nibble of byte i;
+ *   scales: bf16 bits [rows, cols/128] DEVICE (the layout qw_quantize_int4_g128 writes);
+ *   x: f32 [cols] DEVICE; y: f32 [rows] DEVICE; cols a multiple of 128, at most 16384;
+ *   workspace: DEVICE scratch of qw_gemv_int4_workspace_bytes(rows, cols) bytes,
+ *   16-byte aligned, no initialisation needed: the rows are repacked there (a row's
+ *   nibbles, then its scales) and the decode step's int4 GEMV kernel runs on them.
+ * The dequantisation is exact in f32 (a 4-bit integer times a bf16), so with
+ * x = e_j the result is column j of W' bit for bit. Like the other stand-alone
+ * ops it does not report a device-side wait that gave up (its outputs are then
+ * invalid); QW_ERR_ARG for the argument errors above. */
+size_t qw_gemv_int4_workspace_bytes(int32_t rows, int32_t cols);
+int qw_gemv_int4_g128(const uint8_t* packed, const uint16_t* scales, int32_t rows, int32_t cols,
+                      const float* x, float* y, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /* Sampling on the device ("flashmoon demo" README: greedy plus temperature / top-k /
  * top-p sampling, temp = 0 meaning greedy; the demo reads every logits row back to

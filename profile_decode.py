@@ -1,6 +1,6 @@
 """Drive a few decode steps of a workload for profilers (ncu) and quick timing.
 
-  python -m sequence_decode_step_gb300.profile_decode [--workload NAME] [--tokens N]
+  python profile_decode.py [--workload NAME] [--tokens N]
          [--lm-head N] [--prefill-reps N] [--path 0|1] [--sample N]
 
 Draws the workload's weights, prefills its prompt (or preloads its KV cache),
@@ -12,7 +12,7 @@ import argparse
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 

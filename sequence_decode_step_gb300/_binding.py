@@ -114,6 +114,9 @@ _SIG = {
                             C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "qw_sample_last": (C.c_int, [C.c_void_p, C.c_float, C.c_int32, C.c_float, C.c_float,
                                  C.POINTER(C.c_int32)]),
+    "qw_gemv_int4_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "qw_gemv_int4_g128": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
+                                    C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "qw_lm_head_workspace_bytes": (C.c_size_t, []),
     "qw_lm_head_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                     C.c_float, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,

@@ -34,23 +34,39 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 extern "C" size_t qw_attention_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
 
+// Failure with qw_last_error(NULL) text, as the other handle-less calls report.
+static int fail(int code, const char* msg) {
+  qw::set_op_error(msg);
+  return code;
+}
+
 extern "C" int qw_attention_decode_noalloc(const float* qkv, const uint16_t* q_norm,
                                            const uint16_t* k_norm, float* k_cache, float* v_cache,
                                            int32_t nq, int32_t nkv, int32_t hd, int32_t cap,
                                            int32_t pos, float eps, float rope_theta,
                                            int32_t n_splits, float* out, void* stream) {
-  if (!qkv || !k_cache || !v_cache || !out) return QW_ERR_ARG;
+  if (!qkv || !k_cache || !v_cache || !out)
+    return fail(QW_ERR_ARG, "qw_attention_decode_noalloc: null buffer");
   if ((hd != 64 && hd != 128) || nkv <= 0 || nq <= 0 || nq % nkv ||
       nq / nkv > qw::attention_gq_max() || n_splits <= 0 || n_splits > 65535)
-    return QW_ERR_ARG;
-  if (pos < 0 || pos >= cap) return QW_ERR_ARG;
+    return fail(QW_ERR_ARG, "qw_attention_decode_noalloc: unsupported shape");
+  if (!qw::attention_splits_fit(nq / nkv, hd, n_splits))
+    return fail(QW_ERR_ARG,
+                "qw_attention_decode_noalloc: n_splits too large for the combine (query heads "
+                "per KV head x (n_splits + 1) must fit 192 x head_dim floats)");
+  if (pos < 0 || pos >= cap)
+    return fail(QW_ERR_ARG, "qw_attention_decode_noalloc: pos outside [0, cap)");
   const size_t head = align256(((size_t)nkv + 1) * 4);
   const size_t ml = align256((size_t)nq * n_splits * 2 * 4);
   const size_t need = head + ml + (size_t)nq * n_splits * hd * 4;
-  if (need > kNoAllocScratchBytes) return QW_ERR_SIZE;  // shapes beyond the fixed scratch
+  if (need > kNoAllocScratchBytes)  // shapes beyond the fixed scratch
+    return fail(QW_ERR_SIZE,
+                "qw_attention_decode_noalloc: the shape needs more scratch than the fixed 1 MiB "
+                "array (256 + nq * n_splits * (hd + 2) * 4 bytes, rounded)");
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QW_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(QW_ERR_CUDA, "qw_attention_decode_noalloc: no current CUDA device (or id >= 64)");
   void* base = nullptr;
   {
     // Set-up, once per device, with that device current: the host-side name of
@@ -59,8 +75,9 @@ extern "C" int qw_attention_decode_noalloc(const float* qkv, const uint16_t* q_n
     if (!g_scratch_ptr[dev]) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr)
-        return QW_ERR_CUDA;
-      if (qw::set_kernel_attributes() != cudaSuccess) return QW_ERR_CUDA;
+        return fail(QW_ERR_CUDA, "qw_attention_decode_noalloc: cudaGetSymbolAddress failed");
+      if (qw::set_kernel_attributes() != cudaSuccess)
+        return fail(QW_ERR_CUDA, "qw_attention_decode_noalloc: setting kernel attributes failed");
       g_scratch_ptr[dev] = p;
     }
     base = g_scratch_ptr[dev];
@@ -68,7 +85,8 @@ extern "C" int qw_attention_decode_noalloc(const float* qkv, const uint16_t* q_n
   cudaStream_t s = (cudaStream_t)stream;
   // The arrival counters and the error word must start at zero; the partials
   // are fully written by the kernel before they are read.
-  if (cudaMemsetAsync(base, 0, head, s) != cudaSuccess) return QW_ERR_CUDA;
+  if (cudaMemsetAsync(base, 0, head, s) != cudaSuccess)
+    return fail(QW_ERR_CUDA, "qw_attention_decode_noalloc: clearing the counters failed");
 
   uint8_t* ws = (uint8_t*)base;
   qw::AttnArgs t{};
@@ -93,6 +111,7 @@ extern "C" int qw_attention_decode_noalloc(const float* qkv, const uint16_t* q_n
   t.part_o = (float*)(ws + head + ml);
   t.out = out;
   t.wait_ns = 1000000000ull;
-  if (qw::launch_attention(t, hd, false, s) != cudaSuccess) return QW_ERR_CUDA;
+  if (qw::launch_attention(t, hd, false, s) != cudaSuccess)
+    return fail(QW_ERR_CUDA, "qw_attention_decode_noalloc: kernel launch failed");
   return QW_OK;
 }

@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
   // sum (a warp per head), then each thread sums 4 output dims over the splits in
   // order, 16 float4 loads in flight at a time.
   float* wsm = stage0;  // [GQ][nsplit] (the tile stages are free now)
-  float* den_s = wsm + GQM * a.nsplit_max;
+  float* den_s = wsm + GQ * nsplit;  // [GQ]; the host keeps GQ * (nsplit_max + 1) within the stages
   for (int h = warp; h < GQ; h += 8) {
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + (size_t)(g * GQ + h) * a.nsplit_max;
     float m = -INFINITY;
@@ -669,6 +669,11 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
 }
 
 size_t attention_smem_bytes(int hd) { return hd == 64 ? attn_smem<64>() : attn_smem<128>(); }
+bool attention_splits_fit(int gq, int hd, int n_splits) {
+  // the combine keeps GQ x nsplit weights and GQ denominators in the tile stages
+  const long long stage_floats = (long long)kAttnNS * 2 * kAttnTK * hd;
+  return n_splits >= 1 && (long long)gq * ((long long)n_splits + 1) <= stage_floats;
+}
 int attention_gq_max() { return kAttnGQ; }
 
 cudaError_t launch_attention(const AttnArgs& a, int hd, bool pdl, cudaStream_t s) {

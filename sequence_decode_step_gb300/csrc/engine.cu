@@ -14,6 +14,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
@@ -793,14 +794,23 @@ static int ensure_graph_once(qw_handle* h);
 
 // Record (or re-record) the step graph; a persistent kernel that cannot be
 // recorded or instantiated (e.g. no cooperative launch) falls back to the
-// multi-kernel graph for the rest of the handle's life.
+// multi-kernel graph for the rest of the handle's life. The switch is not silent:
+// the handle's last-error text carries a note (the call itself succeeds), one
+// line goes to stderr, and qw_get_decode_path reports 1 from then on.
 static int ensure_graph(qw_handle* h) {
   const int rc = ensure_graph_once(h);
   if (rc == QW_OK || !h->use_mega) return rc;
+  const std::string why = h->err;
   h->use_mega = false;
   h->mega_ok = false;
   h->graph_dirty = true;
-  return ensure_graph_once(h);
+  const int rc2 = ensure_graph_once(h);
+  if (rc2 == QW_OK) {
+    h->err = "note: the persistent decode kernel could not be recorded (" + why +
+             "); this handle runs the multi-kernel decode graph from now on";
+    fprintf(stderr, "qw: %s\n", h->err.c_str());
+  }
+  return rc2;
 }
 
 static int ensure_graph_once(qw_handle* h) {
@@ -1231,6 +1241,10 @@ static int op_sms(int* sms) {
   return QW_OK;
 }
 
+namespace qw {
+void set_op_error(const char* msg) { g_last_error = msg; }
+}  // namespace qw
+
 #define QW_OP_CUDA(call)                                                        \
   do {                                                                          \
     cudaError_t e_ = (call);                                                    \
@@ -1264,9 +1278,13 @@ extern "C" int qw_attention_decode(const float* qkv, const uint16_t* q_norm, con
                                    size_t workspace_bytes, void* stream) {
   if (!qkv || !k_cache || !v_cache || !out || !workspace)
     QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: null buffer");
-  if ((hd != 64 && hd != 128) || nkv <= 0 || nq % nkv || nq / nkv > attention_gq_max() ||
+  if ((hd != 64 && hd != 128) || nkv <= 0 || nq <= 0 || nq % nkv || nq / nkv > attention_gq_max() ||
       n_splits <= 0 || n_splits > 65535)
     QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: unsupported shape");
+  if (!attention_splits_fit(nq / nkv, hd, n_splits))
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            "qw_attention_decode: n_splits too large for the combine (query heads per KV head x "
+            "(n_splits + 1) must fit 192 x head_dim floats)");
   if (pos < 0 || pos >= cap) QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: pos outside [0, cap)");
   if (workspace_bytes < qw_attention_workspace_bytes(nq, nkv, hd, n_splits))
     QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_attention_decode: workspace too small");
@@ -1334,6 +1352,48 @@ extern "C" int qw_lm_head_argmax(const float* x, const uint16_t* g, const uint16
   a.wait_ns = 1000000000ull;
   plan_gemv(a, grid, kStreamStage, kStreamStages);
   QW_OP_CUDA(launch_gemv(EPI_LOGITS, a, grid, false, (cudaStream_t)stream));
+  return QW_OK;
+}
+
+// int4 GEMV workspace: [err int] padded to 256, then the rows repacked as the decode
+// step streams them (int4_row_bytes(cols) each: nibbles, scales, zero pad).
+extern "C" size_t qw_gemv_int4_workspace_bytes(int32_t rows, int32_t cols) {
+  if (rows <= 0 || cols <= 0 || cols % 128) return 0;
+  return 256 + (size_t)rows * int4_row_bytes(cols);
+}
+
+extern "C" int qw_gemv_int4_g128(const uint8_t* packed, const uint16_t* scales, int32_t rows,
+                                 int32_t cols, const float* x, float* y, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!packed || !scales || !x || !y || !workspace)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_gemv_int4_g128: null buffer");
+  if (rows <= 0 || cols <= 0 || cols % 128 || cols > 16384)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            "qw_gemv_int4_g128: rows must be positive and cols a multiple of 128, at most 16384");
+  if (workspace_bytes < qw_gemv_int4_workspace_bytes(rows, cols) || ((uintptr_t)workspace & 15))
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            "qw_gemv_int4_g128: workspace too small or not 16-byte aligned");
+  int sms = 0;
+  if (op_sms(&sms)) return QW_ERR_CUDA;
+  uint8_t* ws = (uint8_t*)workspace;
+  uint8_t* rows_dev = ws + 256;
+  const cudaStream_t st = (cudaStream_t)stream;
+  QW_OP_CUDA(launch_pack_int4_rows(packed, scales, rows, cols, rows_dev, 0, 1, st));
+  const int grid = std::min(rows, sms);
+  GemvArgs a{};
+  a.w = rows_dev;
+  a.n_units = rows;
+  a.rpu = 1;
+  a.K = cols;
+  a.w4 = 1;
+  a.row_bytes = int4_row_bytes(cols);
+  a.scale_off = (uint32_t)cols / 2;
+  a.x = x;
+  a.y = y;
+  a.err = (int*)ws;
+  a.wait_ns = 1000000000ull;
+  plan_gemv(a, grid, kStreamStage, kStreamStages);
+  QW_OP_CUDA(launch_gemv(EPI_STORE, a, grid, false, st));
   return QW_OK;
 }
 

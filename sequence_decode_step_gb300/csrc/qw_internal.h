@@ -111,6 +111,12 @@ cudaError_t launch_gemv(int epi, const GemvArgs& a, int grid, bool pdl, cudaStre
 cudaError_t launch_attention(const AttnArgs& a, int hd, bool pdl, cudaStream_t s);
 size_t attention_smem_bytes(int hd);
 int attention_gq_max();
+// Whether a stand-alone attention call with `n_splits` key splits per KV head and
+// `gq` query heads per KV head fits the combine's scratch in the tile stages.
+bool attention_splits_fit(int gq, int hd, int n_splits);
+// Text for qw_last_error(NULL) after a failed handle-less call (stand-alone ops
+// outside engine.cu).
+void set_op_error(const char* msg);
 constexpr int kAttnMinKeys = 64;
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s);
 const void* embed_kernel_fn();

@@ -94,3 +94,38 @@ def test_sample_arguments_checked_before_cuda(L):
         assert L.qw_sample(1, vocab, t, k, p, u, 1, 1, 1 << 30, None) == B.QW_ERR_ARG, (vocab, k, p, u)
     assert L.qw_sample(1, V, 1.0, 64, 0.9, 0.5, 1, 1, ws - 8, None) == B.QW_ERR_ARG  # workspace
     assert L.qw_sample_last(None, 1.0, 8, 0.9, 0.5, None) == B.QW_ERR_ARG
+
+
+def test_attention_arguments_checked_before_any_launch(L):
+    # every case returns from the host checks: no kernel runs on these dummy pointers
+    a = (1, None, None, 1, 1)
+    # nq = 0 is an empty shape, not a zero-size workspace
+    assert L.qw_attention_decode(*a, 0, 8, 128, 16, 3, 1e-6, 1e6, 4, 1, 1, 1 << 30,
+                                 None) == B.QW_ERR_ARG
+    # head_dim 64, one query head per KV head: 20000 splits overflow the combine's buffers
+    assert L.qw_attention_decode(*a, 1, 1, 64, 40000, 39999, 1e-6, 1e6, 20000, 1, 1, 1 << 34,
+                                 None) == B.QW_ERR_ARG
+    assert "n_splits" in B.last_error()
+    assert L.qw_attention_decode_noalloc(*a, 2, 2, 64, 20000, 19999, 1e-6, 1e6, 13000, 1,
+                                         None) == B.QW_ERR_ARG
+    assert "n_splits" in B.last_error()
+    assert L.qw_attention_decode_noalloc(*a, 0, 2, 64, 8, 3, 1e-6, 1e6, 4, 1, None) == B.QW_ERR_ARG
+    assert "shape" in B.last_error()
+    assert L.qw_attention_decode_noalloc(None, None, None, 1, 1, 2, 2, 64, 8, 3, 1e-6, 1e6, 4, 1,
+                                         None) == B.QW_ERR_ARG
+    assert "null" in B.last_error()
+    # 16 heads x 1000 splits x (128 + 2) floats is about 8 MB, beyond the 1 MiB array
+    assert L.qw_attention_decode_noalloc(*a, 16, 8, 128, 10, 0, 1e-6, 1e6, 1000, 1,
+                                         None) == B.QW_ERR_SIZE
+    assert "1 MiB" in B.last_error()
+
+
+def test_int4_gemv_arguments_checked_before_any_launch(L):
+    assert L.qw_gemv_int4_workspace_bytes(3, 256) == 256 + 3 * (128 + 16)
+    assert L.qw_gemv_int4_workspace_bytes(3, 100) == 0
+    ws = L.qw_gemv_int4_workspace_bytes(8, 384)
+    assert L.qw_gemv_int4_g128(None, 1, 8, 384, 1, 1, 16, ws, None) == B.QW_ERR_ARG
+    assert L.qw_gemv_int4_g128(1, 1, 8, 200, 1, 1, 16, 1 << 20, None) == B.QW_ERR_ARG  # cols % 128
+    assert L.qw_gemv_int4_g128(1, 1, 8, 384, 1, 1, 16, ws - 16, None) == B.QW_ERR_ARG  # short
+    assert L.qw_gemv_int4_g128(1, 1, 8, 384, 1, 1, 8, ws, None) == B.QW_ERR_ARG       # unaligned
+    assert "workspace" in B.last_error()

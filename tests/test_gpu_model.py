@@ -330,3 +330,52 @@ def test_persistent_and_multikernel_paths_agree(workload_name, steps):
     finally:
         m.close()
         m2.close()
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_greedy_argmax_ties_and_nan_in_the_decode_step(path):
+    # Two logits exactly equal: embedding rows i and j set to a * e_c make both logits
+    # a * h[c] whatever the summation order (every other product is an exact zero).
+    # The lowest id must win, across CTAs, across warps of one CTA and within a warp
+    # ("flashmoon demo", Performance: argmax on the device, ties to the lowest id).
+    # A NaN weight in one row makes its logit NaN: QW_ERR_NUMERIC, and the handle
+    # stays usable.
+    wl = W.WORKLOADS["tiny"]
+    d = W.draw(wl)
+    tok = int(d.prompt[0])
+    h = R.build_oracle(d).decode_step(tok)["final_norm"][0]
+    c = int(np.argmax(h))
+    assert h[c] > 0.5
+    row = np.zeros(wl.shape.hidden, np.float32)
+    row[c] = 64.0
+    m = DeviceModel(wl.shape, d.weights, wl.max_ctx)
+    try:
+        B.qw_set_decode_path(m.h, path)
+        assert B.qw_get_decode_path(m.h) == path
+        for i, j in ((100, 3000), (1000, 1001), (2000, 2008), (5, 4095), (3001, 2990)):
+            assert tok not in (i, j)
+            w = dict(d.weights)
+            w["embed"] = d.weights["embed"].copy()
+            w["embed"][[i, j]] = W.f32_to_bf16_bits(row)
+            m.load(w)
+            B.qw_set_decode_path(m.h, path)
+            am, lg = m.decode(tok, logits=True)
+            assert lg[i] == lg[j] == lg.max()
+            want = R.build_oracle(W.DrawnWorkload(wl, w)).decode_step(tok)["logits"]
+            assert want[i] == want[j] and R.greedy_argmax(want) == min(i, j)
+            assert am == min(i, j), (i, j, am)
+        w = dict(d.weights)
+        w["embed"] = d.weights["embed"].copy()
+        w["embed"][777, 3] = 0x7FC0                     # bf16 NaN
+        m.load(w)
+        B.qw_set_decode_path(m.h, path)
+        with pytest.raises(B.QwError) as e:
+            m.decode(tok)
+        assert e.value.code == B.QW_ERR_NUMERIC
+        m.load(d.weights)
+        B.qw_set_decode_path(m.h, path)
+        want = R.build_oracle(d).decode_step(tok)["logits"]
+        am, lg = m.decode(tok, logits=True)
+        assert violation(lg, want) <= 0 and am == R.greedy_argmax(want)
+    finally:
+        m.close()

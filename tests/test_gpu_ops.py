@@ -163,3 +163,40 @@ def test_lm_head_argmax_ties_and_nan(L):
     table[400, 3] = 0x7FC0               # a NaN weight makes one logit NaN
     lg, am = _lm_head(L, x, g, table)
     assert np.isnan(lg[400]) and am == -1
+
+
+# ------------------------------------------------------------------ int4 dequantisation, bit for bit
+def _gemv_int4(L, packed, scales, x):
+    rows, cols = packed.shape[0], packed.shape[1] * 2
+    wsb = L.qw_gemv_int4_workspace_bytes(rows, cols)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    y = torch.full((rows,), float("nan"), device="cuda")
+    dp, ds, dx = dev(packed), dev(scales), dev(x)
+    rc = L.qw_gemv_int4_g128(dp.data_ptr(), ds.data_ptr(), rows, cols, dx.data_ptr(),
+                             y.data_ptr(), ws.data_ptr(), wsb, None)
+    assert rc == 0, B.last_error()
+    return host(y)
+
+
+@pytest.mark.parametrize("rows,cols", [(300, 384), (2048, 11008)])
+def test_int4_gemv_one_hot_is_the_dequantised_column_bit_for_bit(L, rows, cols):
+    # "Emberglass" README, "Why it's hard": int4 group-128. The GEMV dequantises in
+    # registers ((nibble - 8) times the group's bf16 scale); with x = e_j every
+    # product but one is an exact zero, so y is column j of the oracle's
+    # dequantised matrix exactly. cols = 11008 takes the wide-input kernel variant.
+    rng = np.random.default_rng(rows + cols)
+    w = rng.standard_normal((rows, cols)).astype(np.float32) * 0.02
+    w[rows // 3, :128] = 0.0                    # an all-zero group: scale 0
+    packed, scales = R.int4_quantize(w)
+    deq = R.int4_dequantize(packed, scales)
+    for j in sorted({0, 1, 2, 127, 128, 255, 256, cols // 2 + 1, cols - 2, cols - 1,
+                     *rng.integers(0, cols, 4).tolist()}):
+        x = np.zeros(cols, np.float32)
+        x[j] = 1.0
+        got = _gemv_int4(L, packed, scales, x)
+        np.testing.assert_array_equal(got.view(np.uint32), deq[:, j].view(np.uint32),
+                                      err_msg=f"column {j}")
+    # a dense input within the kernel-check tolerance of the f64 product
+    x = rng.standard_normal(cols).astype(np.float32)
+    want = R.linear(x[None], deq.astype(np.float64))[0]
+    assert violation(_gemv_int4(L, packed, scales, x), want, 1e-4, 1e-4) <= 0
