@@ -59,6 +59,10 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # kernel: (sources digest, bytes per launch, what was captured)
+    "decode_mega": ("775e323b5897f239", 1194047488 + 3810816,
+                    "qwen3_0.6b_decode token at position 6, decode_mega_kernel<128, 1, 0, 0>"),
+    "lm_head_gemv": ("79af7532f0ab9dff", 311267072 + 3709696,
+                     "qw_lm_head_argmax on the 151936 x 1024 table, gemv_kernel<3, 4, 0>"),
 }
 
 

@@ -121,15 +121,15 @@ struct qw_handle {
   uint16_t* pf_xn_hi = nullptr;  // [Tmax, H] normalised rows, two-bf16 split
   uint16_t* pf_xn_lo = nullptr;
   float* pf_qkv = nullptr;     // [Tmax, (nq+2nkv) hd]
-  float* pf_q = nullptr;       // [Tmax, nq, hd] after QK-norm, RoPE, 1/sqrt(hd)
+  uint16_t* pf_q_hi = nullptr;  // [Tmax, nq, hd] after QK-norm, RoPE, 1/sqrt(hd): two-bf16 split
+  uint16_t* pf_q_lo = nullptr;
   uint16_t* pf_o_hi = nullptr;   // [Tmax, nq hd] attention output split
   uint16_t* pf_o_lo = nullptr;
   uint16_t* pf_m_hi = nullptr;   // [Tmax, I] SwiGLU output split
   uint16_t* pf_m_lo = nullptr;
-  uint16_t* pf_kvs = nullptr;    // K, V of the context split into bf16 hi/lo rows (attention)
-  void* pf_attn_part = nullptr;  // partial attention outputs of split query blocks + counters
-  int kvs_rows = 0;
+  uint16_t* pf_kvs = nullptr;    // K and V^T of the context as two-bf16 splits (attention)
   CUtensorMap tm_xn_hi, tm_xn_lo, tm_o_hi, tm_o_lo, tm_m_hi, tm_m_lo;
+  FaMaps tm_attn;  // attention operands: Q, K and V^T splits
   std::vector<CUtensorMap> tm_qkv, tm_ow, tm_gu, tm_dw;  // per layer, weight side
   int* d_status = nullptr;  // [2] greedy id, error word (written by the LM head)
   // pinned host staging
@@ -305,15 +305,13 @@ static int alloc_state(qw_handle* h) {
     pieces.push_back({(void**)&h->pf_xn_hi, Tm * H * 2});
     pieces.push_back({(void**)&h->pf_xn_lo, Tm * H * 2});
     pieces.push_back({(void**)&h->pf_qkv, Tm * qkv_rows * 4});
-    pieces.push_back({(void**)&h->pf_q, Tm * qd * 4});
+    pieces.push_back({(void**)&h->pf_q_hi, Tm * qd * 2});
+    pieces.push_back({(void**)&h->pf_q_lo, Tm * qd * 2});
     pieces.push_back({(void**)&h->pf_o_hi, Tm * qd * 2});
     pieces.push_back({(void**)&h->pf_o_lo, Tm * qd * 2});
     pieces.push_back({(void**)&h->pf_m_hi, Tm * I * 2});
     pieces.push_back({(void**)&h->pf_m_lo, Tm * I * 2});
-    h->kvs_rows = kv_split_rows(c.max_ctx);
-    pieces.push_back({(void**)&h->pf_kvs, kv_split_bytes(c.n_kv_heads, h->kvs_rows, c.head_dim)});
-    pieces.push_back({(void**)&h->pf_attn_part,
-                      attn_part_bytes(c.n_q_heads, (int)Tm, c.max_ctx, c.head_dim)});
+    pieces.push_back({(void**)&h->pf_kvs, attn_kv_bytes(c.n_kv_heads, c.head_dim, c.max_ctx)});
   }
   size_t total = 0;
   for (auto& p : pieces) total = align_up(total, 256) + p.bytes;
@@ -331,7 +329,9 @@ static int alloc_state(qw_handle* h) {
               make_tmap_bf16_2d(&h->tm_o_hi, h->pf_o_hi, Tm, qd, 128) &&
               make_tmap_bf16_2d(&h->tm_o_lo, h->pf_o_lo, Tm, qd, 128) &&
               make_tmap_bf16_2d(&h->tm_m_hi, h->pf_m_hi, Tm, I, 128) &&
-              make_tmap_bf16_2d(&h->tm_m_lo, h->pf_m_lo, Tm, I, 128);
+              make_tmap_bf16_2d(&h->tm_m_lo, h->pf_m_lo, Tm, I, 128) &&
+              make_attn_maps(&h->tm_attn, h->pf_q_hi, h->pf_q_lo, (int)Tm, c.n_q_heads,
+                             h->pf_kvs, c.n_kv_heads, c.head_dim, c.max_ctx);
     if (!ok) QW_FAIL(h, QW_ERR_CUDA, "prefill: TMA descriptor encoding failed");
   }
   QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, std::max<size_t>(cap, Tm) * 4, cudaHostAllocPortable));
@@ -1038,10 +1038,11 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
     QW_CUDA(h, gemm(256, GEPI_STORE, h->tm_xn_hi, h->tm_xn_lo, h->tm_qkv[l], qkv_rows, H,
                     h->pf_qkv, lw.qkv_bias, nullptr, nullptr, nullptr));
     QW_CUDA(h, launch_qk_rope_kv_rows(h->pf_qkv, T, p0, c.n_q_heads, c.n_kv_heads, hd, lw.q_norm,
-                                      lw.k_norm, c.eps, h->rope, h->pf_q, kc, vc, c.max_ctx, s));
-    QW_CUDA(h, launch_attn_prefill(h->pf_q, kc, vc, c.max_ctx, p0, T, c.n_q_heads, c.n_kv_heads,
-                                   hd, h->pf_kvs, h->kvs_rows, h->pf_o_hi, h->pf_o_lo,
-                                   h->pf_attn_part, c.max_prefill_t, h->d_err, h->wait_ns, s));
+                                      lw.k_norm, c.eps, h->rope, h->pf_q_hi, h->pf_q_lo, kc, vc,
+                                      c.max_ctx, s));
+    QW_CUDA(h, launch_attn_prefill(h->tm_attn, kc, vc, h->pf_kvs, c.max_ctx, p0, T, c.n_q_heads,
+                                   c.n_kv_heads, hd, h->pf_o_hi, h->pf_o_lo, h->d_err, h->wait_ns,
+                                   s));
     QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, h->tm_ow[l], H, qd, h->pf_x, nullptr,
                     nullptr, nullptr, nullptr));
     QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, lw.mlp_norm, c.eps, h->pf_xn_hi, h->pf_xn_lo,

@@ -250,11 +250,12 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* X, int H
 }
 
 // Row t (position p0 + t): per-head QK-RMSNorm and RoPE of q and k, q scaled by
-// 1/sqrt(hd) into Q [T][nq][hd]; k and v appended to the cache at their position.
+// 1/sqrt(hd) into Q [T][nq][hd] as a two-bf16 split; k and v appended to the cache at
+// their position.
 template <int HD>
 __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
     const float* QKV, int p0, int nq, int nkv, const uint16_t* q_norm, const uint16_t* k_norm,
-    float eps, const float2* rope, float* Q, float* kc, float* vc, int cap) {
+    float eps, const float2* rope, uint16_t* q_hi, uint16_t* q_lo, float* kc, float* vc, int cap) {
   constexpr int EPL = HD / 32;
   const int t = blockIdx.x, pos = p0 + t;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -286,7 +287,12 @@ __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
     }
     if (isq) {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) Q[((size_t)t * nq + hh) * HD + lane + 32 * e] = v[e] * scale;
+      for (int e = 0; e < EPL; ++e) {
+        uint16_t hi, lo;
+        split_bf16(v[e] * scale, hi, lo);
+        q_hi[((size_t)t * nq + hh) * HD + lane + 32 * e] = hi;
+        q_lo[((size_t)t * nq + hh) * HD + lane + 32 * e] = lo;
+      }
     } else {
       float* dst = kc + ((size_t)(hh - nq) * cap + pos) * HD;
 #pragma unroll
@@ -298,10 +304,8 @@ __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
     vc[((size_t)(i / HD) * cap + pos) * HD + (i % HD)] = vsrc[i];
 }
 
-// ---- causal attention on tensor cores (mma.sync m16n8k16, bf16 operands, f32 accumulate)
-// Every f32 operand x enters as two bf16 terms hi = bf16(x), lo = bf16(x - hi); a product
-// a.b is formed as a_hi.b_hi + a_hi.b_lo + a_lo.b_hi (the lo.lo term is below f32
-// rounding of the sum), so scores and outputs carry about 16 bits of the f32 values.
+// Two bf16 terms of a pair of f32 values (hi = bf16(x), lo = bf16(x - hi)), packed as
+// the GEMMs' activation operands take them.
 __device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo_col, uint16_t hi_col) {
   return (uint32_t)lo_col | ((uint32_t)hi_col << 16);
 }
@@ -312,334 +316,339 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   hi = pack_bf16x2(h0, h1);
   lo = pack_bf16x2(l0, l1);
 }
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
+// ---- causal attention on tcgen05 tensor cores (kind::f16, TMEM accumulators)
+// One CTA per (query head, block of 128 query rows), heaviest block first. Every f32
+// operand enters as two bf16 terms hi = bf16(x), lo = bf16(x - hi), and a product a.b
+// is issued as three MMAs, a_hi.b_hi + a_hi.b_lo + a_lo.b_hi, into an f32 TMEM
+// accumulator (the lo.lo term is below the f32 rounding of the sum), so scores and
+// outputs carry about 16 bits of the f32 values.
+// Warp 0 (one thread) brings Q (hi, lo) once and, per tile of 64 keys, the K rows
+// and the V^T rows (hi, lo) with TMA (128-byte swizzle) into a double buffer. Warp 1
+// (one thread) issues S = Q K^T (M 128, N 64, K head_dim) and O += P V (M 128,
+// N head_dim, K 64). Warps 2..5 own the 128 TMEM lanes, one query row per thread:
+// they read the scores, apply the causal mask and the online softmax (base 2),
+// rescale O in TMEM when the row maximum moves, write P (hi, lo) to shared memory in
+// the layout the MMA reads, and at the end normalise O and store it as the two-bf16
+// split the o_proj GEMM takes. S for tile i+1 is issued as soon as the scores of
+// tile i have been read, so it overlaps the softmax of tile i.
+constexpr int kFaBQ = kFaQueryRows;  // query rows per CTA (the MMA's M, one TMEM lane each)
+constexpr int kFaBN = kFaKeyRows;    // keys per tile (one 128-byte bf16 atom)
 
-// K and V of keys [0, n) of every KV head, split into bf16 hi/lo rows of HD + 8
-// elements (the padding keeps the attention kernel's ldmatrix rows in distinct
-// banks): dst[4][nkv][rows][HD + 8] = {K hi, K lo, V hi, V lo}. One warp per (key, head).
 template <int HD>
-__global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const float* vc, int cap,
-                                                       int n, int nkv, int rows, uint16_t* dst) {
-  constexpr int LD = HD + 8, EPL = HD / 32;
-  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (wid >= n * nkv) return;
-  const int key = wid % n, kvh = wid / n;
-  const size_t plane = (size_t)nkv * rows * LD;
-  const size_t row = ((size_t)kvh * rows + key) * LD;
-  const float* ks = kc + ((size_t)kvh * cap + key) * HD;
-  const float* vs = vc + ((size_t)kvh * cap + key) * HD;
-#pragma unroll
-  for (int e = 0; e < EPL; e += 2) {
-    const int d = lane * EPL + e;
-    const float2 k2 = *reinterpret_cast<const float2*>(ks + d);
-    const float2 v2 = *reinterpret_cast<const float2*>(vs + d);
-    uint32_t kh, kl, vh, vl;
-    split2(k2.x, k2.y, kh, kl);
-    split2(v2.x, v2.y, vh, vl);
-    *reinterpret_cast<uint32_t*>(dst + row + d) = kh;
-    *reinterpret_cast<uint32_t*>(dst + plane + row + d) = kl;
-    *reinterpret_cast<uint32_t*>(dst + 2 * plane + row + d) = vh;
-    *reinterpret_cast<uint32_t*>(dst + 3 * plane + row + d) = vl;
-  }
-}
-
-// One CTA: 64 query rows of one head (4 warps x 16 rows), keys in tiles of BK up to
-// the block's last position. The tiles of pre-split K/V rows (kv_split_kernel) come
-// in by one bulk copy per array into a double buffer, the next tile's copies issued
-// before the current tile is used. Scores S = Q.K^T and the online softmax stay in
-// registers (the m16n8 accumulator layout is reused as the A fragment of P.V).
-// Split of the causal work: query block qb reads n_tiles(qb) key tiles; they are cut
-// into chunks of at most CH tiles, one CTA each, listed heavy block first.
-struct AttnSplit {
-  float* part_o;     // [nq][nqb][max_ch][64][HD] unnormalised partial outputs
-  float2* part_ml;   // [nq][nqb][max_ch][64] (row max, row sum)
-  int* counters;     // [nq][nqb] arrivals, 0 between launches
-  int max_ch, ch;
+struct FaLayout {
+  static constexpr int QA = HD / 64;                         // 128-byte atoms across head_dim
+  static constexpr uint32_t kQ1 = QA * kFaBQ * 128;          // Q hi (or lo): QA atoms of 128 rows
+  static constexpr uint32_t kK1 = QA * kFaBN * 128;          // K tile hi (or lo): QA atoms of 64 rows
+  static constexpr uint32_t kV1 = HD * 128;                  // V^T tile hi (or lo): head_dim rows
+  static constexpr uint32_t kP1 = kFaBQ * 128;               // P hi (or lo): 128 rows
+  static constexpr uint32_t kKV = 2 * kK1 + 2 * kV1;         // one buffer: K hi, K lo, V hi, V lo
+  static constexpr uint32_t off_kv = 2 * kQ1;
+  static constexpr uint32_t off_p = off_kv + 2 * kKV;
+  static constexpr uint32_t off_bar = off_p + 2 * kP1;
+  static constexpr uint32_t bytes = off_bar + 128 + 1024;   // barriers, TMEM slot, alignment slack
 };
 
-template <int HD, int BK>
-__global__ void __launch_bounds__(128) attn_prefill_tc_kernel(const float* Q,
-                                                              const uint16_t* kvs, int rows,
-                                                              int p0, int T, int nq, int nkv,
-                                                              uint16_t* o_hi, uint16_t* o_lo,
-                                                              const AttnSplit sp, int* err,
-                                                              uint64_t wait_ns) {
-  constexpr int BQ = 64, LD = HD + 8, KS = HD / 16, NO = HD / 8;
-  constexpr uint32_t kArr = (uint32_t)BK * LD * 2;  // bytes of one array's tile
-  extern __shared__ __align__(128) uint8_t smraw[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smraw + 2 * 4 * kArr);  // [2]
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  // this CTA's (query block, key chunk): blocks from the last (heaviest) down
-  const int nqb = (T + BQ - 1) / BQ;
-  int qb = nqb - 1, chunk = blockIdx.x, nch = 1;
-  for (;; --qb) {
-    const int nr = min(BQ, T - qb * BQ);
-    const int nt = (p0 + qb * BQ + nr - 1) / BK + 1;
-    nch = (nt + sp.ch - 1) / sp.ch;
-    if (chunk < nch || qb == 0) break;
-    chunk -= nch;
+// Wait for an mbarrier phase, bounded; gives up at once when another thread of the
+// launch already reported a timeout.
+__device__ __forceinline__ bool fa_wait(const FaArgs& a, uint64_t* bar, uint32_t parity) {
+  if (a.wait_ns == 0) return false;
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) != 0) continue;
+    const uint64_t now = globaltimer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > a.wait_ns || (*reinterpret_cast<volatile int*>(a.err) & ERR_TIMEOUT)) {
+      return false;
+    }
   }
-  const int t0 = qb * BQ, h = blockIdx.y, kvh = h / (nq / nkv);
-  const int nrows = min(BQ, T - t0);
-  const int last_key = p0 + t0 + nrows - 1;
-  const int r0 = t0 + warp * 16 + g;  // this lane's two rows: r0 and r0 + 8 (block-relative t)
-  const size_t plane = (size_t)nkv * rows * LD;
-  const uint16_t* src = kvs + (size_t)kvh * rows * LD;
-  const int kt0 = chunk * sp.ch, kt1 = min(last_key / BK + 1, kt0 + sp.ch);
-  const int n_tiles = kt1 - kt0;
-  // a whole tile of each array (rows past the last key hold zeros or older keys:
-  // finite, and masked); the i-th tile of the chunk uses buffer i & 1, whose
-  // barrier completes phase i >> 1
-  auto issue = [&](int i) {
-    const int b = i & 1, kt = kt0 + i;
-    mbar_expect_tx(&bar[b], 4 * kArr);
-#pragma unroll
-    for (int arr = 0; arr < 4; ++arr)
-      bulk_load(smraw + (size_t)(b * 4 + arr) * kArr, src + arr * plane + (size_t)kt * BK * LD,
-                kArr, &bar[b]);
-  };
-  if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(192, 1)
+    attn_prefill_fa_kernel(const __grid_constant__ FaMaps mp, const FaArgs a) {
+  using LY = FaLayout<HD>;
+  constexpr int QA = LY::QA;
+  constexpr uint32_t kTmemCols = 256;
+  extern __shared__ uint8_t fa_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(fa_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::off_bar);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* s_empty = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* o_full = bars + 8;
+  uint64_t* done = bars + 9;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = (a.T + kFaBQ - 1) / kFaBQ;
+  const int qb = nqb - 1 - (int)blockIdx.x;  // heaviest (latest) block first
+  const int h = blockIdx.y, kvh = h / (a.nq / a.nkv);
+  const int t0 = qb * kFaBQ;
+  const int nrows = min(kFaBQ, a.T - t0);
+  const int n_tiles = (a.p0 + t0 + nrows - 1) / kFaBN + 1;  // keys 0 .. last query position
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&kv_full[b], 1);
+      mbar_init(&kv_empty[b], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 4);  // one arrival per softmax warp
+    mbar_init(p_full, 4);
+    mbar_init(o_full, 1);
+    mbar_init(done, 1);
     fence_barrier_init();
-    issue(0);
-    if (n_tiles > 1) issue(1);
   }
-  // Q fragments (A operand, row-major 16 x 16 per k-step), split hi/lo
-  uint32_t qh[KS][4], ql[KS][4];
+  if (warp == 1) {
+    tmem_alloc(tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t t_s = tbase, t_o = tbase + kFaBN;  // S: 64 columns, O: head_dim columns
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer
+      mbar_expect_tx(q_full, 2 * LY::kQ1);
+      for (int c = 0; c < QA; ++c) {
+        tma_load_2d(sm + c * (kFaBQ * 128), &mp.q_hi, h * HD + 64 * c, t0, q_full);
+        tma_load_2d(sm + LY::kQ1 + c * (kFaBQ * 128), &mp.q_lo, h * HD + 64 * c, t0, q_full);
+      }
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int b = i & 1;
+        if (i >= 2 && !fa_wait(a, &kv_empty[b], (uint32_t)(((i >> 1) - 1) & 1))) {
+          atomicOr(a.err, ERR_TIMEOUT);
+          break;
+        }
+        uint8_t* kb = sm + LY::off_kv + b * LY::kKV;
+        const int k0 = i * kFaBN, krow = kvh * a.kv_rows + k0;
+        mbar_expect_tx(&kv_full[b], LY::kKV);
+        for (int c = 0; c < QA; ++c) {
+          tma_load_2d(kb + c * (kFaBN * 128), &mp.k_hi, 64 * c, krow, &kv_full[b]);
+          tma_load_2d(kb + LY::kK1 + c * (kFaBN * 128), &mp.k_lo, 64 * c, krow, &kv_full[b]);
+        }
+        tma_load_2d(kb + 2 * LY::kK1, &mp.vt_hi, k0, kvh * HD, &kv_full[b]);
+        tma_load_2d(kb + 2 * LY::kK1 + LY::kV1, &mp.vt_lo, k0, kvh * HD, &kv_full[b]);
+        issued = i + 1;
+      }
+      // leave only once the copies issued into this CTA's shared memory have landed
+      mbar_wait(q_full, 0, kDrainNs);
+      for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+        mbar_wait(&kv_full[i & 1], (uint32_t)((i >> 1) & 1), kDrainNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      constexpr uint32_t id_s = idesc_bf16_f32(kFaBQ, kFaBN);
+      constexpr uint32_t id_o = idesc_bf16_f32(kFaBQ, HD);
+      const uint32_t qh = smem_addr(sm), ql = qh + LY::kQ1;
+      const uint32_t ph = smem_addr(sm + LY::off_p), pl = ph + LY::kP1;
+      auto issue_s = [&](int i) {  // S = Q . K_i^T, three terms per product
+        const uint32_t kh = smem_addr(sm + LY::off_kv + (i & 1) * LY::kKV), kl = kh + LY::kK1;
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
+        for (int c = 0; c < QA; ++c)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int row = r0 + (j & 1) * 8, col = ks * 16 + 2 * t + (j >> 1) * 8;
-      float2 v = make_float2(0.f, 0.f);
-      if (row < T) v = *reinterpret_cast<const float2*>(Q + ((size_t)row * nq + h) * HD + col);
-      split2(v.x, v.y, qh[ks][j], ql[ks][j]);
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t qo = c * (kFaBQ * 128) + k * 32, ko = c * (kFaBN * 128) + k * 32;
+            const uint64_t dkh = sw128_kmajor_desc(kh + ko), dqh = sw128_kmajor_desc(qh + qo);
+            tc_mma_bf16(t_s, dqh, dkh, id_s, (c | k) != 0);
+            tc_mma_bf16(t_s, dqh, sw128_kmajor_desc(kl + ko), id_s, 1);
+            tc_mma_bf16(t_s, sw128_kmajor_desc(ql + qo), dkh, id_s, 1);
+          }
+        tc_commit(s_full);
+      };
+      bool ok = fa_wait(a, q_full, 0) && fa_wait(a, &kv_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        if (i + 1 < n_tiles) {  // the scores of tile i are read: start tile i + 1's
+          ok = fa_wait(a, s_empty, (uint32_t)(i & 1)) &&
+               fa_wait(a, &kv_full[(i + 1) & 1], (uint32_t)(((i + 1) >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i + 1);
+        }
+        ok = fa_wait(a, p_full, (uint32_t)(i & 1));  // P_i written, O rescaled
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vh = smem_addr(sm + LY::off_kv + (i & 1) * LY::kKV + 2 * LY::kK1);
+        const uint32_t vl = vh + LY::kV1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t dph = sw128_kmajor_desc(ph + k * 32), dvh = sw128_kmajor_desc(vh + k * 32);
+          tc_mma_bf16(t_o, dph, dvh, id_o, (i | k) != 0);
+          tc_mma_bf16(t_o, dph, sw128_kmajor_desc(vl + k * 32), id_o, 1);
+          tc_mma_bf16(t_o, sw128_kmajor_desc(pl + k * 32), dvh, id_o, 1);
+        }
+        tc_commit(o_full);
+        tc_commit(&kv_empty[i & 1]);
+      }
+      if (!ok) atomicOr(a.err, ERR_TIMEOUT);
+      // TMEM is released below only after every MMA issued here has finished
+      tc_commit(done);
+      mbar_wait(done, 0, kDrainNs);
+    }
+  } else {
+    // ---- softmax and epilogue: warp w owns TMEM lanes [32 (w % 4), +32) = query rows
+    const int q4 = warp & 3, r = q4 * 32 + lane;
+    const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
+    const int qpos = a.p0 + t0 + r;
+    constexpr float kLog2e = 1.4426950408889634f;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint8_t* prow = sm + LY::off_p + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
+    for (int i = 0; i < n_tiles; ++i) {
+      ok = __all_sync(0xffffffffu, fa_wait(a, s_full, (uint32_t)(i & 1)));
+      if (!ok) break;
+      tc_fence_after();
+      float sv[kFaBN];
+#pragma unroll
+      for (int j = 0; j < kFaBN / 16; ++j) {
+        uint32_t rr[16];
+        tmem_ld16(t_s + lrow + 16 * j, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sv[16 * j + e] = __uint_as_float(rr[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(s_empty);
+      // causal mask (keys after this row's position) and the running maximum, base 2
+      const int k0 = i * kFaBN;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kFaBN; ++j) {
+        const float v = k0 + j <= qpos ? sv[j] * kLog2e : -INFINITY;
+        sv[j] = v;
+        mx = fmaxf(mx, v);
+      }
+      const float m_new = fmaxf(m, mx);  // finite: key 0 is visible to every row
+      const float alpha = exp2f(m - m_new);
+      float ps = 0.f;
+#pragma unroll
+      for (int j = 0; j < kFaBN; ++j) {
+        const float pj = exp2f(sv[j] - m_new);
+        sv[j] = pj;
+        ps += pj;
+      }
+      l = l * alpha + ps;
+      m = m_new;
+      if (i > 0) {
+        // P V of tile i-1 has finished: P's buffer is free and O can be rescaled
+        ok = __all_sync(0xffffffffu, fa_wait(a, o_full, (uint32_t)((i - 1) & 1)));
+        if (!ok) break;
+        tc_fence_after();
+        if (!__all_sync(0xffffffffu, alpha == 1.f)) {
+#pragma unroll 1
+          for (int d0 = 0; d0 < HD; d0 += 16) {
+            uint32_t rr[16];
+            tmem_ld16(t_o + lrow + d0, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+            tmem_st16(t_o + lrow + d0, rr);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P (hi, lo) into shared memory: row r, one 128-byte atom each, 16-byte units
+      // of 8 keys swizzled by the row
+#pragma unroll
+      for (int u = 0; u < kFaBN / 8; ++u) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1], hw[e], lw[e]);
+        const uint32_t off = (uint32_t)((u ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(prow + LY::kP1 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(p_full);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, fa_wait(a, o_full, (uint32_t)((n_tiles - 1) & 1)));
+    if (!ok) {
+      if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+    } else {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      const bool store = r < nrows;
+      uint16_t* oh = a.o_hi + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
+      uint16_t* ol = a.o_lo + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
+#pragma unroll 1
+      for (int d0 = 0; d0 < HD; d0 += 16) {
+        uint32_t rr[16];
+        tmem_ld16(t_o + lrow + d0, rr);
+        tmem_ld_wait();
+        uint32_t hw[8], lw[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          split2(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv, hw[e],
+                 lw[e]);
+        if (store) {
+          *reinterpret_cast<uint4*>(oh + d0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(oh + d0 + 8) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          *reinterpret_cast<uint4*>(ol + d0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(ol + d0 + 8) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        }
+      }
     }
   }
-  __syncthreads();  // barrier initialisation visible to all threads
-  float o[NO][4];
-#pragma unroll
-  for (int nb = 0; nb < NO; ++nb)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[nb][j] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const int qp0 = p0 + r0, qp1 = qp0 + 8;
-  bool ok = true;
-  for (int i = 0; i < n_tiles; ++i) {
-    const int k0 = (kt0 + i) * BK, b = i & 1;
-    const bool got = mbar_wait(&bar[b], (uint32_t)((i >> 1) & 1), wait_ns);
-    ok = __syncthreads_and(got) != 0;  // one decision for the whole block
-    if (!ok) {  // gave up: outputs invalid, the host sees the error word
-      if (tid == 0) atomicOr(err, ERR_TIMEOUT);
-      break;
-    }
-    const uint16_t* Kh = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 0) * kArr);
-    const uint16_t* Kl = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 1) * kArr);
-    const uint16_t* Vh = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 2) * kArr);
-    const uint16_t* Vl = reinterpret_cast<const uint16_t*>(smraw + (size_t)(b * 4 + 3) * kArr);
-    // S = Q K^T: 8 n-blocks of 8 keys
-    float sc[BK / 8][4];
-#pragma unroll
-    for (int nb = 0; nb < BK / 8; ++nb)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sc[nb][j] = 0.f;
-    const int mrow = lane & 7, mi = lane >> 3;  // ldmatrix: matrix mi, row mrow
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-      for (int nb = 0; nb < BK / 8; nb += 2) {
-        const int key = (nb + (mi >> 1)) * 8 + mrow, col = ks * 16 + (mi & 1) * 8;
-        uint32_t bh0, bh1, bh2, bh3, bl0, bl1, bl2, bl3;
-        ldsm_x4(smem_addr(Kh + key * LD + col), bh0, bh1, bh2, bh3);
-        ldsm_x4(smem_addr(Kl + key * LD + col), bl0, bl1, bl2, bl3);
-        mma_bf16(sc[nb], qh[ks], bh0, bh1);
-        mma_bf16(sc[nb], qh[ks], bl0, bl1);
-        mma_bf16(sc[nb], ql[ks], bh0, bh1);
-        mma_bf16(sc[nb + 1], qh[ks], bh2, bh3);
-        mma_bf16(sc[nb + 1], qh[ks], bl2, bl3);
-        mma_bf16(sc[nb + 1], ql[ks], bh2, bh3);
-      }
-    }
-    // causal mask and online softmax (rows r0 and r0 + 8; a quad of lanes shares a row)
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nb = 0; nb < BK / 8; ++nb) {
-      const int key = k0 + nb * 8 + 2 * t;
-      if (key > qp0) sc[nb][0] = -INFINITY;
-      if (key + 1 > qp0) sc[nb][1] = -INFINITY;
-      if (key > qp1) sc[nb][2] = -INFINITY;
-      if (key + 1 > qp1) sc[nb][3] = -INFINITY;
-      mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
-      mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = m0 == -INFINITY ? 0.f : expf(m0 - mn0);
-    const float al1 = m1 == -INFINITY ? 0.f : expf(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-    for (int nb = 0; nb < BK / 8; ++nb) {
-      sc[nb][0] = sc[nb][0] == -INFINITY ? 0.f : expf(sc[nb][0] - mn0);
-      sc[nb][1] = sc[nb][1] == -INFINITY ? 0.f : expf(sc[nb][1] - mn0);
-      sc[nb][2] = sc[nb][2] == -INFINITY ? 0.f : expf(sc[nb][2] - mn1);
-      sc[nb][3] = sc[nb][3] == -INFINITY ? 0.f : expf(sc[nb][3] - mn1);
-      rs0 += sc[nb][0] + sc[nb][1];
-      rs1 += sc[nb][2] + sc[nb][3];
-    }
-    l0 = l0 * al0 + rs0;  // per-lane partial row sums; the quad adds them at the end
-    l1 = l1 * al1 + rs1;
-#pragma unroll
-    for (int nb = 0; nb < NO; ++nb) {
-      o[nb][0] *= al0;
-      o[nb][1] *= al0;
-      o[nb][2] *= al1;
-      o[nb][3] *= al1;
-    }
-    // O += P V: 4 k-steps of 16 keys; P's A fragment comes from two score n-blocks
-#pragma unroll
-    for (int kk = 0; kk < BK / 16; ++kk) {
-      uint32_t ph[4], pl[4];
-      split2(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
-      split2(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
-      split2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
-      split2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
-#pragma unroll
-      for (int nb = 0; nb < NO; nb += 2) {
-        // V rows kk*16 .. +15 (keys), columns nb*8 .. +15 (dims), transposed fragments
-        const int key = kk * 16 + (mi & 1) * 8 + mrow, col = (nb + (mi >> 1)) * 8;
-        uint32_t bh0, bh1, bh2, bh3, bl0, bl1, bl2, bl3;
-        ldsm_x4_t(smem_addr(Vh + key * LD + col), bh0, bh1, bh2, bh3);
-        ldsm_x4_t(smem_addr(Vl + key * LD + col), bl0, bl1, bl2, bl3);
-        mma_bf16(o[nb], ph, bh0, bh1);
-        mma_bf16(o[nb], ph, bl0, bl1);
-        mma_bf16(o[nb], pl, bh0, bh1);
-        mma_bf16(o[nb + 1], ph, bh2, bh3);
-        mma_bf16(o[nb + 1], ph, bl2, bl3);
-        mma_bf16(o[nb + 1], pl, bh2, bh3);
-      }
-    }
-    // buffer b is free once every warp has read it (generic proxy; ordered before the
-    // bulk copy that refills it): refill it with tile kt + 2
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    if (tid == 0 && i + 2 < n_tiles) issue(i + 2);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
   }
-  if (!ok) {  // copies may still be in flight into this CTA's shared memory
-    if (tid == 0) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_wait(&bar[b], 0, kDrainNs);
-        mbar_wait(&bar[b], 1, kDrainNs);
-      }
-      // still arrive, so the block's counter is back at 0 for the next launch
-      if (nch > 1 && atomicAdd(&sp.counters[h * nqb + qb], 1) == nch - 1)
-        sp.counters[h * nqb + qb] = 0;
-    }
-    return;
+}
+
+// Keys [0, n) of one layer's K and V cache as the attention's operands: K rows split
+// into bf16 hi/lo [nkv][kv_rows][HD], and V transposed and split, V^T [nkv][HD][kv_rows];
+// keys [n, next multiple of 32) are written as 0. One CTA per (32 keys, KV head).
+template <int HD>
+__global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const float* vc, int cap,
+                                                       int n, int kv_rows, uint16_t* kh,
+                                                       uint16_t* kl, uint16_t* vth,
+                                                       uint16_t* vtl) {
+  __shared__ float tile[32][HD + 1];
+  const int k0 = blockIdx.x * 32, kvh = blockIdx.y;
+  for (int i = threadIdx.x; i < 32 * HD / 2; i += 256) {
+    const int kk = i / (HD / 2), d = (i % (HD / 2)) * 2;
+    float2 v = make_float2(0.f, 0.f);
+    if (k0 + kk < n)
+      v = *reinterpret_cast<const float2*>(kc + ((size_t)kvh * cap + k0 + kk) * HD + d);
+    uint32_t hi, lo;
+    split2(v.x, v.y, hi, lo);
+    const size_t o = ((size_t)kvh * kv_rows + k0 + kk) * HD + d;
+    *reinterpret_cast<uint32_t*>(kh + o) = hi;
+    *reinterpret_cast<uint32_t*>(kl + o) = lo;
   }
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  if (nch > 1) {  // one chunk of several: partial results, the last to arrive merges
-    const int rr = warp * 16 + g;  // block-relative rows rr and rr + 8
-    const size_t slot = ((size_t)h * nqb + qb) * sp.max_ch;
-    float* po = sp.part_o + (slot + chunk) * BQ * HD;
-#pragma unroll
-    for (int nb = 0; nb < NO; ++nb) {
-      const int d = nb * 8 + 2 * t;
-      *reinterpret_cast<float2*>(po + rr * HD + d) = make_float2(o[nb][0], o[nb][1]);
-      *reinterpret_cast<float2*>(po + (rr + 8) * HD + d) = make_float2(o[nb][2], o[nb][3]);
-    }
-    if (t == 0) {
-      sp.part_ml[(slot + chunk) * BQ + rr] = make_float2(m0, l0);
-      sp.part_ml[(slot + chunk) * BQ + rr + 8] = make_float2(m1, l1);
-    }
-    __threadfence();
-    __syncthreads();
-    int* last = reinterpret_cast<int*>(smraw);
-    if (tid == 0) *last = atomicAdd(&sp.counters[h * nqb + qb], 1) == nch - 1;
-    __syncthreads();
-    if (!*last) return;
-    __threadfence();
-    // merge in chunk order: per row, weights exp(m_c - M) / sum_c exp(m_c - M) l_c
-    float* wsm = reinterpret_cast<float*>(smraw) + 4;  // [BQ][nch]
-    if (tid < BQ) {
-      float M = -INFINITY;
-      for (int c2 = 0; c2 < nch; ++c2) M = fmaxf(M, __ldcg(&sp.part_ml[(slot + c2) * BQ + tid]).x);
-      float den = 0.f;
-      for (int c2 = 0; c2 < nch; ++c2) {
-        const float2 ml = __ldcg(&sp.part_ml[(slot + c2) * BQ + tid]);
-        const float w = ml.x == -INFINITY ? 0.f : expf(ml.x - M);
-        wsm[tid * nch + c2] = w;
-        den = fmaf(w, ml.y, den);
-      }
-      const float inv = 1.0f / den;
-      for (int c2 = 0; c2 < nch; ++c2) wsm[tid * nch + c2] *= inv;
-    }
-    __syncthreads();
-    for (int idx = 2 * tid; idx < BQ * HD; idx += 2 * 128) {
-      const int rr2 = idx / HD, d = idx % HD;
-      float a0 = 0.f, a1 = 0.f;
-      for (int c2 = 0; c2 < nch; ++c2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(
-            sp.part_o + (slot + c2) * BQ * HD + rr2 * HD + d));
-        const float w = wsm[rr2 * nch + c2];
-        a0 = fmaf(w, v.x, a0);
-        a1 = fmaf(w, v.y, a1);
-      }
-      if (rr2 < nrows) {
-        uint32_t hi, lo;
-        split2(a0, a1, hi, lo);
-        const size_t off = (size_t)(t0 + rr2) * nq * HD + h * HD + d;
-        *reinterpret_cast<uint32_t*>(o_hi + off) = hi;
-        *reinterpret_cast<uint32_t*>(o_lo + off) = lo;
-      }
-    }
-    if (tid == 0) sp.counters[h * nqb + qb] = 0;  // not used again in this launch
-    return;
+  for (int i = threadIdx.x; i < 32 * HD; i += 256) {
+    const int kk = i / HD, d = i % HD;
+    tile[kk][d] = k0 + kk < n ? vc[((size_t)kvh * cap + k0 + kk) * HD + d] : 0.f;
   }
-  const float inv0 = 1.0f / l0, inv1 = 1.0f / l1;
-#pragma unroll
-  for (int nb = 0; nb < NO; ++nb) {
-    const int col = h * HD + nb * 8 + 2 * t;
-    if (r0 < t0 + nrows) {
-      uint32_t hi, lo;
-      split2(o[nb][0] * inv0, o[nb][1] * inv0, hi, lo);
-      *reinterpret_cast<uint32_t*>(o_hi + (size_t)r0 * nq * HD + col) = hi;
-      *reinterpret_cast<uint32_t*>(o_lo + (size_t)r0 * nq * HD + col) = lo;
-    }
-    if (r0 + 8 < t0 + nrows) {
-      uint32_t hi, lo;
-      split2(o[nb][2] * inv1, o[nb][3] * inv1, hi, lo);
-      *reinterpret_cast<uint32_t*>(o_hi + (size_t)(r0 + 8) * nq * HD + col) = hi;
-      *reinterpret_cast<uint32_t*>(o_lo + (size_t)(r0 + 8) * nq * HD + col) = lo;
-    }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 16 * HD; i += 256) {
+    const int d = i / 16, kk = (i % 16) * 2;
+    uint32_t hi, lo;
+    split2(tile[kk][d], tile[kk + 1][d], hi, lo);
+    const size_t o = ((size_t)kvh * HD + d) * kv_rows + k0 + kk;
+    *reinterpret_cast<uint32_t*>(vth + o) = hi;
+    *reinterpret_cast<uint32_t*>(vtl + o) = lo;
   }
 }
 
@@ -659,72 +668,72 @@ cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g,
 }
 cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
                                    const uint16_t* qn, const uint16_t* kn, float eps,
-                                   const float2* rope, float* Q, float* kc, float* vc, int cap,
-                                   cudaStream_t s) {
+                                   const float2* rope, uint16_t* q_hi, uint16_t* q_lo,
+                                   float* kc, float* vc, int cap, cudaStream_t s) {
   if (hd == 64)
-    qk_rope_kv_rows_kernel<64><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, Q, kc, vc, cap);
+    qk_rope_kv_rows_kernel<64><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, q_hi, q_lo,
+                                                 kc, vc, cap);
   else if (hd == 128)
-    qk_rope_kv_rows_kernel<128><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, Q, kc, vc, cap);
+    qk_rope_kv_rows_kernel<128><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, q_hi, q_lo,
+                                                  kc, vc, cap);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
-constexpr int kAttnBK = 32;  // keys per tile: 2 buffers x 4 arrays = 70 KB at hd 128, two CTAs per SM
-static size_t attn_prefill_tc_smem(int hd) { return (size_t)2 * 4 * kAttnBK * (hd + 8) * 2 + 16; }
-size_t kv_split_bytes(int nkv, int rows, int hd) { return (size_t)4 * nkv * rows * (hd + 8) * 2; }
-int kv_split_rows(int max_ctx) { return (max_ctx + kAttnBK - 1) / kAttnBK * kAttnBK; }
-constexpr int kAttnChunk = 8;  // key tiles per CTA at most (causal work balanced across CTAs)
-int attn_max_chunks(int max_ctx) {
-  return ((max_ctx + kAttnBK - 1) / kAttnBK + kAttnChunk - 1) / kAttnChunk;
+int attn_kv_rows(int cap) { return (cap + kFaBN - 1) / kFaBN * kFaBN; }
+size_t attn_kv_bytes(int nkv, int hd, int cap) {
+  return (size_t)4 * nkv * hd * attn_kv_rows(cap) * 2;
 }
-size_t attn_part_bytes(int nq, int max_t, int max_ctx, int hd) {
-  const size_t nqb = (size_t)(max_t + 63) / 64, slots = (size_t)nq * nqb * attn_max_chunks(max_ctx);
-  return slots * 64 * ((size_t)hd * 4 + 8) + (size_t)nq * nqb * 4;
-}
-cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
-                                int T, int nq, int nkv, int hd, uint16_t* kvs, int rows,
-                                uint16_t* o_hi, uint16_t* o_lo, void* part, int max_t,
-                                int* err, uint64_t wait_ns, cudaStream_t s) {
-  const int n = p0 + T;  // keys this pass reads
-  const int nqb = (T + 63) / 64, maxqb = (max_t + 63) / 64;
-  AttnSplit sp;
-  sp.ch = kAttnChunk;
-  sp.max_ch = attn_max_chunks(cap);
-  const size_t slots = (size_t)nq * maxqb * sp.max_ch;
-  sp.part_o = reinterpret_cast<float*>(part);
-  sp.part_ml = reinterpret_cast<float2*>(sp.part_o + slots * 64 * hd);
-  sp.counters = reinterpret_cast<int*>(sp.part_ml + slots * 64);
-  int items = 0;  // (query block, key chunk) pairs per head
-  for (int qb = 0; qb < nqb; ++qb) {
-    const int nr = min(64, T - qb * 64);
-    const int nt = (p0 + qb * 64 + nr - 1) / kAttnBK + 1;
-    items += (nt + kAttnChunk - 1) / kAttnChunk;
-  }
-  // counters are indexed [head][block] with this launch's block count
-  const dim3 grid(items, nq), sgrid((n * nkv + 7) / 8);
+cudaError_t launch_attn_prefill(const FaMaps& maps, const float* kc, const float* vc,
+                                uint16_t* kv_split, int cap, int p0, int T, int nq, int nkv,
+                                int hd, uint16_t* o_hi, uint16_t* o_lo, int* err,
+                                uint64_t wait_ns, cudaStream_t s) {
+  if (T <= 0 || nkv <= 0 || nq % nkv) return cudaErrorInvalidValue;
+  const int n = p0 + T;  // keys this pass reads; split up to the tile the last one is in
+  const int kv_rows = attn_kv_rows(cap);
+  const size_t plane = (size_t)nkv * hd * kv_rows;
+  const dim3 sgrid((n + kFaBN - 1) / kFaBN * (kFaBN / 32), nkv);
+  const dim3 grid((T + kFaBQ - 1) / kFaBQ, nq);
+  FaArgs a{p0, T, nq, nkv, kv_rows, o_hi, o_lo, err, wait_ns};
+  uint16_t *kh = kv_split, *kl = kv_split + plane, *vth = kl + plane, *vtl = vth + plane;
   if (hd == 64) {
-    kv_split_kernel<64><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, nkv, rows, kvs);
-    attn_prefill_tc_kernel<64, kAttnBK><<<grid, 128, attn_prefill_tc_smem(64), s>>>(
-        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, sp, err, wait_ns);
+    kv_split_kernel<64><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, kv_rows, kh, kl, vth, vtl);
+    attn_prefill_fa_kernel<64><<<grid, 192, FaLayout<64>::bytes, s>>>(maps, a);
   } else if (hd == 128) {
-    kv_split_kernel<128><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, nkv, rows, kvs);
-    attn_prefill_tc_kernel<128, kAttnBK><<<grid, 128, attn_prefill_tc_smem(128), s>>>(
-        Q, kvs, rows, p0, T, nq, nkv, o_hi, o_lo, sp, err, wait_ns);
+    kv_split_kernel<128><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, kv_rows, kh, kl, vth, vtl);
+    attn_prefill_fa_kernel<128><<<grid, 192, FaLayout<128>::bytes, s>>>(maps, a);
   } else {
     return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+bool make_attn_maps(FaMaps* m, const uint16_t* q_hi, const uint16_t* q_lo, int max_t, int nq,
+                    const uint16_t* kv_split, int nkv, int hd, int cap) {
+  const int kv_rows = attn_kv_rows(cap);
+  const size_t plane = (size_t)nkv * hd * kv_rows;
+  const uint64_t qd = (uint64_t)nq * hd;
+  return make_tmap_bf16_2d(&m->q_hi, q_hi, (uint64_t)max_t, qd, kFaBQ) &&
+         make_tmap_bf16_2d(&m->q_lo, q_lo, (uint64_t)max_t, qd, kFaBQ) &&
+         make_tmap_bf16_2d(&m->k_hi, kv_split, (uint64_t)nkv * kv_rows, hd, kFaBN) &&
+         make_tmap_bf16_2d(&m->k_lo, kv_split + plane, (uint64_t)nkv * kv_rows, hd, kFaBN) &&
+         make_tmap_bf16_2d(&m->vt_hi, kv_split + 2 * plane, (uint64_t)nkv * hd, kv_rows,
+                           (uint32_t)hd) &&
+         make_tmap_bf16_2d(&m->vt_lo, kv_split + 3 * plane, (uint64_t)nkv * hd, kv_rows,
+                           (uint32_t)hd);
 }
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
   set_int_kernel<<<1, 1, 0, s>>>(p, v);
   return cudaGetLastError();
 }
 cudaError_t set_prefill_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<64, kAttnBK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_prefill_tc_smem(64));
+  static_assert(FaLayout<128>::bytes <= 227 * 1024, "attention tiles fit one CTA's shared memory");
+  cudaError_t e = cudaFuncSetAttribute(attn_prefill_fa_kernel<64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)FaLayout<64>::bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_prefill_tc_kernel<128, kAttnBK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn_prefill_tc_smem(128));
+    e = cudaFuncSetAttribute(attn_prefill_fa_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)FaLayout<128>::bytes);
   return e;
 }
 

@@ -156,17 +156,35 @@ cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g,
                                 cudaStream_t s);
 cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
                                    const uint16_t* qn, const uint16_t* kn, float eps,
-                                   const float2* rope, float* Q, float* kc, float* vc, int cap,
-                                   cudaStream_t s);
-// kvs: scratch of kv_split_bytes(nkv, rows, hd) with rows = kv_split_rows(cap), zeroed once
-// part: scratch of attn_part_bytes(nq, max_t, cap, hd), zeroed once (T <= max_t)
-cudaError_t launch_attn_prefill(const float* Q, const float* kc, const float* vc, int cap, int p0,
-                                int T, int nq, int nkv, int hd, uint16_t* kvs, int rows,
-                                uint16_t* o_hi, uint16_t* o_lo, void* part, int max_t,
-                                int* err, uint64_t wait_ns, cudaStream_t s);
-size_t attn_part_bytes(int nq, int max_t, int max_ctx, int hd);
-size_t kv_split_bytes(int nkv, int rows, int hd);
-int kv_split_rows(int max_ctx);
+                                   const float2* rope, uint16_t* q_hi, uint16_t* q_lo,
+                                   float* kc, float* vc, int cap, cudaStream_t s);
+// Causal prefill attention on tcgen05 (kind::f16, three MMAs per product of two-bf16
+// splits): Q rows [T][nq][hd] (scaled by 1/sqrt(hd)) as q_hi/q_lo, keys and values
+// 0 .. p0+T-1 of one layer from its f32 cache (kc, vc: [nkv][cap][hd]), split per call
+// into kv_split (attn_kv_bytes) as K hi, K lo [nkv][kv_rows][hd] and V^T hi, V^T lo
+// [nkv][hd][kv_rows] (kv_rows = attn_kv_rows(cap)); output as the two-bf16 split
+// [T][nq*hd]. The tensor maps (make_attn_maps) cover q_hi/q_lo [max_t, nq*hd] and the
+// four kv_split planes.
+struct FaMaps {
+  CUtensorMap q_hi, q_lo, k_hi, k_lo, vt_hi, vt_lo;
+};
+struct FaArgs {
+  int p0, T, nq, nkv;
+  int kv_rows;
+  uint16_t* o_hi;
+  uint16_t* o_lo;
+  int* err;
+  uint64_t wait_ns;
+};
+constexpr int kFaQueryRows = 128, kFaKeyRows = 64;  // query rows per CTA, keys per tile
+int attn_kv_rows(int cap);
+size_t attn_kv_bytes(int nkv, int hd, int cap);
+bool make_attn_maps(FaMaps* m, const uint16_t* q_hi, const uint16_t* q_lo, int max_t, int nq,
+                    const uint16_t* kv_split, int nkv, int hd, int cap);
+cudaError_t launch_attn_prefill(const FaMaps& maps, const float* kc, const float* vc,
+                                uint16_t* kv_split, int cap, int p0, int T, int nq, int nkv,
+                                int hd, uint16_t* o_hi, uint16_t* o_lo, int* err,
+                                uint64_t wait_ns, cudaStream_t s);
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
 cudaError_t set_prefill_attributes();
 

@@ -259,6 +259,32 @@ def test_batched_prefill_in_two_chunks_and_sequential_fallback():
         m.close()
 
 
+def test_batched_prefill_ragged_chunks_head_dim_128():
+    # Qwen3-0.6B layer shape (head_dim 128, 16 / 8 heads), two layers: chunks of 200 and
+    # 333 ids, so query blocks end mid-block, the second chunk starts at p0 = 200 and
+    # attends to the first chunk's cache, and key tiles end mid-tile
+    shape = W.QWEN3_0_6B.replace(n_layers=2)
+    wl = W.Workload("ragged", shape, seed=21, max_ctx=600)
+    d = W.draw(wl, drawn_gains=True)
+    ids = list(W.random_ids(shape.vocab, 533, seed=22))
+    m = DeviceModel(shape, d.weights, 600, max_prefill_t=400)
+    o = R.build_oracle(d, cache_f64=False)
+    try:
+        m.prefill(ids[:200])
+        am, lg = m.prefill(ids[200:], logits=True)
+        cp = o.prefill(ids)
+        assert violation(lg, cp["logits"]) <= 0
+        for l in range(2):
+            kd, vd = m.kv(l)
+            assert violation(kd.cpu().numpy()[:, :533], o.k_cache[l][:, :533]) <= 0
+            assert violation(vd.cpu().numpy()[:, :533], o.v_cache[l][:, :533]) <= 0
+        if top2_margin(cp["logits"]) > MARGIN:
+            assert am == R.greedy_argmax(cp["logits"])
+        _teacher_forced(m, o, R.greedy_argmax(cp["logits"]), 3)
+    finally:
+        m.close()
+
+
 # ------------------------------------------------------------------ error paths
 def test_error_paths_on_device():
     wl = W.WORKLOADS["tiny"]
