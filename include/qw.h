@@ -52,7 +52,7 @@ enum {
 };
 
 /* qw_config.weight_format */
-enum { QW_WEIGHTS_BF16 = 0, QW_WEIGHTS_INT4_G128 = 1 };
+enum { QW_WEIGHTS_BF16 = 0, QW_WEIGHTS_INT4_G128 = 1, QW_WEIGHTS_Q8_0 = 2 };
 
 /* qw_get_capture `which`: the four checkpoints of the "Failed Star / fs, M2"
  * page ("Four boundaries bisect the whole model"). */
@@ -68,8 +68,8 @@ typedef struct qw_handle qw_handle;
 /* Model shape and options. Set struct_size = sizeof(qw_config) and
  * abi_version = QW_ABI_VERSION. head_dim must be 64 or 128; hidden,
  * n_q_heads*head_dim and intermediate must be multiples of 8 (of 128 for
- * int4); n_q_heads must be a multiple of n_kv_heads with at most 8 query heads
- * per KV head. */
+ * int4, of 32 for Q8_0); n_q_heads must be a multiple of n_kv_heads with at
+ * most 8 query heads per KV head. */
 typedef struct qw_config {
   uint32_t struct_size;
   uint32_t abi_version;
@@ -87,7 +87,7 @@ typedef struct qw_config {
   uint32_t qkv_bias;            /* 1: q/k/v projections carry a bias (Qwen2.5) */
   int32_t max_ctx;              /* KV-cache capacity in positions */
   int32_t max_prefill_t;        /* longest prompt taken by one batched prefill pass */
-  uint32_t weight_format;       /* QW_WEIGHTS_BF16 or QW_WEIGHTS_INT4_G128 */
+  uint32_t weight_format;       /* QW_WEIGHTS_BF16, QW_WEIGHTS_INT4_G128 or QW_WEIGHTS_Q8_0 */
 } qw_config;
 
 /* Weights, all DEVICE pointers owned by the caller; the per-layer members are
@@ -100,7 +100,13 @@ typedef struct qw_config {
  * int4 tensors (weight_format = QW_WEIGHTS_INT4_G128) are nibble-packed
  * [out, in/2] bytes (element 2i in the low nibble, value = nibble - 8) with
  * bf16 scales [out, in/128], one per 128 consecutive inputs of a row; see
- * qw_quantize_int4_g128. Embedding, norms and biases are always bf16. */
+ * qw_quantize_int4_g128. Q8_0 tensors (weight_format = QW_WEIGHTS_Q8_0) are
+ * int8 [out, in] (two's complement) with fp16 scales [out, in/32], one per 32
+ * consecutive inputs of a row, in the *_scales members; see qw_quantize_q8_0.
+ * A Q8_0 model's LM head is Q8_0 too: the untied lm_head is passed quantised,
+ * and a tied model's head is quantised from the embedding table at load (the
+ * "SuperKittens PR #7" page, Q8_0 commit); the gather keeps the bf16 rows.
+ * Embedding, norms and biases are always bf16. */
 typedef struct qw_weights {
   uint32_t struct_size;
   uint32_t reserved0;
@@ -108,7 +114,7 @@ typedef struct qw_weights {
   const void* final_norm;     /* bf16 [hidden] */
   const void* lm_head;        /* [vocab, hidden]; must be NULL iff tie_word_embeddings;
                                * int4 (with lm_head_scales) when weight_format is int4 */
-  const void* lm_head_scales; /* bf16 [vocab, hidden/128] for an int4 lm_head, else NULL */
+  const void* lm_head_scales; /* scales of an int4 or Q8_0 untied lm_head, else NULL */
   const void* const* attn_norm; /* bf16 [hidden] */
   const void* const* q;         /* [n_q_heads*head_dim, hidden] */
   const void* const* k;         /* [n_kv_heads*head_dim, hidden] */
@@ -123,7 +129,7 @@ typedef struct qw_weights {
   const void* const* q_bias;    /* bf16 [n_q_heads*head_dim]; qkv_bias only, else NULL */
   const void* const* k_bias;    /* bf16 [n_kv_heads*head_dim] */
   const void* const* v_bias;    /* bf16 [n_kv_heads*head_dim] */
-  const void* const* q_scales;  /* int4 only: bf16 scales of each linear, else NULL */
+  const void* const* q_scales;  /* int4: bf16, Q8_0: fp16 scales of each linear, else NULL */
   const void* const* k_scales;
   const void* const* v_scales;
   const void* const* o_scales;
@@ -167,9 +173,11 @@ int qw_load_weights(qw_handle* h, const qw_weights* w);
 
 /* Process T prompt ids (HOST array) at positions pos..pos+T-1, appending their
  * keys and values to the cache; afterwards pos += T. Prompts of at most
- * max_prefill_t ids with no LoRA active run as one batched causal pass; longer
- * prompts, any prompt while a LoRA is set, and every prompt of an int4 model
- * run through the sequential decode path ("Emberglass" README, maxPrefillT). logits_dev (DEVICE, vocab
+ * max_prefill_t ids with no LoRA active run as one batched causal pass on the
+ * tensor cores (int4 weights are dequantised exactly, layer by layer, into two
+ * bf16 terms for it); longer prompts, any prompt while a LoRA is set, and every
+ * prompt of a Q8_0 model run through the sequential decode path ("Emberglass"
+ * README, Context window & prefill sizes: maxPrefillT). logits_dev (DEVICE, vocab
  * floats, nullable) receives the last row's logits; argmax_host (nullable)
  * receives its greedy token and makes the call synchronous.
  * Errors: QW_ERR_ARG (T <= 0, id out of range), QW_ERR_CTX (pos+T > max_ctx). */
@@ -330,6 +338,25 @@ size_t qw_gemv_int4_workspace_bytes(int32_t rows, int32_t cols);
 int qw_gemv_int4_g128(const uint8_t* packed, const uint16_t* scales, int32_t rows, int32_t cols,
                       const float* x, float* y, void* workspace, size_t workspace_bytes,
                       void* stream);
+
+/* Q8_0 quantiser ("SuperKittens PR #7" page, Q8_0 commit: GGUF type-8 weights, blocks
+ * of 32 int8 values with one scale). w: f32 [rows, cols] DEVICE, finite, cols % 32 == 0.
+ * q: int8 [rows, cols]; scales: fp16 bits [rows, cols/32]. Per block of 32 inputs:
+ * s = fp16_rne(f32(max|w| / 127)); q = clamp(rint(f32(w / s)), -127, 127) (0 if s == 0). */
+int qw_quantize_q8_0(const float* w, int32_t rows, int32_t cols, int8_t* q, uint16_t* scales,
+                     void* stream);
+
+/* Q8_0 matrix-vector product, the contraction the decode step runs for Q8_0 weights:
+ *   y[r] = sum_c W'[r][c] x[c],  W'[r][c] = q[r][c] * scale[r][c / 32]
+ *   q: int8 [rows, cols] DEVICE; scales: fp16 bits [rows, cols/32] DEVICE; x: f32 [cols];
+ *   y: f32 [rows]; cols a multiple of 32, at most 16384; workspace: DEVICE scratch of
+ *   qw_gemv_q8_0_workspace_bytes(rows, cols) bytes, 16-byte aligned, no initialisation
+ *   needed (the rows are repacked there as the decode step streams them).
+ * The dequantisation is exact in f32, so with x = e_j the result is column j of W' bit
+ * for bit. A device-side wait that gives up is not reported (outputs invalid). */
+size_t qw_gemv_q8_0_workspace_bytes(int32_t rows, int32_t cols);
+int qw_gemv_q8_0(const int8_t* q, const uint16_t* scales, int32_t rows, int32_t cols,
+                 const float* x, float* y, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Sampling on the device ("flashmoon demo" README: greedy plus temperature / top-k /
  * top-p sampling, temp = 0 meaning greedy; the demo reads every logits row back to

@@ -37,7 +37,7 @@ Readings of points the pages leave open (each listed in the design notes):
   * SiLU(z) = z / (1 + exp(-z)).
   * q/k/v bias (Qwen2.5) is added after the projection, before RoPE.
   * LoRA on q_proj and v_proj: y = W x + b + (alpha / rank) * B (A x).
-  * int4 g128: see ``int4_quantize``.
+  * int4 g128: see ``int4_quantize``; Q8_0: see ``q8_0_quantize``.
   * Greedy argmax: ties go to the lowest index; a NaN logit is an error.
 """
 from __future__ import annotations
@@ -253,6 +253,42 @@ def int4_dequantize(packed: np.ndarray, s_bits: np.ndarray) -> np.ndarray:
     return ((nib - 8).astype(F32).reshape(N, -1, INT4_GROUP) * s[:, :, None]).reshape(N, -1)
 
 
+# ----------------------------------------------------------------------------- Q8_0 (block-32 int8)
+Q8_BLOCK = 32
+
+
+def q8_0_quantize(w: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Symmetric int8, one fp16 scale per 32 consecutive inputs of a row (Q8_0).
+
+    "SuperKittens PR #7" page, the Q8_0 commit: Q8_0 weights (GGUF type 8: blocks
+    of 32 int8 values with one scale) read by a q8_0 matvec for decode and for the
+    LM head (quantised from the embedding table when the head is tied). The page
+    gives no formula; the reading used here (the int4 reading with 127 levels):
+      s = fp16(max|w| / 127)    (division in float32, then round-to-nearest-even to fp16)
+      q = clamp(rint(w / s), -127, 127)   (division in float32, ties to even); q = 0 if s = 0
+    w: float32 [N, K] with K % 32 == 0. Returns (q int8 [N, K], scale bits uint16 [N, K/32]).
+    """
+    w = np.ascontiguousarray(w, dtype=F32)
+    N, K = w.shape
+    assert K % Q8_BLOCK == 0
+    wg = w.reshape(N, K // Q8_BLOCK, Q8_BLOCK)
+    m = np.max(np.abs(wg), axis=2)
+    with np.errstate(over="ignore"):
+        s16 = (m / F32(127.0)).astype(F32).astype(np.float16)      # IEEE round to nearest even
+    s = s16.astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (wg / s[:, :, None]).astype(F32)
+    q = np.where(s[:, :, None] == 0, 0, np.clip(np.rint(r), -127, 127)).astype(np.int8)
+    return q.reshape(N, K), s16.view(np.uint16)
+
+
+def q8_0_dequantize(q: np.ndarray, s_bits: np.ndarray) -> np.ndarray:
+    """w' = q * scale, exact in float32 (a 7-bit integer times an fp16)."""
+    N, K = q.shape
+    s = np.ascontiguousarray(s_bits, dtype=np.uint16).view(np.float16).astype(F32)
+    return (q.astype(F32).reshape(N, -1, Q8_BLOCK) * s[:, :, None]).reshape(N, K)
+
+
 # ----------------------------------------------------------------------------- model
 @dataclass
 class Config:
@@ -304,11 +340,16 @@ class OracleModel:
         self.max_ctx = max_ctx
         self.w: Dict[str, np.ndarray] = {}
         self.int4: Dict[str, Tuple[np.ndarray, np.ndarray]] = {}
-        int4_names = set()
+        self.q8: Dict[str, Tuple[np.ndarray, np.ndarray]] = {}
+        int4_names, q8_names = set(), set()
         if cfg.weight_format == "int4_g128":
             int4_names = {f"layers.{l}.{n}" for l in range(cfg.n_layers) for n in _LINEAR}
             if not cfg.tie_word_embeddings and cfg.int4_lm_head:
                 int4_names.add("lm_head")
+        elif cfg.weight_format == "q8_0":
+            q8_names = {f"layers.{l}.{n}" for l in range(cfg.n_layers) for n in _LINEAR}
+            if not cfg.tie_word_embeddings:
+                q8_names.add("lm_head")
         for name, arr in weights.items():
             if name.startswith("lora."):
                 continue
@@ -316,8 +357,17 @@ class OracleModel:
                 packed, sb = int4_quantize(arr)
                 self.int4[name] = (packed, sb)
                 self.w[name] = int4_dequantize(packed, sb)
+            elif name in q8_names:
+                q, sb = q8_0_quantize(arr)
+                self.q8[name] = (q, sb)
+                self.w[name] = q8_0_dequantize(q, sb)
             else:
                 self.w[name] = widen_bf16(arr)
+        if cfg.weight_format == "q8_0" and cfg.tie_word_embeddings:
+            # the tied head reads a Q8_0 copy of the table; the gather keeps bf16 rows
+            q, sb = q8_0_quantize(self.w["embed"])
+            self.q8["lm_head"] = (q, sb)
+            self.w["lm_head_q8"] = q8_0_dequantize(q, sb)
         self.lora: Optional[Dict[str, np.ndarray]] = None
         self.lora_scale = 0.0
         if lora is not None:
@@ -414,6 +464,8 @@ class OracleModel:
         c = self.cfg
         h = rmsnorm(x_last, self._gain("final_norm"), c.eps)
         table = "embed" if c.tie_word_embeddings else "lm_head"
+        if c.tie_word_embeddings and c.weight_format == "q8_0":
+            table = "lm_head_q8"
         logits = linear(h, self.W(table))
         return h, logits
 

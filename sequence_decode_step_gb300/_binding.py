@@ -27,6 +27,7 @@ QW_ERR_STATE = -8
 QW_ERR_NUMERIC = -9
 QW_WEIGHTS_BF16 = 0
 QW_WEIGHTS_INT4_G128 = 1
+QW_WEIGHTS_Q8_0 = 2
 QW_CAPTURE_EMBEDDING = 0
 QW_CAPTURE_BLOCK0 = 1
 QW_CAPTURE_FINAL_NORM = 2
@@ -117,6 +118,11 @@ _SIG = {
     "qw_gemv_int4_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
     "qw_gemv_int4_g128": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
                                     C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "qw_quantize_q8_0": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                   C.c_void_p]),
+    "qw_gemv_q8_0_workspace_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
+    "qw_gemv_q8_0": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
+                               C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
     "qw_lm_head_workspace_bytes": (C.c_size_t, []),
     "qw_lm_head_argmax": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
                                     C.c_float, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
@@ -177,8 +183,8 @@ def make_config(shape, max_ctx: int, max_prefill_t: int = 0) -> qw_config:
         vocab=shape.vocab, eps=shape.eps, rope_theta=shape.rope_theta,
         tie_word_embeddings=int(shape.tie_word_embeddings), qk_norm=int(shape.qk_norm),
         qkv_bias=int(shape.qkv_bias), max_ctx=max_ctx, max_prefill_t=max_prefill_t,
-        weight_format=QW_WEIGHTS_INT4_G128 if shape.weight_format == "int4_g128"
-        else QW_WEIGHTS_BF16)
+        weight_format={"int4_g128": QW_WEIGHTS_INT4_G128,
+                       "q8_0": QW_WEIGHTS_Q8_0}.get(shape.weight_format, QW_WEIGHTS_BF16))
 
 
 # -- thin wrappers with the C names (raise QwError on a non-zero status) --------

@@ -12,6 +12,7 @@
 // sets ERR_TIMEOUT in the device error word, waits (again bounded) for its
 // copies in flight and leaves without hanging.
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -47,7 +48,7 @@ __device__ __forceinline__ void block_argmax_256(float& bv, int& bi, float* r8, 
 // whose weight rows are one contiguous byte range; it streams that range
 // through `n_stages` shared-memory stages with bulk copies. Warps are split
 // into `ks` K-slices (the input slice stays in registers) and 8/ks row groups.
-template <int EPI, int MAXC, int W4>
+template <int EPI, int MAXC, int WF>
 __global__ void __launch_bounds__(256, 1) gemv_kernel(const GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -146,13 +147,20 @@ __global__ void __launch_bounds__(256, 1) gemv_kernel(const GemvArgs a) {
       for (int cc = 0; cc < MAXC; ++cc) {
         const int col = (c_lo + cc) * 256 + lane * 8;
         if ((c_lo + cc < c_hi) && col < K) {
-          if (W4) {  // 8 nibbles (4 bytes) and the scale of their 128-wide group
+          if (WF == 1) {  // 8 nibbles (4 bytes) and the scale of their 128-wide group
             const uint32_t so = a.scale_off + (uint32_t)(col >> 7) * 2;
             acc0 = dot8_i4(*reinterpret_cast<const uint32_t*>(w0 + col / 2), xr[cc],
                            bf16f(*reinterpret_cast<const uint16_t*>(w0 + so)), acc0);
             if (two)
               acc1 = dot8_i4(*reinterpret_cast<const uint32_t*>(w1 + col / 2), xr[cc],
                              bf16f(*reinterpret_cast<const uint16_t*>(w1 + so)), acc1);
+          } else if (WF == 2) {  // 8 int8 (8 bytes) and the fp16 scale of their 32-wide block
+            const uint32_t so = a.scale_off + (uint32_t)(col >> 5) * 2;
+            acc0 = dot8_i8(*reinterpret_cast<const uint2*>(w0 + col), xr[cc],
+                           __half2float(*reinterpret_cast<const __half*>(w0 + so)), acc0);
+            if (two)
+              acc1 = dot8_i8(*reinterpret_cast<const uint2*>(w1 + col), xr[cc],
+                             __half2float(*reinterpret_cast<const __half*>(w1 + so)), acc1);
           } else {
             acc0 = dot8(*reinterpret_cast<const uint4*>(w0 + (size_t)col * 2), xr[cc], acc0);
             if (two)
@@ -315,9 +323,14 @@ static cudaError_t launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, cu
 template <int EPI>
 static cudaError_t launch_gemv_epi(const GemvArgs& a, int grid, bool pdl, cudaStream_t s) {
   const size_t smem = gemv_smem_bytes(a);
-  if (a.w4) {
+  if (a.wfmt == 1) {
     if (a.cpw <= 4) return launch_ex(gemv_kernel<EPI, 4, 1>, dim3(grid), dim3(256), smem, s, pdl, a);
     if (a.cpw <= 8) return launch_ex(gemv_kernel<EPI, 8, 1>, dim3(grid), dim3(256), smem, s, pdl, a);
+    return cudaErrorInvalidValue;
+  }
+  if (a.wfmt == 2) {
+    if (a.cpw <= 4) return launch_ex(gemv_kernel<EPI, 4, 2>, dim3(grid), dim3(256), smem, s, pdl, a);
+    if (a.cpw <= 8) return launch_ex(gemv_kernel<EPI, 8, 2>, dim3(grid), dim3(256), smem, s, pdl, a);
     return cudaErrorInvalidValue;
   }
   if (a.cpw <= 4) return launch_ex(gemv_kernel<EPI, 4, 0>, dim3(grid), dim3(256), smem, s, pdl, a);
@@ -732,6 +745,69 @@ cudaError_t launch_pack_int4_rows(const uint8_t* nib, const uint16_t* scales, in
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ Q8_0 row packing
+// Row r of (q [rows, K] int8, scales [rows, K/32] fp16 bits) -> dst row dst_row0 + r * step
+// in the layout int8 | scales | zero pad (q8_row_bytes(K) bytes per row).
+__global__ void pack_q8_rows_kernel(const int8_t* q, const uint16_t* scales, int K, uint8_t* dst,
+                                    int dst_row0, int step) {
+  const int r = blockIdx.x;
+  const uint32_t rb = q8_row_bytes(K), G = (uint32_t)K / 32;
+  uint8_t* d = dst + (size_t)(dst_row0 + (size_t)r * step) * rb;
+  const int8_t* sq = q + (size_t)r * K;
+  for (uint32_t i = threadIdx.x; i < (uint32_t)K; i += blockDim.x) d[i] = (uint8_t)sq[i];
+  const uint16_t* ss = scales + (size_t)r * G;
+  for (uint32_t i = threadIdx.x; i < (rb - (uint32_t)K) / 2; i += blockDim.x)
+    reinterpret_cast<uint16_t*>(d + K)[i] = i < G ? ss[i] : (uint16_t)0;
+}
+
+cudaError_t launch_pack_q8_rows(const int8_t* q, const uint16_t* scales, int rows, int K,
+                                uint8_t* dst, int dst_row0, int dst_row_step, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  pack_q8_rows_kernel<<<rows, 256, 0, s>>>(q, scales, K, dst, dst_row0, dst_row_step);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ Q8_0 quantiser
+// One warp per block of 32 inputs, a lane per input: s = fp16(max|w| / 127) (f32
+// division, round to nearest even), q = clamp(rint(w / s), -127, 127) (f32 division,
+// ties to even), q = 0 when s = 0.
+template <bool BF16_IN>
+__global__ void __launch_bounds__(256) quantize_q8_kernel(const void* w, int rows, int cols,
+                                                          int8_t* q, size_t q_stride,
+                                                          uint16_t* scales, size_t s_stride) {
+  const int G = cols / 32;
+  const long long gi = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gi >= (long long)rows * G) return;
+  const int r = (int)(gi / G), g = (int)(gi % G);
+  const size_t idx = (size_t)r * cols + g * 32 + lane;
+  const float v = BF16_IN ? bf16f(reinterpret_cast<const uint16_t*>(w)[idx])
+                          : reinterpret_cast<const float*>(w)[idx];
+  const float m = warp_max(fabsf(v));
+  const __half sh = __float2half_rn(__fdiv_rn(m, 127.0f));
+  const float sc = __half2float(sh);
+  float qv = 0.f;
+  if (sc != 0.f) qv = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(v, sc))));
+  q[(size_t)r * q_stride + g * 32 + lane] = (int8_t)(int)qv;
+  if (lane == 0) scales[(size_t)r * s_stride + g] = __half_as_ushort(sh);
+}
+
+cudaError_t launch_quantize_q8(const void* w, bool w_bf16, int rows, int cols, int8_t* q,
+                               size_t q_stride, uint16_t* scales, size_t s_stride,
+                               cudaStream_t s) {
+  const long long groups = (long long)rows * (cols / 32);
+  if (groups == 0) return cudaSuccess;
+  const long long blocks = (groups + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (w_bf16)
+    quantize_q8_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(w, rows, cols, q, q_stride, scales,
+                                                              s_stride);
+  else
+    quantize_q8_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(w, rows, cols, q, q_stride, scales,
+                                                               s_stride);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ RoPE table
 // cos/sin of p * theta^(-2j/hd), formed in fp64 and rounded to f32 once.
 __global__ void rope_table_kernel(float2* t, int cap, int hd, double theta) {
@@ -823,7 +899,9 @@ cudaError_t set_kernel_attributes() {
   QW_ALLOW((gemv_kernel<E, 4, 0>), big); \
   QW_ALLOW((gemv_kernel<E, 8, 0>), big); \
   QW_ALLOW((gemv_kernel<E, 4, 1>), big); \
-  QW_ALLOW((gemv_kernel<E, 8, 1>), big)
+  QW_ALLOW((gemv_kernel<E, 8, 1>), big); \
+  QW_ALLOW((gemv_kernel<E, 4, 2>), big); \
+  QW_ALLOW((gemv_kernel<E, 8, 2>), big)
   QW_ALLOW_GEMV(EPI_STORE);
   QW_ALLOW_GEMV(EPI_RESIDUAL);
   QW_ALLOW_GEMV(EPI_SWIGLU);

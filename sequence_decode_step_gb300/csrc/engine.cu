@@ -131,6 +131,11 @@ struct qw_handle {
   CUtensorMap tm_xn_hi, tm_xn_lo, tm_o_hi, tm_o_lo, tm_m_hi, tm_m_lo;
   FaMaps tm_attn;  // attention operands: Q, K and V^T splits
   std::vector<CUtensorMap> tm_qkv, tm_ow, tm_gu, tm_dw;  // per layer, weight side
+  // int4 models: one layer's weights dequantised into exact two-bf16 planes (reused
+  // by every layer of a prefill) and their tensor maps [hi, lo]
+  uint16_t* pf_w4 = nullptr;
+  uint16_t *w4_qkv[2] = {}, *w4_o[2] = {}, *w4_gu[2] = {}, *w4_dw[2] = {};
+  CUtensorMap tm_qkv4[2], tm_ow4[2], tm_gu4[2], tm_dw4[2];
   int* d_status = nullptr;  // [2] greedy id, error word (written by the LM head)
   // pinned host staging
   int* h_status = nullptr;  // [8]: argmax, error, set_pos staging, error copy, sampled id
@@ -173,8 +178,8 @@ struct qw_handle {
   int lora_rank = 0;
   float lora_scale = 0.f;
   float* lora_t = nullptr;  // [2 * 64]
-  bool w4 = false;          // int4 g128 linear weights
-  bool lm_w4 = false;       // int4 LM head (untied int4 models)
+  int wfmt = 0;             // linear weights: 0 bf16, 1 int4 g128, 2 Q8_0 (GemvArgs::wfmt)
+  int lm_fmt = 0;           // LM head rows: 1 for untied int4 models, 2 for every Q8_0 model
   std::string err;
 };
 
@@ -210,17 +215,21 @@ static int validate_config(const qw_config* c, std::string& why) {
     why = "n_q_heads must be a multiple of n_kv_heads, at most 8 per kv head";
     return QW_ERR_ARG;
   }
-  const int mult = c->weight_format == QW_WEIGHTS_INT4_G128 ? 128 : 8;
+  const int mult = c->weight_format == QW_WEIGHTS_INT4_G128 ? 128
+                 : c->weight_format == QW_WEIGHTS_Q8_0     ? 32
+                                                           : 8;
   if (c->hidden % mult || (c->n_q_heads * c->head_dim) % mult || c->intermediate % mult) {
-    why = "hidden, n_q_heads*head_dim and intermediate must be multiples of 8 (128 for int4)";
+    why = "hidden, n_q_heads*head_dim and intermediate must be multiples of 8 (128 for int4, "
+          "32 for Q8_0)";
     return QW_ERR_ARG;
   }
   if (c->hidden > 16384 || c->intermediate > 16384 || c->n_q_heads * c->head_dim > 16384) {
     why = "hidden, intermediate and n_q_heads*head_dim are limited to 16384";
     return QW_ERR_ARG;
   }
-  if (c->weight_format != QW_WEIGHTS_BF16 && c->weight_format != QW_WEIGHTS_INT4_G128) {
-    why = "weight_format must be QW_WEIGHTS_BF16 or QW_WEIGHTS_INT4_G128";
+  if (c->weight_format != QW_WEIGHTS_BF16 && c->weight_format != QW_WEIGHTS_INT4_G128 &&
+      c->weight_format != QW_WEIGHTS_Q8_0) {
+    why = "weight_format must be QW_WEIGHTS_BF16, QW_WEIGHTS_INT4_G128 or QW_WEIGHTS_Q8_0";
     return QW_ERR_ARG;
   }
   if (c->max_ctx <= 0 || c->max_prefill_t < 0) {
@@ -261,8 +270,8 @@ static int alloc_state(qw_handle* h) {
                                          c.head_dim, c.n_q_heads / c.n_kv_heads, c.n_layers) &&
                (int64_t)c.vocab * h->num_sms < (int64_t)1 << 31;  // 32-bit slice arithmetic
   h->use_mega = h->mega_ok;
-  h->w4 = c.weight_format == QW_WEIGHTS_INT4_G128;
-  h->lm_w4 = h->w4 && !c.tie_word_embeddings;
+  h->wfmt = c.weight_format == QW_WEIGHTS_INT4_G128 ? 1 : c.weight_format == QW_WEIGHTS_Q8_0 ? 2 : 0;
+  h->lm_fmt = h->wfmt == 2 ? 2 : (h->wfmt == 1 && !c.tie_word_embeddings ? 1 : 0);
   h->lm_grid = std::min({c.vocab, h->num_sms, 1024});
   struct Piece { void** p; size_t bytes; };
   const size_t kv_bytes = L * nkv * cap * hd * 4;
@@ -312,6 +321,9 @@ static int alloc_state(qw_handle* h) {
     pieces.push_back({(void**)&h->pf_m_hi, Tm * I * 2});
     pieces.push_back({(void**)&h->pf_m_lo, Tm * I * 2});
     pieces.push_back({(void**)&h->pf_kvs, attn_kv_bytes(c.n_kv_heads, c.head_dim, c.max_ctx)});
+    if (h->wfmt == 1)  // the hi and lo planes of one layer's four weight matrices
+      pieces.push_back({(void**)&h->pf_w4,
+                        2 * 2 * (qkv_rows * H + H * qd + 2 * I * H + H * I)});
   }
   size_t total = 0;
   for (auto& p : pieces) total = align_up(total, 256) + p.bytes;
@@ -333,6 +345,24 @@ static int alloc_state(qw_handle* h) {
               make_attn_maps(&h->tm_attn, h->pf_q_hi, h->pf_q_lo, (int)Tm, c.n_q_heads,
                              h->pf_kvs, c.n_kv_heads, c.head_dim, c.max_ctx);
     if (!ok) QW_FAIL(h, QW_ERR_CUDA, "prefill: TMA descriptor encoding failed");
+    if (h->wfmt == 1) {
+      uint16_t* q = h->pf_w4;
+      for (int t = 0; t < 2; ++t) {
+        h->w4_qkv[t] = q;
+        q += qkv_rows * H;
+        h->w4_o[t] = q;
+        q += H * qd;
+        h->w4_gu[t] = q;
+        q += 2 * I * H;
+        h->w4_dw[t] = q;
+        q += H * I;
+        if (!make_tmap_bf16_2d(&h->tm_qkv4[t], h->w4_qkv[t], qkv_rows, H, 256) ||
+            !make_tmap_bf16_2d(&h->tm_ow4[t], h->w4_o[t], H, qd, 64) ||
+            !make_tmap_bf16_2d(&h->tm_gu4[t], h->w4_gu[t], 2 * I, H, 256) ||
+            !make_tmap_bf16_2d(&h->tm_dw4[t], h->w4_dw[t], H, I, 64))
+          QW_FAIL(h, QW_ERR_CUDA, "prefill: TMA descriptor encoding failed");
+      }
+    }
   }
   QW_CUDA(h, cudaHostAlloc((void**)&h->h_tokens, std::max<size_t>(cap, Tm) * 4, cudaHostAllocPortable));
   QW_CUDA(h, cudaHostAlloc((void**)&h->h_status, 32, cudaHostAllocPortable));
@@ -416,11 +446,12 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: qk_norm set but q_norm/k_norm missing");
   if (c.qkv_bias && (!w->q_bias || !w->k_bias || !w->v_bias))
     QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: qkv_bias set but a bias is missing");
-  if (h->w4 && (!w->q_scales || !w->k_scales || !w->v_scales || !w->o_scales ||
-                !w->gate_scales || !w->up_scales || !w->down_scales ||
-                (h->lm_w4 && !w->lm_head_scales)))
-    QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: int4 weights need every scales tensor");
-  for (int l = 0; l < L && h->w4; ++l)
+  const bool untied_q = h->lm_fmt != 0 && !c.tie_word_embeddings;  // lm_head passed quantised
+  if (h->wfmt && (!w->q_scales || !w->k_scales || !w->v_scales || !w->o_scales ||
+                  !w->gate_scales || !w->up_scales || !w->down_scales ||
+                  (untied_q && !w->lm_head_scales)))
+    QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: int4 / Q8_0 weights need every scales tensor");
+  for (int l = 0; l < L && h->wfmt; ++l)
     if (!w->q_scales[l] || !w->k_scales[l] || !w->v_scales[l] || !w->o_scales[l] ||
         !w->gate_scales[l] || !w->up_scales[l] || !w->down_scales[l])
       QW_FAIL(h, QW_ERR_ARG, "qw_load_weights: NULL scales at layer " + std::to_string(l));
@@ -441,9 +472,12 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     cudaFree(h->warena);
     h->warena = nullptr;
   }
-  // Bytes of one packed row of K inputs: bf16, or int4 nibbles + scales (+ pad).
-  auto rb = [&](size_t K) -> size_t { return h->w4 ? int4_row_bytes((int)K) : K * 2; };
-  const size_t lm_rb = h->lm_w4 ? int4_row_bytes((int)H) : H * 2;
+  // Bytes of one packed row of K inputs: bf16, or int4 nibbles / Q8_0 bytes + scales (+ pad).
+  auto fmt_rb = [](int fmt, size_t K) -> size_t {
+    return fmt == 1 ? int4_row_bytes((int)K) : fmt == 2 ? q8_row_bytes((int)K) : K * 2;
+  };
+  auto rb = [&](size_t K) { return fmt_rb(h->wfmt, K); };
+  const size_t lm_rb = fmt_rb(h->lm_fmt, H);
   // Arena layout, 256-byte aligned pieces.
   const size_t per_layer = align_up((qd + 2 * kd) * rb(H), 256) +
                            (c.qkv_bias ? align_up((qd + 2 * kd) * 2, 256) : 0) +
@@ -451,7 +485,8 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
                            align_up(H * rb(I), 256) + 2 * align_up(H * 2, 256) +
                            (c.qk_norm ? 2 * align_up(hd * 2, 256) : 0);
   const size_t head = align_up((size_t)c.vocab * H * 2, 256) +
-                      (c.tie_word_embeddings ? 0 : align_up((size_t)c.vocab * lm_rb, 256)) +
+                      (c.tie_word_embeddings && h->lm_fmt == 0
+                           ? 0 : align_up((size_t)c.vocab * lm_rb, 256)) +
                       align_up(H * 2, 256);
   h->warena_bytes = per_layer * L + head;
   QW_CUDA(h, cudaMalloc((void**)&h->warena, h->warena_bytes));
@@ -467,12 +502,24 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
   uint8_t* p = take((size_t)c.vocab * H * 2);
   QW_CUDA(h, cp(p, w->embed, (size_t)c.vocab * H * 2));
   h->embed = (const uint16_t*)p;
-  if (c.tie_word_embeddings) {
+  if (c.tie_word_embeddings && h->lm_fmt == 2) {
+    // Q8_0 models read the tied table through a Q8_0 copy ("SuperKittens PR #7", Q8_0
+    // commit: the LM head is quantised from the embedding table); the gather keeps bf16
+    p = take((size_t)c.vocab * lm_rb);
+    QW_CUDA(h, launch_quantize_q8(h->embed, true, c.vocab, (int)H, (int8_t*)p, lm_rb,
+                                  (uint16_t*)(p + H), lm_rb / 2, h->stream));
+    h->lm_head = (const uint16_t*)p;
+  } else if (c.tie_word_embeddings) {
     h->lm_head = h->embed;  // one table serves the gather and the output projection
-  } else if (h->lm_w4) {
+  } else if (h->lm_fmt == 1) {
     p = take((size_t)c.vocab * lm_rb);
     QW_CUDA(h, launch_pack_int4_rows((const uint8_t*)w->lm_head, (const uint16_t*)w->lm_head_scales,
                                      c.vocab, (int)H, p, 0, 1, h->stream));
+    h->lm_head = (const uint16_t*)p;
+  } else if (h->lm_fmt == 2) {
+    p = take((size_t)c.vocab * lm_rb);
+    QW_CUDA(h, launch_pack_q8_rows((const int8_t*)w->lm_head, (const uint16_t*)w->lm_head_scales,
+                                   c.vocab, (int)H, p, 0, 1, h->stream));
     h->lm_head = (const uint16_t*)p;
   } else {
     p = take((size_t)c.vocab * H * 2);
@@ -487,11 +534,14 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     LayerW& lw = h->layers[l];
     auto pack4 = [&](const void* nib, const void* sc, size_t rows, size_t K, uint8_t* dst,
                      size_t row0, int step) {
+      if (h->wfmt == 2)
+        return launch_pack_q8_rows((const int8_t*)nib, (const uint16_t*)sc, (int)rows, (int)K,
+                                   dst, (int)row0, step, h->stream);
       return launch_pack_int4_rows((const uint8_t*)nib, (const uint16_t*)sc, (int)rows, (int)K, dst,
                                    (int)row0, step, h->stream);
     };
     p = take((qd + 2 * kd) * rb(H));  // fused [q; k; v] rows
-    if (h->w4) {
+    if (h->wfmt) {
       QW_CUDA(h, pack4(w->q[l], w->q_scales[l], qd, H, p, 0, 1));
       QW_CUDA(h, pack4(w->k[l], w->k_scales[l], kd, H, p, qd, 1));
       QW_CUDA(h, pack4(w->v[l], w->v_scales[l], kd, H, p, qd + kd, 1));
@@ -509,11 +559,11 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
       lw.qkv_bias = (const uint16_t*)p;
     }
     p = take(H * rb(qd));
-    if (h->w4) QW_CUDA(h, pack4(w->o[l], w->o_scales[l], H, qd, p, 0, 1));
+    if (h->wfmt) QW_CUDA(h, pack4(w->o[l], w->o_scales[l], H, qd, p, 0, 1));
     else QW_CUDA(h, cp(p, w->o[l], H * qd * 2));
     lw.o = (const uint16_t*)p;
     p = take(2 * I * rb(H));  // gate row i -> packed row 2i, up row i -> 2i+1
-    if (h->w4) {
+    if (h->wfmt) {
       QW_CUDA(h, pack4(w->gate[l], w->gate_scales[l], I, H, p, 0, 2));
       QW_CUDA(h, pack4(w->up[l], w->up_scales[l], I, H, p, 1, 2));
     } else {
@@ -524,7 +574,7 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     }
     lw.gateup = (const uint16_t*)p;
     p = take(H * rb(I));
-    if (h->w4) QW_CUDA(h, pack4(w->down[l], w->down_scales[l], H, I, p, 0, 1));
+    if (h->wfmt) QW_CUDA(h, pack4(w->down[l], w->down_scales[l], H, I, p, 0, 1));
     else QW_CUDA(h, cp(p, w->down[l], H * I * 2));
     lw.down = (const uint16_t*)p;
     p = take(H * 2);
@@ -556,7 +606,7 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     QW_CUDA(h, cudaMemcpyAsync(h->d_layers, ld.data(), L * sizeof(LayerDev),
                                cudaMemcpyHostToDevice, h->stream));
   }
-  if (c.max_prefill_t > 0 && !h->w4) {
+  if (c.max_prefill_t > 0 && h->wfmt == 0) {
     h->tm_qkv.resize(L);
     h->tm_ow.resize(L);
     h->tm_gu.resize(L);
@@ -593,15 +643,15 @@ static void plan(GemvArgs& a, int grid) {
 }
 
 static GemvArgs base_gemv(qw_handle* h, const void* w, int n_units, int rpu, int K,
-                          bool w4) {
+                          int wfmt) {
   GemvArgs a{};
   a.w = (const uint8_t*)w;
   a.n_units = n_units;
   a.rpu = rpu;
   a.K = K;
-  a.w4 = w4 ? 1 : 0;
-  a.row_bytes = w4 ? int4_row_bytes(K) : (uint32_t)K * 2;
-  a.scale_off = (uint32_t)K / 2;
+  a.wfmt = wfmt;
+  a.row_bytes = wfmt == 1 ? int4_row_bytes(K) : wfmt == 2 ? q8_row_bytes(K) : (uint32_t)K * 2;
+  a.scale_off = wfmt == 2 ? (uint32_t)K : (uint32_t)K / 2;
   a.eps = h->cfg.eps;
   a.err = h->d_err;
   a.wait_ns = h->wait_ns;
@@ -613,7 +663,7 @@ static GemvArgs base_gemv(qw_handle* h, const void* w, int n_units, int rpu, int
 // the last CTA records the id at the device position and advances it.
 static cudaError_t launch_lm_head(qw_handle* h, const float* x, float* norm_out, bool pdl,
                                   cudaStream_t s) {
-  GemvArgs a = base_gemv(h, h->lm_head, h->cfg.vocab, 1, h->cfg.hidden, h->lm_w4);
+  GemvArgs a = base_gemv(h, h->lm_head, h->cfg.vocab, 1, h->cfg.hidden, h->lm_fmt);
   a.x = x;
   a.norm_g = h->final_norm;
   a.y = h->logits;
@@ -716,7 +766,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       }
     }
     {  // fused QKV projection with the input RMSNorm in its prologue
-      GemvArgs a = base_gemv(h, lw.qkv, qkv_rows, 1, H, h->w4);
+      GemvArgs a = base_gemv(h, lw.qkv, qkv_rows, 1, H, h->wfmt);
       a.x = h->x;
       a.norm_g = lw.attn_norm;
       a.bias = lw.qkv_bias;
@@ -760,7 +810,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       if ((e = launch_attention(t, hd, true, s)) != cudaSuccess) return e;
     }
     {  // o_proj + residual
-      GemvArgs a = base_gemv(h, lw.o, H, 1, qd, h->w4);
+      GemvArgs a = base_gemv(h, lw.o, H, 1, qd, h->wfmt);
       a.x = h->attn_o;
       a.y = h->x;
       const int grid = std::min(H, h->num_sms);
@@ -768,7 +818,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       if ((e = launch_gemv(EPI_RESIDUAL, a, grid, true, s)) != cudaSuccess) return e;
     }
     {  // gate/up with the post-attention RMSNorm in its prologue, SwiGLU epilogue
-      GemvArgs a = base_gemv(h, lw.gateup, I, 2, H, h->w4);
+      GemvArgs a = base_gemv(h, lw.gateup, I, 2, H, h->wfmt);
       a.x = h->x;
       a.norm_g = lw.mlp_norm;
       a.y = h->mlp;
@@ -777,7 +827,7 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       if ((e = launch_gemv(EPI_SWIGLU, a, grid, true, s)) != cudaSuccess) return e;
     }
     {  // down + residual (block-0 checkpoint taken here)
-      GemvArgs a = base_gemv(h, lw.down, H, 1, I, h->w4);
+      GemvArgs a = base_gemv(h, lw.down, H, 1, I, h->wfmt);
       a.x = h->mlp;
       a.y = h->x;
       a.cap_out = (h->capture_on && l == 0) ? h->cap_blk0 : nullptr;
@@ -1009,9 +1059,10 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
   QW_CUDA(h, cudaMemcpyAsync(h->pf_ids, h->h_tokens, (size_t)T * 4, cudaMemcpyHostToDevice, s));
   QW_CUDA(h, launch_embed_rows(h->pf_ids, T, h->embed, c.vocab, H, h->pf_x,
                                h->capture_on ? h->cap_emb : nullptr, p0, h->d_err, s));
+  const bool w4 = h->wfmt == 1;
   auto gemm = [&](int bn, int epi, const CUtensorMap& ahi, const CUtensorMap& alo,
-                  const CUtensorMap& b, int N, int K, float* out, const uint16_t* bias,
-                  uint16_t* ohi, uint16_t* olo, float* cap) {
+                  const CUtensorMap& b, const CUtensorMap* b_lo, int N, int K, float* out,
+                  const uint16_t* bias, uint16_t* ohi, uint16_t* olo, float* cap) {
     GemmArgs g{};
     g.M = T;
     g.N = N;
@@ -1027,29 +1078,43 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
     g.cap_row0 = p0;
     g.err = h->d_err;
     g.wait_ns = h->wait_ns;
-    return launch_gemm(bn, epi, ahi, alo, b, g, s);
+    return launch_gemm(bn, epi, ahi, alo, b, b_lo, g, s);
   };
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& lw = h->layers[l];
     float* kc = h->k_cache + (size_t)l * kv_layer;
     float* vc = h->v_cache + (size_t)l * kv_layer;
+    if (w4) {  // this layer's int4 rows as exact two-bf16 planes
+      QW_CUDA(h, launch_dequant_int4_split((const uint8_t*)lw.qkv, qkv_rows, H, h->w4_qkv[0],
+                                           h->w4_qkv[1], s));
+      QW_CUDA(h, launch_dequant_int4_split((const uint8_t*)lw.o, H, qd, h->w4_o[0], h->w4_o[1], s));
+      QW_CUDA(h, launch_dequant_int4_split((const uint8_t*)lw.gateup, 2 * I, H, h->w4_gu[0],
+                                           h->w4_gu[1], s));
+      QW_CUDA(h, launch_dequant_int4_split((const uint8_t*)lw.down, H, I, h->w4_dw[0],
+                                           h->w4_dw[1], s));
+    }
+    const CUtensorMap& wq = w4 ? h->tm_qkv4[0] : h->tm_qkv[l];
+    const CUtensorMap& wo = w4 ? h->tm_ow4[0] : h->tm_ow[l];
+    const CUtensorMap& wg = w4 ? h->tm_gu4[0] : h->tm_gu[l];
+    const CUtensorMap& wd = w4 ? h->tm_dw4[0] : h->tm_dw[l];
     QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, lw.attn_norm, c.eps, h->pf_xn_hi, h->pf_xn_lo,
                                    nullptr, 0, s));
-    QW_CUDA(h, gemm(256, GEPI_STORE, h->tm_xn_hi, h->tm_xn_lo, h->tm_qkv[l], qkv_rows, H,
-                    h->pf_qkv, lw.qkv_bias, nullptr, nullptr, nullptr));
+    QW_CUDA(h, gemm(256, GEPI_STORE, h->tm_xn_hi, h->tm_xn_lo, wq, w4 ? &h->tm_qkv4[1] : nullptr,
+                    qkv_rows, H, h->pf_qkv, lw.qkv_bias, nullptr, nullptr, nullptr));
     QW_CUDA(h, launch_qk_rope_kv_rows(h->pf_qkv, T, p0, c.n_q_heads, c.n_kv_heads, hd, lw.q_norm,
                                       lw.k_norm, c.eps, h->rope, h->pf_q_hi, h->pf_q_lo, kc, vc,
-                                      c.max_ctx, s));
+                                      c.max_ctx, h->pf_kvs, s));
     QW_CUDA(h, launch_attn_prefill(h->tm_attn, kc, vc, h->pf_kvs, c.max_ctx, p0, T, c.n_q_heads,
                                    c.n_kv_heads, hd, h->pf_o_hi, h->pf_o_lo, h->d_err, h->wait_ns,
                                    s));
-    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, h->tm_ow[l], H, qd, h->pf_x, nullptr,
-                    nullptr, nullptr, nullptr));
+    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, wo, w4 ? &h->tm_ow4[1] : nullptr, H,
+                    qd, h->pf_x, nullptr, nullptr, nullptr, nullptr));
     QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, lw.mlp_norm, c.eps, h->pf_xn_hi, h->pf_xn_lo,
                                    nullptr, 0, s));
-    QW_CUDA(h, gemm(256, GEPI_SWIGLU, h->tm_xn_hi, h->tm_xn_lo, h->tm_gu[l], 2 * I, H, nullptr,
-                    nullptr, h->pf_m_hi, h->pf_m_lo, nullptr));
-    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_m_hi, h->tm_m_lo, h->tm_dw[l], H, I, h->pf_x, nullptr,
+    QW_CUDA(h, gemm(256, GEPI_SWIGLU, h->tm_xn_hi, h->tm_xn_lo, wg, w4 ? &h->tm_gu4[1] : nullptr,
+                    2 * I, H, nullptr, nullptr, h->pf_m_hi, h->pf_m_lo, nullptr));
+    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_m_hi, h->tm_m_lo, wd, w4 ? &h->tm_dw4[1] : nullptr, H, I,
+                    h->pf_x, nullptr,
                     nullptr, nullptr, (h->capture_on && l == 0) ? h->cap_blk0 : nullptr));
   }
   if (h->capture_on)
@@ -1074,7 +1139,7 @@ extern "C" int qw_prefill(qw_handle* h, const int32_t* ids_host, int32_t T, floa
     QW_FAIL(h, QW_ERR_CTX, "qw_prefill: pos + T > max_ctx");
   DeviceGuard dg(h->device);
   const int p0 = h->pos;
-  if (T <= h->cfg.max_prefill_t && !h->lora_active && !h->w4) {
+  if (T <= h->cfg.max_prefill_t && !h->lora_active && h->wfmt != 2) {
     rc = prefill_batched(h, ids_host, T);
   } else {
     // Sequential path ("Emberglass" README, maxPrefillT: longer prompts, or a
@@ -1386,9 +1451,61 @@ extern "C" int qw_gemv_int4_g128(const uint8_t* packed, const uint16_t* scales, 
   a.n_units = rows;
   a.rpu = 1;
   a.K = cols;
-  a.w4 = 1;
+  a.wfmt = 1;
   a.row_bytes = int4_row_bytes(cols);
   a.scale_off = (uint32_t)cols / 2;
+  a.x = x;
+  a.y = y;
+  a.err = (int*)ws;
+  a.wait_ns = 1000000000ull;
+  plan_gemv(a, grid, kStreamStage, kStreamStages);
+  QW_OP_CUDA(launch_gemv(EPI_STORE, a, grid, false, st));
+  return QW_OK;
+}
+
+extern "C" int qw_quantize_q8_0(const float* w, int32_t rows, int32_t cols, int8_t* q,
+                                uint16_t* scales, void* stream) {
+  if (!w || !q || !scales || rows <= 0 || cols <= 0 || cols % 32)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            "qw_quantize_q8_0: null buffer, empty shape or cols % 32 != 0");
+  QW_OP_CUDA(launch_quantize_q8(w, false, rows, cols, q, (size_t)cols, scales, (size_t)cols / 32,
+                                (cudaStream_t)stream));
+  return QW_OK;
+}
+
+// Q8_0 GEMV workspace: [err int] padded to 256, then the rows repacked as the decode
+// step streams them (q8_row_bytes(cols) each: int8 values, scales, zero pad).
+extern "C" size_t qw_gemv_q8_0_workspace_bytes(int32_t rows, int32_t cols) {
+  if (rows <= 0 || cols <= 0 || cols % 32) return 0;
+  return 256 + (size_t)rows * q8_row_bytes(cols);
+}
+
+extern "C" int qw_gemv_q8_0(const int8_t* q, const uint16_t* scales, int32_t rows, int32_t cols,
+                            const float* x, float* y, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!q || !scales || !x || !y || !workspace)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG, "qw_gemv_q8_0: null buffer");
+  if (rows <= 0 || cols <= 0 || cols % 32 || cols > 16384)
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            "qw_gemv_q8_0: rows must be positive and cols a multiple of 32, at most 16384");
+  if (workspace_bytes < qw_gemv_q8_0_workspace_bytes(rows, cols) || ((uintptr_t)workspace & 15))
+    QW_FAIL((qw_handle*)nullptr, QW_ERR_ARG,
+            "qw_gemv_q8_0: workspace too small or not 16-byte aligned");
+  int sms = 0;
+  if (op_sms(&sms)) return QW_ERR_CUDA;
+  uint8_t* ws = (uint8_t*)workspace;
+  uint8_t* rows_dev = ws + 256;
+  const cudaStream_t st = (cudaStream_t)stream;
+  QW_OP_CUDA(launch_pack_q8_rows(q, scales, rows, cols, rows_dev, 0, 1, st));
+  const int grid = std::min(rows, sms);
+  GemvArgs a{};
+  a.w = rows_dev;
+  a.n_units = rows;
+  a.rpu = 1;
+  a.K = cols;
+  a.wfmt = 2;
+  a.row_bytes = q8_row_bytes(cols);
+  a.scale_off = (uint32_t)cols;
   a.x = x;
   a.y = y;
   a.err = (int*)ws;
@@ -1474,7 +1591,7 @@ extern "C" int qw_gemm_bf16(const uint16_t* a_hi, const uint16_t* a_lo, const ui
   g.err = gemm_op_err_word();
   g.wait_ns = 1000000000ull;
   if (!g.err) QW_FAIL((qw_handle*)nullptr, QW_ERR_CUDA, "qw_gemm_bf16: error word lookup failed");
-  QW_OP_CUDA(launch_gemm(bn, GEPI_STORE, ta_hi, ta_lo, tb, g, (cudaStream_t)stream));
+  QW_OP_CUDA(launch_gemm(bn, GEPI_STORE, ta_hi, ta_lo, tb, nullptr, g, (cudaStream_t)stream));
   return QW_OK;
 }
 

@@ -36,12 +36,14 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta_hi,
                    const __grid_constant__ CUtensorMap ta_lo,
-                   const __grid_constant__ CUtensorMap tb, const GemmArgs a) {
+                   const __grid_constant__ CUtensorMap tb,
+                   const __grid_constant__ CUtensorMap tb_lo, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int NS = a.n_stages;
-  const uint32_t stage_bytes = (uint32_t)a.a_split * kATileBytes + (uint32_t)BN * GBK * 2;
+  constexpr uint32_t kBTileBytes = (uint32_t)BN * GBK * 2;
+  const uint32_t stage_bytes = (uint32_t)a.a_split * kATileBytes + (uint32_t)a.b_split * kBTileBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * stage_bytes);
   uint64_t* empty = full + NS;
   uint64_t* accf = empty + NS;
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(192, 1)
       tma_load_2d(st, &ta_hi, kt * GBK, m0, &full[s]);
       if (a.a_split == 2) tma_load_2d(st + kATileBytes, &ta_lo, kt * GBK, m0, &full[s]);
       tma_load_2d(st + a.a_split * kATileBytes, &tb, kt * GBK, n0, &full[s]);
+      if (a.b_split == 2)
+        tma_load_2d(st + a.a_split * kATileBytes + kBTileBytes, &tb_lo, kt * GBK, n0, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -97,9 +101,12 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int k = 0; k < GBK / 16; ++k) {
         const uint64_t bd = sw128_kmajor_desc(sb + k * 32);
-        tc_mma_bf16(tbase, sw128_kmajor_desc(sa + k * 32), bd, idesc, (kt | k) != 0);
+        const uint64_t ad = sw128_kmajor_desc(sa + k * 32);
+        tc_mma_bf16(tbase, ad, bd, idesc, (kt | k) != 0);
         if (a.a_split == 2)
           tc_mma_bf16(tbase, sw128_kmajor_desc(sa + kATileBytes + k * 32), bd, idesc, 1);
+        if (a.b_split == 2)  // the weight's lo term against the activation's hi term
+          tc_mma_bf16(tbase, ad, sw128_kmajor_desc(sb + kBTileBytes + k * 32), idesc, 1);
       }
       tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
     }
@@ -251,11 +258,12 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* X, int H
 
 // Row t (position p0 + t): per-head QK-RMSNorm and RoPE of q and k, q scaled by
 // 1/sqrt(hd) into Q [T][nq][hd] as a two-bf16 split; k and v appended to the cache at
-// their position.
+// their position, and k also as the two-bf16 row the prefill attention reads.
 template <int HD>
 __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
     const float* QKV, int p0, int nq, int nkv, const uint16_t* q_norm, const uint16_t* k_norm,
-    float eps, const float2* rope, uint16_t* q_hi, uint16_t* q_lo, float* kc, float* vc, int cap) {
+    float eps, const float2* rope, uint16_t* q_hi, uint16_t* q_lo, float* kc, float* vc, int cap,
+    uint16_t* k_hi, uint16_t* k_lo, int kv_rows) {
   constexpr int EPL = HD / 32;
   const int t = blockIdx.x, pos = p0 + t;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,8 +303,15 @@ __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
       }
     } else {
       float* dst = kc + ((size_t)(hh - nq) * cap + pos) * HD;
+      const size_t ko = ((size_t)(hh - nq) * kv_rows + pos) * HD;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) dst[lane + 32 * e] = v[e];
+      for (int e = 0; e < EPL; ++e) {
+        dst[lane + 32 * e] = v[e];
+        uint16_t hi, lo;
+        split_bf16(v[e], hi, lo);
+        k_hi[ko + lane + 32 * e] = hi;
+        k_lo[ko + lane + 32 * e] = lo;
+      }
     }
   }
   const float* vsrc = row + (size_t)(nq + nkv) * HD;
@@ -616,21 +631,23 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// Keys [0, n) of one layer's K and V cache as the attention's operands: K rows split
-// into bf16 hi/lo [nkv][kv_rows][HD], and V transposed and split, V^T [nkv][HD][kv_rows];
-// keys [n, next multiple of 32) are written as 0. One CTA per (32 keys, KV head).
+// One layer's K and V cache as the attention's operands: V transposed and split,
+// V^T hi/lo [nkv][HD][kv_rows], for keys [0, n) (keys [n, next multiple of 32) are
+// written as 0); and K rows split, hi/lo [nkv][kv_rows][HD], for keys [0, k_end) only
+// (the keys cached before this pass: the row kernel writes the new keys' split rows
+// itself). One CTA per (32 keys, KV head).
 template <int HD>
 __global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const float* vc, int cap,
-                                                       int n, int kv_rows, uint16_t* kh,
-                                                       uint16_t* kl, uint16_t* vth,
+                                                       int n, int k_end, int kv_rows,
+                                                       uint16_t* kh, uint16_t* kl, uint16_t* vth,
                                                        uint16_t* vtl) {
   __shared__ float tile[32][HD + 1];
   const int k0 = blockIdx.x * 32, kvh = blockIdx.y;
+  if (k0 < k_end)
   for (int i = threadIdx.x; i < 32 * HD / 2; i += 256) {
     const int kk = i / (HD / 2), d = (i % (HD / 2)) * 2;
-    float2 v = make_float2(0.f, 0.f);
-    if (k0 + kk < n)
-      v = *reinterpret_cast<const float2*>(kc + ((size_t)kvh * cap + k0 + kk) * HD + d);
+    if (k0 + kk >= k_end) continue;
+    const float2 v = *reinterpret_cast<const float2*>(kc + ((size_t)kvh * cap + k0 + kk) * HD + d);
     uint32_t hi, lo;
     split2(v.x, v.y, hi, lo);
     const size_t o = ((size_t)kvh * kv_rows + k0 + kk) * HD + d;
@@ -652,6 +669,42 @@ __global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const fl
   }
 }
 
+// int4 g128 rows as the decode step stores them (K/2 nibble bytes, then K/128 bf16
+// scales, padded) -> the exact dequantised value w = (nibble - 8) * scale as two bf16
+// terms, hi = bf16(w) and lo = bf16(w - hi), in row-major planes [rows][K]. w has at
+// most 11 significant bits (a 4-bit integer times an 8-bit bf16 significand), so
+// hi + lo == w exactly. One thread per 8 consecutive inputs.
+__global__ void __launch_bounds__(256) dequant_int4_split_kernel(const uint8_t* src, int rows,
+                                                                 int K, uint16_t* hi,
+                                                                 uint16_t* lo) {
+  const uint32_t rb = int4_row_bytes(K);
+  const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
+  const int per_row = K / 8;
+  if (i >= (long long)rows * per_row) return;
+  const int r = (int)(i / per_row), c = (int)(i % per_row) * 8;
+  const uint8_t* row = src + (size_t)r * rb;
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(row + c / 2);
+  const float sc = bf16f(*reinterpret_cast<const uint16_t*>(row + K / 2 + (c >> 7) * 2));
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float v0 = (float)((int)((w >> (8 * e)) & 15u) - 8) * sc;  // element c + 2e
+    const float v1 = (float)((int)((w >> (8 * e + 4)) & 15u) - 8) * sc;
+    split2(v0, v1, h[e], l[e]);
+  }
+  const size_t o = (size_t)r * K + c;
+  *reinterpret_cast<uint4*>(hi + o) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo + o) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+cudaError_t launch_dequant_int4_split(const uint8_t* src, int rows, int K, uint16_t* hi,
+                                      uint16_t* lo, cudaStream_t s) {
+  const long long n = (long long)rows * (K / 8);
+  if (n <= 0) return cudaSuccess;
+  dequant_int4_split_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src, rows, K, hi, lo);
+  return cudaGetLastError();
+}
+
 __global__ void set_int_kernel(int* p, int v) { *p = v; }
 
 // ------------------------------------------------------------------ launchers
@@ -669,13 +722,17 @@ cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g,
 cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
                                    const uint16_t* qn, const uint16_t* kn, float eps,
                                    const float2* rope, uint16_t* q_hi, uint16_t* q_lo,
-                                   float* kc, float* vc, int cap, cudaStream_t s) {
+                                   float* kc, float* vc, int cap, uint16_t* kv_split,
+                                   cudaStream_t s) {
+  const int kv_rows = attn_kv_rows(cap);
+  uint16_t* k_hi = kv_split;
+  uint16_t* k_lo = kv_split + (size_t)nkv * hd * kv_rows;
   if (hd == 64)
     qk_rope_kv_rows_kernel<64><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, q_hi, q_lo,
-                                                 kc, vc, cap);
+                                                 kc, vc, cap, k_hi, k_lo, kv_rows);
   else if (hd == 128)
     qk_rope_kv_rows_kernel<128><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, q_hi, q_lo,
-                                                  kc, vc, cap);
+                                                  kc, vc, cap, k_hi, k_lo, kv_rows);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -697,10 +754,10 @@ cudaError_t launch_attn_prefill(const FaMaps& maps, const float* kc, const float
   FaArgs a{p0, T, nq, nkv, kv_rows, o_hi, o_lo, err, wait_ns};
   uint16_t *kh = kv_split, *kl = kv_split + plane, *vth = kl + plane, *vtl = vth + plane;
   if (hd == 64) {
-    kv_split_kernel<64><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, kv_rows, kh, kl, vth, vtl);
+    kv_split_kernel<64><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
     attn_prefill_fa_kernel<64><<<grid, 192, FaLayout<64>::bytes, s>>>(maps, a);
   } else if (hd == 128) {
-    kv_split_kernel<128><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, kv_rows, kh, kl, vth, vtl);
+    kv_split_kernel<128><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
     attn_prefill_fa_kernel<128><<<grid, 192, FaLayout<128>::bytes, s>>>(maps, a);
   } else {
     return cudaErrorInvalidValue;
@@ -774,54 +831,61 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
 
 constexpr size_t kGemmSmemBudget = 200 * 1024;
 
-static int gemm_stages(int bn, int a_split) {
-  const size_t stage = (size_t)a_split * kATileBytes + (size_t)bn * GBK * 2;
+static int gemm_stages(int bn, int a_split, int b_split) {
+  const size_t stage = (size_t)a_split * kATileBytes + (size_t)b_split * bn * GBK * 2;
   int ns = (int)((kGemmSmemBudget - 2048) / stage);
   return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
 }
-static size_t gemm_smem(int bn, int a_split, int ns) {
-  return (size_t)ns * ((size_t)a_split * kATileBytes + (size_t)bn * GBK * 2) + 1024 + 256;
+static size_t gemm_smem(int bn, int a_split, int b_split, int ns) {
+  return (size_t)ns * ((size_t)a_split * kATileBytes + (size_t)b_split * bn * GBK * 2) + 1024 +
+         256;
 }
 
 template <int BN, int EPI>
 static cudaError_t launch_gemm_t(const CUtensorMap& a_hi, const CUtensorMap& a_lo,
-                                 const CUtensorMap& b, const GemmArgs& g, cudaStream_t s) {
+                                 const CUtensorMap& b, const CUtensorMap& b_lo, const GemmArgs& g,
+                                 cudaStream_t s) {
   const dim3 grid((g.N + BN - 1) / BN, (g.M + GBM - 1) / GBM);
-  gemm_tc_kernel<BN, EPI><<<grid, 192, gemm_smem(BN, g.a_split, g.n_stages), s>>>(a_hi, a_lo, b,
-                                                                                    g);
+  gemm_tc_kernel<BN, EPI><<<grid, 192, gemm_smem(BN, g.a_split, g.b_split, g.n_stages), s>>>(
+      a_hi, a_lo, b, b_lo, g);
   return cudaGetLastError();
 }
 
 template <int BN>
 static cudaError_t launch_gemm_bn(int epi, const CUtensorMap& a_hi, const CUtensorMap& a_lo,
-                                  const CUtensorMap& b, const GemmArgs& g, cudaStream_t s) {
+                                  const CUtensorMap& b, const CUtensorMap& b_lo,
+                                  const GemmArgs& g, cudaStream_t s) {
   switch (epi) {
-    case GEPI_STORE: return launch_gemm_t<BN, GEPI_STORE>(a_hi, a_lo, b, g, s);
-    case GEPI_RESID: return launch_gemm_t<BN, GEPI_RESID>(a_hi, a_lo, b, g, s);
-    case GEPI_SWIGLU: return launch_gemm_t<BN, GEPI_SWIGLU>(a_hi, a_lo, b, g, s);
+    case GEPI_STORE: return launch_gemm_t<BN, GEPI_STORE>(a_hi, a_lo, b, b_lo, g, s);
+    case GEPI_RESID: return launch_gemm_t<BN, GEPI_RESID>(a_hi, a_lo, b, b_lo, g, s);
+    case GEPI_SWIGLU: return launch_gemm_t<BN, GEPI_SWIGLU>(a_hi, a_lo, b, b_lo, g, s);
   }
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& a_hi, const CUtensorMap& a_lo,
-                        const CUtensorMap& b, GemmArgs g, cudaStream_t s) {
+                        const CUtensorMap& b, const CUtensorMap* b_lo, GemmArgs g,
+                        cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || (g.a_split != 1 && g.a_split != 2))
     return cudaErrorInvalidValue;
   if (epi == GEPI_SWIGLU && (g.N % 2)) return cudaErrorInvalidValue;
-  g.n_stages = gemm_stages(bn, g.a_split);
-  if (bn == 64) return launch_gemm_bn<64>(epi, a_hi, a_lo, b, g, s);
-  if (bn == 128) return launch_gemm_bn<128>(epi, a_hi, a_lo, b, g, s);
-  if (bn == 256) return launch_gemm_bn<256>(epi, a_hi, a_lo, b, g, s);
+  g.b_split = b_lo ? 2 : 1;
+  const CUtensorMap& bl = b_lo ? *b_lo : b;
+  g.n_stages = gemm_stages(bn, g.a_split, g.b_split);
+  if (bn == 64) return launch_gemm_bn<64>(epi, a_hi, a_lo, b, bl, g, s);
+  if (bn == 128) return launch_gemm_bn<128>(epi, a_hi, a_lo, b, bl, g, s);
+  if (bn == 256) return launch_gemm_bn<256>(epi, a_hi, a_lo, b, bl, g, s);
   return cudaErrorInvalidValue;
 }
 
 template <int BN>
 static cudaError_t gemm_attrs_bn() {
   int bytes = 0;
-  for (int split = 1; split <= 2; ++split) {
-    const int b = (int)gemm_smem(BN, split, gemm_stages(BN, split));
-    bytes = b > bytes ? b : bytes;
-  }
+  for (int split = 1; split <= 2; ++split)
+    for (int bsplit = 1; bsplit <= 2; ++bsplit) {
+      const int b = (int)gemm_smem(BN, split, bsplit, gemm_stages(BN, split, bsplit));
+      bytes = b > bytes ? b : bytes;
+    }
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, GEPI_STORE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)

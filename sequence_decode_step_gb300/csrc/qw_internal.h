@@ -31,8 +31,10 @@ struct ArgmaxOut {
 // y = epilogue(W . prologue(x)); W rows grouped in units of `rpu` rows.
 struct GemvArgs {
   const uint8_t* w;       // packed rows, unit u = rows [u*rpu, (u+1)*rpu)
-  int w4;                 // 0: bf16 rows (K*2 bytes); 1: int4 g128 rows = K/2 nibble bytes,
-                          //    then K/128 bf16 scales at byte `scale_off`, padded to 16 bytes
+  int wfmt;               // 0: bf16 rows (K*2 bytes); 1: int4 g128 rows = K/2 nibble bytes,
+                          //    then K/128 bf16 scales at byte `scale_off`, padded to 16 bytes;
+                          // 2: Q8_0 rows = K int8 bytes, then K/32 fp16 scales at `scale_off`,
+                          //    padded to 16 bytes
   uint32_t scale_off;
   int n_units;
   int rpu;                // rows per unit: 1, or 2 for interleaved gate/up
@@ -70,6 +72,16 @@ __host__ __device__ inline uint32_t int4_row_bytes(int K) {
 }
 cudaError_t launch_pack_int4_rows(const uint8_t* nib, const uint16_t* scales, int rows, int K,
                                   uint8_t* dst, int dst_row0, int dst_row_step, cudaStream_t s);
+__host__ __device__ inline uint32_t q8_row_bytes(int K) {
+  return (uint32_t)K + (((uint32_t)K / 32 * 2 + 15) & ~15u);
+}
+cudaError_t launch_pack_q8_rows(const int8_t* q, const uint16_t* scales, int rows, int K,
+                                uint8_t* dst, int dst_row0, int dst_row_step, cudaStream_t s);
+// Q8_0 quantiser: rows of `cols` inputs (f32, or bf16 bits when w_bf16) -> int8 rows at
+// q + r * q_stride (bytes) and fp16 scale bits at scales + r * s_stride (elements).
+cudaError_t launch_quantize_q8(const void* w, bool w_bf16, int rows, int cols, int8_t* q,
+                               size_t q_stride, uint16_t* scales, size_t s_stride,
+                               cudaStream_t s);
 
 struct AttnArgs {
   const float* qkv;        // raw [(nq + 2 nkv) * hd]
@@ -131,6 +143,8 @@ enum : int { GEPI_STORE = 0, GEPI_RESID = 1, GEPI_SWIGLU = 2 };
 struct GemmArgs {
   int M, N, K;
   int a_split;             // 1: A_hi only; 2: A_hi + A_lo (activation split in two bf16)
+  int b_split;             // filled by launch_gemm: 2 when B comes as B_hi + B_lo (a weight
+                           // that bf16 holds only as two terms: dequantised int4)
   int n_stages;            // filled by launch_gemm
   float* out;              // STORE: out[m, n] = acc (+ bias[n]); RESID: out[m, n] += acc
   int ldo;
@@ -145,8 +159,11 @@ struct GemmArgs {
 };
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_rows);
+// b_lo: the weight's lo term (nullptr for exact bf16 weights); with it each product is
+// A_hi B_hi + A_lo B_hi + A_hi B_lo.
 cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& a_hi, const CUtensorMap& a_lo,
-                        const CUtensorMap& b, GemmArgs g, cudaStream_t s);
+                        const CUtensorMap& b, const CUtensorMap* b_lo, GemmArgs g,
+                        cudaStream_t s);
 cudaError_t set_gemm_attributes();
 int* gemm_op_err_word();
 cudaError_t launch_embed_rows(const int* ids, int T, const uint16_t* table, int V, int H,
@@ -157,7 +174,8 @@ cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g,
 cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
                                    const uint16_t* qn, const uint16_t* kn, float eps,
                                    const float2* rope, uint16_t* q_hi, uint16_t* q_lo,
-                                   float* kc, float* vc, int cap, cudaStream_t s);
+                                   float* kc, float* vc, int cap, uint16_t* kv_split,
+                                   cudaStream_t s);
 // Causal prefill attention on tcgen05 (kind::f16, three MMAs per product of two-bf16
 // splits): Q rows [T][nq][hd] (scaled by 1/sqrt(hd)) as q_hi/q_lo, keys and values
 // 0 .. p0+T-1 of one layer from its f32 cache (kc, vc: [nkv][cap][hd]), split per call
@@ -185,6 +203,10 @@ cudaError_t launch_attn_prefill(const FaMaps& maps, const float* kc, const float
                                 uint16_t* kv_split, int cap, int p0, int T, int nq, int nkv,
                                 int hd, uint16_t* o_hi, uint16_t* o_lo, int* err,
                                 uint64_t wait_ns, cudaStream_t s);
+// int4 g128 packed rows (int4_row_bytes(K) each) -> exact two-bf16 planes hi, lo [rows][K]
+// (the weight operand of the int4 prefill GEMMs).
+cudaError_t launch_dequant_int4_split(const uint8_t* src, int rows, int K, uint16_t* hi,
+                                      uint16_t* lo, cudaStream_t s);
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
 cudaError_t set_prefill_attributes();
 

@@ -161,6 +161,26 @@ __device__ __forceinline__ float dot8_i4(uint32_t w, const float (&x)[8], float 
   return fmaf(p, s, acc);
 }
 
+// 8 int8 weights (two 32-bit words, element i in byte i % 4 of word i / 4, two's
+// complement) dotted with 8 floats, times the block scale. A byte is flipped to
+// b ^ 0x80 = q + 128, placed in the mantissa of 2^23 (one byte permute), and
+// subtracting 2^23 + 128 leaves q exactly.
+__device__ __forceinline__ float i8f(uint32_t v, uint32_t b) {
+  return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7540u | b)) - 8388736.0f;
+}
+__device__ __forceinline__ float dot8_i8(uint2 w, const float (&x)[8], float s, float acc) {
+  const uint32_t a = w.x ^ 0x80808080u, b = w.y ^ 0x80808080u;
+  float p = i8f(a, 0) * x[0];
+  p = fmaf(i8f(a, 1), x[1], p);
+  p = fmaf(i8f(a, 2), x[2], p);
+  p = fmaf(i8f(a, 3), x[3], p);
+  p = fmaf(i8f(b, 0), x[4], p);
+  p = fmaf(i8f(b, 1), x[5], p);
+  p = fmaf(i8f(b, 2), x[6], p);
+  p = fmaf(i8f(b, 3), x[7], p);
+  return fmaf(p, s, acc);
+}
+
 // ------------------------------------------------------------------ TMA tensor copies
 // 2-D tiled load global -> shared (box given by the tensor map), completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,

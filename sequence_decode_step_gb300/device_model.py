@@ -39,7 +39,8 @@ class DeviceModel:
     """One qw handle with its weights loaded from a dict of drawn arrays.
 
     ``weights`` maps the workload's names to uint16 bf16 bits (or float32 for
-    tensors an int4 model quantises on the device with qw_quantize_int4_g128).
+    tensors an int4 or Q8_0 model quantises on the device with qw_quantize_int4_g128 or
+    qw_quantize_q8_0).
     """
 
     def __init__(self, shape, weights: Dict[str, np.ndarray], max_ctx: int,
@@ -64,6 +65,7 @@ class DeviceModel:
         keep = []
 
         int4 = s.weight_format == "int4_g128"
+        q8 = s.weight_format == "q8_0"
         L_ = B.lib()
 
         def up(name):
@@ -72,14 +74,22 @@ class DeviceModel:
             return t.data_ptr()
 
         def up_q(name):
-            """float32 [rows, K] -> int4 g128 (packed nibbles, bf16 scales) on the device."""
+            """float32 [rows, K] -> int4 g128 (packed nibbles, bf16 scales) or Q8_0 (int8,
+            fp16 scales) on the device, with the library's quantiser."""
             w32 = _to_dev(np.ascontiguousarray(weights[name], dtype=np.float32))
             rows, K = w32.shape
-            packed = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
-            scales = torch.empty((rows, K // 128), dtype=torch.int16, device="cuda")
-            B.check("qw_quantize_int4_g128",
-                    L_.qw_quantize_int4_g128(w32.data_ptr(), rows, K, packed.data_ptr(),
-                                             scales.data_ptr(), None))
+            if q8:
+                packed = torch.empty((rows, K), dtype=torch.int8, device="cuda")
+                scales = torch.empty((rows, K // 32), dtype=torch.int16, device="cuda")
+                B.check("qw_quantize_q8_0",
+                        L_.qw_quantize_q8_0(w32.data_ptr(), rows, K, packed.data_ptr(),
+                                            scales.data_ptr(), None))
+            else:
+                packed = torch.empty((rows, K // 2), dtype=torch.uint8, device="cuda")
+                scales = torch.empty((rows, K // 128), dtype=torch.int16, device="cuda")
+                B.check("qw_quantize_int4_g128",
+                        L_.qw_quantize_int4_g128(w32.data_ptr(), rows, K, packed.data_ptr(),
+                                                 scales.data_ptr(), None))
             keep.extend([packed, scales])
             torch.cuda.synchronize()
             del w32
@@ -103,14 +113,14 @@ class DeviceModel:
         w.final_norm = up("final_norm")
         if s.tie_word_embeddings:
             w.lm_head = None
-        elif int4:
+        elif int4 or q8:
             w.lm_head, w.lm_head_scales = up_q("lm_head")
         else:
             w.lm_head = up("lm_head")
         for nm in ("attn_norm", "mlp_norm"):
             lists[nm] = per_layer(nm)
         for nm in ("q", "k", "v", "o", "gate", "up", "down"):
-            if int4:
+            if int4 or q8:
                 lists[nm], lists[nm + "_scales"] = per_layer_q(nm)
             else:
                 lists[nm] = per_layer(nm)

@@ -56,7 +56,7 @@ def test_short_config_struct_rejected(L):
 
 
 @pytest.mark.parametrize("field,value", [("head_dim", 96), ("n_kv_heads", 3), ("hidden", 0),
-                                         ("max_ctx", 0), ("hidden", 250)])
+                                         ("max_ctx", 0), ("hidden", 250), ("weight_format", 3)])
 def test_bad_config_rejected_before_cuda(L, field, value):
     cfg = B.make_config(W.TINY, 64)
     setattr(cfg, field, value)
@@ -129,3 +129,19 @@ def test_int4_gemv_arguments_checked_before_any_launch(L):
     assert L.qw_gemv_int4_g128(1, 1, 8, 384, 1, 1, 16, ws - 16, None) == B.QW_ERR_ARG  # short
     assert L.qw_gemv_int4_g128(1, 1, 8, 384, 1, 1, 8, ws, None) == B.QW_ERR_ARG       # unaligned
     assert "workspace" in B.last_error()
+
+
+def test_q8_0_arguments_checked_before_any_launch(L):
+    assert L.qw_quantize_q8_0(None, 4, 64, 1, 1, None) == B.QW_ERR_ARG
+    assert L.qw_quantize_q8_0(1, 4, 48, 1, 1, None) == B.QW_ERR_ARG          # cols % 32
+    assert L.qw_gemv_q8_0_workspace_bytes(3, 64) == 256 + 3 * (64 + 16)
+    assert L.qw_gemv_q8_0_workspace_bytes(3, 40) == 0
+    ws = L.qw_gemv_q8_0_workspace_bytes(8, 96)
+    assert L.qw_gemv_q8_0(None, 1, 8, 96, 1, 1, 16, ws, None) == B.QW_ERR_ARG
+    assert L.qw_gemv_q8_0(1, 1, 8, 96, 1, 1, 16, ws - 16, None) == B.QW_ERR_ARG   # short
+    assert L.qw_gemv_q8_0(1, 1, 8, 96, 1, 1, 8, ws, None) == B.QW_ERR_ARG         # unaligned
+    # a Q8_0 model needs hidden, q width and intermediate in multiples of 32
+    cfg = B.make_config(W.TINY.replace(weight_format="q8_0", hidden=248), 64)
+    h = C.c_void_p()
+    assert L.qw_create(C.byref(cfg), None, C.byref(h)) == B.QW_ERR_ARG
+    assert "32 for Q8_0" in B.last_error()

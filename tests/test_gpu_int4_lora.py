@@ -46,7 +46,7 @@ def _run(m, o, tok, steps, check_ids=True):
 def test_tiny_int4_decode():
     wl = W.Workload("t4", TINY_INT4, seed=5, prompt_len=8, decode_steps=16, max_ctx=64)
     d = W.draw(wl, drawn_gains=True)
-    m = DeviceModel(wl.shape, d.weights, 64, max_prefill_t=64)   # int4 prefill: sequential
+    m = DeviceModel(wl.shape, d.weights, 64, max_prefill_t=0)    # prompt as sequential steps
     o = R.build_oracle(d)
     try:
         assert B.qw_get_decode_path(m.h) == 1
@@ -67,7 +67,8 @@ def test_tiny_lora_on_then_cleared(shape):
     m = DeviceModel(shape, d.weights, 64, max_prefill_t=64)
     fresh = DeviceModel(shape, d.weights, 64, max_prefill_t=64)
     try:
-        # phase A: adapter on (prefill falls back to the sequential path)
+        # phase A: adapter on (prefill falls back to the sequential path; int4 prompts
+        # without an adapter take the batched pass)
         m.set_lora(_lora(d), 8.0)
         o = R.build_oracle(d, lora_on=True)
         am, lg = m.prefill(d.prompt, logits=True)
@@ -138,3 +139,48 @@ def test_qwen25_3b_int4_lora_4k():
     finally:
         m.close()
         fresh.close()
+
+
+def _int4_prefill_check(shape, seed, T, max_ctx, kv_layers, chunks=None):
+    """Batched int4 prefill ("Emberglass" README, Context window & prefill sizes: a
+    prompt up to maxPrefillT ids runs as one tiled int4-GEMM pass) against the oracle's
+    no-cache prefill and against the same ids as sequential steps on the GPU."""
+    wl = W.Workload("p4", shape, seed=seed, max_ctx=max_ctx)
+    d = W.draw(wl, drawn_gains=True)
+    ids = list(W.random_ids(shape.vocab, T, seed=seed + 1))
+    m = DeviceModel(shape, d.weights, max_ctx, max_prefill_t=max(chunks or [T]))
+    seq = DeviceModel(shape, d.weights, max_ctx, max_prefill_t=0)
+    o = R.build_oracle(d, cache_f64=False)
+    d.weights = {}
+    try:
+        if chunks:
+            t0 = 0
+            for n in chunks:
+                am, lg = m.prefill(ids[t0:t0 + n], logits=True)
+                t0 += n
+        else:
+            am, lg = m.prefill(ids, logits=True)
+        cp = o.prefill(ids)
+        assert violation(lg, cp["logits"]) <= 0
+        am_s, lg_s = seq.prefill(ids, logits=True)
+        assert violation(lg, lg_s) <= 0
+        if top2_margin(cp["logits"]) > MARGIN:
+            assert am == am_s == R.greedy_argmax(cp["logits"])
+        for l in kv_layers:
+            kd, vd = m.kv(l)
+            kd, vd = kd.cpu().numpy()[:, :T], vd.cpu().numpy()[:, :T]
+            assert violation(kd, o.k_cache[l][:, :T]) <= 0
+            assert violation(vd, o.v_cache[l][:, :T]) <= 0
+        assert m.pos() == T
+        _run(m, o, R.greedy_argmax(cp["logits"]), 3)
+    finally:
+        m.close()
+        seq.close()
+
+
+def test_tiny_int4_batched_prefill():
+    _int4_prefill_check(TINY_INT4, 25, 45, 64, [0, 1], chunks=[20, 25])
+
+
+def test_qwen25_3b_int4_batched_prefill_512():
+    _int4_prefill_check(W.QWEN25_3B_INT4, 26, 512, 520, [0, 17, 35])

@@ -561,3 +561,69 @@ def test_block_wiring_qk_norm_gains_rope_and_causal_mask_hand_case():
     # swapped q/k norm gains would give s0 = 2 cos1 - 8 sin1: p0 moves far
     p0_swapped = 1.0 / (1.0 + math.exp(s1 - (2 * c - 8 * s)))
     assert abs(p0_swapped - p0) > 0.01
+
+
+# ------------------------------------------------------------------ Q8_0 (block-32 int8)
+def test_q8_0_golden_hand_example():
+    vals, q_want, deq, scales = {}, {}, {}, []
+    with open(os.path.join(GOLDEN, "q8_0_block_example.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            t = line.split()
+            if t[0] == "w":
+                vals[int(t[1])] = float(t[2])
+            elif t[0] == "q":
+                q_want[int(t[1])] = int(t[2])
+            elif t[0] == "dequant":
+                deq[int(t[1])] = float(t[2])
+            elif t[0] == "scale_bits":
+                scales = [int(x, 16) for x in t[1:]]
+    w = np.zeros((1, 96), np.float32)
+    for i, x in vals.items():
+        w[0, i] = x
+    q, sb = R.q8_0_quantize(w)
+    assert list(sb[0]) == scales
+    want = np.zeros(96, np.int8)
+    for i, x in q_want.items():
+        want[i] = x
+    np.testing.assert_array_equal(q[0], want)
+    d = R.q8_0_dequantize(q, sb)
+    for i, x in deq.items():
+        assert d[0, i] == np.float32(x)
+    assert d[0, 0] == np.float32(0.9921875) and d[0, 2] == np.float32(2 / 128)
+
+
+def test_q8_0_round_trip_bounds_and_exact_dequant():
+    w = _rng(19).standard_normal((5, 256)).astype(np.float32) * 0.02
+    q, sb = R.q8_0_quantize(w)
+    d = R.q8_0_dequantize(q, sb)
+    s = sb.view(np.float16).astype(np.float64)
+    err = np.abs(w.astype(np.float64) - d).reshape(5, 8, 32)
+    # s is within an fp16 rounding of max|w|/127, so |w - w'| <= s/2 except a hair at the clamp
+    assert np.all(err <= s[:, :, None] * (0.5 + 2e-3) + 1e-12)
+    assert np.abs(q.astype(np.int32)).max() == 127          # the block maximum reaches 127
+    ratio = d.reshape(5, 8, 32) / s[:, :, None]
+    np.testing.assert_array_equal(ratio, np.rint(ratio))      # integer times the scale
+    # scaling a block by a power of two scales s and keeps q
+    q2, sb2 = R.q8_0_quantize(w * np.float32(4.0))
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(sb2.view(np.float16).astype(np.float64), 4 * s)
+
+
+def test_q8_0_model_uses_exact_dequantised_weights_and_a_q8_tied_head():
+    shape = W.TINY.replace(weight_format="q8_0")
+    d = W.draw(W.Workload("q8", shape, seed=23, max_ctx=8))
+    m = R.build_oracle(d)
+    for name in ("layers.0.q", "layers.1.down", "layers.0.gate"):
+        q, s = R.q8_0_quantize(d.weights[name])
+        np.testing.assert_array_equal(m.w[name], R.q8_0_dequantize(q, s))
+    # the gather keeps the bf16 rows; the tied head dots against Q8_0(embed)
+    E = R.widen_bf16(d.weights["embed"])
+    np.testing.assert_array_equal(m.w["embed"], E)
+    q, s = R.q8_0_quantize(E)
+    head = R.q8_0_dequantize(q, s).astype(np.float64)
+    cp = m.prefill([7, 8, 9])
+    np.testing.assert_allclose(cp["logits"], head @ cp["final_norm"][-1].astype(np.float64),
+                               rtol=1e-5, atol=1e-6)
+    assert np.abs(head - E).max() > 0                        # the head differs from the table

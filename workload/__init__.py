@@ -19,7 +19,7 @@ Draw recipe (numpy ``default_rng(seed)``, PCG64):
   k_norm, o, mlp_norm, gate, up, down; final_norm; [lm_head]; [LoRA A/B for q
   then v, per layer]); norm gains are 1.0 unless a test asks for drawn gains
   (1 + N(0, 0.1)). bf16 tensors are the float32 draw rounded to nearest-even
-  bf16. Tensors bound for int4 stay float32 (each side quantises them itself).
+  bf16. Tensors bound for int4 or Q8_0 stay float32 (each side quantises them itself).
   After the weights: the KV prefill (N(0,1) rounded to bf16, stored as f32, in
   order layer -> K then V -> kv head -> position -> dim), then token ids,
   uniform in [0, vocab).
@@ -54,7 +54,7 @@ class ModelShape:
     tie_word_embeddings: bool = True
     qk_norm: bool = True
     qkv_bias: bool = False
-    weight_format: str = "bf16"  # "bf16" or "int4_g128"
+    weight_format: str = "bf16"  # "bf16", "int4_g128" or "q8_0"
     int4_lm_head: bool = False   # untied lm_head quantised too (int4 models)
 
     @property
@@ -98,6 +98,9 @@ QWEN25_3B_INT4 = ModelShape("qwen2.5-3b-int4g128", n_layers=36, hidden=2048, n_q
                             n_kv_heads=2, head_dim=128, intermediate=11008, vocab=151936,
                             tie_word_embeddings=False, qk_norm=False, qkv_bias=True,
                             weight_format="int4_g128", int4_lm_head=True)
+# Qwen3-0.6B with Q8_0 weights ("SuperKittens PR #7" page, Q8_0 commit: decode of the
+# same model with GGUF Q8_0 projections and LM head)
+QWEN3_0_6B_Q8 = QWEN3_0_6B.replace(name="qwen3-0.6b-q8_0", weight_format="q8_0")
 
 WORKLOADS: Dict[str, Workload] = {
     "tiny": Workload("tiny", TINY, seed=0, prompt_len=8, decode_steps=16, max_ctx=64,
@@ -119,6 +122,10 @@ WORKLOADS: Dict[str, Workload] = {
                                      description="Qwen2.5-3B shape, int4 g128, q/k/v bias, untied "
                                                  "head, KV pre-filled to 4096, 64 greedy steps with "
                                                  "a rank-16 LoRA on q/v and 64 without"),
+    "qwen3_0.6b_q8_0_decode": Workload("qwen3_0.6b_q8_0_decode", QWEN3_0_6B_Q8, seed=5,
+                                       prompt_len=5, decode_steps=64, max_ctx=256,
+                                       description="Qwen3-0.6B shape with Q8_0 projections and "
+                                                   "LM head, 5-id prompt then 64 greedy steps"),
 }
 
 
@@ -148,8 +155,9 @@ def _linear_shapes(s: ModelShape) -> List[Tuple[str, Tuple[int, int]]]:
 
 def weight_draw_order(s: ModelShape, lora: Optional[LoraShape] = None,
                       drawn_gains: bool = False) -> List[Tuple[str, Tuple[int, ...], str]]:
-    """(name, shape, kind) in draw order. kind: 'bf16', 'f32q' (int4-bound float32), 'gain'."""
-    lin_kind = "f32q" if s.weight_format == "int4_g128" else "bf16"
+    """(name, shape, kind) in draw order. kind: 'bf16', 'f32q' (float32 bound for int4 or
+    Q8_0 quantisation), 'gain'."""
+    lin_kind = "f32q" if s.weight_format in ("int4_g128", "q8_0") else "bf16"
     out: List[Tuple[str, Tuple[int, ...], str]] = [("embed", (s.vocab, s.hidden), "bf16")]
     for l in range(s.n_layers):
         p = f"layers.{l}."
@@ -168,7 +176,8 @@ def weight_draw_order(s: ModelShape, lora: Optional[LoraShape] = None,
     out.append(("final_norm", (s.hidden,), "gain"))
     if not s.tie_word_embeddings:
         out.append(("lm_head", (s.vocab, s.hidden),
-                    "f32q" if (s.int4_lm_head and s.weight_format == "int4_g128") else "bf16"))
+                    "f32q" if ((s.int4_lm_head and s.weight_format == "int4_g128")
+                               or s.weight_format == "q8_0") else "bf16"))
     if lora is not None:
         r = lora.rank
         for l in range(s.n_layers):
