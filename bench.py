@@ -265,6 +265,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
     # ---- prefill of T=1024 ids (the prompt path at that length)
     pre = prefill_timing(torch, W, DeviceModel, stream) if args.prefill else None
     m.close()
+    extra = {}
+    if args.extras:  # the other workloads' lines: long context (f32 / bf16 KV), Q8_0, int4 prefill
+        extra["longctx"] = longctx_timing(torch, W, B, DeviceModel, stream)
+        extra["q8_0_decode"] = q8_timing(torch, W, B, DeviceModel, stream)
+        extra["prefill_int4"] = int4_prefill_timing(torch, W, B, DeviceModel, stream)
 
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
@@ -311,6 +316,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
         "wall_s_timed_region": wall,
         "clocks": clk.summary(),
         "prefill": pre,
+        **extra,
     }
     return res
 
@@ -447,6 +453,125 @@ def prefill_timing(torch, W, DeviceModel, stream) -> dict:
                          else "fallback 1900 TFLOP/s"}}
 
 
+def device_draw(W, torch, shape, seed: int, lora=None) -> dict:
+    """The workload's tensors (names, shapes, kinds and distributions of its draw order)
+    drawn on the device with a seeded torch generator: the timing-only runs of the large
+    shapes use this instead of the host draw, which takes minutes at 3 B parameters."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    out = {}
+    for name, shp, kind in W.weight_draw_order(shape, lora):
+        if kind == "gain":
+            out[name] = torch.full(shp, 0x3F80, dtype=torch.int16, device="cuda")
+            continue
+        std = W.LORA_STD if kind == "lora" else W.WEIGHT_STD
+        w = torch.randn(shp, generator=g, device="cuda", dtype=torch.float32) * std
+        out[name] = w if kind == "f32q" else w.to(torch.bfloat16).view(torch.int16)
+    return out
+
+
+def decode_timing(torch, B, DeviceModel, shape, weights, stream, start: int, tokens: int,
+                  max_ctx: int, kv=None) -> float:
+    """us per token of `tokens` greedy steps from position `start` (graph replays on the
+    handle's stream, CUDA events), after a warm-up pass; kv = (k, v) per layer preloaded."""
+    m = DeviceModel(shape, weights, max_ctx, stream=stream.cuda_stream)
+    try:
+        if kv is not None:
+            for l, (k, v) in enumerate(kv):
+                m.set_kv(l, k, v)
+        L = B.lib()
+        best = None
+        for rep in range(3):
+            B.qw_set_pos(m.h, start)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            rc = L.qw_decode_step(m.h, 1, None, None)
+            for _ in range(tokens - 1):
+                rc |= L.qw_decode_step(m.h, -1, None, None)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if rc:
+                raise RuntimeError(B.last_error(m.h))
+            if rep > 0:
+                us = e0.elapsed_time(e1) * 1e3 / tokens
+                best = us if best is None else min(best, us)
+        return best
+    finally:
+        m.close()
+
+
+def longctx_timing(torch, W, B, DeviceModel, stream) -> dict:
+    """Decode at 8K keys (the long-context workload) with the f32 and the bf16 KV cache:
+    32 greedy steps from position 8192, us/token and the byte roofline of each."""
+    wl = W.WORKLOADS["qwen3_0.6b_longctx"]
+    s = wl.shape
+    d = W.draw(wl)
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    out = {"workload": wl.name, "positions": f"{wl.kv_prefill}..{wl.kv_prefill + wl.decode_steps - 1}"}
+    for fmt, elem in (("f32", 4), ("bf16", 2)):
+        shape = s.replace(kv_format=fmt)
+        us = decode_timing(torch, B, DeviceModel, shape, d.weights, stream, wl.kv_prefill,
+                           wl.decode_steps, wl.max_ctx, kv=d.kv)
+        kvb = sum(kv_bytes(s, p) for p in range(wl.kv_prefill, wl.kv_prefill + wl.decode_steps))
+        byt = weight_bytes(s) + kvb * elem // 4 / wl.decode_steps
+        out[fmt] = {"us_per_token": us, "tok_per_s": 1e6 / us, "bytes_per_token": byt,
+                    "roofline_frac": byt / (us * 1e-6) / 1e9 / hbm}
+    return out
+
+
+def q8_timing(torch, W, B, DeviceModel, stream) -> dict:
+    """Q8_0 decode of the Qwen3-0.6B shape (projections and tied head in Q8_0; the
+    multi-kernel graph): us/token from position 5 and the byte roofline."""
+    wl = W.WORKLOADS["qwen3_0.6b_q8_0_decode"]
+    s = wl.shape
+    w = device_draw(W, torch, s, wl.seed)
+    us = decode_timing(torch, B, DeviceModel, s, w, stream, wl.prompt_len, wl.decode_steps,
+                       wl.max_ctx)
+    per_layer = (s.hidden * s.q_dim + 2 * s.hidden * s.kv_dim + s.q_dim * s.hidden
+                 + 3 * s.hidden * s.intermediate)
+    byt = (s.n_layers * per_layer + s.vocab * s.hidden) * (1 + 2 / 32) + \
+        sum(kv_bytes(s, p) for p in range(wl.prompt_len, wl.prompt_len + wl.decode_steps)) / wl.decode_steps
+    hbm = measured_peaks().get("hbm_gbs", 6800.0)
+    return {"workload": wl.name, "us_per_token": us, "tok_per_s": 1e6 / us,
+            "bytes_per_token": byt, "roofline_frac": byt / (us * 1e-6) / 1e9 / hbm,
+            "path": "multi-kernel graph, int8 GEMV with fp16 block scales",
+            "data": "seeded device draw (torch), the workload's shapes and distributions"}
+
+
+def int4_prefill_timing(torch, W, B, DeviceModel, stream, T: int = 1024) -> dict:
+    """Batched prefill of T ids on the Qwen2.5-3B int4 g128 shape: weights dequantised
+    layer by layer into exact two-bf16 planes, tcgen05 GEMMs with three MMAs per product."""
+    s = W.QWEN25_3B_INT4
+    w = device_draw(W, torch, s, 4)
+    m = DeviceModel(s, w, T + 8, max_prefill_t=T, stream=stream.cuda_stream)
+    del w
+    ids = list(W.random_ids(s.vocab, T, seed=4))
+    try:
+        ms = []
+        for rep in range(4):
+            m.reset()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            m.prefill(ids)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if rep > 0:
+                ms.append(e0.elapsed_time(e1))
+    finally:
+        m.close()
+    t = sum(ms) / len(ms)
+    fl = prefill_flops(s, T)
+    tc = measured_peaks().get("bf16_tflops", 1900.0)
+    return {"shape": s.name, "T": T, "ms": t, "tok_per_s": T / (t / 1e3),
+            "roofline": {"bound": "tensor", "algorithmic_tflop": fl / 1e12,
+                         "achieved": fl / (t / 1e3) / 1e12, "peak": tc, "unit": "TFLOP/s",
+                         "frac": fl / (t / 1e3) / 1e12 / tc},
+            "data": "seeded device draw (torch), the workload's shapes and distributions"}
+
+
 # ============================================================================ CPU oracle legs
 def oracle_sample(budget_s: float, min_tokens: int, max_tokens: int) -> dict:
     """Time the oracle (as it stands) decoding the benchmark workload on this host.
@@ -524,6 +649,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_base", action="store_false")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the long-context, Q8_0 and int4-prefill lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -35,7 +35,7 @@
 extern "C" {
 #endif
 
-#define QW_ABI_VERSION 1u
+#define QW_ABI_VERSION 2u
 
 /* Status codes. */
 enum {
@@ -53,6 +53,12 @@ enum {
 
 /* qw_config.weight_format */
 enum { QW_WEIGHTS_BF16 = 0, QW_WEIGHTS_INT4_G128 = 1, QW_WEIGHTS_Q8_0 = 2 };
+
+/* qw_config.kv_format: how keys (after QK-norm and RoPE) and values are stored. bf16
+ * halves the cache ("Emberglass" README, Context window & prefill sizes: the f32
+ * cache could be quantised to roughly half); each value is rounded to the nearest
+ * bf16 when stored, and attention reads the stored values, widened to f32. */
+enum { QW_KV_F32 = 0, QW_KV_BF16 = 1 };
 
 /* qw_get_capture `which`: the four checkpoints of the "Failed Star / fs, M2"
  * page ("Four boundaries bisect the whole model"). */
@@ -88,6 +94,7 @@ typedef struct qw_config {
   int32_t max_ctx;              /* KV-cache capacity in positions */
   int32_t max_prefill_t;        /* longest prompt taken by one batched prefill pass */
   uint32_t weight_format;       /* QW_WEIGHTS_BF16, QW_WEIGHTS_INT4_G128 or QW_WEIGHTS_Q8_0 */
+  uint32_t kv_format;           /* QW_KV_F32 or QW_KV_BF16 */
 } qw_config;
 
 /* Weights, all DEVICE pointers owned by the caller; the per-layer members are
@@ -163,7 +170,8 @@ size_t qw_sizeof_lora(void);
 /* Create a handle on the current CUDA device. cuda_stream is a cudaStream_t
  * the handle will use (borrowed), or NULL for a stream the handle creates and
  * owns. Allocates the KV cache (2 * n_layers * n_kv_heads * max_ctx * head_dim
- * floats) and work buffers. *out is set only on success. */
+ * elements of 4 bytes, or 2 with QW_KV_BF16) and work buffers. *out is set only
+ * on success. */
 int qw_create(const qw_config* cfg, void* cuda_stream, qw_handle** out);
 
 /* Copy and repack the weights into library memory (fused [q;k;v] rows,
@@ -206,11 +214,11 @@ int qw_reset(qw_handle* h);
  * clearing restores bit-identical outputs. */
 int qw_set_lora(qw_handle* h, const qw_lora* lora);
 
-/* Test hooks. qw_kv_cache returns DEVICE pointers to layer `layer`'s f32 K and
- * V cache, each [n_kv_heads, max_ctx, head_dim] (keys stored after QK-norm and
- * RoPE), owned by the handle. qw_set_pos / qw_get_pos move or read the
- * position (0 <= pos <= max_ctx). */
-int qw_kv_cache(qw_handle* h, int32_t layer, float** k_dev, float** v_dev);
+/* Test hooks. qw_kv_cache returns DEVICE pointers to layer `layer`'s K and V
+ * cache, each [n_kv_heads, max_ctx, head_dim] (keys stored after QK-norm and
+ * RoPE) of f32, or of bf16 bits with QW_KV_BF16, owned by the handle.
+ * qw_set_pos / qw_get_pos move or read the position (0 <= pos <= max_ctx). */
+int qw_kv_cache(qw_handle* h, int32_t layer, void** k_dev, void** v_dev);
 int qw_set_pos(qw_handle* h, int32_t pos);
 int qw_get_pos(const qw_handle* h, int32_t* pos);
 

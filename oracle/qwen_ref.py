@@ -39,6 +39,8 @@ Readings of points the pages leave open (each listed in the design notes):
   * LoRA on q_proj and v_proj: y = W x + b + (alpha / rank) * B (A x).
   * int4 g128: see ``int4_quantize``; Q8_0: see ``q8_0_quantize``.
   * Greedy argmax: ties go to the lowest index; a NaN logit is an error.
+  * bf16 KV cache (option): keys (after QK-norm and RoPE) and values are rounded
+    to the nearest bf16 when stored, and attention reads the stored values.
 """
 from __future__ import annotations
 
@@ -58,6 +60,17 @@ def widen_bf16(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> float32. Exact: a bf16 is the top half of an f32
     ("Failed Star / fs, M2", Correct before fast: BF16 weights widen once)."""
     return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(F32)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bf16 (ties to even), returned as float32.
+
+    Used for the bf16 KV cache ("Emberglass" README, Context window & prefill sizes:
+    the f32 cache could be quantised to roughly half its size): keys and values are
+    stored, and read back, at bf16 precision. Finite inputs only."""
+    u = np.ascontiguousarray(x, dtype=F32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(F32)
 
 
 # ----------------------------------------------------------------------------- basic ops
@@ -306,6 +319,7 @@ class Config:
     qkv_bias: bool = False
     weight_format: str = "bf16"
     int4_lm_head: bool = False
+    kv_format: str = "f32"       # "f32" or "bf16": precision of the stored keys and values
 
     @property
     def q_dim(self) -> int:
@@ -452,7 +466,10 @@ class OracleModel:
             q = rmsnorm(q, self._gain(f"layers.{l}.q_norm"), c.eps)
             k = rmsnorm(k, self._gain(f"layers.{l}.k_norm"), c.eps)
         cos, sin = rope_cos_sin(positions, c.head_dim, c.rope_theta)
-        return apply_rope(q, cos, sin), apply_rope(k, cos, sin), v
+        k, v = apply_rope(k, cos, sin), v
+        if c.kv_format == "bf16":          # what the cache stores is what attention reads
+            k, v = round_bf16(k), round_bf16(v)
+        return apply_rope(q, cos, sin), k, v
 
     def _mlp(self, l: int, x: np.ndarray) -> np.ndarray:
         p = f"layers.{l}."

@@ -14,7 +14,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqw.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "qw.h")
 
-QW_ABI_VERSION = 1
+QW_ABI_VERSION = 2
 QW_OK = 0
 QW_ERR_ABI = -1
 QW_ERR_ARG = -2
@@ -28,6 +28,8 @@ QW_ERR_NUMERIC = -9
 QW_WEIGHTS_BF16 = 0
 QW_WEIGHTS_INT4_G128 = 1
 QW_WEIGHTS_Q8_0 = 2
+QW_KV_F32 = 0
+QW_KV_BF16 = 1
 QW_CAPTURE_EMBEDDING = 0
 QW_CAPTURE_BLOCK0 = 1
 QW_CAPTURE_FINAL_NORM = 2
@@ -52,7 +54,7 @@ class qw_config(C.Structure):
                 ("vocab", C.c_int32), ("eps", C.c_float), ("rope_theta", C.c_float),
                 ("tie_word_embeddings", C.c_uint32), ("qk_norm", C.c_uint32),
                 ("qkv_bias", C.c_uint32), ("max_ctx", C.c_int32), ("max_prefill_t", C.c_int32),
-                ("weight_format", C.c_uint32)]
+                ("weight_format", C.c_uint32), ("kv_format", C.c_uint32)]
 
 
 _WEIGHT_LISTS = ["attn_norm", "q", "k", "v", "o", "mlp_norm", "gate", "up", "down", "q_norm",
@@ -184,7 +186,8 @@ def make_config(shape, max_ctx: int, max_prefill_t: int = 0) -> qw_config:
         tie_word_embeddings=int(shape.tie_word_embeddings), qk_norm=int(shape.qk_norm),
         qkv_bias=int(shape.qkv_bias), max_ctx=max_ctx, max_prefill_t=max_prefill_t,
         weight_format={"int4_g128": QW_WEIGHTS_INT4_G128,
-                       "q8_0": QW_WEIGHTS_Q8_0}.get(shape.weight_format, QW_WEIGHTS_BF16))
+                       "q8_0": QW_WEIGHTS_Q8_0}.get(shape.weight_format, QW_WEIGHTS_BF16),
+        kv_format=QW_KV_BF16 if getattr(shape, "kv_format", "f32") == "bf16" else QW_KV_F32)
 
 
 # -- thin wrappers with the C names (raise QwError on a non-zero status) --------

@@ -386,9 +386,11 @@ __device__ __forceinline__ void rope_cs(const float2* row, int pos, int j, int h
   }
 }
 
-template <int HD>
+template <int HD, bool KB>
 __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
   constexpr int TK = kAttnTK, NS = kAttnNS, GQM = kAttnGQ, EPL = HD / 32;
+  using KV = KvElem<KB>;
+  using KT = typename KV::T;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* q_s = reinterpret_cast<float*>(smem + 64);  // [GQM][HD]
@@ -399,7 +401,8 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
   float* ml_s = p_s + GQM * TK;                       // [GQM][2]
   float* al_s = ml_s + 2 * GQM;                       // [GQM]
   int* flag_s = reinterpret_cast<int*>(al_s + GQM);
-  float* stage0 = reinterpret_cast<float*>(smem + attn_stage_off<HD>());
+  uint8_t* stage_base = smem + attn_stage_off<HD>();
+  float* stage0 = reinterpret_cast<float*>(stage_base);  // the combine reuses the stages as f32
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y, s = blockIdx.x;
@@ -416,8 +419,8 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
   const int k1 = min(n_keys, k0 + kps);
   const int ntiles = (k1 - k0 + TK - 1) / TK;
   const bool owns_pos = pos >= k0 && pos < k1;
-  float* kc = a.k_cache + (size_t)g * a.cap * HD;
-  float* vc = a.v_cache + (size_t)g * a.cap * HD;
+  KT* kc = reinterpret_cast<KT*>(a.k_cache) + (size_t)g * a.cap * HD;
+  KT* vc = reinterpret_cast<KT*>(a.v_cache) + (size_t)g * a.cap * HD;
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
@@ -425,8 +428,8 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
     const int pre = ntiles < NS ? ntiles : NS;
     for (int i = 0; i < pre; ++i) {
       const int t0 = k0 + i * TK, nk = min(TK, k1 - t0);
-      const uint32_t bytes = (uint32_t)nk * HD * 4;
-      float* dK = stage0 + (size_t)i * 2 * TK * HD;
+      const uint32_t bytes = (uint32_t)(nk * HD * sizeof(KT));
+      KT* dK = reinterpret_cast<KT*>(stage_base) + (size_t)i * 2 * TK * HD;
       mbar_expect_tx(&bars[i], 2 * bytes);
       bulk_load(dK, kc + (size_t)t0 * HD, bytes, &bars[i]);
       bulk_load(dK + TK * HD, vc + (size_t)t0 * HD, bytes, &bars[i]);
@@ -472,13 +475,13 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
     } else {
       const float* vsrc = a.qkv + (size_t)(a.nq + a.nkv + g) * HD;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) {
+      for (int e = 0; e < EPL; ++e) {  // the stored (for bf16: rounded) values are used
         const int d = lane + 32 * e;
-        kn_s[d] = v[e];
-        kc[(size_t)pos * HD + d] = v[e];
-        const float vv = __ldcg(vsrc + d);
-        vn_s[d] = vv;
-        vc[(size_t)pos * HD + d] = vv;
+        const KT ks = KV::store(v[e]), vs = KV::store(__ldcg(vsrc + d));
+        kn_s[d] = KV::load(&ks);
+        kc[(size_t)pos * HD + d] = ks;
+        vn_s[d] = KV::load(&vs);
+        vc[(size_t)pos * HD + d] = vs;
       }
     }
   }
@@ -506,12 +509,12 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
       break;
     }
     const int t0 = k0 + it * TK, nk = min(TK, k1 - t0);
-    float* Ks = stage0 + (size_t)st * 2 * TK * HD;
-    float* Vs = Ks + TK * HD;
+    KT* Ks = reinterpret_cast<KT*>(stage_base) + (size_t)st * 2 * TK * HD;
+    KT* Vs = Ks + TK * HD;
     if (owns_pos && pos >= t0 && pos < t0 + nk) {
       for (int e = tid; e < HD; e += 256) {
-        Ks[(pos - t0) * HD + e] = kn_s[e];
-        Vs[(pos - t0) * HD + e] = vn_s[e];
+        Ks[(pos - t0) * HD + e] = KV::store(kn_s[e]);
+        Vs[(pos - t0) * HD + e] = KV::store(vn_s[e]);
       }
       // order these generic writes before a later bulk copy into the same stage
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -524,8 +527,14 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
       for (int k = 0; k < 4; ++k) {
         const int j = warp * 4 + k;
         float kv[EPL];
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) kv[e] = j < nk ? Ks[j * HD + lane * EPL + e] : 0.f;
+        if constexpr (EPL == 4) {
+          const float4 k4 = j < nk ? KV::load4(Ks + j * HD + lane * EPL)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          kv[0] = k4.x; kv[1] = k4.y; kv[2 % EPL] = k4.z; kv[3 % EPL] = k4.w;
+        } else {
+          const float2 k2 = j < nk ? KV::load2(Ks + j * HD + lane * EPL) : make_float2(0.f, 0.f);
+          kv[0] = k2.x; kv[1 % EPL] = k2.y;
+        }
 #pragma unroll
         for (int h = 0; h < GQM; ++h) {
           float p = 0.f;
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
         const float* pr = p_s + h * TK;
         for (int j = 0; j < nk; ++j) {
           const float pj = pr[j];
-          const float4 v4 = *reinterpret_cast<const float4*>(Vs + j * HD + d4);
+          const float4 v4 = KV::load4(Vs + j * HD + d4);
           acc.x = fmaf(pj, v4.x, acc.x);
           acc.y = fmaf(pj, v4.y, acc.y);
           acc.z = fmaf(pj, v4.z, acc.z);
@@ -579,7 +588,7 @@ __global__ void __launch_bounds__(256, 1) attn_decode_kernel(const AttnArgs a) {
     if (tid == 0 && it + NS < ntiles) {
       const int nx = it + NS;
       const int t1 = k0 + nx * TK, nk1 = min(TK, k1 - t1);
-      const uint32_t bytes = (uint32_t)nk1 * HD * 4;
+      const uint32_t bytes = (uint32_t)(nk1 * HD * sizeof(KT));
       mbar_expect_tx(&bars[st], 2 * bytes);
       bulk_load(Ks, kc + (size_t)t1 * HD, bytes, &bars[st]);
       bulk_load(Vs, vc + (size_t)t1 * HD, bytes, &bars[st]);
@@ -692,9 +701,14 @@ int attention_gq_max() { return kAttnGQ; }
 cudaError_t launch_attention(const AttnArgs& a, int hd, bool pdl, cudaStream_t s) {
   const dim3 grid(a.nsplit_max, a.nkv);
   if (hd == 64)
-    return launch_ex(attn_decode_kernel<64>, grid, dim3(256), attn_smem<64>(), s, pdl, a);
+    return a.kv_bf16
+               ? launch_ex(attn_decode_kernel<64, true>, grid, dim3(256), attn_smem<64>(), s, pdl, a)
+               : launch_ex(attn_decode_kernel<64, false>, grid, dim3(256), attn_smem<64>(), s, pdl, a);
   if (hd == 128)
-    return launch_ex(attn_decode_kernel<128>, grid, dim3(256), attn_smem<128>(), s, pdl, a);
+    return a.kv_bf16 ? launch_ex(attn_decode_kernel<128, true>, grid, dim3(256), attn_smem<128>(),
+                                 s, pdl, a)
+                     : launch_ex(attn_decode_kernel<128, false>, grid, dim3(256),
+                                 attn_smem<128>(), s, pdl, a);
   return cudaErrorInvalidValue;
 }
 
@@ -907,8 +921,10 @@ cudaError_t set_kernel_attributes() {
   QW_ALLOW_GEMV(EPI_SWIGLU);
   QW_ALLOW_GEMV(EPI_LOGITS);
 #undef QW_ALLOW_GEMV
-  QW_ALLOW(attn_decode_kernel<64>, attn_smem<64>());
-  QW_ALLOW(attn_decode_kernel<128>, attn_smem<128>());
+  QW_ALLOW((attn_decode_kernel<64, false>), attn_smem<64>());
+  QW_ALLOW((attn_decode_kernel<128, false>), attn_smem<128>());
+  QW_ALLOW((attn_decode_kernel<64, true>), attn_smem<64>());
+  QW_ALLOW((attn_decode_kernel<128, true>), attn_smem<128>());
   QW_ALLOW(embed_kernel, 0);
 #undef QW_ALLOW
   return e;

@@ -639,11 +639,13 @@ __device__ __forceinline__ int slice_chunks(const Slice& sl) { return sl.n_chunk
 // softmax, then a partial (or the final output when there is one split); split
 // 0 of a KV head polls the other splits' partials and combines them in split
 // order.
-template <int HD>
+template <int HD, bool KB>
 __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l,
                                            int pos, const Split& sp, const LayerDev& Ld,
                                            uint32_t tag_in, uint32_t tag_out, bool& abort) {
   constexpr int EPL = HD / 32, OUTS = (kGQ * HD + kNT - 1) / kNT;
+  using KV = KvElem<KB>;  // cache element: f32, or bf16 (values rounded when stored)
+  using KT = typename KV::T;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // GQ: query heads handled here; HB: global index of the first of them
   const int GQ = sp.nh, g = sp.g, HB = g * (a.nq / a.nkv) + sp.h0;
@@ -657,8 +659,8 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       ring_wait(a, &S.full[(c + t) % kNS], (uint32_t)(((c + t) / kNS) & 1), abort);
   }
   const size_t kv_layer = (size_t)a.nkv * a.cap * HD;
-  float* kc = a.k_cache + (size_t)l * kv_layer + (size_t)g * a.cap * HD;
-  float* vc = a.v_cache + (size_t)l * kv_layer + (size_t)g * a.cap * HD;
+  KT* kc = reinterpret_cast<KT*>(a.k_cache) + (size_t)l * kv_layer + (size_t)g * a.cap * HD;
+  KT* vc = reinterpret_cast<KT*>(a.v_cache) + (size_t)l * kv_layer + (size_t)g * a.cap * HD;
   const bool owns_pos = pos >= sp.k0 && pos < sp.k1;
   const float scale = 1.0f / sqrtf((float)HD);
   const float2* rrow = a.rope + (size_t)pos * (HD / 2);
@@ -703,13 +705,14 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int e = 0; e < EPL; ++e) S.q_s[hh * HD + lane + 32 * e] = v[e] * scale;
     } else {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) {
+      for (int e = 0; e < EPL; ++e) {  // the stored (for bf16: rounded) row is what is used
         const int d = lane + 32 * e;
-        S.kn_s[d] = v[e];
-        S.vn_s[d] = vv[e];
+        const KT ks = KV::store(v[e]), vs = KV::store(vv[e]);
+        S.kn_s[d] = KV::load(&ks);
+        S.vn_s[d] = KV::load(&vs);
         if (sp.h0 == 0) {  // one CTA of the group appends the row
-          kc[(size_t)pos * HD + d] = v[e];
-          vc[(size_t)pos * HD + d] = vv[e];
+          kc[(size_t)pos * HD + d] = ks;
+          vc[(size_t)pos * HD + d] = vs;
         }
       }
     }
@@ -741,13 +744,13 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int t = 0; t < nt; ++t)
         ring_wait(a, &S.full[(c + t) % kNS], (uint32_t)(((c + t) / kNS) & 1), abort);
     abort = csync_or(abort);
-    auto kt = [&](int t) { return reinterpret_cast<float*>(ring + (size_t)((c + t) % kNS) * kStage); };
+    auto kt = [&](int t) { return reinterpret_cast<KT*>(ring + (size_t)((c + t) % kNS) * kStage); };
     if (!abort) {
       if (owns_pos && pos >= p0 && pos < p0 + nkp) {
-        float* Kp = kt((pos - p0) / kTK) + ((pos - p0) % kTK) * HD;
+        KT* Kp = kt((pos - p0) / kTK) + ((pos - p0) % kTK) * HD;
         for (int e = tid; e < HD; e += kNT) {
-          Kp[e] = S.kn_s[e];
-          Kp[kTK * HD + e] = S.vn_s[e];
+          Kp[e] = KV::store(S.kn_s[e]);
+          Kp[kTK * HD + e] = KV::store(S.vn_s[e]);
         }
         // these generic writes into a ring stage must be ordered before the
         // producer's next bulk copy into the same stage (async proxy)
@@ -760,7 +763,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       constexpr int GPT = kTK / 8;  // 8-key groups per tile
       for (int gi = warp; gi < nt * GPT; gi += kConsumers) {
         const int t = gi / GPT, j0 = (gi % GPT) * 8;
-        const float* Kt = kt(t) + lane * DPL;
+        const KT* Kt = kt(t) + lane * DPL;
         const int nk = min(kTK, nkp - t * kTK);
         for (int h0 = 0; h0 < GQ; h0 += 2) {
           const bool two = h0 + 1 < GQ;
@@ -783,10 +786,10 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
             for (int j = 0; j < 8; ++j) {
               float kv[DPL];
               if constexpr (DPL == 4) {
-                const float4 k4 = *reinterpret_cast<const float4*>(Kt + (j0 + j) * HD);
+                const float4 k4 = KV::load4(Kt + (j0 + j) * HD);
                 kv[0] = k4.x; kv[1] = k4.y; kv[2 % DPL] = k4.z; kv[3 % DPL] = k4.w;
               } else {
-                const float2 k2 = *reinterpret_cast<const float2*>(Kt + (j0 + j) * HD);
+                const float2 k2 = KV::load2(Kt + (j0 + j) * HD);
                 kv[0] = k2.x; kv[1] = k2.y;
               }
               float a0 = 0.f, a1 = 0.f;
@@ -845,7 +848,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int i = warp; i < nt * KP; i += kConsumers) {
         const int t = i >> kpl, ja = (i & (KP - 1)) * (kTK >> kpl);
         const int jb = min(min(kTK, nkp - t * kTK), ja + (kTK >> kpl));
-        const float* Vt = kt(t) + kTK * HD + lane * DPL;
+        const KT* Vt = kt(t) + kTK * HD + lane * DPL;
         for (int h0 = 0; h0 < GQ; h0 += 2) {
           const bool two = h0 + 1 < GQ;
           const float* p0r = pp + h0 * stride + t * kTK;
@@ -856,10 +859,10 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
           for (int j = ja; j < jb; ++j) {
             float vv[DPL];
             if constexpr (DPL == 4) {
-              const float4 v4 = *reinterpret_cast<const float4*>(Vt + j * HD);
+              const float4 v4 = KV::load4(Vt + j * HD);
               vv[0] = v4.x; vv[1] = v4.y; vv[2 % DPL] = v4.z; vv[3 % DPL] = v4.w;
             } else {
-              const float2 v2 = *reinterpret_cast<const float2*>(Vt + j * HD);
+              const float2 v2 = KV::load2(Vt + j * HD);
               vv[0] = v2.x; vv[1] = v2.y;
             }
             const float pa = p0r[j], pb = p1r[j];
@@ -1030,11 +1033,14 @@ __device__ void produce(const MegaArgs& a, uint8_t* ring, Smem& S, int pos) {
   for (int l = 0; l < a.L && ok; ++l) {
     const LayerDev Ld = a.layers[l];
     ok = stream_slice(layer_slice(K_QKV, Ld));
-    const float* kc = a.k_cache + (size_t)l * kv_layer + (size_t)sp.g * a.cap * a.hd;
-    const float* vc = a.v_cache + (size_t)l * kv_layer + (size_t)sp.g * a.cap * a.hd;
+    const uint32_t eb = a.kv_bf16 ? 2u : 4u;  // bytes per cache element
+    const size_t row0 = (size_t)l * kv_layer + (size_t)sp.g * a.cap * a.hd;
+    const uint8_t* kc = reinterpret_cast<const uint8_t*>(a.k_cache) + row0 * eb;
+    const uint8_t* vc = reinterpret_cast<const uint8_t*>(a.v_cache) + row0 * eb;
     for (int t0 = sp.k0; ok && t0 < sp.k1; t0 += kTK) {
-      const uint32_t n = (uint32_t)min(kTK, sp.k1 - t0) * a.hd * 4;
-      ok = issue(kc + (size_t)t0 * a.hd, n, vc + (size_t)t0 * a.hd, n, (uint32_t)kTK * a.hd * 4);
+      const uint32_t n = (uint32_t)min(kTK, sp.k1 - t0) * a.hd * eb;
+      ok = issue(kc + (size_t)t0 * a.hd * eb, n, vc + (size_t)t0 * a.hd * eb, n,
+                 (uint32_t)kTK * a.hd * eb);
     }
     ok = ok && stream_slice(layer_slice(K_O, Ld));
     ok = ok && stream_slice(layer_slice(K_GU, Ld));
@@ -1115,7 +1121,7 @@ __device__ void argmax_finalize(const MegaArgs& a, Smem& S, const Best& o, int p
 // the hidden, q and intermediate inputs (see gemv). Only the variants a shape
 // needs are compiled into its kernel: the token loop's code is large and every
 // unused variant inlined into it costs instruction-cache misses.
-template <int HD, int XH, int XQ, int XI>
+template <int HD, int XH, int XQ, int XI, bool KB>
 __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint32_t epoch) {
   const int b = blockIdx.x, G = gridDim.x, tid = threadIdx.x;
   const int qd = a.nq * a.hd;
@@ -1151,8 +1157,8 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
-      if (HD == 64 || (HD == 0 && a.hd == 64)) attn_phase<64>(a, ring, S, c, l, pos, sp, Ld, tq, ta, abort);
-      else attn_phase<128>(a, ring, S, c, l, pos, sp, Ld, tq, ta, abort);
+      if (HD == 64 || (HD == 0 && a.hd == 64)) attn_phase<64, KB>(a, ring, S, c, l, pos, sp, Ld, tq, ta, abort);
+      else attn_phase<128, KB>(a, ring, S, c, l, pos, sp, Ld, tq, ta, abort);
     }
     // o_proj + residual
     if (os.u1 > os.u0) {
@@ -1199,7 +1205,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
   argmax_finalize(a, S, best, pos, epoch);
 }
 
-template <int HD, int XH, int XQ, int XI>
+template <int HD, int XH, int XQ, int XI, bool KB>
 __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -1215,7 +1221,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs
   // The position changes only at the end of a token, so every thread reads it once.
   const int pos = __ldcg(a.pos);
   const uint32_t epoch = __ldcg(a.epoch);
-  if (threadIdx.x < kConsumers * 32) consume<HD, XH, XQ, XI>(a, ring, S, pos, epoch);
+  if (threadIdx.x < kConsumers * 32) consume<HD, XH, XQ, XI, KB>(a, ring, S, pos, epoch);
   else if (threadIdx.x == kConsumers * 32) produce(a, ring, S, pos);
 }
 
@@ -1236,17 +1242,23 @@ size_t mega_smem_bytes() { return (size_t)kNS * kStage + sizeof(Smem); }
 
 // The kernel for a shape: the Qwen3-0.6B class (head dim 128, hidden <= 1024, q
 // and intermediate wider) gets its own instantiation; other shapes the generic one.
+static const void* const kMegaFns[4] = {
+    reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, false>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, false>),
+    reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, true>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, true>)};
+
 static const void* mega_kernel_for(const MegaArgs& a) {
-  if (a.hd == 128 && a.H <= 1024 && a.nq * a.hd > 1024 && a.I > 1024)
-    return reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0>);
-  return reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2>);
+  const int kv = a.kv_bf16 ? 2 : 0;
+  if (a.hd == 128 && a.H <= 1024 && a.nq * a.hd > 1024 && a.I > 1024) return kMegaFns[kv];
+  return kMegaFns[kv + 1];
 }
 
 cudaError_t set_mega_attributes() {
-  const void* fns[2] = {reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0>),
-                        reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2>)};
+  const void* const* fns = kMegaFns;
   cudaError_t e = cudaSuccess;
-  for (const void* f : fns) {
+  for (int i = 0; i < 4; ++i) {
+    const void* f = fns[i];
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)mega_smem_bytes());
@@ -1258,8 +1270,9 @@ cudaError_t set_mega_attributes() {
 }
 
 bool is_mega_kernel(const void* fn) {
-  return fn == reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0>) ||
-         fn == reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2>);
+  for (int i = 0; i < 4; ++i)
+    if (fn == kMegaFns[i]) return true;
+  return false;
 }
 
 cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s) {

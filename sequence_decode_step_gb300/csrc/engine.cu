@@ -91,8 +91,10 @@ struct qw_handle {
   bool weights_loaded = false;
   // state buffers (one device allocation)
   uint8_t* sarena = nullptr;
-  float* k_cache = nullptr;  // [L][nkv][cap][hd]
-  float* v_cache = nullptr;
+  uint8_t* k_cache = nullptr;  // [L][nkv][cap][hd] elements of kv_elem bytes (f32 or bf16)
+  uint8_t* v_cache = nullptr;
+  bool kv_bf16 = false;
+  size_t kv_elem = 4;
   float* x = nullptr;
   float* qkv = nullptr;
   float* attn_o = nullptr;
@@ -128,6 +130,7 @@ struct qw_handle {
   uint16_t* pf_m_hi = nullptr;   // [Tmax, I] SwiGLU output split
   uint16_t* pf_m_lo = nullptr;
   uint16_t* pf_kvs = nullptr;    // K and V^T of the context as two-bf16 splits (attention)
+  void* pf_attn_part = nullptr;  // partial attention outputs of query blocks cut into chunks
   CUtensorMap tm_xn_hi, tm_xn_lo, tm_o_hi, tm_o_lo, tm_m_hi, tm_m_lo;
   FaMaps tm_attn;  // attention operands: Q, K and V^T splits
   std::vector<CUtensorMap> tm_qkv, tm_ow, tm_gu, tm_dw;  // per layer, weight side
@@ -232,6 +235,10 @@ static int validate_config(const qw_config* c, std::string& why) {
     why = "weight_format must be QW_WEIGHTS_BF16, QW_WEIGHTS_INT4_G128 or QW_WEIGHTS_Q8_0";
     return QW_ERR_ARG;
   }
+  if (c->kv_format != QW_KV_F32 && c->kv_format != QW_KV_BF16) {
+    why = "kv_format must be QW_KV_F32 or QW_KV_BF16";
+    return QW_ERR_ARG;
+  }
   if (c->max_ctx <= 0 || c->max_prefill_t < 0) {
     why = "max_ctx must be positive and max_prefill_t non-negative";
     return QW_ERR_ARG;
@@ -274,7 +281,9 @@ static int alloc_state(qw_handle* h) {
   h->lm_fmt = h->wfmt == 2 ? 2 : (h->wfmt == 1 && !c.tie_word_embeddings ? 1 : 0);
   h->lm_grid = std::min({c.vocab, h->num_sms, 1024});
   struct Piece { void** p; size_t bytes; };
-  const size_t kv_bytes = L * nkv * cap * hd * 4;
+  h->kv_bf16 = c.kv_format == QW_KV_BF16;
+  h->kv_elem = h->kv_bf16 ? 2 : 4;
+  const size_t kv_bytes = L * nkv * cap * hd * h->kv_elem;
   std::vector<Piece> pieces = {
       {(void**)&h->k_cache, kv_bytes},
       {(void**)&h->v_cache, kv_bytes},
@@ -321,6 +330,8 @@ static int alloc_state(qw_handle* h) {
     pieces.push_back({(void**)&h->pf_m_hi, Tm * I * 2});
     pieces.push_back({(void**)&h->pf_m_lo, Tm * I * 2});
     pieces.push_back({(void**)&h->pf_kvs, attn_kv_bytes(c.n_kv_heads, c.head_dim, c.max_ctx)});
+    pieces.push_back({(void**)&h->pf_attn_part,
+                      attn_part_bytes(c.n_q_heads, (int)Tm, c.max_ctx, c.head_dim)});
     if (h->wfmt == 1)  // the hi and lo planes of one layer's four weight matrices
       pieces.push_back({(void**)&h->pf_w4,
                         2 * 2 * (qkv_rows * H + H * qd + 2 * I * H + H * I)});
@@ -698,6 +709,7 @@ static MegaArgs mega_args(qw_handle* h) {
   m.layers = h->d_layers;
   m.k_cache = h->k_cache;
   m.v_cache = h->v_cache;
+  m.kv_bf16 = h->kv_bf16 ? 1 : 0;
   m.cap = c.max_ctx;
   m.rope = h->rope;
   m.x = h->mx;
@@ -792,8 +804,9 @@ static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
       t.k_norm = lw.k_norm;
       t.rope = h->rope;
       t.rope_theta = c.rope_theta;
-      t.k_cache = h->k_cache + (size_t)l * kv_layer;
-      t.v_cache = h->v_cache + (size_t)l * kv_layer;
+      t.k_cache = h->k_cache + (size_t)l * kv_layer * h->kv_elem;
+      t.v_cache = h->v_cache + (size_t)l * kv_layer * h->kv_elem;
+      t.kv_bf16 = h->kv_bf16 ? 1 : 0;
       t.cap = c.max_ctx;
       t.pos_ptr = h->d_pos;
       t.nq = c.n_q_heads;
@@ -1082,8 +1095,8 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
   };
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerW& lw = h->layers[l];
-    float* kc = h->k_cache + (size_t)l * kv_layer;
-    float* vc = h->v_cache + (size_t)l * kv_layer;
+    uint8_t* kc = h->k_cache + (size_t)l * kv_layer * h->kv_elem;
+    uint8_t* vc = h->v_cache + (size_t)l * kv_layer * h->kv_elem;
     if (w4) {  // this layer's int4 rows as exact two-bf16 planes
       QW_CUDA(h, launch_dequant_int4_split((const uint8_t*)lw.qkv, qkv_rows, H, h->w4_qkv[0],
                                            h->w4_qkv[1], s));
@@ -1103,8 +1116,9 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
                     qkv_rows, H, h->pf_qkv, lw.qkv_bias, nullptr, nullptr, nullptr));
     QW_CUDA(h, launch_qk_rope_kv_rows(h->pf_qkv, T, p0, c.n_q_heads, c.n_kv_heads, hd, lw.q_norm,
                                       lw.k_norm, c.eps, h->rope, h->pf_q_hi, h->pf_q_lo, kc, vc,
-                                      c.max_ctx, h->pf_kvs, s));
-    QW_CUDA(h, launch_attn_prefill(h->tm_attn, kc, vc, h->pf_kvs, c.max_ctx, p0, T, c.n_q_heads,
+                                      h->kv_bf16, c.max_ctx, h->pf_kvs, s));
+    QW_CUDA(h, launch_attn_prefill(h->tm_attn, kc, vc, h->kv_bf16, h->pf_kvs, h->pf_attn_part,
+                                   c.max_prefill_t, c.max_ctx, p0, T, c.n_q_heads,
                                    c.n_kv_heads, hd, h->pf_o_hi, h->pf_o_lo, h->d_err, h->wait_ns,
                                    s));
     QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, wo, w4 ? &h->tm_ow4[1] : nullptr, H,
@@ -1194,12 +1208,12 @@ extern "C" int qw_get_pos(const qw_handle* h, int32_t* pos) {
   return QW_OK;
 }
 
-extern "C" int qw_kv_cache(qw_handle* h, int32_t layer, float** k_dev, float** v_dev) {
+extern "C" int qw_kv_cache(qw_handle* h, int32_t layer, void** k_dev, void** v_dev) {
   if (!h || !k_dev || !v_dev) QW_FAIL(h, QW_ERR_ARG, "qw_kv_cache: null argument");
   if (layer < 0 || layer >= h->cfg.n_layers) QW_FAIL(h, QW_ERR_ARG, "qw_kv_cache: bad layer");
   const size_t kv_layer = (size_t)h->cfg.n_kv_heads * h->cfg.max_ctx * h->cfg.head_dim;
-  *k_dev = h->k_cache + (size_t)layer * kv_layer;
-  *v_dev = h->v_cache + (size_t)layer * kv_layer;
+  *k_dev = h->k_cache + (size_t)layer * kv_layer * h->kv_elem;
+  *v_dev = h->v_cache + (size_t)layer * kv_layer * h->kv_elem;
   return QW_OK;
 }
 

@@ -259,12 +259,16 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* X, int H
 // Row t (position p0 + t): per-head QK-RMSNorm and RoPE of q and k, q scaled by
 // 1/sqrt(hd) into Q [T][nq][hd] as a two-bf16 split; k and v appended to the cache at
 // their position, and k also as the two-bf16 row the prefill attention reads.
-template <int HD>
+template <int HD, bool KB>
 __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
     const float* QKV, int p0, int nq, int nkv, const uint16_t* q_norm, const uint16_t* k_norm,
-    float eps, const float2* rope, uint16_t* q_hi, uint16_t* q_lo, float* kc, float* vc, int cap,
+    float eps, const float2* rope, uint16_t* q_hi, uint16_t* q_lo, void* kc_, void* vc_, int cap,
     uint16_t* k_hi, uint16_t* k_lo, int kv_rows) {
   constexpr int EPL = HD / 32;
+  using KV = KvElem<KB>;  // cache element: f32, or bf16 (rounded when stored)
+  using KT = typename KV::T;
+  KT* kc = reinterpret_cast<KT*>(kc_);
+  KT* vc = reinterpret_cast<KT*>(vc_);
   const int t = blockIdx.x, pos = p0 + t;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* row = QKV + (size_t)t * (nq + 2 * nkv) * HD;
@@ -302,13 +306,14 @@ __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
         q_lo[((size_t)t * nq + hh) * HD + lane + 32 * e] = lo;
       }
     } else {
-      float* dst = kc + ((size_t)(hh - nq) * cap + pos) * HD;
+      KT* dst = kc + ((size_t)(hh - nq) * cap + pos) * HD;
       const size_t ko = ((size_t)(hh - nq) * kv_rows + pos) * HD;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
-        dst[lane + 32 * e] = v[e];
+        const KT stored = KV::store(v[e]);
+        dst[lane + 32 * e] = stored;
         uint16_t hi, lo;
-        split_bf16(v[e], hi, lo);
+        split_bf16(KV::load(&stored), hi, lo);
         k_hi[ko + lane + 32 * e] = hi;
         k_lo[ko + lane + 32 * e] = lo;
       }
@@ -316,7 +321,7 @@ __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
   }
   const float* vsrc = row + (size_t)(nq + nkv) * HD;
   for (int i = threadIdx.x; i < nkv * HD; i += 256)
-    vc[((size_t)(i / HD) * cap + pos) * HD + (i % HD)] = vsrc[i];
+    vc[((size_t)(i / HD) * cap + pos) * HD + (i % HD)] = KV::store(vsrc[i]);
 }
 
 // Two bf16 terms of a pair of f32 values (hi = bf16(x), lo = bf16(x - hi)), packed as
@@ -346,8 +351,15 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
 // the layout the MMA reads, and at the end normalise O and store it as the two-bf16
 // split the o_proj GEMM takes. S for tile i+1 is issued as soon as the scores of
 // tile i have been read, so it overlaps the softmax of tile i.
+// The causal work is balanced by cutting each query block's keys into chunks of at
+// most kFaChunk tiles, one CTA each, all heads' heaviest items first; a chunk of a
+// block with several writes its unnormalised O and (m, l) per row, and the last one
+// to arrive merges them in chunk order. The reference maximum of a row moves only
+// when the row maximum rises by more than 2^8 (P then stays below 256), so most
+// tiles leave O in TMEM untouched; O / l does not depend on the reference.
 constexpr int kFaBQ = kFaQueryRows;  // query rows per CTA (the MMA's M, one TMEM lane each)
 constexpr int kFaBN = kFaKeyRows;    // keys per tile (one 128-byte bf16 atom)
+constexpr int kFaChunk = 8;          // key tiles per CTA at most
 
 template <int HD>
 struct FaLayout {
@@ -402,11 +414,21 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (a.T + kFaBQ - 1) / kFaBQ;
-  const int qb = nqb - 1 - (int)blockIdx.x;  // heaviest (latest) block first
-  const int h = blockIdx.y, kvh = h / (a.nq / a.nkv);
+  // this CTA's (query block, key chunk): blocks from the last (heaviest) down, every
+  // head's item of one rank before the next rank (blockIdx.x is the head)
+  int qb = nqb - 1, chunk = blockIdx.y, nch = 1, bt = 1;
+  for (;; --qb) {
+    const int nr = min(kFaBQ, a.T - qb * kFaBQ);
+    bt = (a.p0 + qb * kFaBQ + nr - 1) / kFaBN + 1;  // key tiles of the block
+    nch = (bt + kFaChunk - 1) / kFaChunk;
+    if (chunk < nch || qb == 0) break;
+    chunk -= nch;
+  }
+  const int h = blockIdx.x, kvh = h / (a.nq / a.nkv);
   const int t0 = qb * kFaBQ;
   const int nrows = min(kFaBQ, a.T - t0);
-  const int n_tiles = (a.p0 + t0 + nrows - 1) / kFaBN + 1;  // keys 0 .. last query position
+  const int kt0 = chunk * kFaChunk;
+  const int n_tiles = min(bt, kt0 + kFaChunk) - kt0;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -447,7 +469,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         uint8_t* kb = sm + LY::off_kv + b * LY::kKV;
-        const int k0 = i * kFaBN, krow = kvh * a.kv_rows + k0;
+        const int k0 = (kt0 + i) * kFaBN, krow = kvh * a.kv_rows + k0;
         mbar_expect_tx(&kv_full[b], LY::kKV);
         for (int c = 0; c < QA; ++c) {
           tma_load_2d(kb + c * (kFaBN * 128), &mp.k_hi, 64 * c, krow, &kv_full[b]);
@@ -542,7 +564,7 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(s_empty);
       // causal mask (keys after this row's position) and the running maximum, base 2
-      const int k0 = i * kFaBN;
+      const int k0 = (kt0 + i) * kFaBN;
       float mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kFaBN; ++j) {
@@ -550,12 +572,15 @@ __global__ void __launch_bounds__(192, 1)
         sv[j] = v;
         mx = fmaxf(mx, v);
       }
-      const float m_new = fmaxf(m, mx);  // finite: key 0 is visible to every row
-      const float alpha = exp2f(m - m_new);
+      // the reference moves only when the maximum rises by more than 8 (P < 2^8); a row
+      // that has seen no key yet keeps m = -inf, alpha = 0 and P = 0
+      const float m_new = mx > m + 8.f ? mx : m;
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m - m_use);
       float ps = 0.f;
 #pragma unroll
       for (int j = 0; j < kFaBN; ++j) {
-        const float pj = exp2f(sv[j] - m_new);
+        const float pj = exp2f(sv[j] - m_use);
         sv[j] = pj;
         ps += pj;
       }
@@ -596,30 +621,95 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive_cta(p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, fa_wait(a, o_full, (uint32_t)((n_tiles - 1) & 1)));
-    if (!ok) {
-      if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
-    } else {
-      tc_fence_after();
-      const float inv = 1.0f / l;
-      const bool store = r < nrows;
-      uint16_t* oh = a.o_hi + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
-      uint16_t* ol = a.o_lo + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
+    if (!ok && lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+    const bool store = r < nrows;
+    uint16_t* oh = a.o_hi + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
+    uint16_t* ol = a.o_lo + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
+    if (nch == 1) {
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.0f / l;
 #pragma unroll 1
-      for (int d0 = 0; d0 < HD; d0 += 16) {
-        uint32_t rr[16];
-        tmem_ld16(t_o + lrow + d0, rr);
-        tmem_ld_wait();
-        uint32_t hw[8], lw[8];
+        for (int d0 = 0; d0 < HD; d0 += 16) {
+          uint32_t rr[16];
+          tmem_ld16(t_o + lrow + d0, rr);
+          tmem_ld_wait();
+          uint32_t hw[8], lw[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          split2(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv, hw[e],
-                 lw[e]);
-        if (store) {
-          *reinterpret_cast<uint4*>(oh + d0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(oh + d0 + 8) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-          *reinterpret_cast<uint4*>(ol + d0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-          *reinterpret_cast<uint4*>(ol + d0 + 8) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+          for (int e = 0; e < 8; ++e)
+            split2(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv, hw[e],
+                   lw[e]);
+          if (store) {
+            *reinterpret_cast<uint4*>(oh + d0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(oh + d0 + 8) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            *reinterpret_cast<uint4*>(ol + d0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4*>(ol + d0 + 8) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+          }
         }
+      }
+    } else {
+      // one chunk of several: the unnormalised O and (m, l) of each row, then the last
+      // chunk of the block to arrive merges all of them in chunk order
+      const size_t slot = ((size_t)h * a.nqb + qb) * a.max_ch;
+      float* po = a.part_o + ((slot + chunk) * kFaBQ + r) * HD;
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int d0 = 0; d0 < HD; d0 += 16) {
+          uint32_t rr[16];
+          tmem_ld16(t_o + lrow + d0, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(po + d0 + e) =
+                make_float4(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1]),
+                            __uint_as_float(rr[e + 2]), __uint_as_float(rr[e + 3]));
+        }
+      }
+      a.part_ml[(slot + chunk) * kFaBQ + r] = make_float2(m, l);
+      __threadfence();
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
+      int* flag = reinterpret_cast<int*>(tslot + 1);
+      if (warp == 2 && lane == 0) *flag = atomicAdd(&a.counters[h * a.nqb + qb], 1) == nch - 1;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (*flag) {
+        __threadfence();
+        float M = -INFINITY;
+        for (int c2 = 0; c2 < nch; ++c2)
+          M = fmaxf(M, __ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]).x);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float den = 0.f;
+        for (int c2 = 0; c2 < nch; ++c2) {
+          const float2 ml = __ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]);
+          den = fmaf(exp2f(ml.x - Mu), ml.y, den);
+        }
+        const float inv = 1.0f / den;
+#pragma unroll 1
+        for (int d0 = 0; d0 < HD; d0 += 8) {
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int c2 = 0; c2 < nch; ++c2) {
+            const float w = exp2f(__ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]).x - Mu);
+            const float* src = a.part_o + ((slot + c2) * kFaBQ + r) * HD + d0;
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
+            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+            acc[0] = fmaf(w, x0.x, acc[0]);
+            acc[1] = fmaf(w, x0.y, acc[1]);
+            acc[2] = fmaf(w, x0.z, acc[2]);
+            acc[3] = fmaf(w, x0.w, acc[3]);
+            acc[4] = fmaf(w, x1.x, acc[4]);
+            acc[5] = fmaf(w, x1.y, acc[5]);
+            acc[6] = fmaf(w, x1.z, acc[6]);
+            acc[7] = fmaf(w, x1.w, acc[7]);
+          }
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(acc[2 * e] * inv, acc[2 * e + 1] * inv, hw[e], lw[e]);
+          if (store) {
+            *reinterpret_cast<uint4*>(oh + d0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(ol + d0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+        if (warp == 2 && lane == 0) a.counters[h * a.nqb + qb] = 0;  // ready for the next launch
       }
     }
   }
@@ -636,18 +726,22 @@ __global__ void __launch_bounds__(192, 1)
 // written as 0); and K rows split, hi/lo [nkv][kv_rows][HD], for keys [0, k_end) only
 // (the keys cached before this pass: the row kernel writes the new keys' split rows
 // itself). One CTA per (32 keys, KV head).
-template <int HD>
-__global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const float* vc, int cap,
+template <int HD, bool KB>
+__global__ void __launch_bounds__(256) kv_split_kernel(const void* kc_, const void* vc_, int cap,
                                                        int n, int k_end, int kv_rows,
                                                        uint16_t* kh, uint16_t* kl, uint16_t* vth,
                                                        uint16_t* vtl) {
+  using KV = KvElem<KB>;
+  using KT = typename KV::T;
+  const KT* kc = reinterpret_cast<const KT*>(kc_);
+  const KT* vc = reinterpret_cast<const KT*>(vc_);
   __shared__ float tile[32][HD + 1];
   const int k0 = blockIdx.x * 32, kvh = blockIdx.y;
   if (k0 < k_end)
   for (int i = threadIdx.x; i < 32 * HD / 2; i += 256) {
     const int kk = i / (HD / 2), d = (i % (HD / 2)) * 2;
     if (k0 + kk >= k_end) continue;
-    const float2 v = *reinterpret_cast<const float2*>(kc + ((size_t)kvh * cap + k0 + kk) * HD + d);
+    const float2 v = KV::load2(kc + ((size_t)kvh * cap + k0 + kk) * HD + d);
     uint32_t hi, lo;
     split2(v.x, v.y, hi, lo);
     const size_t o = ((size_t)kvh * kv_rows + k0 + kk) * HD + d;
@@ -656,7 +750,7 @@ __global__ void __launch_bounds__(256) kv_split_kernel(const float* kc, const fl
   }
   for (int i = threadIdx.x; i < 32 * HD; i += 256) {
     const int kk = i / HD, d = i % HD;
-    tile[kk][d] = k0 + kk < n ? vc[((size_t)kvh * cap + k0 + kk) * HD + d] : 0.f;
+    tile[kk][d] = k0 + kk < n ? KV::load(vc + ((size_t)kvh * cap + k0 + kk) * HD + d) : 0.f;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 16 * HD; i += 256) {
@@ -722,42 +816,70 @@ cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g,
 cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
                                    const uint16_t* qn, const uint16_t* kn, float eps,
                                    const float2* rope, uint16_t* q_hi, uint16_t* q_lo,
-                                   float* kc, float* vc, int cap, uint16_t* kv_split,
-                                   cudaStream_t s) {
+                                   void* kc, void* vc, bool kv_bf16, int cap,
+                                   uint16_t* kv_split, cudaStream_t s) {
   const int kv_rows = attn_kv_rows(cap);
   uint16_t* k_hi = kv_split;
   uint16_t* k_lo = kv_split + (size_t)nkv * hd * kv_rows;
-  if (hd == 64)
-    qk_rope_kv_rows_kernel<64><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, q_hi, q_lo,
-                                                 kc, vc, cap, k_hi, k_lo, kv_rows);
-  else if (hd == 128)
-    qk_rope_kv_rows_kernel<128><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, q_hi, q_lo,
-                                                  kc, vc, cap, k_hi, k_lo, kv_rows);
-  else
-    return cudaErrorInvalidValue;
+#define QW_ROPE_ROWS(HDV, KBV)                                                                  \
+  qk_rope_kv_rows_kernel<HDV, KBV><<<T, 256, 0, s>>>(QKV, p0, nq, nkv, qn, kn, eps, rope, q_hi, \
+                                                     q_lo, kc, vc, cap, k_hi, k_lo, kv_rows)
+  if (hd == 64 && kv_bf16) QW_ROPE_ROWS(64, true);
+  else if (hd == 64) QW_ROPE_ROWS(64, false);
+  else if (hd == 128 && kv_bf16) QW_ROPE_ROWS(128, true);
+  else if (hd == 128) QW_ROPE_ROWS(128, false);
+  else return cudaErrorInvalidValue;
+#undef QW_ROPE_ROWS
   return cudaGetLastError();
 }
 int attn_kv_rows(int cap) { return (cap + kFaBN - 1) / kFaBN * kFaBN; }
 size_t attn_kv_bytes(int nkv, int hd, int cap) {
   return (size_t)4 * nkv * hd * attn_kv_rows(cap) * 2;
 }
-cudaError_t launch_attn_prefill(const FaMaps& maps, const float* kc, const float* vc,
-                                uint16_t* kv_split, int cap, int p0, int T, int nq, int nkv,
-                                int hd, uint16_t* o_hi, uint16_t* o_lo, int* err,
-                                uint64_t wait_ns, cudaStream_t s) {
+int attn_max_chunks(int cap) { return (attn_kv_rows(cap) / kFaBN + kFaChunk - 1) / kFaChunk; }
+int attn_max_qblocks(int max_t) { return (max_t + kFaBQ - 1) / kFaBQ; }
+size_t attn_part_bytes(int nq, int max_t, int cap, int hd) {
+  const size_t slots = (size_t)nq * attn_max_qblocks(max_t) * attn_max_chunks(cap);
+  return slots * kFaBQ * ((size_t)hd * 4 + 8) + (size_t)nq * attn_max_qblocks(max_t) * 4;
+}
+cudaError_t launch_attn_prefill(const FaMaps& maps, const void* kc, const void* vc, bool kv_bf16,
+                                uint16_t* kv_split, void* part, int max_t, int cap, int p0,
+                                int T, int nq, int nkv, int hd, uint16_t* o_hi, uint16_t* o_lo,
+                                int* err, uint64_t wait_ns, cudaStream_t s) {
   if (T <= 0 || nkv <= 0 || nq % nkv) return cudaErrorInvalidValue;
   const int n = p0 + T;  // keys this pass reads; split up to the tile the last one is in
   const int kv_rows = attn_kv_rows(cap);
   const size_t plane = (size_t)nkv * hd * kv_rows;
   const dim3 sgrid((n + kFaBN - 1) / kFaBN * (kFaBN / 32), nkv);
-  const dim3 grid((T + kFaBQ - 1) / kFaBQ, nq);
+  const int nqb = (T + kFaBQ - 1) / kFaBQ;
+  int items = 0;  // (query block, key chunk) pairs per head
+  for (int qb = 0; qb < nqb; ++qb) {
+    const int nr = min(kFaBQ, T - qb * kFaBQ);
+    const int bt = (p0 + qb * kFaBQ + nr - 1) / kFaBN + 1;
+    items += (bt + kFaChunk - 1) / kFaChunk;
+  }
+  const dim3 grid(nq, items);
   FaArgs a{p0, T, nq, nkv, kv_rows, o_hi, o_lo, err, wait_ns};
+  a.nqb = nqb;
+  a.max_ch = attn_max_chunks(cap);
+  const size_t slots = (size_t)nq * attn_max_qblocks(max_t) * a.max_ch;
+  a.part_o = reinterpret_cast<float*>(part);
+  a.part_ml = reinterpret_cast<float2*>(a.part_o + slots * kFaBQ * hd);
+  a.counters = reinterpret_cast<int*>(a.part_ml + slots * kFaBQ);
+  if (nqb > attn_max_qblocks(max_t)) return cudaErrorInvalidValue;
   uint16_t *kh = kv_split, *kl = kv_split + plane, *vth = kl + plane, *vtl = vth + plane;
   if (hd == 64) {
-    kv_split_kernel<64><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
+    if (kv_bf16)
+      kv_split_kernel<64, true><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
+    else
+      kv_split_kernel<64, false><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
     attn_prefill_fa_kernel<64><<<grid, 192, FaLayout<64>::bytes, s>>>(maps, a);
   } else if (hd == 128) {
-    kv_split_kernel<128><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
+    if (kv_bf16)
+      kv_split_kernel<128, true><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
+    else
+      kv_split_kernel<128, false><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth,
+                                                        vtl);
     attn_prefill_fa_kernel<128><<<grid, 192, FaLayout<128>::bytes, s>>>(maps, a);
   } else {
     return cudaErrorInvalidValue;

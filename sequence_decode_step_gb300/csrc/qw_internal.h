@@ -89,8 +89,9 @@ struct AttnArgs {
   const uint16_t* k_norm;
   const float2* rope;      // [cap][hd/2] (cos, sin) or nullptr (formed in fp64 in-kernel)
   float rope_theta;
-  float* k_cache;          // [nkv][cap][hd] of this layer
-  float* v_cache;
+  void* k_cache;           // [nkv][cap][hd] of this layer: f32, or bf16 bits when kv_bf16
+  void* v_cache;
+  int kv_bf16;
   int cap;
   const int* pos_ptr;      // device position, or nullptr to use pos_const
   int pos_const;
@@ -174,12 +175,12 @@ cudaError_t launch_rmsnorm_rows(const float* X, int T, int H, const uint16_t* g,
 cudaError_t launch_qk_rope_kv_rows(const float* QKV, int T, int p0, int nq, int nkv, int hd,
                                    const uint16_t* qn, const uint16_t* kn, float eps,
                                    const float2* rope, uint16_t* q_hi, uint16_t* q_lo,
-                                   float* kc, float* vc, int cap, uint16_t* kv_split,
-                                   cudaStream_t s);
+                                   void* kc, void* vc, bool kv_bf16, int cap,
+                                   uint16_t* kv_split, cudaStream_t s);
 // Causal prefill attention on tcgen05 (kind::f16, three MMAs per product of two-bf16
 // splits): Q rows [T][nq][hd] (scaled by 1/sqrt(hd)) as q_hi/q_lo, keys and values
 // 0 .. p0+T-1 of one layer from its f32 cache (kc, vc: [nkv][cap][hd]), split per call
-// into kv_split (attn_kv_bytes) as K hi, K lo [nkv][kv_rows][hd] and V^T hi, V^T lo
+// (f32, or bf16 when kv_bf16) into kv_split (attn_kv_bytes) as K hi, K lo [nkv][kv_rows][hd] and V^T hi, V^T lo
 // [nkv][hd][kv_rows] (kv_rows = attn_kv_rows(cap)); output as the two-bf16 split
 // [T][nq*hd]. The tensor maps (make_attn_maps) cover q_hi/q_lo [max_t, nq*hd] and the
 // four kv_split planes.
@@ -193,16 +194,24 @@ struct FaArgs {
   uint16_t* o_lo;
   int* err;
   uint64_t wait_ns;
+  int nqb, max_ch;   // query blocks of this launch; key chunks per block at most
+  float* part_o;     // [nq][max_qblocks][max_ch][128][hd] unnormalised partial outputs
+  float2* part_ml;   // [nq][max_qblocks][max_ch][128] (reference maximum, row sum), base 2
+  int* counters;     // [nq][nqb] chunk arrivals, 0 between launches
 };
 constexpr int kFaQueryRows = 128, kFaKeyRows = 64;  // query rows per CTA, keys per tile
 int attn_kv_rows(int cap);
 size_t attn_kv_bytes(int nkv, int hd, int cap);
 bool make_attn_maps(FaMaps* m, const uint16_t* q_hi, const uint16_t* q_lo, int max_t, int nq,
                     const uint16_t* kv_split, int nkv, int hd, int cap);
-cudaError_t launch_attn_prefill(const FaMaps& maps, const float* kc, const float* vc,
-                                uint16_t* kv_split, int cap, int p0, int T, int nq, int nkv,
-                                int hd, uint16_t* o_hi, uint16_t* o_lo, int* err,
-                                uint64_t wait_ns, cudaStream_t s);
+// part: scratch of attn_part_bytes(nq, max_t, cap, hd), zeroed once (T <= max_t)
+size_t attn_part_bytes(int nq, int max_t, int cap, int hd);
+int attn_max_chunks(int cap);
+int attn_max_qblocks(int max_t);
+cudaError_t launch_attn_prefill(const FaMaps& maps, const void* kc, const void* vc, bool kv_bf16,
+                                uint16_t* kv_split, void* part, int max_t, int cap, int p0,
+                                int T, int nq, int nkv, int hd, uint16_t* o_hi, uint16_t* o_lo,
+                                int* err, uint64_t wait_ns, cudaStream_t s);
 // int4 g128 packed rows (int4_row_bytes(K) each) -> exact two-bf16 planes hi, lo [rows][K]
 // (the weight operand of the int4 prefill GEMMs).
 cudaError_t launch_dequant_int4_split(const uint8_t* src, int rows, int K, uint16_t* hi,
@@ -237,8 +246,9 @@ struct MegaArgs {
   const uint8_t* lm_head;
   const uint16_t* final_norm;
   const LayerDev* layers;  // device array [L]
-  float* k_cache;          // [L][nkv][cap][hd]
-  float* v_cache;
+  void* k_cache;           // [L][nkv][cap][hd]: f32, or bf16 bits when kv_bf16
+  void* v_cache;
+  int kv_bf16;
   int cap;
   const float2* rope;
   // activations as tagged words (f32 value low, phase tag high)

@@ -68,6 +68,41 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, ui
 }
 
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+// f32 -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint16_t bf16_rne(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
+// Key/value cache elements: f32, or bf16 bits (the cache format of a handle). Loads of
+// 2 or 4 consecutive elements widened to f32, and the stored form of a value.
+template <bool KB>
+struct KvElem {
+  using T = float;
+  static __device__ __forceinline__ T store(float x) { return x; }
+  static __device__ __forceinline__ float load(const T* p) { return *p; }
+  static __device__ __forceinline__ float2 load2(const T* p) {
+    return *reinterpret_cast<const float2*>(p);
+  }
+  static __device__ __forceinline__ float4 load4(const T* p) {
+    return *reinterpret_cast<const float4*>(p);
+  }
+};
+template <>
+struct KvElem<true> {
+  using T = uint16_t;
+  static __device__ __forceinline__ T store(float x) { return bf16_rne(x); }
+  static __device__ __forceinline__ float load(const T* p) { return bf16f(*p); }
+  static __device__ __forceinline__ float2 load2(const T* p) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  }
+  static __device__ __forceinline__ float4 load4(const T* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  }
+};
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -27,8 +27,11 @@ def device_view(ptr: int, shape, dtype: str = "<f4"):
     return torch.as_tensor(_CudaArray(ptr, shape, dtype), device="cuda")
 
 
-def _to_dev(arr: np.ndarray):
+def _to_dev(arr):
+    """A host array (uint16 bf16 bits become int16) on the device; device tensors pass."""
     import torch
+    if isinstance(arr, torch.Tensor):
+        return arr
     a = np.ascontiguousarray(arr)
     if a.dtype == np.uint16:
         a = a.view(np.int16)
@@ -40,7 +43,7 @@ class DeviceModel:
 
     ``weights`` maps the workload's names to uint16 bf16 bits (or float32 for
     tensors an int4 or Q8_0 model quantises on the device with qw_quantize_int4_g128 or
-    qw_quantize_q8_0).
+    qw_quantize_q8_0), as host arrays or as device tensors (int16 for bf16 bits).
     """
 
     def __init__(self, shape, weights: Dict[str, np.ndarray], max_ctx: int,
@@ -76,7 +79,9 @@ class DeviceModel:
         def up_q(name):
             """float32 [rows, K] -> int4 g128 (packed nibbles, bf16 scales) or Q8_0 (int8,
             fp16 scales) on the device, with the library's quantiser."""
-            w32 = _to_dev(np.ascontiguousarray(weights[name], dtype=np.float32))
+            src = weights[name]
+            w32 = src if isinstance(src, torch.Tensor) else \
+                _to_dev(np.ascontiguousarray(src, dtype=np.float32))
             rows, K = w32.shape
             if q8:
                 packed = torch.empty((rows, K), dtype=torch.int8, device="cuda")
@@ -162,10 +167,22 @@ class DeviceModel:
         return self._lg
 
     # -- state hooks -------------------------------------------------------------------
-    def kv(self, layer: int):
+    def _kv_raw(self, layer: int):
+        """Live device views of one layer's K and V cache (f32, or int16-typed bf16 bits)."""
         k, v = B.qw_kv_cache(self.h, layer)
         shp = (self.shape.n_kv_heads, self.max_ctx, self.shape.head_dim)
-        return device_view(k, shp), device_view(v, shp)
+        dt = "<i2" if getattr(self.shape, "kv_format", "f32") == "bf16" else "<f4"
+        return device_view(k, shp, dt), device_view(v, shp, dt)
+
+    def kv(self, layer: int):
+        """K and V of one layer as f32 tensors: live views of an f32 cache, widened
+        copies of a bf16 one."""
+        import torch
+        k, v = self._kv_raw(layer)
+        if k.dtype == torch.int16:
+            widen = lambda t: (t.to(torch.int32) << 16).view(torch.float32)
+            return widen(k), widen(v)
+        return k, v
 
     def set_lora(self, lora, alpha: float = 0.0) -> None:
         """Set (dict 'lora.{l}.q_a' ... of bf16 bits) or clear (None) the adapter; the
@@ -189,11 +206,16 @@ class DeviceModel:
         self._lora_keep = (keep, arrays)
 
     def set_kv(self, layer: int, k: np.ndarray, v: np.ndarray) -> None:
+        """Write f32 K, V [n_kv_heads, n, head_dim] into positions 0..n-1 (rounded to the
+        nearest bf16 for a bf16 cache)."""
         import torch
-        kd, vd = self.kv(layer)
+        kd, vd = self._kv_raw(layer)
         n = k.shape[1]
-        kd[:, :n].copy_(torch.from_numpy(np.ascontiguousarray(k)))
-        vd[:, :n].copy_(torch.from_numpy(np.ascontiguousarray(v)))
+        for dst, src in ((kd, k), (vd, v)):
+            t = torch.from_numpy(np.ascontiguousarray(src, dtype=np.float32))
+            if dst.dtype == torch.int16:
+                t = t.to(torch.bfloat16).view(torch.int16)
+            dst[:, :n].copy_(t)
         torch.cuda.synchronize()
 
     def set_pos(self, pos: int) -> None:

@@ -37,7 +37,7 @@ def test_exports_every_header_symbol(L):
 
 def test_struct_layouts_match(L):
     assert L.qw_abi_version() == B.QW_ABI_VERSION
-    assert L.qw_sizeof_config() == C.sizeof(B.qw_config) == 68
+    assert L.qw_sizeof_config() == C.sizeof(B.qw_config) == 72
     assert L.qw_sizeof_weights() == C.sizeof(B.qw_weights) == 208
     assert L.qw_sizeof_lora() == C.sizeof(B.qw_lora) == 48
     assert B.qw_weights.lm_head.offset == 24 and B.qw_weights.attn_norm.offset == 40
@@ -56,7 +56,8 @@ def test_short_config_struct_rejected(L):
 
 
 @pytest.mark.parametrize("field,value", [("head_dim", 96), ("n_kv_heads", 3), ("hidden", 0),
-                                         ("max_ctx", 0), ("hidden", 250), ("weight_format", 3)])
+                                         ("max_ctx", 0), ("hidden", 250), ("weight_format", 3),
+                                         ("kv_format", 2)])
 def test_bad_config_rejected_before_cuda(L, field, value):
     cfg = B.make_config(W.TINY, 64)
     setattr(cfg, field, value)

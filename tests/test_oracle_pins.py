@@ -627,3 +627,38 @@ def test_q8_0_model_uses_exact_dequantised_weights_and_a_q8_tied_head():
     np.testing.assert_allclose(cp["logits"], head @ cp["final_norm"][-1].astype(np.float64),
                                rtol=1e-5, atol=1e-6)
     assert np.abs(head - E).max() > 0                        # the head differs from the table
+
+
+# ------------------------------------------------------------------ bf16 KV cache
+def test_round_bf16_hand_values():
+    # bf16 keeps 7 fraction bits: 1 + 2^-8 is halfway between 1 and 1 + 2^-7 (ties to
+    # even: 1); 1 + 3 2^-8 is halfway between 1 + 2^-7 and 1 + 2^-6 (even: 1 + 2^-6);
+    # 1 + 2^-8 + 2^-20 is just above halfway (rounds up); bf16 values are fixed points
+    x = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 + 2 ** -8 + 2 ** -20, -2.5, 0.0, 3.140625],
+                 np.float32)
+    want = [1.0, 1 + 2 ** -6, 1 + 2 ** -7, -2.5, 0.0, 3.140625]
+    assert list(R.round_bf16(x)) == want
+
+
+def test_bf16_kv_cache_stores_rounded_rows_and_decode_equals_prefill():
+    d, wl = _tiny(seed=27)
+    cfg = R.Config.from_shape(wl.shape.replace(kv_format="bf16"))
+    ids = [11, 12, 13, 14, 15, 16]
+    a = R.OracleModel(cfg, d.weights, 16)
+    ref = a.prefill(ids)
+    b = R.OracleModel(cfg, d.weights, 16)
+    for t in ids:
+        cp = b.decode_step(t)
+    np.testing.assert_allclose(cp["logits"], ref["logits"], rtol=1e-5, atol=1e-6)
+    for l in range(wl.shape.n_layers):
+        k = a.k_cache[l][:, :6]
+        np.testing.assert_array_equal(R.round_bf16(k), k)          # bf16 values stored
+        np.testing.assert_allclose(b.k_cache[l][:, :6], k, rtol=1e-5, atol=1e-6)
+    # the rounding is the only difference from the f32 cache, and it is visible; layer
+    # 0's keys see the same input either way, so they are the f32 keys rounded
+    f32m = R.build_oracle(d)
+    f32 = f32m.prefill(ids)
+    diff = np.abs(f32["logits"] - ref["logits"]).max()
+    assert 0 < diff < 1e-2
+    np.testing.assert_array_equal(a.k_cache[0][:, :6], R.round_bf16(f32m.k_cache[0][:, :6]))
+    np.testing.assert_array_equal(a.v_cache[0][:, :6], R.round_bf16(f32m.v_cache[0][:, :6]))

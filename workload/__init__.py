@@ -56,6 +56,7 @@ class ModelShape:
     qkv_bias: bool = False
     weight_format: str = "bf16"  # "bf16", "int4_g128" or "q8_0"
     int4_lm_head: bool = False   # untied lm_head quantised too (int4 models)
+    kv_format: str = "f32"       # "f32" or "bf16" KV cache
 
     @property
     def q_dim(self) -> int:
@@ -122,6 +123,12 @@ WORKLOADS: Dict[str, Workload] = {
                                      description="Qwen2.5-3B shape, int4 g128, q/k/v bias, untied "
                                                  "head, KV pre-filled to 4096, 64 greedy steps with "
                                                  "a rank-16 LoRA on q/v and 64 without"),
+    "qwen3_0.6b_longctx_bf16kv": Workload("qwen3_0.6b_longctx_bf16kv",
+                                          QWEN3_0_6B.replace(kv_format="bf16"), seed=2,
+                                          kv_prefill=8192, decode_steps=32, max_ctx=8192 + 32,
+                                          description="the long-context workload with a bf16 "
+                                                      "KV cache (the pre-filled values are "
+                                                      "bf16 already)"),
     "qwen3_0.6b_q8_0_decode": Workload("qwen3_0.6b_q8_0_decode", QWEN3_0_6B_Q8, seed=5,
                                        prompt_len=5, decode_steps=64, max_ctx=256,
                                        description="Qwen3-0.6B shape with Q8_0 projections and "
