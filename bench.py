@@ -522,8 +522,8 @@ def longctx_timing(torch, W, B, DeviceModel, stream) -> dict:
 
 
 def q8_timing(torch, W, B, DeviceModel, stream) -> dict:
-    """Q8_0 decode of the Qwen3-0.6B shape (projections and tied head in Q8_0; the
-    multi-kernel graph): us/token from position 5 and the byte roofline."""
+    """Q8_0 decode of the Qwen3-0.6B shape (projections and tied head in Q8_0, on the
+    persistent kernel): us/token from position 5 and the byte roofline."""
     wl = W.WORKLOADS["qwen3_0.6b_q8_0_decode"]
     s = wl.shape
     w = device_draw(W, torch, s, wl.seed)
@@ -536,7 +536,7 @@ def q8_timing(torch, W, B, DeviceModel, stream) -> dict:
     hbm = measured_peaks().get("hbm_gbs", 6800.0)
     return {"workload": wl.name, "us_per_token": us, "tok_per_s": 1e6 / us,
             "bytes_per_token": byt, "roofline_frac": byt / (us * 1e-6) / 1e9 / hbm,
-            "path": "multi-kernel graph, int8 GEMV with fp16 block scales",
+            "path": "persistent kernel, int8 rows with fp16 block scales decoded in the GEMV",
             "data": "seeded device draw (torch), the workload's shapes and distributions"}
 
 

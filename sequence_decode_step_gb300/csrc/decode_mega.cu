@@ -28,6 +28,7 @@
 // to its end without hanging. All reductions have a fixed order, so results
 // are bit-identical run to run.
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -126,16 +127,22 @@ __device__ __forceinline__ Slice make_slice(const uint8_t* w, int n_units, uint3
   return s;
 }
 
+// Bytes of one weight row of K inputs: bf16, or Q8_0 (K int8, then K/32 fp16 scales,
+// padded to 16 bytes).
+__device__ __forceinline__ uint32_t row_bytes(const MegaArgs& a, int K) {
+  return a.wfmt == 2 ? q8_row_bytes(K) : (uint32_t)K * 2;
+}
+
 // Geometry of a phase (its base is set per layer by the producer; the consumers
 // never read it).
 __device__ __forceinline__ Slice phase_slice(const MegaArgs& a, int kind, int b, int G) {
   const int qd = a.nq * a.hd, kd = a.nkv * a.hd;
   switch (kind) {
-    case K_QKV: return make_slice(nullptr, qd + 2 * kd, (uint32_t)a.H * 2, phase_upi(K_QKV), b, G);
-    case K_O: return make_slice(nullptr, a.H, (uint32_t)qd * 2, phase_upi(K_O), b, G);
-    case K_GU: return make_slice(nullptr, a.I, (uint32_t)a.H * 4, phase_upi(K_GU), b, G);
-    case K_DOWN: return make_slice(nullptr, a.H, (uint32_t)a.I * 2, phase_upi(K_DOWN), b, G);
-    default: return make_slice(a.lm_head, a.V, (uint32_t)a.H * 2, phase_upi(K_LM), b, G);
+    case K_QKV: return make_slice(nullptr, qd + 2 * kd, row_bytes(a, a.H), phase_upi(K_QKV), b, G);
+    case K_O: return make_slice(nullptr, a.H, row_bytes(a, qd), phase_upi(K_O), b, G);
+    case K_GU: return make_slice(nullptr, a.I, 2 * row_bytes(a, a.H), phase_upi(K_GU), b, G);
+    case K_DOWN: return make_slice(nullptr, a.H, row_bytes(a, a.I), phase_upi(K_DOWN), b, G);
+    default: return make_slice(a.lm_head, a.V, row_bytes(a, a.H), phase_upi(K_LM), b, G);
   }
 }
 __device__ __forceinline__ const uint8_t* phase_base(int kind, const LayerDev& L) {
@@ -444,9 +451,22 @@ __device__ __forceinline__ void x_regs(const Smem& S, int K, float (&xr)[MAXC][8
   }
 }
 
-// Per-lane partial dots of NR weight rows (bf16, in shared memory) with the input:
-// the input either held in registers (MAXC chunks of 256) or read from xs.
-template <int NR, int MAXC>
+// 8 weights of row w at input `col` dotted with x: bf16 (16 bytes), or Q8_0 (8 int8
+// bytes and the fp16 scale of their 32-wide block, at byte K + (col / 32) * 2).
+template <int WF>
+__device__ __forceinline__ float dot8w(const uint8_t* w, int col, int K, const float (&x)[8],
+                                       float acc) {
+  if constexpr (WF == 2) {
+    const float sc = __half2float(*reinterpret_cast<const __half*>(w + K + (col >> 5) * 2));
+    return dot8_i8(*reinterpret_cast<const uint2*>(w + col), x, sc, acc);
+  } else {
+    return dot8(*reinterpret_cast<const uint4*>(w + (size_t)col * 2), x, acc);
+  }
+}
+
+// Per-lane partial dots of NR weight rows (bf16 or Q8_0, in shared memory) with the
+// input: the input either held in registers (MAXC chunks of 256) or read from xs.
+template <int NR, int MAXC, int WF>
 __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
                                      const float (&xr)[MAXC > 0 ? MAXC : 1][8], const float* xs,
                                      float (&out)[NR]) {
@@ -457,13 +477,18 @@ __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
 #pragma unroll
     for (int c = 0; c < MAXC; ++c) {
       const int col = c * 256 + lane * 8;
-      uint4 wv[NR];
+      if constexpr (WF == 2) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r)
-        wv[r] = col < K ? *reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2)
-                        : make_uint4(0, 0, 0, 0);
+        for (int r = 0; r < NR; ++r) p[r][c] = col < K ? dot8w<WF>(w[r], col, K, xr[c], 0.f) : 0.f;
+      } else {
+        uint4 wv[NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) p[r][c] = dot8(wv[r], xr[c], 0.f);
+        for (int r = 0; r < NR; ++r)
+          wv[r] = col < K ? *reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2)
+                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < NR; ++r) p[r][c] = dot8(wv[r], xr[c], 0.f);
+      }
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -487,16 +512,24 @@ __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
       const float4 h1 = *reinterpret_cast<const float4*>(xl + cb + 384);
       const float x0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
       const float x1[8] = {l1.x, l1.y, l1.z, l1.w, h1.x, h1.y, h1.z, h1.w};
-      uint4 wa[NR], wb[NR];
+      if constexpr (WF == 2) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        wa[r] = *reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2);
-        wb[r] = *reinterpret_cast<const uint4*>(w[r] + (size_t)(col + 256) * 2);
-      }
+        for (int r = 0; r < NR; ++r) {
+          a0[r] = dot8w<WF>(w[r], col, K, x0, a0[r]);
+          a1[r] = dot8w<WF>(w[r], col + 256, K, x1, a1[r]);
+        }
+      } else {
+        uint4 wa[NR], wb[NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        a0[r] = dot8(wa[r], x0, a0[r]);
-        a1[r] = dot8(wb[r], x1, a1[r]);
+        for (int r = 0; r < NR; ++r) {
+          wa[r] = *reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2);
+          wb[r] = *reinterpret_cast<const uint4*>(w[r] + (size_t)(col + 256) * 2);
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          a0[r] = dot8(wa[r], x0, a0[r]);
+          a1[r] = dot8(wb[r], x1, a1[r]);
+        }
       }
     }
     if (col < K) {
@@ -504,8 +537,7 @@ __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
       const float4 h0 = *reinterpret_cast<const float4*>(xl + cb + 128);
       const float x0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
 #pragma unroll
-      for (int r = 0; r < NR; ++r)
-        a0[r] = dot8(*reinterpret_cast<const uint4*>(w[r] + (size_t)col * 2), x0, a0[r]);
+      for (int r = 0; r < NR; ++r) a0[r] = dot8w<WF>(w[r], col, K, x0, a0[r]);
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) out[r] = a0[r] + a1[r];
@@ -537,7 +569,7 @@ __device__ __forceinline__ void prewait(const MegaArgs& a, Smem& S, int c, int n
 // A warp takes NR rows per iteration (NR / 2 gate/up units for SwiGLU). When the
 // phase fits in the ring its chunks were waited for by prewait() and released
 // together at the end; otherwise each warp waits for and releases them one at a time.
-template <int MAXC, int EPI, int NR>
+template <int MAXC, int EPI, int NR, int WF>
 __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
                                            const Slice& sl, int K, float rs, uint64_t* ty,
                                            uint32_t tag,
@@ -577,7 +609,7 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int r = 0; r < NR; ++r)  // rows past the stage's units reuse its last unit
         w[r] = stage + (size_t)min(t + r / RPU, cn - 1) * unit_bytes + (r % RPU) * row_bytes;
       float v[NR];
-      dotn<NR, MAXC>(w, K, xr, S.xs, v);
+      dotn<NR, MAXC, WF>(w, K, xr, S.xs, v);
       const float sum = rows_reduce<NR>(v, lane) * rs;  // the input's RMS factor
       if constexpr (EPI == EPI_SWIGLU) {
         const float up = __shfl_down_sync(0xffffffffu, sum, SH);  // row 2k+1 onto row 2k
@@ -621,14 +653,14 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
 // memory inside the dot (keeps the kernel under its register budget). X is the
 // kernel's compile-time knowledge of the width: 1 at most 1024, 0 wider, 2 decided
 // at run time (both bodies compiled in).
-template <int EPI, int X, int NR>
+template <int EPI, int X, int NR, int WF>
 __device__ __forceinline__ void gemv(const MegaArgs& a, uint8_t* ring, Smem& S, int& c,
                                      const Slice& sl, int K, float rs, uint64_t* ty, uint32_t tag,
                                      const uint16_t* bias, float* cap, Best& best, bool& abort) {
   if (X == 1 || (X == 2 && K <= 1024))
-    gemv_phase<4, EPI, NR>(a, ring, S, c, sl, K, rs, ty, tag, bias, cap, best, abort);
+    gemv_phase<4, EPI, NR, WF>(a, ring, S, c, sl, K, rs, ty, tag, bias, cap, best, abort);
   else
-    gemv_phase<0, EPI, NR>(a, ring, S, c, sl, K, rs, ty, tag, bias, cap, best, abort);
+    gemv_phase<0, EPI, NR, WF>(a, ring, S, c, sl, K, rs, ty, tag, bias, cap, best, abort);
 }
 
 // Chunks of a slice (the producer streams them in this count).
@@ -1121,7 +1153,7 @@ __device__ void argmax_finalize(const MegaArgs& a, Smem& S, const Best& o, int p
 // the hidden, q and intermediate inputs (see gemv). Only the variants a shape
 // needs are compiled into its kernel: the token loop's code is large and every
 // unused variant inlined into it costs instruction-cache misses.
-template <int HD, int XH, int XQ, int XI, bool KB>
+template <int HD, int XH, int XQ, int XI, bool KB, int WF>
 __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint32_t epoch) {
   const int b = blockIdx.x, G = gridDim.x, tid = threadIdx.x;
   const int qd = a.nq * a.hd;
@@ -1153,7 +1185,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       const float rn = load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
                                   Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr,
                                   min(qs.u1 - qs.u0, kUnitPre), abort);
-      gemv<EPI_STORE, XH, kNrQkv>(a, ring, S, c, qs, a.H, rn, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
+      gemv<EPI_STORE, XH, kNrQkv, WF>(a, ring, S, c, qs, a.H, rn, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
     }
     // attention of this CTA's (kv head, key split)
     if (sp.active) {
@@ -1165,21 +1197,21 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       prewait(a, S, c, slice_chunks(os), abort);
       load_input(a, S, a.attn_o, ta, qd, nullptr, false, 0, a.x + os.u0, nullptr,
                  min(os.u1 - os.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XQ, kNrO>(a, ring, S, c, os, qd, 1.f, a.x, to, nullptr, nullptr, best, abort);
+      gemv<EPI_RESIDUAL, XQ, kNrO, WF>(a, ring, S, c, os, qd, 1.f, a.x, to, nullptr, nullptr, best, abort);
     }
     // gate/up with SwiGLU
     if (gs.u1 > gs.u0) {
       prewait(a, S, c, slice_chunks(gs), abort);
       const float rn = load_input(a, S, a.x, to, a.H, Ld.mlp_norm, false, 0, nullptr, nullptr, 0,
                                   abort);
-      gemv<EPI_SWIGLU, XH, kNrGu>(a, ring, S, c, gs, a.H, rn, a.mlp, tg, nullptr, nullptr, best, abort);
+      gemv<EPI_SWIGLU, XH, kNrGu, WF>(a, ring, S, c, gs, a.H, rn, a.mlp, tg, nullptr, nullptr, best, abort);
     }
     // down + residual (block-0 checkpoint)
     if (ds.u1 > ds.u0) {
       prewait(a, S, c, slice_chunks(ds), abort);
       load_input(a, S, a.mlp, tg, a.I, nullptr, false, 0, a.x + ds.u0, nullptr,
                  min(ds.u1 - ds.u0, kUnitPre), abort);
-      gemv<EPI_RESIDUAL, XI, kNrDown>(a, ring, S, c, ds, a.I, 1.f, a.x, td, nullptr,
+      gemv<EPI_RESIDUAL, XI, kNrDown, WF>(a, ring, S, c, ds, a.I, 1.f, a.x, td, nullptr,
                          (l == 0 && a.cap_blk0) ? a.cap_blk0 + (size_t)pos * a.H : nullptr, best,
                          abort);
     }
@@ -1192,7 +1224,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
     if (a.cap_final && b == 0)
       for (int r = tid; r < a.H; r += kConsumers * 32)
         a.cap_final[(size_t)pos * a.H + r] = S.xs[xs_pos(r)] * rn;
-    gemv<EPI_LOGITS, XH, kNrLm>(a, ring, S, c, ls, a.H, rn, nullptr, 0u, nullptr, nullptr, best, abort);
+    gemv<EPI_LOGITS, XH, kNrLm, WF>(a, ring, S, c, ls, a.H, rn, nullptr, 0u, nullptr, nullptr, best, abort);
   }
   // each lane holding rows kept its own best: merge them onto lane 0 (ties to the lower index)
   best.nan = __any_sync(0xffffffffu, best.nan != 0) ? 1 : 0;
@@ -1205,7 +1237,7 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
   argmax_finalize(a, S, best, pos, epoch);
 }
 
-template <int HD, int XH, int XQ, int XI, bool KB>
+template <int HD, int XH, int XQ, int XI, bool KB, int WF>
 __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -1221,7 +1253,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs
   // The position changes only at the end of a token, so every thread reads it once.
   const int pos = __ldcg(a.pos);
   const uint32_t epoch = __ldcg(a.epoch);
-  if (threadIdx.x < kConsumers * 32) consume<HD, XH, XQ, XI, KB>(a, ring, S, pos, epoch);
+  if (threadIdx.x < kConsumers * 32) consume<HD, XH, XQ, XI, KB, WF>(a, ring, S, pos, epoch);
   else if (threadIdx.x == kConsumers * 32) produce(a, ring, S, pos);
 }
 
@@ -1242,22 +1274,28 @@ size_t mega_smem_bytes() { return (size_t)kNS * kStage + sizeof(Smem); }
 
 // The kernel for a shape: the Qwen3-0.6B class (head dim 128, hidden <= 1024, q
 // and intermediate wider) gets its own instantiation; other shapes the generic one.
-static const void* const kMegaFns[4] = {
-    reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, false>),
-    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, false>),
-    reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, true>),
-    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, true>)};
+// [shape class][cache format][weight format]: the Qwen3-0.6B class (head dim 128,
+// hidden <= 1024, q and intermediate wider) and the generic instantiation; f32 or bf16
+// cache; bf16 or Q8_0 weights (Q8_0 with the f32 cache only).
+constexpr int kMegaCount = 6;
+static const void* const kMegaFns[kMegaCount] = {
+    reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, false, 0>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, false, 0>),
+    reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, true, 0>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, true, 0>),
+    reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, false, 2>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, false, 2>)};
 
 static const void* mega_kernel_for(const MegaArgs& a) {
-  const int kv = a.kv_bf16 ? 2 : 0;
-  if (a.hd == 128 && a.H <= 1024 && a.nq * a.hd > 1024 && a.I > 1024) return kMegaFns[kv];
-  return kMegaFns[kv + 1];
+  const int fmt = a.wfmt == 2 ? 4 : (a.kv_bf16 ? 2 : 0);
+  if (a.hd == 128 && a.H <= 1024 && a.nq * a.hd > 1024 && a.I > 1024) return kMegaFns[fmt];
+  return kMegaFns[fmt + 1];
 }
 
 cudaError_t set_mega_attributes() {
   const void* const* fns = kMegaFns;
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < kMegaCount; ++i) {
     const void* f = fns[i];
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1270,7 +1308,7 @@ cudaError_t set_mega_attributes() {
 }
 
 bool is_mega_kernel(const void* fn) {
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kMegaCount; ++i)
     if (fn == kMegaFns[i]) return true;
   return false;
 }

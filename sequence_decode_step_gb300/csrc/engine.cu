@@ -270,7 +270,9 @@ static int alloc_state(qw_handle* h) {
   const size_t L = c.n_layers, nkv = c.n_kv_heads, hd = c.head_dim, cap = c.max_ctx;
   const size_t qkv_rows = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * hd;
   h->nsplit_max = std::max(1, h->num_sms / c.n_kv_heads);
-  h->mega_ok = c.weight_format == QW_WEIGHTS_BF16 &&
+  // the persistent kernel takes bf16 weights, and Q8_0 weights with the f32 cache
+  h->mega_ok = (c.weight_format == QW_WEIGHTS_BF16 ||
+                (c.weight_format == QW_WEIGHTS_Q8_0 && c.kv_format == QW_KV_F32)) &&
                mega::mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim,
                                     c.head_dim, c.n_q_heads / c.n_kv_heads, c.n_layers) &&
                mega_wide::mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim,
@@ -710,6 +712,7 @@ static MegaArgs mega_args(qw_handle* h) {
   m.k_cache = h->k_cache;
   m.v_cache = h->v_cache;
   m.kv_bf16 = h->kv_bf16 ? 1 : 0;
+  m.wfmt = h->wfmt == 2 ? 2 : 0;
   m.cap = c.max_ctx;
   m.rope = h->rope;
   m.x = h->mx;

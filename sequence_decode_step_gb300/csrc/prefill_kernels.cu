@@ -257,8 +257,9 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* X, int H
 }
 
 // Row t (position p0 + t): per-head QK-RMSNorm and RoPE of q and k, q scaled by
-// 1/sqrt(hd) into Q [T][nq][hd] as a two-bf16 split; k and v appended to the cache at
-// their position, and k also as the two-bf16 row the prefill attention reads.
+// log2(e)/sqrt(hd) into Q [T][nq][hd] as a two-bf16 split (the attention works in base
+// 2); k and v appended to the cache at their position, and k also as the two-bf16 row
+// the prefill attention reads.
 template <int HD, bool KB>
 __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
     const float* QKV, int p0, int nq, int nkv, const uint16_t* q_norm, const uint16_t* k_norm,
@@ -272,7 +273,8 @@ __global__ void __launch_bounds__(256) qk_rope_kv_rows_kernel(
   const int t = blockIdx.x, pos = p0 + t;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* row = QKV + (size_t)t * (nq + 2 * nkv) * HD;
-  const float scale = 1.0f / sqrtf((float)HD);
+  // Q carries 1/sqrt(hd) and log2(e): the attention's scores come out in base-2 units
+  const float scale = 1.4426950408889634f / sqrtf((float)HD);
   const float2* rr = rope + (size_t)pos * (HD / 2);
   for (int hh = warp; hh < nq + nkv; hh += 8) {
     const bool isq = hh < nq;
@@ -374,6 +376,22 @@ struct FaLayout {
   static constexpr uint32_t off_bar = off_p + 2 * kP1;
   static constexpr uint32_t bytes = off_bar + 128 + 1024;   // barriers, TMEM slot, alignment slack
 };
+
+// 2^x with the special-function unit (ex2.approx.ftz: relative error about 2^-22;
+// 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Two f32 values as two bf16 terms each (hi = bf16(x), lo = bf16(x - hi)), packed as
+// bf16x2 words: the first value in the low half.
+__device__ __forceinline__ void split2_packed(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
 
 // Wait for an mbarrier phase, bounded; gives up at once when another thread of the
 // launch already reported a timeout.
@@ -543,7 +561,7 @@ __global__ void __launch_bounds__(192, 1)
     const int q4 = warp & 3, r = q4 * 32 + lane;
     const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
     const int qpos = a.p0 + t0 + r;
-    constexpr float kLog2e = 1.4426950408889634f;
+    const int first_pos = a.p0 + t0;  // the block's first row: tiles past it need the mask
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     uint8_t* prow = sm + LY::off_p + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
@@ -563,28 +581,31 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(s_empty);
-      // causal mask (keys after this row's position) and the running maximum, base 2
+      // causal mask (keys after this row's position; only tiles that reach past the
+      // block's first row) and the running maximum; scores are in base-2 units already
       const int k0 = (kt0 + i) * kFaBN;
-      float mx = -INFINITY;
+      if (k0 + kFaBN - 1 > first_pos) {
 #pragma unroll
-      for (int j = 0; j < kFaBN; ++j) {
-        const float v = k0 + j <= qpos ? sv[j] * kLog2e : -INFINITY;
-        sv[j] = v;
-        mx = fmaxf(mx, v);
+        for (int j = 0; j < kFaBN; ++j)
+          if (k0 + j > qpos) sv[j] = -INFINITY;
       }
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int j = 0; j < kFaBN; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], sv[j]);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       // the reference moves only when the maximum rises by more than 8 (P < 2^8); a row
       // that has seen no key yet keeps m = -inf, alpha = 0 and P = 0
       const float m_new = mx > m + 8.f ? mx : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m - m_use);
-      float ps = 0.f;
+      const float alpha = fast_exp2(m - m_use);
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < kFaBN; ++j) {
-        const float pj = exp2f(sv[j] - m_use);
+        const float pj = fast_exp2(sv[j] - m_use);
         sv[j] = pj;
-        ps += pj;
+        ps4[j & 3] += pj;
       }
-      l = l * alpha + ps;
+      l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
       m = m_new;
       if (i > 0) {
         // P V of tile i-1 has finished: P's buffer is free and O can be rescaled
@@ -610,7 +631,8 @@ __global__ void __launch_bounds__(192, 1)
       for (int u = 0; u < kFaBN / 8; ++u) {
         uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split2(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1], hw[e], lw[e]);
+        for (int e = 0; e < 4; ++e)
+          split2_packed(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1], hw[e], lw[e]);
         const uint32_t off = (uint32_t)((u ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *reinterpret_cast<uint4*>(prow + LY::kP1 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -681,14 +703,14 @@ __global__ void __launch_bounds__(192, 1)
         float den = 0.f;
         for (int c2 = 0; c2 < nch; ++c2) {
           const float2 ml = __ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]);
-          den = fmaf(exp2f(ml.x - Mu), ml.y, den);
+          den = fmaf(fast_exp2(ml.x - Mu), ml.y, den);
         }
         const float inv = 1.0f / den;
 #pragma unroll 1
         for (int d0 = 0; d0 < HD; d0 += 8) {
           float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           for (int c2 = 0; c2 < nch; ++c2) {
-            const float w = exp2f(__ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]).x - Mu);
+            const float w = fast_exp2(__ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]).x - Mu);
             const float* src = a.part_o + ((slot + c2) * kFaBQ + r) * HD + d0;
             const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
             const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));

@@ -249,6 +249,7 @@ struct MegaArgs {
   void* k_cache;           // [L][nkv][cap][hd]: f32, or bf16 bits when kv_bf16
   void* v_cache;
   int kv_bf16;
+  int wfmt;                // weight rows (projections and LM head): 0 bf16, 2 Q8_0
   int cap;
   const float2* rope;
   // activations as tagged words (f32 value low, phase tag high)

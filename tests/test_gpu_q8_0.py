@@ -3,7 +3,8 @@ projections and LM head read by a q8_0 matvec at decode).
 
 The device quantiser and the int8 dequantisation inside the GEMV are checked bit for
 bit against the oracle; whole-model decode (tied head quantised from the embedding
-table, and an untied head) against the oracle's Q8_0 model at the model tolerance.
+table, and an untied head) on both decode paths (the persistent kernel and the graph of
+separate kernels) against the oracle's Q8_0 model at the model tolerance.
 """
 import numpy as np
 import pytest
@@ -102,12 +103,13 @@ def test_q8_0_gemv_one_hot_is_the_dequantised_column_bit_for_bit(L, rows, cols):
     assert violation(_gemv_q8(L, q, s, x), want, 1e-4, 1e-4) <= 0
 
 
-def _decode_vs_oracle(wl, steps):
+def _decode_vs_oracle(wl, steps, path=0):
     d = W.draw(wl)
     m = DeviceModel(wl.shape, d.weights, wl.max_ctx)
     o = R.build_oracle(d)
     try:
-        assert B.qw_get_decode_path(m.h) == 1           # Q8_0 runs the multi-kernel graph
+        B.qw_set_decode_path(m.h, path)                 # 0: the persistent kernel, 1: the graph
+        assert B.qw_get_decode_path(m.h) == path
         am, lg = m.prefill(d.prompt, logits=True)
         want = o.prefill(d.prompt)["logits"]
         assert violation(lg, want) <= 0
@@ -125,11 +127,13 @@ def _decode_vs_oracle(wl, steps):
         m.close()
 
 
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("tied", [True, False])
-def test_tiny_q8_0_decode(tied):
+def test_tiny_q8_0_decode(tied, path):
     shape = W.TINY.replace(weight_format="q8_0", tie_word_embeddings=tied)
-    _decode_vs_oracle(W.Workload("tiny_q8", shape, seed=32, prompt_len=6, max_ctx=64), 12)
+    _decode_vs_oracle(W.Workload("tiny_q8", shape, seed=32, prompt_len=6, max_ctx=64), 12, path)
 
 
-def test_qwen3_06b_q8_0_decode():
-    _decode_vs_oracle(W.WORKLOADS["qwen3_0.6b_q8_0_decode"], 16)
+@pytest.mark.parametrize("path", [0, 1])
+def test_qwen3_06b_q8_0_decode(path):
+    _decode_vs_oracle(W.WORKLOADS["qwen3_0.6b_q8_0_decode"], 16, path)
