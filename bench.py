@@ -445,7 +445,7 @@ def prefill_timing(torch, W, DeviceModel, stream) -> dict:
     return {"workload": PREFILL_WORKLOAD, "T": wl.prompt_len, "ms": ms,
             "tok_per_s": wl.prompt_len / (ms / 1e3),
             "path": "batched: tcgen05 GEMMs (bf16 weights x two-bf16 activations), "
-                    "causal flash attention on mma.sync tensor cores (bf16 hi/lo operands)",
+                    "causal flash attention on tcgen05 (TMA-fed tiles, S and O in TMEM, bf16 hi/lo operands)",
             "roofline": {"bound": "tensor", "algorithmic_tflop": fl / 1e12,
                          "achieved": fl / (ms / 1e3) / 1e12, "peak": tc, "unit": "TFLOP/s",
                          "frac": fl / (ms / 1e3) / 1e12 / tc,
