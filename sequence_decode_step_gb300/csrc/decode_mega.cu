@@ -42,10 +42,25 @@
 // contexts), and decode_mega_wide.cu builds it again with 11 under another
 // namespace for long contexts, where the attention passes dominate and spread
 // over more warps (at short context the GEMV phases have too few rows per CTA
-// for the extra warps, and the wider barriers cost more).
+// for the extra warps, and the wider barriers cost more). decode_mega_big.cu
+// builds it a third time for wide inputs (up to 44 x 256 = 11264, e.g. an 11008-wide
+// SwiGLU vector) and int4 g128 weights: a larger input buffer in shared memory
+// and one ring stage fewer.
 #ifndef QW_MEGA_CONSUMERS
 #define QW_MEGA_CONSUMERS 7
 #define QW_MEGA_NS mega
+#endif
+#ifndef QW_MEGA_MAXC
+#define QW_MEGA_MAXC 12
+#endif
+#ifndef QW_MEGA_STAGES
+#define QW_MEGA_STAGES 6
+#endif
+#ifndef QW_MEGA_BIG
+#define QW_MEGA_BIG 0
+#endif
+#ifndef QW_MEGA_ROUND_PAIRS
+#define QW_MEGA_ROUND_PAIRS 8
 #endif
 
 namespace qw {
@@ -56,9 +71,9 @@ namespace {
 constexpr int kConsumers = QW_MEGA_CONSUMERS;
 constexpr int kNT = kConsumers * 32;         // consumer threads
 constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kNS = 6;                       // ring stages
+constexpr int kNS = QW_MEGA_STAGES;          // ring stages
 constexpr uint32_t kStage = 32 * 1024;       // bytes per stage
-constexpr int kMaxC = 12;                    // input vectors up to 12 x 256 = 3072 wide
+constexpr int kMaxC = QW_MEGA_MAXC;          // input vectors up to kMaxC x 256 wide
 constexpr int kTK = 32;                      // keys per attention tile (K + V = 32 KB at hd 128)
 constexpr int kGQ = 8;
 constexpr int kMinKeys = 128;               // keys per split at least (one pass)
@@ -68,7 +83,7 @@ constexpr int kMinKeys = 128;               // keys per split at least (one pass
 // split against 662-705 with the head split's two passes.
 constexpr int kHeadSplitKeys = 128;
 constexpr int kPass = 4;                     // tiles per attention pass
-constexpr int kUnitPre = 64;                 // units of a phase whose epilogue values are prefetched
+constexpr int kUnitPre = kMegaUnitPre;       // units of a phase whose epilogue values are prefetched
 
 enum Kind { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GU = 3, K_DOWN = 4, K_LM = 5 };
 
@@ -81,12 +96,15 @@ struct Smem {
   int flag;
   alignas(16) float xs[kMaxC * 256];  // phase input vector (normalised when the phase has a norm);
                                       // written with float4 stores, so 16-byte aligned
+  float xsum[kMaxC * 32];  // int4 weights: 136 x the sum of each lane's 8 inputs of a chunk
   float q_s[kGQ * 128];
   float kn_s[128];
   float vn_s[128];
   float ml_s[2 * kGQ];
   float al_s[kGQ];
-  float unit_s[kUnitPre];        // per-unit values the epilogue needs (residual rows or bias)
+  float unit_s[kUnitPre];        // per-unit values the epilogue needs (residual rows, or bias
+                                 // plus the LoRA update)
+  float lora_t[128];             // LoRA: A_q . x_n, then A_v . x_n (rank <= 64 each)
   float pml_s[2 * kGQ * 160];    // split partials (m, l) for the combine; before it, the
                                  // scores and probabilities of an attention pass
 };
@@ -127,10 +145,14 @@ __device__ __forceinline__ Slice make_slice(const uint8_t* w, int n_units, uint3
   return s;
 }
 
-// Bytes of one weight row of K inputs: bf16, or Q8_0 (K int8, then K/32 fp16 scales,
-// padded to 16 bytes).
+// Bytes of one weight row of K inputs: bf16; int4 g128 (K/2 nibble bytes, then K/128
+// bf16 scales, padded to 16 bytes); or Q8_0 (K int8, then K/32 fp16 scales, padded to
+// 16 bytes).
+__host__ __device__ __forceinline__ uint32_t row_bytes_fmt(int wfmt, int K) {
+  return wfmt == 2 ? q8_row_bytes(K) : wfmt == 1 ? int4_row_bytes(K) : (uint32_t)K * 2;
+}
 __device__ __forceinline__ uint32_t row_bytes(const MegaArgs& a, int K) {
-  return a.wfmt == 2 ? q8_row_bytes(K) : (uint32_t)K * 2;
+  return row_bytes_fmt(a.wfmt, K);
 }
 
 // Geometry of a phase (its base is set per layer by the producer; the consumers
@@ -150,8 +172,9 @@ __device__ __forceinline__ const uint8_t* phase_base(int kind, const LayerDev& L
 }
 
 // Attention work of CTA b (all derived from the device position): KV head g and
-// either a key split s (its query heads all together, partials combined by
-// split 0) or, up to kHeadSplitKeys keys, query head h0 of the group over all
+// either a key split s (its query heads all together, the partials combined by
+// all splits, each a slice of the outputs) or, up to kHeadSplitKeys keys, query
+// head h0 of the group over all
 // keys (the group's heads on separate CTAs, no combine).
 struct Split {
   int g, s, k0, k1, nsplit;
@@ -328,7 +351,7 @@ __device__ __forceinline__ int xs_pos(int k) {
 // Out of line: its word pairs in flight would otherwise push the inlined token
 // loop past the register budget (spills go to L2, since shared memory takes
 // nearly all of L1).
-template <int NP>  // (value, tag) word pairs per thread: K <= 2 * NP * kNT
+template <int NP>  // (value, tag) word pairs per thread and round: a round covers 2 * NP * kNT inputs
 __device__ __noinline__ float load_input_n(const MegaArgs& a, Smem& S, const uint64_t* v,
                                           uint32_t tag, int K, const uint16_t* g, bool from_embed,
                                           int tok, const uint64_t* unit_own,
@@ -338,66 +361,79 @@ __device__ __noinline__ float load_input_n(const MegaArgs& a, Smem& S, const uin
   float uv = 0.f;
   if (tid < n_unit)
     uv = unit_own ? word_value(__ldcg(unit_own + tid)) : (unit_bf16 ? bf16f(unit_bf16[tid]) : 0.f);
-  // the norm gain (bf16), one pair per word pair, in the same batch of loads
-  uint32_t gv[NP];
-  if (g != nullptr) {
-#pragma unroll
-    for (int i = 0; i < NP; ++i) {
-      const int idx = tid + i * NT;
-      gv[i] = idx * 2 < K ? *reinterpret_cast<const uint32_t*>(g + idx * 2) : 0u;
-    }
-  }
   float ss = 0.f;
-  if (from_embed) {
-    const uint4* e = reinterpret_cast<const uint4*>(a.embed + (size_t)tok * K);
-    constexpr int NE = (NP + 3) / 4;
-    uint4 w[NE];
+  // Inputs wider than one round (only in the wide-input build) take several rounds;
+  // the first one waits at the barrier for the previous phase's readers of xs.
+  for (int r0 = 0; r0 < K; r0 += 2 * NP * NT) {
+    const int p0 = r0 / 2;  // first word pair of the round
+    // the norm gain (bf16), one pair per word pair, in the same batch of loads
+    uint32_t gv[NP];
+    if (g != nullptr) {
 #pragma unroll
-    for (int i = 0; i < NE; ++i) {
-      const int idx = tid + i * NT;
-      w[i] = idx * 8 < K ? e[idx] : make_uint4(0, 0, 0, 0);
-    }
-    csync();  // the previous phase's readers of xs / unit_s are done
-#pragma unroll
-    for (int i = 0; i < NE; ++i) {
-      const int idx = tid + i * NT;
-      if (idx * 8 < K) {
-        float* d = &S.xs[(idx >> 5) * 256 + (idx & 31) * 4];
-        *reinterpret_cast<float4*>(d) =
-            make_float4(__uint_as_float(w[i].x << 16), __uint_as_float(w[i].x & 0xffff0000u),
-                        __uint_as_float(w[i].y << 16), __uint_as_float(w[i].y & 0xffff0000u));
-        *reinterpret_cast<float4*>(d + 128) =
-            make_float4(__uint_as_float(w[i].z << 16), __uint_as_float(w[i].z & 0xffff0000u),
-                        __uint_as_float(w[i].w << 16), __uint_as_float(w[i].w & 0xffff0000u));
+      for (int i = 0; i < NP; ++i) {
+        const int idx = p0 + tid + i * NT;
+        gv[i] = idx * 2 < K ? *reinterpret_cast<const uint32_t*>(g + idx * 2) : 0u;
       }
     }
-  } else {
-    uint64_t w[NP][2];
-    unsigned pend = 0;
+    if (from_embed) {
+      const uint4* e = reinterpret_cast<const uint4*>(a.embed + (size_t)tok * K);
+      constexpr int NE = (NP + 3) / 4;  // 8-element groups per thread: cover the round's
+      const int e0 = r0 / 8;             // NP * NT / 4 groups, starting at group e0
+      uint4 w[NE];
 #pragma unroll
-    for (int i = 0; i < NP; ++i)
-      if ((tid + i * NT) * 2 < K) pend |= 1u << i;
-    uint64_t t0 = 0;
-    for (uint32_t n = 1; pend && !abort; ++n) {
+      for (int i = 0; i < NE; ++i) {
+        const int j = tid + i * NT, idx = e0 + j;
+        w[i] = j < NP * NT / 4 && idx * 8 < K ? e[idx] : make_uint4(0, 0, 0, 0);
+      }
+      if (r0 == 0) csync();  // the previous phase's readers of xs / unit_s are done
+#pragma unroll
+      for (int i = 0; i < NE; ++i) {
+        const int j = tid + i * NT, idx = e0 + j;
+        if (j < NP * NT / 4 && idx * 8 < K) {
+          float* d = &S.xs[(idx >> 5) * 256 + (idx & 31) * 4];
+          *reinterpret_cast<float4*>(d) =
+              make_float4(__uint_as_float(w[i].x << 16), __uint_as_float(w[i].x & 0xffff0000u),
+                          __uint_as_float(w[i].y << 16), __uint_as_float(w[i].y & 0xffff0000u));
+          *reinterpret_cast<float4*>(d + 128) =
+              make_float4(__uint_as_float(w[i].z << 16), __uint_as_float(w[i].z & 0xffff0000u),
+                          __uint_as_float(w[i].w << 16), __uint_as_float(w[i].w & 0xffff0000u));
+        }
+      }
+    } else {
+      uint64_t w[NP][2];
+      unsigned pend = 0;
 #pragma unroll
       for (int i = 0; i < NP; ++i)
-        if ((pend >> i) & 1u) ld_words2(v + 2 * (tid + i * NT), w[i][0], w[i][1]);
+        if ((p0 + tid + i * NT) * 2 < K) pend |= 1u << i;
+      uint64_t t0 = 0;
+      for (uint32_t n = 1; pend && !abort; ++n) {
 #pragma unroll
-      for (int i = 0; i < NP; ++i)
-        if (((pend >> i) & 1u) && word_tag(w[i][0]) == tag && word_tag(w[i][1]) == tag)
-          pend &= ~(1u << i);
-      if (pend) poll_bound(a, n, t0, abort);
-    }
-    csync();  // the previous phase's readers of xs / unit_s / red are done
+        for (int i = 0; i < NP; ++i)
+          if ((pend >> i) & 1u) ld_words2(v + 2 * (p0 + tid + i * NT), w[i][0], w[i][1]);
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
-      const int idx = tid + i * NT;
-      if (idx * 2 < K) {
-        const float x0 = word_value(w[i][0]), x1 = word_value(w[i][1]);
-        ss = fmaf(x0, x0, fmaf(x1, x1, ss));
-        const float g0 = g != nullptr ? __uint_as_float(gv[i] << 16) : 1.f;
-        const float g1 = g != nullptr ? __uint_as_float(gv[i] & 0xffff0000u) : 1.f;
-        *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = make_float2(x0 * g0, x1 * g1);
+        for (int i = 0; i < NP; ++i)
+          if (((pend >> i) & 1u) && word_tag(w[i][0]) == tag && word_tag(w[i][1]) == tag)
+            pend &= ~(1u << i);
+        if (pend) poll_bound(a, n, t0, abort);
+      }
+      if (r0 == 0) csync();  // the previous phase's readers of xs / unit_s / red are done
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const int idx = p0 + tid + i * NT;
+        float ps = 0.f;
+        if (idx * 2 < K) {
+          const float x0 = word_value(w[i][0]), x1 = word_value(w[i][1]);
+          ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+          const float g0 = g != nullptr ? __uint_as_float(gv[i] << 16) : 1.f;
+          const float g1 = g != nullptr ? __uint_as_float(gv[i] & 0xffff0000u) : 1.f;
+          *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = make_float2(x0 * g0, x1 * g1);
+          ps = x0 * g0 + x1 * g1;
+        }
+        if (a.wfmt == 1) {  // pairs 4m .. 4m + 3 (8 inputs) sit on 4 neighbouring lanes
+          ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+          ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+          if ((idx & 3) == 0 && idx * 2 < K) S.xsum[idx >> 2] = 136.f * ps;
+        }
       }
     }
   }
@@ -414,6 +450,15 @@ __device__ __noinline__ float load_input_n(const MegaArgs& a, Smem& S, const uin
     ss = warp_sum(ss);
     if ((tid & 31) == 0) S.red[tid >> 5] = ss;
   }
+  if (from_embed && a.wfmt == 1) {  // the gained embedding row is in xs
+    csync();
+    for (int m = tid; m * 8 < K; m += NT) {
+      const float* q = &S.xs[(m >> 5) * 256 + (m & 31) * 4];
+      const float4 lo = *reinterpret_cast<const float4*>(q);
+      const float4 hi = *reinterpret_cast<const float4*>(q + 128);
+      S.xsum[m] = 136.f * (((lo.x + lo.y) + (lo.z + lo.w)) + ((hi.x + hi.y) + (hi.z + hi.w)));
+    }
+  }
   abort = csync_or(abort);
   if (g == nullptr) return 1.f;
   float tot = 0.f;
@@ -427,7 +472,10 @@ __device__ __forceinline__ float load_input(const MegaArgs& a, Smem& S, const ui
                                            int tok, const uint64_t* unit_own,
                                            const uint16_t* unit_bf16, int n_unit, bool& abort) {
   constexpr int NP_1K = (1024 + 2 * kNT - 1) / (2 * kNT);      // pairs per thread, K <= 1024
-  constexpr int NP_MAX = (kMaxC * 256 + 2 * kNT - 1) / (2 * kNT);
+  // wider inputs: one round when the buffer holds at most 3072, else rounds of
+  // QW_MEGA_ROUND_PAIRS pairs per thread
+  constexpr int NP_MAX = kMaxC * 256 <= 3072 ? (kMaxC * 256 + 2 * kNT - 1) / (2 * kNT)
+                                             : QW_MEGA_ROUND_PAIRS;
   if (K <= 2 * NP_1K * kNT)
     return load_input_n<NP_1K>(a, S, v, tag, K, g, from_embed, tok, unit_own, unit_bf16, n_unit,
                                abort);
@@ -451,12 +499,19 @@ __device__ __forceinline__ void x_regs(const Smem& S, int K, float (&xr)[MAXC][8
   }
 }
 
-// 8 weights of row w at input `col` dotted with x: bf16 (16 bytes), or Q8_0 (8 int8
-// bytes and the fp16 scale of their 32-wide block, at byte K + (col / 32) * 2).
+// 8 weights of row w at input `col` dotted with x: bf16 (16 bytes); int4 g128 (one
+// 32-bit word of nibbles at byte col / 2, and the bf16 scale of their 128-wide group
+// at byte K / 2 + (col / 128) * 2); or Q8_0 (8 int8 bytes and the fp16 scale of their
+// 32-wide block, at byte K + (col / 32) * 2).
+// For int4, xc is 136 x the sum of the 8 inputs (see dot8_i4_biased).
 template <int WF>
 __device__ __forceinline__ float dot8w(const uint8_t* w, int col, int K, const float (&x)[8],
-                                       float acc) {
-  if constexpr (WF == 2) {
+                                       float acc, float xc = 0.f) {
+  if constexpr (WF == 1) {
+    const float sc = bf16f(*reinterpret_cast<const uint16_t*>(w + (K >> 1) + (col >> 7) * 2));
+    return fmaf(dot8_i4_biased(*reinterpret_cast<const uint32_t*>(w + (col >> 1)), x) - xc, sc,
+                acc);
+  } else if constexpr (WF == 2) {
     const float sc = __half2float(*reinterpret_cast<const __half*>(w + K + (col >> 5) * 2));
     return dot8_i8(*reinterpret_cast<const uint2*>(w + col), x, sc, acc);
   } else {
@@ -464,12 +519,15 @@ __device__ __forceinline__ float dot8w(const uint8_t* w, int col, int K, const f
   }
 }
 
-// Per-lane partial dots of NR weight rows (bf16 or Q8_0, in shared memory) with the
+// Per-lane partial dots of NR weight rows (bf16, int4 or Q8_0, in shared memory) with the
 // input: the input either held in registers (MAXC chunks of 256) or read from xs.
+// For int4 rows, xcr (registers) / xsum (shared memory) hold 136 x the sum of each
+// lane's 8 inputs of a chunk.
 template <int NR, int MAXC, int WF>
 __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
-                                     const float (&xr)[MAXC > 0 ? MAXC : 1][8], const float* xs,
-                                     float (&out)[NR]) {
+                                     const float (&xr)[MAXC > 0 ? MAXC : 1][8],
+                                     const float (&xcr)[MAXC > 0 ? MAXC : 1], const float* xs,
+                                     const float* xsum, float (&out)[NR]) {
   const int lane = threadIdx.x & 31;
   if constexpr (MAXC > 0) {
     // one FMA chain per (row, chunk), summed over chunks in order
@@ -477,9 +535,10 @@ __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
 #pragma unroll
     for (int c = 0; c < MAXC; ++c) {
       const int col = c * 256 + lane * 8;
-      if constexpr (WF == 2) {
+      if constexpr (WF != 0) {
 #pragma unroll
-        for (int r = 0; r < NR; ++r) p[r][c] = col < K ? dot8w<WF>(w[r], col, K, xr[c], 0.f) : 0.f;
+        for (int r = 0; r < NR; ++r)
+          p[r][c] = col < K ? dot8w<WF>(w[r], col, K, xr[c], 0.f, xcr[c]) : 0.f;
       } else {
         uint4 wv[NR];
 #pragma unroll
@@ -512,11 +571,13 @@ __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
       const float4 h1 = *reinterpret_cast<const float4*>(xl + cb + 384);
       const float x0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
       const float x1[8] = {l1.x, l1.y, l1.z, l1.w, h1.x, h1.y, h1.z, h1.w};
-      if constexpr (WF == 2) {
+      if constexpr (WF != 0) {
+        const float c0 = WF == 1 ? xsum[(col >> 3)] : 0.f;
+        const float c1 = WF == 1 ? xsum[(col >> 3) + 32] : 0.f;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-          a0[r] = dot8w<WF>(w[r], col, K, x0, a0[r]);
-          a1[r] = dot8w<WF>(w[r], col + 256, K, x1, a1[r]);
+          a0[r] = dot8w<WF>(w[r], col, K, x0, a0[r], c0);
+          a1[r] = dot8w<WF>(w[r], col + 256, K, x1, a1[r], c1);
         }
       } else {
         uint4 wa[NR], wb[NR];
@@ -536,8 +597,9 @@ __device__ __forceinline__ void dotn(const uint8_t* const (&w)[NR], int K,
       const float4 l0 = *reinterpret_cast<const float4*>(xl + cb);
       const float4 h0 = *reinterpret_cast<const float4*>(xl + cb + 128);
       const float x0[8] = {l0.x, l0.y, l0.z, l0.w, h0.x, h0.y, h0.z, h0.w};
+      const float c0 = WF == 1 ? xsum[(col >> 3)] : 0.f;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) a0[r] = dot8w<WF>(w[r], col, K, x0, a0[r]);
+      for (int r = 0; r < NR; ++r) a0[r] = dot8w<WF>(w[r], col, K, x0, a0[r], c0);
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) out[r] = a0[r] + a1[r];
@@ -580,8 +642,15 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
   constexpr int UPI = NR / RPU;                   // units per warp iteration (one item)
   constexpr int SH = 32 / NR;                     // lanes per reduced row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float xr[XR][8];
+  float xr[XR][8], xcr[XR];
   if (MAXC > 0) x_regs<XR>(S, K, xr);
+#pragma unroll
+  for (int c = 0; c < XR; ++c) {  // int4: 136 x the sum of the lane's 8 inputs of chunk c
+    xcr[c] = 0.f;
+    if (WF == 1 && MAXC > 0)
+      xcr[c] = 136.f * (((xr[c][0] + xr[c][1]) + (xr[c][2] + xr[c][3])) +
+                        ((xr[c][4] + xr[c][5]) + (xr[c][6] + xr[c][7])));
+  }
   const int pc = sl.per_chunk, n_units = sl.u1 - sl.u0, n_chunks = sl.n_chunks;
   const uint32_t unit_bytes = sl.unit_bytes, row_bytes = unit_bytes / RPU;
   const bool whole = EPI != EPI_LOGITS && n_chunks <= kNS;  // waited for by prewait()
@@ -609,7 +678,7 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
       for (int r = 0; r < NR; ++r)  // rows past the stage's units reuse its last unit
         w[r] = stage + (size_t)min(t + r / RPU, cn - 1) * unit_bytes + (r % RPU) * row_bytes;
       float v[NR];
-      dotn<NR, MAXC, WF>(w, K, xr, S.xs, v);
+      dotn<NR, MAXC, WF>(w, K, xr, xcr, S.xs, S.xsum, v);
       const float sum = rows_reduce<NR>(v, lane) * rs;  // the input's RMS factor
       if constexpr (EPI == EPI_SWIGLU) {
         const float up = __shfl_down_sync(0xffffffffu, sum, SH);  // row 2k+1 onto row 2k
@@ -621,8 +690,11 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
         if (lane % SH == 0 && tl < cn) {
           const int iu = cu0 + tl, uu = sl.u0 + iu;
           if constexpr (EPI == EPI_STORE) {
+            // unit_s: the bias (and, with an adapter, the LoRA update) of the first
+            // kUnitPre units; an adapter is taken only when the slice fits unit_s
+            const bool pre = bias != nullptr || a.lora_r > 0;
             st_tagged(ty + uu,
-                      sum + (bias ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(bias[uu])) : 0.f), tag);
+                      sum + (pre ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(bias[uu])) : 0.f), tag);
           } else if constexpr (EPI == EPI_RESIDUAL) {
             const float nv = (iu < kUnitPre ? S.unit_s[iu] : word_value(__ldcg(ty + uu))) + sum;
             st_tagged(ty + uu, nv, tag);
@@ -649,6 +721,73 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
   c += n_chunks;
 }
 
+// LoRA on q_proj and v_proj ("Emberglass" README, LoRA hot-swap): with the QKV
+// phase's input in xs (gained, RMS factor rn not yet applied), t_q = A_q . x_n and
+// t_v = A_v . x_n for the halves this CTA's rows need, then the update
+// scale * B_row . t of each of its q and v rows is added to unit_s (which already
+// holds the row's bias, or 0), so the QKV epilogue adds both at once. A_q / A_v are
+// [r, K] and B_q / B_v [rows, r] bf16; the slice [u0, u1) of fused q/k/v rows has at
+// most kUnitPre rows (checked on the host). Ends with a consumer barrier.
+__device__ __noinline__ void lora_update(const MegaArgs& a, Smem& S, int l, int u0, int u1, int K,
+                                         float rn) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = a.lora_r, qd = a.nq * a.hd, vd0 = qd + a.nkv * a.hd;
+  const uint16_t* const* lp = a.lora + 4 * l;  // A_q, B_q, A_v, B_v
+  const int j0 = u0 < qd ? 0 : r, j1 = u1 > vd0 ? 2 * r : r;  // rows of [A_q; A_v] needed
+  // each warp: up to two A rows at a time, 8 chunks of 256 inputs per round of loads
+  for (int j = j0 + warp; j < j1; j += 2 * kConsumers) {
+    const int jb = j + kConsumers;
+    const uint16_t* ra = j < r ? lp[0] + (size_t)j * K : lp[2] + (size_t)(j - r) * K;
+    const uint16_t* rb = jb < j1 ? (jb < r ? lp[0] + (size_t)jb * K : lp[2] + (size_t)(jb - r) * K)
+                                 : nullptr;
+    float acc = 0.f, accb = 0.f;
+    for (int c0 = 0; c0 * 256 < K; c0 += 8) {
+      uint4 wa[8], wb[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int col = (c0 + i) * 256 + lane * 8;
+        wa[i] = col < K ? *reinterpret_cast<const uint4*>(ra + col) : make_uint4(0, 0, 0, 0);
+        wb[i] = col < K && rb ? *reinterpret_cast<const uint4*>(rb + col) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + i;
+        if (c * 256 + lane * 8 < K) {
+          const float4 lo = *reinterpret_cast<const float4*>(&S.xs[c * 256 + lane * 4]);
+          const float4 hi = *reinterpret_cast<const float4*>(&S.xs[c * 256 + 128 + lane * 4]);
+          const float x[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          acc = dot8(wa[i], x, acc);
+          accb = dot8(wb[i], x, accb);
+        }
+      }
+    }
+    acc = warp_sum(acc);
+    accb = warp_sum(accb);
+    if (lane == 0) {
+      S.lora_t[j] = acc * rn;
+      if (rb) S.lora_t[jb] = accb * rn;
+    }
+  }
+  csync();
+  for (int iu = tid; iu < u1 - u0; iu += kConsumers * 32) {
+    const int uu = u0 + iu;
+    const uint16_t* br = uu < qd ? lp[1] + (size_t)uu * r
+                       : uu >= vd0 ? lp[3] + (size_t)(uu - vd0) * r : nullptr;
+    if (br == nullptr) continue;
+    const float* t = uu < qd ? S.lora_t : S.lora_t + r;
+    float d = 0.f;
+    for (int j = 0; j < r; j += 8) {
+      float b[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) b[e] = j + e < r ? bf16f(br[j + e]) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) d = j + e < r ? fmaf(b[e], t[j + e], d) : d;
+    }
+    S.unit_s[iu] = fmaf(a.lora_scale, d, S.unit_s[iu]);
+  }
+  csync();
+}
+
 // Inputs up to 1024 wide stay in registers; wider ones are read from shared
 // memory inside the dot (keeps the kernel under its register budget). X is the
 // kernel's compile-time knowledge of the width: 1 at most 1024, 0 wider, 2 decided
@@ -668,9 +807,9 @@ __device__ __forceinline__ int slice_chunks(const Slice& sl) { return sl.n_chunk
 
 // Split-K attention of CTA b: QK-norm + RoPE of its group's queries (and of the
 // new key when its split holds pos), tiles of 32 keys from the ring, online
-// softmax, then a partial (or the final output when there is one split); split
-// 0 of a KV head polls the other splits' partials and combines them in split
-// order.
+// softmax, then a partial (or the final output when there is one split); every
+// split of a KV head then polls all splits' partials for a slice of the outputs
+// and combines them in split order.
 template <int HD, bool KB>
 __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l,
                                            int pos, const Split& sp, const LayerDev& Ld,
@@ -946,14 +1085,17 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     }
     return;
   }
-  // Key split: every split but the first publishes its partial outputs and
-  // (m, l) per head as tagged words; split 0 polls them (one L2 round trip once
-  // they are there) and combines in split order. The partial slots are reused
-  // by the next layer only after the combined output has gone through o_proj,
-  // gate/up, down and the next QKV, all of which the writers wait for.
+  // Key split: every split publishes its partial outputs and (m, l) per head as
+  // tagged words, then combines a contiguous slice of the group's GQ * HD outputs
+  // over all splits: out = sum_s f_s o_s with f_s = exp(m_s - M) / sum_s' exp(m_s' - M) l_s',
+  // M the heads' maximum, summed in split order. Each split polls the (m, l) words
+  // and the partials of its slice in one batch of loads (one L2 round trip once they
+  // are there). The partial slots are reused by the next layer only after the
+  // combined outputs have gone through o_proj, gate/up, down and the next QKV, all
+  // of which the writers wait for.
   const size_t hs = (size_t)a.splits * (HD + 2);  // words per query head
   uint64_t* mp = a.mpart + (size_t)HB * hs;
-  if (sp.s != 0) {
+  {
     uint64_t* my = mp + (size_t)sp.s * (HD + 2);
 #pragma unroll
     for (int oi = 0; oi < OUTS; ++oi) {
@@ -967,64 +1109,78 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
       st_tagged(my + (size_t)tid * hs + HD, S.ml_s[2 * tid], tag_out);
       st_tagged(my + (size_t)tid * hs + HD + 1, S.ml_s[2 * tid + 1], tag_out);
     }
-    return;
   }
-  const int ns = sp.nsplit;
+  const int ns = sp.nsplit, n_out = GQ * HD;
+  const int o0 = (int)((uint32_t)n_out * sp.s / ns), o1 = (int)((uint32_t)n_out * (sp.s + 1) / ns);
+  const int nw = (o1 - o0) * ns;  // partial words of this split's slice
+  csync();  // every warp has folded its last pass out of xs and pml_s
+  // (m, l) of every split and head -> pml_s[2 (h ns + s)]
   for (int i = tid; i < GQ * ns; i += kNT) {
     const int h = i / ns, s2 = i % ns;
-    float m = S.ml_s[2 * h], lsum = S.ml_s[2 * h + 1];
-    if (s2 != 0) {
-      const uint64_t* src = mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + HD;
-      uint64_t w0 = 0, w1 = 0;
-      uint64_t t0 = 0;
-      for (uint32_t n = 1; !abort; ++n) {
-        ld_words2(src, w0, w1);
-        if (word_tag(w0) == tag_out && word_tag(w1) == tag_out) break;
-        poll_bound(a, n, t0, abort);
-      }
-      m = word_value(w0);
-      lsum = word_value(w1);
+    const uint64_t* src = mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + HD;
+    uint64_t w0 = 0, w1 = 0, t0 = 0;
+    for (uint32_t n = 1; !abort; ++n) {
+      ld_words2(src, w0, w1);
+      if (word_tag(w0) == tag_out && word_tag(w1) == tag_out) break;
+      poll_bound(a, n, t0, abort);
     }
-    S.pml_s[2 * i] = m;
-    S.pml_s[2 * i + 1] = lsum;
+    S.pml_s[2 * i] = word_value(w0);
+    S.pml_s[2 * i + 1] = word_value(w1);
   }
   abort = csync_or(abort);
+  // per head: f_s in place of m_s
+  if (tid < GQ) {
+    float* pm = S.pml_s + 2 * tid * ns;
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pm[2 * s2]);
+    float den = 0.f;
+    for (int s2 = 0; s2 < ns; ++s2) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
+    const float inv = 1.0f / den;
+    for (int s2 = 0; s2 < ns; ++s2) pm[2 * s2] = expf(pm[2 * s2] - M) * inv;
+  }
+  csync();
+  // the slice's partials, weighted, into xs[s n_o + (o - o0)] (consecutive threads read
+  // consecutive outputs of one split); 8 polled loads per thread per round
+  const int n_o = o1 - o0;
+  float* wsum = S.xs;
+  for (int base = 0; base < nw; base += 8 * kNT) {
+    uint64_t w[8];
+    unsigned pend = 0;
 #pragma unroll
-  for (int oi = 0; oi < OUTS; ++oi) {
-    const int idx = tid + oi * kNT;
-    if (idx < GQ * HD) {
-      const int h = idx / HD, d = idx % HD;
-      const float* pm = S.pml_s + 2 * h * ns;
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pm[2 * s2]);
-      float den = 0.f;
-      for (int s2 = 0; s2 < ns; ++s2) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
-      const uint64_t* po = mp + (size_t)h * hs + d;
-      float num = expf(pm[0] - M) * oacc[oi];
-      for (int s0 = 1; s0 < ns; s0 += 8) {  // the others' outputs, 8 polled loads at a time
-        uint64_t w[8];
-        unsigned pend = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          w[j] = 0;
-          if (s0 + j < ns) pend |= 1u << j;
-        }
-        uint64_t t0 = 0;
-        for (uint32_t n = 1; pend && !abort; ++n) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if ((pend >> j) & 1u) w[j] = ld_word(po + (size_t)(s0 + j) * (HD + 2));
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (((pend >> j) & 1u) && word_tag(w[j]) == tag_out) pend &= ~(1u << j);
-          if (pend) poll_bound(a, n, t0, abort);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (s0 + j < ns) num = fmaf(expf(pm[2 * (s0 + j)] - M), word_value(w[j]), num);
-      }
-      st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, num / den, tag_out);
+    for (int j = 0; j < 8; ++j) {
+      w[j] = 0;
+      if (base + tid + j * kNT < nw) pend |= 1u << j;
     }
+    auto word_at = [&](int i) {
+      const int s2 = i / n_o, o = o0 + i % n_o, h = o / HD, d = o % HD;
+      return mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + d;
+    };
+    uint64_t t0 = 0;
+    for (uint32_t n = 1; pend && !abort; ++n) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if ((pend >> j) & 1u) w[j] = ld_word(word_at(base + tid + j * kNT));
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (((pend >> j) & 1u) && word_tag(w[j]) == tag_out) pend &= ~(1u << j);
+      if (pend) poll_bound(a, n, t0, abort);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + tid + j * kNT;
+      if (i < nw) {
+        const int s2 = i / n_o, o = o0 + i % n_o;
+        wsum[i] = S.pml_s[2 * ((o / HD) * ns + s2)] * word_value(w[j]);
+      }
+    }
+  }
+  abort = csync_or(abort);
+  for (int o = o0 + tid; o < o1; o += kNT) {
+    const float* v = wsum + (o - o0);
+    float acc = 0.f;
+    for (int s2 = 0; s2 < ns; ++s2) acc += v[(size_t)s2 * n_o];
+    const int h = o / HD, d = o % HD;
+    st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, acc, tag_out);
   }
 }
 
@@ -1185,6 +1341,8 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       const float rn = load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
                                   Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr,
                                   min(qs.u1 - qs.u0, kUnitPre), abort);
+      if (a.lora_r > 0 && (qs.u0 < qd || qs.u1 > qd + a.nkv * a.hd))
+        lora_update(a, S, l, qs.u0, qs.u1, a.H, rn);
       gemv<EPI_STORE, XH, kNrQkv, WF>(a, ring, S, c, qs, a.H, rn, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
     }
     // attention of this CTA's (kv head, key split)
@@ -1261,22 +1419,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mega_kernel(const MegaArgs
 
 namespace QW_MEGA_NS {
 
-bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers) {
+bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers, int wfmt) {
+  // every unit a producer copies fits one ring stage: a fused q/k/v, o_proj, down or
+  // LM-head row, or an interleaved gate/up row pair
+  const int gran = wfmt == 1 ? 128 : wfmt == 2 ? 32 : 8;  // inputs per scale group
   return H <= kMaxC * 256 && I <= kMaxC * 256 && qd <= kMaxC * 256 && (hd == 64 || hd == 128) &&
-         H % 8 == 0 && I % 8 == 0 && qd % 8 == 0 && n_layers >= 1 &&
-         gq >= 1 && gq <= kGQ && (uint32_t)H * 4 <= kStage && (uint32_t)I * 2 <= kStage &&
-         (uint32_t)qd * 2 <= kStage;
+         H % gran == 0 && I % gran == 0 && qd % gran == 0 && n_layers >= 1 && gq >= 1 &&
+         gq <= kGQ && wfmt >= 0 && wfmt <= 2 && 2 * row_bytes_fmt(wfmt, H) <= kStage &&
+         row_bytes_fmt(wfmt, I) <= kStage && row_bytes_fmt(wfmt, qd) <= kStage &&
+         (QW_MEGA_BIG || wfmt != 1);
 }
 
 static_assert(offsetof(Smem, xs) % 16 == 0, "float4 stores into xs need 16-byte alignment");
 static_assert(2 * kGQ * kPass * kTK <= 2 * kGQ * 160, "an attention pass's scores fit in pml_s");
+static_assert((size_t)kNS * kStage + sizeof(Smem) <= 227 * 1024, "ring and state fit a CTA");
 size_t mega_smem_bytes() { return (size_t)kNS * kStage + sizeof(Smem); }
 
-// The kernel for a shape: the Qwen3-0.6B class (head dim 128, hidden <= 1024, q
-// and intermediate wider) gets its own instantiation; other shapes the generic one.
-// [shape class][cache format][weight format]: the Qwen3-0.6B class (head dim 128,
-// hidden <= 1024, q and intermediate wider) and the generic instantiation; f32 or bf16
-// cache; bf16 or Q8_0 weights (Q8_0 with the f32 cache only).
+#if QW_MEGA_BIG
+// Wide inputs and int4 weights: [weight format bf16 / int4 / Q8_0][cache f32 / bf16],
+// generic shape class, plus the Qwen2.5-3B class (head dim 128, hidden, q and
+// intermediate all wider than 1024) with int4 weights and the f32 cache.
+constexpr int kMegaCount = 7;
+static const void* const kMegaFns[kMegaCount] = {
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, false, 0>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, true, 0>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, false, 1>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, true, 1>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, false, 2>),
+    reinterpret_cast<const void*>(decode_mega_kernel<0, 2, 2, 2, true, 2>),
+    reinterpret_cast<const void*>(decode_mega_kernel<128, 0, 0, 0, false, 1>)};
+
+static const void* mega_kernel_for(const MegaArgs& a) {
+  if (a.wfmt == 1 && !a.kv_bf16 && a.hd == 128 && a.H > 1024 && a.nq * a.hd > 1024 && a.I > 1024)
+    return kMegaFns[6];
+  return kMegaFns[a.wfmt * 2 + (a.kv_bf16 ? 1 : 0)];
+}
+#else
+// [weight format bf16 / Q8_0][cache f32 / bf16][shape class]: the Qwen3-0.6B class
+// (head dim 128, hidden <= 1024, q and intermediate wider) and the generic
+// instantiation (Q8_0 with the f32 cache only).
 constexpr int kMegaCount = 6;
 static const void* const kMegaFns[kMegaCount] = {
     reinterpret_cast<const void*>(decode_mega_kernel<128, 1, 0, 0, false, 0>),
@@ -1291,6 +1472,7 @@ static const void* mega_kernel_for(const MegaArgs& a) {
   if (a.hd == 128 && a.H <= 1024 && a.nq * a.hd > 1024 && a.I > 1024) return kMegaFns[fmt];
   return kMegaFns[fmt + 1];
 }
+#endif
 
 cudaError_t set_mega_attributes() {
   const void* const* fns = kMegaFns;

@@ -68,6 +68,7 @@ cudaError_t ensure_attributes(int dev) {
   if (e == cudaSuccess) e = set_sample_attributes();
   if (e == cudaSuccess) e = mega::set_mega_attributes();
   if (e == cudaSuccess) e = mega_wide::set_mega_attributes();
+  if (e == cudaSuccess) e = mega_big::set_mega_attributes();
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attrs_set[dev] = true;
   return e;
 }
@@ -163,6 +164,11 @@ struct qw_handle {
   bool use_mega = false;
   bool mega_ok = false;
   bool mega_wide = false;  // the recorded step uses the 11-warp build (long contexts)
+  bool mega_big = false;   // the shape takes the wide-input / int4 build at every position
+  bool mega_lora_ok = false;  // a CTA's fused q/k/v slice fits the kernel's LoRA update
+  int path_pref = 0;          // the decode path asked for (qw_set_decode_path)
+  const uint16_t** d_lora = nullptr;  // device [L][4] LoRA pointers for the persistent kernel
+  std::vector<const uint16_t*> lora_tab;  // their host copy
   LayerDev* d_layers = nullptr;
   // the persistent kernel's activations as tagged words, and its launch epoch
   uint64_t* mx = nullptr;
@@ -271,14 +277,31 @@ static int alloc_state(qw_handle* h) {
   const size_t qkv_rows = (size_t)(c.n_q_heads + 2 * c.n_kv_heads) * hd;
   h->nsplit_max = std::max(1, h->num_sms / c.n_kv_heads);
   // the persistent kernel takes bf16 weights, and Q8_0 weights with the f32 cache
-  h->mega_ok = (c.weight_format == QW_WEIGHTS_BF16 ||
-                (c.weight_format == QW_WEIGHTS_Q8_0 && c.kv_format == QW_KV_F32)) &&
-               mega::mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim,
-                                    c.head_dim, c.n_q_heads / c.n_kv_heads, c.n_layers) &&
-               mega_wide::mega_supported(c.hidden, c.intermediate, c.n_q_heads * c.head_dim,
-                                         c.head_dim, c.n_q_heads / c.n_kv_heads, c.n_layers) &&
-               (int64_t)c.vocab * h->num_sms < (int64_t)1 << 31;  // 32-bit slice arithmetic
+  {
+    // bf16, or Q8_0 with the f32 cache, at inputs up to 3072 wide: the 7- and 11-warp
+    // builds; wider shapes, int4 weights with an untied int4 head, and Q8_0 with the
+    // bf16 cache: the wide-input build
+    const int wf = c.weight_format == QW_WEIGHTS_INT4_G128 ? 1
+                 : c.weight_format == QW_WEIGHTS_Q8_0 ? 2 : 0;
+    const int qd = c.n_q_heads * c.head_dim, gq = c.n_q_heads / c.n_kv_heads;
+    const bool slices_ok = (int64_t)c.vocab * h->num_sms < (int64_t)1 << 31;  // 32-bit slices
+    const bool small = (wf == 0 || (wf == 2 && c.kv_format == QW_KV_F32)) &&
+                       mega::mega_supported(c.hidden, c.intermediate, qd, c.head_dim, gq,
+                                            c.n_layers, wf) &&
+                       mega_wide::mega_supported(c.hidden, c.intermediate, qd, c.head_dim, gq,
+                                                 c.n_layers, wf);
+    const bool big = !small && (wf != 1 || !c.tie_word_embeddings) &&
+                     mega_big::mega_supported(c.hidden, c.intermediate, qd, c.head_dim, gq,
+                                              c.n_layers, wf);
+    h->mega_ok = slices_ok && (small || big);
+    h->mega_big = slices_ok && big;
+  }
   h->use_mega = h->mega_ok;
+  {
+    const int grid = h->nsplit_max * c.n_kv_heads;
+    const int rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+    h->mega_lora_ok = h->mega_ok && (rows + grid - 1) / grid <= kMegaUnitPre;
+  }
   h->wfmt = c.weight_format == QW_WEIGHTS_INT4_G128 ? 1 : c.weight_format == QW_WEIGHTS_Q8_0 ? 2 : 0;
   h->lm_fmt = h->wfmt == 2 ? 2 : (h->wfmt == 1 && !c.tie_word_embeddings ? 1 : 0);
   h->lm_grid = std::min({c.vocab, h->num_sms, 1024});
@@ -304,6 +327,7 @@ static int alloc_state(qw_handle* h) {
       {(void**)&h->blk_val, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->blk_idx, (size_t)std::max(h->lm_grid, h->num_sms) * 4},
       {(void**)&h->am_counter, 4},
+      {(void**)&h->d_lora, (size_t)L * 4 * sizeof(void*)},
       {(void**)&h->d_pos, 4},
       {(void**)&h->d_next_token, 4},
       {(void**)&h->d_argmax, 4},
@@ -712,7 +736,7 @@ static MegaArgs mega_args(qw_handle* h) {
   m.k_cache = h->k_cache;
   m.v_cache = h->v_cache;
   m.kv_bf16 = h->kv_bf16 ? 1 : 0;
-  m.wfmt = h->wfmt == 2 ? 2 : 0;
+  m.wfmt = h->wfmt;
   m.cap = c.max_ctx;
   m.rope = h->rope;
   m.x = h->mx;
@@ -737,6 +761,9 @@ static MegaArgs mega_args(qw_handle* h) {
   m.cap_emb = h->capture_on ? h->cap_emb : nullptr;
   m.cap_blk0 = h->capture_on ? h->cap_blk0 : nullptr;
   m.cap_final = h->capture_on ? h->cap_final : nullptr;
+  m.lora = h->lora_active ? h->d_lora : nullptr;
+  m.lora_r = h->lora_active ? h->lora_rank : 0;
+  m.lora_scale = h->lora_scale;
   m.err = h->d_err;
   m.wait_ns = h->wait_ns;
   return m;
@@ -745,8 +772,9 @@ static MegaArgs mega_args(qw_handle* h) {
 // Launch one step's kernels on stream s (recorded into the graph).
 static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
   if (h->use_mega)
-    return (h->mega_wide ? mega_wide::launch_mega : mega::launch_mega)(
-        mega_args(h), h->nsplit_max * h->cfg.n_kv_heads, s);
+    return (h->mega_big    ? mega_big::launch_mega
+            : h->mega_wide ? mega_wide::launch_mega
+                           : mega::launch_mega)(mega_args(h), h->nsplit_max * h->cfg.n_kv_heads, s);
   const qw_config& c = h->cfg;
   const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
   const int qd = c.n_q_heads * hd, kd = c.n_kv_heads * hd;
@@ -920,7 +948,8 @@ static int ensure_graph_once(qw_handle* h) {
     if (kp.func == embed_kernel_fn()) {
       bytes = sizeof(EmbedArgs);
       off = offsetof(EmbedArgs, tok);
-    } else if (mega::is_mega_kernel(kp.func) || mega_wide::is_mega_kernel(kp.func)) {
+    } else if (mega::is_mega_kernel(kp.func) || mega_wide::is_mega_kernel(kp.func) ||
+               mega_big::is_mega_kernel(kp.func)) {
       bytes = sizeof(MegaArgs);
       off = offsetof(MegaArgs, tok);
     } else {
@@ -978,7 +1007,7 @@ static constexpr int kMegaWideFrom = 1536;
 static int run_steps(qw_handle* h, int n, const int32_t* tokens, int first) {
   int last = -2;
   for (int i = 0; i < n; ++i) {
-    const bool wide = h->use_mega && h->pos + i >= kMegaWideFrom;
+    const bool wide = h->use_mega && !h->mega_big && h->pos + i >= kMegaWideFrom;
     if (wide != h->mega_wide) {
       h->mega_wide = wide;
       h->graph_dirty = true;
@@ -1229,7 +1258,9 @@ extern "C" int qw_set_lora(qw_handle* h, const qw_lora* lora) {
     h->lora_qb.clear();
     h->lora_va.clear();
     h->lora_vb.clear();
-    if (h->mega_ok) h->use_mega = true;
+    const bool mega = h->path_pref == 0 && h->mega_ok;
+    if (mega != h->use_mega) h->graph_dirty = true;
+    h->use_mega = mega;
     return QW_OK;
   }
   if (lora->struct_size != sizeof(qw_lora)) QW_FAIL(h, QW_ERR_ABI, "qw_set_lora: struct_size mismatch");
@@ -1257,7 +1288,22 @@ extern "C" int qw_set_lora(qw_handle* h, const qw_lora* lora) {
   h->lora_rank = lora->rank;
   h->lora_scale = lora->alpha / (float)lora->rank;
   h->lora_active = true;
-  h->use_mega = false;  // the LoRA branch runs on the multi-kernel path
+  h->lora_tab.resize((size_t)L * 4);
+  for (int l = 0; l < L; ++l) {
+    h->lora_tab[4 * l + 0] = h->lora_qa[l];
+    h->lora_tab[4 * l + 1] = h->lora_qb[l];
+    h->lora_tab[4 * l + 2] = h->lora_va[l];
+    h->lora_tab[4 * l + 3] = h->lora_vb[l];
+  }
+  {
+    DeviceGuard dg(h->device);
+    QW_CUDA(h, cudaMemcpyAsync(h->d_lora, h->lora_tab.data(), h->lora_tab.size() * sizeof(void*),
+                               cudaMemcpyHostToDevice, h->stream));
+    QW_CUDA(h, cudaStreamSynchronize(h->stream));
+  }
+  // the persistent kernel runs the adapter when a CTA's q/k/v rows fit its update;
+  // otherwise the multi-kernel graph does
+  h->use_mega = h->path_pref == 0 && h->mega_ok && h->mega_lora_ok;
   h->graph_dirty = true;
   return QW_OK;
 }
@@ -1615,7 +1661,8 @@ extern "C" int qw_gemm_bf16(const uint16_t* a_hi, const uint16_t* a_lo, const ui
 extern "C" int qw_set_decode_path(qw_handle* h, int32_t path) {
   if (!h) QW_FAIL(h, QW_ERR_ARG, "qw_set_decode_path: null handle");
   if (path != 0 && path != 1) QW_FAIL(h, QW_ERR_ARG, "qw_set_decode_path: path must be 0 or 1");
-  const bool mega = path == 0 && h->mega_ok && !h->lora_active;
+  h->path_pref = path;
+  const bool mega = path == 0 && h->mega_ok && (!h->lora_active || h->mega_lora_ok);
   if (mega != h->use_mega) h->graph_dirty = true;
   h->use_mega = mega;
   return QW_OK;

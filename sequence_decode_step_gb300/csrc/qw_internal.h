@@ -249,7 +249,8 @@ struct MegaArgs {
   void* k_cache;           // [L][nkv][cap][hd]: f32, or bf16 bits when kv_bf16
   void* v_cache;
   int kv_bf16;
-  int wfmt;                // weight rows (projections and LM head): 0 bf16, 2 Q8_0
+  int wfmt;                // weight rows (projections and LM head): 0 bf16, 1 int4 g128
+                           // (the mega_big build), 2 Q8_0
   int cap;
   const float2* rope;
   // activations as tagged words (f32 value low, phase tag high)
@@ -269,23 +270,31 @@ struct MegaArgs {
   float* cap_emb;          // capture rows or nullptr
   float* cap_blk0;
   float* cap_final;
+  // LoRA on q_proj and v_proj: device array [L][4] of A_q, B_q, A_v, B_v (bf16 [r, H],
+  // [q rows, r], [r, H], [v rows, r]); lora_r = 0 without an adapter
+  const uint16_t* const* lora;
+  int lora_r;
+  float lora_scale;
   int* err;
   uint64_t wait_ns;
 };
-// Two builds of the kernel: mega (7 consumer warps) and mega_wide (11).
-namespace mega {
-bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers);
-size_t mega_smem_bytes();
-cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);
-cudaError_t set_mega_attributes();
-bool is_mega_kernel(const void* fn);  // one of this build's kernel instantiations
-}  // namespace mega
-namespace mega_wide {
-bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers);
-size_t mega_smem_bytes();
-cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);
-cudaError_t set_mega_attributes();
-bool is_mega_kernel(const void* fn);
-}  // namespace mega_wide
+// Units of a phase whose epilogue values the persistent kernel prefetches per CTA; a
+// LoRA adapter runs on that kernel only when a CTA's fused q/k/v slice fits.
+constexpr int kMegaUnitPre = 64;
+// Three builds of the kernel: mega (7 consumer warps) and mega_wide (11) for bf16 and
+// Q8_0 weights with inputs up to 3072 wide; mega_big (11 warps, inputs up to 11264
+// wide, one ring stage fewer) for wider shapes and int4 g128 weights.
+#define QW_MEGA_BUILD_DECL(NS)                                                          \
+  namespace NS {                                                                        \
+  bool mega_supported(int H, int I, int qd, int hd, int gq, int n_layers, int wfmt);   \
+  size_t mega_smem_bytes();                                                             \
+  cudaError_t launch_mega(const MegaArgs& a, int grid, cudaStream_t s);                 \
+  cudaError_t set_mega_attributes();                                                    \
+  bool is_mega_kernel(const void* fn); /* one of this build's kernel instantiations */ \
+  }
+QW_MEGA_BUILD_DECL(mega)
+QW_MEGA_BUILD_DECL(mega_wide)
+QW_MEGA_BUILD_DECL(mega_big)
+#undef QW_MEGA_BUILD_DECL
 
 }  // namespace qw

@@ -196,6 +196,27 @@ __device__ __forceinline__ float dot8_i4(uint32_t w, const float (&x)[8], float 
   return fmaf(p, s, acc);
 }
 
+// The same 8 nibbles as floats 128 + n (n = q + 8 in the mantissa of 128, one byte
+// permute, exact) dotted with 8 floats: sum (128 + n_i) x_i. No subtraction per
+// weight; the caller removes 136 sum x_i, which leaves sum q_i x_i. The offset costs
+// about 5 of the 24 mantissa bits of a 128-input group's sum (its terms are ~136 |x|
+// against a result of ~5 sqrt(128) |x|), a relative error near 1e-6.
+__device__ __forceinline__ float b128f(uint32_t v, uint32_t b) {
+  return __uint_as_float(__byte_perm(v, 0x43000000u, 0x7044u | (b << 8)));
+}
+__device__ __forceinline__ float dot8_i4_biased(uint32_t w, const float (&x)[8]) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+  float p = b128f(lo, 0) * x[0];
+  p = fmaf(b128f(hi, 0), x[1], p);
+  p = fmaf(b128f(lo, 1), x[2], p);
+  p = fmaf(b128f(hi, 1), x[3], p);
+  p = fmaf(b128f(lo, 2), x[4], p);
+  p = fmaf(b128f(hi, 2), x[5], p);
+  p = fmaf(b128f(lo, 3), x[6], p);
+  p = fmaf(b128f(hi, 3), x[7], p);
+  return p;
+}
+
 // 8 int8 weights (two 32-bit words, element i in byte i % 4 of word i / 4, two's
 // complement) dotted with 8 floats, times the block scale. A byte is flipped to
 // b ^ 0x80 = q + 128, placed in the mantissa of 2^23 (one byte permute), and

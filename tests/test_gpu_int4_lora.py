@@ -30,7 +30,7 @@ def _lora(d):
 
 
 def _run(m, o, tok, steps, check_ids=True):
-    """Teacher-forced steps; returns the GPU logits of every step."""
+    """Teacher-forced steps; returns the GPU logits of every step and the next token."""
     out = []
     for i in range(steps):
         want = o.decode_step(tok)["logits"]
@@ -40,16 +40,23 @@ def _run(m, o, tok, steps, check_ids=True):
             assert got_id == R.greedy_argmax(want)
         out.append(got)
         tok = R.greedy_argmax(want)
-    return out
+    return out, tok
 
 
-def test_tiny_int4_decode():
-    wl = W.Workload("t4", TINY_INT4, seed=5, prompt_len=8, decode_steps=16, max_ctx=64)
+# 0: the persistent kernel (its wide-input build takes int4 weights), 1: the graph
+@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("shape", [TINY_INT4, TINY_INT4.replace(kv_format="bf16"),
+                                   TINY_INT4.replace(intermediate=3584)],
+                         ids=["f32kv", "bf16kv", "wide"])
+def test_tiny_int4_decode(shape, path):
+    wl = W.Workload("t4", shape, seed=5, prompt_len=8, decode_steps=16, max_ctx=64)
     d = W.draw(wl, drawn_gains=True)
     m = DeviceModel(wl.shape, d.weights, 64, max_prefill_t=0)    # prompt as sequential steps
     o = R.build_oracle(d)
     try:
-        assert B.qw_get_decode_path(m.h) == 1
+        assert B.qw_get_decode_path(m.h) == 0
+        B.qw_set_decode_path(m.h, path)
+        assert B.qw_get_decode_path(m.h) == path
         am, lg = m.prefill(d.prompt, logits=True)
         ref = o.prefill(d.prompt)["logits"]
         assert violation(lg, ref) <= 0
@@ -58,18 +65,24 @@ def test_tiny_int4_decode():
         m.close()
 
 
-@pytest.mark.parametrize("shape", [TINY_INT4, W.TINY.replace(qkv_bias=True)],
-                         ids=["int4", "bf16"])
-def test_tiny_lora_on_then_cleared(shape):
+@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("shape", [TINY_INT4, W.TINY.replace(qkv_bias=True),
+                                   W.TINY.replace(qkv_bias=False)],
+                         ids=["int4", "bf16", "bf16_nobias"])
+def test_tiny_lora_on_then_cleared(shape, path):
     wl = W.Workload("tl", shape, seed=6, prompt_len=6, decode_steps=12, max_ctx=64,
                     lora=W.LoraShape(4, 8.0))
     d = W.draw(wl, drawn_gains=True)
     m = DeviceModel(shape, d.weights, 64, max_prefill_t=64)
     fresh = DeviceModel(shape, d.weights, 64, max_prefill_t=64)
     try:
+        # 0: the persistent kernel adds the LoRA update in its QKV phase; 1: the graph
+        B.qw_set_decode_path(m.h, path)
+        B.qw_set_decode_path(fresh.h, path)
         # phase A: adapter on (prefill falls back to the sequential path; int4 prompts
         # without an adapter take the batched pass)
         m.set_lora(_lora(d), 8.0)
+        assert B.qw_get_decode_path(m.h) == path
         o = R.build_oracle(d, lora_on=True)
         am, lg = m.prefill(d.prompt, logits=True)
         ref = o.prefill(d.prompt)["logits"]
@@ -79,6 +92,7 @@ def test_tiny_lora_on_then_cleared(shape):
         _run(m, o, R.greedy_argmax(ref), wl.decode_steps)
         # phase B: cleared; same inputs as a handle that never had an adapter
         m.set_lora(None)
+        assert B.qw_get_decode_path(m.h) == path
         m.reset()
         o2 = R.build_oracle(d)
         am, lg = m.prefill(d.prompt, logits=True)
@@ -108,17 +122,26 @@ def test_qwen25_3b_int4_lora_4k():
     d.weights = {}                                            # the oracle keeps its own copies
     P = wl.kv_prefill
     try:
+        assert B.qw_get_decode_path(fresh.h) == 0     # int4 on the persistent kernel
         for l, (k, v) in enumerate(d.kv):
             m.set_kv(l, k, v)
             fresh.set_kv(l, k, v)
         m.set_pos(P)
         fresh.set_pos(P)
-        # phase A: 64 steps with the adapter
+        # phase A: 64 steps with the adapter, the last 8 on the multi-kernel graph
         m.set_lora(lora, wl.lora.alpha)
-        _run(m, o, d.start_token, wl.decode_steps)
+        assert B.qw_get_decode_path(m.h) == 0         # the adapter on the persistent kernel
+        n0 = wl.decode_steps - 8
+        tok = d.start_token
+        for path, n in ((0, n0), (1, 8)):
+            B.qw_set_decode_path(m.h, path)
+            assert B.qw_get_decode_path(m.h) == path
+            _, tok = _run(m, o, tok, n)
+        B.qw_set_decode_path(m.h, 0)
         # phase B: cleared, cache and position restored, 64 steps; bit-identical to a
         # handle that never had the adapter, and within tolerance of the oracle
         m.set_lora(None)
+        assert B.qw_get_decode_path(m.h) == 0         # back on the persistent kernel
         o.set_lora(None)
         o.reset()
         for l, (k, v) in enumerate(d.kv):

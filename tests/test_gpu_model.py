@@ -72,6 +72,8 @@ TINY_VARIANTS = {
                                          n_kv_heads=1), True),
     "tiny_hd128_gq8": (W.TINY.replace(n_q_heads=8, n_kv_heads=1, head_dim=128, hidden=512,
                                       intermediate=1280), True),
+    # an intermediate width above 3072: the persistent kernel's wide-input build
+    "tiny_wide_mlp": (W.TINY.replace(intermediate=3584), True),
 }
 
 

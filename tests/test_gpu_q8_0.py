@@ -135,5 +135,15 @@ def test_tiny_q8_0_decode(tied, path):
 
 
 @pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("shape", [W.TINY.replace(weight_format="q8_0", kv_format="bf16"),
+                                   W.TINY.replace(weight_format="q8_0", intermediate=3584)],
+                         ids=["bf16kv", "wide"])
+def test_tiny_q8_0_wide_build(shape, path):
+    # Q8_0 with the bf16 cache, and inputs wider than 3072: the persistent kernel's
+    # wide-input build
+    _decode_vs_oracle(W.Workload("tiny_q8w", shape, seed=33, prompt_len=6, max_ctx=64), 12, path)
+
+
+@pytest.mark.parametrize("path", [0, 1])
 def test_qwen3_06b_q8_0_decode(path):
     _decode_vs_oracle(W.WORKLOADS["qwen3_0.6b_q8_0_decode"], 16, path)
