@@ -270,6 +270,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict:
         extra["longctx"] = longctx_timing(torch, W, B, DeviceModel, stream)
         extra["q8_0_decode"] = q8_timing(torch, W, B, DeviceModel, stream)
         extra["prefill_int4"] = int4_prefill_timing(torch, W, B, DeviceModel, stream)
+        extra["int4_decode"] = int4_decode_timing(torch, W, B, DeviceModel, stream)
 
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
@@ -538,6 +539,64 @@ def q8_timing(torch, W, B, DeviceModel, stream) -> dict:
             "bytes_per_token": byt, "roofline_frac": byt / (us * 1e-6) / 1e9 / hbm,
             "path": "persistent kernel, int8 rows with fp16 block scales decoded in the GEMV",
             "data": "seeded device draw (torch), the workload's shapes and distributions"}
+
+
+def int4_decode_timing(torch, W, B, DeviceModel, stream) -> dict:
+    """Decode of the Qwen2.5-3B int4 g128 shape (q/k/v bias, untied int4 head) from a
+    cache pre-filled to 4096 keys, on the persistent kernel, without and with the rank-16
+    LoRA on q and v: us/token over the workload's steps and the byte roofline."""
+    wl = W.WORKLOADS["qwen2.5_3b_int4_lora"]
+    s = wl.shape
+    w = device_draw(W, torch, s, wl.seed, wl.lora)
+    lora = {k: v for k, v in w.items() if k.startswith("lora.")}
+    m = DeviceModel(s, {k: v for k, v in w.items() if not k.startswith("lora.")}, wl.max_ctx,
+                    stream=stream.cuda_stream)
+    del w
+    g = torch.Generator(device="cuda")
+    g.manual_seed(wl.seed)
+    shp = (s.n_kv_heads, wl.kv_prefill, s.head_dim)
+    for l in range(s.n_layers):  # N(0, 1) in bf16-representable f32, as the workload's prefill
+        k, v = (torch.randn(shp, generator=g, device="cuda").to(torch.bfloat16).float()
+                for _ in range(2))
+        m.set_kv(l, k, v)
+    torch.cuda.empty_cache()
+    L = B.lib()
+    per_layer = (s.hidden * s.q_dim + 2 * s.hidden * s.kv_dim + s.q_dim * s.hidden
+                 + 3 * s.hidden * s.intermediate)
+    wbytes = (s.n_layers * per_layer + s.vocab * s.hidden) * (0.5 + 2 / 128)
+    kvb = sum(kv_bytes(s, p) for p in range(wl.kv_prefill, wl.kv_prefill + wl.decode_steps))
+    r = wl.lora.rank
+    lora_bytes = s.n_layers * 2 * r * (2 * s.hidden + s.q_dim + s.kv_dim)
+    hbm = measured_peaks().get("hbm_gbs", 6800.0)
+    out = {"workload": wl.name, "positions": f"{wl.kv_prefill}..{wl.kv_prefill + wl.decode_steps - 1}",
+           "path": "persistent kernel (wide-input build), int4 nibbles decoded in the GEMV",
+           "data": "seeded device draw (torch), the workload's shapes and distributions"}
+    try:
+        for mode in ("lora_off", "lora_on"):
+            m.set_lora(lora if mode == "lora_on" else None, wl.lora.alpha)
+            path = B.qw_get_decode_path(m.h)
+            ts = []
+            for rep in range(3):
+                B.qw_set_pos(m.h, wl.kv_prefill)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                rc = L.qw_decode_step(m.h, 1, None, None)
+                for _ in range(wl.decode_steps - 1):
+                    rc |= L.qw_decode_step(m.h, -1, None, None)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if rc:
+                    raise RuntimeError(B.last_error(m.h))
+                if rep > 0:
+                    ts.append(e0.elapsed_time(e1) * 1e3 / wl.decode_steps)
+            us = sum(ts) / len(ts)
+            byt = wbytes + kvb / wl.decode_steps + (lora_bytes if mode == "lora_on" else 0)
+            out[mode] = {"us_per_token": us, "tok_per_s": 1e6 / us, "bytes_per_token": byt,
+                         "roofline_frac": byt / (us * 1e-6) / 1e9 / hbm, "decode_path": path}
+    finally:
+        m.close()
+    return out
 
 
 def int4_prefill_timing(torch, W, B, DeviceModel, stream, T: int = 1024) -> dict:

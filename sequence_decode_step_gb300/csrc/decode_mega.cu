@@ -76,7 +76,7 @@ constexpr uint32_t kStage = 32 * 1024;       // bytes per stage
 constexpr int kMaxC = QW_MEGA_MAXC;          // input vectors up to kMaxC x 256 wide
 constexpr int kTK = 32;                      // keys per attention tile (K + V = 32 KB at hd 128)
 constexpr int kGQ = 8;
-constexpr int kMinKeys = 128;               // keys per split at least (one pass)
+constexpr int kMinKeys = 64;                // keys per split at least
 // Up to this many keys a group's query heads go to separate CTAs over all keys
 // (one pass, no combine); beyond it the keys are split and combined. Measured
 // (us/token, Qwen3-0.6B shape, same box) at 145-256 keys: 652-680 with the key
@@ -1128,15 +1128,18 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     S.pml_s[2 * i + 1] = word_value(w1);
   }
   abort = csync_or(abort);
-  // per head: f_s in place of m_s
-  if (tid < GQ) {
-    float* pm = S.pml_s + 2 * tid * ns;
+  // per head (one warp each, lanes over the splits): f_s in place of m_s; the
+  // denominator is summed lane-strided, then over the lanes in a fixed order
+  for (int h = warp; h < GQ; h += kConsumers) {
+    float* pm = S.pml_s + 2 * h * ns;
     float M = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pm[2 * s2]);
+    for (int s2 = lane; s2 < ns; s2 += 32) M = fmaxf(M, pm[2 * s2]);
+    M = warp_max(M);
     float den = 0.f;
-    for (int s2 = 0; s2 < ns; ++s2) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
-    const float inv = 1.0f / den;
-    for (int s2 = 0; s2 < ns; ++s2) pm[2 * s2] = expf(pm[2 * s2] - M) * inv;
+    for (int s2 = lane; s2 < ns; s2 += 32) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
+    const float inv = 1.0f / warp_sum(den);
+    __syncwarp();
+    for (int s2 = lane; s2 < ns; s2 += 32) pm[2 * s2] = expf(pm[2 * s2] - M) * inv;
   }
   csync();
   // the slice's partials, weighted, into xs[s n_o + (o - o0)] (consecutive threads read

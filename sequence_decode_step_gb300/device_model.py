@@ -212,7 +212,8 @@ class DeviceModel:
         kd, vd = self._kv_raw(layer)
         n = k.shape[1]
         for dst, src in ((kd, k), (vd, v)):
-            t = torch.from_numpy(np.ascontiguousarray(src, dtype=np.float32))
+            t = src if isinstance(src, torch.Tensor) else \
+                torch.from_numpy(np.ascontiguousarray(src, dtype=np.float32))
             if dst.dtype == torch.int16:
                 t = t.to(torch.bfloat16).view(torch.int16)
             dst[:, :n].copy_(t)
