@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t r[16];
       tmem_ld16(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
       tmem_ld_wait();
+      tmem_regs_ready(r);
       const int col0 = n0 + c0;
       if (!ok || row >= a.M || col0 >= a.N) continue;
       float v[16];
@@ -570,13 +571,17 @@ __global__ void __launch_bounds__(192, 1)
       if (!ok) break;
       tc_fence_after();
       float sv[kFaBN];
+      {  // the row's scores: all column blocks in flight, one wait
+        uint32_t rr[kFaBN / 16][16];
 #pragma unroll
-      for (int j = 0; j < kFaBN / 16; ++j) {
-        uint32_t rr[16];
-        tmem_ld16(t_s + lrow + 16 * j, rr);
+        for (int j = 0; j < kFaBN / 16; ++j) tmem_ld16(t_s + lrow + 16 * j, rr[j]);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sv[16 * j + e] = __uint_as_float(rr[e]);
+        for (int j = 0; j < kFaBN / 16; ++j) {
+          tmem_regs_ready(rr[j]);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) sv[16 * j + e] = __uint_as_float(rr[j][e]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -618,6 +623,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t rr[16];
             tmem_ld16(t_o + lrow + d0, rr);
             tmem_ld_wait();
+            tmem_regs_ready(rr);
 #pragma unroll
             for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
             tmem_st16(t_o + lrow + d0, rr);
@@ -656,6 +662,7 @@ __global__ void __launch_bounds__(192, 1)
           uint32_t rr[16];
           tmem_ld16(t_o + lrow + d0, rr);
           tmem_ld_wait();
+          tmem_regs_ready(rr);
           uint32_t hw[8], lw[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -681,6 +688,7 @@ __global__ void __launch_bounds__(192, 1)
           uint32_t rr[16];
           tmem_ld16(t_o + lrow + d0, rr);
           tmem_ld_wait();
+          tmem_regs_ready(rr);
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
             *reinterpret_cast<float4*>(po + d0 + e) =
@@ -706,29 +714,57 @@ __global__ void __launch_bounds__(192, 1)
           den = fmaf(fast_exp2(ml.x - Mu), ml.y, den);
         }
         const float inv = 1.0f / den;
+        // 32 dims at a time, two chunks' rows per round of loads (each chunk's weight
+        // exp2(m_c - M) recomputed from its (m, l)), summed in chunk order
 #pragma unroll 1
-        for (int d0 = 0; d0 < HD; d0 += 8) {
-          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int c2 = 0; c2 < nch; ++c2) {
-            const float w = fast_exp2(__ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]).x - Mu);
-            const float* src = a.part_o + ((slot + c2) * kFaBQ + r) * HD + d0;
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(src));
-            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-            acc[0] = fmaf(w, x0.x, acc[0]);
-            acc[1] = fmaf(w, x0.y, acc[1]);
-            acc[2] = fmaf(w, x0.z, acc[2]);
-            acc[3] = fmaf(w, x0.w, acc[3]);
-            acc[4] = fmaf(w, x1.x, acc[4]);
-            acc[5] = fmaf(w, x1.y, acc[5]);
-            acc[6] = fmaf(w, x1.z, acc[6]);
-            acc[7] = fmaf(w, x1.w, acc[7]);
-          }
-          uint32_t hw[4], lw[4];
+        for (int d0 = 0; d0 < HD; d0 += 32) {
+          float acc[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split2(acc[2 * e] * inv, acc[2 * e + 1] * inv, hw[e], lw[e]);
-          if (store) {
-            *reinterpret_cast<uint4*>(oh + d0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(ol + d0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll 1
+          for (int c2 = 0; c2 < nch; c2 += 2) {
+            const bool two = c2 + 1 < nch;
+            const float2 ml0 = __ldcg(&a.part_ml[(slot + c2) * kFaBQ + r]);
+            const float2 ml1 = two ? __ldcg(&a.part_ml[(slot + c2 + 1) * kFaBQ + r])
+                                   : make_float2(-INFINITY, 0.f);
+            const float4* s0 =
+                reinterpret_cast<const float4*>(a.part_o + ((slot + c2) * kFaBQ + r) * HD + d0);
+            const float4* s1 = reinterpret_cast<const float4*>(
+                a.part_o + ((slot + c2 + (two ? 1 : 0)) * kFaBQ + r) * HD + d0);
+            float4 x0[8], x1[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              x0[q] = __ldcg(s0 + q);
+              x1[q] = two ? __ldcg(s1 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const float w0 = fast_exp2(ml0.x - Mu), w1 = two ? fast_exp2(ml1.x - Mu) : 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              acc[4 * q + 0] = fmaf(w0, x0[q].x, acc[4 * q + 0]);
+              acc[4 * q + 1] = fmaf(w0, x0[q].y, acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(w0, x0[q].z, acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(w0, x0[q].w, acc[4 * q + 3]);
+            }
+            if (two) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                acc[4 * q + 0] = fmaf(w1, x1[q].x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(w1, x1[q].y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(w1, x1[q].z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(w1, x1[q].w, acc[4 * q + 3]);
+              }
+            }
+          }
+#pragma unroll
+          for (int e8 = 0; e8 < 32; e8 += 8) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              split2(acc[e8 + 2 * e] * inv, acc[e8 + 2 * e + 1] * inv, hw[e], lw[e]);
+            if (store) {
+              *reinterpret_cast<uint4*>(oh + d0 + e8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(ol + d0 + e8) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
           }
         }
         if (warp == 2 && lane == 0) a.counters[h * a.nqb + qb] = 0;  // ready for the next launch
