@@ -131,6 +131,7 @@ struct qw_handle {
   uint16_t* pf_m_hi = nullptr;   // [Tmax, I] SwiGLU output split
   uint16_t* pf_m_lo = nullptr;
   uint16_t* pf_kvs = nullptr;    // K and V^T of the context as two-bf16 splits (attention)
+  int* pf_gemm_flags = nullptr;  // split-K hand-over per output tile of the residual GEMMs
   void* pf_attn_part = nullptr;  // partial attention outputs of query blocks cut into chunks
   CUtensorMap tm_xn_hi, tm_xn_lo, tm_o_hi, tm_o_lo, tm_m_hi, tm_m_lo;
   FaMaps tm_attn;  // attention operands: Q, K and V^T splits
@@ -345,6 +346,7 @@ static int alloc_state(qw_handle* h) {
   const size_t qd = (size_t)c.n_q_heads * hd;
   if (Tm > 0) {
     pieces.push_back({(void**)&h->pf_ids, Tm * 4});
+    pieces.push_back({(void**)&h->pf_gemm_flags, ((Tm + 127) / 128) * ((H + 127) / 128) * 4});
     pieces.push_back({(void**)&h->pf_x, Tm * H * 4});
     pieces.push_back({(void**)&h->pf_xn_hi, Tm * H * 2});
     pieces.push_back({(void**)&h->pf_xn_lo, Tm * H * 2});
@@ -394,9 +396,9 @@ static int alloc_state(qw_handle* h) {
         h->w4_dw[t] = q;
         q += H * I;
         if (!make_tmap_bf16_2d(&h->tm_qkv4[t], h->w4_qkv[t], qkv_rows, H, 256) ||
-            !make_tmap_bf16_2d(&h->tm_ow4[t], h->w4_o[t], H, qd, 64) ||
+            !make_tmap_bf16_2d(&h->tm_ow4[t], h->w4_o[t], H, qd, kResidBN) ||
             !make_tmap_bf16_2d(&h->tm_gu4[t], h->w4_gu[t], 2 * I, H, 256) ||
-            !make_tmap_bf16_2d(&h->tm_dw4[t], h->w4_dw[t], H, I, 64))
+            !make_tmap_bf16_2d(&h->tm_dw4[t], h->w4_dw[t], H, I, kResidBN))
           QW_FAIL(h, QW_ERR_CUDA, "prefill: TMA descriptor encoding failed");
       }
     }
@@ -651,9 +653,9 @@ extern "C" int qw_load_weights(qw_handle* h, const qw_weights* w) {
     for (int l = 0; l < L; ++l) {
       const LayerW& lw = h->layers[l];
       const bool ok = make_tmap_bf16_2d(&h->tm_qkv[l], lw.qkv, qd + 2 * kd, H, 256) &&
-                      make_tmap_bf16_2d(&h->tm_ow[l], lw.o, H, qd, 64) &&
+                      make_tmap_bf16_2d(&h->tm_ow[l], lw.o, H, qd, kResidBN) &&
                       make_tmap_bf16_2d(&h->tm_gu[l], lw.gateup, 2 * I, H, 256) &&
-                      make_tmap_bf16_2d(&h->tm_dw[l], lw.down, H, I, 64);
+                      make_tmap_bf16_2d(&h->tm_dw[l], lw.down, H, I, kResidBN);
       if (!ok) QW_FAIL(h, QW_ERR_CUDA, "qw_load_weights: TMA descriptor encoding failed");
     }
   }
@@ -982,6 +984,11 @@ static int finish_sync(qw_handle* h) {
   QW_CUDA(h, cudaMemsetAsync(h->attn_counters, 0,
                              (size_t)h->cfg.n_layers * h->cfg.n_kv_heads * 4, h->stream));
   QW_CUDA(h, cudaMemsetAsync(h->am_counter, 0, 4, h->stream));
+  if (h->pf_gemm_flags)
+    QW_CUDA(h, cudaMemsetAsync(h->pf_gemm_flags, 0,
+                               ((size_t)(h->cfg.max_prefill_t + 127) / 128) *
+                                   ((h->cfg.hidden + 127) / 128) * 4,
+                               h->stream));
   QW_CUDA(h, cudaStreamSynchronize(h->stream));
   if (err & ERR_TIMEOUT)
     QW_FAIL(h, QW_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up; outputs are invalid");
@@ -1121,6 +1128,10 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
     g.ldb = N / 2;
     g.cap_out = cap;
     g.cap_row0 = p0;
+    if (epi == GEPI_RESID) {  // narrow outputs (N = hidden): K split in two, fixed order
+      g.ksplit = kResidSplit;
+      g.flags = h->pf_gemm_flags;
+    }
     g.err = h->d_err;
     g.wait_ns = h->wait_ns;
     return launch_gemm(bn, epi, ahi, alo, b, b_lo, g, s);
@@ -1153,13 +1164,13 @@ static int prefill_batched(qw_handle* h, const int32_t* ids_host, int T) {
                                    c.max_prefill_t, c.max_ctx, p0, T, c.n_q_heads,
                                    c.n_kv_heads, hd, h->pf_o_hi, h->pf_o_lo, h->d_err, h->wait_ns,
                                    s));
-    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, wo, w4 ? &h->tm_ow4[1] : nullptr, H,
+    QW_CUDA(h, gemm(kResidBN, GEPI_RESID, h->tm_o_hi, h->tm_o_lo, wo, w4 ? &h->tm_ow4[1] : nullptr, H,
                     qd, h->pf_x, nullptr, nullptr, nullptr, nullptr));
     QW_CUDA(h, launch_rmsnorm_rows(h->pf_x, T, H, lw.mlp_norm, c.eps, h->pf_xn_hi, h->pf_xn_lo,
                                    nullptr, 0, s));
     QW_CUDA(h, gemm(256, GEPI_SWIGLU, h->tm_xn_hi, h->tm_xn_lo, wg, w4 ? &h->tm_gu4[1] : nullptr,
                     2 * I, H, nullptr, nullptr, h->pf_m_hi, h->pf_m_lo, nullptr));
-    QW_CUDA(h, gemm(64, GEPI_RESID, h->tm_m_hi, h->tm_m_lo, wd, w4 ? &h->tm_dw4[1] : nullptr, H, I,
+    QW_CUDA(h, gemm(kResidBN, GEPI_RESID, h->tm_m_hi, h->tm_m_lo, wd, w4 ? &h->tm_dw4[1] : nullptr, H, I,
                     h->pf_x, nullptr,
                     nullptr, nullptr, (h->capture_on && l == 0) ? h->cap_blk0 : nullptr));
   }

@@ -13,6 +13,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <math.h>
 #include <stdint.h>
 
@@ -51,7 +53,11 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.y * GBM, n0 = blockIdx.x * BN;
-  const int KT = (a.K + GBK - 1) / GBK;
+  // this CTA's k-tiles [kt_a, kt_b): all of K, or split blockIdx.z of a split-K launch
+  const int KT_all = (a.K + GBK - 1) / GBK, ks = EPI == GEPI_RESID && a.ksplit > 1 ? a.ksplit : 1;
+  const int split = ks > 1 ? (int)blockIdx.z : 0;
+  const int kt_a = split * KT_all / ks, kt_b = (split + 1) * KT_all / ks;
+  const int KT = kt_b - kt_a;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -79,12 +85,13 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       uint8_t* st = smem + (size_t)s * stage_bytes;
+      const int kx = (kt_a + kt) * GBK;
       mbar_expect_tx(&full[s], stage_bytes);
-      tma_load_2d(st, &ta_hi, kt * GBK, m0, &full[s]);
-      if (a.a_split == 2) tma_load_2d(st + kATileBytes, &ta_lo, kt * GBK, m0, &full[s]);
-      tma_load_2d(st + a.a_split * kATileBytes, &tb, kt * GBK, n0, &full[s]);
+      tma_load_2d(st, &ta_hi, kx, m0, &full[s]);
+      if (a.a_split == 2) tma_load_2d(st + kATileBytes, &ta_lo, kx, m0, &full[s]);
+      tma_load_2d(st + a.a_split * kATileBytes, &tb, kx, n0, &full[s]);
       if (a.b_split == 2)
-        tma_load_2d(st + a.a_split * kATileBytes + kBTileBytes, &tb_lo, kt * GBK, n0, &full[s]);
+        tma_load_2d(st + a.a_split * kATileBytes + kBTileBytes, &tb_lo, kx, n0, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -115,11 +122,32 @@ __global__ void __launch_bounds__(192, 1)
     mbar_wait(accf, 0, kDrainNs);
   } else if (warp >= 2) {
     // ---- epilogue: warp w reads TMEM lanes [32 (w % 4), +32) = rows of the tile
-    const bool ok = mbar_wait(accf, 0, a.wait_ns);
+    bool ok = mbar_wait(accf, 0, a.wait_ns);
     if (!ok && lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+    int* flag = ks > 1 ? a.flags + blockIdx.y * gridDim.x + blockIdx.x : nullptr;
+    if (flag != nullptr && split > 0) {  // split s adds after split s - 1 (a fixed order)
+      if (threadIdx.x == 64) {
+        bool got = false;
+        uint64_t t0 = 0;
+        for (uint32_t n = 1; a.wait_ns != 0; ++n) {
+          int f;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(flag) : "memory");
+          if (f == split) { got = true; break; }
+          if ((n & 15u) == 0) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > a.wait_ns || (*reinterpret_cast<volatile int*>(a.err) & ERR_TIMEOUT)) break;
+          }
+        }
+        if (!got) atomicOr(a.err, ERR_TIMEOUT);
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+      ok = ok && (*reinterpret_cast<volatile int*>(a.err) & ERR_TIMEOUT) == 0;
+    }
     tc_fence_after();
     const int q = warp & 3;
     const int row = m0 + q * 32 + lane;
+    float* const cap_out = split == ks - 1 ? a.cap_out : nullptr;  // the final rows only
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       uint32_t r[16];
@@ -160,22 +188,22 @@ __global__ void __launch_bounds__(192, 1)
         if (vec) {
           float4 cur[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) cur[j] = *reinterpret_cast<const float4*>(o + 4 * j);
+          for (int j = 0; j < 4; ++j) cur[j] = __ldcg(reinterpret_cast<const float4*>(o + 4 * j));
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float4 n4 = make_float4(cur[j].x + v[4 * j], cur[j].y + v[4 * j + 1],
                                           cur[j].z + v[4 * j + 2], cur[j].w + v[4 * j + 3]);
             *reinterpret_cast<float4*>(o + 4 * j) = n4;
-            if (a.cap_out)
-              *reinterpret_cast<float4*>(a.cap_out + (size_t)(a.cap_row0 + row) * a.ldo + col0 + 4 * j) = n4;
+            if (cap_out)
+              *reinterpret_cast<float4*>(cap_out + (size_t)(a.cap_row0 + row) * a.ldo + col0 + 4 * j) = n4;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (j < nv) {
-              const float nvl = o[j] + v[j];
+              const float nvl = __ldcg(o + j) + v[j];
               o[j] = nvl;
-              if (a.cap_out) a.cap_out[(size_t)(a.cap_row0 + row) * a.ldo + col0 + j] = nvl;
+              if (cap_out) cap_out[(size_t)(a.cap_row0 + row) * a.ldo + col0 + j] = nvl;
             }
         }
       } else if (vec) {  // GEPI_SWIGLU, 8 units as one 16-byte store per half
@@ -204,6 +232,15 @@ __global__ void __launch_bounds__(192, 1)
             a.out_lo[(size_t)row * a.ldb + u0 + j] = lo;
           }
       }
+    }
+  }
+  if (ks > 1 && warp >= 2) {  // this split's sums are in out: hand the tile to the next split
+    __threadfence();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (threadIdx.x == 64) {
+      int* flag = a.flags + blockIdx.y * gridDim.x + blockIdx.x;
+      const int nxt = split + 1 == ks ? 0 : split + 1;  // the last split leaves it at rest
+      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(nxt) : "memory");
     }
   }
   tc_fence_before();
@@ -1025,7 +1062,8 @@ template <int BN, int EPI>
 static cudaError_t launch_gemm_t(const CUtensorMap& a_hi, const CUtensorMap& a_lo,
                                  const CUtensorMap& b, const CUtensorMap& b_lo, const GemmArgs& g,
                                  cudaStream_t s) {
-  const dim3 grid((g.N + BN - 1) / BN, (g.M + GBM - 1) / GBM);
+  // split-K: split index slowest, so every split's CTAs come after the previous split's
+  const dim3 grid((g.N + BN - 1) / BN, (g.M + GBM - 1) / GBM, g.ksplit);
   gemm_tc_kernel<BN, EPI><<<grid, 192, gemm_smem(BN, g.a_split, g.b_split, g.n_stages), s>>>(
       a_hi, a_lo, b, b_lo, g);
   return cudaGetLastError();
@@ -1051,6 +1089,8 @@ cudaError_t launch_gemm(int bn, int epi, const CUtensorMap& a_hi, const CUtensor
   if (epi == GEPI_SWIGLU && (g.N % 2)) return cudaErrorInvalidValue;
   g.b_split = b_lo ? 2 : 1;
   const CUtensorMap& bl = b_lo ? *b_lo : b;
+  const int kt_all = (g.K + GBK - 1) / GBK;  // every split gets at least one k-tile
+  g.ksplit = epi == GEPI_RESID && g.flags != nullptr ? std::max(1, std::min(g.ksplit, kt_all)) : 1;
   g.n_stages = gemm_stages(bn, g.a_split, g.b_split);
   if (bn == 64) return launch_gemm_bn<64>(epi, a_hi, a_lo, b, bl, g, s);
   if (bn == 128) return launch_gemm_bn<128>(epi, a_hi, a_lo, b, bl, g, s);

@@ -155,9 +155,17 @@ struct GemmArgs {
   int ldb;
   float* cap_out;          // RESID: also write the updated rows at [cap_row0 + m] (or nullptr)
   int cap_row0;
+  // RESID only: K split over ksplit CTAs per output tile (grid z), whose epilogues add
+  // their partial sums to out in split order; flags: one int per output tile, 0 at rest
+  int ksplit;
+  int* flags;
   int* err;
   uint64_t wait_ns;
 };
+// The residual GEMMs of a prefill (o_proj, down: N = hidden) run with 128-column
+// tiles and K split in two, so that twice as many CTAs share the narrow output.
+constexpr int kResidBN = 128;
+constexpr int kResidSplit = 2;
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_rows);
 // b_lo: the weight's lo term (nullptr for exact bf16 weights); with it each product is
