@@ -233,14 +233,17 @@ int qw_capture_size(qw_handle* h, int32_t which, size_t* n_floats);
 int qw_get_capture(qw_handle* h, int32_t which, float* out_host, size_t n_floats);
 
 /* Decode path (test and benchmarking hook). 0: one persistent cooperative kernel
- * per token (the default whenever the shape fits: bf16 weights, hidden,
- * intermediate and n_q_heads*head_dim <= 3072); 1: the graph of separate
- * kernels (always available). Asking for 0 on a shape that does not fit keeps 1.
- * Both compute the same step; results agree to f32 rounding. If the persistent
+ * per token, the default whenever the shape fits: head_dim 64 or 128, at most 8
+ * query heads per KV head, hidden, intermediate and n_q_heads*head_dim <= 11264,
+ * any weight format (int4 only with an untied lm_head) and either cache format,
+ * and with a LoRA adapter when each CTA's share of the fused q/k/v rows is at
+ * most 64 (every shape up to ~9.7K fused rows); 1: the graph of separate kernels (always
+ * available). Asking for 0 on a shape that does not fit keeps 1. Both compute
+ * the same step; results agree to f32 rounding. If the persistent
  * kernel cannot be recorded on this device (no cooperative launch), the handle
  * switches to 1 for the rest of its life: the step still succeeds, one line goes
  * to stderr, qw_last_error(h) holds a note saying why, and qw_get_decode_path
- * returns 1. */
+ * returns 1. The choice is kept across qw_set_lora. */
 int qw_set_decode_path(qw_handle* h, int32_t path);
 int qw_get_decode_path(const qw_handle* h, int32_t* path);
 
