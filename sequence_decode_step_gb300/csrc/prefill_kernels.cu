@@ -400,6 +400,10 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
 constexpr int kFaBQ = kFaQueryRows;  // query rows per CTA (the MMA's M, one TMEM lane each)
 constexpr int kFaBN = kFaKeyRows;    // keys per tile (one 128-byte bf16 atom)
 constexpr int kFaChunk = 8;          // key tiles per CTA at most
+// Softmax warps: two per TMEM sub-partition, each taking half of a row's key columns
+// (and, at the end, half of its head dimensions); with the producer and MMA warps.
+constexpr int kFaSoftmaxWarps = 8;
+constexpr int kFaThreads = (2 + kFaSoftmaxWarps) * 32;
 
 template <int HD>
 struct FaLayout {
@@ -449,7 +453,7 @@ __device__ __forceinline__ bool fa_wait(const FaArgs& a, uint64_t* bar, uint32_t
 }
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFaThreads, 1)
     attn_prefill_fa_kernel(const __grid_constant__ FaMaps mp, const FaArgs a) {
   using LY = FaLayout<HD>;
   constexpr int QA = LY::QA;
@@ -493,8 +497,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&kv_empty[b], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_empty, 4);  // one arrival per softmax warp
-    mbar_init(p_full, 4);
+    mbar_init(s_empty, kFaSoftmaxWarps);  // one arrival per softmax warp
+    mbar_init(p_full, kFaSoftmaxWarps);
     mbar_init(o_full, 1);
     mbar_init(done, 1);
     fence_barrier_init();
@@ -595,26 +599,41 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(done, 0, kDrainNs);
     }
   } else {
-    // ---- softmax and epilogue: warp w owns TMEM lanes [32 (w % 4), +32) = query rows
-    const int q4 = warp & 3, r = q4 * 32 + lane;
+    // ---- softmax and epilogue: warps 2..9; warp w owns TMEM lanes [32 (w % 4), +32) = query
+    // rows, and half hf of each row's key columns (and of its head dims at the end). The two
+    // halves of a row exchange their maxima (and finally their sums) through two spare TMEM
+    // columns per tile parity, at a barrier of the eight warps that also ORs a failed wait,
+    // so all of them leave the loop together.
+    constexpr int kHalf = kFaBN / 2, kHD2 = HD / 2;
+    const int q4 = warp & 3, r = q4 * 32 + lane, hf = (warp - 2) >> 2;
     const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
+    const uint32_t t_x = tbase + kFaBN + HD + lrow;  // exchange columns [parity][half], sums
     const int qpos = a.p0 + t0 + r;
     const int first_pos = a.p0 + t0;  // the block's first row: tiles past it need the mask
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
+    float m = -INFINITY, l = 0.f;     // l: this half's running sum
+    bool bad = false;
     uint8_t* prow = sm + LY::off_p + (uint32_t)(r >> 3) * 1024 + (uint32_t)(r & 7) * 128;
+    auto bar_or = [](bool v) {  // the eight softmax warps; returns whether any passed true
+      unsigned rr;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(rr)
+          : "r"((unsigned)v), "r"(kFaSoftmaxWarps * 32)
+          : "memory");
+      return rr != 0;
+    };
     for (int i = 0; i < n_tiles; ++i) {
-      ok = __all_sync(0xffffffffu, fa_wait(a, s_full, (uint32_t)(i & 1)));
-      if (!ok) break;
+      bad = bad || !__all_sync(0xffffffffu, fa_wait(a, s_full, (uint32_t)(i & 1)));
       tc_fence_after();
-      float sv[kFaBN];
-      {  // the row's scores: all column blocks in flight, one wait
-        uint32_t rr[kFaBN / 16][16];
+      float sv[kHalf];
+      {  // this half's scores: both column blocks in flight, one wait
+        uint32_t rr[kHalf / 16][16];
 #pragma unroll
-        for (int j = 0; j < kFaBN / 16; ++j) tmem_ld16(t_s + lrow + 16 * j, rr[j]);
+        for (int j = 0; j < kHalf / 16; ++j) tmem_ld16(t_s + lrow + hf * kHalf + 16 * j, rr[j]);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < kFaBN / 16; ++j) {
+        for (int j = 0; j < kHalf / 16; ++j) {
           tmem_regs_ready(rr[j]);
 #pragma unroll
           for (int e = 0; e < 16; ++e) sv[16 * j + e] = __uint_as_float(rr[j][e]);
@@ -625,24 +644,31 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive_cta(s_empty);
       // causal mask (keys after this row's position; only tiles that reach past the
       // block's first row) and the running maximum; scores are in base-2 units already
-      const int k0 = (kt0 + i) * kFaBN;
-      if (k0 + kFaBN - 1 > first_pos) {
+      const int k0 = (kt0 + i) * kFaBN + hf * kHalf;
+      if ((kt0 + i) * kFaBN + kFaBN - 1 > first_pos) {
 #pragma unroll
-        for (int j = 0; j < kFaBN; ++j)
+        for (int j = 0; j < kHalf; ++j)
           if (k0 + j > qpos) sv[j] = -INFINITY;
       }
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int j = 0; j < kFaBN; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], sv[j]);
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      for (int j = 0; j < kHalf; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], sv[j]);
+      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      tmem_st1(t_x + 2 * (i & 1) + hf, __float_as_uint(mx));
+      tmem_st_wait();
+      tc_fence_before();
+      bad = bar_or(bad);
+      tc_fence_after();
+      if (bad) break;
+      mx = fmaxf(mx, __uint_as_float(tmem_ld1(t_x + 2 * (i & 1) + (1 - hf))));
       // the reference moves only when the maximum rises by more than 8 (P < 2^8); a row
-      // that has seen no key yet keeps m = -inf, alpha = 0 and P = 0
+      // that has seen no key yet keeps m = -inf, alpha = 0 and P = 0 (both halves decide alike)
       const float m_new = mx > m + 8.f ? mx : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = fast_exp2(m - m_use);
       float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < kFaBN; ++j) {
+      for (int j = 0; j < kHalf; ++j) {
         const float pj = fast_exp2(sv[j] - m_use);
         sv[j] = pj;
         ps4[j & 3] += pj;
@@ -650,13 +676,16 @@ __global__ void __launch_bounds__(192, 1)
       l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
       m = m_new;
       if (i > 0) {
-        // P V of tile i-1 has finished: P's buffer is free and O can be rescaled
-        ok = __all_sync(0xffffffffu, fa_wait(a, o_full, (uint32_t)((i - 1) & 1)));
-        if (!ok) break;
+        // P V of tile i-1 has finished: P's buffer is free and O can be rescaled (a failed
+        // wait is carried to the next tile's barrier)
+        if (!__all_sync(0xffffffffu, fa_wait(a, o_full, (uint32_t)((i - 1) & 1)))) {
+          bad = true;
+          continue;
+        }
         tc_fence_after();
         if (!__all_sync(0xffffffffu, alpha == 1.f)) {
 #pragma unroll 1
-          for (int d0 = 0; d0 < HD; d0 += 16) {
+          for (int d0 = hf * kHD2; d0 < (hf + 1) * kHD2; d0 += 16) {
             uint32_t rr[16];
             tmem_ld16(t_o + lrow + d0, rr);
             tmem_ld_wait();
@@ -668,14 +697,15 @@ __global__ void __launch_bounds__(192, 1)
           tmem_st_wait();
         }
       }
-      // P (hi, lo) into shared memory: row r, one 128-byte atom each, 16-byte units
-      // of 8 keys swizzled by the row
+      // this half of P (hi, lo) into shared memory: row r, one 128-byte atom each,
+      // 16-byte units of 8 keys swizzled by the row
 #pragma unroll
-      for (int u = 0; u < kFaBN / 8; ++u) {
+      for (int uu = 0; uu < kHalf / 8; ++uu) {
+        const int u = hf * (kHalf / 8) + uu;
         uint32_t hw[4], lw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          split2_packed(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1], hw[e], lw[e]);
+          split2_packed(sv[8 * uu + 2 * e], sv[8 * uu + 2 * e + 1], hw[e], lw[e]);
         const uint32_t off = (uint32_t)((u ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *reinterpret_cast<uint4*>(prow + LY::kP1 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -685,8 +715,16 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(p_full);
     }
+    bool ok = !bad;
     if (ok) ok = __all_sync(0xffffffffu, fa_wait(a, o_full, (uint32_t)((n_tiles - 1) & 1)));
+    // the row's sum: both halves, in a fixed order
+    tmem_st1(t_x + 4 + hf, __float_as_uint(l));
+    tmem_st_wait();
+    tc_fence_before();
+    ok = !bar_or(!ok);
+    tc_fence_after();
     if (!ok && lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+    l = __uint_as_float(tmem_ld1(t_x + 4)) + __uint_as_float(tmem_ld1(t_x + 5));
     const bool store = r < nrows;
     uint16_t* oh = a.o_hi + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
     uint16_t* ol = a.o_lo + (size_t)(t0 + r) * a.nq * HD + (size_t)h * HD;
@@ -695,7 +733,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const float inv = 1.0f / l;
 #pragma unroll 1
-        for (int d0 = 0; d0 < HD; d0 += 16) {
+        for (int d0 = hf * kHD2; d0 < (hf + 1) * kHD2; d0 += 16) {
           uint32_t rr[16];
           tmem_ld16(t_o + lrow + d0, rr);
           tmem_ld_wait();
@@ -721,7 +759,7 @@ __global__ void __launch_bounds__(192, 1)
       if (ok) {
         tc_fence_after();
 #pragma unroll 1
-        for (int d0 = 0; d0 < HD; d0 += 16) {
+        for (int d0 = hf * kHD2; d0 < (hf + 1) * kHD2; d0 += 16) {
           uint32_t rr[16];
           tmem_ld16(t_o + lrow + d0, rr);
           tmem_ld_wait();
@@ -733,12 +771,12 @@ __global__ void __launch_bounds__(192, 1)
                             __uint_as_float(rr[e + 2]), __uint_as_float(rr[e + 3]));
         }
       }
-      a.part_ml[(slot + chunk) * kFaBQ + r] = make_float2(m, l);
+      if (hf == 0) a.part_ml[(slot + chunk) * kFaBQ + r] = make_float2(m, l);
       __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
+      asm volatile("bar.sync 1, %0;" ::"r"(kFaSoftmaxWarps * 32) : "memory");  // softmax warps
       int* flag = reinterpret_cast<int*>(tslot + 1);
       if (warp == 2 && lane == 0) *flag = atomicAdd(&a.counters[h * a.nqb + qb], 1) == nch - 1;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(kFaSoftmaxWarps * 32) : "memory");
       if (*flag) {
         __threadfence();
         float M = -INFINITY;
@@ -754,7 +792,7 @@ __global__ void __launch_bounds__(192, 1)
         // 32 dims at a time, two chunks' rows per round of loads (each chunk's weight
         // exp2(m_c - M) recomputed from its (m, l)), summed in chunk order
 #pragma unroll 1
-        for (int d0 = 0; d0 < HD; d0 += 32) {
+        for (int d0 = hf * kHD2; d0 < (hf + 1) * kHD2; d0 += 32) {
           float acc[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc[e] = 0.f;
@@ -968,14 +1006,14 @@ cudaError_t launch_attn_prefill(const FaMaps& maps, const void* kc, const void* 
       kv_split_kernel<64, true><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
     else
       kv_split_kernel<64, false><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
-    attn_prefill_fa_kernel<64><<<grid, 192, FaLayout<64>::bytes, s>>>(maps, a);
+    attn_prefill_fa_kernel<64><<<grid, kFaThreads, FaLayout<64>::bytes, s>>>(maps, a);
   } else if (hd == 128) {
     if (kv_bf16)
       kv_split_kernel<128, true><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth, vtl);
     else
       kv_split_kernel<128, false><<<sgrid, 256, 0, s>>>(kc, vc, cap, n, p0, kv_rows, kh, kl, vth,
                                                         vtl);
-    attn_prefill_fa_kernel<128><<<grid, 192, FaLayout<128>::bytes, s>>>(maps, a);
+    attn_prefill_fa_kernel<128><<<grid, kFaThreads, FaLayout<128>::bytes, s>>>(maps, a);
   } else {
     return cudaErrorInvalidValue;
   }
