@@ -96,7 +96,6 @@ struct Smem {
   int flag;
   alignas(16) float xs[kMaxC * 256];  // phase input vector (normalised when the phase has a norm);
                                       // written with float4 stores, so 16-byte aligned
-  float xsum[kMaxC * 32];  // int4 weights: 136 x the sum of each lane's 8 inputs of a chunk
   float q_s[kGQ * 128];
   float kn_s[128];
   float vn_s[128];
@@ -104,9 +103,10 @@ struct Smem {
   float al_s[kGQ];
   float unit_s[kUnitPre];        // per-unit values the epilogue needs (residual rows, or bias
                                  // plus the LoRA update)
-  float lora_t[128];             // LoRA: A_q . x_n, then A_v . x_n (rank <= 64 each)
   float pml_s[2 * kGQ * 160];    // split partials (m, l) for the combine; before it, the
                                  // scores and probabilities of an attention pass
+  float xsum[kMaxC * 32];        // int4 weights: 136 x the sum of each lane's 8 inputs of a chunk
+  float lora_t[128];             // LoRA: A_q . x_n, then A_v . x_n (rank <= 64 each)
 };
 
 // The contiguous slice of a row-streamed phase owned by CTA b: units [u0, u1),
@@ -351,6 +351,8 @@ __device__ __forceinline__ int xs_pos(int k) {
 // Out of line: its word pairs in flight would otherwise push the inlined token
 // loop past the register budget (spills go to L2, since shared memory takes
 // nearly all of L1).
+#if QW_MEGA_BIG
+// Wide inputs in rounds, and the per-lane input sums that int4 rows need (xsum).
 template <int NP>  // (value, tag) word pairs per thread and round: a round covers 2 * NP * kNT inputs
 __device__ __noinline__ float load_input_n(const MegaArgs& a, Smem& S, const uint64_t* v,
                                           uint32_t tag, int K, const uint16_t* g, bool from_embed,
@@ -466,6 +468,102 @@ __device__ __noinline__ float load_input_n(const MegaArgs& a, Smem& S, const uin
   for (int i = 0; i < kConsumers; ++i) tot += S.red[i];
   return 1.0f / sqrtf(tot / (float)K + a.eps);
 }
+#else
+// One round; no input sums (the 7- and 11-warp builds take no int4 rows).
+template <int NP>  // (value, tag) word pairs per thread: K <= 2 * NP * kNT
+__device__ __noinline__ float load_input_n(const MegaArgs& a, Smem& S, const uint64_t* v,
+                                          uint32_t tag, int K, const uint16_t* g, bool from_embed,
+                                          int tok, const uint64_t* unit_own,
+                                          const uint16_t* unit_bf16, int n_unit, bool& abort) {
+  constexpr int NT = kConsumers * 32;
+  const int tid = threadIdx.x;
+  float uv = 0.f;
+  if (tid < n_unit)
+    uv = unit_own ? word_value(__ldcg(unit_own + tid)) : (unit_bf16 ? bf16f(unit_bf16[tid]) : 0.f);
+  // the norm gain (bf16), one pair per word pair, in the same batch of loads
+  uint32_t gv[NP];
+  if (g != nullptr) {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int idx = tid + i * NT;
+      gv[i] = idx * 2 < K ? *reinterpret_cast<const uint32_t*>(g + idx * 2) : 0u;
+    }
+  }
+  float ss = 0.f;
+  if (from_embed) {
+    const uint4* e = reinterpret_cast<const uint4*>(a.embed + (size_t)tok * K);
+    constexpr int NE = (NP + 3) / 4;
+    uint4 w[NE];
+#pragma unroll
+    for (int i = 0; i < NE; ++i) {
+      const int idx = tid + i * NT;
+      w[i] = idx * 8 < K ? e[idx] : make_uint4(0, 0, 0, 0);
+    }
+    csync();  // the previous phase's readers of xs / unit_s are done
+#pragma unroll
+    for (int i = 0; i < NE; ++i) {
+      const int idx = tid + i * NT;
+      if (idx * 8 < K) {
+        float* d = &S.xs[(idx >> 5) * 256 + (idx & 31) * 4];
+        *reinterpret_cast<float4*>(d) =
+            make_float4(__uint_as_float(w[i].x << 16), __uint_as_float(w[i].x & 0xffff0000u),
+                        __uint_as_float(w[i].y << 16), __uint_as_float(w[i].y & 0xffff0000u));
+        *reinterpret_cast<float4*>(d + 128) =
+            make_float4(__uint_as_float(w[i].z << 16), __uint_as_float(w[i].z & 0xffff0000u),
+                        __uint_as_float(w[i].w << 16), __uint_as_float(w[i].w & 0xffff0000u));
+      }
+    }
+  } else {
+    uint64_t w[NP][2];
+    unsigned pend = 0;
+#pragma unroll
+    for (int i = 0; i < NP; ++i)
+      if ((tid + i * NT) * 2 < K) pend |= 1u << i;
+    uint64_t t0 = 0;
+    for (uint32_t n = 1; pend && !abort; ++n) {
+#pragma unroll
+      for (int i = 0; i < NP; ++i)
+        if ((pend >> i) & 1u) ld_words2(v + 2 * (tid + i * NT), w[i][0], w[i][1]);
+#pragma unroll
+      for (int i = 0; i < NP; ++i)
+        if (((pend >> i) & 1u) && word_tag(w[i][0]) == tag && word_tag(w[i][1]) == tag)
+          pend &= ~(1u << i);
+      if (pend) poll_bound(a, n, t0, abort);
+    }
+    csync();  // the previous phase's readers of xs / unit_s / red are done
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int idx = tid + i * NT;
+      if (idx * 2 < K) {
+        const float x0 = word_value(w[i][0]), x1 = word_value(w[i][1]);
+        ss = fmaf(x0, x0, fmaf(x1, x1, ss));
+        const float g0 = g != nullptr ? __uint_as_float(gv[i] << 16) : 1.f;
+        const float g1 = g != nullptr ? __uint_as_float(gv[i] & 0xffff0000u) : 1.f;
+        *reinterpret_cast<float2*>(&S.xs[xs_pos(idx * 2)]) = make_float2(x0 * g0, x1 * g1);
+      }
+    }
+  }
+  if (tid < n_unit) S.unit_s[tid] = uv;
+  if (g != nullptr) {
+    if (from_embed) {  // once per token: the gain goes on in a second pass
+      csync();
+      for (int k = tid; k < K; k += NT) {
+        const float xk = S.xs[xs_pos(k)];
+        ss = fmaf(xk, xk, ss);
+        S.xs[xs_pos(k)] = xk * bf16f(g[k]);
+      }
+    }
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) S.red[tid >> 5] = ss;
+  }
+  abort = csync_or(abort);
+  if (g == nullptr) return 1.f;
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kConsumers; ++i) tot += S.red[i];
+  return 1.0f / sqrtf(tot / (float)K + a.eps);
+}
+#endif
 
 __device__ __forceinline__ float load_input(const MegaArgs& a, Smem& S, const uint64_t* v,
                                            uint32_t tag, int K, const uint16_t* g, bool from_embed,
@@ -692,7 +790,7 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
           if constexpr (EPI == EPI_STORE) {
             // unit_s: the bias (and, with an adapter, the LoRA update) of the first
             // kUnitPre units; an adapter is taken only when the slice fits unit_s
-            const bool pre = bias != nullptr || a.lora_r > 0;
+            const bool pre = bias != nullptr || (QW_MEGA_BIG && a.lora_r > 0);
             st_tagged(ty + uu,
                       sum + (pre ? (iu < kUnitPre ? S.unit_s[iu] : bf16f(bias[uu])) : 0.f), tag);
           } else if constexpr (EPI == EPI_RESIDUAL) {
@@ -728,7 +826,8 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
 // holds the row's bias, or 0), so the QKV epilogue adds both at once. A_q / A_v are
 // [r, K] and B_q / B_v [rows, r] bf16; the slice [u0, u1) of fused q/k/v rows has at
 // most kUnitPre rows (checked on the host). Ends with a consumer barrier.
-__device__ __noinline__ void lora_update(const MegaArgs& a, Smem& S, int l, int u0, int u1, int K,
+// Inlined: an out-of-line call here costs register spills around the call site.
+__device__ __forceinline__ void lora_update(const MegaArgs& a, Smem& S, int l, int u0, int u1, int K,
                                          float rn) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = a.lora_r, qd = a.nq * a.hd, vd0 = qd + a.nkv * a.hd;
@@ -804,6 +903,114 @@ __device__ __forceinline__ void gemv(const MegaArgs& a, uint8_t* ring, Smem& S, 
 
 // Chunks of a slice (the producer streams them in this count).
 __device__ __forceinline__ int slice_chunks(const Slice& sl) { return sl.n_chunks; }
+
+// Key-split combine of CTA sp (its partial outputs oacc and (m, l) in ml_s).
+template <int HD>
+__device__ __forceinline__ void attn_combine(const MegaArgs& a, Smem& S, const Split& sp, int HB, int GQ,
+                  const float (&oacc)[(kGQ * HD + kNT - 1) / kNT], uint32_t tag_out, bool& abort) {
+  constexpr int OUTS = (kGQ * HD + kNT - 1) / kNT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Every split publishes its partial outputs and (m, l) per head as
+  // tagged words, then combines a contiguous slice of the group's GQ * HD outputs
+  // over all splits: out = sum_s f_s o_s with f_s = exp(m_s - M) / sum_s' exp(m_s' - M) l_s',
+  // M the heads' maximum, summed in split order. Each split polls the (m, l) words
+  // and the partials of its slice in one batch of loads (one L2 round trip once they
+  // are there). The partial slots are reused by the next layer only after the
+  // combined outputs have gone through o_proj, gate/up, down and the next QKV, all
+  // of which the writers wait for.
+  const size_t hs = (size_t)a.splits * (HD + 2);  // words per query head
+  uint64_t* mp = a.mpart + (size_t)HB * hs;
+  {
+    uint64_t* my = mp + (size_t)sp.s * (HD + 2);
+#pragma unroll
+    for (int oi = 0; oi < OUTS; ++oi) {
+      const int idx = tid + oi * kNT;
+      if (idx < GQ * HD) {
+        const int h = idx / HD, d = idx % HD;
+        st_tagged(my + (size_t)h * hs + d, oacc[oi], tag_out);
+      }
+    }
+    if (tid < GQ) {
+      st_tagged(my + (size_t)tid * hs + HD, S.ml_s[2 * tid], tag_out);
+      st_tagged(my + (size_t)tid * hs + HD + 1, S.ml_s[2 * tid + 1], tag_out);
+    }
+  }
+  const int ns = sp.nsplit, n_out = GQ * HD;
+  const int o0 = (int)((uint32_t)n_out * sp.s / ns), o1 = (int)((uint32_t)n_out * (sp.s + 1) / ns);
+  const int nw = (o1 - o0) * ns;  // partial words of this split's slice
+  csync();  // every warp has folded its last pass out of xs and pml_s
+  // (m, l) of every split and head -> pml_s[2 (h ns + s)]
+  for (int i = tid; i < GQ * ns; i += kNT) {
+    const int h = i / ns, s2 = i % ns;
+    const uint64_t* src = mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + HD;
+    uint64_t w0 = 0, w1 = 0, t0 = 0;
+    for (uint32_t n = 1; !abort; ++n) {
+      ld_words2(src, w0, w1);
+      if (word_tag(w0) == tag_out && word_tag(w1) == tag_out) break;
+      poll_bound(a, n, t0, abort);
+    }
+    S.pml_s[2 * i] = word_value(w0);
+    S.pml_s[2 * i + 1] = word_value(w1);
+  }
+  abort = csync_or(abort);
+  // per head (one warp each, lanes over the splits): f_s in place of m_s; the
+  // denominator is summed lane-strided, then over the lanes in a fixed order
+  for (int h = warp; h < GQ; h += kConsumers) {
+    float* pm = S.pml_s + 2 * h * ns;
+    float M = -INFINITY;
+    for (int s2 = lane; s2 < ns; s2 += 32) M = fmaxf(M, pm[2 * s2]);
+    M = warp_max(M);
+    float den = 0.f;
+    for (int s2 = lane; s2 < ns; s2 += 32) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
+    const float inv = 1.0f / warp_sum(den);
+    __syncwarp();
+    for (int s2 = lane; s2 < ns; s2 += 32) pm[2 * s2] = expf(pm[2 * s2] - M) * inv;
+  }
+  csync();
+  // the slice's partials, weighted, into xs[s n_o + (o - o0)] (consecutive threads read
+  // consecutive outputs of one split); 8 polled loads per thread per round
+  const int n_o = o1 - o0;
+  float* wsum = S.xs;
+  for (int base = 0; base < nw; base += 8 * kNT) {
+    uint64_t w[8];
+    unsigned pend = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      w[j] = 0;
+      if (base + tid + j * kNT < nw) pend |= 1u << j;
+    }
+    auto word_at = [&](int i) {
+      const int s2 = i / n_o, o = o0 + i % n_o, h = o / HD, d = o % HD;
+      return mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + d;
+    };
+    uint64_t t0 = 0;
+    for (uint32_t n = 1; pend && !abort; ++n) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if ((pend >> j) & 1u) w[j] = ld_word(word_at(base + tid + j * kNT));
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (((pend >> j) & 1u) && word_tag(w[j]) == tag_out) pend &= ~(1u << j);
+      if (pend) poll_bound(a, n, t0, abort);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + tid + j * kNT;
+      if (i < nw) {
+        const int s2 = i / n_o, o = o0 + i % n_o;
+        wsum[i] = S.pml_s[2 * ((o / HD) * ns + s2)] * word_value(w[j]);
+      }
+    }
+  }
+  abort = csync_or(abort);
+  for (int o = o0 + tid; o < o1; o += kNT) {
+    const float* v = wsum + (o - o0);
+    float acc = 0.f;
+    for (int s2 = 0; s2 < ns; ++s2) acc += v[(size_t)s2 * n_o];
+    const int h = o / HD, d = o % HD;
+    st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, acc, tag_out);
+  }
+}
 
 // Split-K attention of CTA b: QK-norm + RoPE of its group's queries (and of the
 // new key when its split holds pos), tiles of 32 keys from the ring, online
@@ -1085,106 +1292,7 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     }
     return;
   }
-  // Key split: every split publishes its partial outputs and (m, l) per head as
-  // tagged words, then combines a contiguous slice of the group's GQ * HD outputs
-  // over all splits: out = sum_s f_s o_s with f_s = exp(m_s - M) / sum_s' exp(m_s' - M) l_s',
-  // M the heads' maximum, summed in split order. Each split polls the (m, l) words
-  // and the partials of its slice in one batch of loads (one L2 round trip once they
-  // are there). The partial slots are reused by the next layer only after the
-  // combined outputs have gone through o_proj, gate/up, down and the next QKV, all
-  // of which the writers wait for.
-  const size_t hs = (size_t)a.splits * (HD + 2);  // words per query head
-  uint64_t* mp = a.mpart + (size_t)HB * hs;
-  {
-    uint64_t* my = mp + (size_t)sp.s * (HD + 2);
-#pragma unroll
-    for (int oi = 0; oi < OUTS; ++oi) {
-      const int idx = tid + oi * kNT;
-      if (idx < GQ * HD) {
-        const int h = idx / HD, d = idx % HD;
-        st_tagged(my + (size_t)h * hs + d, oacc[oi], tag_out);
-      }
-    }
-    if (tid < GQ) {
-      st_tagged(my + (size_t)tid * hs + HD, S.ml_s[2 * tid], tag_out);
-      st_tagged(my + (size_t)tid * hs + HD + 1, S.ml_s[2 * tid + 1], tag_out);
-    }
-  }
-  const int ns = sp.nsplit, n_out = GQ * HD;
-  const int o0 = (int)((uint32_t)n_out * sp.s / ns), o1 = (int)((uint32_t)n_out * (sp.s + 1) / ns);
-  const int nw = (o1 - o0) * ns;  // partial words of this split's slice
-  csync();  // every warp has folded its last pass out of xs and pml_s
-  // (m, l) of every split and head -> pml_s[2 (h ns + s)]
-  for (int i = tid; i < GQ * ns; i += kNT) {
-    const int h = i / ns, s2 = i % ns;
-    const uint64_t* src = mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + HD;
-    uint64_t w0 = 0, w1 = 0, t0 = 0;
-    for (uint32_t n = 1; !abort; ++n) {
-      ld_words2(src, w0, w1);
-      if (word_tag(w0) == tag_out && word_tag(w1) == tag_out) break;
-      poll_bound(a, n, t0, abort);
-    }
-    S.pml_s[2 * i] = word_value(w0);
-    S.pml_s[2 * i + 1] = word_value(w1);
-  }
-  abort = csync_or(abort);
-  // per head (one warp each, lanes over the splits): f_s in place of m_s; the
-  // denominator is summed lane-strided, then over the lanes in a fixed order
-  for (int h = warp; h < GQ; h += kConsumers) {
-    float* pm = S.pml_s + 2 * h * ns;
-    float M = -INFINITY;
-    for (int s2 = lane; s2 < ns; s2 += 32) M = fmaxf(M, pm[2 * s2]);
-    M = warp_max(M);
-    float den = 0.f;
-    for (int s2 = lane; s2 < ns; s2 += 32) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
-    const float inv = 1.0f / warp_sum(den);
-    __syncwarp();
-    for (int s2 = lane; s2 < ns; s2 += 32) pm[2 * s2] = expf(pm[2 * s2] - M) * inv;
-  }
-  csync();
-  // the slice's partials, weighted, into xs[s n_o + (o - o0)] (consecutive threads read
-  // consecutive outputs of one split); 8 polled loads per thread per round
-  const int n_o = o1 - o0;
-  float* wsum = S.xs;
-  for (int base = 0; base < nw; base += 8 * kNT) {
-    uint64_t w[8];
-    unsigned pend = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      w[j] = 0;
-      if (base + tid + j * kNT < nw) pend |= 1u << j;
-    }
-    auto word_at = [&](int i) {
-      const int s2 = i / n_o, o = o0 + i % n_o, h = o / HD, d = o % HD;
-      return mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + d;
-    };
-    uint64_t t0 = 0;
-    for (uint32_t n = 1; pend && !abort; ++n) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if ((pend >> j) & 1u) w[j] = ld_word(word_at(base + tid + j * kNT));
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (((pend >> j) & 1u) && word_tag(w[j]) == tag_out) pend &= ~(1u << j);
-      if (pend) poll_bound(a, n, t0, abort);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = base + tid + j * kNT;
-      if (i < nw) {
-        const int s2 = i / n_o, o = o0 + i % n_o;
-        wsum[i] = S.pml_s[2 * ((o / HD) * ns + s2)] * word_value(w[j]);
-      }
-    }
-  }
-  abort = csync_or(abort);
-  for (int o = o0 + tid; o < o1; o += kNT) {
-    const float* v = wsum + (o - o0);
-    float acc = 0.f;
-    for (int s2 = 0; s2 < ns; ++s2) acc += v[(size_t)s2 * n_o];
-    const int h = o / HD, d = o % HD;
-    st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, acc, tag_out);
-  }
+  attn_combine<HD>(a, S, sp, HB, GQ, oacc, tag_out, abort);
 }
 
 
@@ -1344,8 +1452,10 @@ __device__ void consume(const MegaArgs& a, uint8_t* ring, Smem& S, int pos, uint
       const float rn = load_input(a, S, a.x, tq - 1u, a.H, Ld.attn_norm, l == 0, tok, nullptr,
                                   Ld.qkv_bias ? Ld.qkv_bias + qs.u0 : nullptr,
                                   min(qs.u1 - qs.u0, kUnitPre), abort);
+#if QW_MEGA_BIG  // handles with an adapter run the wide-input build
       if (a.lora_r > 0 && (qs.u0 < qd || qs.u1 > qd + a.nkv * a.hd))
         lora_update(a, S, l, qs.u0, qs.u1, a.H, rn);
+#endif
       gemv<EPI_STORE, XH, kNrQkv, WF>(a, ring, S, c, qs, a.H, rn, a.qkv, tq, Ld.qkv_bias, nullptr, best, abort);
     }
     // attention of this CTA's (kv head, key split)

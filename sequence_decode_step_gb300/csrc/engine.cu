@@ -166,7 +166,8 @@ struct qw_handle {
   bool mega_ok = false;
   bool mega_wide = false;  // the recorded step uses the 11-warp build (long contexts)
   bool mega_big = false;   // the shape takes the wide-input / int4 build at every position
-  bool mega_lora_ok = false;  // a CTA's fused q/k/v slice fits the kernel's LoRA update
+  bool mega_big_ok = false;   // the wide-input build takes the shape (it runs every adapter)
+  bool mega_lora_ok = false;  // ... and a CTA's fused q/k/v slice fits its LoRA update
   int path_pref = 0;          // the decode path asked for (qw_set_decode_path)
   const uint16_t** d_lora = nullptr;  // device [L][4] LoRA pointers for the persistent kernel
   std::vector<const uint16_t*> lora_tab;  // their host copy
@@ -291,17 +292,18 @@ static int alloc_state(qw_handle* h) {
                                             c.n_layers, wf) &&
                        mega_wide::mega_supported(c.hidden, c.intermediate, qd, c.head_dim, gq,
                                                  c.n_layers, wf);
-    const bool big = !small && (wf != 1 || !c.tie_word_embeddings) &&
-                     mega_big::mega_supported(c.hidden, c.intermediate, qd, c.head_dim, gq,
-                                              c.n_layers, wf);
-    h->mega_ok = slices_ok && (small || big);
-    h->mega_big = slices_ok && big;
+    const bool big_ok = (wf != 1 || !c.tie_word_embeddings) &&
+                        mega_big::mega_supported(c.hidden, c.intermediate, qd, c.head_dim, gq,
+                                                 c.n_layers, wf);
+    h->mega_ok = slices_ok && (small || big_ok);
+    h->mega_big = slices_ok && !small && big_ok;
+    h->mega_big_ok = slices_ok && big_ok;
   }
   h->use_mega = h->mega_ok;
   {
     const int grid = h->nsplit_max * c.n_kv_heads;
     const int rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-    h->mega_lora_ok = h->mega_ok && (rows + grid - 1) / grid <= kMegaUnitPre;
+    h->mega_lora_ok = h->mega_big_ok && (rows + grid - 1) / grid <= kMegaUnitPre;
   }
   h->wfmt = c.weight_format == QW_WEIGHTS_INT4_G128 ? 1 : c.weight_format == QW_WEIGHTS_Q8_0 ? 2 : 0;
   h->lm_fmt = h->wfmt == 2 ? 2 : (h->wfmt == 1 && !c.tie_word_embeddings ? 1 : 0);
@@ -774,9 +776,12 @@ static MegaArgs mega_args(qw_handle* h) {
 // Launch one step's kernels on stream s (recorded into the graph).
 static cudaError_t record_step(qw_handle* h, cudaStream_t s) {
   if (h->use_mega)
-    return (h->mega_big    ? mega_big::launch_mega
-            : h->mega_wide ? mega_wide::launch_mega
-                           : mega::launch_mega)(mega_args(h), h->nsplit_max * h->cfg.n_kv_heads, s);
+    // the wide-input build for its shapes and for every handle with an adapter (the LoRA
+    // step is compiled into that build only)
+    return (h->mega_big || h->lora_active ? mega_big::launch_mega
+            : h->mega_wide                ? mega_wide::launch_mega
+                                          : mega::launch_mega)(mega_args(h),
+                                                               h->nsplit_max * h->cfg.n_kv_heads, s);
   const qw_config& c = h->cfg;
   const int H = c.hidden, I = c.intermediate, hd = c.head_dim;
   const int qd = c.n_q_heads * hd, kd = c.n_kv_heads * hd;
@@ -1014,7 +1019,7 @@ static constexpr int kMegaWideFrom = 1536;
 static int run_steps(qw_handle* h, int n, const int32_t* tokens, int first) {
   int last = -2;
   for (int i = 0; i < n; ++i) {
-    const bool wide = h->use_mega && !h->mega_big && h->pos + i >= kMegaWideFrom;
+    const bool wide = h->use_mega && !h->mega_big && !h->lora_active && h->pos + i >= kMegaWideFrom;
     if (wide != h->mega_wide) {
       h->mega_wide = wide;
       h->graph_dirty = true;

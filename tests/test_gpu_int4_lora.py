@@ -67,8 +67,9 @@ def test_tiny_int4_decode(shape, path):
 
 @pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("shape", [TINY_INT4, W.TINY.replace(qkv_bias=True),
-                                   W.TINY.replace(qkv_bias=False)],
-                         ids=["int4", "bf16", "bf16_nobias"])
+                                   W.TINY.replace(qkv_bias=False),
+                                   W.TINY.replace(qkv_bias=True, kv_format="bf16")],
+                         ids=["int4", "bf16", "bf16_nobias", "bf16_kvbf16"])
 def test_tiny_lora_on_then_cleared(shape, path):
     wl = W.Workload("tl", shape, seed=6, prompt_len=6, decode_steps=12, max_ctx=64,
                     lora=W.LoraShape(4, 8.0))
