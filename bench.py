@@ -55,13 +55,17 @@ def step_bytes(s, p0: int, n: int) -> int:
 # the digest no longer matches and the line reports traffic as null.
 KERNEL_SOURCES = {
     "decode_mega": ["decode_mega.cu", "qw_ptx.cuh", "qw_internal.h"],
+    "decode_mega_big": ["decode_mega.cu", "decode_mega_big.cu", "qw_ptx.cuh", "qw_internal.h"],
     "lm_head_gemv": ["decode_kernels.cu", "qw_ptx.cuh", "qw_internal.h"],
 }
 NCU_TRAFFIC = {
     # kernel: (sources digest, bytes per launch, what was captured)
-    "decode_mega": ("775e323b5897f239", 1194047488 + 3810816,
-                    "qwen3_0.6b_decode token at position 6, decode_mega_kernel<128, 1, 0, 0>"),
-    "lm_head_gemv": ("79af7532f0ab9dff", 311267072 + 3709696,
+    "decode_mega": ("d6d9446ccd05e3bb", 1194223872 + 3795968,
+                    "qwen3_0.6b_decode token at position 6, decode_mega_kernel<128, 1, 0, 0, false, 0>"),
+    "decode_mega_big": ("147ca706f57da3dc", 1895093504 + 7688448,
+                        "qwen2.5_3b_int4_lora token at position 4098 without the adapter, "
+                        "decode_mega_kernel<128, 0, 0, 0, false, 1> (wide-input build)"),
+    "lm_head_gemv": ("080190fbaea159fa", 311220992 + 3417856,
                      "qw_lm_head_argmax on the 151936 x 1024 table, gemv_kernel<3, 4, 0>"),
 }
 
@@ -594,6 +598,7 @@ def int4_decode_timing(torch, W, B, DeviceModel, stream) -> dict:
             byt = wbytes + kvb / wl.decode_steps + (lora_bytes if mode == "lora_on" else 0)
             out[mode] = {"us_per_token": us, "tok_per_s": 1e6 / us, "bytes_per_token": byt,
                          "roofline_frac": byt / (us * 1e-6) / 1e9 / hbm, "decode_path": path}
+        out["traffic"], out["traffic_source"] = recorded_traffic("decode_mega_big")
     finally:
         m.close()
     return out
