@@ -76,7 +76,7 @@ constexpr uint32_t kStage = 32 * 1024;       // bytes per stage
 constexpr int kMaxC = QW_MEGA_MAXC;          // input vectors up to kMaxC x 256 wide
 constexpr int kTK = 32;                      // keys per attention tile (K + V = 32 KB at hd 128)
 constexpr int kGQ = 8;
-constexpr int kMinKeys = 64;                // keys per split at least
+constexpr int kMinKeys = QW_MEGA_BIG ? 64 : 128;  // keys per split at least
 // Up to this many keys a group's query heads go to separate CTAs over all keys
 // (one pass, no combine); beyond it the keys are split and combined. Measured
 // (us/token, Qwen3-0.6B shape, same box) at 145-256 keys: 652-680 with the key
@@ -1292,7 +1292,94 @@ __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Sme
     }
     return;
   }
+#if QW_MEGA_BIG
+  // every split combines a slice of the outputs (at GQ = 8 and 64 keys per split the
+  // combine is a large part of the attention)
   attn_combine<HD>(a, S, sp, HB, GQ, oacc, tag_out, abort);
+#else
+  // split 0 combines; in the 7- and 11-warp builds this ran faster than the spread
+  // combine (Qwen3-0.6B 575 against 596 us/token, 8K context 1086 against 1109, same box)
+  // Key split: every split but the first publishes its partial outputs and
+  // (m, l) per head as tagged words; split 0 polls them (one L2 round trip once
+  // they are there) and combines in split order. The partial slots are reused
+  // by the next layer only after the combined output has gone through o_proj,
+  // gate/up, down and the next QKV, all of which the writers wait for.
+  const size_t hs = (size_t)a.splits * (HD + 2);  // words per query head
+  uint64_t* mp = a.mpart + (size_t)HB * hs;
+  if (sp.s != 0) {
+    uint64_t* my = mp + (size_t)sp.s * (HD + 2);
+#pragma unroll
+    for (int oi = 0; oi < OUTS; ++oi) {
+      const int idx = tid + oi * kNT;
+      if (idx < GQ * HD) {
+        const int h = idx / HD, d = idx % HD;
+        st_tagged(my + (size_t)h * hs + d, oacc[oi], tag_out);
+      }
+    }
+    if (tid < GQ) {
+      st_tagged(my + (size_t)tid * hs + HD, S.ml_s[2 * tid], tag_out);
+      st_tagged(my + (size_t)tid * hs + HD + 1, S.ml_s[2 * tid + 1], tag_out);
+    }
+    return;
+  }
+  const int ns = sp.nsplit;
+  for (int i = tid; i < GQ * ns; i += kNT) {
+    const int h = i / ns, s2 = i % ns;
+    float m = S.ml_s[2 * h], lsum = S.ml_s[2 * h + 1];
+    if (s2 != 0) {
+      const uint64_t* src = mp + (size_t)h * hs + (size_t)s2 * (HD + 2) + HD;
+      uint64_t w0 = 0, w1 = 0;
+      uint64_t t0 = 0;
+      for (uint32_t n = 1; !abort; ++n) {
+        ld_words2(src, w0, w1);
+        if (word_tag(w0) == tag_out && word_tag(w1) == tag_out) break;
+        poll_bound(a, n, t0, abort);
+      }
+      m = word_value(w0);
+      lsum = word_value(w1);
+    }
+    S.pml_s[2 * i] = m;
+    S.pml_s[2 * i + 1] = lsum;
+  }
+  abort = csync_or(abort);
+#pragma unroll
+  for (int oi = 0; oi < OUTS; ++oi) {
+    const int idx = tid + oi * kNT;
+    if (idx < GQ * HD) {
+      const int h = idx / HD, d = idx % HD;
+      const float* pm = S.pml_s + 2 * h * ns;
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, pm[2 * s2]);
+      float den = 0.f;
+      for (int s2 = 0; s2 < ns; ++s2) den = fmaf(expf(pm[2 * s2] - M), pm[2 * s2 + 1], den);
+      const uint64_t* po = mp + (size_t)h * hs + d;
+      float num = expf(pm[0] - M) * oacc[oi];
+      for (int s0 = 1; s0 < ns; s0 += 8) {  // the others' outputs, 8 polled loads at a time
+        uint64_t w[8];
+        unsigned pend = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          w[j] = 0;
+          if (s0 + j < ns) pend |= 1u << j;
+        }
+        uint64_t t0 = 0;
+        for (uint32_t n = 1; pend && !abort; ++n) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if ((pend >> j) & 1u) w[j] = ld_word(po + (size_t)(s0 + j) * (HD + 2));
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (((pend >> j) & 1u) && word_tag(w[j]) == tag_out) pend &= ~(1u << j);
+          if (pend) poll_bound(a, n, t0, abort);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j < ns) num = fmaf(expf(pm[2 * (s0 + j)] - M), word_value(w[j]), num);
+      }
+      st_tagged(a.attn_o + (size_t)(HB + h) * HD + d, num / den, tag_out);
+    }
+  }
+#endif
 }
 
 
