@@ -172,10 +172,10 @@ __device__ __forceinline__ const uint8_t* phase_base(int kind, const LayerDev& L
 }
 
 // Attention work of CTA b (all derived from the device position): KV head g and
-// either a key split s (its query heads all together, the partials combined by
-// all splits, each a slice of the outputs) or, up to kHeadSplitKeys keys, query
-// head h0 of the group over all
-// keys (the group's heads on separate CTAs, no combine).
+// either a key split s (its query heads all together; the partials combined by split
+// 0, or in the wide-input build by all splits, each a slice of the outputs) or, up to
+// kHeadSplitKeys keys, query head h0 of the group over all keys (the group's heads
+// on separate CTAs, no combine).
 struct Split {
   int g, s, k0, k1, nsplit;
   int h0, nh;  // the group's query heads [h0, h0 + nh) handled here
@@ -826,6 +826,7 @@ __device__ __forceinline__ void gemv_phase(const MegaArgs& a, uint8_t* ring, Sme
 // holds the row's bias, or 0), so the QKV epilogue adds both at once. A_q / A_v are
 // [r, K] and B_q / B_v [rows, r] bf16; the slice [u0, u1) of fused q/k/v rows has at
 // most kUnitPre rows (checked on the host). Ends with a consumer barrier.
+#if QW_MEGA_BIG  // the adapter runs in the wide-input build only
 // Inlined: an out-of-line call here costs register spills around the call site.
 __device__ __forceinline__ void lora_update(const MegaArgs& a, Smem& S, int l, int u0, int u1, int K,
                                          float rn) {
@@ -886,6 +887,7 @@ __device__ __forceinline__ void lora_update(const MegaArgs& a, Smem& S, int l, i
   }
   csync();
 }
+#endif
 
 // Inputs up to 1024 wide stay in registers; wider ones are read from shared
 // memory inside the dot (keeps the kernel under its register budget). X is the
@@ -1014,9 +1016,9 @@ __device__ __forceinline__ void attn_combine(const MegaArgs& a, Smem& S, const S
 
 // Split-K attention of CTA b: QK-norm + RoPE of its group's queries (and of the
 // new key when its split holds pos), tiles of 32 keys from the ring, online
-// softmax, then a partial (or the final output when there is one split); every
-// split of a KV head then polls all splits' partials for a slice of the outputs
-// and combines them in split order.
+// softmax, then a partial (or the final output when there is one split); the
+// partials are combined in split order, by split 0 (7- and 11-warp builds) or by
+// every split for a slice of the outputs (wide-input build).
 template <int HD, bool KB>
 __device__ __forceinline__ void attn_phase(const MegaArgs& a, uint8_t* ring, Smem& S, int& c, int l,
                                            int pos, const Split& sp, const LayerDev& Ld,
