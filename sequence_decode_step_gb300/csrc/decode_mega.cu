@@ -121,7 +121,10 @@ struct Slice {
 
 // Rows a warp takes per GEMV iteration in each phase (a power of two up to 8; for
 // gate/up, rows of interleaved gate/up pairs).
-constexpr int kNrQkv = 2, kNrO = 1, kNrGu = 4, kNrDown = 1, kNrLm = 8;
+// One gate/up unit (two rows) per item in the 7- and 11-warp builds: 20 units per CTA
+// for the Qwen3-0.6B shape spread over three rounds of the 7 warps instead of two rounds
+// with four rows (575 -> 546 us/token, same box).
+constexpr int kNrQkv = 2, kNrO = 1, kNrGu = QW_MEGA_BIG ? 4 : 2, kNrDown = 1, kNrLm = 8;
 // Units per iteration (rows / rows per unit); a ring stage holds a whole number
 // of them when it can.
 __host__ __device__ constexpr int phase_upi(int kind) {
