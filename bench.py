@@ -60,9 +60,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # kernel: (sources digest, bytes per launch, what was captured)
-    "decode_mega": ("b1cbfa07888e6174", 1194050304 + 3765248,
+    "decode_mega": ("d7846fd82ef54d55", 1194048256 + 3808512,
                     "qwen3_0.6b_decode token at position 6, decode_mega_kernel<128, 1, 0, 0, false, 0>"),
-    "decode_mega_big": ("0b13a8b99c2aacd6", 1894992640 + 7449856,
+    "decode_mega_big": ("6a6826f8f9d92b00", 1895046656 + 7786240,
                         "qwen2.5_3b_int4_lora token at position 4098 without the adapter, "
                         "decode_mega_kernel<128, 0, 0, 0, false, 1> (wide-input build)"),
     "lm_head_gemv": ("080190fbaea159fa", 311220992 + 3417856,
